@@ -1,0 +1,373 @@
+"""Benchmark: exact-attention forward TFLOP/s on GB300.
+
+One step = one fa_fwd call over the whole workload (all of the hot path: tile
+loads, QK^T, masking, online softmax, PV, epilogue) on inputs resident in HBM.
+Workload at one GPU: B=8, H=32, Nq=Nk=8192, d=128, bf16, causal
+(4*B*H*N^2*d/2 = 4.398 TFLOP per step); its 1.6 GB of inputs exceed the
+129 MB L2, so no flush is needed between steps.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl fa|reference]
+
+Under torchrun (N > 1) each rank runs its own copy of the workload on its own
+GPU (weak scaling; the heads are independent, so nothing is exchanged); the
+timed region is bracketed by barriers and the max over ranks is reported.
+``--impl reference`` times the float64 CPU oracle on a bounded sample of the
+same workload (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import glob
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "attn fwd TFLOP/s (4·B·H·N²·d, ½ if causal) and % of GB300 dense peak"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for p in sorted(glob.glob(os.path.join(ROOT, "exact_attention_57_gb300", "csrc", "*"))):
+        with open(p, "rb") as f:
+            h.update(os.path.basename(p).encode())
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            return json.load(f), "measured"
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+def profiled_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on
+    the current kernel sources; else None."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        rec = json.load(f)
+    ent = rec.get(kernel, {}).get(workload)
+    if not ent or ent.get("source_hash") != kernel_source_hash():
+        return None
+    return ent.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clocks/throttle reasons sampled every 200 ms while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def cpu_oracle_sample(w, budget_s: float, seed: int = 7):
+    """Time the float64 oracle on sampled query rows of the workload.
+
+    Returns (GFLOP/s in the metric's units, threads, description).  Rows are
+    drawn uniformly over (b, h, i); the metric FLOPs of row i are
+    4*d*|K(i)| (|K(i)| = i+1 keys when causal), so the rate is comparable with
+    the GPU's 4*B*H*N^2*d/2.
+    """
+    import numpy as np
+
+    import oracle
+    from exact_attention_57_gb300.workloads import workload_inputs
+
+    q, k, v = workload_inputs(w)
+    qf, kf, vf = (t.float().numpy() for t in (q, k, v))
+    causal = w.causal[0]
+    rng = np.random.default_rng(seed)
+    threads = os.cpu_count() or 1
+
+    def run(n):
+        rows = rng.integers(0, w.B * w.H * w.Nq, size=n)
+        i = rows % w.Nq
+        keys = np.minimum(i + 1, w.Nk) if causal else np.full(n, w.Nk)
+        flops = float(np.sum(4.0 * w.d * keys))
+        t0 = time.perf_counter()
+        oracle.attn_rows(qf, kf, vf, rows, w.scale, causal, nthreads=threads)
+        return flops, time.perf_counter() - t0
+
+    n = 256
+    flops, dt = run(n)
+    while dt < budget_s / 8 and n < 1 << 20:
+        n *= 4
+        flops, dt = run(n)
+    if dt < budget_s / 2:
+        n = int(n * budget_s / max(dt, 1e-3))
+        flops, dt = run(n)
+    desc = (f"{n} query rows sampled uniformly from the workload, full key range each "
+            f"({'causal' if causal else 'non-causal'}), float64, {threads} threads")
+    return flops / dt / 1e9, threads, desc, dt
+
+
+def run_reference(args, w):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return
+    rates = []
+    per_step = max(2.0, 120.0 / max(1, args.steps + args.warmup))
+    tot_t = 0.0
+    for s in range(args.warmup + args.steps):
+        g, threads, desc, dt = cpu_oracle_sample(w, per_step, seed=100 + s)
+        if s >= args.warmup:
+            rates.append(g)
+            tot_t += dt
+    value = statistics.median(rates) / 1e3  # TFLOP/s
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+        "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * tot_t / max(1, args.steps), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "H": w.H, "Nq": w.Nq, "Nk": w.Nk, "d": w.d,
+                   "causal": w.causal[0], "io_dtype": "bf16"},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads,
+                         "kind": "oracle", "sample": desc},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="fa", choices=["fa", "reference"])
+    ap.add_argument("--workload", default=None)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)
+
+    from exact_attention_57_gb300.workloads import BENCH_WORKLOAD, WORKLOADS
+    w = WORKLOADS[args.workload or BENCH_WORKLOAD]
+    if args.impl == "reference":
+        return run_reference(args, w)
+
+    import torch
+    import torch.distributed as dist
+
+    from exact_attention_57_gb300 import fa
+    from exact_attention_57_gb300.workloads import DTYPE_NAMES
+
+    ws, rank, local = dist_env()
+    if ws > 1:
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local if ws > 1 else 0)
+    torch.cuda.set_device(dev)
+    causal = w.causal[0]
+    tdt = w.torch_dtype
+
+    # Inputs drawn on the device (seeded per rank), resident before timing.
+    g = torch.Generator(device=dev).manual_seed(w.seed + 1000 * rank)
+    q = torch.randn(w.B, w.H, w.Nq, w.d, device=dev, generator=g).to(tdt)
+    k = torch.randn(w.B, w.H, w.Nk, w.d, device=dev, generator=g).mul_(w.k_mult).to(tdt)
+    v = torch.randn(w.B, w.H, w.Nk, w.d, device=dev, generator=g).to(tdt)
+    o = torch.empty_like(q)
+    lse = torch.empty(w.B, w.H, w.Nq, device=dev, dtype=torch.float32)
+    stream = torch.cuda.Stream(device=dev)
+    sh = stream.cuda_stream
+    impl = "simt" if w.dtype == 2 else "tc"
+
+    def step():
+        st = fa.fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                       w.B, w.H, w.Nq, w.Nk, w.d, w.scale, int(causal), w.dtype, sh)
+        if st != fa.FA_OK:
+            raise fa.FaError(st, "fa_fwd")
+
+    torch.cuda.synchronize(dev)
+    for _ in range(args.warmup):
+        step()
+    st, word = fa.fa_fwd_status(sh)
+    if st != fa.FA_OK:
+        raise RuntimeError(f"warm-up device status {word}")
+
+    sampler = ClockSampler(dev.index) if rank == 0 or ws > 1 else None
+    if ws > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    if sampler:
+        sampler.start()
+        time.sleep(0.3)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
+    with torch.cuda.stream(stream):
+        ev[0].record(stream)
+        for i in range(args.steps):
+            step()
+            ev[i + 1].record(stream)
+    stream.synchronize()
+    torch.cuda.synchronize(dev)
+    if ws > 1:
+        dist.barrier()
+    clocks = sampler.stop() if sampler else None
+    st, word = fa.fa_fwd_status(sh)
+    if st != fa.FA_OK:
+        raise RuntimeError(f"timed-region device status {word}")
+    launch_ms = [ev[i].elapsed_time(ev[i + 1]) for i in range(args.steps)]
+    total_ms = ev[0].elapsed_time(ev[-1])
+    if ws > 1:
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+    flops_step = w.flops(causal)
+    value = ws * flops_step * args.steps / (total_ms / 1e3) / 1e12
+
+    # End to end through the host-buffer entry point: H2D of q, k, v from
+    # pinned memory, the forward, D2H of o and lse, every step.
+    e2e = None
+    if not args.no_e2e:
+        qh, kh, vh = (t.cpu().pin_memory() for t in (q, k, v))
+        oh = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+        lh = torch.empty(lse.shape, dtype=torch.float32).pin_memory()
+        h2d = sum(t.numel() * t.element_size() for t in (qh, kh, vh))
+        d2h = oh.numel() * oh.element_size() + lh.numel() * 4
+
+        def e2e_step():
+            r = fa.fa_fwd_host(qh.data_ptr(), kh.data_ptr(), vh.data_ptr(), oh.data_ptr(),
+                               lh.data_ptr(), q.data_ptr(), k.data_ptr(), v.data_ptr(),
+                               o.data_ptr(), lse.data_ptr(), w.B, w.H, w.Nq, w.Nk, w.d,
+                               w.scale, int(causal), w.dtype, sh)
+            if r != fa.FA_OK:
+                raise fa.FaError(r, "fa_fwd_host")
+
+        e2e_steps = max(3, min(args.steps, 10))
+        for _ in range(2):
+            e2e_step()
+        if ws > 1:
+            dist.barrier()
+        t0 = time.perf_counter()
+        for _ in range(e2e_steps):
+            e2e_step()
+        dt = time.perf_counter() - t0
+        if ws > 1:
+            t = torch.tensor([dt], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            dt = float(t.item())
+        e2e = {"value": ws * flops_step * e2e_steps / dt / 1e12, "unit": "TFLOP/s",
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+               "ms_per_step": 1e3 * dt / e2e_steps}
+
+    if rank != 0:
+        if ws > 1:
+            dist.barrier()
+            dist.destroy_process_group()
+        return
+
+    peaks, peak_src = measured_peaks()
+    avg_launch_ms = sum(launch_ms) / len(launch_ms)
+    achieved = flops_step / (avg_launch_ms / 1e3) / 1e12
+    peak = float(peaks["bf16_tflops"]) if w.dtype == 0 else float(peaks["bf16_tflops"]) / 2.0
+    kname = {0: "fa_tc_fwd_kernel<bf16>", 1: "fa_tc_fwd_kernel<tf32>",
+             2: "fa_simt_fwd_kernel"}[w.dtype]
+    traffic = profiled_traffic(kname, w.name)
+    roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                "frac": achieved / peak, "traffic": traffic,
+                "peak_source": f"{peak_src} {'bf16 burst' if w.dtype == 0 else 'bf16 burst / 2 (tf32 nominal ratio)'}",
+                "kernel": kname}
+
+    cpu = None
+    if not args.no_cpu_baseline:
+        g, threads, desc, _ = cpu_oracle_sample(w, 15.0)
+        cpu = {"value": g / 1e3, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+               "sample": desc}
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": DTYPE_NAMES[w.dtype] if w.dtype != 0 else "bf16",
+        "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "H": w.H, "Nq": w.Nq, "Nk": w.Nk, "d": w.d,
+                   "causal": causal, "flops_per_step": flops_step,
+                   "parallelism": f"replicas{ws}" if ws > 1 else "single",
+                   "l2": "inputs larger than L2 (no flush)"},
+        "roofline": roofline,
+        "pct_of_peak": 100.0 * value / ws / peak,
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": args.steps,
+        "clocks": clocks,
+    }
+    print(json.dumps(line), flush=True)
+    if ws > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,253 @@
+// fa_api.cu — host side of the C ABI declared in include/fa.h: argument
+// validation, device checks, TMA tensor-map encoding, kernel dispatch and the
+// per-device status word.  Nothing here computes attention; every step of the
+// forward runs in the kernels of fa_tc_*.cu and fa_simt.cu.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "fa.h"
+#include "fa_internal.h"
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+std::mutex g_mu;
+unsigned *g_status[kMaxDevices] = {};   // device status word per device
+int g_dev_ok[kMaxDevices] = {};         // 0 unknown, 1 sm_103, -1 other
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::atomic<int> g_skip_v_load{0};
+std::atomic<unsigned long long> g_wait_limit_ns{0};
+
+size_t elem_size(int dtype) { return dtype == FA_DTYPE_BF16 ? 2 : 4; }
+
+bool overlap(const void *a, size_t an, const void *b, size_t bn) {
+  const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+  return x < y + bn && y < x + an;
+}
+
+// Host-side checks shared by fa_fwd and fa_fwd_host.
+int validate(const void *q, const void *k, const void *v, const void *o, const float *lse,
+             int B, int H, int Nq, int Nk, int d, float scale, int causal, int dtype) {
+  if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
+  if (B < 1 || H < 1 || Nq < 1 || Nk < 1 || d < 1) return FA_ERR_INVALID_ARG;
+  if (B > 65535 || H > 65535) return FA_ERR_INVALID_ARG;
+  if (!std::isfinite(scale)) return FA_ERR_INVALID_ARG;
+  if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
+  if (dtype != FA_DTYPE_BF16 && dtype != FA_DTYPE_F32 && dtype != FA_DTYPE_F32_SIMT)
+    return FA_ERR_INVALID_ARG;
+  for (const void *ptr : {q, k, v, o})
+    if (reinterpret_cast<uintptr_t>(ptr) % 16 != 0) return FA_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(lse) % 4 != 0) return FA_ERR_INVALID_ARG;
+  // Sizes: every flat index must fit comfortably in 63 bits and the TMA
+  // coordinates in 31 bits.
+  const double rows_q = static_cast<double>(B) * H * Nq, rows_k = static_cast<double>(B) * H * Nk;
+  if (rows_q * d >= 9.0e18 || rows_k * d >= 9.0e18) return FA_ERR_INVALID_ARG;
+  const size_t es = elem_size(dtype);
+  const size_t qn = static_cast<size_t>(B) * H * Nq * d * es;
+  const size_t kn = static_cast<size_t>(B) * H * Nk * d * es;
+  const size_t ln = static_cast<size_t>(B) * H * Nq * sizeof(float);
+  if (overlap(o, qn, q, qn) || overlap(o, qn, k, kn) || overlap(o, qn, v, kn) ||
+      overlap(o, qn, lse, ln) || overlap(lse, ln, q, qn) || overlap(lse, ln, k, kn) ||
+      overlap(lse, ln, v, kn))
+    return FA_ERR_INVALID_ARG;
+  // The compiled set of kernels.
+  if (dtype == FA_DTYPE_BF16 && d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+  if (dtype == FA_DTYPE_F32 && d != 64) return FA_ERR_UNSUPPORTED;
+  if (dtype == FA_DTYPE_F32_SIMT && d > 128) return FA_ERR_UNSUPPORTED;
+  return FA_OK;
+}
+
+// The current device must be sm_103 (the only code compiled in); also makes
+// sure its status word exists.  Returns FA_OK and the status pointer.
+int device_setup(unsigned **status) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return FA_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return FA_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (g_dev_ok[dev] == 0) {
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+      return FA_ERR_CUDA;
+    g_dev_ok[dev] = (major == 10 && minor == 3) ? 1 : -1;
+  }
+  if (g_dev_ok[dev] != 1) return FA_ERR_UNSUPPORTED;
+  if (g_status[dev] == nullptr) {
+    unsigned *ptr = nullptr;
+    if (cudaMalloc(&ptr, 256) != cudaSuccess) return FA_ERR_CUDA;
+    if (cudaMemset(ptr, 0, 256) != cudaSuccess) {
+      cudaFree(ptr);
+      return FA_ERR_CUDA;
+    }
+    g_status[dev] = ptr;
+  }
+  *status = g_status[dev];
+  return FA_OK;
+}
+
+int get_encoder() {
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (g_encode) return FA_OK;
+  void *fn = nullptr;
+  cudaDriverEntryPointQueryResult qres = cudaDriverEntryPointSymbolNotFound;
+  if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                       &qres) != cudaSuccess ||
+      qres != cudaDriverEntryPointSuccess || fn == nullptr)
+    return FA_ERR_CUDA;
+  g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  return FA_OK;
+}
+
+// 3-D view [B*H, N, d] of a [B, H, N, d] tensor, boxes of {128 bytes of d,
+// 128 rows, 1 head}, 128-byte swizzle, zero fill outside the tensor (rows past
+// N read as zeros and are clipped on store).
+int encode_map(CUtensorMap *map, const void *base, int dtype, int BH, int N, int d) {
+  const CUtensorMapDataType dt =
+      dtype == FA_DTYPE_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+  const cuuint64_t es = elem_size(dtype);
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N),
+                        static_cast<cuuint64_t>(BH)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * es,
+                           static_cast<cuuint64_t>(d) * static_cast<cuuint64_t>(N) * es};
+  cuuint32_t box[3] = {static_cast<cuuint32_t>(128 / es), static_cast<cuuint32_t>(fa::BM), 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = g_encode(map, dt, 3, const_cast<void *>(base), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? FA_OK : FA_ERR_CUDA;
+}
+
+int ceil_div(int a, int b) { return (a + b - 1) / b; }
+
+}  // namespace
+
+extern "C" {
+
+int fa_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H,
+           int Nq, int Nk, int d, float scale, int causal, int dtype, void *stream) {
+  int rc = validate(q, k, v, o, lse, B, H, Nq, Nk, d, scale, causal, dtype);
+  if (rc != FA_OK) return rc;
+  unsigned *status = nullptr;
+  if ((rc = device_setup(&status)) != FA_OK) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+
+  if (dtype == FA_DTYPE_F32_SIMT) {
+    fa::SimtParams p;
+    p.q = static_cast<const float *>(q);
+    p.k = static_cast<const float *>(k);
+    p.v = static_cast<const float *>(v);
+    p.o = static_cast<float *>(o);
+    p.lse = lse;
+    p.status = status;
+    p.H = H;
+    p.Nq = Nq;
+    p.Nk = Nk;
+    p.d = d;
+    p.n_qtiles = ceil_div(Nq, fa::BM);
+    p.scale = scale;
+    p.causal = causal;
+    return fa::launch_simt(p, B, s) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+  }
+
+  if ((rc = get_encoder()) != FA_OK) return rc;
+  CUtensorMap mq, mk, mv, mo;
+  const int BH = B * H;
+  if ((rc = encode_map(&mq, q, dtype, BH, Nq, d)) != FA_OK) return rc;
+  if ((rc = encode_map(&mk, k, dtype, BH, Nk, d)) != FA_OK) return rc;
+  if ((rc = encode_map(&mv, v, dtype, BH, Nk, d)) != FA_OK) return rc;
+  if ((rc = encode_map(&mo, o, dtype, BH, Nq, d)) != FA_OK) return rc;
+
+  fa::TcParams p;
+  p.lse = lse;
+  p.status = status;
+  p.H = H;
+  p.Nq = Nq;
+  p.Nk = Nk;
+  p.n_qtiles = ceil_div(Nq, fa::BM);
+  p.n_ktiles = ceil_div(Nk, fa::BN);
+  p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+  p.scale_neg = scale < 0.f ? 1 : 0;
+  const unsigned long long lim = g_wait_limit_ns.load();
+  p.wait_limit_ns = lim ? lim : fa::kDefaultWaitLimitNs;
+  p.skip_v_load = g_skip_v_load.load();
+
+  cudaError_t e;
+  if (dtype == FA_DTYPE_BF16)
+    e = (d == 64) ? fa::launch_tc_bf16_d64(mq, mk, mv, mo, p, B, causal, s)
+                  : fa::launch_tc_bf16_d128(mq, mk, mv, mo, p, B, causal, s);
+  else
+    e = fa::launch_tc_f32_d64(mq, mk, mv, mo, p, B, causal, s);
+  return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+int fa_fwd_host(const void *q_h, const void *k_h, const void *v_h, void *o_h, float *lse_h,
+                void *q_d, void *k_d, void *v_d, void *o_d, float *lse_d, int B, int H, int Nq,
+                int Nk, int d, float scale, int causal, int dtype, void *stream) {
+  if (!q_h || !k_h || !v_h || !o_h || !lse_h) return FA_ERR_INVALID_ARG;
+  int rc = validate(q_d, k_d, v_d, o_d, lse_d, B, H, Nq, Nk, d, scale, causal, dtype);
+  if (rc != FA_OK) return rc;
+  const size_t es = elem_size(dtype);
+  const size_t qn = static_cast<size_t>(B) * H * Nq * d * es;
+  const size_t kn = static_cast<size_t>(B) * H * Nk * d * es;
+  const size_t ln = static_cast<size_t>(B) * H * Nq * sizeof(float);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaMemcpyAsync(q_d, q_h, qn, cudaMemcpyHostToDevice, s) != cudaSuccess ||
+      cudaMemcpyAsync(k_d, k_h, kn, cudaMemcpyHostToDevice, s) != cudaSuccess ||
+      cudaMemcpyAsync(v_d, v_h, kn, cudaMemcpyHostToDevice, s) != cudaSuccess)
+    return FA_ERR_CUDA;
+  rc = fa_fwd(q_d, k_d, v_d, o_d, lse_d, B, H, Nq, Nk, d, scale, causal, dtype, stream);
+  if (rc != FA_OK) return rc;
+  if (cudaMemcpyAsync(o_h, o_d, qn, cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+      cudaMemcpyAsync(lse_h, lse_d, ln, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return FA_ERR_CUDA;
+  return cudaStreamSynchronize(s) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+int fa_fwd_status(void *stream, int *device_status) {
+  if (device_status) *device_status = 0;
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return FA_ERR_CUDA;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return FA_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return FA_ERR_UNSUPPORTED;
+  unsigned *ptr;
+  {
+    std::lock_guard<std::mutex> lock(g_mu);
+    ptr = g_status[dev];
+  }
+  if (ptr == nullptr) return FA_OK;  // nothing has run on this device
+  unsigned word = 0;
+  if (cudaMemcpy(&word, ptr, sizeof word, cudaMemcpyDeviceToHost) != cudaSuccess)
+    return FA_ERR_CUDA;
+  if (word != 0 && cudaMemset(ptr, 0, sizeof word) != cudaSuccess) return FA_ERR_CUDA;
+  if (device_status) *device_status = static_cast<int>(word);
+  return word ? FA_ERR_DEVICE_TIMEOUT : FA_OK;
+}
+
+const char *fa_status_string(int status) {
+  switch (status) {
+    case FA_OK: return "FA_OK";
+    case FA_ERR_INVALID_ARG: return "FA_ERR_INVALID_ARG";
+    case FA_ERR_UNSUPPORTED: return "FA_ERR_UNSUPPORTED";
+    case FA_ERR_CUDA: return "FA_ERR_CUDA";
+    case FA_ERR_DEVICE_TIMEOUT: return "FA_ERR_DEVICE_TIMEOUT";
+    default: return "FA_ERR_UNKNOWN";
+  }
+}
+
+int fa_version(void) { return FA_VERSION; }
+
+int fa_set_test_hooks(int skip_v_load, unsigned long long wait_limit_ns) {
+  g_skip_v_load.store(skip_v_load ? 1 : 0);
+  g_wait_limit_ns.store(wait_limit_ns);
+  return FA_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,59 @@
+// fa_internal.h — declarations shared by the host API and the kernel
+// translation units (not part of the public ABI).
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace fa {
+
+// Tile shape of the tensor-core kernels: one CTA owns BM query rows of one
+// (batch, head) and streams the keys in tiles of BN.
+constexpr int BM = 128;
+constexpr int BN = 128;
+
+// Status-word bits (see fa_fwd_status in fa.h).
+constexpr unsigned kStatusProducer = 1u;
+constexpr unsigned kStatusMma = 2u;
+constexpr unsigned kStatusSoftmax = 4u;
+constexpr unsigned kStatusInjected = 8u;
+
+constexpr unsigned long long kDefaultWaitLimitNs = 2000000000ull;  // 2 s
+
+struct TcParams {
+  float *lse;                     // [B*H*Nq]
+  unsigned *status;               // per-device status word
+  int H, Nq, Nk;
+  int n_qtiles, n_ktiles;         // ceil(Nq/BM), ceil(Nk/BN)
+  float scale_log2;               // scale * log2(e)
+  int scale_neg;                  // scale < 0
+  unsigned long long wait_limit_ns;
+  int skip_v_load;                // test hook
+};
+
+struct SimtParams {
+  const float *q, *k, *v;
+  float *o, *lse;
+  unsigned *status;
+  int H, Nq, Nk, d;
+  int n_qtiles;
+  float scale;
+  int causal;
+};
+
+// Tensor-core forward for one (head dim, input type); causal chosen inside.
+// Returns the launch's cudaError_t.
+cudaError_t launch_tc_bf16_d64(const CUtensorMap &q, const CUtensorMap &k, const CUtensorMap &v,
+                               const CUtensorMap &o, const TcParams &p, int B, int causal,
+                               cudaStream_t s);
+cudaError_t launch_tc_bf16_d128(const CUtensorMap &q, const CUtensorMap &k, const CUtensorMap &v,
+                                const CUtensorMap &o, const TcParams &p, int B, int causal,
+                                cudaStream_t s);
+cudaError_t launch_tc_f32_d64(const CUtensorMap &q, const CUtensorMap &k, const CUtensorMap &v,
+                              const CUtensorMap &o, const TcParams &p, int B, int causal,
+                              cudaStream_t s);
+
+cudaError_t launch_simt(const SimtParams &p, int B, cudaStream_t s);
+
+}  // namespace fa

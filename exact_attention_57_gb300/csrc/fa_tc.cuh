@@ -1,0 +1,498 @@
+// fa_tc.cuh — tensor-core (tcgen05) exact-attention forward for sm_103a.
+//
+// Method: the forward kernel of "flash_attention_2.cu"
+// (leloykun/flash-hyperbolic-attention-minimal) — scores S = scale * Q K^T,
+// online softmax with a running row max m and row sum l, the partial output
+// rescaled by exp(m_old - m_new), and at the end O = O / l, L = m + log(l).
+// Loop order: the swapped one from "parallel execution of read/write
+// operations (paper vs implementation)" (one query tile per CTA, keys inner,
+// O kept on chip and written once).  Parallelism: over queries as well as
+// batch and heads, as in "Meta's xFormers has Attention kernel written in
+// CUTLASS".  exp2 with log2(e) folded into the scale, as in "Add Fused
+// Multi-Head Attention example" (cuTile.jl).
+//
+// GB300 design (one CTA = one (batch, head, 128-row query tile)):
+//   warp 4       TMA producer: Q once, then K_j / V_j through shared-memory
+//                rings (full/empty mbarriers), L2 evict-last for K/V.
+//   warp 5       UMMA issuer (one lane): S_j = Q K_j^T into a double-buffered
+//                tensor-memory score tile, O += P_j V_j with P read from
+//                tensor memory, both fp32-accumulating.  Owns the TMEM
+//                allocation.
+//   warps 0-3    softmax, correction and epilogue: one query row per thread
+//                (= one TMEM lane).  Loads the 128 scores of its row, masks
+//                the causal diagonal / ragged key tail, updates m and l, writes
+//                P (bf16, or tf32 for fp32 inputs) back over S in TMEM, and at
+//                the end normalises O, stages it swizzled in shared memory for
+//                a TMA store, and writes LSE.
+// Tensor memory: S0 cols [0,128), S1 [128,256), O [256, 256+D).
+//
+// Rescaling: the running max used as the exponent offset only moves when a
+// row's max grows by more than 2^8; otherwise the stale offset is kept.  The
+// softmax is invariant to the offset, so the result is exact up to rounding;
+// unshifted terms are at most 2^8, far inside the fp32/bf16 range.
+//
+// Every wait is bounded (globaltimer); on expiry the CTA sets an abort flag,
+// records its role in the device status word, drains in-flight TMA loads and
+// UMMAs, frees tensor memory and exits.
+#pragma once
+
+#include <cuda_bf16.h>
+
+#include <type_traits>
+
+#include "fa_internal.h"
+#include "ptx.cuh"
+
+namespace fa {
+
+template <int D, bool TF32>
+struct TcCfg {
+  static constexpr int ESZ = TF32 ? 4 : 2;                 // bytes per element
+  static constexpr int NCH = D * ESZ / 128;                 // 128-byte swizzle chunks per row
+  static constexpr int CH_ELEMS = 128 / ESZ;                // elements per chunk
+  static constexpr int CHUNK_BYTES = 128 * 128;             // one chunk of 128 rows
+  static constexpr int TILE_BYTES = NCH * CHUNK_BYTES;      // one 128-row tile
+  static constexpr int UK = 32 / ESZ;                       // K extent of one UMMA
+  static constexpr int KST = (TILE_BYTES <= 16384) ? 3 : 2; // K ring depth
+  static constexpr int VST = (TILE_BYTES <= 16384) ? 3 : 2; // V ring depth
+  static constexpr int OFF_Q = 0;
+  static constexpr int OFF_K = OFF_Q + TILE_BYTES;
+  static constexpr int OFF_V = OFF_K + KST * TILE_BYTES;
+  static constexpr int OFF_BAR = OFF_V + VST * TILE_BYTES;
+  // q, kfull[KST], kempty[KST], vfull[VST], vempty[VST], sfull[2], pfull[2], odone, fin
+  static constexpr int NBAR = 1 + 2 * KST + 2 * VST + 2 + 2 + 1 + 1;
+  static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;       // tmem base, abort flag
+  static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;   // + alignment slack
+  static constexpr uint32_t TMEM_COLS = 512;
+  static constexpr uint32_t COL_S0 = 0, COL_S1 = 128, COL_O = 256;
+  static constexpr int THREADS = 192;
+  static_assert(NCH >= 1 && D % 32 == 0, "head dim must fill whole 128-byte chunks");
+  static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
+};
+
+constexpr float kRescaleThreshold = 8.0f;   // log2 units: factor 256
+constexpr float kLn2 = 0.693147180559945309f;
+constexpr unsigned kFull = 0xffffffffu;
+
+struct WaitCtl {
+  volatile int *abort;
+  unsigned *status;
+  unsigned long long limit_ns;
+  unsigned role;
+};
+
+// Bounded wait for an mbarrier phase.  Returns false if the CTA is aborting
+// (unless honour_abort is false) or the wait ran past the limit, in which case
+// it raises the abort flag and records its role in the status word.
+__device__ __forceinline__ bool bounded_wait(uint32_t bar, uint32_t parity, const WaitCtl &w,
+                                             bool honour_abort = true) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 7u) == 0) {
+      if (honour_abort && *w.abort) return false;
+      if (globaltimer_ns() - t0 > w.limit_ns) {
+        *w.abort = 1;
+        atomicOr(w.status, w.role);
+        return false;
+      }
+    }
+  }
+}
+
+template <int D, bool TF32, bool CAUSAL>
+__global__ void __launch_bounds__(192, 1)
+    fa_tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
+                     const __grid_constant__ CUtensorMap tm_k,
+                     const __grid_constant__ CUtensorMap tm_v,
+                     const __grid_constant__ CUtensorMap tm_o, const TcParams p) {
+  using C = TcCfg<D, TF32>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t sQ = sbase + C::OFF_Q;
+  const uint32_t sK = sbase + C::OFF_K;
+  const uint32_t sV = sbase + C::OFF_V;
+  const uint32_t bQ = sbase + C::OFF_BAR;
+  const uint32_t bKfull = bQ + 8;                      // + 8*stage
+  const uint32_t bKempty = bKfull + 8 * C::KST;
+  const uint32_t bVfull = bKempty + 8 * C::KST;
+  const uint32_t bVempty = bVfull + 8 * C::VST;
+  const uint32_t bSfull = bVempty + 8 * C::VST;        // + 8*buffer
+  const uint32_t bPfull = bSfull + 16;                 // + 8*buffer
+  const uint32_t bOdone = bPfull + 16;
+  const uint32_t bFin = bOdone + 8;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::OFF_MISC);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::OFF_MISC + 4);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  // Causal: heaviest query tiles first (blockIdx.x = 0 gets the last tile).
+  const int qt = CAUSAL ? (p.n_qtiles - 1 - static_cast<int>(blockIdx.x))
+                        : static_cast<int>(blockIdx.x);
+  const int bh = static_cast<int>(blockIdx.z) * p.H + static_cast<int>(blockIdx.y);
+  const int q0 = qt * BM;
+  // Key tiles this query tile needs (top-left causal: keys <= last row).
+  const int n_kt = CAUSAL ? min(qt + 1, p.n_ktiles) : p.n_ktiles;
+
+  if (threadIdx.x == 0) {
+    mbar_init(bQ, 1);
+#pragma unroll
+    for (int s = 0; s < C::KST; ++s) {
+      mbar_init(bKfull + 8 * s, 1);
+      mbar_init(bKempty + 8 * s, 1);
+    }
+#pragma unroll
+    for (int s = 0; s < C::VST; ++s) {
+      mbar_init(bVfull + 8 * s, 1);
+      mbar_init(bVempty + 8 * s, 1);
+    }
+    mbar_init(bSfull, 1);
+    mbar_init(bSfull + 8, 1);
+    mbar_init(bPfull, 128);
+    mbar_init(bPfull + 8, 128);
+    mbar_init(bOdone, 1);
+    mbar_init(bFin, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+    fence_proxy_async_smem();
+  }
+  if (warp == 4 && lane == 0) {
+    tma_prefetch_desc(&tm_q);
+    tma_prefetch_desc(&tm_k);
+    tma_prefetch_desc(&tm_v);
+    tma_prefetch_desc(&tm_o);
+  }
+  if (warp == 5) {
+    tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  WaitCtl w{abort_flag, p.status, p.wait_limit_ns, 0u};
+
+  if (warp == 4) {
+    // ------------------------------------------------------------ producer
+    w.role = kStatusProducer;
+    if (lane == 0) {
+      const uint64_t pol_q = l2_policy_evict_first();
+      const uint64_t pol_kv = l2_policy_evict_last();
+      mbar_arrive_expect_tx(bQ, C::TILE_BYTES);
+#pragma unroll
+      for (int c = 0; c < C::NCH; ++c)
+        tma_load_3d(sQ + c * C::CHUNK_BYTES, &tm_q, bQ, c * C::CH_ELEMS, q0, bh, pol_q);
+      int nk = 0, nv = 0;  // loads issued
+      bool ok = true;
+      // Load order = consumption order: K0, K1, V0, K2, V1, ...
+      for (int j = -1; ok && j < n_kt; ++j) {
+        const int jk = j + 1;  // next K tile
+        if (jk < n_kt) {
+          const int s = jk % C::KST, r = jk / C::KST;
+          if (r > 0) ok = bounded_wait(bKempty + 8 * s, (r - 1) & 1, w);
+          if (!ok) break;
+          mbar_arrive_expect_tx(bKfull + 8 * s, C::TILE_BYTES);
+#pragma unroll
+          for (int c = 0; c < C::NCH; ++c)
+            tma_load_3d(sK + s * C::TILE_BYTES + c * C::CHUNK_BYTES, &tm_k, bKfull + 8 * s,
+                        c * C::CH_ELEMS, jk * BN, bh, pol_kv);
+          ++nk;
+        }
+        if (j >= 0) {
+          if (p.skip_v_load && j == 0) {  // test hook: starve the MMA issuer
+            atomicOr(p.status, kStatusInjected);
+            break;
+          }
+          const int s = j % C::VST, r = j / C::VST;
+          if (r > 0) ok = bounded_wait(bVempty + 8 * s, (r - 1) & 1, w);
+          if (!ok) break;
+          mbar_arrive_expect_tx(bVfull + 8 * s, C::TILE_BYTES);
+#pragma unroll
+          for (int c = 0; c < C::NCH; ++c)
+            tma_load_3d(sV + s * C::TILE_BYTES + c * C::CHUNK_BYTES, &tm_v, bVfull + 8 * s,
+                        c * C::CH_ELEMS, j * BN, bh, pol_kv);
+          ++nv;
+        }
+      }
+      // Drain: no TMA write may still be in flight when the CTA exits.
+      bounded_wait(bQ, 0, w, false);
+      for (int s = 0; s < C::KST; ++s) {
+        const int cnt = (nk > s) ? (nk - 1 - s) / C::KST + 1 : 0;
+        if (cnt > 0) bounded_wait(bKfull + 8 * s, (cnt - 1) & 1, w, false);
+      }
+      for (int s = 0; s < C::VST; ++s) {
+        const int cnt = (nv > s) ? (nv - 1 - s) / C::VST + 1 : 0;
+        if (cnt > 0) bounded_wait(bVfull + 8 * s, (cnt - 1) & 1, w, false);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 5) {
+    // ------------------------------------------------------------ UMMA issuer
+    w.role = kStatusMma;
+    if (lane == 0) {
+      constexpr uint32_t kFmt = TF32 ? 2u : 1u;
+      constexpr uint32_t kIdescQK = make_idesc(kFmt, BM, BN, 0u, 0u);  // Q, K both K-major
+      constexpr uint32_t kIdescPV = make_idesc(kFmt, BM, D, 0u, 1u);   // V is MN-major
+      bool ok = bounded_wait(bQ, 0, w);
+      auto issue_qk = [&](int j) -> bool {
+        const int s = j % C::KST;
+        if (!bounded_wait(bKfull + 8 * s, (j / C::KST) & 1, w)) return false;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem + ((j & 1) ? C::COL_S1 : C::COL_S0);
+        const uint32_t kb = sK + s * C::TILE_BYTES;
+#pragma unroll
+        for (int kk = 0; kk < D / C::UK; ++kk) {
+          // 32 bytes of K per UMMA; 4 steps per 128-byte swizzle chunk.
+          const uint32_t off = (kk >> 2) * C::CHUNK_BYTES + (kk & 3) * 32;
+          umma_ss<TF32>(d_tmem, sdesc_sw128(sQ + off, 16, 1024), sdesc_sw128(kb + off, 16, 1024),
+                        kIdescQK, kk > 0 ? 1u : 0u);
+        }
+        tc_commit(bKempty + 8 * s);
+        tc_commit(bSfull + 8 * (j & 1));
+        return true;
+      };
+      if (ok) ok = issue_qk(0);
+      for (int j = 0; ok && j < n_kt; ++j) {
+        if (j + 1 < n_kt && !(ok = issue_qk(j + 1))) break;
+        if (!(ok = bounded_wait(bPfull + 8 * (j & 1), (j >> 1) & 1, w))) break;
+        const int s = j % C::VST;
+        if (!(ok = bounded_wait(bVfull + 8 * s, (j / C::VST) & 1, w))) break;
+        tc_fence_after();
+        const uint32_t a_tmem = tmem + ((j & 1) ? C::COL_S1 : C::COL_S0);
+        const uint32_t vb = sV + s * C::TILE_BYTES;
+#pragma unroll
+        for (int kk = 0; kk < BN / C::UK; ++kk) {
+          // UK keys per UMMA: UK rows of 128 bytes; P advances 8 TMEM columns.
+          umma_ts<TF32>(tmem + C::COL_O, a_tmem + kk * 8,
+                        sdesc_sw128(vb + kk * C::UK * 128, C::CHUNK_BYTES, 1024), kIdescPV,
+                        (j > 0 || kk > 0) ? 1u : 0u);
+        }
+        tc_commit(bVempty + 8 * s);
+        tc_commit(bOdone);
+      }
+      // Every UMMA issued above must be complete before TMEM is freed.
+      tc_commit(bFin);
+      bounded_wait(bFin, 0, w, false);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------ softmax + epilogue
+    w.role = kStatusSoftmax;
+    const int r = threadIdx.x;  // TMEM lane == row within the tile
+    const int row = q0 + r;
+    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+    const uint32_t o_tm = tmem + lane_off + C::COL_O;
+    const float sl2 = p.scale_log2;
+    const bool neg = p.scale_neg != 0;
+    const int row_lim = CAUSAL ? min(row + 1, p.Nk) : p.Nk;  // keys [0, row_lim)
+    float m_used = -INFINITY;  // exponent offset, log2 units of the scaled score
+    float l = 0.f;
+    bool ok = true;
+
+    for (int j = 0; j < n_kt; ++j) {
+      const int buf = j & 1;
+      ok = __all_sync(kFull, bounded_wait(bSfull + 8 * buf, (j >> 1) & 1, w));
+      if (!ok) break;
+      tc_fence_after();
+      const uint32_t s_tm = tmem + lane_off + (buf ? C::COL_S1 : C::COL_S0);
+      uint32_t sr[4][32];
+      tmem_ld32(s_tm + 0, sr[0]);
+      tmem_ld32(s_tm + 32, sr[1]);
+      tmem_ld32(s_tm + 64, sr[2]);
+      tmem_ld32(s_tm + 96, sr[3]);
+      tmem_ld_wait();
+      reg_fence32(sr[0]);
+      reg_fence32(sr[1]);
+      reg_fence32(sr[2]);
+      reg_fence32(sr[3]);
+
+      const int lim = row_lim - j * BN;  // valid columns c < lim
+      // Row max (raw score; for a negative scale the min becomes the max).
+      // Masked tiles (causal diagonal, ragged key tail) take a separate
+      // compile-time path so unmasked tiles carry no selects.
+      auto row_max = [&](auto mask_tag) -> float {
+        constexpr bool kMask = decltype(mask_tag)::value;
+        const float fill = neg ? INFINITY : -INFINITY;
+        float part[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) part[i] = fill;
+#pragma unroll
+        for (int c = 0; c < BN; ++c) {
+          float x = __uint_as_float(sr[c >> 5][c & 31]);
+          if constexpr (kMask) x = (c < lim) ? x : fill;
+          part[c & 7] = neg ? fminf(part[c & 7], x) : fmaxf(part[c & 7], x);
+        }
+#pragma unroll
+        for (int i = 1; i < 8; ++i) part[0] = neg ? fminf(part[0], part[i]) : fmaxf(part[0], part[i]);
+        return part[0];
+      };
+      const bool masked = __any_sync(kFull, lim < BN);
+      const float mx = masked ? row_max(std::true_type{}) : row_max(std::false_type{});
+      const float m_new = fmaxf(m_used, mx * sl2);
+      if (j == 0) {
+        m_used = m_new;
+      } else {
+        // O may be touched (and P_j written) only after P_{j-1} V_{j-1} is done.
+        ok = __all_sync(kFull, bounded_wait(bOdone, (j - 1) & 1, w));
+        if (!ok) break;
+        const bool need = (m_new - m_used) > kRescaleThreshold;
+        if (__any_sync(kFull, need)) {
+          tc_fence_after();
+          const float alpha = need ? ex2_approx(m_used - m_new) : 1.f;
+#pragma unroll
+          for (int c = 0; c < D; c += 32) {
+            uint32_t o[32];
+            tmem_ld32(o_tm + c, o);
+            tmem_ld_wait();
+            reg_fence32(o);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+            tmem_st32(o_tm + c, o);
+          }
+          tmem_st_wait();
+          if (need) {
+            l *= alpha;
+            m_used = m_new;
+          }
+        }
+      }
+      // P = exp2(s * scale*log2e - m_used), written over S in TMEM.
+      const float neg_m = -m_used;
+      float psum[4] = {0.f, 0.f, 0.f, 0.f};
+      auto write_p = [&](auto mask_tag) {
+        constexpr bool kMask = decltype(mask_tag)::value;
+        if constexpr (!TF32) {
+#pragma unroll
+          for (int hblk = 0; hblk < 2; ++hblk) {
+            uint32_t pk[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              const int c0 = hblk * 64 + 2 * i;
+              float p0 = ex2_approx(fmaf(__uint_as_float(sr[c0 >> 5][c0 & 31]), sl2, neg_m));
+              float p1 =
+                  ex2_approx(fmaf(__uint_as_float(sr[(c0 + 1) >> 5][(c0 + 1) & 31]), sl2, neg_m));
+              if constexpr (kMask) {
+                p0 = (c0 < lim) ? p0 : 0.f;
+                p1 = (c0 + 1 < lim) ? p1 : 0.f;
+              }
+              psum[i & 3] += p0 + p1;
+              pk[i] = pack_bf16x2(p0, p1);
+            }
+            tmem_st32(s_tm + hblk * 32, pk);
+          }
+        } else {
+#pragma unroll
+          for (int qblk = 0; qblk < 4; ++qblk) {
+            uint32_t pk[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              const int c = qblk * 32 + i;
+              float pv = ex2_approx(fmaf(__uint_as_float(sr[qblk][i]), sl2, neg_m));
+              if constexpr (kMask) pv = (c < lim) ? pv : 0.f;
+              psum[i & 3] += pv;
+              pk[i] = to_tf32(pv);
+            }
+            tmem_st32(s_tm + qblk * 32, pk);
+          }
+        }
+      };
+      if (masked) write_p(std::true_type{});
+      else write_p(std::false_type{});
+      l += (psum[0] + psum[1]) + (psum[2] + psum[3]);
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(bPfull + 8 * buf);
+    }
+
+    // ------------------------------------------------ epilogue
+    if (ok) ok = __all_sync(kFull, bounded_wait(bOdone, (n_kt - 1) & 1, w));
+    if (ok) {
+      tc_fence_after();
+      const float inv_l = 1.f / l;
+      uint8_t *stage = smem + C::OFF_Q;  // Q is no longer read: every S_j is done
+#pragma unroll
+      for (int c = 0; c < D; c += 32) {
+        uint32_t o[32];
+        tmem_ld32(o_tm + c, o);
+        tmem_ld_wait();
+        reg_fence32(o);
+        if constexpr (TF32) {
+          // 32 fp32 = 8 units of 16 bytes = one full chunk (chunk c/32).
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            uint4 val;
+            val.x = __float_as_uint(__uint_as_float(o[4 * u + 0]) * inv_l);
+            val.y = __float_as_uint(__uint_as_float(o[4 * u + 1]) * inv_l);
+            val.z = __float_as_uint(__uint_as_float(o[4 * u + 2]) * inv_l);
+            val.w = __float_as_uint(__uint_as_float(o[4 * u + 3]) * inv_l);
+            const int ch = c / 32;
+            *reinterpret_cast<uint4 *>(stage + ch * C::CHUNK_BYTES + r * 128 +
+                                       ((u ^ (r & 7)) << 4)) = val;
+          }
+        } else {
+          // 32 bf16 = 4 units of 16 bytes; global unit index c/8 + u.
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            uint4 val;
+            val.x = pack_bf16x2(__uint_as_float(o[8 * u + 0]) * inv_l,
+                                __uint_as_float(o[8 * u + 1]) * inv_l);
+            val.y = pack_bf16x2(__uint_as_float(o[8 * u + 2]) * inv_l,
+                                __uint_as_float(o[8 * u + 3]) * inv_l);
+            val.z = pack_bf16x2(__uint_as_float(o[8 * u + 4]) * inv_l,
+                                __uint_as_float(o[8 * u + 5]) * inv_l);
+            val.w = pack_bf16x2(__uint_as_float(o[8 * u + 6]) * inv_l,
+                                __uint_as_float(o[8 * u + 7]) * inv_l);
+            const int gu = c / 8 + u;
+            const int ch = gu >> 3, uu = gu & 7;
+            *reinterpret_cast<uint4 *>(stage + ch * C::CHUNK_BYTES + r * 128 +
+                                       ((uu ^ (r & 7)) << 4)) = val;
+          }
+        }
+      }
+      if (row < p.Nq) p.lse[static_cast<size_t>(bh) * p.Nq + row] = m_used * kLn2 + logf(l);
+    }
+    fence_proxy_async_smem();
+    named_bar_sync(1, 128);
+    if (threadIdx.x == 0 && *abort_flag == 0) {
+#pragma unroll
+      for (int c = 0; c < C::NCH; ++c) tma_store_3d(&tm_o, sQ + c * C::CHUNK_BYTES, c * C::CH_ELEMS, q0, bh);
+      tma_store_commit();
+      tma_store_wait_read_all();
+    }
+  }
+
+  // ------------------------------------------------------------ teardown
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 5) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+}
+
+template <int D, bool TF32>
+cudaError_t launch_tc(const CUtensorMap &q, const CUtensorMap &k, const CUtensorMap &v,
+                      const CUtensorMap &o, const TcParams &p, int B, int causal,
+                      cudaStream_t stream) {
+  using C = TcCfg<D, TF32>;
+  void (*kern)(const CUtensorMap, const CUtensorMap, const CUtensorMap, const CUtensorMap,
+               const TcParams) =
+      causal ? fa_tc_fwd_kernel<D, TF32, true> : fa_tc_fwd_kernel<D, TF32, false>;
+  cudaError_t e =
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(p.n_qtiles), static_cast<unsigned>(p.H),
+                     static_cast<unsigned>(B));
+  cfg.blockDim = dim3(C::THREADS, 1, 1);
+  cfg.dynamicSmemBytes = C::SMEM_BYTES;
+  cfg.stream = stream;
+  cfg.attrs = nullptr;
+  cfg.numAttrs = 0;
+  return cudaLaunchKernelEx(&cfg, kern, q, k, v, o, p);
+}
+
+}  // namespace fa

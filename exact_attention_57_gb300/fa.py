@@ -1,0 +1,151 @@
+"""ctypes binding of ``libfa.so`` (the C ABI in include/fa.h).
+
+The functions ``fa_fwd``, ``fa_fwd_host``, ``fa_fwd_status``,
+``fa_status_string``, ``fa_version`` and ``fa_set_test_hooks`` mirror the C
+entry points one to one and only marshal arguments.  ``attention`` is a
+convenience wrapper for torch tensors: it allocates the outputs with torch
+(device memory is the only thing torch provides here) and calls ``fa_fwd``.
+
+There is no fallback: if the library is missing or its call fails, these
+functions raise.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG, "libfa.so")
+
+FA_OK = 0
+FA_ERR_INVALID_ARG = 1
+FA_ERR_UNSUPPORTED = 2
+FA_ERR_CUDA = 3
+FA_ERR_DEVICE_TIMEOUT = 4
+
+FA_DTYPE_BF16 = 0
+FA_DTYPE_F32 = 1
+FA_DTYPE_F32_SIMT = 2
+
+EXPORTED = ("fa_fwd", "fa_fwd_host", "fa_fwd_status", "fa_status_string", "fa_version",
+            "fa_set_test_hooks")
+
+_lib = None
+
+
+class FaError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {fa_status_string(status)} ({status})")
+
+
+def load(path: str | None = None):
+    """Load libfa.so (raises if it has not been built)."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    p = path or LIB_PATH
+    if not os.path.exists(p):
+        raise RuntimeError(f"{p} is missing: build it with exact_attention_57_gb300.build")
+    lib = ctypes.CDLL(p)
+    vp, i, f = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+    lib.fa_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, i, vp]
+    lib.fa_fwd.restype = i
+    lib.fa_fwd_host.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp,
+                                i, i, i, i, i, f, i, i, vp]
+    lib.fa_fwd_host.restype = i
+    lib.fa_fwd_status.argtypes = [vp, ctypes.POINTER(i)]
+    lib.fa_fwd_status.restype = i
+    lib.fa_status_string.argtypes = [i]
+    lib.fa_status_string.restype = ctypes.c_char_p
+    lib.fa_version.argtypes = []
+    lib.fa_version.restype = i
+    lib.fa_set_test_hooks.argtypes = [i, ctypes.c_ulonglong]
+    lib.fa_set_test_hooks.restype = i
+    if path is None:
+        _lib = lib
+    return lib
+
+
+def fa_fwd(q, k, v, o, lse, B, H, Nq, Nk, d, scale, causal, dtype, stream) -> int:
+    """Raw C call; pointers and stream are integers (0 = NULL)."""
+    return load().fa_fwd(q, k, v, o, lse, B, H, Nq, Nk, d, float(scale), int(causal),
+                         int(dtype), stream)
+
+
+def fa_fwd_host(q_h, k_h, v_h, o_h, lse_h, q_d, k_d, v_d, o_d, lse_d,
+                B, H, Nq, Nk, d, scale, causal, dtype, stream) -> int:
+    return load().fa_fwd_host(q_h, k_h, v_h, o_h, lse_h, q_d, k_d, v_d, o_d, lse_d,
+                              B, H, Nq, Nk, d, float(scale), int(causal), int(dtype), stream)
+
+
+def fa_fwd_status(stream=None):
+    """Returns (status, raw device status word)."""
+    word = ctypes.c_int(0)
+    st = load().fa_fwd_status(stream, ctypes.byref(word))
+    return st, word.value
+
+
+def fa_status_string(status: int) -> str:
+    try:
+        return load().fa_status_string(int(status)).decode()
+    except RuntimeError:
+        return f"status {status}"
+
+
+def fa_version() -> int:
+    return load().fa_version()
+
+
+def fa_set_test_hooks(skip_v_load: int = 0, wait_limit_ns: int = 0) -> int:
+    return load().fa_set_test_hooks(int(skip_v_load), int(wait_limit_ns))
+
+
+# --------------------------------------------------------------- torch helpers
+def _dtype_code(t, impl: str) -> int:
+    import torch
+    if t.dtype == torch.bfloat16:
+        if impl != "tc":
+            raise ValueError("bf16 inputs run on the tensor-core kernel only")
+        return FA_DTYPE_BF16
+    if t.dtype == torch.float32:
+        return FA_DTYPE_F32 if impl == "tc" else FA_DTYPE_F32_SIMT
+    raise ValueError(f"unsupported dtype {t.dtype}")
+
+
+def attention(q, k, v, scale: float | None = None, causal: bool = False, impl: str = "tc",
+              out=None, lse=None, stream=None):
+    """O, LSE for contiguous CUDA tensors q [B,H,Nq,d], k/v [B,H,Nk,d].
+
+    impl "tc": bf16 -> tcgen05 kind::f16, fp32 -> tcgen05 kind::tf32;
+    impl "simt": fp32 only, plain fp32 kernel.  Raises FaError on failure.
+    """
+    import torch
+    if not (q.is_cuda and k.is_cuda and v.is_cuda):
+        raise ValueError("attention() needs CUDA tensors")
+    if q.dim() != 4 or k.dim() != 4 or v.shape != k.shape:
+        raise ValueError("q [B,H,Nq,d], k and v [B,H,Nk,d] expected")
+    B, H, Nq, d = q.shape
+    Nk = k.shape[2]
+    if k.shape[0] != B or k.shape[1] != H or k.shape[3] != d:
+        raise ValueError("k/v shape does not match q")
+    if not (q.is_contiguous() and k.is_contiguous() and v.is_contiguous()):
+        raise ValueError("contiguous [B,H,N,d] tensors expected")
+    code = _dtype_code(q, impl)
+    if k.dtype != q.dtype or v.dtype != q.dtype:
+        raise ValueError("q, k, v must share a dtype")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, H, Nq), device=q.device, dtype=torch.float32)
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device).cuda_stream
+    with torch.cuda.device(q.device):
+        st = fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
+                    B, H, Nq, Nk, d, scale, int(bool(causal)), code, stream)
+    if st != FA_OK:
+        raise FaError(st, "fa_fwd")
+    return out, lse

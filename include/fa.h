@@ -1,0 +1,147 @@
+/*
+ * fa.h — C ABI of the GB300 (sm_103a) exact-attention forward library.
+ *
+ * One operation: the fused, tiled, exact multi-head attention forward pass
+ *
+ *     O   = softmax(scale * Q K^T  [+ causal mask]) V
+ *     LSE = per-row log-sum-exp of the scaled, masked scores (natural log)
+ *
+ * as computed by the forward kernel of "flash_attention_2.cu"
+ * (leloykun/flash-hyperbolic-attention-minimal): scores are scaled before the
+ * row max, the softmax runs online over key tiles (running max m and sum l,
+ * partial O rescaled by exp(m_old - m_new)), and the kernel returns
+ * O = O / l together with L = m + log(l).  The loop order is the swapped one
+ * of "parallel execution of read/write operations (paper vs implementation)"
+ * (query tile outer, key tiles inner, O written once), and the grid runs over
+ * queries as well as batch and heads, as in "Meta's xFormers has Attention
+ * kernel written in CUTLASS" (forward parallelised across the queries).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * Layout:   q [B, H, Nq, d]; k, v [B, H, Nk, d]; o [B, H, Nq, d];
+ *           lse [B, H, Nq]; all contiguous, row-major (d fastest).  The
+ *           element (b, h, n, x) of q sits at ((b*H + h)*Nq + n)*d + x.
+ * Types:    dtype FA_DTYPE_BF16      q, k, v, o are bf16; fp32 accumulation.
+ *           dtype FA_DTYPE_F32       q, k, v, o are fp32; tensor-core TF32
+ *                                    products, fp32 accumulation.
+ *           dtype FA_DTYPE_F32_SIMT  q, k, v, o are fp32; plain fp32 FMA
+ *                                    kernel, no tensor cores.
+ *           lse is always fp32, natural log, in units of the scaled score.
+ * Masking:  causal = 1 keeps key j for query i iff j <= i (top-left aligned,
+ *           the rule of the forward kernel of "flash_attention_2.cu").  Keys
+ *           j >= Nk never take part; rows i >= Nq are not written.
+ * Scale:    any finite float; it multiplies q.k before the softmax.
+ * Streams:  `stream` is a cudaStream_t passed as void*; NULL means the legacy
+ *           default stream.  Work is enqueued asynchronously on that stream.
+ * Ownership: the caller owns every buffer.  The library never frees caller
+ *           memory and never keeps a pointer after the call returns.  Its
+ *           only allocation is one small per-device status buffer, made with
+ *           cudaMalloc on the first call on each device and kept until exit.
+ * Errors:   every function returns an fa_status code; nothing is printed and
+ *           nothing aborts the process.
+ * Threads:  entry points are reentrant; calls on different streams may run
+ *           concurrently.  The status word is shared per device.
+ */
+#ifndef FA_H
+#define FA_H
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define FA_VERSION 10000 /* 1.0.0 */
+
+typedef enum {
+    FA_DTYPE_BF16 = 0,
+    FA_DTYPE_F32 = 1,
+    FA_DTYPE_F32_SIMT = 2
+} fa_dtype;
+
+typedef enum {
+    FA_OK = 0,
+    FA_ERR_INVALID_ARG = 1,    /* null/misaligned pointer, size < 1, bad flag,
+                                  non-finite scale, overlapping buffers       */
+    FA_ERR_UNSUPPORTED = 2,    /* valid problem outside the compiled set, e.g.
+                                  head dim, or a device that is not sm_103    */
+    FA_ERR_CUDA = 3,           /* a CUDA runtime call or a launch failed      */
+    FA_ERR_DEVICE_TIMEOUT = 4  /* a kernel gave up waiting (see fa_fwd_status)*/
+} fa_status;
+
+/*
+ * fa_fwd — attention forward on device buffers.
+ *
+ * q, k, v   device pointers to the inputs (layout above), 16-byte aligned.
+ * o         device pointer to the output, 16-byte aligned; must not overlap
+ *           q, k, v or lse.  It need not be zeroed: every element of every
+ *           row i < Nq is written.
+ * lse       device pointer to B*H*Nq floats, 4-byte aligned; every entry is
+ *           written.
+ * B, H      batch size and number of heads, 1 .. 65535.
+ * Nq, Nk    query and key sequence lengths, >= 1 (ragged lengths allowed).
+ * d         head dimension.  FA_DTYPE_BF16: 64 or 128.  FA_DTYPE_F32: 64.
+ *           FA_DTYPE_F32_SIMT: 1 .. 128.  Anything else is
+ *           FA_ERR_UNSUPPORTED (the role of the "Failed to find groupsize ...
+ *           Shared Memory constraint" error of "Flash Attention Shared Memory
+ *           constraint", returned rather than raised).
+ * scale     finite multiplier of q.k (commonly 1/sqrt(d)).
+ * causal    0 or 1.
+ * dtype     an fa_dtype value.
+ * stream    cudaStream_t (as void*), or NULL.
+ *
+ * Returns FA_OK once the work is enqueued; argument errors are detected on
+ * the host before anything is enqueued.  A kernel that stops waiting on one of
+ * its internal barriers (a bounded wait, about two seconds) records it in the
+ * per-device status word; read it with fa_fwd_status.
+ */
+int fa_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
+           int B, int H, int Nq, int Nk, int d, float scale, int causal,
+           int dtype, void *stream);
+
+/*
+ * fa_fwd_host — the same forward on HOST buffers.
+ *
+ * q_h, k_h, v_h   host inputs (pinned memory gives full copy speed).
+ * o_h, lse_h      host outputs.
+ * q_d .. lse_d    caller-owned device buffers of the same sizes, used as the
+ *                 staging area; same alignment rules as fa_fwd.
+ * The call copies the inputs host->device on `stream`, runs fa_fwd, copies o
+ * and lse device->host, and synchronises `stream` before returning, so the
+ * host outputs are ready on return.  Returns the first failing status.
+ */
+int fa_fwd_host(const void *q_h, const void *k_h, const void *v_h,
+                void *o_h, float *lse_h,
+                void *q_d, void *k_d, void *v_d, void *o_d, float *lse_d,
+                int B, int H, int Nq, int Nk, int d, float scale, int causal,
+                int dtype, void *stream);
+
+/*
+ * fa_fwd_status — synchronise `stream`, then read and clear the current
+ * device's status word.  *device_status (may be NULL) receives the raw word:
+ * 0 when every kernel finished normally; otherwise bit r set means a warp of
+ * role r gave up on a bounded wait (1 = TMA producer, 2 = MMA issuer,
+ * 4 = softmax/epilogue warps, 8 = fault injected by the test hook).
+ * Returns FA_OK, FA_ERR_DEVICE_TIMEOUT (word != 0) or FA_ERR_CUDA.
+ */
+int fa_fwd_status(void *stream, int *device_status);
+
+/* Human-readable name of an fa_status value (static storage). */
+const char *fa_status_string(int status);
+
+/* FA_VERSION of the compiled library. */
+int fa_version(void);
+
+/*
+ * fa_set_test_hooks — testing aid, process-wide.
+ * skip_v_load != 0 makes the next launches of the tensor-core kernels skip the
+ * first V-tile load, so the MMA issuer's bounded wait runs out and the kernel
+ * returns through its error path (status bit 8 plus the role bits).
+ * wait_limit_ns sets the bounded-wait limit in nanoseconds (0 = default,
+ * 2e9).  Returns FA_OK.
+ */
+int fa_set_test_hooks(int skip_v_load, unsigned long long wait_limit_ns);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_H */

@@ -1,0 +1,89 @@
+"""The C-ABI library loads and exports what include/fa.h declares; host-side
+argument checks (no GPU needed: these calls return before any CUDA work)."""
+import os
+import re
+
+import pytest
+
+from exact_attention_57_gb300 import fa
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def header_functions():
+    txt = open(os.path.join(ROOT, "include", "fa.h")).read()
+    txt = re.sub(r"/\*.*?\*/", "", txt, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(fa_\w+)\s*\(", txt, flags=re.M)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(fa.LIB_PATH):
+        from exact_attention_57_gb300 import build
+        build.build_library()
+    return fa.load()
+
+
+def test_header_declares_the_entry_points():
+    names = header_functions()
+    assert set(names) == set(fa.EXPORTED), names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in header_functions():
+        assert hasattr(lib, name), f"libfa.so does not export {name}"
+
+
+def test_version_and_strings(lib):
+    assert fa.fa_version() == 10000
+    assert fa.fa_status_string(0) == "FA_OK"
+    assert fa.fa_status_string(1) == "FA_ERR_INVALID_ARG"
+    assert fa.fa_status_string(2) == "FA_ERR_UNSUPPORTED"
+    assert fa.fa_status_string(4) == "FA_ERR_DEVICE_TIMEOUT"
+    assert fa.fa_status_string(99) == "FA_ERR_UNKNOWN"
+
+
+# Fake, never-dereferenced device addresses (16-byte aligned, disjoint).
+Q, K, V, O, L = 0x100000, 0x200000, 0x300000, 0x400000, 0x500000
+
+
+def call(**kw):
+    a = dict(q=Q, k=K, v=V, o=O, lse=L, B=1, H=1, Nq=16, Nk=16, d=64, scale=0.125,
+             causal=0, dtype=fa.FA_DTYPE_BF16, stream=None)
+    a.update(kw)
+    return fa.fa_fwd(a["q"], a["k"], a["v"], a["o"], a["lse"], a["B"], a["H"], a["Nq"], a["Nk"],
+                     a["d"], a["scale"], a["causal"], a["dtype"], a["stream"])
+
+
+@pytest.mark.parametrize("kw", [
+    dict(q=None), dict(k=None), dict(v=None), dict(o=None), dict(lse=None),
+    dict(B=0), dict(H=0), dict(Nq=0), dict(Nk=0), dict(d=0), dict(B=-3),
+    dict(B=70000), dict(H=70000),
+    dict(scale=float("nan")), dict(scale=float("inf")),
+    dict(causal=2), dict(causal=-1), dict(dtype=3), dict(dtype=-1),
+    dict(q=Q + 8), dict(o=O + 4), dict(lse=L + 2),
+    dict(o=Q), dict(o=Q + 1024), dict(lse=O + 16), dict(lse=K + 64),
+], ids=lambda kw: ",".join(f"{k}={v}" for k, v in kw.items()))
+def test_invalid_arguments(lib, kw):
+    assert call(**kw) == fa.FA_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("kw", [
+    dict(dtype=fa.FA_DTYPE_BF16, d=32), dict(dtype=fa.FA_DTYPE_BF16, d=96),
+    dict(dtype=fa.FA_DTYPE_BF16, d=256), dict(dtype=fa.FA_DTYPE_F32, d=128),
+    dict(dtype=fa.FA_DTYPE_F32, d=32), dict(dtype=fa.FA_DTYPE_F32_SIMT, d=129),
+], ids=lambda kw: ",".join(f"{k}={v}" for k, v in kw.items()))
+def test_unsupported_problems(lib, kw):
+    """Valid problems outside the compiled set are refused, not attempted."""
+    assert call(**kw) == fa.FA_ERR_UNSUPPORTED
+
+
+def test_host_variant_rejects_null_host_buffers(lib):
+    r = fa.fa_fwd_host(None, 0x10, 0x20, 0x30, 0x40, Q, K, V, O, L, 1, 1, 16, 16, 64, 0.1, 0,
+                       fa.FA_DTYPE_BF16, None)
+    assert r == fa.FA_ERR_INVALID_ARG
+
+
+def test_binding_fails_loudly_without_library(tmp_path):
+    with pytest.raises(RuntimeError):
+        fa.load(str(tmp_path / "missing.so"))

@@ -1,0 +1,35 @@
+"""Bounded waits: a starved kernel gives up, reports through the status word,
+and leaves the context usable.  The failure is made on the host (a test hook
+that skips one V-tile load), never by faulting or trapping the GPU."""
+import math
+
+import pytest
+import torch
+
+from exact_attention_57_gb300 import fa
+from exact_attention_57_gb300.workloads import DTYPE_BF16, make_inputs
+from parity_util import compare, run_gpu, run_oracle
+
+pytestmark = pytest.mark.gpu
+
+
+def test_starved_kernel_times_out_and_recovers():
+    dev = torch.device("cuda:0")
+    q, k, v = (t.to(dev) for t in make_inputs(1, 2, 512, 512, 128, DTYPE_BF16, seed=3))
+    stream = torch.cuda.current_stream(dev).cuda_stream
+    assert fa.fa_fwd_status(stream)[0] == fa.FA_OK
+    try:
+        fa.fa_set_test_hooks(skip_v_load=1, wait_limit_ns=200_000_000)  # 0.2 s
+        fa.attention(q, k, v, causal=False)
+        st, word = fa.fa_fwd_status(stream)
+    finally:
+        fa.fa_set_test_hooks(0, 0)
+    assert st == fa.FA_ERR_DEVICE_TIMEOUT
+    assert word & 8, word          # the injected skip was recorded
+    assert word & 2, word          # the UMMA issuer gave up waiting for V
+    # the status word was cleared by the read, and the context still works
+    assert fa.fa_fwd_status(stream) == (fa.FA_OK, 0)
+    qc, kc, vc = (t.cpu() for t in (q, k, v))
+    o, lse = run_gpu(qc, kc, vc, 1 / math.sqrt(128), False, DTYPE_BF16)
+    ro, rl = run_oracle(qc, kc, vc, 1 / math.sqrt(128), False)
+    compare(o, lse, ro, rl, DTYPE_BF16, "after timeout")
