@@ -124,6 +124,17 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+def max_over_ranks(x: float, device=None) -> float:
+    """Max of a per-rank scalar over every rank (identity without a group)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def dist_env():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -131,7 +142,13 @@ def dist_env():
     return ws, rank, local
 
 
-def cpu_oracle_sample(w, budget_s: float, seed: int = 7):
+def oracle_inputs(w):
+    """The workload's seeded CPU inputs as float32 numpy arrays for the oracle."""
+    from exact_attention_57_gb300.workloads import workload_inputs
+    return tuple(t.float().numpy() for t in workload_inputs(w))
+
+
+def cpu_oracle_sample(w, budget_s: float, seed: int = 7, arrays=None):
     """Time the float64 oracle on sampled query rows of the workload.
 
     Returns (GFLOP/s in the metric's units, threads, description).  Rows are
@@ -142,10 +159,8 @@ def cpu_oracle_sample(w, budget_s: float, seed: int = 7):
     import numpy as np
 
     import oracle
-    from exact_attention_57_gb300.workloads import workload_inputs
 
-    q, k, v = workload_inputs(w)
-    qf, kf, vf = (t.float().numpy() for t in (q, k, v))
+    qf, kf, vf = arrays if arrays is not None else oracle_inputs(w)
     causal = w.causal[0]
     rng = np.random.default_rng(seed)
     threads = os.cpu_count() or 1
@@ -179,8 +194,9 @@ def run_reference(args, w):
     rates = []
     per_step = max(2.0, 120.0 / max(1, args.steps + args.warmup))
     tot_t = 0.0
+    arrays = oracle_inputs(w)
     for s in range(args.warmup + args.steps):
-        g, threads, desc, dt = cpu_oracle_sample(w, per_step, seed=100 + s)
+        g, threads, desc, dt = cpu_oracle_sample(w, per_step, seed=100 + s, arrays=arrays)
         if s >= args.warmup:
             rates.append(g)
             tot_t += dt
@@ -278,11 +294,7 @@ def main():
     if st != fa.FA_OK:
         raise RuntimeError(f"timed-region device status {word}")
     launch_ms = [ev[i].elapsed_time(ev[i + 1]) for i in range(args.steps)]
-    total_ms = ev[0].elapsed_time(ev[-1])
-    if ws > 1:
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(ev[0].elapsed_time(ev[-1]), dev)
     ms_per_step = total_ms / args.steps
     flops_step = w.flops(causal)
     value = ws * flops_step * args.steps / (total_ms / 1e3) / 1e12
@@ -313,11 +325,7 @@ def main():
         t0 = time.perf_counter()
         for _ in range(e2e_steps):
             e2e_step()
-        dt = time.perf_counter() - t0
-        if ws > 1:
-            t = torch.tensor([dt], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            dt = float(t.item())
+        dt = max_over_ranks(time.perf_counter() - t0, dev)
         e2e = {"value": ws * flops_step * e2e_steps / dt / 1e12, "unit": "TFLOP/s",
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                "ms_per_step": 1e3 * dt / e2e_steps}
