@@ -66,7 +66,7 @@ def profiled_traffic(kernel: str, workload: str):
 
 
 class ClockSampler:
-    """nvidia-smi clocks/throttle reasons sampled every 200 ms while running."""
+    """nvidia-smi clocks/throttle reasons sampled every 100 ms while running."""
 
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -82,7 +82,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "100"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
@@ -219,7 +219,7 @@ def run_reference(args, w):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="fa", choices=["fa", "reference"])
     ap.add_argument("--workload", default=None)
@@ -228,8 +228,8 @@ def main():
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
 
-    from exact_attention_57_gb300.workloads import BENCH_WORKLOAD, WORKLOADS
-    w = WORKLOADS[args.workload or BENCH_WORKLOAD]
+    from exact_attention_57_gb300.workloads import BENCH_WORKLOAD, PROFILE_WORKLOADS, WORKLOADS
+    w = {**WORKLOADS, **PROFILE_WORKLOADS}[args.workload or BENCH_WORKLOAD]
     if args.impl == "reference":
         return run_reference(args, w)
 

@@ -78,6 +78,14 @@ WORKLOADS = {
 # The workload the benchmark times at one GPU.
 BENCH_WORKLOAD = "b8h32n8192d128-bf16-causal"
 
+# Same shape per head as the benchmark with 1/8 of the heads (inputs still
+# larger than L2): the case the detailed profiler captures are taken on.
+PROFILE_WORKLOADS = {
+    "b2h16n8192d128-bf16-causal": Workload(
+        "b2h16n8192d128-bf16-causal", 2, 16, 8192, 8192, 128, DTYPE_BF16,
+        causal=(True,), seed=57005, note="profiling case, 1/8 of the benchmark's heads"),
+}
+
 
 def make_inputs(B: int, H: int, Nq: int, Nk: int, d: int, dtype: int,
                 seed: int, k_mult: float = 1.0):
