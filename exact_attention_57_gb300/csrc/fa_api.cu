@@ -251,3 +251,125 @@ int fa_set_test_hooks(int skip_v_load, unsigned long long wait_limit_ns) {
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// No-allocation variant.
+//
+// fa_fwd keeps its per-device status word in memory it obtains with
+// cudaMalloc on the first call.  Some callers cannot let a library do that: a
+// serving process that reserves all of the GPU's memory for its own pool at
+// start-up (a cudaMalloc from inside a call then fails, or eats into memory
+// the pool has promised elsewhere), a latency-critical loop where the implicit
+// device-wide synchronisation of cudaMalloc would stall other streams, or a
+// framework whose memory manager must account for every device allocation.
+// fa_fwd_noalloc gives them the same forward with the status word kept in a
+// fixed array that is part of the library's device image instead.
+// ---------------------------------------------------------------------------
+namespace {
+
+// Scratch of the no-allocation path: word 0 is the status word the kernels OR
+// their give-up bits into; the rest is padding to the alignment.  It is part
+// of the library's device image, so every GPU that loads the library holds
+// these 256 bytes until the process exits.  All calls share it.
+constexpr size_t kNoallocScratchBytes = 256;
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoallocScratchBytes];
+
+unsigned *g_noalloc_status[kMaxDevices] = {};  // device address of word 0, per device
+
+// sm_103 check and the scratch's device address for the current device; the
+// address is looked up once per device, with that device current.
+int noalloc_setup(unsigned **status) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return FA_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return FA_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (g_dev_ok[dev] == 0) {
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+      return FA_ERR_CUDA;
+    g_dev_ok[dev] = (major == 10 && minor == 3) ? 1 : -1;
+  }
+  if (g_dev_ok[dev] != 1) return FA_ERR_UNSUPPORTED;
+  if (g_noalloc_status[dev] == nullptr) {
+    void *ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || ptr == nullptr)
+      return FA_ERR_CUDA;
+    g_noalloc_status[dev] = static_cast<unsigned *>(ptr);
+  }
+  *status = g_noalloc_status[dev];
+  return FA_OK;
+}
+
+}  // namespace
+
+extern "C" int fa_fwd_noalloc(const void *q, const void *k, const void *v, void *o, float *lse,
+                              int B, int H, int Nq, int Nk, int d, float scale, int causal,
+                              int dtype, void *stream, int *device_status) {
+  if (device_status) *device_status = 0;
+  int rc = validate(q, k, v, o, lse, B, H, Nq, Nk, d, scale, causal, dtype);
+  if (rc != FA_OK) return rc;
+  // Scratch this call needs: one status word, whatever the problem size.
+  const size_t need = sizeof(unsigned);
+  if (need > kNoallocScratchBytes) return FA_ERR_UNSUPPORTED;
+  unsigned *status = nullptr;
+  if ((rc = noalloc_setup(&status)) != FA_OK) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // The array keeps the previous call's contents: the status word must start
+  // at zero for this call.
+  if (cudaMemsetAsync(status, 0, need, s) != cudaSuccess) return FA_ERR_CUDA;
+
+  if (dtype == FA_DTYPE_F32_SIMT) {
+    fa::SimtParams p;
+    p.q = static_cast<const float *>(q);
+    p.k = static_cast<const float *>(k);
+    p.v = static_cast<const float *>(v);
+    p.o = static_cast<float *>(o);
+    p.lse = lse;
+    p.status = status;
+    p.H = H;
+    p.Nq = Nq;
+    p.Nk = Nk;
+    p.d = d;
+    p.n_qtiles = ceil_div(Nq, fa::BM);
+    p.scale = scale;
+    p.causal = causal;
+    if (fa::launch_simt(p, B, s) != cudaSuccess) return FA_ERR_CUDA;
+  } else {
+    if ((rc = get_encoder()) != FA_OK) return rc;
+    CUtensorMap mq, mk, mv, mo;
+    const int BH = B * H;
+    if ((rc = encode_map(&mq, q, dtype, BH, Nq, d)) != FA_OK) return rc;
+    if ((rc = encode_map(&mk, k, dtype, BH, Nk, d)) != FA_OK) return rc;
+    if ((rc = encode_map(&mv, v, dtype, BH, Nk, d)) != FA_OK) return rc;
+    if ((rc = encode_map(&mo, o, dtype, BH, Nq, d)) != FA_OK) return rc;
+    fa::TcParams p;
+    p.lse = lse;
+    p.status = status;
+    p.H = H;
+    p.Nq = Nq;
+    p.Nk = Nk;
+    p.n_qtiles = ceil_div(Nq, fa::BM);
+    p.n_ktiles = ceil_div(Nk, fa::BN);
+    p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+    p.scale_neg = scale < 0.f ? 1 : 0;
+    const unsigned long long lim = g_wait_limit_ns.load();
+    p.wait_limit_ns = lim ? lim : fa::kDefaultWaitLimitNs;
+    p.skip_v_load = g_skip_v_load.load();
+    cudaError_t e;
+    if (dtype == FA_DTYPE_BF16)
+      e = (d == 64) ? fa::launch_tc_bf16_d64(mq, mk, mv, mo, p, B, causal, s)
+                    : fa::launch_tc_bf16_d128(mq, mk, mv, mo, p, B, causal, s);
+    else
+      e = fa::launch_tc_f32_d64(mq, mk, mv, mo, p, B, causal, s);
+    if (e != cudaSuccess) return FA_ERR_CUDA;
+  }
+  if (device_status == nullptr) return FA_OK;
+  // Synchronous form: wait for the kernel and report its status word.
+  unsigned word = 0;
+  if (cudaMemcpyAsync(&word, status, sizeof word, cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+      cudaStreamSynchronize(s) != cudaSuccess)
+    return FA_ERR_CUDA;
+  *device_status = static_cast<int>(word);
+  return word ? FA_ERR_DEVICE_TIMEOUT : FA_OK;
+}

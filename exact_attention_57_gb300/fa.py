@@ -29,7 +29,7 @@ FA_DTYPE_F32 = 1
 FA_DTYPE_F32_SIMT = 2
 
 EXPORTED = ("fa_fwd", "fa_fwd_host", "fa_fwd_status", "fa_status_string", "fa_version",
-            "fa_set_test_hooks")
+            "fa_set_test_hooks", "fa_fwd_noalloc")
 
 _lib = None
 
@@ -52,6 +52,9 @@ def load(path: str | None = None):
     vp, i, f = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
     lib.fa_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, i, vp]
     lib.fa_fwd.restype = i
+    lib.fa_fwd_noalloc.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, i, vp,
+                                   ctypes.POINTER(i)]
+    lib.fa_fwd_noalloc.restype = i
     lib.fa_fwd_host.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp,
                                 i, i, i, i, i, f, i, i, vp]
     lib.fa_fwd_host.restype = i
@@ -72,6 +75,19 @@ def fa_fwd(q, k, v, o, lse, B, H, Nq, Nk, d, scale, causal, dtype, stream) -> in
     """Raw C call; pointers and stream are integers (0 = NULL)."""
     return load().fa_fwd(q, k, v, o, lse, B, H, Nq, Nk, d, float(scale), int(causal),
                          int(dtype), stream)
+
+
+def fa_fwd_noalloc(q, k, v, o, lse, B, H, Nq, Nk, d, scale, causal, dtype, stream,
+                   wait: bool = True):
+    """Raw C call of the entry point that allocates no device memory.
+
+    With wait=True the call synchronises the stream and returns
+    (status, raw status word); with wait=False it only enqueues and returns
+    (status, None)."""
+    word = ctypes.c_int(0)
+    st = load().fa_fwd_noalloc(q, k, v, o, lse, B, H, Nq, Nk, d, float(scale), int(causal),
+                               int(dtype), stream, ctypes.byref(word) if wait else None)
+    return st, (word.value if wait else None)
 
 
 def fa_fwd_host(q_h, k_h, v_h, o_h, lse_h, q_d, k_d, v_d, o_d, lse_d,

@@ -98,6 +98,40 @@ int fa_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
            int dtype, void *stream);
 
 /*
+ * fa_fwd_noalloc — fa_fwd for callers that cannot allocate device memory.
+ * The pages have no counterpart to this entry point; it exists for how the
+ * library is deployed, not for the method.
+ *
+ * fa_fwd obtains its per-device status word with cudaMalloc on its first call
+ * on each device.  Some callers cannot allow that: a serving process that
+ * reserves all of the GPU's memory for its own pool at start-up, a
+ * latency-critical loop that must not pay the device-wide synchronisation a
+ * cudaMalloc implies, or a framework whose memory manager has to account for
+ * every device allocation.  This entry point runs the same kernels but keeps
+ * the status word in a fixed 256-byte array that is part of the library's
+ * device image (every GPU that loads the library holds it until exit), and
+ * calls no cudaMalloc, cudaFree or other allocating routine.
+ *
+ * Arguments q .. stream are those of fa_fwd, with the same layout, alignment
+ * and validation.  The scratch this call needs is one status word whatever the
+ * problem size; a need beyond the 256-byte array would be refused with
+ * FA_ERR_UNSUPPORTED before anything is enqueued.
+ * device_status  NULL: the call returns once the work is enqueued and does
+ *                not report the status word.  Non-NULL: the call waits for the
+ *                stream, stores the raw status word there (bits as in
+ *                fa_fwd_status) and returns FA_ERR_DEVICE_TIMEOUT if it is
+ *                non-zero.
+ * Set-up: the first call on each device looks up the array's device address
+ * (with that device current); make that first call before any stream capture.
+ * Sharing: every call uses the same array and clears the status word on its
+ * stream before launching; calls whose work overlaps on the GPU (different
+ * streams, or another thread) race on that word, so serialise them.
+ */
+int fa_fwd_noalloc(const void *q, const void *k, const void *v, void *o, float *lse,
+                   int B, int H, int Nq, int Nk, int d, float scale, int causal,
+                   int dtype, void *stream, int *device_status);
+
+/*
  * fa_fwd_host — the same forward on HOST buffers.
  *
  * q_h, k_h, v_h   host inputs (pinned memory gives full copy speed).
