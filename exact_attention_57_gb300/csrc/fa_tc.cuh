@@ -12,19 +12,28 @@
 // Multi-Head Attention example" (cuTile.jl).
 //
 // GB300 design (one CTA = one (batch, head, 128-row query tile)):
-//   warp 4       TMA producer: Q once, then K_j / V_j through shared-memory
-//                rings (full/empty mbarriers), L2 evict-last for K/V.
-//   warp 5       UMMA issuer (one lane): S_j = Q K_j^T into a double-buffered
-//                tensor-memory score tile, O += P_j V_j with P read from
-//                tensor memory, both fp32-accumulating.  Owns the TMEM
-//                allocation.
 //   warps 0-3    softmax, correction and epilogue: one query row per thread
-//                (= one TMEM lane).  Loads the 128 scores of its row, masks
-//                the causal diagonal / ragged key tail, updates m and l, writes
-//                P (bf16, or tf32 for fp32 inputs) back over S in TMEM, and at
-//                the end normalises O, stages it swizzled in shared memory for
-//                a TMA store, and writes LSE.
-// Tensor memory: S0 cols [0,128), S1 [128,256), O [256, 256+D).
+//                (= one TMEM lane).  First copy the thread's Q row from global
+//                memory into tensor memory (the A operand of S = Q K^T, so
+//                shared memory only carries K and V).  Per key tile: load the
+//                row's 128 scores, mask the causal diagonal / ragged key tail,
+//                update m and l, write P back over S in TMEM.  A fixed share
+//                of the exponentials runs as a polynomial on the FMA pipes to
+//                relieve the MUFU unit.  At the end normalise O, stage it
+//                swizzled in shared memory for a TMA store, and write LSE.
+//   warp 4       TMA producer: K_j / V_j through shared-memory rings
+//                (full/empty mbarriers), L2 evict-last.
+//   warp 5       UMMA issuer (one lane): S_j = Q K_j^T (A from TMEM, B = K_j
+//                K-major in shared memory) into a double-buffered score tile,
+//                then O += P_j V_j (A = P from TMEM), fp32 accumulation.  Owns
+//                the TMEM allocation.
+// bf16 inputs (kind::f16): P is bf16; V_j is an MN-major B operand as loaded.
+// fp32 inputs (kind::tf32): the tensor core truncates fp32 operands to tf32,
+// which biases the scores; so Q (on its way to TMEM) and K_j (in place, by the
+// softmax warps, before S_j is issued) are rounded to nearest first.  P is
+// tf32.  kind::tf32 takes its B operand K-major only, so the softmax warps
+// also transpose each V_j into a tf32 V_j^T buffer (d rows of 128 keys).
+// Tensor memory: S0 cols [0,128), S1 [128,256), O [256, 256+D), Q [384, ...).
 //
 // Rescaling: the running max used as the exponent offset only moves when a
 // row's max grows by more than 2^8; otherwise the stale offset is kept.  The
@@ -53,20 +62,30 @@ struct TcCfg {
   static constexpr int CHUNK_BYTES = 128 * 128;             // one chunk of 128 rows
   static constexpr int TILE_BYTES = NCH * CHUNK_BYTES;      // one 128-row tile
   static constexpr int UK = 32 / ESZ;                       // K extent of one UMMA
-  static constexpr int KST = (TILE_BYTES <= 16384) ? 3 : 2; // K ring depth
-  static constexpr int VST = (TILE_BYTES <= 16384) ? 3 : 2; // V ring depth
-  static constexpr int OFF_Q = 0;
-  static constexpr int OFF_K = OFF_Q + TILE_BYTES;
+  static constexpr int KST = TF32 ? 2 : (TILE_BYTES <= 16384 ? 4 : 3); // K ring depth
+  static constexpr int VST = TF32 ? 2 : (TILE_BYTES <= 16384 ? 4 : 3); // V ring depth
+  // fp32 path: V_j is transposed by the softmax warps into a K-major copy
+  // (V^T, d rows of 128 keys, tf32-rounded) because P V runs as kind::tf32
+  // with V^T as a K-major B operand.  Two copies alternate.
+  static constexpr int NVT = TF32 ? 2 : 0;
+  static constexpr int VT_CHUNK_BYTES = D * 128;            // 32 keys x D rows
+  static constexpr int OFF_K = 0;
   static constexpr int OFF_V = OFF_K + KST * TILE_BYTES;
-  static constexpr int OFF_BAR = OFF_V + VST * TILE_BYTES;
-  // q, kfull[KST], kempty[KST], vfull[VST], vempty[VST], sfull[2], pfull[2], odone, fin
-  static constexpr int NBAR = 1 + 2 * KST + 2 * VST + 2 + 2 + 1 + 1;
+  static constexpr int OFF_VT = OFF_V + VST * TILE_BYTES;
+  static constexpr int OFF_BAR = OFF_VT + NVT * TILE_BYTES;
+  // qready, kfull[KST], kempty[KST], vfull[VST], vempty[VST], sfull[2], pfull[2],
+  // odone, fin, kready[KST]
+  static constexpr int NBAR = 1 + 2 * KST + 2 * VST + 2 + 2 + 1 + 1 + KST;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;       // tmem base, abort flag
   static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;   // + alignment slack
   static constexpr uint32_t TMEM_COLS = 512;
-  static constexpr uint32_t COL_S0 = 0, COL_S1 = 128, COL_O = 256;
+  static constexpr uint32_t COL_S0 = 0, COL_S1 = 128, COL_O = 256, COL_Q = 384;
+  static constexpr int Q_COLS = D * ESZ / 4;                // 32-bit columns of one Q row
   static constexpr int THREADS = 192;
+  // Exponentials per 8 column pairs computed by the FMA-pipe polynomial.
+  static constexpr int EMU_PER_8 = TF32 ? 0 : 3;
   static_assert(NCH >= 1 && D % 32 == 0, "head dim must fill whole 128-byte chunks");
+  static_assert(COL_O + D <= COL_Q && COL_Q + Q_COLS <= TMEM_COLS, "tensor memory budget");
   static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
 };
 
@@ -103,8 +122,7 @@ __device__ __forceinline__ bool bounded_wait(uint32_t bar, uint32_t parity, cons
 
 template <int D, bool TF32, bool CAUSAL>
 __global__ void __launch_bounds__(192, 1)
-    fa_tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
-                     const __grid_constant__ CUtensorMap tm_k,
+    fa_tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_v,
                      const __grid_constant__ CUtensorMap tm_o, const TcParams p) {
   using C = TcCfg<D, TF32>;
@@ -112,11 +130,11 @@ __global__ void __launch_bounds__(192, 1)
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const uint32_t sbase = smem_u32(smem);
-  const uint32_t sQ = sbase + C::OFF_Q;
   const uint32_t sK = sbase + C::OFF_K;
   const uint32_t sV = sbase + C::OFF_V;
-  const uint32_t bQ = sbase + C::OFF_BAR;
-  const uint32_t bKfull = bQ + 8;                      // + 8*stage
+  const uint32_t sVT = sbase + C::OFF_VT;
+  const uint32_t bQready = sbase + C::OFF_BAR;
+  const uint32_t bKfull = bQready + 8;                 // + 8*stage
   const uint32_t bKempty = bKfull + 8 * C::KST;
   const uint32_t bVfull = bKempty + 8 * C::KST;
   const uint32_t bVempty = bVfull + 8 * C::VST;
@@ -124,6 +142,7 @@ __global__ void __launch_bounds__(192, 1)
   const uint32_t bPfull = bSfull + 16;                 // + 8*buffer
   const uint32_t bOdone = bPfull + 16;
   const uint32_t bFin = bOdone + 8;
+  const uint32_t bKready = bFin + 8;                   // + 8*stage (fp32 path)
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::OFF_MISC);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::OFF_MISC + 4);
 
@@ -138,7 +157,7 @@ __global__ void __launch_bounds__(192, 1)
   const int n_kt = CAUSAL ? min(qt + 1, p.n_ktiles) : p.n_ktiles;
 
   if (threadIdx.x == 0) {
-    mbar_init(bQ, 1);
+    mbar_init(bQready, 128);
 #pragma unroll
     for (int s = 0; s < C::KST; ++s) {
       mbar_init(bKfull + 8 * s, 1);
@@ -147,8 +166,11 @@ __global__ void __launch_bounds__(192, 1)
 #pragma unroll
     for (int s = 0; s < C::VST; ++s) {
       mbar_init(bVfull + 8 * s, 1);
-      mbar_init(bVempty + 8 * s, 1);
+      // fp32 path: the softmax warps release a V stage once they transposed it
+      mbar_init(bVempty + 8 * s, TF32 ? 128 : 1);
     }
+#pragma unroll
+    for (int s = 0; s < C::KST; ++s) mbar_init(bKready + 8 * s, 128);
     mbar_init(bSfull, 1);
     mbar_init(bSfull + 8, 1);
     mbar_init(bPfull, 128);
@@ -160,7 +182,6 @@ __global__ void __launch_bounds__(192, 1)
     fence_proxy_async_smem();
   }
   if (warp == 4 && lane == 0) {
-    tma_prefetch_desc(&tm_q);
     tma_prefetch_desc(&tm_k);
     tma_prefetch_desc(&tm_v);
     tma_prefetch_desc(&tm_o);
@@ -179,12 +200,7 @@ __global__ void __launch_bounds__(192, 1)
     // ------------------------------------------------------------ producer
     w.role = kStatusProducer;
     if (lane == 0) {
-      const uint64_t pol_q = l2_policy_evict_first();
       const uint64_t pol_kv = l2_policy_evict_last();
-      mbar_arrive_expect_tx(bQ, C::TILE_BYTES);
-#pragma unroll
-      for (int c = 0; c < C::NCH; ++c)
-        tma_load_3d(sQ + c * C::CHUNK_BYTES, &tm_q, bQ, c * C::CH_ELEMS, q0, bh, pol_q);
       int nk = 0, nv = 0;  // loads issued
       bool ok = true;
       // Load order = consumption order: K0, K1, V0, K2, V1, ...
@@ -218,7 +234,6 @@ __global__ void __launch_bounds__(192, 1)
         }
       }
       // Drain: no TMA write may still be in flight when the CTA exits.
-      bounded_wait(bQ, 0, w, false);
       for (int s = 0; s < C::KST; ++s) {
         const int cnt = (nk > s) ? (nk - 1 - s) / C::KST + 1 : 0;
         if (cnt > 0) bounded_wait(bKfull + 8 * s, (cnt - 1) & 1, w, false);
@@ -234,20 +249,24 @@ __global__ void __launch_bounds__(192, 1)
     w.role = kStatusMma;
     if (lane == 0) {
       constexpr uint32_t kFmt = TF32 ? 2u : 1u;
-      constexpr uint32_t kIdescQK = make_idesc(kFmt, BM, BN, 0u, 0u);  // Q, K both K-major
-      constexpr uint32_t kIdescPV = make_idesc(kFmt, BM, D, 0u, 1u);   // V is MN-major
-      bool ok = bounded_wait(bQ, 0, w);
+      constexpr uint32_t kIdescQK = make_idesc(kFmt, BM, BN, 0u, 0u);  // K is K-major
+      // bf16: V is an MN-major B operand.  fp32: V^T is a K-major B operand.
+      constexpr uint32_t kIdescPV = make_idesc(kFmt, BM, D, 0u, TF32 ? 0u : 1u);
+      bool ok = bounded_wait(bQready, 0, w);
+      if (ok) tc_fence_after();
       auto issue_qk = [&](int j) -> bool {
         const int s = j % C::KST;
-        if (!bounded_wait(bKfull + 8 * s, (j / C::KST) & 1, w)) return false;
+        // fp32 path: K_j must first be rounded to tf32 by the softmax warps
+        if (!bounded_wait((TF32 ? bKready : bKfull) + 8 * s, (j / C::KST) & 1, w)) return false;
         tc_fence_after();
         const uint32_t d_tmem = tmem + ((j & 1) ? C::COL_S1 : C::COL_S0);
         const uint32_t kb = sK + s * C::TILE_BYTES;
 #pragma unroll
         for (int kk = 0; kk < D / C::UK; ++kk) {
-          // 32 bytes of K per UMMA; 4 steps per 128-byte swizzle chunk.
+          // 32 bytes of K per UMMA (4 steps per 128-byte swizzle chunk); the
+          // matching Q slice is 8 TMEM columns.
           const uint32_t off = (kk >> 2) * C::CHUNK_BYTES + (kk & 3) * 32;
-          umma_ss<TF32>(d_tmem, sdesc_sw128(sQ + off, 16, 1024), sdesc_sw128(kb + off, 16, 1024),
+          umma_ts<TF32>(d_tmem, tmem + C::COL_Q + kk * 8, sdesc_sw128(kb + off, 16, 1024),
                         kIdescQK, kk > 0 ? 1u : 0u);
         }
         tc_commit(bKempty + 8 * s);
@@ -257,20 +276,30 @@ __global__ void __launch_bounds__(192, 1)
       if (ok) ok = issue_qk(0);
       for (int j = 0; ok && j < n_kt; ++j) {
         if (j + 1 < n_kt && !(ok = issue_qk(j + 1))) break;
+        // P_j ready (fp32 path: also V_j^T written).
         if (!(ok = bounded_wait(bPfull + 8 * (j & 1), (j >> 1) & 1, w))) break;
         const int s = j % C::VST;
-        if (!(ok = bounded_wait(bVfull + 8 * s, (j / C::VST) & 1, w))) break;
+        if constexpr (!TF32) {
+          if (!(ok = bounded_wait(bVfull + 8 * s, (j / C::VST) & 1, w))) break;
+        }
         tc_fence_after();
         const uint32_t a_tmem = tmem + ((j & 1) ? C::COL_S1 : C::COL_S0);
-        const uint32_t vb = sV + s * C::TILE_BYTES;
 #pragma unroll
         for (int kk = 0; kk < BN / C::UK; ++kk) {
-          // UK keys per UMMA: UK rows of 128 bytes; P advances 8 TMEM columns.
-          umma_ts<TF32>(tmem + C::COL_O, a_tmem + kk * 8,
-                        sdesc_sw128(vb + kk * C::UK * 128, C::CHUNK_BYTES, 1024), kIdescPV,
+          // UK keys per UMMA; the P slice is 8 TMEM columns.
+          uint64_t bdesc;
+          if constexpr (TF32) {
+            // V^T: D rows of 128 keys, K-major, 32 keys per 128-byte chunk
+            const uint32_t vt = sVT + (j & 1) * C::TILE_BYTES;
+            bdesc = sdesc_sw128(vt + (kk >> 2) * C::VT_CHUNK_BYTES + (kk & 3) * 32, 16, 1024);
+          } else {
+            // V: UK key rows of 128 bytes per step, MN-major
+            bdesc = sdesc_sw128(sV + s * C::TILE_BYTES + kk * C::UK * 128, C::CHUNK_BYTES, 1024);
+          }
+          umma_ts<TF32>(tmem + C::COL_O, a_tmem + kk * 8, bdesc, kIdescPV,
                         (j > 0 || kk > 0) ? 1u : 0u);
         }
-        tc_commit(bVempty + 8 * s);
+        if constexpr (!TF32) tc_commit(bVempty + 8 * s);
         tc_commit(bOdone);
       }
       // Every UMMA issued above must be complete before TMEM is freed.
@@ -292,8 +321,99 @@ __global__ void __launch_bounds__(192, 1)
     float l = 0.f;
     bool ok = true;
 
-    for (int j = 0; j < n_kt; ++j) {
+    // fp32 path: round this thread's row r of K tile t (stage t % KST) to
+    // tf32 in place, then release it to the UMMA issuer.  Row r occupies 16
+    // 16-byte units of the 128-byte-swizzled tile (2 chunks of 32 elements).
+    auto round_k_row = [&](int t) -> bool {
+      const int s = t % C::KST;
+      if (!__all_sync(kFull, bounded_wait(bKfull + 8 * s, (t / C::KST) & 1, w))) return false;
+      uint8_t *kt = smem + C::OFF_K + s * C::TILE_BYTES;
+#pragma unroll
+      for (int ch = 0; ch < C::NCH; ++ch) {
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          uint4 *ptr = reinterpret_cast<uint4 *>(kt + ch * C::CHUNK_BYTES + r * 128 +
+                                                 ((u ^ (r & 7)) << 4));
+          uint4 val = *ptr;
+          val.x = to_tf32(__uint_as_float(val.x));
+          val.y = to_tf32(__uint_as_float(val.y));
+          val.z = to_tf32(__uint_as_float(val.z));
+          val.w = to_tf32(__uint_as_float(val.w));
+          *ptr = val;
+        }
+      }
+      fence_proxy_async_smem();
+      mbar_arrive(bKready + 8 * s);
+      return true;
+    };
+    // fp32 path: transpose key row r of V tile j into column r of V^T
+    // (tf32-rounded), then release the fp32 stage to the producer.  For a fixed
+    // d the 32 threads of a warp write 32 consecutive keys of one 128-byte row
+    // of V^T: one word each, no bank conflicts.
+    auto transpose_v_row = [&](int j) -> bool {
+      const int s = j % C::VST;
+      if (!__all_sync(kFull, bounded_wait(bVfull + 8 * s, (j / C::VST) & 1, w))) return false;
+      const uint8_t *vt32 = smem + C::OFF_V + s * C::TILE_BYTES;
+      uint8_t *vtT = smem + C::OFF_VT + (j & 1) * C::TILE_BYTES;
+      const int key_chunk = r >> 5, key_unit = (r & 31) >> 2, key_word = r & 3;
+#pragma unroll
+      for (int ch = 0; ch < C::NCH; ++ch) {
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const uint4 val = *reinterpret_cast<const uint4 *>(
+              vt32 + ch * C::CHUNK_BYTES + r * 128 + ((u ^ (r & 7)) << 4));
+          const uint32_t e[4] = {val.x, val.y, val.z, val.w};
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int dd = ch * C::CH_ELEMS + 4 * u + i;  // head-dim index
+            *reinterpret_cast<uint32_t *>(vtT + key_chunk * C::VT_CHUNK_BYTES + dd * 128 +
+                                          ((key_unit ^ (dd & 7)) << 4) + key_word * 4) =
+                to_tf32(__uint_as_float(e[i]));
+          }
+        }
+      }
+      fence_proxy_async_smem();
+      mbar_arrive(bVempty + 8 * s);
+      return true;
+    };
+
+    // Q row -> tensor memory (A operand layout: lane = row, 32-bit column c
+    // holds bf16 elements 2c, 2c+1, or one tf32 element).  Rows past Nq are 0.
+    {
+      const uint4 *src = reinterpret_cast<const uint4 *>(
+          static_cast<const uint8_t *>(p.q) +
+          (static_cast<size_t>(bh) * p.Nq + (row < p.Nq ? row : 0)) * (D * C::ESZ));
+      const bool in = row < p.Nq;
+#pragma unroll
+      for (int blk = 0; blk < C::Q_COLS / 32; ++blk) {
+        uint32_t wq[32];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          uint4 val = in ? __ldg(src + blk * 8 + u) : make_uint4(0u, 0u, 0u, 0u);
+          wq[4 * u + 0] = val.x;
+          wq[4 * u + 1] = val.y;
+          wq[4 * u + 2] = val.z;
+          wq[4 * u + 3] = val.w;
+        }
+        if constexpr (TF32) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) wq[i] = to_tf32(__uint_as_float(wq[i]));
+        }
+        tmem_st32(tmem + lane_off + C::COL_Q + blk * 32, wq);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(bQready);
+    }
+    if constexpr (TF32) ok = round_k_row(0);
+
+    for (int j = 0; ok && j < n_kt; ++j) {
       const int buf = j & 1;
+      if constexpr (TF32) {
+        // the next K tile is rounded before this tile's softmax so that
+        // S_{j+1} = Q K_{j+1}^T still overlaps it
+        if (j + 1 < n_kt && !(ok = round_k_row(j + 1))) break;
+      }
       ok = __all_sync(kFull, bounded_wait(bSfull + 8 * buf, (j >> 1) & 1, w));
       if (!ok) break;
       tc_fence_after();
@@ -308,29 +428,38 @@ __global__ void __launch_bounds__(192, 1)
       reg_fence32(sr[1]);
       reg_fence32(sr[2]);
       reg_fence32(sr[3]);
+      auto S = [&](int c) -> float { return __uint_as_float(sr[c >> 5][c & 31]); };
 
       const int lim = row_lim - j * BN;  // valid columns c < lim
-      // Row max (raw score; for a negative scale the min becomes the max).
-      // Masked tiles (causal diagonal, ragged key tail) take a separate
-      // compile-time path so unmasked tiles carry no selects.
-      auto row_max = [&](auto mask_tag) -> float {
+      // Row max of the raw scores over the valid columns (for a negative
+      // scale the min becomes the max); masked tiles (causal diagonal, ragged
+      // key tail) take a separate compile-time path.
+      auto row_max = [&](auto mask_tag, auto neg_tag) -> float {
         constexpr bool kMask = decltype(mask_tag)::value;
-        const float fill = neg ? INFINITY : -INFINITY;
-        float part[8];
+        constexpr bool kNeg = decltype(neg_tag)::value;
+        constexpr float fill = kNeg ? INFINITY : -INFINITY;
+        float part[4] = {fill, fill, fill, fill};
 #pragma unroll
-        for (int i = 0; i < 8; ++i) part[i] = fill;
-#pragma unroll
-        for (int c = 0; c < BN; ++c) {
-          float x = __uint_as_float(sr[c >> 5][c & 31]);
-          if constexpr (kMask) x = (c < lim) ? x : fill;
-          part[c & 7] = neg ? fminf(part[c & 7], x) : fmaxf(part[c & 7], x);
+        for (int c = 0; c < BN; c += 2) {
+          float a = S(c), b = S(c + 1);
+          if constexpr (kMask) {
+            a = (c < lim) ? a : fill;
+            b = (c + 1 < lim) ? b : fill;
+          }
+          const int i = (c >> 1) & 3;
+          part[i] = kNeg ? min3f(part[i], a, b) : max3f(part[i], a, b);
         }
-#pragma unroll
-        for (int i = 1; i < 8; ++i) part[0] = neg ? fminf(part[0], part[i]) : fmaxf(part[0], part[i]);
-        return part[0];
+        return kNeg ? min3f(part[0], part[1], fminf(part[2], part[3]))
+                    : max3f(part[0], part[1], fmaxf(part[2], part[3]));
       };
       const bool masked = __any_sync(kFull, lim < BN);
-      const float mx = masked ? row_max(std::true_type{}) : row_max(std::false_type{});
+      float mx;
+      if (masked)
+        mx = neg ? row_max(std::true_type{}, std::true_type{})
+                 : row_max(std::true_type{}, std::false_type{});
+      else
+        mx = neg ? row_max(std::false_type{}, std::true_type{})
+                 : row_max(std::false_type{}, std::false_type{});
       const float m_new = fmaxf(m_used, mx * sl2);
       if (j == 0) {
         m_used = m_new;
@@ -342,6 +471,7 @@ __global__ void __launch_bounds__(192, 1)
         if (__any_sync(kFull, need)) {
           tc_fence_after();
           const float alpha = need ? ex2_approx(m_used - m_new) : 1.f;
+          const uint64_t a2 = pk2(alpha, alpha);
 #pragma unroll
           for (int c = 0; c < D; c += 32) {
             uint32_t o[32];
@@ -349,7 +479,12 @@ __global__ void __launch_bounds__(192, 1)
             tmem_ld_wait();
             reg_fence32(o);
 #pragma unroll
-            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+            for (int i = 0; i < 32; i += 2) {
+              float lo, hi;
+              upk2(fmul2(pk2(__uint_as_float(o[i]), __uint_as_float(o[i + 1])), a2), lo, hi);
+              o[i] = __float_as_uint(lo);
+              o[i + 1] = __float_as_uint(hi);
+            }
             tmem_st32(o_tm + c, o);
           }
           tmem_st_wait();
@@ -359,49 +494,60 @@ __global__ void __launch_bounds__(192, 1)
           }
         }
       }
-      // P = exp2(s * scale*log2e - m_used), written over S in TMEM.
-      const float neg_m = -m_used;
-      float psum[4] = {0.f, 0.f, 0.f, 0.f};
+      // P = exp2(s * scale*log2e - m_used), written over S in TMEM; pairs of
+      // columns go through packed f32x2 arithmetic.
+      const uint64_t sl2_2 = pk2(sl2, sl2);
+      const uint64_t nm_2 = pk2(-m_used, -m_used);
+      uint64_t acc[2] = {0ull, 0ull};  // packed partial row sums (+0.0f bits)
       auto write_p = [&](auto mask_tag) {
         constexpr bool kMask = decltype(mask_tag)::value;
-        if constexpr (!TF32) {
+        constexpr int kBlk = TF32 ? 16 : 32;  // column pairs per TMEM store
 #pragma unroll
-          for (int hblk = 0; hblk < 2; ++hblk) {
-            uint32_t pk[32];
+        for (int blk = 0; blk < 64 / kBlk; ++blk) {
+          uint32_t pk[32];
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-              const int c0 = hblk * 64 + 2 * i;
-              float p0 = ex2_approx(fmaf(__uint_as_float(sr[c0 >> 5][c0 & 31]), sl2, neg_m));
-              float p1 =
-                  ex2_approx(fmaf(__uint_as_float(sr[(c0 + 1) >> 5][(c0 + 1) & 31]), sl2, neg_m));
-              if constexpr (kMask) {
-                p0 = (c0 < lim) ? p0 : 0.f;
-                p1 = (c0 + 1 < lim) ? p1 : 0.f;
-              }
-              psum[i & 3] += p0 + p1;
+          for (int i = 0; i < kBlk; ++i) {
+            const int c0 = 2 * (blk * kBlk + i);
+            const uint64_t x2 = ffma2(pk2(S(c0), S(c0 + 1)), sl2_2, nm_2);
+            float p0, p1;
+            if ((i & 7) < C::EMU_PER_8) {
+              exp2_poly_pair(x2, p0, p1);
+            } else {
+              float x0, x1;
+              upk2(x2, x0, x1);
+              p0 = ex2_approx(x0);
+              p1 = ex2_approx(x1);
+            }
+            if constexpr (kMask) {
+              p0 = (c0 < lim) ? p0 : 0.f;
+              p1 = (c0 + 1 < lim) ? p1 : 0.f;
+            }
+            acc[i & 1] = fadd2(acc[i & 1], pk2(p0, p1));
+            if constexpr (TF32) {
+              pk[2 * i] = to_tf32(p0);
+              pk[2 * i + 1] = to_tf32(p1);
+            } else {
               pk[i] = pack_bf16x2(p0, p1);
             }
-            tmem_st32(s_tm + hblk * 32, pk);
           }
-        } else {
-#pragma unroll
-          for (int qblk = 0; qblk < 4; ++qblk) {
-            uint32_t pk[32];
-#pragma unroll
-            for (int i = 0; i < 32; ++i) {
-              const int c = qblk * 32 + i;
-              float pv = ex2_approx(fmaf(__uint_as_float(sr[qblk][i]), sl2, neg_m));
-              if constexpr (kMask) pv = (c < lim) ? pv : 0.f;
-              psum[i & 3] += pv;
-              pk[i] = to_tf32(pv);
-            }
-            tmem_st32(s_tm + qblk * 32, pk);
-          }
+          tmem_st32(s_tm + blk * 32, pk);
         }
       };
-      if (masked) write_p(std::true_type{});
-      else write_p(std::false_type{});
-      l += (psum[0] + psum[1]) + (psum[2] + psum[3]);
+      if (masked)
+        write_p(std::true_type{});
+      else
+        write_p(std::false_type{});
+      {
+        float a0, a1, b0, b1;
+        upk2(acc[0], a0, a1);
+        upk2(acc[1], b0, b1);
+        l += (a0 + a1) + (b0 + b1);
+      }
+      if constexpr (TF32) {
+        // V^T buffer j&1 was last read by P_{j-2} V_{j-2}, complete since the
+        // wait on P_{j-1} V_{j-1} above.
+        if (!(ok = transpose_v_row(j))) break;
+      }
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(bPfull + 8 * buf);
@@ -412,7 +558,9 @@ __global__ void __launch_bounds__(192, 1)
     if (ok) {
       tc_fence_after();
       const float inv_l = 1.f / l;
-      uint8_t *stage = smem + C::OFF_Q;  // Q is no longer read: every S_j is done
+      // Staging in K stage 0: every S_j is complete, so no UMMA reads K any
+      // more and the producer has no K load outstanding.
+      uint8_t *stage = smem + C::OFF_K;
 #pragma unroll
       for (int c = 0; c < D; c += 32) {
         uint32_t o[32];
@@ -458,7 +606,8 @@ __global__ void __launch_bounds__(192, 1)
     named_bar_sync(1, 128);
     if (threadIdx.x == 0 && *abort_flag == 0) {
 #pragma unroll
-      for (int c = 0; c < C::NCH; ++c) tma_store_3d(&tm_o, sQ + c * C::CHUNK_BYTES, c * C::CH_ELEMS, q0, bh);
+      for (int c = 0; c < C::NCH; ++c)
+        tma_store_3d(&tm_o, sK + c * C::CHUNK_BYTES, c * C::CH_ELEMS, q0, bh);
       tma_store_commit();
       tma_store_wait_read_all();
     }
@@ -474,12 +623,10 @@ __global__ void __launch_bounds__(192, 1)
 }
 
 template <int D, bool TF32>
-cudaError_t launch_tc(const CUtensorMap &q, const CUtensorMap &k, const CUtensorMap &v,
-                      const CUtensorMap &o, const TcParams &p, int B, int causal,
-                      cudaStream_t stream) {
+cudaError_t launch_tc(const CUtensorMap &k, const CUtensorMap &v, const CUtensorMap &o,
+                      const TcParams &p, int B, int causal, cudaStream_t stream) {
   using C = TcCfg<D, TF32>;
-  void (*kern)(const CUtensorMap, const CUtensorMap, const CUtensorMap, const CUtensorMap,
-               const TcParams) =
+  void (*kern)(const CUtensorMap, const CUtensorMap, const CUtensorMap, const TcParams) =
       causal ? fa_tc_fwd_kernel<D, TF32, true> : fa_tc_fwd_kernel<D, TF32, false>;
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
@@ -492,7 +639,7 @@ cudaError_t launch_tc(const CUtensorMap &q, const CUtensorMap &k, const CUtensor
   cfg.stream = stream;
   cfg.attrs = nullptr;
   cfg.numAttrs = 0;
-  return cudaLaunchKernelEx(&cfg, kern, q, k, v, o, p);
+  return cudaLaunchKernelEx(&cfg, kern, k, v, o, p);
 }
 
 }  // namespace fa

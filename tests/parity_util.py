@@ -40,8 +40,24 @@ def run_oracle(q, k, v, scale, causal):
                            scale, causal)
 
 
-def compare(o, lse, ro, rl, dtype, tag=""):
-    tol = TOL[dtype]
+def tf32_score_bound(q, k, scale, causal):
+    """Worst-case |score error| of the TF32 path: q and k are rounded to
+    nearest tf32 (relative error u = 2^-11 each), so every product q_x*k_x is
+    off by at most (2u + u^2)|q_x k_x|, plus fp32 accumulation; a score moves
+    by at most |scale| * 2^-10 * 1.01 * sum_x |q_x||k_x| (max over allowed
+    pairs), and the log-sum-exp of the scores by no more than that."""
+    import torch as _t
+    qa, ka = _t.as_tensor(q).double().abs(), _t.as_tensor(k).double().abs()
+    dots = qa @ ka.transpose(-1, -2)
+    if causal:
+        Nq, Nk = dots.shape[-2:]
+        allowed = _t.ones(Nq, Nk, dtype=_t.bool).tril()
+        dots = dots.masked_fill(~allowed, 0.0)
+    return float(abs(scale) * 2.0 ** -10 * 1.01 * dots.max())
+
+
+def compare(o, lse, ro, rl, dtype, tag="", tol=None):
+    tol = dict(TOL[dtype], **(tol or {}))
     assert np.isfinite(o).all(), f"{tag}: non-finite O (unwritten rows?)"
     assert np.isfinite(lse).all(), f"{tag}: non-finite LSE (unwritten rows?)"
     eo = np.abs(o - ro)

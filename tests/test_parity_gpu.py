@@ -9,7 +9,7 @@ import oracle
 from exact_attention_57_gb300 import fa
 from exact_attention_57_gb300.workloads import (DTYPE_BF16, DTYPE_F32, DTYPE_F32_SIMT,
                                                 WORKLOADS, make_inputs, workload_inputs)
-from parity_util import TOL, compare, run_gpu, run_oracle
+from parity_util import TOL, compare, run_gpu, run_oracle, tf32_score_bound
 
 pytestmark = pytest.mark.gpu
 
@@ -78,7 +78,17 @@ def test_scales(scale, dtype, d):
     for causal in (False, True):
         o, lse = run_gpu(q, k, v, scale, causal, dtype)
         ro, rl = run_oracle(q, k, v, scale, causal)
-        compare(o, lse, ro, rl, dtype, f"scale={scale} causal={causal}")
+        tol = None
+        if dtype == DTYPE_F32:
+            # Beyond the 1/sqrt(d) scale of the fp32 workload the fixed
+            # tolerances no longer cover TF32 rounding of the scores; use the
+            # bound that rounding implies (LSE moves by at most the largest
+            # score error, O by at most twice that times max|v|).
+            b = tf32_score_bound(q, k, scale, causal)
+            vmax = float(v.abs().max())
+            tol = dict(max_lse=max(TOL[dtype]["max_lse"], b),
+                       max_o=max(TOL[dtype]["max_o"], 2 * b * vmax + 1e-3))
+        compare(o, lse, ro, rl, dtype, f"scale={scale} causal={causal}", tol=tol)
 
 
 def test_large_score_range():
