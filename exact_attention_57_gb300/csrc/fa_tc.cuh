@@ -23,10 +23,15 @@
 //                swizzled in shared memory for a TMA store, and write LSE.
 //   warp 4       TMA producer: K_j / V_j through shared-memory rings
 //                (full/empty mbarriers), L2 evict-last.
-//   warp 5       UMMA issuer (one lane): S_j = Q K_j^T (A from TMEM, B = K_j
-//                K-major in shared memory) into a double-buffered score tile,
-//                then O += P_j V_j (A = P from TMEM), fp32 accumulation.  Owns
-//                the TMEM allocation.
+//   warp 5       UMMA issuer (one lane) for S_j = Q K_j^T (A from TMEM, B = K_j
+//                K-major in shared memory) into a double-buffered score tile.
+//                Owns the TMEM allocation.
+//   warp 6       UMMA issuer (one lane) for O += P_j V_j (A = P from TMEM),
+//                fp32 accumulation.  A tcgen05.mma issue returns at about the
+//                rate the tensor pipe executes it, so one issuing thread would
+//                leave the pipe idle during every wait and commit between its
+//                batches; with two, each batch's bookkeeping overlaps the other
+//                product's MMAs.
 // bf16 inputs (kind::f16): P is bf16; V_j is an MN-major B operand as loaded.
 // fp32 inputs (kind::tf32): the tensor core truncates fp32 operands to tf32,
 // which biases the scores; so Q (on its way to TMEM) and K_j (in place, by the
@@ -74,16 +79,16 @@ struct TcCfg {
   static constexpr int OFF_VT = OFF_V + VST * TILE_BYTES;
   static constexpr int OFF_BAR = OFF_VT + NVT * TILE_BYTES;
   // qready, kfull[KST], kempty[KST], vfull[VST], vempty[VST], sfull[2], pfull[2],
-  // odone, fin, kready[KST]
-  static constexpr int NBAR = 1 + 2 * KST + 2 * VST + 2 + 2 + 1 + 1 + KST;
+  // odone[2], fin[2], kready[KST]
+  static constexpr int NBAR = 1 + 2 * KST + 2 * VST + 2 + 2 + 2 + 2 + KST;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;       // tmem base, abort flag
   static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;   // + alignment slack
   static constexpr uint32_t TMEM_COLS = 512;
   static constexpr uint32_t COL_S0 = 0, COL_S1 = 128, COL_O = 256, COL_Q = 384;
   static constexpr int Q_COLS = D * ESZ / 4;                // 32-bit columns of one Q row
-  static constexpr int THREADS = 192;
+  static constexpr int THREADS = 224;
   // Exponentials per 8 column pairs computed by the FMA-pipe polynomial.
-  static constexpr int EMU_PER_8 = TF32 ? 0 : 3;
+  static constexpr int EMU_PER_8 = 0;
   static_assert(NCH >= 1 && D % 32 == 0, "head dim must fill whole 128-byte chunks");
   static_assert(COL_O + D <= COL_Q && COL_Q + Q_COLS <= TMEM_COLS, "tensor memory budget");
   static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
@@ -121,7 +126,7 @@ __device__ __forceinline__ bool bounded_wait(uint32_t bar, uint32_t parity, cons
 }
 
 template <int D, bool TF32, bool CAUSAL>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(224, 1)
     fa_tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_v,
                      const __grid_constant__ CUtensorMap tm_o, const TcParams p) {
@@ -140,9 +145,10 @@ __global__ void __launch_bounds__(192, 1)
   const uint32_t bVempty = bVfull + 8 * C::VST;
   const uint32_t bSfull = bVempty + 8 * C::VST;        // + 8*buffer
   const uint32_t bPfull = bSfull + 16;                 // + 8*buffer
-  const uint32_t bOdone = bPfull + 16;
-  const uint32_t bFin = bOdone + 8;
-  const uint32_t bKready = bFin + 8;                   // + 8*stage (fp32 path)
+  const uint32_t bOdone = bPfull + 16;                 // + 8*(tile parity)
+  const uint32_t bFin = bOdone + 16;                   // S issuer's teardown
+  const uint32_t bFin2 = bFin + 8;                     // P V issuer's teardown
+  const uint32_t bKready = bFin2 + 8;                  // + 8*stage (fp32 path)
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::OFF_MISC);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::OFF_MISC + 4);
 
@@ -176,7 +182,9 @@ __global__ void __launch_bounds__(192, 1)
     mbar_init(bPfull, 128);
     mbar_init(bPfull + 8, 128);
     mbar_init(bOdone, 1);
+    mbar_init(bOdone + 8, 1);
     mbar_init(bFin, 1);
+    mbar_init(bFin2, 1);
     *abort_flag = 0;
     fence_barrier_init();
     fence_proxy_async_smem();
@@ -245,19 +253,21 @@ __global__ void __launch_bounds__(192, 1)
     }
     __syncwarp();
   } else if (warp == 5) {
-    // ------------------------------------------------------------ UMMA issuer
+    // ------------------------------------------------ UMMA issuer: S = Q K^T
+    // Issues S_j = Q K_j^T into score buffer j&1.  That buffer last held P_{j-2}
+    // (written over S_{j-2}), read by P_{j-2} V_{j-2} from the other issuer
+    // warp, so S_j waits for that P V to complete.
     w.role = kStatusMma;
     if (lane == 0) {
       constexpr uint32_t kFmt = TF32 ? 2u : 1u;
       constexpr uint32_t kIdescQK = make_idesc(kFmt, BM, BN, 0u, 0u);  // K is K-major
-      // bf16: V is an MN-major B operand.  fp32: V^T is a K-major B operand.
-      constexpr uint32_t kIdescPV = make_idesc(kFmt, BM, D, 0u, TF32 ? 0u : 1u);
       bool ok = bounded_wait(bQready, 0, w);
       if (ok) tc_fence_after();
-      auto issue_qk = [&](int j) -> bool {
+      for (int j = 0; ok && j < n_kt; ++j) {
         const int s = j % C::KST;
+        if (j >= 2 && !(ok = bounded_wait(bOdone + 8 * (j & 1), ((j - 2) >> 1) & 1, w))) break;
         // fp32 path: K_j must first be rounded to tf32 by the softmax warps
-        if (!bounded_wait((TF32 ? bKready : bKfull) + 8 * s, (j / C::KST) & 1, w)) return false;
+        if (!(ok = bounded_wait((TF32 ? bKready : bKfull) + 8 * s, (j / C::KST) & 1, w))) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem + ((j & 1) ? C::COL_S1 : C::COL_S0);
         const uint32_t kb = sK + s * C::TILE_BYTES;
@@ -271,11 +281,23 @@ __global__ void __launch_bounds__(192, 1)
         }
         tc_commit(bKempty + 8 * s);
         tc_commit(bSfull + 8 * (j & 1));
-        return true;
-      };
-      if (ok) ok = issue_qk(0);
+      }
+      // Every UMMA issued above must be complete before TMEM is freed.
+      tc_commit(bFin);
+      bounded_wait(bFin, 0, w, false);
+    }
+    __syncwarp();
+  } else if (warp == 6) {
+    // ------------------------------------------------ UMMA issuer: O += P V
+    // A second issuing warp, so that neither product's waits and commits
+    // leave the tensor pipe idle while the other has work ready.
+    w.role = kStatusMma;
+    if (lane == 0) {
+      constexpr uint32_t kFmt = TF32 ? 2u : 1u;
+      // bf16: V is an MN-major B operand.  fp32: V^T is a K-major B operand.
+      constexpr uint32_t kIdescPV = make_idesc(kFmt, BM, D, 0u, TF32 ? 0u : 1u);
+      bool ok = true;
       for (int j = 0; ok && j < n_kt; ++j) {
-        if (j + 1 < n_kt && !(ok = issue_qk(j + 1))) break;
         // P_j ready (fp32 path: also V_j^T written).
         if (!(ok = bounded_wait(bPfull + 8 * (j & 1), (j >> 1) & 1, w))) break;
         const int s = j % C::VST;
@@ -300,11 +322,10 @@ __global__ void __launch_bounds__(192, 1)
                         (j > 0 || kk > 0) ? 1u : 0u);
         }
         if constexpr (!TF32) tc_commit(bVempty + 8 * s);
-        tc_commit(bOdone);
+        tc_commit(bOdone + 8 * (j & 1));
       }
-      // Every UMMA issued above must be complete before TMEM is freed.
-      tc_commit(bFin);
-      bounded_wait(bFin, 0, w, false);
+      tc_commit(bFin2);
+      bounded_wait(bFin2, 0, w, false);
     }
     __syncwarp();
   } else {
@@ -438,7 +459,11 @@ __global__ void __launch_bounds__(192, 1)
         constexpr bool kMask = decltype(mask_tag)::value;
         constexpr bool kNeg = decltype(neg_tag)::value;
         constexpr float fill = kNeg ? INFINITY : -INFINITY;
-        float part[4] = {fill, fill, fill, fill};
+        // eight independent chains of three-input max keep the dependency
+        // depth at 8 for the 128 columns
+        float part[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) part[i] = fill;
 #pragma unroll
         for (int c = 0; c < BN; c += 2) {
           float a = S(c), b = S(c + 1);
@@ -446,11 +471,15 @@ __global__ void __launch_bounds__(192, 1)
             a = (c < lim) ? a : fill;
             b = (c + 1 < lim) ? b : fill;
           }
-          const int i = (c >> 1) & 3;
+          const int i = (c >> 1) & 7;
           part[i] = kNeg ? min3f(part[i], a, b) : max3f(part[i], a, b);
         }
-        return kNeg ? min3f(part[0], part[1], fminf(part[2], part[3]))
-                    : max3f(part[0], part[1], fmaxf(part[2], part[3]));
+        if constexpr (kNeg)
+          return min3f(min3f(part[0], part[1], part[2]), min3f(part[3], part[4], part[5]),
+                       fminf(part[6], part[7]));
+        else
+          return max3f(max3f(part[0], part[1], part[2]), max3f(part[3], part[4], part[5]),
+                       fmaxf(part[6], part[7]));
       };
       const bool masked = __any_sync(kFull, lim < BN);
       float mx;
@@ -464,11 +493,16 @@ __global__ void __launch_bounds__(192, 1)
       if (j == 0) {
         m_used = m_new;
       } else {
-        // O may be touched (and P_j written) only after P_{j-1} V_{j-1} is done.
-        ok = __all_sync(kFull, bounded_wait(bOdone, (j - 1) & 1, w));
-        if (!ok) break;
+        // P_j may overwrite P_{j-2} without waiting: S_j was only issued after
+        // P_{j-2} V_{j-2} had completed.  Only a rescale of O has to wait, for
+        // P_{j-1} V_{j-1} (the last UMMA into O before P_j V_j); the
+        // done-barriers alternate with the tile parity, and P_{j-3} V_{j-3}
+        // completed before S_{j-1} was issued, so a skipped wait never makes a
+        // later one ambiguous.
         const bool need = (m_new - m_used) > kRescaleThreshold;
         if (__any_sync(kFull, need)) {
+          ok = __all_sync(kFull, bounded_wait(bOdone + 8 * ((j - 1) & 1), ((j - 1) >> 1) & 1, w));
+          if (!ok) break;
           tc_fence_after();
           const float alpha = need ? ex2_approx(m_used - m_new) : 1.f;
           const uint64_t a2 = pk2(alpha, alpha);
@@ -544,8 +578,8 @@ __global__ void __launch_bounds__(192, 1)
         l += (a0 + a1) + (b0 + b1);
       }
       if constexpr (TF32) {
-        // V^T buffer j&1 was last read by P_{j-2} V_{j-2}, complete since the
-        // wait on P_{j-1} V_{j-1} above.
+        // V^T buffer j&1 was last read by P_{j-2} V_{j-2}, which completed
+        // before S_j was issued.
         if (!(ok = transpose_v_row(j))) break;
       }
       tmem_st_wait();
@@ -554,7 +588,9 @@ __global__ void __launch_bounds__(192, 1)
     }
 
     // ------------------------------------------------ epilogue
-    if (ok) ok = __all_sync(kFull, bounded_wait(bOdone, (n_kt - 1) & 1, w));
+    // The last P V; its commit also covers every earlier UMMA.
+    if (ok)
+      ok = __all_sync(kFull, bounded_wait(bOdone + 8 * ((n_kt - 1) & 1), ((n_kt - 1) >> 1) & 1, w));
     if (ok) {
       tc_fence_after();
       const float inv_l = 1.f / l;
