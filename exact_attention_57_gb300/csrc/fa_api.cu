@@ -158,8 +158,9 @@ int fa_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int
   }
 
   if ((rc = get_encoder()) != FA_OK) return rc;
-  CUtensorMap mk, mv, mo;
+  CUtensorMap mq, mk, mv, mo;
   const int BH = B * H;
+  if ((rc = encode_map(&mq, q, dtype, BH, Nq, d)) != FA_OK) return rc;
   if ((rc = encode_map(&mk, k, dtype, BH, Nk, d)) != FA_OK) return rc;
   if ((rc = encode_map(&mv, v, dtype, BH, Nk, d)) != FA_OK) return rc;
   if ((rc = encode_map(&mo, o, dtype, BH, Nq, d)) != FA_OK) return rc;
@@ -181,10 +182,10 @@ int fa_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int
 
   cudaError_t e;
   if (dtype == FA_DTYPE_BF16)
-    e = (d == 64) ? fa::launch_tc_bf16_d64(mk, mv, mo, p, B, causal, s)
-                  : fa::launch_tc_bf16_d128(mk, mv, mo, p, B, causal, s);
+    e = (d == 64) ? fa::launch_tc_bf16_d64(mq, mk, mv, mo, p, B, causal, s)
+                  : fa::launch_tc_bf16_d128(mq, mk, mv, mo, p, B, causal, s);
   else
-    e = fa::launch_tc_f32_d64(mk, mv, mo, p, B, causal, s);
+    e = fa::launch_tc_f32_d64(mq, mk, mv, mo, p, B, causal, s);
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
@@ -337,8 +338,9 @@ extern "C" int fa_fwd_noalloc(const void *q, const void *k, const void *v, void 
     if (fa::launch_simt(p, B, s) != cudaSuccess) return FA_ERR_CUDA;
   } else {
     if ((rc = get_encoder()) != FA_OK) return rc;
-    CUtensorMap mk, mv, mo;
+    CUtensorMap mq, mk, mv, mo;
     const int BH = B * H;
+    if ((rc = encode_map(&mq, q, dtype, BH, Nq, d)) != FA_OK) return rc;
     if ((rc = encode_map(&mk, k, dtype, BH, Nk, d)) != FA_OK) return rc;
     if ((rc = encode_map(&mv, v, dtype, BH, Nk, d)) != FA_OK) return rc;
     if ((rc = encode_map(&mo, o, dtype, BH, Nq, d)) != FA_OK) return rc;
@@ -358,10 +360,10 @@ extern "C" int fa_fwd_noalloc(const void *q, const void *k, const void *v, void 
     p.skip_v_load = g_skip_v_load.load();
     cudaError_t e;
     if (dtype == FA_DTYPE_BF16)
-      e = (d == 64) ? fa::launch_tc_bf16_d64(mk, mv, mo, p, B, causal, s)
-                    : fa::launch_tc_bf16_d128(mk, mv, mo, p, B, causal, s);
+      e = (d == 64) ? fa::launch_tc_bf16_d64(mq, mk, mv, mo, p, B, causal, s)
+                    : fa::launch_tc_bf16_d128(mq, mk, mv, mo, p, B, causal, s);
     else
-      e = fa::launch_tc_f32_d64(mk, mv, mo, p, B, causal, s);
+      e = fa::launch_tc_f32_d64(mq, mk, mv, mo, p, B, causal, s);
     if (e != cudaSuccess) return FA_ERR_CUDA;
   }
   if (device_status == nullptr) return FA_OK;

@@ -22,7 +22,7 @@ constexpr unsigned kStatusInjected = 8u;
 constexpr unsigned long long kDefaultWaitLimitNs = 2000000000ull;  // 2 s
 
 struct TcParams {
-  const void *q;                  // [B*H*Nq*d], read row by row into tensor memory
+  const void *q;                  // [B*H*Nq*d], read row by row when Q goes to TMEM
   float *lse;                     // [B*H*Nq]
   unsigned *status;               // per-device status word
   int H, Nq, Nk;
@@ -45,11 +45,14 @@ struct SimtParams {
 
 // Tensor-core forward for one (head dim, input type); causal chosen inside.
 // Returns the launch's cudaError_t.
-cudaError_t launch_tc_bf16_d64(const CUtensorMap &k, const CUtensorMap &v, const CUtensorMap &o, const TcParams &p, int B, int causal,
+cudaError_t launch_tc_bf16_d64(const CUtensorMap &q, const CUtensorMap &k, const CUtensorMap &v,
+                               const CUtensorMap &o, const TcParams &p, int B, int causal,
                                cudaStream_t s);
-cudaError_t launch_tc_bf16_d128(const CUtensorMap &k, const CUtensorMap &v, const CUtensorMap &o, const TcParams &p, int B, int causal,
+cudaError_t launch_tc_bf16_d128(const CUtensorMap &q, const CUtensorMap &k, const CUtensorMap &v,
+                                const CUtensorMap &o, const TcParams &p, int B, int causal,
                                 cudaStream_t s);
-cudaError_t launch_tc_f32_d64(const CUtensorMap &k, const CUtensorMap &v, const CUtensorMap &o, const TcParams &p, int B, int causal,
+cudaError_t launch_tc_f32_d64(const CUtensorMap &q, const CUtensorMap &k, const CUtensorMap &v,
+                              const CUtensorMap &o, const TcParams &p, int B, int causal,
                               cudaStream_t s);
 
 cudaError_t launch_simt(const SimtParams &p, int B, cudaStream_t s);

@@ -13,19 +13,21 @@
 //
 // GB300 design (one CTA = one (batch, head, 128-row query tile)):
 //   warps 0-3    softmax, correction and epilogue: one query row per thread
-//                (= one TMEM lane).  First copy the thread's Q row from global
-//                memory into tensor memory (the A operand of S = Q K^T, so
-//                shared memory only carries K and V).  Per key tile: load the
+//                (= one TMEM lane).  Where Q lives in tensor memory, first copy
+//                the thread's Q row there from global memory (the A operand of
+//                S = Q K^T).  Per key tile: load the
 //                row's 128 scores, mask the causal diagonal / ragged key tail,
 //                update m and l, write P back over S in TMEM.  A fixed share
 //                of the exponentials runs as a polynomial on the FMA pipes to
 //                relieve the MUFU unit.  At the end normalise O, stage it
 //                swizzled in shared memory for a TMA store, and write LSE.
-//   warp 4       TMA producer: K_j / V_j through shared-memory rings
-//                (full/empty mbarriers), L2 evict-last.
-//   warp 5       UMMA issuer (one lane) for S_j = Q K_j^T (A from TMEM, B = K_j
-//                K-major in shared memory) into a double-buffered score tile.
-//                Owns the TMEM allocation.
+//   warp 4       TMA producer: Q (when in shared memory), then K_j / V_j
+//                through shared-memory rings (full/empty mbarriers), L2
+//                evict-last for K/V.
+//   warp 5       UMMA issuer (one lane) for S_j = Q K_j^T (A = Q from TMEM or
+//                shared memory, B = K_j K-major in shared memory) into score
+//                buffer j % NS (NS = 3 for bf16: two score tiles can be
+//                computed ahead of the softmax).  Owns the TMEM allocation.
 //   warp 6       UMMA issuer (one lane) for O += P_j V_j (A = P from TMEM),
 //                fp32 accumulation.  A tcgen05.mma issue returns at about the
 //                rate the tensor pipe executes it, so one issuing thread would
@@ -38,7 +40,8 @@
 // softmax warps, before S_j is issued) are rounded to nearest first.  P is
 // tf32.  kind::tf32 takes its B operand K-major only, so the softmax warps
 // also transpose each V_j into a tf32 V_j^T buffer (d rows of 128 keys).
-// Tensor memory: S0 cols [0,128), S1 [128,256), O [256, 256+D), Q [384, ...).
+// Tensor memory: S_b cols [128b, 128b+128) for b < NS, then O (D cols), then Q
+// when it fits (bf16 D=64, fp32 D=64); bf16 D=128 keeps Q in shared memory.
 //
 // Rescaling: the running max used as the exponent offset only moves when a
 // row's max grows by more than 2^8; otherwise the stale offset is kept.  The
@@ -67,30 +70,41 @@ struct TcCfg {
   static constexpr int CHUNK_BYTES = 128 * 128;             // one chunk of 128 rows
   static constexpr int TILE_BYTES = NCH * CHUNK_BYTES;      // one 128-row tile
   static constexpr int UK = 32 / ESZ;                       // K extent of one UMMA
+  // Score buffers in tensor memory: S_j lives in buffer j % NS; S_j may be
+  // issued once P_{j-NS} V_{j-NS} is done, so NS - 1 score tiles can be
+  // computed ahead of the softmax.
+  static constexpr int NS = TF32 ? 2 : 3;
+  static constexpr uint32_t TMEM_COLS = 512;
+  static constexpr uint32_t COL_O = NS * 128;               // O after the score buffers
+  static constexpr int Q_COLS = D * ESZ / 4;                // 32-bit columns of one Q row
+  // Q is the A operand of S = Q K^T: from tensor memory when it fits after O,
+  // else from shared memory (bf16, D = 128).
+  static constexpr bool QTMEM = COL_O + D + Q_COLS <= TMEM_COLS;
+  static constexpr uint32_t COL_Q = COL_O + D;
+  static constexpr int NQ = QTMEM ? 0 : 1;                  // Q tiles in shared memory
   static constexpr int KST = TF32 ? 2 : (TILE_BYTES <= 16384 ? 4 : 3); // K ring depth
-  static constexpr int VST = TF32 ? 2 : (TILE_BYTES <= 16384 ? 4 : 3); // V ring depth
+  static constexpr int VST = TF32 ? 2 : (TILE_BYTES <= 16384 ? 4 : (QTMEM ? 3 : 2)); // V ring
   // fp32 path: V_j is transposed by the softmax warps into a K-major copy
   // (V^T, d rows of 128 keys, tf32-rounded) because P V runs as kind::tf32
   // with V^T as a K-major B operand.  Two copies alternate.
   static constexpr int NVT = TF32 ? 2 : 0;
   static constexpr int VT_CHUNK_BYTES = D * 128;            // 32 keys x D rows
-  static constexpr int OFF_K = 0;
+  static constexpr int OFF_Q = 0;
+  static constexpr int OFF_K = OFF_Q + NQ * TILE_BYTES;
   static constexpr int OFF_V = OFF_K + KST * TILE_BYTES;
   static constexpr int OFF_VT = OFF_V + VST * TILE_BYTES;
   static constexpr int OFF_BAR = OFF_VT + NVT * TILE_BYTES;
-  // qready, kfull[KST], kempty[KST], vfull[VST], vempty[VST], sfull[2], pfull[2],
-  // odone[2], fin[2], kready[KST]
-  static constexpr int NBAR = 1 + 2 * KST + 2 * VST + 2 + 2 + 2 + 2 + KST;
+  // q, kfull[KST], kempty[KST], vfull[VST], vempty[VST], sfull[NS], pfull[NS],
+  // odone[NS], fin[2], kready[KST]
+  static constexpr int NBAR = 1 + 2 * KST + 2 * VST + 3 * NS + 2 + KST;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;       // tmem base, abort flag
   static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;   // + alignment slack
-  static constexpr uint32_t TMEM_COLS = 512;
-  static constexpr uint32_t COL_S0 = 0, COL_S1 = 128, COL_O = 256, COL_Q = 384;
-  static constexpr int Q_COLS = D * ESZ / 4;                // 32-bit columns of one Q row
   static constexpr int THREADS = 224;
   // Exponentials per 8 column pairs computed by the FMA-pipe polynomial.
   static constexpr int EMU_PER_8 = 0;
   static_assert(NCH >= 1 && D % 32 == 0, "head dim must fill whole 128-byte chunks");
-  static_assert(COL_O + D <= COL_Q && COL_Q + Q_COLS <= TMEM_COLS, "tensor memory budget");
+  static_assert(COL_O + D <= TMEM_COLS, "tensor memory budget");
+  static_assert(!TF32 || QTMEM, "the fp32 path rounds Q on its way into tensor memory");
   static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
 };
 
@@ -127,7 +141,8 @@ __device__ __forceinline__ bool bounded_wait(uint32_t bar, uint32_t parity, cons
 
 template <int D, bool TF32, bool CAUSAL>
 __global__ void __launch_bounds__(224, 1)
-    fa_tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_k,
+    fa_tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
+                     const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_v,
                      const __grid_constant__ CUtensorMap tm_o, const TcParams p) {
   using C = TcCfg<D, TF32>;
@@ -135,18 +150,19 @@ __global__ void __launch_bounds__(224, 1)
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const uint32_t sbase = smem_u32(smem);
+  const uint32_t sQ = sbase + C::OFF_Q;   // used when Q is not in tensor memory
   const uint32_t sK = sbase + C::OFF_K;
   const uint32_t sV = sbase + C::OFF_V;
   const uint32_t sVT = sbase + C::OFF_VT;
-  const uint32_t bQready = sbase + C::OFF_BAR;
-  const uint32_t bKfull = bQready + 8;                 // + 8*stage
+  const uint32_t bQ = sbase + C::OFF_BAR;             // Q in place (TMEM or smem)
+  const uint32_t bKfull = bQ + 8;                      // + 8*stage
   const uint32_t bKempty = bKfull + 8 * C::KST;
   const uint32_t bVfull = bKempty + 8 * C::KST;
   const uint32_t bVempty = bVfull + 8 * C::VST;
-  const uint32_t bSfull = bVempty + 8 * C::VST;        // + 8*buffer
-  const uint32_t bPfull = bSfull + 16;                 // + 8*buffer
-  const uint32_t bOdone = bPfull + 16;                 // + 8*(tile parity)
-  const uint32_t bFin = bOdone + 16;                   // S issuer's teardown
+  const uint32_t bSfull = bVempty + 8 * C::VST;        // + 8*score buffer
+  const uint32_t bPfull = bSfull + 8 * C::NS;          // + 8*score buffer
+  const uint32_t bOdone = bPfull + 8 * C::NS;          // + 8*score buffer
+  const uint32_t bFin = bOdone + 8 * C::NS;            // S issuer's teardown
   const uint32_t bFin2 = bFin + 8;                     // P V issuer's teardown
   const uint32_t bKready = bFin2 + 8;                  // + 8*stage (fp32 path)
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::OFF_MISC);
@@ -163,7 +179,8 @@ __global__ void __launch_bounds__(224, 1)
   const int n_kt = CAUSAL ? min(qt + 1, p.n_ktiles) : p.n_ktiles;
 
   if (threadIdx.x == 0) {
-    mbar_init(bQready, 128);
+    // Q: written to TMEM by the 128 softmax threads, or one TMA transaction
+    mbar_init(bQ, C::QTMEM ? 128 : 1);
 #pragma unroll
     for (int s = 0; s < C::KST; ++s) {
       mbar_init(bKfull + 8 * s, 1);
@@ -177,12 +194,12 @@ __global__ void __launch_bounds__(224, 1)
     }
 #pragma unroll
     for (int s = 0; s < C::KST; ++s) mbar_init(bKready + 8 * s, 128);
-    mbar_init(bSfull, 1);
-    mbar_init(bSfull + 8, 1);
-    mbar_init(bPfull, 128);
-    mbar_init(bPfull + 8, 128);
-    mbar_init(bOdone, 1);
-    mbar_init(bOdone + 8, 1);
+#pragma unroll
+    for (int b = 0; b < C::NS; ++b) {
+      mbar_init(bSfull + 8 * b, 1);
+      mbar_init(bPfull + 8 * b, 128);
+      mbar_init(bOdone + 8 * b, 1);
+    }
     mbar_init(bFin, 1);
     mbar_init(bFin2, 1);
     *abort_flag = 0;
@@ -190,6 +207,7 @@ __global__ void __launch_bounds__(224, 1)
     fence_proxy_async_smem();
   }
   if (warp == 4 && lane == 0) {
+    if constexpr (!C::QTMEM) tma_prefetch_desc(&tm_q);
     tma_prefetch_desc(&tm_k);
     tma_prefetch_desc(&tm_v);
     tma_prefetch_desc(&tm_o);
@@ -209,6 +227,13 @@ __global__ void __launch_bounds__(224, 1)
     w.role = kStatusProducer;
     if (lane == 0) {
       const uint64_t pol_kv = l2_policy_evict_last();
+      if constexpr (!C::QTMEM) {
+        mbar_arrive_expect_tx(bQ, C::TILE_BYTES);
+#pragma unroll
+        for (int c = 0; c < C::NCH; ++c)
+          tma_load_3d(sQ + c * C::CHUNK_BYTES, &tm_q, bQ, c * C::CH_ELEMS, q0, bh,
+                      l2_policy_evict_first());
+      }
       int nk = 0, nv = 0;  // loads issued
       bool ok = true;
       // Load order = consumption order: K0, K1, V0, K2, V1, ...
@@ -242,6 +267,7 @@ __global__ void __launch_bounds__(224, 1)
         }
       }
       // Drain: no TMA write may still be in flight when the CTA exits.
+      if constexpr (!C::QTMEM) bounded_wait(bQ, 0, w, false);
       for (int s = 0; s < C::KST; ++s) {
         const int cnt = (nk > s) ? (nk - 1 - s) / C::KST + 1 : 0;
         if (cnt > 0) bounded_wait(bKfull + 8 * s, (cnt - 1) & 1, w, false);
@@ -254,33 +280,40 @@ __global__ void __launch_bounds__(224, 1)
     __syncwarp();
   } else if (warp == 5) {
     // ------------------------------------------------ UMMA issuer: S = Q K^T
-    // Issues S_j = Q K_j^T into score buffer j&1.  That buffer last held P_{j-2}
-    // (written over S_{j-2}), read by P_{j-2} V_{j-2} from the other issuer
-    // warp, so S_j waits for that P V to complete.
+    // Issues S_j = Q K_j^T into score buffer j % NS.  That buffer last held
+    // P_{j-NS} (written over S_{j-NS}), read by P_{j-NS} V_{j-NS} from the
+    // other issuer warp, so S_j waits for that P V to complete.
     w.role = kStatusMma;
     if (lane == 0) {
       constexpr uint32_t kFmt = TF32 ? 2u : 1u;
       constexpr uint32_t kIdescQK = make_idesc(kFmt, BM, BN, 0u, 0u);  // K is K-major
-      bool ok = bounded_wait(bQready, 0, w);
+      bool ok = bounded_wait(bQ, 0, w);
       if (ok) tc_fence_after();
+      int b = 0, bph = 0;   // score buffer of tile j and the parity of its use
+      int s = 0, sph = 0;   // K stage of tile j and its parity
       for (int j = 0; ok && j < n_kt; ++j) {
-        const int s = j % C::KST;
-        if (j >= 2 && !(ok = bounded_wait(bOdone + 8 * (j & 1), ((j - 2) >> 1) & 1, w))) break;
+        if (j >= C::NS && !(ok = bounded_wait(bOdone + 8 * b, bph ^ 1, w))) break;
         // fp32 path: K_j must first be rounded to tf32 by the softmax warps
-        if (!(ok = bounded_wait((TF32 ? bKready : bKfull) + 8 * s, (j / C::KST) & 1, w))) break;
+        if (!(ok = bounded_wait((TF32 ? bKready : bKfull) + 8 * s, sph, w))) break;
         tc_fence_after();
-        const uint32_t d_tmem = tmem + ((j & 1) ? C::COL_S1 : C::COL_S0);
+        const uint32_t d_tmem = tmem + b * 128;
         const uint32_t kb = sK + s * C::TILE_BYTES;
 #pragma unroll
         for (int kk = 0; kk < D / C::UK; ++kk) {
           // 32 bytes of K per UMMA (4 steps per 128-byte swizzle chunk); the
-          // matching Q slice is 8 TMEM columns.
+          // matching Q slice is 8 TMEM columns or the same 32 bytes of Q.
           const uint32_t off = (kk >> 2) * C::CHUNK_BYTES + (kk & 3) * 32;
-          umma_ts<TF32>(d_tmem, tmem + C::COL_Q + kk * 8, sdesc_sw128(kb + off, 16, 1024),
-                        kIdescQK, kk > 0 ? 1u : 0u);
+          if constexpr (C::QTMEM)
+            umma_ts<TF32>(d_tmem, tmem + C::COL_Q + kk * 8, sdesc_sw128(kb + off, 16, 1024),
+                          kIdescQK, kk > 0 ? 1u : 0u);
+          else
+            umma_ss<TF32>(d_tmem, sdesc_sw128(sQ + off, 16, 1024),
+                          sdesc_sw128(kb + off, 16, 1024), kIdescQK, kk > 0 ? 1u : 0u);
         }
         tc_commit(bKempty + 8 * s);
-        tc_commit(bSfull + 8 * (j & 1));
+        tc_commit(bSfull + 8 * b);
+        if (++b == C::NS) { b = 0; bph ^= 1; }
+        if (++s == C::KST) { s = 0; sph ^= 1; }
       }
       // Every UMMA issued above must be complete before TMEM is freed.
       tc_commit(bFin);
@@ -297,15 +330,16 @@ __global__ void __launch_bounds__(224, 1)
       // bf16: V is an MN-major B operand.  fp32: V^T is a K-major B operand.
       constexpr uint32_t kIdescPV = make_idesc(kFmt, BM, D, 0u, TF32 ? 0u : 1u);
       bool ok = true;
+      int b = 0, bph = 0;   // score buffer of tile j and the parity of its use
+      int s = 0, sph = 0;   // V stage of tile j and its parity
       for (int j = 0; ok && j < n_kt; ++j) {
         // P_j ready (fp32 path: also V_j^T written).
-        if (!(ok = bounded_wait(bPfull + 8 * (j & 1), (j >> 1) & 1, w))) break;
-        const int s = j % C::VST;
+        if (!(ok = bounded_wait(bPfull + 8 * b, bph, w))) break;
         if constexpr (!TF32) {
-          if (!(ok = bounded_wait(bVfull + 8 * s, (j / C::VST) & 1, w))) break;
+          if (!(ok = bounded_wait(bVfull + 8 * s, sph, w))) break;
         }
         tc_fence_after();
-        const uint32_t a_tmem = tmem + ((j & 1) ? C::COL_S1 : C::COL_S0);
+        const uint32_t a_tmem = tmem + b * 128;
 #pragma unroll
         for (int kk = 0; kk < BN / C::UK; ++kk) {
           // UK keys per UMMA; the P slice is 8 TMEM columns.
@@ -322,7 +356,9 @@ __global__ void __launch_bounds__(224, 1)
                         (j > 0 || kk > 0) ? 1u : 0u);
         }
         if constexpr (!TF32) tc_commit(bVempty + 8 * s);
-        tc_commit(bOdone + 8 * (j & 1));
+        tc_commit(bOdone + 8 * b);
+        if (++b == C::NS) { b = 0; bph ^= 1; }
+        if (++s == C::VST) { s = 0; sph ^= 1; }
       }
       tc_commit(bFin2);
       bounded_wait(bFin2, 0, w, false);
@@ -400,7 +436,8 @@ __global__ void __launch_bounds__(224, 1)
 
     // Q row -> tensor memory (A operand layout: lane = row, 32-bit column c
     // holds bf16 elements 2c, 2c+1, or one tf32 element).  Rows past Nq are 0.
-    {
+    // (Otherwise the producer loads Q into shared memory with TMA.)
+    if constexpr (C::QTMEM) {
       const uint4 *src = reinterpret_cast<const uint4 *>(
           static_cast<const uint8_t *>(p.q) +
           (static_cast<size_t>(bh) * p.Nq + (row < p.Nq ? row : 0)) * (D * C::ESZ));
@@ -424,21 +461,22 @@ __global__ void __launch_bounds__(224, 1)
       }
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(bQready);
+      mbar_arrive(bQ);
     }
     if constexpr (TF32) ok = round_k_row(0);
 
+    int buf = 0, bph = 0;            // score buffer of tile j and the parity of its use
+    int pbuf = C::NS - 1, pbph = 1;  // the same for tile j - 1
     for (int j = 0; ok && j < n_kt; ++j) {
-      const int buf = j & 1;
       if constexpr (TF32) {
         // the next K tile is rounded before this tile's softmax so that
         // S_{j+1} = Q K_{j+1}^T still overlaps it
         if (j + 1 < n_kt && !(ok = round_k_row(j + 1))) break;
       }
-      ok = __all_sync(kFull, bounded_wait(bSfull + 8 * buf, (j >> 1) & 1, w));
+      ok = __all_sync(kFull, bounded_wait(bSfull + 8 * buf, bph, w));
       if (!ok) break;
       tc_fence_after();
-      const uint32_t s_tm = tmem + lane_off + (buf ? C::COL_S1 : C::COL_S0);
+      const uint32_t s_tm = tmem + lane_off + buf * 128;
       uint32_t sr[4][32];
       tmem_ld32(s_tm + 0, sr[0]);
       tmem_ld32(s_tm + 32, sr[1]);
@@ -493,15 +531,15 @@ __global__ void __launch_bounds__(224, 1)
       if (j == 0) {
         m_used = m_new;
       } else {
-        // P_j may overwrite P_{j-2} without waiting: S_j was only issued after
-        // P_{j-2} V_{j-2} had completed.  Only a rescale of O has to wait, for
-        // P_{j-1} V_{j-1} (the last UMMA into O before P_j V_j); the
-        // done-barriers alternate with the tile parity, and P_{j-3} V_{j-3}
-        // completed before S_{j-1} was issued, so a skipped wait never makes a
-        // later one ambiguous.
+        // P_j may overwrite P_{j-NS} without waiting: S_j was only issued
+        // after P_{j-NS} V_{j-NS} had completed.  Only a rescale of O has to
+        // wait, for P_{j-1} V_{j-1} (the last UMMA into O before P_j V_j); the
+        // done-barriers are per score buffer, and the previous use of tile
+        // j-1's buffer (P_{j-1-NS} V_{j-1-NS}) completed before S_{j-1} was
+        // issued, so a skipped wait never makes a later one ambiguous.
         const bool need = (m_new - m_used) > kRescaleThreshold;
         if (__any_sync(kFull, need)) {
-          ok = __all_sync(kFull, bounded_wait(bOdone + 8 * ((j - 1) & 1), ((j - 1) >> 1) & 1, w));
+          ok = __all_sync(kFull, bounded_wait(bOdone + 8 * pbuf, pbph, w));
           if (!ok) break;
           tc_fence_after();
           const float alpha = need ? ex2_approx(m_used - m_new) : 1.f;
@@ -585,12 +623,15 @@ __global__ void __launch_bounds__(224, 1)
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(bPfull + 8 * buf);
+      pbuf = buf;
+      pbph = bph;
+      if (++buf == C::NS) { buf = 0; bph ^= 1; }
     }
 
     // ------------------------------------------------ epilogue
     // The last P V; its commit also covers every earlier UMMA.
     if (ok)
-      ok = __all_sync(kFull, bounded_wait(bOdone + 8 * ((n_kt - 1) & 1), ((n_kt - 1) >> 1) & 1, w));
+      ok = __all_sync(kFull, bounded_wait(bOdone + 8 * pbuf, pbph, w));
     if (ok) {
       tc_fence_after();
       const float inv_l = 1.f / l;
@@ -659,10 +700,12 @@ __global__ void __launch_bounds__(224, 1)
 }
 
 template <int D, bool TF32>
-cudaError_t launch_tc(const CUtensorMap &k, const CUtensorMap &v, const CUtensorMap &o,
-                      const TcParams &p, int B, int causal, cudaStream_t stream) {
+cudaError_t launch_tc(const CUtensorMap &q, const CUtensorMap &k, const CUtensorMap &v,
+                      const CUtensorMap &o, const TcParams &p, int B, int causal,
+                      cudaStream_t stream) {
   using C = TcCfg<D, TF32>;
-  void (*kern)(const CUtensorMap, const CUtensorMap, const CUtensorMap, const TcParams) =
+  void (*kern)(const CUtensorMap, const CUtensorMap, const CUtensorMap, const CUtensorMap,
+               const TcParams) =
       causal ? fa_tc_fwd_kernel<D, TF32, true> : fa_tc_fwd_kernel<D, TF32, false>;
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
@@ -675,7 +718,7 @@ cudaError_t launch_tc(const CUtensorMap &k, const CUtensorMap &v, const CUtensor
   cfg.stream = stream;
   cfg.attrs = nullptr;
   cfg.numAttrs = 0;
-  return cudaLaunchKernelEx(&cfg, kern, k, v, o, p);
+  return cudaLaunchKernelEx(&cfg, kern, q, k, v, o, p);
 }
 
 }  // namespace fa

@@ -4,10 +4,10 @@
 
 namespace fa {
 
-cudaError_t launch_tc_bf16_d64(const CUtensorMap &k, const CUtensorMap &v, const CUtensorMap &o,
-                         const TcParams &p, int B, int causal,
+cudaError_t launch_tc_bf16_d64(const CUtensorMap &q, const CUtensorMap &k, const CUtensorMap &v,
+                         const CUtensorMap &o, const TcParams &p, int B, int causal,
                          cudaStream_t s) {
-  return launch_tc<64, false>(k, v, o, p, B, causal, s);
+  return launch_tc<64, false>(q, k, v, o, p, B, causal, s);
 }
 
 }  // namespace fa
