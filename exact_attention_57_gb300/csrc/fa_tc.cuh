@@ -83,7 +83,7 @@ struct TcCfg {
   static constexpr uint32_t COL_Q = COL_O + D;
   static constexpr int NQ = QTMEM ? 0 : 1;                  // Q tiles in shared memory
   static constexpr int KST = TF32 ? 2 : (TILE_BYTES <= 16384 ? 4 : 3); // K ring depth
-  static constexpr int VST = TF32 ? 2 : (TILE_BYTES <= 16384 ? 4 : (QTMEM ? 3 : 2)); // V ring
+  static constexpr int VST = TF32 ? 2 : (TILE_BYTES <= 16384 ? 4 : 3); // V ring depth
   // fp32 path: V_j is transposed by the softmax warps into a K-major copy
   // (V^T, d rows of 128 keys, tf32-rounded) because P V runs as kind::tf32
   // with V^T as a K-major B operand.  Two copies alternate.
@@ -236,9 +236,12 @@ __global__ void __launch_bounds__(224, 1)
       }
       int nk = 0, nv = 0;  // loads issued
       bool ok = true;
-      // Load order = consumption order: K0, K1, V0, K2, V1, ...
-      for (int j = -1; ok && j < n_kt; ++j) {
-        const int jk = j + 1;  // next K tile
+      // Load order = consumption order: S runs NS - 1 tiles ahead of P V, so
+      // K_{j+NS-1} is loaded just before V_j (K0, K1, K2, V0, K3, V1, ... for
+      // NS = 3).
+      constexpr int kAhead = C::NS - 1;
+      for (int j = -kAhead; ok && j < n_kt; ++j) {
+        const int jk = j + kAhead;  // next K tile
         if (jk < n_kt) {
           const int s = jk % C::KST, r = jk / C::KST;
           if (r > 0) ok = bounded_wait(bKempty + 8 * s, (r - 1) & 1, w);
