@@ -26,7 +26,7 @@ PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 std::atomic<int> g_skip_v_load{0};
 std::atomic<unsigned long long> g_wait_limit_ns{0};
 
-size_t elem_size(int dtype) { return dtype == FA_DTYPE_BF16 ? 2 : 4; }
+size_t elem_size(int dtype) { return (dtype == FA_DTYPE_BF16 || dtype == FA_DTYPE_F16) ? 2 : 4; }
 
 bool overlap(const void *a, size_t an, const void *b, size_t bn) {
   const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
@@ -41,7 +41,8 @@ int validate(const void *q, const void *k, const void *v, const void *o, const f
   if (B > 65535 || H > 65535) return FA_ERR_INVALID_ARG;
   if (!std::isfinite(scale)) return FA_ERR_INVALID_ARG;
   if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
-  if (dtype != FA_DTYPE_BF16 && dtype != FA_DTYPE_F32 && dtype != FA_DTYPE_F32_SIMT)
+  if (dtype != FA_DTYPE_BF16 && dtype != FA_DTYPE_F32 && dtype != FA_DTYPE_F32_SIMT &&
+      dtype != FA_DTYPE_F16)
     return FA_ERR_INVALID_ARG;
   for (const void *ptr : {q, k, v, o})
     if (reinterpret_cast<uintptr_t>(ptr) % 16 != 0) return FA_ERR_INVALID_ARG;
@@ -59,7 +60,8 @@ int validate(const void *q, const void *k, const void *v, const void *o, const f
       overlap(lse, ln, v, kn))
     return FA_ERR_INVALID_ARG;
   // The compiled set of kernels.
-  if (dtype == FA_DTYPE_BF16 && d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+  if ((dtype == FA_DTYPE_BF16 || dtype == FA_DTYPE_F16) && d != 64 && d != 128)
+    return FA_ERR_UNSUPPORTED;
   if (dtype == FA_DTYPE_F32 && d != 64) return FA_ERR_UNSUPPORTED;
   if (dtype == FA_DTYPE_F32_SIMT && d > 128) return FA_ERR_UNSUPPORTED;
   return FA_OK;
@@ -110,8 +112,9 @@ int get_encoder() {
 // 128 rows, 1 head}, 128-byte swizzle, zero fill outside the tensor (rows past
 // N read as zeros and are clipped on store).
 int encode_map(CUtensorMap *map, const void *base, int dtype, int BH, int N, int d) {
-  const CUtensorMapDataType dt =
-      dtype == FA_DTYPE_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+  const CUtensorMapDataType dt = dtype == FA_DTYPE_BF16  ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                 : dtype == FA_DTYPE_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                                         : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
   const cuuint64_t es = elem_size(dtype);
   cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N),
                         static_cast<cuuint64_t>(BH)};
@@ -126,6 +129,17 @@ int encode_map(CUtensorMap *map, const void *base, int dtype, int BH, int N, int
 }
 
 int ceil_div(int a, int b) { return (a + b - 1) / b; }
+
+// The tensor-core kernels take |scale| * log2(e) > 0 and apply a negative
+// scale by negating Q inside the S = Q K^T product.  A zero scale becomes
+// 1e-30: for scores below 1e20 in magnitude every exponent is then below
+// 2^-40, so each exp2 rounds to exactly 1 and the weights are exactly uniform,
+// as they are for scale 0.
+void set_tc_scale(float scale, fa::TcParams *p) {
+  const double a = scale == 0.f ? 1e-30 : std::fabs(static_cast<double>(scale));
+  p->scale_log2 = static_cast<float>(a * 1.4426950408889634);
+  p->scale_neg = scale < 0.f ? 1 : 0;
+}
 
 }  // namespace
 
@@ -174,14 +188,16 @@ int fa_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int
   p.Nk = Nk;
   p.n_qtiles = ceil_div(Nq, fa::BM);
   p.n_ktiles = ceil_div(Nk, fa::BN);
-  p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
-  p.scale_neg = scale < 0.f ? 1 : 0;
+  set_tc_scale(scale, &p);
   const unsigned long long lim = g_wait_limit_ns.load();
   p.wait_limit_ns = lim ? lim : fa::kDefaultWaitLimitNs;
   p.skip_v_load = g_skip_v_load.load();
 
   cudaError_t e;
-  if (dtype == FA_DTYPE_BF16)
+  if (dtype == FA_DTYPE_F16)
+    e = (d == 64) ? fa::launch_tc_f16_d64(mq, mk, mv, mo, p, B, causal, s)
+                  : fa::launch_tc_f16_d128(mq, mk, mv, mo, p, B, causal, s);
+  else if (dtype == FA_DTYPE_BF16)
     e = (d == 64) ? fa::launch_tc_bf16_d64(mq, mk, mv, mo, p, B, causal, s)
                   : fa::launch_tc_bf16_d128(mq, mk, mv, mo, p, B, causal, s);
   else
@@ -353,13 +369,15 @@ extern "C" int fa_fwd_noalloc(const void *q, const void *k, const void *v, void 
     p.Nk = Nk;
     p.n_qtiles = ceil_div(Nq, fa::BM);
     p.n_ktiles = ceil_div(Nk, fa::BN);
-    p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
-    p.scale_neg = scale < 0.f ? 1 : 0;
+    set_tc_scale(scale, &p);
     const unsigned long long lim = g_wait_limit_ns.load();
     p.wait_limit_ns = lim ? lim : fa::kDefaultWaitLimitNs;
     p.skip_v_load = g_skip_v_load.load();
     cudaError_t e;
-    if (dtype == FA_DTYPE_BF16)
+    if (dtype == FA_DTYPE_F16)
+      e = (d == 64) ? fa::launch_tc_f16_d64(mq, mk, mv, mo, p, B, causal, s)
+                    : fa::launch_tc_f16_d128(mq, mk, mv, mo, p, B, causal, s);
+    else if (dtype == FA_DTYPE_BF16)
       e = (d == 64) ? fa::launch_tc_bf16_d64(mq, mk, mv, mo, p, B, causal, s)
                     : fa::launch_tc_bf16_d128(mq, mk, mv, mo, p, B, causal, s);
     else

@@ -27,8 +27,8 @@ struct TcParams {
   unsigned *status;               // per-device status word
   int H, Nq, Nk;
   int n_qtiles, n_ktiles;         // ceil(Nq/BM), ceil(Nk/BN)
-  float scale_log2;               // scale * log2(e)
-  int scale_neg;                  // scale < 0
+  float scale_log2;               // |scale| * log2(e) > 0
+  int scale_neg;                  // scale < 0: S is computed as (-Q) K^T
   unsigned long long wait_limit_ns;
   int skip_v_load;                // test hook
 };
@@ -54,6 +54,13 @@ cudaError_t launch_tc_bf16_d128(const CUtensorMap &q, const CUtensorMap &k, cons
 cudaError_t launch_tc_f32_d64(const CUtensorMap &q, const CUtensorMap &k, const CUtensorMap &v,
                               const CUtensorMap &o, const TcParams &p, int B, int causal,
                               cudaStream_t s);
+
+cudaError_t launch_tc_f16_d64(const CUtensorMap &q, const CUtensorMap &k, const CUtensorMap &v,
+                              const CUtensorMap &o, const TcParams &p, int B, int causal,
+                              cudaStream_t s);
+cudaError_t launch_tc_f16_d128(const CUtensorMap &q, const CUtensorMap &k, const CUtensorMap &v,
+                               const CUtensorMap &o, const TcParams &p, int B, int causal,
+                               cudaStream_t s);
 
 cudaError_t launch_simt(const SimtParams &p, int B, cudaStream_t s);
 

@@ -139,7 +139,9 @@ __device__ __forceinline__ bool bounded_wait(uint32_t bar, uint32_t parity, cons
   }
 }
 
-template <int D, bool TF32, bool CAUSAL>
+// HALF selects fp16 instead of bf16 for the 16-bit path (kind::f16 either
+// way; P and O are packed in the input type).
+template <int D, bool TF32, bool CAUSAL, bool HALF>
 __global__ void __launch_bounds__(224, 1)
     fa_tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                      const __grid_constant__ CUtensorMap tm_k,
@@ -288,8 +290,11 @@ __global__ void __launch_bounds__(224, 1)
     // other issuer warp, so S_j waits for that P V to complete.
     w.role = kStatusMma;
     if (lane == 0) {
-      constexpr uint32_t kFmt = TF32 ? 2u : 1u;
+      constexpr uint32_t kFmt = TF32 ? 2u : (HALF ? 0u : 1u);  // tf32 / f16 / bf16
       constexpr uint32_t kIdescQK = make_idesc(kFmt, BM, BN, 0u, 0u);  // K is K-major
+      // A negative scale is applied as S = (-Q) K^T (the descriptor's negate-A
+      // bit) with |scale|, so the softmax only ever sees a positive scale.
+      const uint32_t idesc_qk = kIdescQK | (p.scale_neg ? (1u << 13) : 0u);
       bool ok = bounded_wait(bQ, 0, w);
       if (ok) tc_fence_after();
       int b = 0, bph = 0;   // score buffer of tile j and the parity of its use
@@ -308,10 +313,10 @@ __global__ void __launch_bounds__(224, 1)
           const uint32_t off = (kk >> 2) * C::CHUNK_BYTES + (kk & 3) * 32;
           if constexpr (C::QTMEM)
             umma_ts<TF32>(d_tmem, tmem + C::COL_Q + kk * 8, sdesc_sw128(kb + off, 16, 1024),
-                          kIdescQK, kk > 0 ? 1u : 0u);
+                          idesc_qk, kk > 0 ? 1u : 0u);
           else
             umma_ss<TF32>(d_tmem, sdesc_sw128(sQ + off, 16, 1024),
-                          sdesc_sw128(kb + off, 16, 1024), kIdescQK, kk > 0 ? 1u : 0u);
+                          sdesc_sw128(kb + off, 16, 1024), idesc_qk, kk > 0 ? 1u : 0u);
         }
         tc_commit(bKempty + 8 * s);
         tc_commit(bSfull + 8 * b);
@@ -329,7 +334,7 @@ __global__ void __launch_bounds__(224, 1)
     // leave the tensor pipe idle while the other has work ready.
     w.role = kStatusMma;
     if (lane == 0) {
-      constexpr uint32_t kFmt = TF32 ? 2u : 1u;
+      constexpr uint32_t kFmt = TF32 ? 2u : (HALF ? 0u : 1u);  // tf32 / f16 / bf16
       // bf16: V is an MN-major B operand.  fp32: V^T is a K-major B operand.
       constexpr uint32_t kIdescPV = make_idesc(kFmt, BM, D, 0u, TF32 ? 0u : 1u);
       bool ok = true;
@@ -375,7 +380,6 @@ __global__ void __launch_bounds__(224, 1)
     const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
     const uint32_t o_tm = tmem + lane_off + C::COL_O;
     const float sl2 = p.scale_log2;
-    const bool neg = p.scale_neg != 0;
     const int row_lim = CAUSAL ? min(row + 1, p.Nk) : p.Nk;  // keys [0, row_lim)
     float m_used = -INFINITY;  // exponent offset, log2 units of the scaled score
     float l = 0.f;
@@ -493,43 +497,26 @@ __global__ void __launch_bounds__(224, 1)
       auto S = [&](int c) -> float { return __uint_as_float(sr[c >> 5][c & 31]); };
 
       const int lim = row_lim - j * BN;  // valid columns c < lim
-      // Row max of the raw scores over the valid columns (for a negative
-      // scale the min becomes the max); masked tiles (causal diagonal, ragged
-      // key tail) take a separate compile-time path.
-      auto row_max = [&](auto mask_tag, auto neg_tag) -> float {
-        constexpr bool kMask = decltype(mask_tag)::value;
-        constexpr bool kNeg = decltype(neg_tag)::value;
-        constexpr float fill = kNeg ? INFINITY : -INFINITY;
-        // eight independent chains of three-input max keep the dependency
-        // depth at 8 for the 128 columns
+      // Masked tiles (causal diagonal, ragged key tail; at most two per CTA)
+      // set the excluded scores to -inf, so one code path serves every tile:
+      // they drop out of the max, and exp2(-inf) = 0 (the scale is > 0 here).
+      if (__any_sync(kFull, lim < BN)) {
+#pragma unroll
+        for (int c = 0; c < BN; ++c)
+          if (c >= lim) sr[c >> 5][c & 31] = 0xff800000u;  // -inf
+      }
+      // Row max: eight independent chains of three-input max keep the
+      // dependency depth at 8 for the 128 columns.
+      float mx;
+      {
         float part[8];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) part[i] = fill;
+        for (int i = 0; i < 8; ++i) part[i] = -INFINITY;
 #pragma unroll
-        for (int c = 0; c < BN; c += 2) {
-          float a = S(c), b = S(c + 1);
-          if constexpr (kMask) {
-            a = (c < lim) ? a : fill;
-            b = (c + 1 < lim) ? b : fill;
-          }
-          const int i = (c >> 1) & 7;
-          part[i] = kNeg ? min3f(part[i], a, b) : max3f(part[i], a, b);
-        }
-        if constexpr (kNeg)
-          return min3f(min3f(part[0], part[1], part[2]), min3f(part[3], part[4], part[5]),
-                       fminf(part[6], part[7]));
-        else
-          return max3f(max3f(part[0], part[1], part[2]), max3f(part[3], part[4], part[5]),
-                       fmaxf(part[6], part[7]));
-      };
-      const bool masked = __any_sync(kFull, lim < BN);
-      float mx;
-      if (masked)
-        mx = neg ? row_max(std::true_type{}, std::true_type{})
-                 : row_max(std::true_type{}, std::false_type{});
-      else
-        mx = neg ? row_max(std::false_type{}, std::true_type{})
-                 : row_max(std::false_type{}, std::false_type{});
+        for (int c = 0; c < BN; c += 2) part[(c >> 1) & 7] = max3f(part[(c >> 1) & 7], S(c), S(c + 1));
+        mx = max3f(max3f(part[0], part[1], part[2]), max3f(part[3], part[4], part[5]),
+                   fmaxf(part[6], part[7]));
+      }
       const float m_new = fmaxf(m_used, mx * sl2);
       if (j == 0) {
         m_used = m_new;
@@ -574,8 +561,7 @@ __global__ void __launch_bounds__(224, 1)
       const uint64_t sl2_2 = pk2(sl2, sl2);
       const uint64_t nm_2 = pk2(-m_used, -m_used);
       uint64_t acc[2] = {0ull, 0ull};  // packed partial row sums (+0.0f bits)
-      auto write_p = [&](auto mask_tag) {
-        constexpr bool kMask = decltype(mask_tag)::value;
+      {
         constexpr int kBlk = TF32 ? 16 : 32;  // column pairs per TMEM store
 #pragma unroll
         for (int blk = 0; blk < 64 / kBlk; ++blk) {
@@ -593,25 +579,17 @@ __global__ void __launch_bounds__(224, 1)
               p0 = ex2_approx(x0);
               p1 = ex2_approx(x1);
             }
-            if constexpr (kMask) {
-              p0 = (c0 < lim) ? p0 : 0.f;
-              p1 = (c0 + 1 < lim) ? p1 : 0.f;
-            }
             acc[i & 1] = fadd2(acc[i & 1], pk2(p0, p1));
             if constexpr (TF32) {
               pk[2 * i] = to_tf32(p0);
               pk[2 * i + 1] = to_tf32(p1);
             } else {
-              pk[i] = pack_bf16x2(p0, p1);
+              pk[i] = HALF ? pack_f16x2(p0, p1) : pack_bf16x2(p0, p1);
             }
           }
           tmem_st32(s_tm + blk * 32, pk);
         }
-      };
-      if (masked)
-        write_p(std::true_type{});
-      else
-        write_p(std::false_type{});
+      }
       {
         float a0, a1, b0, b1;
         upk2(acc[0], a0, a1);
@@ -661,17 +639,20 @@ __global__ void __launch_bounds__(224, 1)
                                        ((u ^ (r & 7)) << 4)) = val;
           }
         } else {
-          // 32 bf16 = 4 units of 16 bytes; global unit index c/8 + u.
+          // 32 16-bit values = 4 units of 16 bytes; global unit index c/8 + u.
+          auto pack16 = [](float lo, float hi) {
+            return HALF ? pack_f16x2(lo, hi) : pack_bf16x2(lo, hi);
+          };
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
             uint4 val;
-            val.x = pack_bf16x2(__uint_as_float(o[8 * u + 0]) * inv_l,
+            val.x = pack16(__uint_as_float(o[8 * u + 0]) * inv_l,
                                 __uint_as_float(o[8 * u + 1]) * inv_l);
-            val.y = pack_bf16x2(__uint_as_float(o[8 * u + 2]) * inv_l,
+            val.y = pack16(__uint_as_float(o[8 * u + 2]) * inv_l,
                                 __uint_as_float(o[8 * u + 3]) * inv_l);
-            val.z = pack_bf16x2(__uint_as_float(o[8 * u + 4]) * inv_l,
+            val.z = pack16(__uint_as_float(o[8 * u + 4]) * inv_l,
                                 __uint_as_float(o[8 * u + 5]) * inv_l);
-            val.w = pack_bf16x2(__uint_as_float(o[8 * u + 6]) * inv_l,
+            val.w = pack16(__uint_as_float(o[8 * u + 6]) * inv_l,
                                 __uint_as_float(o[8 * u + 7]) * inv_l);
             const int gu = c / 8 + u;
             const int ch = gu >> 3, uu = gu & 7;
@@ -702,14 +683,14 @@ __global__ void __launch_bounds__(224, 1)
   }
 }
 
-template <int D, bool TF32>
+template <int D, bool TF32, bool HALF = false>
 cudaError_t launch_tc(const CUtensorMap &q, const CUtensorMap &k, const CUtensorMap &v,
                       const CUtensorMap &o, const TcParams &p, int B, int causal,
                       cudaStream_t stream) {
   using C = TcCfg<D, TF32>;
   void (*kern)(const CUtensorMap, const CUtensorMap, const CUtensorMap, const CUtensorMap,
                const TcParams) =
-      causal ? fa_tc_fwd_kernel<D, TF32, true> : fa_tc_fwd_kernel<D, TF32, false>;
+      causal ? fa_tc_fwd_kernel<D, TF32, true, HALF> : fa_tc_fwd_kernel<D, TF32, false, HALF>;
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
   if (e != cudaSuccess) return e;

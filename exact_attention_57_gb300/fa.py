@@ -27,6 +27,7 @@ FA_ERR_DEVICE_TIMEOUT = 4
 FA_DTYPE_BF16 = 0
 FA_DTYPE_F32 = 1
 FA_DTYPE_F32_SIMT = 2
+FA_DTYPE_F16 = 3
 
 EXPORTED = ("fa_fwd", "fa_fwd_host", "fa_fwd_status", "fa_status_string", "fa_version",
             "fa_set_test_hooks", "fa_fwd_noalloc")
@@ -125,6 +126,10 @@ def _dtype_code(t, impl: str) -> int:
         if impl != "tc":
             raise ValueError("bf16 inputs run on the tensor-core kernel only")
         return FA_DTYPE_BF16
+    if t.dtype == torch.float16:
+        if impl != "tc":
+            raise ValueError("fp16 inputs run on the tensor-core kernel only")
+        return FA_DTYPE_F16
     if t.dtype == torch.float32:
         return FA_DTYPE_F32 if impl == "tc" else FA_DTYPE_F32_SIMT
     raise ValueError(f"unsupported dtype {t.dtype}")
@@ -134,7 +139,7 @@ def attention(q, k, v, scale: float | None = None, causal: bool = False, impl: s
               out=None, lse=None, stream=None):
     """O, LSE for contiguous CUDA tensors q [B,H,Nq,d], k/v [B,H,Nk,d].
 
-    impl "tc": bf16 -> tcgen05 kind::f16, fp32 -> tcgen05 kind::tf32;
+    impl "tc": bf16 / fp16 -> tcgen05 kind::f16, fp32 -> tcgen05 kind::tf32;
     impl "simt": fp32 only, plain fp32 kernel.  Raises FaError on failure.
     """
     import torch

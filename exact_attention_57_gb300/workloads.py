@@ -21,8 +21,10 @@ import torch
 DTYPE_BF16 = 0      # bf16 in/out, tcgen05 kind::f16
 DTYPE_F32 = 1       # fp32 in/out, tcgen05 kind::tf32
 DTYPE_F32_SIMT = 2  # fp32 in/out, plain fp32 FMA kernel (no tensor cores)
+DTYPE_F16 = 3       # fp16 in/out, tcgen05 kind::f16
 
-DTYPE_NAMES = {DTYPE_BF16: "bf16", DTYPE_F32: "f32", DTYPE_F32_SIMT: "f32_simt"}
+DTYPE_NAMES = {DTYPE_BF16: "bf16", DTYPE_F32: "f32", DTYPE_F32_SIMT: "f32_simt",
+               DTYPE_F16: "f16"}
 
 
 @dataclass(frozen=True)
@@ -45,7 +47,8 @@ class Workload:
 
     @property
     def torch_dtype(self):
-        return torch.bfloat16 if self.dtype == DTYPE_BF16 else torch.float32
+        return {DTYPE_BF16: torch.bfloat16, DTYPE_F16: torch.float16}.get(self.dtype,
+                                                                         torch.float32)
 
     def flops(self, causal: bool) -> float:
         """Metric FLOPs: 4*B*H*Nq*Nk*d, halved for causal."""
@@ -98,6 +101,8 @@ def make_inputs(B: int, H: int, Nq: int, Nk: int, d: int, dtype: int,
         k.mul_(float(k_mult))
     if dtype == DTYPE_BF16:
         q, k, v = q.to(torch.bfloat16), k.to(torch.bfloat16), v.to(torch.bfloat16)
+    elif dtype == DTYPE_F16:
+        q, k, v = q.to(torch.float16), k.to(torch.float16), v.to(torch.float16)
     return q, k, v
 
 

@@ -26,6 +26,8 @@
  *                                    products, fp32 accumulation.
  *           dtype FA_DTYPE_F32_SIMT  q, k, v, o are fp32; plain fp32 FMA
  *                                    kernel, no tensor cores.
+ *           dtype FA_DTYPE_F16       q, k, v, o are fp16; fp32 accumulation
+ *                                    (the bf16 kernels with fp16 operands).
  *           lse is always fp32, natural log, in units of the scaled score.
  * Masking:  causal = 1 keeps key j for query i iff j <= i (top-left aligned,
  *           the rule of the forward kernel of "flash_attention_2.cu").  Keys
@@ -54,7 +56,8 @@ extern "C" {
 typedef enum {
     FA_DTYPE_BF16 = 0,
     FA_DTYPE_F32 = 1,
-    FA_DTYPE_F32_SIMT = 2
+    FA_DTYPE_F32_SIMT = 2,
+    FA_DTYPE_F16 = 3
 } fa_dtype;
 
 typedef enum {
@@ -78,7 +81,8 @@ typedef enum {
  *           written.
  * B, H      batch size and number of heads, 1 .. 65535.
  * Nq, Nk    query and key sequence lengths, >= 1 (ragged lengths allowed).
- * d         head dimension.  FA_DTYPE_BF16: 64 or 128.  FA_DTYPE_F32: 64.
+ * d         head dimension.  FA_DTYPE_BF16, FA_DTYPE_F16: 64 or 128.
+ *           FA_DTYPE_F32: 64.
  *           FA_DTYPE_F32_SIMT: 1 .. 128.  Anything else is
  *           FA_ERR_UNSUPPORTED (the role of the "Failed to find groupsize ...
  *           Shared Memory constraint" error of "Flash Attention Shared Memory

@@ -60,7 +60,7 @@ def call(**kw):
     dict(B=0), dict(H=0), dict(Nq=0), dict(Nk=0), dict(d=0), dict(B=-3),
     dict(B=70000), dict(H=70000),
     dict(scale=float("nan")), dict(scale=float("inf")),
-    dict(causal=2), dict(causal=-1), dict(dtype=3), dict(dtype=-1),
+    dict(causal=2), dict(causal=-1), dict(dtype=4), dict(dtype=-1),
     dict(q=Q + 8), dict(o=O + 4), dict(lse=L + 2),
     dict(o=Q), dict(o=Q + 1024), dict(lse=O + 16), dict(lse=K + 64),
 ], ids=lambda kw: ",".join(f"{k}={v}" for k, v in kw.items()))
@@ -72,6 +72,7 @@ def test_invalid_arguments(lib, kw):
     dict(dtype=fa.FA_DTYPE_BF16, d=32), dict(dtype=fa.FA_DTYPE_BF16, d=96),
     dict(dtype=fa.FA_DTYPE_BF16, d=256), dict(dtype=fa.FA_DTYPE_F32, d=128),
     dict(dtype=fa.FA_DTYPE_F32, d=32), dict(dtype=fa.FA_DTYPE_F32_SIMT, d=129),
+    dict(dtype=fa.FA_DTYPE_F16, d=96), dict(dtype=fa.FA_DTYPE_F16, d=256),
 ], ids=lambda kw: ",".join(f"{k}={v}" for k, v in kw.items()))
 def test_unsupported_problems(lib, kw):
     """Valid problems outside the compiled set are refused, not attempted."""
