@@ -225,6 +225,8 @@ def main():
     ap.add_argument("--workload", default=None)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--splits", type=int, default=None,
+                    help="run fa_fwd_splitkv with this many key chunks (0 = automatic)")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
 
@@ -259,9 +261,20 @@ def main():
     sh = stream.cuda_stream
     impl = "simt" if w.dtype == 2 else "tc"
 
+    wspace = None  # split-KV workspace
+    if args.splits is not None:
+        wsb = fa.fa_fwd_splitkv_workspace(w.B, w.H, w.Nq, w.d, args.splits if args.splits else 64)
+        wspace = torch.empty(max(wsb, 256), dtype=torch.uint8, device=dev)
+
     def step():
-        st = fa.fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
-                       w.B, w.H, w.Nq, w.Nk, w.d, w.scale, int(causal), w.dtype, sh)
+        if wspace is None:
+            st = fa.fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                           w.B, w.H, w.Nq, w.Nk, w.d, w.scale, int(causal), w.dtype, sh)
+        else:
+            st = fa.fa_fwd_splitkv(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                   lse.data_ptr(), w.B, w.H, w.Nq, w.Nk, w.d, w.scale,
+                                   int(causal), w.dtype, args.splits, wspace.data_ptr(),
+                                   wspace.numel(), sh)
         if st != fa.FA_OK:
             raise fa.FaError(st, "fa_fwd")
 
@@ -363,12 +376,13 @@ def main():
         "config": {"workload": w.name, "B": w.B, "H": w.H, "Nq": w.Nq, "Nk": w.Nk, "d": w.d,
                    "causal": causal, "flops_per_step": flops_step,
                    "parallelism": f"replicas{ws}" if ws > 1 else "single",
+                   "key_splits": args.splits,
                    "l2": "inputs larger than L2 (no flush)"},
         "roofline": roofline,
         "pct_of_peak": 100.0 * value / ws / peak,
         "cpu_baseline": cpu,
         "e2e": e2e,
-        "gpu_launches": args.steps,
+        "gpu_launches": args.steps * (2 if wspace is not None else 1),
         "clocks": clocks,
     }
     print(json.dumps(line), flush=True)

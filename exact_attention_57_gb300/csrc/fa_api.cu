@@ -393,3 +393,120 @@ extern "C" int fa_fwd_noalloc(const void *q, const void *k, const void *v, void 
   *device_status = static_cast<int>(word);
   return word ? FA_ERR_DEVICE_TIMEOUT : FA_OK;
 }
+
+// ---------------------------------------------------------------------------
+// Split over the key range.
+// ---------------------------------------------------------------------------
+namespace {
+
+constexpr int kMaxSplits = 64;
+
+size_t splitkv_ws_bytes(int B, int H, int Nq, int d, int nsp) {
+  const size_t rows = static_cast<size_t>(nsp) * B * H * Nq;
+  const size_t o_bytes = (rows * d * sizeof(float) + 255) & ~static_cast<size_t>(255);
+  const size_t l_bytes = (rows * sizeof(float) + 255) & ~static_cast<size_t>(255);
+  return o_bytes + l_bytes;
+}
+
+int sm_count() {
+  static int count[kMaxDevices] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
+  if (count[dev] == 0) {
+    int c = 0;
+    if (cudaDeviceGetAttribute(&c, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    count[dev] = c;
+  }
+  return count[dev];
+}
+
+}  // namespace
+
+extern "C" unsigned long long fa_fwd_splitkv_workspace(int B, int H, int Nq, int d, int num_splits) {
+  if (B < 1 || H < 1 || Nq < 1 || d < 1 || num_splits < 1 || num_splits > kMaxSplits) return 0;
+  return splitkv_ws_bytes(B, H, Nq, d, num_splits);
+}
+
+extern "C" int fa_fwd_splitkv(const void *q, const void *k, const void *v, void *o, float *lse,
+                              int B, int H, int Nq, int Nk, int d, float scale, int causal,
+                              int dtype, int num_splits, void *workspace,
+                              unsigned long long workspace_bytes, void *stream) {
+  int rc = validate(q, k, v, o, lse, B, H, Nq, Nk, d, scale, causal, dtype);
+  if (rc != FA_OK) return rc;
+  if (num_splits < 0 || num_splits > kMaxSplits) return FA_ERR_INVALID_ARG;
+  if (dtype == FA_DTYPE_F32_SIMT) return FA_ERR_UNSUPPORTED;
+  const int n_qtiles = ceil_div(Nq, fa::BM), n_ktiles = ceil_div(Nk, fa::BN);
+  if (num_splits > 0) {
+    // The workspace is checked before anything touches the device.
+    const size_t need = splitkv_ws_bytes(B, H, Nq, d, num_splits);
+    if (num_splits > 1 &&
+        (workspace == nullptr || reinterpret_cast<uintptr_t>(workspace) % 256 != 0 ||
+         workspace_bytes < need))
+      return FA_ERR_INVALID_ARG;
+  }
+  int nsp = num_splits;
+  if (nsp == 0) {
+    // About two CTAs' worth of work per SM, at least one key tile per chunk.
+    const int sms = sm_count();
+    if (sms == 0) return FA_ERR_CUDA;
+    const long long ctas = static_cast<long long>(n_qtiles) * B * H;
+    nsp = static_cast<int>((2LL * sms + ctas - 1) / ctas);
+    nsp = nsp < 1 ? 1 : (nsp > n_ktiles ? n_ktiles : nsp);
+    if (nsp > kMaxSplits) nsp = kMaxSplits;
+    while (nsp > 1 && (workspace == nullptr ||
+                       reinterpret_cast<uintptr_t>(workspace) % 256 != 0 ||
+                       workspace_bytes < splitkv_ws_bytes(B, H, Nq, d, nsp)))
+      --nsp;  // the largest split count the workspace holds
+  }
+  if (nsp <= 1) return fa_fwd(q, k, v, o, lse, B, H, Nq, Nk, d, scale, causal, dtype, stream);
+  const size_t need = splitkv_ws_bytes(B, H, Nq, d, nsp);
+  const size_t o_part = need - ((static_cast<size_t>(nsp) * B * H * Nq * sizeof(float) + 255) &
+                                ~static_cast<size_t>(255));
+  float *ws_o = static_cast<float *>(workspace);
+  float *ws_lse = reinterpret_cast<float *>(static_cast<char *>(workspace) + o_part);
+  if (overlap(workspace, need, q, static_cast<size_t>(B) * H * Nq * d * elem_size(dtype)) ||
+      overlap(workspace, need, k, static_cast<size_t>(B) * H * Nk * d * elem_size(dtype)) ||
+      overlap(workspace, need, v, static_cast<size_t>(B) * H * Nk * d * elem_size(dtype)) ||
+      overlap(workspace, need, o, static_cast<size_t>(B) * H * Nq * d * elem_size(dtype)) ||
+      overlap(workspace, need, lse, static_cast<size_t>(B) * H * Nq * sizeof(float)))
+    return FA_ERR_INVALID_ARG;
+
+  unsigned *status = nullptr;
+  if ((rc = device_setup(&status)) != FA_OK) return rc;
+  if ((rc = get_encoder()) != FA_OK) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  CUtensorMap mq, mk, mv, mo;
+  const int BH = B * H;
+  if ((rc = encode_map(&mq, q, dtype, BH, Nq, d)) != FA_OK) return rc;
+  if ((rc = encode_map(&mk, k, dtype, BH, Nk, d)) != FA_OK) return rc;
+  if ((rc = encode_map(&mv, v, dtype, BH, Nk, d)) != FA_OK) return rc;
+  if ((rc = encode_map(&mo, o, dtype, BH, Nq, d)) != FA_OK) return rc;
+  fa::TcParams p;
+  p.q = q;
+  p.lse = lse;
+  p.status = status;
+  p.H = H;
+  p.Nq = Nq;
+  p.Nk = Nk;
+  p.n_qtiles = n_qtiles;
+  p.n_ktiles = n_ktiles;
+  set_tc_scale(scale, &p);
+  const unsigned long long lim = g_wait_limit_ns.load();
+  p.wait_limit_ns = lim ? lim : fa::kDefaultWaitLimitNs;
+  p.skip_v_load = g_skip_v_load.load();
+  p.n_splits = nsp;
+  p.ws_o = ws_o;
+  p.ws_lse = ws_lse;
+  cudaError_t e;
+  if (dtype == FA_DTYPE_F16)
+    e = (d == 64) ? fa::launch_tc_f16_d64(mq, mk, mv, mo, p, B, causal, s)
+                  : fa::launch_tc_f16_d128(mq, mk, mv, mo, p, B, causal, s);
+  else if (dtype == FA_DTYPE_BF16)
+    e = (d == 64) ? fa::launch_tc_bf16_d64(mq, mk, mv, mo, p, B, causal, s)
+                  : fa::launch_tc_bf16_d128(mq, mk, mv, mo, p, B, causal, s);
+  else
+    e = fa::launch_tc_f32_d64(mq, mk, mv, mo, p, B, causal, s);
+  if (e != cudaSuccess) return FA_ERR_CUDA;
+  e = fa::launch_splitkv_combine(ws_o, ws_lse, o, lse, BH, Nq, d, n_ktiles, nsp, causal, dtype, s);
+  return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}

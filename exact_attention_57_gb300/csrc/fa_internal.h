@@ -31,6 +31,12 @@ struct TcParams {
   int scale_neg;                  // scale < 0: S is computed as (-Q) K^T
   unsigned long long wait_limit_ns;
   int skip_v_load;                // test hook
+  // Split over the key range (1 = off): CTA x covers query tile x / n_splits
+  // and chunk x % n_splits of that tile's key tiles, writing O/l (fp32) and
+  // LSE of its chunk to ws_o [n_splits][B*H][Nq][d] and ws_lse [n_splits][B*H][Nq].
+  int n_splits = 1;
+  float *ws_o = nullptr;
+  float *ws_lse = nullptr;
 };
 
 struct SimtParams {
@@ -61,6 +67,11 @@ cudaError_t launch_tc_f16_d64(const CUtensorMap &q, const CUtensorMap &k, const 
 cudaError_t launch_tc_f16_d128(const CUtensorMap &q, const CUtensorMap &k, const CUtensorMap &v,
                                const CUtensorMap &o, const TcParams &p, int B, int causal,
                                cudaStream_t s);
+
+// Merge of the split-mode chunks into o (dtype: bf16, f16 or f32) and lse.
+cudaError_t launch_splitkv_combine(const float *ws_o, const float *ws_lse, void *o, float *lse,
+                                   int BH, int Nq, int d, int n_ktiles, int nsp, int causal,
+                                   int dtype, cudaStream_t s);
 
 cudaError_t launch_simt(const SimtParams &p, int B, cudaStream_t s);
 

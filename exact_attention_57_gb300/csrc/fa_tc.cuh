@@ -173,12 +173,18 @@ __global__ void __launch_bounds__(224, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   // Causal: heaviest query tiles first (blockIdx.x = 0 gets the last tile).
-  const int qt = CAUSAL ? (p.n_qtiles - 1 - static_cast<int>(blockIdx.x))
-                        : static_cast<int>(blockIdx.x);
+  const int nsp = p.n_splits;
+  const int qidx = nsp > 1 ? static_cast<int>(blockIdx.x) / nsp : static_cast<int>(blockIdx.x);
+  const int split = static_cast<int>(blockIdx.x) - qidx * nsp;
+  const int qt = CAUSAL ? (p.n_qtiles - 1 - qidx) : qidx;
   const int bh = static_cast<int>(blockIdx.z) * p.H + static_cast<int>(blockIdx.y);
   const int q0 = qt * BM;
   // Key tiles this query tile needs (top-left causal: keys <= last row).
-  const int n_kt = CAUSAL ? min(qt + 1, p.n_ktiles) : p.n_ktiles;
+  const int n_all = CAUSAL ? min(qt + 1, p.n_ktiles) : p.n_ktiles;
+  // This CTA's key tiles: [kt0, kt0 + n_kt), chunk `split` of n_all.
+  const int kt0 = static_cast<int>(static_cast<long long>(split) * n_all / nsp);
+  const int n_kt = static_cast<int>(static_cast<long long>(split + 1) * n_all / nsp) - kt0;
+  if (n_kt == 0) return;  // empty chunk (split mode only); the combine step skips it
 
   if (threadIdx.x == 0) {
     // Q: written to TMEM by the 128 softmax threads, or one TMA transaction
@@ -252,7 +258,7 @@ __global__ void __launch_bounds__(224, 1)
 #pragma unroll
           for (int c = 0; c < C::NCH; ++c)
             tma_load_3d(sK + s * C::TILE_BYTES + c * C::CHUNK_BYTES, &tm_k, bKfull + 8 * s,
-                        c * C::CH_ELEMS, jk * BN, bh, pol_kv);
+                        c * C::CH_ELEMS, (kt0 + jk) * BN, bh, pol_kv);
           ++nk;
         }
         if (j >= 0) {
@@ -267,7 +273,7 @@ __global__ void __launch_bounds__(224, 1)
 #pragma unroll
           for (int c = 0; c < C::NCH; ++c)
             tma_load_3d(sV + s * C::TILE_BYTES + c * C::CHUNK_BYTES, &tm_v, bVfull + 8 * s,
-                        c * C::CH_ELEMS, j * BN, bh, pol_kv);
+                        c * C::CH_ELEMS, (kt0 + j) * BN, bh, pol_kv);
           ++nv;
         }
       }
@@ -496,7 +502,7 @@ __global__ void __launch_bounds__(224, 1)
       reg_fence32(sr[3]);
       auto S = [&](int c) -> float { return __uint_as_float(sr[c >> 5][c & 31]); };
 
-      const int lim = row_lim - j * BN;  // valid columns c < lim
+      const int lim = row_lim - (kt0 + j) * BN;  // valid columns c < lim
       // Masked tiles (causal diagonal, ragged key tail; at most two per CTA)
       // set the excluded scores to -inf, so one code path serves every tile:
       // they drop out of the max, and exp2(-inf) = 0 (the scale is > 0 here).
@@ -613,7 +619,32 @@ __global__ void __launch_bounds__(224, 1)
     // The last P V; its commit also covers every earlier UMMA.
     if (ok)
       ok = __all_sync(kFull, bounded_wait(bOdone + 8 * pbuf, pbph, w));
-    if (ok) {
+    if (nsp > 1) {
+      // Split mode: this chunk's O / l (fp32) and LSE go to the workspace with
+      // plain vector stores; the combine kernel merges the chunks.
+      if (ok) {
+        tc_fence_after();
+        const float inv_l = 1.f / l;
+        const size_t prow = (static_cast<size_t>(split) * gridDim.z * p.H + bh) * p.Nq + row;
+#pragma unroll
+        for (int c = 0; c < D; c += 32) {
+          uint32_t o[32];
+          tmem_ld32(o_tm + c, o);
+          tmem_ld_wait();
+          reg_fence32(o);
+          if (row < p.Nq) {
+            float4 *dst = reinterpret_cast<float4 *>(p.ws_o + prow * D + c);
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+              dst[u] = make_float4(__uint_as_float(o[4 * u + 0]) * inv_l,
+                                   __uint_as_float(o[4 * u + 1]) * inv_l,
+                                   __uint_as_float(o[4 * u + 2]) * inv_l,
+                                   __uint_as_float(o[4 * u + 3]) * inv_l);
+          }
+        }
+        if (row < p.Nq) p.ws_lse[prow] = m_used * kLn2 + logf(l);
+      }
+    } else if (ok) {
       tc_fence_after();
       const float inv_l = 1.f / l;
       // Staging in K stage 0: every S_j is complete, so no UMMA reads K any
@@ -665,7 +696,7 @@ __global__ void __launch_bounds__(224, 1)
     }
     fence_proxy_async_smem();
     named_bar_sync(1, 128);
-    if (threadIdx.x == 0 && *abort_flag == 0) {
+    if (nsp == 1 && threadIdx.x == 0 && *abort_flag == 0) {
 #pragma unroll
       for (int c = 0; c < C::NCH; ++c)
         tma_store_3d(&tm_o, sK + c * C::CHUNK_BYTES, c * C::CH_ELEMS, q0, bh);
@@ -695,7 +726,7 @@ cudaError_t launch_tc(const CUtensorMap &q, const CUtensorMap &k, const CUtensor
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(p.n_qtiles), static_cast<unsigned>(p.H),
+  cfg.gridDim = dim3(static_cast<unsigned>(p.n_qtiles * p.n_splits), static_cast<unsigned>(p.H),
                      static_cast<unsigned>(B));
   cfg.blockDim = dim3(C::THREADS, 1, 1);
   cfg.dynamicSmemBytes = C::SMEM_BYTES;

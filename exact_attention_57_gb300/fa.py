@@ -30,7 +30,7 @@ FA_DTYPE_F32_SIMT = 2
 FA_DTYPE_F16 = 3
 
 EXPORTED = ("fa_fwd", "fa_fwd_host", "fa_fwd_status", "fa_status_string", "fa_version",
-            "fa_set_test_hooks", "fa_fwd_noalloc")
+            "fa_set_test_hooks", "fa_fwd_noalloc", "fa_fwd_splitkv", "fa_fwd_splitkv_workspace")
 
 _lib = None
 
@@ -56,6 +56,11 @@ def load(path: str | None = None):
     lib.fa_fwd_noalloc.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, i, vp,
                                    ctypes.POINTER(i)]
     lib.fa_fwd_noalloc.restype = i
+    lib.fa_fwd_splitkv.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, i, i, vp,
+                                   ctypes.c_ulonglong, vp]
+    lib.fa_fwd_splitkv.restype = i
+    lib.fa_fwd_splitkv_workspace.argtypes = [i, i, i, i, i]
+    lib.fa_fwd_splitkv_workspace.restype = ctypes.c_ulonglong
     lib.fa_fwd_host.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp,
                                 i, i, i, i, i, f, i, i, vp]
     lib.fa_fwd_host.restype = i
@@ -89,6 +94,17 @@ def fa_fwd_noalloc(q, k, v, o, lse, B, H, Nq, Nk, d, scale, causal, dtype, strea
     st = load().fa_fwd_noalloc(q, k, v, o, lse, B, H, Nq, Nk, d, float(scale), int(causal),
                                int(dtype), stream, ctypes.byref(word) if wait else None)
     return st, (word.value if wait else None)
+
+
+def fa_fwd_splitkv(q, k, v, o, lse, B, H, Nq, Nk, d, scale, causal, dtype, num_splits,
+                   workspace, workspace_bytes, stream) -> int:
+    return load().fa_fwd_splitkv(q, k, v, o, lse, B, H, Nq, Nk, d, float(scale), int(causal),
+                                 int(dtype), int(num_splits), workspace, int(workspace_bytes),
+                                 stream)
+
+
+def fa_fwd_splitkv_workspace(B, H, Nq, d, num_splits) -> int:
+    return load().fa_fwd_splitkv_workspace(B, H, Nq, d, num_splits)
 
 
 def fa_fwd_host(q_h, k_h, v_h, o_h, lse_h, q_d, k_d, v_d, o_d, lse_d,
@@ -136,11 +152,14 @@ def _dtype_code(t, impl: str) -> int:
 
 
 def attention(q, k, v, scale: float | None = None, causal: bool = False, impl: str = "tc",
-              out=None, lse=None, stream=None):
+              out=None, lse=None, stream=None, num_splits: int | None = None):
     """O, LSE for contiguous CUDA tensors q [B,H,Nq,d], k/v [B,H,Nk,d].
 
     impl "tc": bf16 / fp16 -> tcgen05 kind::f16, fp32 -> tcgen05 kind::tf32;
-    impl "simt": fp32 only, plain fp32 kernel.  Raises FaError on failure.
+    impl "simt": fp32 only, plain fp32 kernel.  num_splits (tensor-core
+    dtypes): split each query tile's key range into that many chunks (0 =
+    automatic) through fa_fwd_splitkv, with a torch-allocated workspace.
+    Raises FaError on failure.
     """
     import torch
     if not (q.is_cuda and k.is_cuda and v.is_cuda):
@@ -165,8 +184,18 @@ def attention(q, k, v, scale: float | None = None, causal: bool = False, impl: s
     if stream is None:
         stream = torch.cuda.current_stream(q.device).cuda_stream
     with torch.cuda.device(q.device):
-        st = fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
-                    B, H, Nq, Nk, d, scale, int(bool(causal)), code, stream)
+        if num_splits is None:
+            st = fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                        lse.data_ptr(), B, H, Nq, Nk, d, scale, int(bool(causal)), code, stream)
+            where = "fa_fwd"
+        else:
+            nws = num_splits if num_splits > 0 else 64
+            ws_bytes = fa_fwd_splitkv_workspace(B, H, Nq, d, nws)
+            ws = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=q.device)
+            st = fa_fwd_splitkv(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                                lse.data_ptr(), B, H, Nq, Nk, d, scale, int(bool(causal)), code,
+                                num_splits, ws.data_ptr(), ws_bytes, stream)
+            where = "fa_fwd_splitkv"
     if st != FA_OK:
-        raise FaError(st, "fa_fwd")
+        raise FaError(st, where)
     return out, lse

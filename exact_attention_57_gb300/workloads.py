@@ -87,6 +87,11 @@ PROFILE_WORKLOADS = {
     "b2h16n8192d128-bf16-causal": Workload(
         "b2h16n8192d128-bf16-causal", 2, 16, 8192, 8192, 128, DTYPE_BF16,
         causal=(True,), seed=57005, note="profiling case, 1/8 of the benchmark's heads"),
+    # Short queries against long keys: 8 query tiles in all, far fewer CTAs
+    # than SMs unless the key range is split.
+    "b1h8nq128nk65536d128-bf16": Workload(
+        "b1h8nq128nk65536d128-bf16", 1, 8, 128, 65536, 128, DTYPE_BF16,
+        causal=(False,), seed=57006, note="decode-like: one query tile per head"),
 }
 
 

@@ -136,6 +136,41 @@ int fa_fwd_noalloc(const void *q, const void *k, const void *v, void *o, float *
                    int dtype, void *stream, int *device_status);
 
 /*
+ * fa_fwd_splitkv — fa_fwd with the key range of every query tile split into
+ * chunks that run as separate CTAs, then merged.  For grids too small to fill
+ * the GPU (few heads and few query tiles, e.g. short queries against long
+ * keys): one CTA per (batch, head, query tile) leaves most SMs idle, which the
+ * per-head parallelism of "parallel execution of read/write operations (paper
+ * vs implementation)" already needs B*H of about 80 to avoid.  Each chunk
+ * keeps its own running max and sum; the merge is the same online-softmax
+ * update applied across chunks: LSE = log sum_s e^{LSE_s},
+ * O = sum_s e^{LSE_s - LSE} O_s.
+ *
+ * Arguments q .. dtype and stream as for fa_fwd (tensor-core dtypes only;
+ * FA_DTYPE_F32_SIMT is FA_ERR_UNSUPPORTED).
+ * num_splits       chunks per query tile, 1 .. 64, or 0 to choose one that
+ *                  gives about two CTAs per SM (limited to what the workspace
+ *                  holds).  1 (or a choice of 1) runs fa_fwd itself.
+ * workspace        caller-owned device memory, 256-byte aligned, of at least
+ *                  fa_fwd_splitkv_workspace(B, H, Nq, d, num_splits) bytes;
+ *                  it must not overlap q, k, v, o or lse.  It holds fp32
+ *                  partial outputs between the two kernels of one call; calls
+ *                  that share a workspace must not overlap on the GPU.
+ * workspace_bytes  its size.
+ * Returns FA_ERR_INVALID_ARG for a missing, misaligned or too small workspace
+ * (when num_splits > 1), before anything is enqueued.
+ */
+int fa_fwd_splitkv(const void *q, const void *k, const void *v, void *o, float *lse,
+                   int B, int H, int Nq, int Nk, int d, float scale, int causal,
+                   int dtype, int num_splits, void *workspace,
+                   unsigned long long workspace_bytes, void *stream);
+
+/* Bytes of workspace fa_fwd_splitkv needs for num_splits chunks (1 .. 64):
+ * num_splits * B * H * Nq * (d + 1) floats, each part rounded up to 256
+ * bytes.  0 for invalid arguments. */
+unsigned long long fa_fwd_splitkv_workspace(int B, int H, int Nq, int d, int num_splits);
+
+/*
  * fa_fwd_host — the same forward on HOST buffers.
  *
  * q_h, k_h, v_h   host inputs (pinned memory gives full copy speed).

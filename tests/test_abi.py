@@ -13,7 +13,8 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 def header_functions():
     txt = open(os.path.join(ROOT, "include", "fa.h")).read()
     txt = re.sub(r"/\*.*?\*/", "", txt, flags=re.S)
-    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(fa_\w+)\s*\(", txt, flags=re.M)))
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?(?:\w+\s+)*\w+\s*\*?\s*(fa_\w+)\s*\(", txt,
+                                 flags=re.M)))
 
 
 @pytest.fixture(scope="module")
@@ -88,3 +89,38 @@ def test_host_variant_rejects_null_host_buffers(lib):
 def test_binding_fails_loudly_without_library(tmp_path):
     with pytest.raises(RuntimeError):
         fa.load(str(tmp_path / "missing.so"))
+
+
+def test_splitkv_workspace_size(lib):
+    """num_splits * B * H * Nq * (d + 1) floats, each part rounded up to 256 B."""
+    def want(B, H, Nq, d, s):
+        r = s * B * H * Nq
+        up = lambda n: (n + 255) // 256 * 256
+        return up(r * d * 4) + up(r * 4)
+    for args in [(1, 1, 1, 64, 1), (2, 8, 3001, 128, 7), (1, 32, 128, 64, 64)]:
+        assert fa.fa_fwd_splitkv_workspace(*args) == want(*args)
+    for bad in [(0, 1, 1, 64, 2), (1, 1, 1, 64, 0), (1, 1, 1, 64, 65), (1, 1, 0, 64, 2)]:
+        assert fa.fa_fwd_splitkv_workspace(*bad) == 0
+
+
+@pytest.mark.parametrize("kw", [
+    dict(num_splits=-1), dict(num_splits=65),
+    dict(num_splits=4, ws=None), dict(num_splits=4, ws=0x600010),
+    dict(num_splits=4, ws_bytes=100), dict(num_splits=4, ws=Q),
+], ids=lambda kw: ",".join(f"{k}={v}" for k, v in kw.items()))
+def test_splitkv_invalid_arguments(lib, kw):
+    """Bad split counts and missing, misaligned, short or overlapping
+    workspaces are refused before any device work."""
+    ns = kw.get("num_splits", 4)
+    need = fa.fa_fwd_splitkv_workspace(1, 1, 16, 64, max(1, min(ns, 64)))
+    ws = kw.get("ws", 0x600000)
+    wsb = kw.get("ws_bytes", need)
+    r = fa.fa_fwd_splitkv(Q, K, V, O, L, 1, 1, 16, 16, 64, 0.125, 0, fa.FA_DTYPE_BF16, ns,
+                          ws, wsb, None)
+    assert r == fa.FA_ERR_INVALID_ARG
+
+
+def test_splitkv_refuses_simt(lib):
+    r = fa.fa_fwd_splitkv(Q, K, V, O, L, 1, 1, 16, 16, 64, 0.125, 0, fa.FA_DTYPE_F32_SIMT, 4,
+                          0x600000, 1 << 20, None)
+    assert r == fa.FA_ERR_UNSUPPORTED
