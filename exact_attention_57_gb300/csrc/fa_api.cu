@@ -181,6 +181,10 @@ int fa_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int
 
   fa::TcParams p;
   p.q = q;
+  p.o = o;
+  p.q_head_stride = static_cast<long long>(Nq) * d;
+  p.q_row_stride = d;
+  p.lse_head_stride = Nq;
   p.lse = lse;
   p.status = status;
   p.H = H;
@@ -362,6 +366,14 @@ extern "C" int fa_fwd_noalloc(const void *q, const void *k, const void *v, void 
     if ((rc = encode_map(&mo, o, dtype, BH, Nq, d)) != FA_OK) return rc;
     fa::TcParams p;
     p.q = q;
+    p.o = o;
+    p.q_head_stride = static_cast<long long>(Nq) * d;
+    p.q_row_stride = d;
+    p.lse_head_stride = Nq;
+  p.o = o;
+  p.q_head_stride = static_cast<long long>(Nq) * d;
+  p.q_row_stride = d;
+  p.lse_head_stride = Nq;
     p.lse = lse;
     p.status = status;
     p.H = H;
@@ -446,11 +458,13 @@ extern "C" int fa_fwd_splitkv(const void *q, const void *k, const void *v, void 
   }
   int nsp = num_splits;
   if (nsp == 0) {
-    // About two CTAs' worth of work per SM, at least one key tile per chunk.
+    // One wave: about one CTA per SM (a CTA holds a whole SM's tensor
+    // memory, so a second wave would run after the first), at least one key
+    // tile per chunk.
     const int sms = sm_count();
     if (sms == 0) return FA_ERR_CUDA;
     const long long ctas = static_cast<long long>(n_qtiles) * B * H;
-    nsp = static_cast<int>((2LL * sms + ctas - 1) / ctas);
+    nsp = static_cast<int>(sms / ctas);
     nsp = nsp < 1 ? 1 : (nsp > n_ktiles ? n_ktiles : nsp);
     if (nsp > kMaxSplits) nsp = kMaxSplits;
     while (nsp > 1 && (workspace == nullptr ||
@@ -483,6 +497,10 @@ extern "C" int fa_fwd_splitkv(const void *q, const void *k, const void *v, void 
   if ((rc = encode_map(&mo, o, dtype, BH, Nq, d)) != FA_OK) return rc;
   fa::TcParams p;
   p.q = q;
+  p.o = o;
+  p.q_head_stride = static_cast<long long>(Nq) * d;
+  p.q_row_stride = d;
+  p.lse_head_stride = Nq;
   p.lse = lse;
   p.status = status;
   p.H = H;
@@ -508,5 +526,85 @@ extern "C" int fa_fwd_splitkv(const void *q, const void *k, const void *v, void 
     e = fa::launch_tc_f32_d64(mq, mk, mv, mo, p, B, causal, s);
   if (e != cudaSuccess) return FA_ERR_CUDA;
   e = fa::launch_splitkv_combine(ws_o, ws_lse, o, lse, BH, Nq, d, n_ktiles, nsp, causal, dtype, s);
+  return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+// ---------------------------------------------------------------------------
+// Variable-length batches.
+// ---------------------------------------------------------------------------
+namespace {
+
+// 3-D view {d, total rows, H} of a token-major [total, H, d] tensor: rows of
+// one head are H*d elements apart, heads d apart.  Boxes as encode_map.
+int encode_map_tokens(CUtensorMap *map, const void *base, int dtype, int total, int H, int d) {
+  const CUtensorMapDataType dt = dtype == FA_DTYPE_BF16  ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                 : dtype == FA_DTYPE_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                                         : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+  const cuuint64_t es = elem_size(dtype);
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(total),
+                        static_cast<cuuint64_t>(H)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(H) * d * es, static_cast<cuuint64_t>(d) * es};
+  cuuint32_t box[3] = {static_cast<cuuint32_t>(128 / es), static_cast<cuuint32_t>(fa::BM), 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = g_encode(map, dt, 3, const_cast<void *>(base), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? FA_OK : FA_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" int fa_fwd_varlen(const void *q, const void *k, const void *v, void *o, float *lse,
+                             const int *cu_seqlens_q, const int *cu_seqlens_k, int B, int H,
+                             int total_q, int total_k, int max_seqlen_q, int d, float scale,
+                             int causal, int dtype, void *stream) {
+  if (!cu_seqlens_q || !cu_seqlens_k) return FA_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(cu_seqlens_q) % 4 || reinterpret_cast<uintptr_t>(cu_seqlens_k) % 4)
+    return FA_ERR_INVALID_ARG;
+  if (max_seqlen_q < 1 || max_seqlen_q > total_q) return FA_ERR_INVALID_ARG;
+  // The tensors as one [1, H, total, d]-sized problem for the shared checks
+  // (pointers, alignment, sizes, overlaps, supported dtype and d).
+  int rc = validate(q, k, v, o, lse, 1, H, total_q, total_k, d, scale, causal, dtype);
+  if (rc != FA_OK) return rc;
+  if (B < 1 || B > 65535) return FA_ERR_INVALID_ARG;
+  if (dtype == FA_DTYPE_F32_SIMT) return FA_ERR_UNSUPPORTED;
+  unsigned *status = nullptr;
+  if ((rc = device_setup(&status)) != FA_OK) return rc;
+  if ((rc = get_encoder()) != FA_OK) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  CUtensorMap mq, mk, mv, mo;
+  if ((rc = encode_map_tokens(&mq, q, dtype, total_q, H, d)) != FA_OK) return rc;
+  if ((rc = encode_map_tokens(&mk, k, dtype, total_k, H, d)) != FA_OK) return rc;
+  if ((rc = encode_map_tokens(&mv, v, dtype, total_k, H, d)) != FA_OK) return rc;
+  if ((rc = encode_map_tokens(&mo, o, dtype, total_q, H, d)) != FA_OK) return rc;
+  fa::TcParams p;
+  p.q = q;
+  p.o = o;
+  p.lse = lse;
+  p.status = status;
+  p.H = H;
+  p.Nq = max_seqlen_q;
+  p.Nk = total_k;
+  p.n_qtiles = ceil_div(max_seqlen_q, fa::BM);  // grid: the longest sequence
+  p.n_ktiles = ceil_div(total_k, fa::BN);
+  set_tc_scale(scale, &p);
+  const unsigned long long lim = g_wait_limit_ns.load();
+  p.wait_limit_ns = lim ? lim : fa::kDefaultWaitLimitNs;
+  p.skip_v_load = g_skip_v_load.load();
+  p.q_head_stride = d;
+  p.q_row_stride = static_cast<long long>(H) * d;
+  p.lse_head_stride = total_q;
+  p.cu_q = cu_seqlens_q;
+  p.cu_k = cu_seqlens_k;
+  p.total_q = total_q;
+  cudaError_t e;
+  if (dtype == FA_DTYPE_F16)
+    e = (d == 64) ? fa::launch_tc_f16_d64(mq, mk, mv, mo, p, B, causal, s)
+                  : fa::launch_tc_f16_d128(mq, mk, mv, mo, p, B, causal, s);
+  else if (dtype == FA_DTYPE_BF16)
+    e = (d == 64) ? fa::launch_tc_bf16_d64(mq, mk, mv, mo, p, B, causal, s)
+                  : fa::launch_tc_bf16_d128(mq, mk, mv, mo, p, B, causal, s);
+  else
+    e = fa::launch_tc_f32_d64(mq, mk, mv, mo, p, B, causal, s);
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }

@@ -23,6 +23,7 @@ constexpr unsigned long long kDefaultWaitLimitNs = 2000000000ull;  // 2 s
 
 struct TcParams {
   const void *q;                  // [B*H*Nq*d], read row by row when Q goes to TMEM
+  void *o;                        // output, written row by row for variable lengths
   float *lse;                     // [B*H*Nq]
   unsigned *status;               // per-device status word
   int H, Nq, Nk;
@@ -37,6 +38,16 @@ struct TcParams {
   int n_splits = 1;
   float *ws_o = nullptr;
   float *ws_lse = nullptr;
+  // Element strides of Q and O (and of LSE) for the head coordinate and the
+  // row: [B,H,N,d] uses (Nq*d, d) and Nq with the head coordinate b*H+h; the
+  // variable-length layout [total, H, d] uses (d, H*d) and total_q with h.
+  long long q_head_stride = 0, q_row_stride = 0, lse_head_stride = 0;
+  // Variable-length batches: device cu_seqlens (B+1 entries each), or null.
+  // Sequence b covers rows [cu_q[b], cu_q[b+1]) of Q/O and [cu_k[b], cu_k[b+1])
+  // of K/V; total_q bounds every row index (defends against bad offsets).
+  const int *cu_q = nullptr;
+  const int *cu_k = nullptr;
+  int total_q = 0;
 };
 
 struct SimtParams {

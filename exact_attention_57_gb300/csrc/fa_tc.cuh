@@ -176,11 +176,41 @@ __global__ void __launch_bounds__(224, 1)
   const int nsp = p.n_splits;
   const int qidx = nsp > 1 ? static_cast<int>(blockIdx.x) / nsp : static_cast<int>(blockIdx.x);
   const int split = static_cast<int>(blockIdx.x) - qidx * nsp;
-  const int qt = CAUSAL ? (p.n_qtiles - 1 - qidx) : qidx;
   const int bh = static_cast<int>(blockIdx.z) * p.H + static_cast<int>(blockIdx.y);
+  // This CTA's sequence: rows [q_row0, q_row0 + Nq) of Q/O and [k_row0,
+  // k_row0 + Nk) of K/V in head plane hc of the tensor maps.
+  int Nq = p.Nq, Nk = p.Nk, q_row0 = 0, k_row0 = 0, hc = bh;
+  int n_qtiles = p.n_qtiles, n_ktiles = p.n_ktiles;
+  if (p.cu_q != nullptr) {
+    const int b = static_cast<int>(blockIdx.z);
+    q_row0 = p.cu_q[b];
+    k_row0 = p.cu_k[b];
+    Nq = max(0, min(p.cu_q[b + 1], p.total_q) - q_row0);
+    Nk = max(0, p.cu_k[b + 1] - k_row0);
+    hc = static_cast<int>(blockIdx.y);
+    n_qtiles = (Nq + BM - 1) / BM;
+    n_ktiles = (Nk + BN - 1) / BN;
+    if (qidx >= n_qtiles) return;  // the grid covers the longest sequence
+  }
+  const int qt = CAUSAL ? (n_qtiles - 1 - qidx) : qidx;
   const int q0 = qt * BM;
+  if (Nk == 0) {
+    // A sequence without keys: the softmax over an empty set gives O = 0 and
+    // LSE = log 0 = -inf (variable-length batches only).
+    if (threadIdx.x < BM) {
+      const int row = q0 + static_cast<int>(threadIdx.x);
+      if (row < Nq) {
+        const long long gr = q_row0 + row;
+        uint8_t *orow = static_cast<uint8_t *>(p.o) +
+                        (hc * p.q_head_stride + gr * p.q_row_stride) * C::ESZ;
+        for (int x = 0; x < D * C::ESZ; x += 16) *reinterpret_cast<uint4 *>(orow + x) = make_uint4(0, 0, 0, 0);
+        p.lse[hc * p.lse_head_stride + gr] = -INFINITY;
+      }
+    }
+    return;
+  }
   // Key tiles this query tile needs (top-left causal: keys <= last row).
-  const int n_all = CAUSAL ? min(qt + 1, p.n_ktiles) : p.n_ktiles;
+  const int n_all = CAUSAL ? min(qt + 1, n_ktiles) : n_ktiles;
   // This CTA's key tiles: [kt0, kt0 + n_kt), chunk `split` of n_all.
   const int kt0 = static_cast<int>(static_cast<long long>(split) * n_all / nsp);
   const int n_kt = static_cast<int>(static_cast<long long>(split + 1) * n_all / nsp) - kt0;
@@ -239,7 +269,7 @@ __global__ void __launch_bounds__(224, 1)
         mbar_arrive_expect_tx(bQ, C::TILE_BYTES);
 #pragma unroll
         for (int c = 0; c < C::NCH; ++c)
-          tma_load_3d(sQ + c * C::CHUNK_BYTES, &tm_q, bQ, c * C::CH_ELEMS, q0, bh,
+          tma_load_3d(sQ + c * C::CHUNK_BYTES, &tm_q, bQ, c * C::CH_ELEMS, q_row0 + q0, hc,
                       l2_policy_evict_first());
       }
       int nk = 0, nv = 0;  // loads issued
@@ -258,7 +288,7 @@ __global__ void __launch_bounds__(224, 1)
 #pragma unroll
           for (int c = 0; c < C::NCH; ++c)
             tma_load_3d(sK + s * C::TILE_BYTES + c * C::CHUNK_BYTES, &tm_k, bKfull + 8 * s,
-                        c * C::CH_ELEMS, (kt0 + jk) * BN, bh, pol_kv);
+                        c * C::CH_ELEMS, k_row0 + (kt0 + jk) * BN, hc, pol_kv);
           ++nk;
         }
         if (j >= 0) {
@@ -273,7 +303,7 @@ __global__ void __launch_bounds__(224, 1)
 #pragma unroll
           for (int c = 0; c < C::NCH; ++c)
             tma_load_3d(sV + s * C::TILE_BYTES + c * C::CHUNK_BYTES, &tm_v, bVfull + 8 * s,
-                        c * C::CH_ELEMS, (kt0 + j) * BN, bh, pol_kv);
+                        c * C::CH_ELEMS, k_row0 + (kt0 + j) * BN, hc, pol_kv);
           ++nv;
         }
       }
@@ -386,7 +416,7 @@ __global__ void __launch_bounds__(224, 1)
     const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
     const uint32_t o_tm = tmem + lane_off + C::COL_O;
     const float sl2 = p.scale_log2;
-    const int row_lim = CAUSAL ? min(row + 1, p.Nk) : p.Nk;  // keys [0, row_lim)
+    const int row_lim = CAUSAL ? min(row + 1, Nk) : Nk;  // keys [0, row_lim)
     float m_used = -INFINITY;  // exponent offset, log2 units of the scaled score
     float l = 0.f;
     bool ok = true;
@@ -451,10 +481,10 @@ __global__ void __launch_bounds__(224, 1)
     // holds bf16 elements 2c, 2c+1, or one tf32 element).  Rows past Nq are 0.
     // (Otherwise the producer loads Q into shared memory with TMA.)
     if constexpr (C::QTMEM) {
+      const bool in = row < Nq;
       const uint4 *src = reinterpret_cast<const uint4 *>(
           static_cast<const uint8_t *>(p.q) +
-          (static_cast<size_t>(bh) * p.Nq + (row < p.Nq ? row : 0)) * (D * C::ESZ));
-      const bool in = row < p.Nq;
+          (hc * p.q_head_stride + (q_row0 + (in ? row : 0)) * p.q_row_stride) * C::ESZ);
 #pragma unroll
       for (int blk = 0; blk < C::Q_COLS / 32; ++blk) {
         uint32_t wq[32];
@@ -632,7 +662,7 @@ __global__ void __launch_bounds__(224, 1)
           tmem_ld32(o_tm + c, o);
           tmem_ld_wait();
           reg_fence32(o);
-          if (row < p.Nq) {
+          if (row < Nq) {
             float4 *dst = reinterpret_cast<float4 *>(p.ws_o + prow * D + c);
 #pragma unroll
             for (int u = 0; u < 8; ++u)
@@ -642,7 +672,49 @@ __global__ void __launch_bounds__(224, 1)
                                    __uint_as_float(o[4 * u + 3]) * inv_l);
           }
         }
-        if (row < p.Nq) p.ws_lse[prow] = m_used * kLn2 + logf(l);
+        if (row < Nq) p.ws_lse[prow] = m_used * kLn2 + logf(l);
+      }
+    } else if (p.cu_q != nullptr) {
+      // Variable-length batches: the rows after this sequence belong to the
+      // next one, so O is written row by row from registers (no TMA store).
+      if (ok) {
+        tc_fence_after();
+        const float inv_l = 1.f / l;
+        const long long gr = q_row0 + row;
+        uint8_t *orow = static_cast<uint8_t *>(p.o) +
+                        (hc * p.q_head_stride + gr * p.q_row_stride) * C::ESZ;
+#pragma unroll
+        for (int c = 0; c < D; c += 32) {
+          uint32_t o[32];
+          tmem_ld32(o_tm + c, o);
+          tmem_ld_wait();
+          reg_fence32(o);
+          if (row < Nq) {
+            if constexpr (TF32) {
+#pragma unroll
+              for (int u = 0; u < 8; ++u)
+                reinterpret_cast<float4 *>(orow + c * 4)[u] =
+                    make_float4(__uint_as_float(o[4 * u + 0]) * inv_l,
+                                __uint_as_float(o[4 * u + 1]) * inv_l,
+                                __uint_as_float(o[4 * u + 2]) * inv_l,
+                                __uint_as_float(o[4 * u + 3]) * inv_l);
+            } else {
+              auto pack16 = [](float lo, float hi) {
+                return HALF ? pack_f16x2(lo, hi) : pack_bf16x2(lo, hi);
+              };
+#pragma unroll
+              for (int u = 0; u < 4; ++u) {
+                uint4 val;
+                val.x = pack16(__uint_as_float(o[8 * u + 0]) * inv_l, __uint_as_float(o[8 * u + 1]) * inv_l);
+                val.y = pack16(__uint_as_float(o[8 * u + 2]) * inv_l, __uint_as_float(o[8 * u + 3]) * inv_l);
+                val.z = pack16(__uint_as_float(o[8 * u + 4]) * inv_l, __uint_as_float(o[8 * u + 5]) * inv_l);
+                val.w = pack16(__uint_as_float(o[8 * u + 6]) * inv_l, __uint_as_float(o[8 * u + 7]) * inv_l);
+                reinterpret_cast<uint4 *>(orow + c * 2)[u] = val;
+              }
+            }
+          }
+        }
+        if (row < Nq) p.lse[hc * p.lse_head_stride + gr] = m_used * kLn2 + logf(l);
       }
     } else if (ok) {
       tc_fence_after();
@@ -692,11 +764,11 @@ __global__ void __launch_bounds__(224, 1)
           }
         }
       }
-      if (row < p.Nq) p.lse[static_cast<size_t>(bh) * p.Nq + row] = m_used * kLn2 + logf(l);
+      if (row < Nq) p.lse[static_cast<size_t>(bh) * Nq + row] = m_used * kLn2 + logf(l);
     }
     fence_proxy_async_smem();
     named_bar_sync(1, 128);
-    if (nsp == 1 && threadIdx.x == 0 && *abort_flag == 0) {
+    if (nsp == 1 && p.cu_q == nullptr && threadIdx.x == 0 && *abort_flag == 0) {
 #pragma unroll
       for (int c = 0; c < C::NCH; ++c)
         tma_store_3d(&tm_o, sK + c * C::CHUNK_BYTES, c * C::CH_ELEMS, q0, bh);

@@ -30,7 +30,8 @@ FA_DTYPE_F32_SIMT = 2
 FA_DTYPE_F16 = 3
 
 EXPORTED = ("fa_fwd", "fa_fwd_host", "fa_fwd_status", "fa_status_string", "fa_version",
-            "fa_set_test_hooks", "fa_fwd_noalloc", "fa_fwd_splitkv", "fa_fwd_splitkv_workspace")
+            "fa_set_test_hooks", "fa_fwd_noalloc", "fa_fwd_splitkv", "fa_fwd_splitkv_workspace",
+            "fa_fwd_varlen")
 
 _lib = None
 
@@ -61,6 +62,8 @@ def load(path: str | None = None):
     lib.fa_fwd_splitkv.restype = i
     lib.fa_fwd_splitkv_workspace.argtypes = [i, i, i, i, i]
     lib.fa_fwd_splitkv_workspace.restype = ctypes.c_ulonglong
+    lib.fa_fwd_varlen.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i, i, vp]
+    lib.fa_fwd_varlen.restype = i
     lib.fa_fwd_host.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp,
                                 i, i, i, i, i, f, i, i, vp]
     lib.fa_fwd_host.restype = i
@@ -105,6 +108,48 @@ def fa_fwd_splitkv(q, k, v, o, lse, B, H, Nq, Nk, d, scale, causal, dtype, num_s
 
 def fa_fwd_splitkv_workspace(B, H, Nq, d, num_splits) -> int:
     return load().fa_fwd_splitkv_workspace(B, H, Nq, d, num_splits)
+
+
+def fa_fwd_varlen(q, k, v, o, lse, cu_seqlens_q, cu_seqlens_k, B, H, total_q, total_k,
+                  max_seqlen_q, d, scale, causal, dtype, stream) -> int:
+    return load().fa_fwd_varlen(q, k, v, o, lse, cu_seqlens_q, cu_seqlens_k, B, H, total_q,
+                                total_k, max_seqlen_q, d, float(scale), int(causal), int(dtype),
+                                stream)
+
+
+def attention_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int,
+                     scale: float | None = None, causal: bool = False, out=None, lse=None,
+                     stream=None):
+    """Packed sequences: q [total_q, H, d], k/v [total_k, H, d], cu_seqlens
+    int32 CUDA tensors of B+1 offsets.  Returns (o [total_q, H, d],
+    lse [H, total_q])."""
+    import torch
+    total_q, H, d = q.shape
+    total_k = k.shape[0]
+    if k.shape[1:] != (H, d) or v.shape != k.shape:
+        raise ValueError("q [total_q,H,d], k and v [total_k,H,d] expected")
+    if cu_seqlens_q.dtype != torch.int32 or cu_seqlens_k.dtype != torch.int32:
+        raise ValueError("cu_seqlens must be int32")
+    B = cu_seqlens_q.numel() - 1
+    if cu_seqlens_k.numel() != B + 1:
+        raise ValueError("cu_seqlens_q and cu_seqlens_k need the same batch size")
+    code = _dtype_code(q, "tc")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((H, total_q), device=q.device, dtype=torch.float32)
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device).cuda_stream
+    with torch.cuda.device(q.device):
+        st = fa_fwd_varlen(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                           lse.data_ptr(), cu_seqlens_q.data_ptr(), cu_seqlens_k.data_ptr(), B,
+                           H, total_q, total_k, max_seqlen_q, d, scale, int(bool(causal)), code,
+                           stream)
+    if st != FA_OK:
+        raise FaError(st, "fa_fwd_varlen")
+    return out, lse
 
 
 def fa_fwd_host(q_h, k_h, v_h, o_h, lse_h, q_d, k_d, v_d, o_d, lse_d,

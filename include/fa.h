@@ -148,9 +148,9 @@ int fa_fwd_noalloc(const void *q, const void *k, const void *v, void *o, float *
  *
  * Arguments q .. dtype and stream as for fa_fwd (tensor-core dtypes only;
  * FA_DTYPE_F32_SIMT is FA_ERR_UNSUPPORTED).
- * num_splits       chunks per query tile, 1 .. 64, or 0 to choose one that
- *                  gives about two CTAs per SM (limited to what the workspace
- *                  holds).  1 (or a choice of 1) runs fa_fwd itself.
+ * num_splits       chunks per query tile, 1 .. 64, or 0 to choose one wave of
+ *                  about one CTA per SM (limited to what the workspace holds).
+ *                  1 (or a choice of 1) runs fa_fwd itself.
  * workspace        caller-owned device memory, 256-byte aligned, of at least
  *                  fa_fwd_splitkv_workspace(B, H, Nq, d, num_splits) bytes;
  *                  it must not overlap q, k, v, o or lse.  It holds fp32
@@ -169,6 +169,31 @@ int fa_fwd_splitkv(const void *q, const void *k, const void *v, void *o, float *
  * num_splits * B * H * Nq * (d + 1) floats, each part rounded up to 256
  * bytes.  0 for invalid arguments. */
 unsigned long long fa_fwd_splitkv_workspace(int B, int H, int Nq, int d, int num_splits);
+
+/*
+ * fa_fwd_varlen — the forward over a batch of sequences of different lengths
+ * packed end to end, each attending only within itself (the "variable
+ * sequence length" case of "Meta's xFormers has Attention kernel written in
+ * CUTLASS").  Causal masking is top-left within each sequence.
+ *
+ * Layout (token-major, heads interleaved):
+ *   q, o [total_q, H, d]; k, v [total_k, H, d]; lse [H, total_q] (fp32).
+ * cu_seqlens_q, cu_seqlens_k  device int32 arrays of B+1 offsets: sequence b
+ *   holds rows [cu_seqlens_q[b], cu_seqlens_q[b+1]) of q/o and
+ *   [cu_seqlens_k[b], cu_seqlens_k[b+1]) of k/v; nondecreasing, starting at
+ *   0 and ending at total_q / total_k.  They are read on the device, so they
+ *   are not checked on the host: rows are never read or written past total_q
+ *   or total_k whatever they hold, but wrong offsets give wrong results.
+ * max_seqlen_q  the longest query length (sizes the grid; 1 .. total_q).
+ * A sequence with queries and no keys gets O = 0 and LSE = -inf.
+ * Other arguments as for fa_fwd (tensor-core dtypes only; the SIMT dtype is
+ * FA_ERR_UNSUPPORTED).  All pointers 16-byte aligned except lse and the
+ * offsets (4 bytes).
+ */
+int fa_fwd_varlen(const void *q, const void *k, const void *v, void *o, float *lse,
+                  const int *cu_seqlens_q, const int *cu_seqlens_k, int B, int H,
+                  int total_q, int total_k, int max_seqlen_q, int d, float scale,
+                  int causal, int dtype, void *stream);
 
 /*
  * fa_fwd_host — the same forward on HOST buffers.

@@ -124,3 +124,27 @@ def test_splitkv_refuses_simt(lib):
     r = fa.fa_fwd_splitkv(Q, K, V, O, L, 1, 1, 16, 16, 64, 0.125, 0, fa.FA_DTYPE_F32_SIMT, 4,
                           0x600000, 1 << 20, None)
     assert r == fa.FA_ERR_UNSUPPORTED
+
+
+CUQ, CUK = 0x700000, 0x700100
+
+
+@pytest.mark.parametrize("kw", [
+    dict(cu_q=None), dict(cu_k=None), dict(cu_q=CUQ + 2), dict(B=0), dict(max_q=0),
+    dict(max_q=17), dict(total_q=0), dict(d=0), dict(o=Q),
+], ids=lambda kw: ",".join(f"{k}={v}" for k, v in kw.items()))
+def test_varlen_invalid_arguments(lib, kw):
+    a = dict(cu_q=CUQ, cu_k=CUK, B=2, max_q=8, total_q=16, total_k=16, d=64, o=O)
+    a.update(kw)
+    r = fa.fa_fwd_varlen(Q, K, V, a["o"], L, a["cu_q"], a["cu_k"], a["B"], 2, a["total_q"],
+                         a["total_k"], a["max_q"], a["d"], 0.125, 1, fa.FA_DTYPE_BF16, None)
+    assert r == fa.FA_ERR_INVALID_ARG
+
+
+def test_varlen_refuses_simt_and_unsupported_dims(lib):
+    r = fa.fa_fwd_varlen(Q, K, V, O, L, CUQ, CUK, 2, 2, 16, 16, 8, 64, 0.125, 1,
+                         fa.FA_DTYPE_F32_SIMT, None)
+    assert r == fa.FA_ERR_UNSUPPORTED
+    r = fa.fa_fwd_varlen(Q, K, V, O, L, CUQ, CUK, 2, 2, 16, 16, 8, 96, 0.125, 1,
+                         fa.FA_DTYPE_BF16, None)
+    assert r == fa.FA_ERR_UNSUPPORTED
