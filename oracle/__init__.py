@@ -9,5 +9,6 @@ from .oracle import (  # noqa: F401
     attn_rows,
     attn_probs,
     attn_fwd_online,
+    attn_bwd,
     lib_path,
 )

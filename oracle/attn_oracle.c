@@ -37,6 +37,8 @@
  *   oracle_attn_fwd_online  the online-softmax recurrence over key tiles, in
  *                           double; it exists only so the tests can show the
  *                           tiled algorithm equals the definition.
+ *   oracle_attn_bwd         the gradients dQ, dK, dV of the forward for an
+ *                           upstream gradient dO (see its comment).
  * Every function returns 0 on success and -1 on a bad argument.
  */
 #include <math.h>
@@ -283,4 +285,120 @@ int oracle_attn_fwd_online(const float *q, const float *k, const float *v,
     }
     free(s);
     return 0;
+}
+
+/*
+ * Gradients of the forward above for an upstream gradient dO (the quantities
+ * of the backward kernel of "flash_attention_2.cu"), from the definition:
+ *   P_ij  = softmax over allowed keys j of s_ij = scale * q_i . k_j
+ *   dV_j  = sum_i P_ij dO_i
+ *   dP_ij = dO_i . v_j
+ *   D_i   = sum_j P_ij dP_ij
+ *   dS_ij = P_ij (dP_ij - D_i)
+ *   dQ_i  = scale * sum_j dS_ij k_j
+ *   dK_j  = scale * sum_i dS_ij q_i
+ * The page forms D_i as rowsum(dO_i * O_i); D_i = sum_j P_ij dP_ij is the same
+ * number because O_i = sum_j P_ij v_j, and needs no forward output.
+ * Excluded keys have P_ij = 0 and take no part.  Outputs are float64 with the
+ * layouts of q (dq) and k (dk, dv).
+ */
+typedef struct {
+    const float *q, *k, *v, *dout;
+    double *dq, *dk, *dv;
+    long B, H, Nq, Nk, d;
+    double scale;
+    int causal;
+    long next;
+    pthread_mutex_t mu;
+} bjob_t;
+
+static void bwd_head(bjob_t *J, long bh, double *p, double *dp)
+{
+    const long Nq = J->Nq, Nk = J->Nk, d = J->d;
+    const float *qh = J->q + bh * Nq * d, *kh = J->k + bh * Nk * d;
+    const float *vh = J->v + bh * Nk * d, *doh = J->dout + bh * Nq * d;
+    double *dqh = J->dq + bh * Nq * d, *dkh = J->dk + bh * Nk * d, *dvh = J->dv + bh * Nk * d;
+    for (long x = 0; x < Nk * d; ++x) { dkh[x] = 0.0; dvh[x] = 0.0; }
+    for (long i = 0; i < Nq; ++i) {
+        const float *qi = qh + i * d, *doi = doh + i * d;
+        const long nk = allowed_keys(i, Nk, J->causal);
+        /* probabilities of row i (two passes, as the forward) */
+        double m = -INFINITY;
+        for (long j = 0; j < nk; ++j) {
+            double dot = 0.0;
+            for (long x = 0; x < d; ++x) dot += (double)qi[x] * (double)kh[j * d + x];
+            p[j] = J->scale * dot;
+            if (p[j] > m) m = p[j];
+        }
+        double l = 0.0;
+        for (long j = 0; j < nk; ++j) { p[j] = exp(p[j] - m); l += p[j]; }
+        for (long j = 0; j < nk; ++j) p[j] /= l;
+        /* dP, D */
+        double D = 0.0;
+        for (long j = 0; j < nk; ++j) {
+            double dot = 0.0;
+            for (long x = 0; x < d; ++x) dot += (double)doi[x] * (double)vh[j * d + x];
+            dp[j] = dot;
+            D += p[j] * dot;
+        }
+        /* dS and the three gradients */
+        for (long x = 0; x < d; ++x) dqh[i * d + x] = 0.0;
+        for (long j = 0; j < nk; ++j) {
+            const double ds = p[j] * (dp[j] - D);
+            for (long x = 0; x < d; ++x) {
+                dqh[i * d + x] += J->scale * ds * (double)kh[j * d + x];
+                dkh[j * d + x] += J->scale * ds * (double)qi[x];
+                dvh[j * d + x] += p[j] * (double)doi[x];
+            }
+        }
+    }
+}
+
+static void *bwd_worker(void *arg)
+{
+    bjob_t *J = (bjob_t *)arg;
+    double *p = (double *)malloc(sizeof(double) * (size_t)J->Nk);
+    double *dp = (double *)malloc(sizeof(double) * (size_t)J->Nk);
+    if (!p || !dp) { free(p); free(dp); return (void *)1; }
+    for (;;) {
+        pthread_mutex_lock(&J->mu);
+        long bh = J->next++;
+        pthread_mutex_unlock(&J->mu);
+        if (bh >= J->B * J->H) break;
+        bwd_head(J, bh, p, dp);
+    }
+    free(p);
+    free(dp);
+    return NULL;
+}
+
+int oracle_attn_bwd(const float *q, const float *k, const float *v, const float *dout,
+                    double *dq, double *dk, double *dv,
+                    long B, long H, long Nq, long Nk, long d,
+                    double scale, int causal, int nthreads)
+{
+    if (!q || !k || !v || !dout || !dq || !dk || !dv || bad_sizes(B, H, Nq, Nk, d)) return -1;
+    bjob_t J;
+    memset(&J, 0, sizeof J);
+    J.q = q; J.k = k; J.v = v; J.dout = dout; J.dq = dq; J.dk = dk; J.dv = dv;
+    J.B = B; J.H = H; J.Nq = Nq; J.Nk = Nk; J.d = d; J.scale = scale;
+    J.causal = causal ? 1 : 0;
+    if (nthreads < 1) nthreads = 1;
+    if (nthreads > 1024) nthreads = 1024;
+    if ((long)nthreads > B * H) nthreads = (int)(B * H);
+    pthread_mutex_init(&J.mu, NULL);
+    pthread_t th[1024];
+    int started = 0, rc = 0;
+    for (int t = 0; t < nthreads; ++t) {
+        if (pthread_create(&th[t], NULL, bwd_worker, &J) != 0) break;
+        ++started;
+    }
+    if (started == 0) rc = (bwd_worker(&J) == NULL) ? 0 : -1;
+    for (int t = 0; t < started; ++t) {
+        void *ret = NULL;
+        pthread_join(th[t], &ret);
+        if (ret != NULL) rc = -1;
+    }
+    pthread_mutex_destroy(&J.mu);
+    return rc;
 }

@@ -83,6 +83,10 @@ def _declare(lib):
                                            _L, _L, _L, _L, _L, ctypes.c_double,
                                            ctypes.c_int, _L]
     lib.oracle_attn_fwd_online.restype = ctypes.c_int
+    lib.oracle_attn_bwd.argtypes = [_F32P, _F32P, _F32P, _F32P, _F64P, _F64P, _F64P,
+                                    _L, _L, _L, _L, _L, ctypes.c_double, ctypes.c_int,
+                                    ctypes.c_int]
+    lib.oracle_attn_bwd.restype = ctypes.c_int
 
 
 def _f32(a) -> np.ndarray:
@@ -171,3 +175,21 @@ def attn_fwd_online(q, k, v, scale: float, causal: bool, bc: int = 128, lib=None
     if rc != 0:
         raise RuntimeError("oracle_attn_fwd_online failed")
     return o, lse
+
+
+def attn_bwd(q, k, v, dout, scale: float, causal: bool, nthreads: int | None = None, lib=None):
+    """Gradients (dQ, dK, dV), float64, for upstream gradient dout [B,H,Nq,d]."""
+    lib = lib or load()
+    q, k, v, dout = _f32(q), _f32(k), _f32(v), _f32(dout)
+    B, H, Nq, Nk, d = _shapes(q, k, v)
+    if dout.shape != q.shape:
+        raise ValueError("dout must have the shape of q")
+    dq = np.empty(q.shape, np.float64)
+    dk = np.empty(k.shape, np.float64)
+    dv = np.empty(v.shape, np.float64)
+    rc = lib.oracle_attn_bwd(_ptr(q, _F32P), _ptr(k, _F32P), _ptr(v, _F32P), _ptr(dout, _F32P),
+                             _ptr(dq, _F64P), _ptr(dk, _F64P), _ptr(dv, _F64P),
+                             B, H, Nq, Nk, d, float(scale), int(bool(causal)), _threads(nthreads))
+    if rc != 0:
+        raise RuntimeError("oracle_attn_bwd failed")
+    return dq, dk, dv

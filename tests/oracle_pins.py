@@ -315,6 +315,86 @@ def pin_rows_api(lib, seed=10):
     return fails
 
 
+def pin_bwd_finite_differences(lib, seed=11):
+    """dL/dq, dL/dk, dL/dv of L = sum(O * G) by central differences of the
+    forward oracle, Richardson-extrapolated from steps 2^-6 and 2^-7.  Inputs
+    are multiples of 1/8, so every perturbed value is exact in float32."""
+    fails = []
+    rng = np.random.default_rng(seed)
+    for causal in (False, True):
+        q = (rng.integers(-12, 13, (1, 2, 4, 3)) / 8).astype(np.float32)
+        k = (rng.integers(-12, 13, (1, 2, 5, 3)) / 8).astype(np.float32)
+        v = (rng.integers(-12, 13, (1, 2, 5, 3)) / 8).astype(np.float32)
+        g = rng.standard_normal((1, 2, 4, 3))
+        dq, dk, dv = oracle.attn_bwd(q, k, v, g.astype(np.float32), 0.75, causal, lib=lib)
+        # the oracle's dO must be the float32 G the loss uses
+        g = g.astype(np.float32).astype(np.float64)
+
+        def loss(qq, kk, vv):
+            o, _ = oracle.attn_fwd(qq, kk, vv, 0.75, causal, lib=lib)
+            return float(np.sum(o * g))
+
+        for name, arr, grad in (("q", q, dq), ("k", k, dk), ("v", v, dv)):
+            for idx in np.ndindex(arr.shape):
+                est = []
+                for h in (2.0 ** -6, 2.0 ** -7):
+                    plus, minus = arr.copy(), arr.copy()
+                    plus[idx] += np.float32(h)
+                    minus[idx] -= np.float32(h)
+                    args = {"q": (q, k, v), "k": (q, k, v), "v": (q, k, v)}[name]
+                    if name == "q":
+                        lp, lm = loss(plus, k, v), loss(minus, k, v)
+                    elif name == "k":
+                        lp, lm = loss(q, plus, v), loss(q, minus, v)
+                    else:
+                        lp, lm = loss(q, k, plus), loss(q, k, minus)
+                    est.append((lp - lm) / (2 * h))
+                fd = (4 * est[1] - est[0]) / 3
+                if abs(fd - grad[idx]) > 1e-7 + 1e-6 * abs(grad[idx]):
+                    fails.append(f"bwd FD causal={causal} d{name}{idx}: {grad[idx]} vs {fd}")
+    return fails
+
+
+def pin_bwd_torch(lib, seed=12):
+    """torch float64 autograd through scaled_dot_product_attention."""
+    import torch
+    fails = []
+    rng = np.random.default_rng(seed)
+    q, k, v, g = (rng.standard_normal((2, 2, 40, 8)).astype(np.float32) for _ in range(4))
+    for causal in (False, True):
+        dq, dk, dv = oracle.attn_bwd(q, k, v, g, 0.3, causal, lib=lib)
+        tq, tk, tv = (torch.from_numpy(a).double().requires_grad_() for a in (q, k, v))
+        out = torch.nn.functional.scaled_dot_product_attention(tq, tk, tv, is_causal=causal,
+                                                               scale=0.3)
+        out.backward(torch.from_numpy(g).double())
+        for name, a, t in (("dq", dq, tq), ("dk", dk, tk), ("dv", dv, tv)):
+            if not _close(a, t.grad.numpy(), 1e-11, 1e-11):
+                fails.append(f"bwd torch causal={causal} {name}: "
+                             f"{np.max(np.abs(a - t.grad.numpy())):.2e}")
+    return fails
+
+
+def pin_bwd_identities(lib, seed=13):
+    """Every row of dS sums to zero (the probabilities sum to one), so the key
+    gradients sum to zero over keys and a constant key row gives dQ = 0; and
+    the value gradients sum to the summed upstream gradient."""
+    fails = []
+    rng = np.random.default_rng(seed)
+    q, k, v, g = (rng.standard_normal((1, 3, 9, 4)).astype(np.float32) for _ in range(4))
+    for causal in (False, True):
+        dq, dk, dv = oracle.attn_bwd(q, k, v, g, 0.6, causal, lib=lib)
+        if not np.all(np.abs(dk.sum(axis=2)) <= 1e-13):
+            fails.append(f"bwd identity causal={causal}: sum_j dK_j != 0")
+        if not _close(dv.sum(axis=2), g.astype(np.float64).sum(axis=2), 1e-13, 1e-13):
+            fails.append(f"bwd identity causal={causal}: sum_j dV_j != sum_i dO_i")
+        kc = np.broadcast_to(k[:, :, :1], k.shape).copy()
+        dq0, _, _ = oracle.attn_bwd(q, kc, v, g, 0.6, causal, lib=lib)
+        if not np.all(np.abs(dq0) <= 1e-13):
+            fails.append(f"bwd identity causal={causal}: constant keys but dQ != 0")
+    return fails
+
+
 ALL_PINS = [pin_golden, pin_brute_force, pin_probs, pin_constant_v, pin_causal_row0,
             pin_single_key, pin_uniform, pin_invariants, pin_online_recurrence,
-            pin_torch_sdpa, pin_rows_api]
+            pin_torch_sdpa, pin_rows_api, pin_bwd_finite_differences, pin_bwd_torch,
+            pin_bwd_identities]

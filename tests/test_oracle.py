@@ -30,6 +30,12 @@ MUTANTS = [
      "key reversed along d"),
     ("const float *kh = J->k + bh * J->Nk * J->d;",
      "const float *kh = J->k + (bh % J->H) * J->Nk * J->d;", "wrong head's keys"),
+    ("dvh[j * d + x] += p[j] * (double)doi[x];",
+     "dvh[j * d + x] += p[j] * (double)doh[(j % Nq) * d + x];",
+     "dV takes the key's row of dO (the page's backward indexing slip)"),
+    ("            D += p[j] * dot;", "            D += dot;", "D without the probabilities"),
+    ("dqh[i * d + x] += J->scale * ds * (double)kh[j * d + x];",
+     "dqh[i * d + x] += ds * (double)kh[j * d + x];", "dQ without the scale"),
 ]
 
 
