@@ -7,6 +7,12 @@ Workload at one GPU: B=8, H=32, Nq=Nk=8192, d=128, bf16, causal
 129 MB L2, so no flush is needed between steps.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl fa|reference]
+                  [--pass fwd|bwd]
+
+``--pass bwd`` times the backward instead (one step = one fa_bwd call: the
+per-row D / LSE kernel, the tensor-core gradient kernel and the dq rounding),
+reporting 2.5x the forward's FLOPs (five products of 2*Nq*Nk*d where the
+forward has two), the usual convention for attention backward.
 
 Under torchrun (N > 1) each rank runs its own copy of the workload on its own
 GPU (weak scaling; the heads are independent, so nothing is exchanged); the
@@ -32,6 +38,7 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 METRIC = "attn fwd TFLOP/s (4·B·H·N²·d, ½ if causal) and % of GB300 dense peak"
+METRIC_BWD = "attn bwd TFLOP/s (10·B·H·N²·d, ½ if causal) and % of GB300 dense peak"
 
 
 def kernel_source_hash() -> str:
@@ -227,6 +234,7 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--splits", type=int, default=None,
                     help="run fa_fwd_splitkv with this many key chunks (0 = automatic)")
+    ap.add_argument("--pass", dest="which", default="fwd", choices=["fwd", "bwd"])
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
 
@@ -266,7 +274,28 @@ def main():
         wsb = fa.fa_fwd_splitkv_workspace(w.B, w.H, w.Nq, w.d, args.splits if args.splits else 64)
         wspace = torch.empty(max(wsb, 256), dtype=torch.uint8, device=dev)
 
+    bwd = args.which == "bwd"
+    if bwd:
+        if w.dtype not in (0, 3):
+            raise SystemExit("--pass bwd needs a bf16 or fp16 workload")
+        # forward outputs and upstream gradient, resident before timing
+        fa.attention(q, k, v, scale=w.scale, causal=causal, out=o, lse=lse)
+        dout = torch.randn(w.B, w.H, w.Nq, w.d, device=dev, generator=g).to(tdt)
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+        bws = fa.fa_bwd_workspace(w.B, w.H, w.Nq, w.d)
+        bwork = torch.empty(bws, dtype=torch.uint8, device=dev)
+        args.no_e2e = True
+        args.no_cpu_baseline = True
+
     def step():
+        if bwd:
+            st = fa.fa_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                           dout.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), w.B,
+                           w.H, w.Nq, w.Nk, w.d, w.scale, int(causal), w.dtype,
+                           bwork.data_ptr(), bws, sh)
+            if st != fa.FA_OK:
+                raise fa.FaError(st, "fa_bwd")
+            return
         if wspace is None:
             st = fa.fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
                            w.B, w.H, w.Nq, w.Nk, w.d, w.scale, int(causal), w.dtype, sh)
@@ -309,7 +338,7 @@ def main():
     launch_ms = [ev[i].elapsed_time(ev[i + 1]) for i in range(args.steps)]
     total_ms = max_over_ranks(ev[0].elapsed_time(ev[-1]), dev)
     ms_per_step = total_ms / args.steps
-    flops_step = w.flops(causal)
+    flops_step = w.flops(causal) * (2.5 if bwd else 1.0)
     value = ws * flops_step * args.steps / (total_ms / 1e3) / 1e12
 
     # End to end through the host-buffer entry point: H2D of q, k, v from
@@ -352,13 +381,18 @@ def main():
     peaks, peak_src = measured_peaks()
     avg_launch_ms = sum(launch_ms) / len(launch_ms)
     achieved = flops_step / (avg_launch_ms / 1e3) / 1e12
-    peak = float(peaks["bf16_tflops"]) if w.dtype == 0 else float(peaks["bf16_tflops"]) / 2.0
+    half_io = w.dtype in (0, 3)   # bf16 / fp16: the same kind::f16 tensor rate
+    peak = float(peaks["bf16_tflops"]) if half_io else float(peaks["bf16_tflops"]) / 2.0
     kname = {0: "fa_tc_fwd_kernel<bf16>", 1: "fa_tc_fwd_kernel<tf32>",
-             2: "fa_simt_fwd_kernel"}[w.dtype]
+             2: "fa_simt_fwd_kernel", 3: "fa_tc_fwd_kernel<f16>"}[w.dtype]
+    if bwd:
+        # The step's three launches are timed together, so `achieved` is a
+        # lower bound for the gradient kernel alone.
+        kname = "fa_bwd (prep + fa_bwd_kernel + dq rounding)"
     traffic = profiled_traffic(kname, w.name)
     roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                 "frac": achieved / peak, "traffic": traffic,
-                "peak_source": f"{peak_src} {'bf16 burst' if w.dtype == 0 else 'bf16 burst / 2 (tf32 nominal ratio)'}",
+                "peak_source": f"{peak_src} {'bf16 burst' if half_io else 'bf16 burst / 2 (tf32 nominal ratio)'}",
                 "kernel": kname}
 
     cpu = None
@@ -368,7 +402,7 @@ def main():
                "sample": desc}
 
     line = {
-        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": ws,
+        "metric": METRIC_BWD if bwd else METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": ws,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": DTYPE_NAMES[w.dtype] if w.dtype != 0 else "bf16",
@@ -376,13 +410,13 @@ def main():
         "config": {"workload": w.name, "B": w.B, "H": w.H, "Nq": w.Nq, "Nk": w.Nk, "d": w.d,
                    "causal": causal, "flops_per_step": flops_step,
                    "parallelism": f"replicas{ws}" if ws > 1 else "single",
-                   "key_splits": args.splits,
+                   "key_splits": args.splits, "pass": args.which,
                    "l2": "inputs larger than L2 (no flush)"},
         "roofline": roofline,
         "pct_of_peak": 100.0 * value / ws / peak,
         "cpu_baseline": cpu,
         "e2e": e2e,
-        "gpu_launches": args.steps * (2 if wspace is not None else 1),
+        "gpu_launches": args.steps * (3 if bwd else 2 if wspace is not None else 1),
         "clocks": clocks,
     }
     print(json.dumps(line), flush=True)

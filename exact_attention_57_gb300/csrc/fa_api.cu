@@ -608,3 +608,106 @@ extern "C" int fa_fwd_varlen(const void *q, const void *k, const void *v, void *
     e = fa::launch_tc_f32_d64(mq, mk, mv, mo, p, B, causal, s);
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
+
+// ---------------------------------------------------------------------------
+// Backward.
+// ---------------------------------------------------------------------------
+namespace {
+
+size_t round256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+// Workspace parts: dq_acc [B*H][Nq][d] fp32, then lse2 and dd [B*H][Nq_pad].
+void bwd_ws_parts(int B, int H, int Nq, int d, size_t *acc, size_t *row) {
+  const size_t bh = static_cast<size_t>(B) * H;
+  const size_t nq_pad = static_cast<size_t>(ceil_div(Nq, fa::BM)) * fa::BM;
+  *acc = round256(bh * Nq * d * sizeof(float));
+  *row = round256(bh * nq_pad * sizeof(float));
+}
+
+}  // namespace
+
+extern "C" unsigned long long fa_bwd_workspace(int B, int H, int Nq, int d) {
+  if (B < 1 || H < 1 || Nq < 1 || d < 1) return 0;
+  size_t acc, row;
+  bwd_ws_parts(B, H, Nq, d, &acc, &row);
+  return acc + 2 * row;
+}
+
+extern "C" int fa_bwd(const void *q, const void *k, const void *v, const void *o,
+                      const float *lse, const void *dout, void *dq, void *dk, void *dv, int B,
+                      int H, int Nq, int Nk, int d, float scale, int causal, int dtype,
+                      void *workspace, unsigned long long workspace_bytes, void *stream) {
+  // The forward's checks cover q, k, v, o, lse, the sizes, scale and dtype.
+  int rc = validate(q, k, v, o, lse, B, H, Nq, Nk, d, scale, causal, dtype);
+  if (rc != FA_OK) return rc;
+  if (!dout || !dq || !dk || !dv || !workspace) return FA_ERR_INVALID_ARG;
+  for (const void *ptr : {dout, static_cast<const void *>(dq), static_cast<const void *>(dk),
+                          static_cast<const void *>(dv)})
+    if (reinterpret_cast<uintptr_t>(ptr) % 16 != 0) return FA_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(workspace) % 256 != 0) return FA_ERR_INVALID_ARG;
+  size_t acc, row;
+  bwd_ws_parts(B, H, Nq, d, &acc, &row);
+  const size_t need = acc + 2 * row;
+  if (workspace_bytes < need) return FA_ERR_INVALID_ARG;
+  const size_t es = elem_size(dtype);
+  const size_t qn = static_cast<size_t>(B) * H * Nq * d * es;
+  const size_t kn = static_cast<size_t>(B) * H * Nk * d * es;
+  const size_t ln = static_cast<size_t>(B) * H * Nq * sizeof(float);
+  // Outputs and workspace must not overlap each other or any input.
+  const struct { const void *p; size_t n; } in[] = {{q, qn}, {k, kn}, {v, kn}, {o, qn},
+                                                    {lse, ln}, {dout, qn}};
+  const struct { const void *p; size_t n; } out[] = {{dq, qn}, {dk, kn}, {dv, kn},
+                                                     {workspace, need}};
+  for (int a = 0; a < 4; ++a) {
+    for (const auto &x : in)
+      if (overlap(out[a].p, out[a].n, x.p, x.n)) return FA_ERR_INVALID_ARG;
+    for (int b = a + 1; b < 4; ++b)
+      if (overlap(out[a].p, out[a].n, out[b].p, out[b].n)) return FA_ERR_INVALID_ARG;
+  }
+  if (dtype != FA_DTYPE_BF16 && dtype != FA_DTYPE_F16) return FA_ERR_UNSUPPORTED;
+
+  unsigned *status = nullptr;
+  if ((rc = device_setup(&status)) != FA_OK) return rc;
+  if ((rc = get_encoder()) != FA_OK) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int BH = B * H;
+  CUtensorMap mq, mk, mv, mdo;
+  if ((rc = encode_map(&mq, q, dtype, BH, Nq, d)) != FA_OK) return rc;
+  if ((rc = encode_map(&mk, k, dtype, BH, Nk, d)) != FA_OK) return rc;
+  if ((rc = encode_map(&mv, v, dtype, BH, Nk, d)) != FA_OK) return rc;
+  if ((rc = encode_map(&mdo, dout, dtype, BH, Nq, d)) != FA_OK) return rc;
+
+  fa::BwdParams p;
+  p.dq_acc = static_cast<float *>(workspace);
+  float *lse2 = reinterpret_cast<float *>(static_cast<char *>(workspace) + acc);
+  float *dd = reinterpret_cast<float *>(static_cast<char *>(workspace) + acc + row);
+  p.lse2 = lse2;
+  p.dd = dd;
+  p.dk = dk;
+  p.dv = dv;
+  p.status = status;
+  p.H = H;
+  p.Nq = Nq;
+  p.Nk = Nk;
+  p.n_qtiles = ceil_div(Nq, fa::BM);
+  p.n_ktiles = ceil_div(Nk, fa::BN);
+  p.Nq_pad = p.n_qtiles * fa::BM;
+  p.scale = scale;
+  p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+  const unsigned long long lim = g_wait_limit_ns.load();
+  p.wait_limit_ns = lim ? lim : fa::kDefaultWaitLimitNs;
+  const int half = dtype == FA_DTYPE_F16 ? 1 : 0;
+
+  cudaError_t e = fa::launch_bwd_prep(o, dout, lse, lse2, dd, p.dq_acc, BH, Nq, p.Nq_pad, d,
+                                      half, s);
+  if (e != cudaSuccess) return FA_ERR_CUDA;
+  if (half)
+    e = (d == 64) ? fa::launch_bwd_f16_d64(mq, mk, mv, mdo, p, B, causal, s)
+                  : fa::launch_bwd_f16_d128(mq, mk, mv, mdo, p, B, causal, s);
+  else
+    e = (d == 64) ? fa::launch_bwd_bf16_d64(mq, mk, mv, mdo, p, B, causal, s)
+                  : fa::launch_bwd_bf16_d128(mq, mk, mv, mdo, p, B, causal, s);
+  if (e != cudaSuccess) return FA_ERR_CUDA;
+  e = fa::launch_bwd_convert(p.dq_acc, dq, static_cast<long long>(BH) * Nq * d, half, s);
+  return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}

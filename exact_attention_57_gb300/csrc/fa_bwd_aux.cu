@@ -1,0 +1,121 @@
+// fa_bwd_aux.cu — the two memory-bound steps around the tensor-core backward.
+//
+// Before it: per query row, D = rowsum(dO * O) (the D of the backward kernel
+// of "flash_attention_2.cu", leloykun/flash-hyperbolic-attention-minimal),
+// the saved LSE in log2 units, and a zeroed fp32 dQ accumulator row.  Rows
+// from Nq up to the padded tile end get LSE = +inf and D = 0, which makes
+// their probabilities exactly 0 in the main kernel.
+// After it: dQ rounded from the fp32 accumulator to the input type.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include <cmath>
+
+#include "fa_internal.h"
+
+namespace fa {
+
+namespace {
+
+constexpr int kPrepRowsPerBlock = 8;  // one warp per row
+
+__device__ __forceinline__ float2 load2(const void *base, size_t idx, bool half) {
+  const uint32_t w = *reinterpret_cast<const uint32_t *>(static_cast<const uint16_t *>(base) + idx);
+  if (half) {
+    const __half2 h = *reinterpret_cast<const __half2 *>(&w);
+    return __half22float2(h);
+  }
+  const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162 *>(&w);
+  return __bfloat1622float2(b);
+}
+
+template <int D>
+__global__ void __launch_bounds__(32 * kPrepRowsPerBlock)
+    fa_bwd_prep_kernel(const void *__restrict__ o, const void *__restrict__ dout,
+                       const float *__restrict__ lse, float *__restrict__ lse2,
+                       float *__restrict__ dd, float *__restrict__ dq_acc, int BH, int Nq,
+                       int Nq_pad, int half) {
+  const int lane = threadIdx.x & 31;
+  const long long prow =
+      static_cast<long long>(blockIdx.x) * kPrepRowsPerBlock + (threadIdx.x >> 5);
+  if (prow >= static_cast<long long>(BH) * Nq_pad) return;  // whole warp
+  const int bh = static_cast<int>(prow / Nq_pad);
+  const int q = static_cast<int>(prow - static_cast<long long>(bh) * Nq_pad);
+  if (q >= Nq) {
+    if (lane == 0) {
+      lse2[prow] = INFINITY;
+      dd[prow] = 0.f;
+    }
+    return;
+  }
+  const size_t row = static_cast<size_t>(bh) * Nq + q;
+  // lane covers elements [2*lane + 64*i, +2)
+  float acc = 0.f;
+#pragma unroll
+  for (int i = 0; i < D / 64; ++i) {
+    const size_t idx = row * D + 64 * i + 2 * lane;
+    const float2 a = load2(o, idx, half != 0), b = load2(dout, idx, half != 0);
+    acc = fmaf(a.x, b.x, acc);
+    acc = fmaf(a.y, b.y, acc);
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+  float *zrow = dq_acc + row * D;
+#pragma unroll
+  for (int i = 0; i < D / 128; ++i)
+    reinterpret_cast<float4 *>(zrow)[32 * i + lane] = make_float4(0.f, 0.f, 0.f, 0.f);
+  if constexpr (D % 128 != 0) {
+    if (lane < 16) reinterpret_cast<float4 *>(zrow)[(D / 128) * 32 + lane] = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+  if (lane == 0) {
+    lse2[prow] = lse[row] * 1.4426950408889634f;
+    dd[prow] = acc;
+  }
+}
+
+__global__ void fa_bwd_convert_kernel(const float *__restrict__ src, void *__restrict__ dst,
+                                      long long n8, int half) {
+  const long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i >= n8) return;
+  const float4 a = reinterpret_cast<const float4 *>(src)[2 * i];
+  const float4 b = reinterpret_cast<const float4 *>(src)[2 * i + 1];
+  uint4 out;
+  if (half) {
+    const __half2 h0 = __floats2half2_rn(a.x, a.y), h1 = __floats2half2_rn(a.z, a.w);
+    const __half2 h2 = __floats2half2_rn(b.x, b.y), h3 = __floats2half2_rn(b.z, b.w);
+    out = make_uint4(*reinterpret_cast<const uint32_t *>(&h0), *reinterpret_cast<const uint32_t *>(&h1),
+                     *reinterpret_cast<const uint32_t *>(&h2), *reinterpret_cast<const uint32_t *>(&h3));
+  } else {
+    const __nv_bfloat162 h0 = __floats2bfloat162_rn(a.x, a.y), h1 = __floats2bfloat162_rn(a.z, a.w);
+    const __nv_bfloat162 h2 = __floats2bfloat162_rn(b.x, b.y), h3 = __floats2bfloat162_rn(b.z, b.w);
+    out = make_uint4(*reinterpret_cast<const uint32_t *>(&h0), *reinterpret_cast<const uint32_t *>(&h1),
+                     *reinterpret_cast<const uint32_t *>(&h2), *reinterpret_cast<const uint32_t *>(&h3));
+  }
+  reinterpret_cast<uint4 *>(dst)[i] = out;
+}
+
+}  // namespace
+
+cudaError_t launch_bwd_prep(const void *o, const void *dout, const float *lse, float *lse2,
+                            float *dd, float *dq_acc, int BH, int Nq, int Nq_pad, int d, int half,
+                            cudaStream_t s) {
+  const long long rows = static_cast<long long>(BH) * Nq_pad;
+  const unsigned blocks = static_cast<unsigned>((rows + kPrepRowsPerBlock - 1) / kPrepRowsPerBlock);
+  if (d == 64)
+    fa_bwd_prep_kernel<64><<<blocks, 32 * kPrepRowsPerBlock, 0, s>>>(o, dout, lse, lse2, dd,
+                                                                     dq_acc, BH, Nq, Nq_pad, half);
+  else
+    fa_bwd_prep_kernel<128><<<blocks, 32 * kPrepRowsPerBlock, 0, s>>>(o, dout, lse, lse2, dd,
+                                                                      dq_acc, BH, Nq, Nq_pad, half);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_convert(const float *dq_acc, void *dq, long long n, int half,
+                               cudaStream_t s) {
+  const long long n8 = n / 8;  // n is a multiple of 64 (d is 64 or 128)
+  const unsigned blocks = static_cast<unsigned>((n8 + 255) / 256);
+  fa_bwd_convert_kernel<<<blocks, 256, 0, s>>>(dq_acc, dq, n8, half);
+  return cudaGetLastError();
+}
+
+}  // namespace fa

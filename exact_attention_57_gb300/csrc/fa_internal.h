@@ -18,6 +18,7 @@ constexpr unsigned kStatusProducer = 1u;
 constexpr unsigned kStatusMma = 2u;
 constexpr unsigned kStatusSoftmax = 4u;
 constexpr unsigned kStatusInjected = 8u;
+constexpr unsigned kStatusSmemLayout = 16u;  // shared memory base not aligned as needed
 
 constexpr unsigned long long kDefaultWaitLimitNs = 2000000000ull;  // 2 s
 
@@ -85,5 +86,42 @@ cudaError_t launch_splitkv_combine(const float *ws_o, const float *ws_lse, void 
                                    int dtype, cudaStream_t s);
 
 cudaError_t launch_simt(const SimtParams &p, int B, cudaStream_t s);
+
+// ------------------------------------------------------------------ backward
+// Tensor-core backward: one CTA per (key tile, head, batch).  The TMA maps
+// view q/dO as [B*H, Nq, d] and k/v as [B*H, Nk, d] (16-bit).
+struct BwdParams {
+  float *dq_acc;                  // [B*H][Nq][d] fp32, zeroed by the prep kernel
+  const float *lse2;              // [B*H][Nq_pad]: LSE * log2(e); +inf on padded rows
+  const float *dd;                // [B*H][Nq_pad]: D = rowsum(dO * O); 0 on padded rows
+  void *dk, *dv;                  // [B*H][Nk][d], input type
+  unsigned *status;
+  int H, Nq, Nk, Nq_pad;          // Nq_pad = 128 * n_qtiles
+  int n_qtiles, n_ktiles;
+  float scale;                    // signed softmax scale
+  float scale_log2;               // scale * log2(e), signed
+  unsigned long long wait_limit_ns;
+};
+
+cudaError_t launch_bwd_bf16_d64(const CUtensorMap &q, const CUtensorMap &k, const CUtensorMap &v,
+                                const CUtensorMap &dout, const BwdParams &p, int B, int causal,
+                                cudaStream_t s);
+cudaError_t launch_bwd_bf16_d128(const CUtensorMap &q, const CUtensorMap &k, const CUtensorMap &v,
+                                 const CUtensorMap &dout, const BwdParams &p, int B, int causal,
+                                 cudaStream_t s);
+cudaError_t launch_bwd_f16_d64(const CUtensorMap &q, const CUtensorMap &k, const CUtensorMap &v,
+                               const CUtensorMap &dout, const BwdParams &p, int B, int causal,
+                               cudaStream_t s);
+cudaError_t launch_bwd_f16_d128(const CUtensorMap &q, const CUtensorMap &k, const CUtensorMap &v,
+                                const CUtensorMap &dout, const BwdParams &p, int B, int causal,
+                                cudaStream_t s);
+
+// D = rowsum(dO * O) and LSE * log2(e) per padded row, and dq_acc zeroed.
+cudaError_t launch_bwd_prep(const void *o, const void *dout, const float *lse, float *lse2,
+                            float *dd, float *dq_acc, int BH, int Nq, int Nq_pad, int d, int half,
+                            cudaStream_t s);
+// dq = dq_acc rounded to the input type.
+cudaError_t launch_bwd_convert(const float *dq_acc, void *dq, long long n, int half,
+                               cudaStream_t s);
 
 }  // namespace fa

@@ -58,6 +58,7 @@
 #include <type_traits>
 
 #include "fa_internal.h"
+#include "fa_wait.cuh"
 #include "ptx.cuh"
 
 namespace fa {
@@ -111,33 +112,6 @@ struct TcCfg {
 constexpr float kRescaleThreshold = 8.0f;   // log2 units: factor 256
 constexpr float kLn2 = 0.693147180559945309f;
 constexpr unsigned kFull = 0xffffffffu;
-
-struct WaitCtl {
-  volatile int *abort;
-  unsigned *status;
-  unsigned long long limit_ns;
-  unsigned role;
-};
-
-// Bounded wait for an mbarrier phase.  Returns false if the CTA is aborting
-// (unless honour_abort is false) or the wait ran past the limit, in which case
-// it raises the abort flag and records its role in the status word.
-__device__ __forceinline__ bool bounded_wait(uint32_t bar, uint32_t parity, const WaitCtl &w,
-                                             bool honour_abort = true) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = globaltimer_ns();
-  for (uint32_t it = 1;; ++it) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 7u) == 0) {
-      if (honour_abort && *w.abort) return false;
-      if (globaltimer_ns() - t0 > w.limit_ns) {
-        *w.abort = 1;
-        atomicOr(w.status, w.role);
-        return false;
-      }
-    }
-  }
-}
 
 // HALF selects fp16 instead of bf16 for the 16-bit path (kind::f16 either
 // way; P and O are packed in the input type).

@@ -1,10 +1,10 @@
 """ctypes binding of ``libfa.so`` (the C ABI in include/fa.h).
 
-The functions ``fa_fwd``, ``fa_fwd_host``, ``fa_fwd_status``,
-``fa_status_string``, ``fa_version`` and ``fa_set_test_hooks`` mirror the C
-entry points one to one and only marshal arguments.  ``attention`` is a
-convenience wrapper for torch tensors: it allocates the outputs with torch
-(device memory is the only thing torch provides here) and calls ``fa_fwd``.
+The ``fa_*`` functions mirror the C entry points one to one and only marshal
+arguments.  ``attention``, ``attention_varlen`` and ``attention_backward`` are
+convenience wrappers for torch tensors: they allocate outputs and workspaces
+with torch (device memory is the only thing torch provides here) and call the
+C entry points.
 
 There is no fallback: if the library is missing or its call fails, these
 functions raise.
@@ -31,7 +31,7 @@ FA_DTYPE_F16 = 3
 
 EXPORTED = ("fa_fwd", "fa_fwd_host", "fa_fwd_status", "fa_status_string", "fa_version",
             "fa_set_test_hooks", "fa_fwd_noalloc", "fa_fwd_splitkv", "fa_fwd_splitkv_workspace",
-            "fa_fwd_varlen")
+            "fa_fwd_varlen", "fa_bwd", "fa_bwd_workspace")
 
 _lib = None
 
@@ -64,6 +64,11 @@ def load(path: str | None = None):
     lib.fa_fwd_splitkv_workspace.restype = ctypes.c_ulonglong
     lib.fa_fwd_varlen.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i, i, vp]
     lib.fa_fwd_varlen.restype = i
+    lib.fa_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, i, i, vp,
+                           ctypes.c_ulonglong, vp]
+    lib.fa_bwd.restype = i
+    lib.fa_bwd_workspace.argtypes = [i, i, i, i]
+    lib.fa_bwd_workspace.restype = ctypes.c_ulonglong
     lib.fa_fwd_host.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp,
                                 i, i, i, i, i, f, i, i, vp]
     lib.fa_fwd_host.restype = i
@@ -150,6 +155,53 @@ def attention_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int,
     if st != FA_OK:
         raise FaError(st, "fa_fwd_varlen")
     return out, lse
+
+
+def fa_bwd(q, k, v, o, lse, dout, dq, dk, dv, B, H, Nq, Nk, d, scale, causal, dtype,
+           workspace, workspace_bytes, stream) -> int:
+    return load().fa_bwd(q, k, v, o, lse, dout, dq, dk, dv, B, H, Nq, Nk, d, float(scale),
+                         int(causal), int(dtype), workspace, int(workspace_bytes), stream)
+
+
+def fa_bwd_workspace(B, H, Nq, d) -> int:
+    return load().fa_bwd_workspace(B, H, Nq, d)
+
+
+def attention_backward(q, k, v, out, lse, dout, scale: float | None = None,
+                       causal: bool = False, dq=None, dk=None, dv=None, workspace=None,
+                       stream=None):
+    """Gradients (dq, dk, dv) of attention() for the upstream gradient dout.
+
+    q, k, v, dout, out: contiguous bf16 / fp16 CUDA tensors as for attention();
+    out and lse are that forward's outputs.  The workspace (fa_bwd_workspace
+    bytes) is allocated with torch unless given.  Raises FaError on failure."""
+    import torch
+    B, H, Nq, d = q.shape
+    Nk = k.shape[2]
+    for t in (k, v, out, dout):
+        if t.dtype != q.dtype or not t.is_contiguous():
+            raise ValueError("q, k, v, out, dout: contiguous tensors of one dtype")
+    if out.shape != q.shape or dout.shape != q.shape or v.shape != k.shape:
+        raise ValueError("shape mismatch")
+    code = _dtype_code(q, "tc")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    ws_bytes = fa_bwd_workspace(B, H, Nq, d)
+    if workspace is None:
+        workspace = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=q.device)
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device).cuda_stream
+    with torch.cuda.device(q.device):
+        st = fa_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
+                    dout.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, Nq, Nk,
+                    d, scale, int(bool(causal)), code, workspace.data_ptr(),
+                    workspace.numel() * workspace.element_size(), stream)
+    if st != FA_OK:
+        raise FaError(st, "fa_bwd")
+    return dq, dk, dv
 
 
 def fa_fwd_host(q_h, k_h, v_h, o_h, lse_h, q_d, k_d, v_d, o_d, lse_d,

@@ -111,5 +111,17 @@ def make_inputs(B: int, H: int, Nq: int, Nk: int, d: int, dtype: int,
     return q, k, v
 
 
+def make_dout(B: int, H: int, Nq: int, d: int, dtype: int, seed: int):
+    """Seeded upstream gradient dO [B, H, Nq, d] on the CPU, N(0, 1) values in
+    the I/O dtype of ``dtype`` (the gradient of sum(O * dO))."""
+    g = torch.Generator("cpu").manual_seed(int(seed) + 7919)
+    do = torch.randn(B, H, Nq, d, generator=g, dtype=torch.float32)
+    if dtype == DTYPE_BF16:
+        do = do.to(torch.bfloat16)
+    elif dtype == DTYPE_F16:
+        do = do.to(torch.float16)
+    return do
+
+
 def workload_inputs(w: Workload):
     return make_inputs(w.B, w.H, w.Nq, w.Nk, w.d, w.dtype, w.seed, w.k_mult)

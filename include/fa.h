@@ -1,7 +1,7 @@
 /*
- * fa.h — C ABI of the GB300 (sm_103a) exact-attention forward library.
+ * fa.h — C ABI of the GB300 (sm_103a) exact-attention library.
  *
- * One operation: the fused, tiled, exact multi-head attention forward pass
+ * The operation: the fused, tiled, exact multi-head attention forward pass
  *
  *     O   = softmax(scale * Q K^T  [+ causal mask]) V
  *     LSE = per-row log-sum-exp of the scaled, masked scores (natural log)
@@ -15,6 +15,7 @@
  * (query tile outer, key tiles inner, O written once), and the grid runs over
  * queries as well as batch and heads, as in "Meta's xFormers has Attention
  * kernel written in CUTLASS" (forward parallelised across the queries).
+ * fa_bwd computes its gradients (dq, dk, dv) for an upstream gradient.
  *
  * Conventions shared by every entry point
  * ---------------------------------------
@@ -196,6 +197,43 @@ int fa_fwd_varlen(const void *q, const void *k, const void *v, void *o, float *l
                   int causal, int dtype, void *stream);
 
 /*
+ * fa_bwd — gradients of the forward for an upstream gradient dout: the
+ * backward kernel of "flash_attention_2.cu"
+ * (leloykun/flash-hyperbolic-attention-minimal), with the probabilities
+ * recomputed from the saved log-sum-exp:
+ *   P = exp(scale * Q K^T - LSE) (causal keys masked),  D = rowsum(dout * o),
+ *   dv = P^T dout,  dS = P * (dout V^T - D),  dq = scale * dS K,
+ *   dk = scale * dS^T Q.
+ *
+ * q, k, v, o, lse  the forward's inputs and outputs, as for fa_fwd (o and
+ *                  lse must come from fa_fwd, or hold the same values).
+ * dout             upstream gradient [B,H,Nq,d], the type of q.
+ * dq [B,H,Nq,d], dk and dv [B,H,Nk,d]: outputs, the type of q, every element
+ *                  written (keys that no query sees get zero gradients).
+ * dtype            FA_DTYPE_BF16 or FA_DTYPE_F16 with d 64 or 128 (tcgen05
+ *                  kind::f16; P and dS are rounded to the input type, the
+ *                  products accumulate in fp32); anything else is
+ *                  FA_ERR_UNSUPPORTED.
+ * workspace        caller-owned device memory, 256-byte aligned, of at least
+ *                  fa_bwd_workspace(B, H, Nq, d) bytes: an fp32 dq
+ *                  accumulator and two fp32 values per query row.  Calls that
+ *                  share a workspace must not overlap on the GPU.
+ * All pointers 16-byte aligned except lse (4 bytes); outputs and workspace
+ * must not overlap each other or any input.  Asynchronous on `stream` (three
+ * kernels: per-row D and LSE, the tensor-core kernel, dq rounding); bounded
+ * waits report through the status word (fa_fwd_status).  Arguments are
+ * checked before anything is enqueued (FA_ERR_INVALID_ARG).
+ */
+int fa_bwd(const void *q, const void *k, const void *v, const void *o, const float *lse,
+           const void *dout, void *dq, void *dk, void *dv,
+           int B, int H, int Nq, int Nk, int d, float scale, int causal, int dtype,
+           void *workspace, unsigned long long workspace_bytes, void *stream);
+
+/* Bytes of workspace fa_bwd needs: B*H*Nq*d floats plus 2*B*H*ceil(Nq/128)*128
+ * floats, each part rounded up to 256 bytes.  0 for invalid arguments. */
+unsigned long long fa_bwd_workspace(int B, int H, int Nq, int d);
+
+/*
  * fa_fwd_host — the same forward on HOST buffers.
  *
  * q_h, k_h, v_h   host inputs (pinned memory gives full copy speed).
@@ -217,7 +255,8 @@ int fa_fwd_host(const void *q_h, const void *k_h, const void *v_h,
  * device's status word.  *device_status (may be NULL) receives the raw word:
  * 0 when every kernel finished normally; otherwise bit r set means a warp of
  * role r gave up on a bounded wait (1 = TMA producer, 2 = MMA issuer,
- * 4 = softmax/epilogue warps, 8 = fault injected by the test hook).
+ * 4 = softmax/epilogue warps, 8 = fault injected by the test hook,
+ * 16 = shared memory not aligned as the backward kernel needs).
  * Returns FA_OK, FA_ERR_DEVICE_TIMEOUT (word != 0) or FA_ERR_CUDA.
  */
 int fa_fwd_status(void *stream, int *device_status);

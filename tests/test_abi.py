@@ -148,3 +148,49 @@ def test_varlen_refuses_simt_and_unsupported_dims(lib):
     r = fa.fa_fwd_varlen(Q, K, V, O, L, CUQ, CUK, 2, 2, 16, 16, 8, 96, 0.125, 1,
                          fa.FA_DTYPE_BF16, None)
     assert r == fa.FA_ERR_UNSUPPORTED
+
+
+DO, DQ, DK, DV, WS = 0x800000, 0x900000, 0xA00000, 0xB00000, 0xC00000
+
+
+def test_bwd_workspace_size(lib):
+    """B*H*Nq*d floats plus two floats per padded query row, parts rounded up
+    to 256 bytes."""
+    up = lambda n: (n + 255) // 256 * 256
+    for B, H, Nq, d in [(1, 1, 1, 64), (2, 16, 8192, 128), (1, 3, 300, 64)]:
+        pad = (Nq + 127) // 128 * 128
+        assert fa.fa_bwd_workspace(B, H, Nq, d) == up(B * H * Nq * d * 4) + 2 * up(B * H * pad * 4)
+    for bad in [(0, 1, 1, 64), (1, 0, 1, 64), (1, 1, 0, 64), (1, 1, 1, 0)]:
+        assert fa.fa_bwd_workspace(*bad) == 0
+
+
+def call_bwd(**kw):
+    a = dict(q=Q, k=K, v=V, o=O, lse=L, do=DO, dq=DQ, dk=DK, dv=DV, B=1, H=1, Nq=16, Nk=16, d=64,
+             scale=0.125, causal=0, dtype=fa.FA_DTYPE_BF16, ws=WS, ws_bytes=None)
+    a.update(kw)
+    if a["ws_bytes"] is None:
+        a["ws_bytes"] = fa.fa_bwd_workspace(a["B"], a["H"], max(a["Nq"], 1), max(a["d"], 1))
+    return fa.fa_bwd(a["q"], a["k"], a["v"], a["o"], a["lse"], a["do"], a["dq"], a["dk"],
+                     a["dv"], a["B"], a["H"], a["Nq"], a["Nk"], a["d"], a["scale"], a["causal"],
+                     a["dtype"], a["ws"], a["ws_bytes"], None)
+
+
+@pytest.mark.parametrize("kw", [
+    dict(do=None), dict(dq=None), dict(dk=None), dict(dv=None), dict(ws=None),
+    dict(q=None), dict(lse=None), dict(Nq=0), dict(Nk=0), dict(scale=float("nan")),
+    dict(causal=3), dict(dtype=7),
+    dict(do=DO + 8), dict(dq=DQ + 4), dict(dk=DK + 2), dict(ws=WS + 16), dict(ws_bytes=1000),
+    dict(dq=Q), dict(dk=V + 64), dict(dv=DO), dict(dq=DK), dict(ws=DV), dict(dv=L),
+], ids=lambda kw: ",".join(f"{k}={v}" for k, v in kw.items()))
+def test_bwd_invalid_arguments(lib, kw):
+    """Missing, misaligned, short or overlapping buffers are refused before
+    any device work."""
+    assert call_bwd(**kw) == fa.FA_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("kw", [
+    dict(dtype=fa.FA_DTYPE_F32), dict(dtype=fa.FA_DTYPE_F32_SIMT), dict(d=96),
+    dict(dtype=fa.FA_DTYPE_F16, d=256),
+], ids=lambda kw: ",".join(f"{k}={v}" for k, v in kw.items()))
+def test_bwd_unsupported_problems(lib, kw):
+    assert call_bwd(**kw) == fa.FA_ERR_UNSUPPORTED

@@ -1,0 +1,107 @@
+"""fa_bwd (tensor-core backward) against the float64 oracle gradients on the
+same inputs: the forward's o and lse come from fa_fwd, the expected dq, dk,
+dv from oracle.attn_bwd (needs a GB300)."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from exact_attention_57_gb300 import fa
+from exact_attention_57_gb300.workloads import DTYPE_BF16, DTYPE_F16, make_dout, make_inputs
+
+pytestmark = pytest.mark.gpu
+
+# Normwise tolerances on each gradient X: max|dX| <= max_rel * max|X| and
+# mean|dX| <= mean_rel * mean|X|.  The products accumulate in fp32; what moves
+# the result is the rounding to the 16-bit input type (unit roundoff u = 2^-9
+# for bf16, 2^-12 for fp16) of P (the A operand of dV), of dS (the A operand
+# of dQ and dK), of the forward's O (through D), and of the outputs.  Each
+# term of every sum carries a relative error of about u, so the typical
+# error is about u of the typical gradient: mean_rel = 2.5u, max_rel = 8u.
+U = {DTYPE_BF16: 2.0 ** -9, DTYPE_F16: 2.0 ** -12}
+TOL = {dt: dict(max_rel=8 * u, mean_rel=2.5 * u) for dt, u in U.items()}
+
+CASES = [
+    # B, H, Nq, Nk, d, causal, dtype, scale (None = 1/sqrt(d))
+    (1, 2, 128, 128, 64, False, DTYPE_BF16, None),
+    (1, 2, 128, 128, 128, True, DTYPE_BF16, None),
+    (2, 2, 300, 300, 128, True, DTYPE_BF16, None),
+    (1, 2, 200, 457, 64, False, DTYPE_BF16, None),
+    (1, 2, 457, 200, 128, True, DTYPE_BF16, None),
+    (1, 2, 100, 400, 128, True, DTYPE_BF16, None),   # keys past the last query
+    (1, 3, 1, 1, 64, False, DTYPE_BF16, None),
+    (1, 2, 384, 256, 64, True, DTYPE_F16, None),
+    (2, 1, 333, 517, 128, False, DTYPE_F16, None),
+    (1, 2, 256, 256, 128, True, DTYPE_BF16, -0.2),
+    (1, 2, 256, 300, 64, False, DTYPE_BF16, 0.0),
+    (1, 4, 1024, 1024, 128, True, DTYPE_BF16, None),
+    (1, 4, 1024, 1024, 64, False, DTYPE_BF16, None),
+]
+
+
+def run_bwd(q, k, v, do, scale, causal):
+    dev = torch.device("cuda:0")
+    qd, kd, vd, dod = (t.to(dev) for t in (q, k, v, do))
+    o, lse = fa.attention(qd, kd, vd, scale=scale, causal=causal)
+    grads = [torch.full_like(t, float("nan")) for t in (qd, kd, vd)]
+    fa.attention_backward(qd, kd, vd, o, lse, dod, scale=scale, causal=causal,
+                          dq=grads[0], dk=grads[1], dv=grads[2])
+    st, word = fa.fa_fwd_status(torch.cuda.current_stream(dev).cuda_stream)
+    assert st == fa.FA_OK, f"device status word {word}"
+    return [g.double().cpu().numpy() for g in grads]
+
+
+def check(got, ref, dtype, what):
+    tol = TOL[dtype]
+    for name, a, b in zip(("dq", "dk", "dv"), got, ref):
+        assert np.all(np.isfinite(a)), f"{what} {name}: non-finite values"
+        err = np.abs(a - b)
+        mx, mn = float(err.max()), float(err.mean())
+        ref_max, ref_mean = float(np.abs(b).max()), float(np.abs(b).mean())
+        print(f"{what} {name}: max {mx:.3e} ({mx / max(ref_max, 1e-30):.2e} of max) "
+              f"mean {mn:.3e} ({mn / max(ref_mean, 1e-30):.2e} of mean)")
+        assert mx <= tol["max_rel"] * ref_max + 1e-6, f"{what} {name}: max |err| {mx:.3e}"
+        assert mn <= tol["mean_rel"] * ref_mean + 1e-7, f"{what} {name}: mean |err| {mn:.3e}"
+
+
+@pytest.mark.parametrize("B,H,Nq,Nk,d,causal,dtype,scale", CASES)
+def test_bwd_matches_oracle(B, H, Nq, Nk, d, causal, dtype, scale):
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    seed = 3 * Nq + Nk + d
+    q, k, v = make_inputs(B, H, Nq, Nk, d, dtype, seed=seed)
+    do = make_dout(B, H, Nq, d, dtype, seed=seed)
+    got = run_bwd(q, k, v, do, scale, causal)
+    ref = oracle.attn_bwd(q.float().numpy(), k.float().numpy(), v.float().numpy(),
+                          do.float().numpy(), scale, causal)
+    check(got, ref, dtype, f"{B,H,Nq,Nk,d} causal={causal} scale={scale:.3g}")
+    if causal and Nk > Nq:
+        # keys no query sees: exactly zero gradients
+        assert np.all(got[1][:, :, Nq:] == 0) and np.all(got[2][:, :, Nq:] == 0)
+
+
+def test_bwd_rejects_bad_arguments():
+    dev = torch.device("cuda:0")
+    q, k, v = (t.to(dev) for t in make_inputs(1, 1, 128, 128, 64, DTYPE_BF16, seed=1))
+    o, lse = fa.attention(q, k, v)
+    do = torch.randn_like(q)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    need = fa.fa_bwd_workspace(1, 1, 128, 64)
+    ws = torch.empty(fa.fa_bwd_workspace(1, 1, 128, 128) + 512, dtype=torch.uint8, device=dev)
+    s = torch.cuda.current_stream(dev).cuda_stream
+    args = [q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+            do.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), 1, 1, 128, 128, 64,
+            0.125, 0, fa.FA_DTYPE_BF16]
+    assert fa.fa_bwd(*args, ws.data_ptr(), need - 1, s) == fa.FA_ERR_INVALID_ARG
+    assert fa.fa_bwd(*args, ws.data_ptr() + 16, need, s) == fa.FA_ERR_INVALID_ARG
+    bad = list(args)
+    bad[6] = q.data_ptr()   # dq over q
+    assert fa.fa_bwd(*bad, ws.data_ptr(), need, s) == fa.FA_ERR_INVALID_ARG
+    bad = list(args)
+    bad[13] = 32   # head dim outside the compiled set (extents within the buffers)
+    assert fa.fa_bwd(*bad, ws.data_ptr(), fa.fa_bwd_workspace(1, 1, 128, 32),
+                     s) == fa.FA_ERR_UNSUPPORTED
+    assert fa.fa_bwd(*args, ws.data_ptr(), need, s) == fa.FA_OK
+    assert fa.fa_fwd_status(s)[0] == fa.FA_OK
