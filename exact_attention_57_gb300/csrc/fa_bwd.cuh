@@ -16,7 +16,7 @@
 //               key, warp w covers lanes 32*(w%4) and query half w/4), form
 //               P^T (packed to 16 bits, back into tensor memory: the A operand
 //               of dV) and dS = scale * P (dP - D) (16 bits, shared memory).
-//               Then drain dQ from tensor memory with vector atomic adds.  At
+//               Then drain dQ from tensor memory with fp32 atomic adds.  At
 //               the end, write dV and dK.
 //   warp 8      TMA producer: K_j and V_j once, then per query tile Q_i, dO_i
 //               (2-stage ring) and the 128 rows' LSE*log2(e) and D (bulk copies).
@@ -24,7 +24,7 @@
 //                 S^T  = K_j Q_i^T,  dP^T = V_j dO_i^T      (both operands K-major)
 //                 dV  += P^T dO_i                            (A in TMEM, B MN-major)
 //                 dK  += dS^T Q_i                            (A K-major, B MN-major)
-//                 dQ_i = dS K_j                              (A, B MN-major)
+//                 dQ_i = dS K_j, for D = 128 as dQ_i^T = K_j^T dS^T (A, B MN-major)
 // dS is stored once, one 128-byte-swizzled row of queries per key, and read
 // as both A operands: rows = keys, queries contiguous is dS^T K-major and
 // dS MN-major.
@@ -66,6 +66,10 @@ struct BwdCfg {
   // dQ over dP^T when a separate region does not fit (D = 128)
   static constexpr bool ALIAS = 2 * D + 256 + D > static_cast<int>(TMEM_COLS);
   static constexpr uint32_t COL_P = COL_S + 32;                  // P^T, 64 columns
+  // D = 128: dQ^T = K^T dS^T (lane = head-dim index), so that a warp's
+  // atomic adds cover 32 consecutive floats of one dQ row.  D = 64 keeps
+  // dQ = dS K (lane = query; an M = 64 product would use half the lanes).
+  static constexpr bool DQT = D == 128;
   static constexpr uint32_t COL_DQ = ALIAS ? COL_DP : COL_DP + 128;
   static constexpr int OFF_K = 0;
   static constexpr int OFF_V = OFF_K + TILE_BYTES;
@@ -210,7 +214,8 @@ __global__ void __launch_bounds__(320, 1)
       constexpr uint32_t kFmt = HALF ? 0u : 1u;                         // f16 / bf16
       constexpr uint32_t kIdescT = make_idesc(kFmt, 128, 128, 0u, 0u);  // S^T, dP^T
       constexpr uint32_t kIdescAcc = make_idesc(kFmt, 128, D, 0u, 1u);  // dV
-      constexpr uint32_t kIdescDQ = make_idesc(kFmt, 128, D, 1u, 1u);   // dQ
+      // dQ: M = 128 queries, N = D; dQ^T: M = 128 = D, N = 128 queries
+      constexpr uint32_t kIdescDQ = make_idesc(kFmt, 128, C::DQT ? 128 : D, 1u, 1u);
       constexpr uint32_t kIdescDK = make_idesc(kFmt, 128, D, 0u, 1u);  // dK
       bool ok = bounded_wait(bKV, 0, w);
       for (int it = 0; ok && it < n_it; ++it) {
@@ -260,14 +265,17 @@ __global__ void __launch_bounds__(320, 1)
           if (!(ok = bounded_wait(bDQfree, (it - 1) & 1, w))) break;
           tc_fence_after();
         }
-        // dQ_i = dS K_j: 16 keys per UMMA; dS is MN-major A (two 64-query
-        // panels), K_j the MN-major B.
+        // dQ_i = dS K_j, or for D = 128 its transpose K_j^T dS^T: 16 keys per
+        // UMMA; dS (two 64-query panels) and K_j are both read MN-major.
 #pragma unroll
-        for (int kk = 0; kk < BN / C::UK; ++kk)
-          umma_ss<false>(tmem + C::COL_DQ,
-                         sdesc_sw128(sDS + kk * C::UK * 128, C::CHUNK_BYTES, 1024),
-                         sdesc_sw128(sK + kk * C::UK * 128, C::CHUNK_BYTES, 1024), kIdescDQ,
-                         kk > 0 ? 1u : 0u);
+        for (int kk = 0; kk < BN / C::UK; ++kk) {
+          const uint64_t ds_desc = sdesc_sw128(sDS + kk * C::UK * 128, C::CHUNK_BYTES, 1024);
+          const uint64_t k_desc = sdesc_sw128(sK + kk * C::UK * 128, C::CHUNK_BYTES, 1024);
+          if constexpr (C::DQT)
+            umma_ss<false>(tmem + C::COL_DQ, k_desc, ds_desc, kIdescDQ, kk > 0 ? 1u : 0u);
+          else
+            umma_ss<false>(tmem + C::COL_DQ, ds_desc, k_desc, kIdescDQ, kk > 0 ? 1u : 0u);
+        }
         tc_commit(bQempty + 8 * s);
         tc_commit(bBdone);
         tc_commit(bDQfull);
@@ -353,23 +361,41 @@ __global__ void __launch_bounds__(320, 1)
       tc_fence_before();
       mbar_arrive(bPfull);
 
-      // dQ_i (lane = query row r, columns = this half of d) -> dq_acc.
+      // dQ_i -> dq_acc with fp32 atomic adds.
       ok = __all_sync(kFullMask, bounded_wait(bDQfull, it & 1, w));
       if (!ok) break;
       tc_fence_after();
-      const int qrow = qt * BM + r;
-      float *dst = p.dq_acc + (static_cast<size_t>(bh) * p.Nq + qrow) * D + g * (D / 2);
+      if constexpr (C::DQT) {
+        // dQ^T: lane r = head-dim index, columns = this half's 64 queries; the
+        // warp's 32 lanes add to 32 consecutive floats of one dQ row.
+        const int qbase = qt * BM + cb;
+        float *dst = p.dq_acc + (static_cast<size_t>(bh) * p.Nq + qbase) * D + r;
 #pragma unroll
-      for (int c = 0; c < D / 2; c += 32) {
-        uint32_t v[32];
-        tmem_ld32(tmem + lane_off + C::COL_DQ + g * (D / 2) + c, v);
-        tmem_ld_wait();
-        reg_fence32(v);
-        if (qrow < p.Nq) {
+        for (int c = 0; c < 64; c += 32) {
+          uint32_t v[32];
+          tmem_ld32(tmem + lane_off + C::COL_DQ + cb + c, v);
+          tmem_ld_wait();
+          reg_fence32(v);
 #pragma unroll
-          for (int u = 0; u < 8; ++u)
-            red_add_v4(dst + c + 4 * u, __uint_as_float(v[4 * u]), __uint_as_float(v[4 * u + 1]),
-                       __uint_as_float(v[4 * u + 2]), __uint_as_float(v[4 * u + 3]));
+          for (int i = 0; i < 32; ++i)
+            if (qbase + c + i < p.Nq) red_add(dst + static_cast<size_t>(c + i) * D, __uint_as_float(v[i]));
+        }
+      } else {
+        // dQ: lane r = query row, columns = this half of d.
+        const int qrow = qt * BM + r;
+        float *dst = p.dq_acc + (static_cast<size_t>(bh) * p.Nq + qrow) * D + g * (D / 2);
+#pragma unroll
+        for (int c = 0; c < D / 2; c += 32) {
+          uint32_t v[32];
+          tmem_ld32(tmem + lane_off + C::COL_DQ + g * (D / 2) + c, v);
+          tmem_ld_wait();
+          reg_fence32(v);
+          if (qrow < p.Nq) {
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+              red_add_v4(dst + c + 4 * u, __uint_as_float(v[4 * u]), __uint_as_float(v[4 * u + 1]),
+                         __uint_as_float(v[4 * u + 2]), __uint_as_float(v[4 * u + 3]));
+          }
         }
       }
       tc_fence_before();

@@ -301,6 +301,11 @@ __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
   return y;
 }
 
+// Fire-and-forget atomic add of one fp32 value.
+__device__ __forceinline__ void red_add(float *addr, float a) {
+  asm volatile("red.global.add.f32 [%0], %1;" ::"l"(addr), "f"(a) : "memory");
+}
+
 // Fire-and-forget atomic add of four consecutive fp32 values (16-byte aligned).
 __device__ __forceinline__ void red_add_v4(float *addr, float a, float b, float c, float d) {
   asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "f"(a), "f"(b),
