@@ -11,30 +11,35 @@
 // atomic adds.  The page's dV update reads the upstream gradient of the key's
 // row instead of the query's; the product above is the derivative.
 //
-// GB300 design (one CTA = one (batch, head, 128-key tile)):
-//   warps 0-7   per query tile: read S^T and dP^T from tensor memory (lane =
-//               key, warp w covers lanes 32*(w%4) and query half w/4), form
-//               P^T (packed to 16 bits, back into tensor memory: the A operand
-//               of dV) and dS = scale * P (dP - D) (16 bits, shared memory).
-//               Then drain dQ from tensor memory with fp32 atomic adds.  At
-//               the end, write dV and dK.
+// GB300 design (one CTA = one (batch, head, 128-key tile)).  Each 128-query
+// tile is processed as two halves h of 64 queries with their own tensor
+// memory, so that the dQ drain of one half overlaps the other half's softmax
+// and products:
+//   warps 0-7   per half: read S_h^T and dP_h^T from tensor memory (lane =
+//               key, warp w covers lanes 32*(w%4) and queries 32*(w/4) of the
+//               half), form P^T (packed to 16 bits, back into tensor memory:
+//               the A operand of dV) and dS = scale * P (dP - D) (16 bits,
+//               shared memory).  Then drain dQ_h^T from tensor memory with fp32
+//               atomic adds.  At the end, write dV and dK.
 //   warp 8      TMA producer: K_j and V_j once, then per query tile Q_i, dO_i
 //               (2-stage ring) and the 128 rows' LSE*log2(e) and D (bulk copies).
-//   warp 9      UMMA issuer (one lane), owner of tensor memory:
-//                 S^T  = K_j Q_i^T,  dP^T = V_j dO_i^T      (both operands K-major)
-//                 dV  += P^T dO_i                            (A in TMEM, B MN-major)
-//                 dK  += dS^T Q_i                            (A K-major, B MN-major)
-//                 dQ_i = dS K_j, for D = 128 as dQ_i^T = K_j^T dS^T (A, B MN-major)
-// dS is stored once, one 128-byte-swizzled row of queries per key, and read
-// as both A operands: rows = keys, queries contiguous is dS^T K-major and
-// dS MN-major.
-// Tensor memory (512 columns): dV [0, D), dK [D, 2D), S^T [2D, 2D+128),
-// dP^T [2D+128, 2D+256), and for D = 64 dQ after them.  P^T (64 columns)
-// goes over columns 32..95 of S^T: each query half then writes only columns
-// it has itself read (the half with queries 0..63 reads its upper 32 columns
-// first), so neither half waits for the other.  For D = 128, dQ goes over
-// dP^T once the softmax has read it; the next S^T is issued as soon as the
-// previous products complete and the next dP^T once dQ has been drained.
+//   warp 9      UMMA issuer (one lane), owner of tensor memory, per half h:
+//                 S_h^T = K_j Q_h^T,  dP_h^T = V_j dO_h^T   (both operands K-major)
+//                 dV  += P_h^T dO_h                         (A in TMEM, B MN-major)
+//                 dK  += dS_h^T Q_h                         (A K-major, B MN-major)
+//                 dQ_h^T = K_j^T dS_h^T                     (A, B MN-major)
+// dS_h is stored once, one 128-byte-swizzled row of 64 queries per key, and
+// read as two operands: rows = keys with queries contiguous is dS_h^T K-major
+// (dK) and dS_h^T MN-major (dQ^T).  dQ^T has the head dimension on the TMEM
+// lanes, so a warp's 32 atomic adds cover 32 consecutive floats of one dQ
+// row.  (For D = 64 the dQ^T product still has M = 128: its A operand reads
+// one 64-column panel past K_j, into V_j, and lanes 64-127 are not drained.)
+// Tensor memory (512 columns): dV [0, D), dK [D, 2D), then per half h
+// S_h^T [2D + 128h, +64) and dP_h^T [2D + 128h + 64, +64).  P_h^T (32
+// columns) goes over columns 16..47 of S_h^T: each query quarter then writes
+// only columns it has itself read, so neither waits for the other.  dQ_h^T
+// goes over dP_h^T once the softmax has read it; the next tile's dP_h^T is
+// issued once dQ_h^T has been drained.
 //
 // Every wait is bounded (globaltimer); on expiry the CTA raises an abort
 // flag, records its role in the status word, drains in-flight copies and
@@ -58,37 +63,33 @@ struct BwdCfg {
   static constexpr int TILE_BYTES = NCH * CHUNK_BYTES;      // one 128-row tile
   static constexpr int UK = 16;                             // K extent of one UMMA
   static constexpr int NQS = 2;                             // Q / dO ring depth
+  static constexpr int HQ = 64;                             // queries per half tile
   static constexpr uint32_t TMEM_COLS = 512;
   static constexpr uint32_t COL_DV = 0;
   static constexpr uint32_t COL_DK = D;
-  static constexpr uint32_t COL_S = 2 * D;
-  static constexpr uint32_t COL_DP = 2 * D + 128;
-  // dQ over dP^T when a separate region does not fit (D = 128)
-  static constexpr bool ALIAS = 2 * D + 256 + D > static_cast<int>(TMEM_COLS);
-  static constexpr uint32_t COL_P = COL_S + 32;                  // P^T, 64 columns
-  // D = 128: dQ^T = K^T dS^T (lane = head-dim index), so that a warp's
-  // atomic adds cover 32 consecutive floats of one dQ row.  D = 64 keeps
-  // dQ = dS K (lane = query; an M = 64 product would use half the lanes).
-  static constexpr bool DQT = D == 128;
-  static constexpr uint32_t COL_DQ = ALIAS ? COL_DP : COL_DP + 128;
+  static constexpr uint32_t COL_S0 = 2 * D;                 // + 128 h: S_h^T
+  static constexpr uint32_t COL_HALF = 128;                 // columns per half
+  static constexpr uint32_t DP_OFF = 64;                    // dP_h^T after S_h^T
+  static constexpr uint32_t P_OFF = 16;                     // P_h^T inside S_h^T
   static constexpr int OFF_K = 0;
   static constexpr int OFF_V = OFF_K + TILE_BYTES;
   static constexpr int OFF_Q = OFF_V + TILE_BYTES;
   static constexpr int OFF_DO = OFF_Q + NQS * TILE_BYTES;
-  static constexpr int OFF_DS = OFF_DO + NQS * TILE_BYTES;  // 2 panels of 64 queries
-  static constexpr int DS_BYTES = 2 * CHUNK_BYTES;
-  static constexpr int OFF_ROW = OFF_DS + DS_BYTES;          // per stage: lse2[128], dd[128]
+  static constexpr int OFF_DS = OFF_DO + NQS * TILE_BYTES;  // + 16 KB h: dS_h
+  static constexpr int DS_HALF_BYTES = 128 * 128;           // 128 keys x 64 queries
+  static constexpr int OFF_ROW = OFF_DS + 2 * DS_HALF_BYTES; // per stage: lse2[128], dd[128]
   static constexpr int ROW_BYTES = 1024;
   static constexpr int OFF_BAR = OFF_ROW + NQS * ROW_BYTES;
-  // kv, qfull[NQS], qempty[NQS], sfull, pfull, dqfull, dqfree, bdone, fin
-  static constexpr int NBAR = 1 + 2 * NQS + 6;
+  // kv, qfull[NQS], qempty[NQS], then per half: sfull, pfull, dqfull,
+  // dqfree, hdone; fin
+  static constexpr int NBAR = 1 + 2 * NQS + 2 * 5 + 1;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;       // tmem base, abort flag
   static constexpr int USED = OFF_MISC + 16;
   static constexpr int MAX_SMEM = 227 * 1024;
   static constexpr int SMEM_BYTES = USED + 1024 <= MAX_SMEM ? USED + 1024 : MAX_SMEM;
   static constexpr int THREADS = 320;
   static_assert(D == 64 || D == 128, "head dim");
-  static_assert(COL_DQ + D <= TMEM_COLS, "tensor memory budget");
+  static_assert(COL_S0 + 2 * COL_HALF <= TMEM_COLS, "tensor memory budget");
   static_assert(USED + 16 <= SMEM_BYTES, "shared memory budget");
 };
 
@@ -115,12 +116,12 @@ __global__ void __launch_bounds__(320, 1)
   const uint32_t bKV = sbase + C::OFF_BAR;
   const uint32_t bQfull = bKV + 8;                 // + 8*stage
   const uint32_t bQempty = bQfull + 8 * C::NQS;    // + 8*stage
-  const uint32_t bSfull = bQempty + 8 * C::NQS;
-  const uint32_t bPfull = bSfull + 8;
-  const uint32_t bDQfull = bPfull + 8;
-  const uint32_t bDQfree = bDQfull + 8;
-  const uint32_t bBdone = bDQfree + 8;
-  const uint32_t bFin = bBdone + 8;
+  const uint32_t bSfull = bQempty + 8 * C::NQS;    // + 8*half
+  const uint32_t bPfull = bSfull + 16;             // + 8*half
+  const uint32_t bDQfull = bPfull + 16;            // + 8*half
+  const uint32_t bDQfree = bDQfull + 16;           // + 8*half
+  const uint32_t bHdone = bDQfree + 16;            // + 8*half
+  const uint32_t bFin = bHdone + 16;
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::OFF_MISC);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::OFF_MISC + 4);
 
@@ -140,11 +141,14 @@ __global__ void __launch_bounds__(320, 1)
       mbar_init(bQfull + 8 * s, 1);
       mbar_init(bQempty + 8 * s, 1);
     }
-    mbar_init(bSfull, 1);
-    mbar_init(bPfull, 256);
-    mbar_init(bDQfull, 1);
-    mbar_init(bDQfree, 256);
-    mbar_init(bBdone, 1);
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      mbar_init(bSfull + 8 * h, 1);
+      mbar_init(bPfull + 8 * h, 256);
+      mbar_init(bDQfull + 8 * h, 1);
+      mbar_init(bDQfree + 8 * h, 256);
+      mbar_init(bHdone + 8 * h, 1);
+    }
     mbar_init(bFin, 1);
     *abort_flag = 0;
     fence_barrier_init();
@@ -211,74 +215,73 @@ __global__ void __launch_bounds__(320, 1)
     // ------------------------------------------------------------ UMMA issuer
     w.role = kStatusMma;
     if (lane == 0 && n_it > 0) {
-      constexpr uint32_t kFmt = HALF ? 0u : 1u;                         // f16 / bf16
-      constexpr uint32_t kIdescT = make_idesc(kFmt, 128, 128, 0u, 0u);  // S^T, dP^T
-      constexpr uint32_t kIdescAcc = make_idesc(kFmt, 128, D, 0u, 1u);  // dV
-      // dQ: M = 128 queries, N = D; dQ^T: M = 128 = D, N = 128 queries
-      constexpr uint32_t kIdescDQ = make_idesc(kFmt, 128, C::DQT ? 128 : D, 1u, 1u);
-      constexpr uint32_t kIdescDK = make_idesc(kFmt, 128, D, 0u, 1u);  // dK
+      constexpr uint32_t kFmt = HALF ? 0u : 1u;                        // f16 / bf16
+      constexpr uint32_t kIdescS = make_idesc(kFmt, 128, C::HQ, 0u, 0u); // S^T, dP^T
+      constexpr uint32_t kIdescAcc = make_idesc(kFmt, 128, D, 0u, 1u);   // dV, dK
+      constexpr uint32_t kIdescDQ = make_idesc(kFmt, 128, C::HQ, 1u, 1u); // dQ^T
       bool ok = bounded_wait(bKV, 0, w);
       for (int it = 0; ok && it < n_it; ++it) {
         const int s = it % C::NQS;
         if (!(ok = bounded_wait(bQfull + 8 * s, (it / C::NQS) & 1, w))) break;
-        // S^T overwrites P^T of the previous tile, and the softmax rewrites dS
-        // in shared memory after it: the previous products must be complete.
-        if (it > 0 && !(ok = bounded_wait(bBdone, (it - 1) & 1, w))) break;
-        tc_fence_after();
         const uint32_t qb = sQ + s * C::TILE_BYTES, db = sDO + s * C::TILE_BYTES;
+        // S_h^T and dP_h^T for both halves.  S_h^T overwrites P_h^T of the
+        // previous tile (and dS_h is rewritten after it): that tile's products
+        // of half h must be complete.  dP_h^T overwrites its dQ_h^T, which
+        // must have been drained.
 #pragma unroll
-        for (int kk = 0; kk < D / C::UK; ++kk) {
-          const uint32_t off = (kk >> 2) * C::CHUNK_BYTES + (kk & 3) * 32;
-          umma_ss<false>(tmem + C::COL_S, sdesc_sw128(sK + off, 16, 1024),
-                         sdesc_sw128(qb + off, 16, 1024), kIdescT, kk > 0 ? 1u : 0u);
-        }
-        // D = 128: dP^T overwrites the previous dQ, which must be drained.
-        if (C::ALIAS && it > 0) {
-          if (!(ok = bounded_wait(bDQfree, (it - 1) & 1, w))) break;
+        for (int h = 0; h < 2; ++h) {
+          const uint32_t col = C::COL_S0 + h * C::COL_HALF;
+          if (it > 0 && !(ok = bounded_wait(bHdone + 8 * h, (it - 1) & 1, w))) break;
           tc_fence_after();
-        }
 #pragma unroll
-        for (int kk = 0; kk < D / C::UK; ++kk) {
-          const uint32_t off = (kk >> 2) * C::CHUNK_BYTES + (kk & 3) * 32;
-          umma_ss<false>(tmem + C::COL_DP, sdesc_sw128(sV + off, 16, 1024),
-                         sdesc_sw128(db + off, 16, 1024), kIdescT, kk > 0 ? 1u : 0u);
-        }
-        tc_commit(bSfull);
-        if (!(ok = bounded_wait(bPfull, it & 1, w))) break;
-        tc_fence_after();
-        // dV += P^T dO: 16 queries per UMMA (8 packed TMEM columns of A; 16
-        // rows of 128 bytes of the MN-major B).
-#pragma unroll
-        for (int kk = 0; kk < BM / C::UK; ++kk)
-          umma_ts<false>(tmem + C::COL_DV, tmem + C::COL_P + kk * 8,
-                         sdesc_sw128(db + kk * C::UK * 128, C::CHUNK_BYTES, 1024), kIdescAcc,
-                         (it > 0 || kk > 0) ? 1u : 0u);
-        // dK += dS^T Q: A = dS rows (keys) K-major, 16 queries = 32 bytes per
-        // UMMA, two 64-query panels.
-#pragma unroll
-        for (int kk = 0; kk < BM / C::UK; ++kk)
-          umma_ss<false>(tmem + C::COL_DK,
-                         sdesc_sw128(sDS + (kk >> 2) * C::CHUNK_BYTES + (kk & 3) * 32, 16, 1024),
-                         sdesc_sw128(qb + kk * C::UK * 128, C::CHUNK_BYTES, 1024), kIdescDK,
-                         (it > 0 || kk > 0) ? 1u : 0u);
-        if (!C::ALIAS && it > 0) {
-          if (!(ok = bounded_wait(bDQfree, (it - 1) & 1, w))) break;
+          for (int kk = 0; kk < D / C::UK; ++kk) {
+            const uint32_t off = (kk >> 2) * C::CHUNK_BYTES + (kk & 3) * 32;
+            umma_ss<false>(tmem + col, sdesc_sw128(sK + off, 16, 1024),
+                           sdesc_sw128(qb + h * C::HQ * 128 + off, 16, 1024), kIdescS,
+                           kk > 0 ? 1u : 0u);
+          }
+          if (it > 0 && !(ok = bounded_wait(bDQfree + 8 * h, (it - 1) & 1, w))) break;
           tc_fence_after();
-        }
-        // dQ_i = dS K_j, or for D = 128 its transpose K_j^T dS^T: 16 keys per
-        // UMMA; dS (two 64-query panels) and K_j are both read MN-major.
 #pragma unroll
-        for (int kk = 0; kk < BN / C::UK; ++kk) {
-          const uint64_t ds_desc = sdesc_sw128(sDS + kk * C::UK * 128, C::CHUNK_BYTES, 1024);
-          const uint64_t k_desc = sdesc_sw128(sK + kk * C::UK * 128, C::CHUNK_BYTES, 1024);
-          if constexpr (C::DQT)
-            umma_ss<false>(tmem + C::COL_DQ, k_desc, ds_desc, kIdescDQ, kk > 0 ? 1u : 0u);
-          else
-            umma_ss<false>(tmem + C::COL_DQ, ds_desc, k_desc, kIdescDQ, kk > 0 ? 1u : 0u);
+          for (int kk = 0; kk < D / C::UK; ++kk) {
+            const uint32_t off = (kk >> 2) * C::CHUNK_BYTES + (kk & 3) * 32;
+            umma_ss<false>(tmem + col + C::DP_OFF, sdesc_sw128(sV + off, 16, 1024),
+                           sdesc_sw128(db + h * C::HQ * 128 + off, 16, 1024), kIdescS,
+                           kk > 0 ? 1u : 0u);
+          }
+          tc_commit(bSfull + 8 * h);
+        }
+        if (!ok) break;
+        // The products of each half once its P^T and dS are written.
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const uint32_t col = C::COL_S0 + h * C::COL_HALF;
+          if (!(ok = bounded_wait(bPfull + 8 * h, it & 1, w))) break;
+          tc_fence_after();
+          const uint32_t ds = sDS + h * C::DS_HALF_BYTES;
+          // dV += P_h^T dO_h and dK += dS_h^T Q_h: 16 queries per UMMA (8
+          // packed TMEM columns of P^T, 32 bytes of a dS row; 16 rows of
+          // 128 bytes of the MN-major B).
+#pragma unroll
+          for (int kk = 0; kk < C::HQ / C::UK; ++kk) {
+            const uint32_t brow = (h * C::HQ + kk * C::UK) * 128;
+            const uint32_t acc = (it > 0 || h > 0 || kk > 0) ? 1u : 0u;
+            umma_ts<false>(tmem + C::COL_DV, tmem + col + C::P_OFF + kk * 8,
+                           sdesc_sw128(db + brow, C::CHUNK_BYTES, 1024), kIdescAcc, acc);
+            umma_ss<false>(tmem + C::COL_DK, sdesc_sw128(ds + kk * 32, 16, 1024),
+                           sdesc_sw128(qb + brow, C::CHUNK_BYTES, 1024), kIdescAcc, acc);
+          }
+          // dQ_h^T = K_j^T dS_h^T over dP_h^T: 16 keys per UMMA.
+#pragma unroll
+          for (int kk = 0; kk < BN / C::UK; ++kk)
+            umma_ss<false>(tmem + col + C::DP_OFF,
+                           sdesc_sw128(sK + kk * C::UK * 128, C::CHUNK_BYTES, 1024),
+                           sdesc_sw128(ds + kk * C::UK * 128, C::CHUNK_BYTES, 1024), kIdescDQ,
+                           kk > 0 ? 1u : 0u);
+          tc_commit(bHdone + 8 * h);
+          tc_commit(bDQfull + 8 * h);
         }
         tc_commit(bQempty + 8 * s);
-        tc_commit(bBdone);
-        tc_commit(bDQfull);
       }
       (void)ok;
       tc_commit(bFin);
@@ -288,36 +291,33 @@ __global__ void __launch_bounds__(320, 1)
   } else {
     // ------------------------------------------------------------ softmax warps
     w.role = kStatusSoftmax;
-    const int g = warp >> 2;                  // query half of the tile
+    const int g = warp >> 2;                  // query quarter within a half
     const int wq = warp & 3;
-    const int r = wq * 32 + lane;             // TMEM lane: key (S^T) or query (dQ)
+    const int r = wq * 32 + lane;             // TMEM lane: key (S^T) or head dim (dQ^T)
     const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
-    const int cb = 64 * g;                    // first query column of this half
+    const int cq = 32 * g;                    // first query column of this quarter
     const float sl2 = p.scale_log2;
     const uint64_t sl2_2 = pk2(sl2, sl2);
     const uint64_t sc_2 = pk2(p.scale, p.scale);
-    uint8_t *ds_row = smem + C::OFF_DS + g * C::CHUNK_BYTES + r * 128;
     bool ok = true;
     for (int it = 0; ok && it < n_it; ++it) {
       const int s = it % C::NQS;
       const int qt = i_first + it;
       ok = __all_sync(kFullMask, bounded_wait(bQfull + 8 * s, (it / C::NQS) & 1, w));
-      if (ok) ok = __all_sync(kFullMask, bounded_wait(bSfull, it & 1, w));
       if (!ok) break;
-      tc_fence_after();
       const float *lse2 = reinterpret_cast<const float *>(smem + C::OFF_ROW + s * C::ROW_BYTES);
       const float *dd = lse2 + 128;
       const bool diag = CAUSAL && qt == jt;   // key r sees query c only if r <= c
 #pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {
-        // P^T of query half g lands in columns 32 + 32g .. of S^T: half 0
-        // handles its upper 32 queries first, so no column is written before
-        // this thread has read it.
-        const int h = g == 0 ? 1 - hh : hh;
-        const int c0 = cb + 32 * h;
+      for (int h = 0; h < 2; ++h) {
+        const uint32_t col = C::COL_S0 + h * C::COL_HALF;
+        ok = __all_sync(kFullMask, bounded_wait(bSfull + 8 * h, it & 1, w));
+        if (!ok) break;
+        tc_fence_after();
+        const int c0 = h * C::HQ + cq;          // query index in the tile of column 0
         uint32_t sr[32], dr[32];
-        tmem_ld32(tmem + lane_off + C::COL_S + c0, sr);
-        tmem_ld32(tmem + lane_off + C::COL_DP + c0, dr);
+        tmem_ld32(tmem + lane_off + col + cq, sr);
+        tmem_ld32(tmem + lane_off + col + C::DP_OFF + cq, dr);
         tmem_ld_wait();
         reg_fence32(sr);
         reg_fence32(dr);
@@ -348,74 +348,62 @@ __global__ void __launch_bounds__(320, 1)
             dsp[c >> 1] = HALF ? pack_f16x2(s0, s1) : pack_bf16x2(s0, s1);
           }
         }
-        tmem_st16(tmem + lane_off + C::COL_P + (c0 >> 1), pp);
-        // dS row r of panel g: 16-byte unit u holds queries 8u..8u+7 of the
-        // half; this chunk is units 4h..4h+3.
+        // P^T columns 16 + 16g ..: inside the 32 columns this quarter read.
+        tmem_st16(tmem + lane_off + col + C::P_OFF + 16 * g, pp);
+        // dS_h row r: 16-byte unit u holds queries 8u..8u+7 of the half; this
+        // quarter's 32 queries are units 4g..4g+3.
+        uint8_t *ds_row = smem + C::OFF_DS + h * C::DS_HALF_BYTES + r * 128;
 #pragma unroll
         for (int u = 0; u < 4; ++u)
-          *reinterpret_cast<uint4 *>(ds_row + (((4 * h + u) ^ (r & 7)) << 4)) =
+          *reinterpret_cast<uint4 *>(ds_row + (((4 * g + u) ^ (r & 7)) << 4)) =
               make_uint4(dsp[4 * u], dsp[4 * u + 1], dsp[4 * u + 2], dsp[4 * u + 3]);
+        fence_proxy_async_smem();
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(bPfull + 8 * h);
       }
-      fence_proxy_async_smem();
-      tmem_st_wait();
-      tc_fence_before();
-      mbar_arrive(bPfull);
-
-      // dQ_i -> dq_acc with fp32 atomic adds.
-      ok = __all_sync(kFullMask, bounded_wait(bDQfull, it & 1, w));
       if (!ok) break;
-      tc_fence_after();
-      if constexpr (C::DQT) {
-        // dQ^T: lane r = head-dim index, columns = this half's 64 queries; the
-        // warp's 32 lanes add to 32 consecutive floats of one dQ row.
-        const int qbase = qt * BM + cb;
-        float *dst = p.dq_acc + (static_cast<size_t>(bh) * p.Nq + qbase) * D + r;
+
+      // dQ_h^T -> dq_acc with fp32 atomic adds: lane r = head-dim index,
+      // this quarter's 32 queries of the half; the warp's 32 lanes add to 32
+      // consecutive floats of one dQ row.  (D = 64: lanes 64-127 hold no dQ.)
 #pragma unroll
-        for (int c = 0; c < 64; c += 32) {
+      for (int h = 0; h < 2; ++h) {
+        const uint32_t col = C::COL_S0 + h * C::COL_HALF;
+        ok = __all_sync(kFullMask, bounded_wait(bDQfull + 8 * h, it & 1, w));
+        if (!ok) break;
+        tc_fence_after();
+        if (r < D) {   // whole warps
           uint32_t v[32];
-          tmem_ld32(tmem + lane_off + C::COL_DQ + cb + c, v);
+          tmem_ld32(tmem + lane_off + col + C::DP_OFF + cq, v);
           tmem_ld_wait();
           reg_fence32(v);
+          const int qbase = qt * BM + h * C::HQ + cq;
+          float *dst = p.dq_acc + (static_cast<size_t>(bh) * p.Nq + qbase) * D + r;
 #pragma unroll
           for (int i = 0; i < 32; ++i)
-            if (qbase + c + i < p.Nq) red_add(dst + static_cast<size_t>(c + i) * D, __uint_as_float(v[i]));
+            if (qbase + i < p.Nq) red_add(dst + static_cast<size_t>(i) * D, __uint_as_float(v[i]));
         }
-      } else {
-        // dQ: lane r = query row, columns = this half of d.
-        const int qrow = qt * BM + r;
-        float *dst = p.dq_acc + (static_cast<size_t>(bh) * p.Nq + qrow) * D + g * (D / 2);
-#pragma unroll
-        for (int c = 0; c < D / 2; c += 32) {
-          uint32_t v[32];
-          tmem_ld32(tmem + lane_off + C::COL_DQ + g * (D / 2) + c, v);
-          tmem_ld_wait();
-          reg_fence32(v);
-          if (qrow < p.Nq) {
-#pragma unroll
-            for (int u = 0; u < 8; ++u)
-              red_add_v4(dst + c + 4 * u, __uint_as_float(v[4 * u]), __uint_as_float(v[4 * u + 1]),
-                         __uint_as_float(v[4 * u + 2]), __uint_as_float(v[4 * u + 3]));
-          }
-        }
+        tc_fence_before();
+        mbar_arrive(bDQfree + 8 * h);
       }
-      tc_fence_before();
-      mbar_arrive(bDQfree);
     }
 
     // ---------------------------------------------------------- dV, dK out
-    // Query half 0 writes dV, half 1 writes dK (row r = key k0 + r).
-    if (ok && n_it > 0) ok = __all_sync(kFullMask, bounded_wait(bBdone, (n_it - 1) & 1, w));
+    // Quarter 0 writes dV, quarter 1 writes dK (row r = key k0 + r).  The
+    // last tile's half-1 products complete after every earlier UMMA.
+    if (ok && n_it > 0) ok = __all_sync(kFullMask, bounded_wait(bHdone + 8, (n_it - 1) & 1, w));
     if (ok) {
       tc_fence_after();
       const int key = k0 + r;
       uint8_t *dst = static_cast<uint8_t *>(g == 0 ? p.dv : p.dk) +
                      (static_cast<size_t>(bh) * p.Nk + key) * D * 2;
-      const uint32_t col = g == 0 ? C::COL_DV : C::COL_DK;
+      const uint32_t colv = g == 0 ? C::COL_DV : C::COL_DK;
 #pragma unroll
       for (int c = 0; c < D; c += 32) {
         uint32_t v[32];
         if (n_it > 0) {
-          tmem_ld32(tmem + lane_off + col + c, v);
+          tmem_ld32(tmem + lane_off + colv + c, v);
           tmem_ld_wait();
           reg_fence32(v);
         } else {
