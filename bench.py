@@ -41,11 +41,23 @@ METRIC = "attn fwd TFLOP/s (4·B·H·N²·d, ½ if causal) and % of GB300 dense 
 METRIC_BWD = "attn bwd TFLOP/s (10·B·H·N²·d, ½ if causal) and % of GB300 dense peak"
 
 
-def kernel_source_hash() -> str:
+# Sources a kernel's behaviour depends on: its template, instantiation,
+# shared headers and the host code that encodes its tensor maps and launches.
+KERNEL_SOURCES = {
+    "fa_tc_fwd_kernel": ["fa_tc.cuh", "fa_tc_bf16_d128.cu", "fa_tc_bf16_d64.cu", "fa_tc_f16_d128.cu",
+                         "fa_tc_f16_d64.cu", "fa_tc_f32_d64.cu"],
+    "fa_bwd": ["fa_bwd.cuh", "fa_bwd_bf16.cu", "fa_bwd_f16.cu", "fa_bwd_aux.cu"],
+}
+COMMON_SOURCES = ["ptx.cuh", "fa_wait.cuh", "fa_internal.h", "fa_api.cu"]
+
+
+def kernel_source_hash(kernel: str) -> str:
+    """Hash of the sources of the kernel family named by the key's prefix."""
+    fam = next(f for f in KERNEL_SOURCES if kernel.startswith(f))
     h = hashlib.sha256()
-    for p in sorted(glob.glob(os.path.join(ROOT, "exact_attention_57_gb300", "csrc", "*"))):
-        with open(p, "rb") as f:
-            h.update(os.path.basename(p).encode())
+    for name in sorted(KERNEL_SOURCES[fam] + COMMON_SOURCES):
+        with open(os.path.join(ROOT, "exact_attention_57_gb300", "csrc", name), "rb") as f:
+            h.update(name.encode())
             h.update(f.read())
     return h.hexdigest()[:16]
 
@@ -67,7 +79,7 @@ def profiled_traffic(kernel: str, workload: str):
     with open(path) as f:
         rec = json.load(f)
     ent = rec.get(kernel, {}).get(workload)
-    if not ent or ent.get("source_hash") != kernel_source_hash():
+    if not ent or ent.get("source_hash") != kernel_source_hash(kernel):
         return None
     return ent.get("dram_bytes_per_launch")
 
@@ -386,9 +398,10 @@ def main():
     kname = {0: "fa_tc_fwd_kernel<bf16>", 1: "fa_tc_fwd_kernel<tf32>",
              2: "fa_simt_fwd_kernel", 3: "fa_tc_fwd_kernel<f16>"}[w.dtype]
     if bwd:
-        # The step's three launches are timed together, so `achieved` is a
-        # lower bound for the gradient kernel alone.
-        kname = "fa_bwd (prep + fa_bwd_kernel + dq rounding)"
+        # The step's three launches (prep, gradient kernel, dq rounding) are
+        # timed together, so `achieved` is a lower bound for the gradient
+        # kernel alone; `traffic` is the gradient kernel's.
+        kname = {0: "fa_bwd_kernel<bf16>", 3: "fa_bwd_kernel<f16>"}[w.dtype]
     traffic = profiled_traffic(kname, w.name)
     roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                 "frac": achieved / peak, "traffic": traffic,
