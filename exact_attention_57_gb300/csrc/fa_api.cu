@@ -60,7 +60,7 @@ int validate(const void *q, const void *k, const void *v, const void *o, const f
       overlap(lse, ln, v, kn))
     return FA_ERR_INVALID_ARG;
   // The compiled set of kernels.
-  if ((dtype == FA_DTYPE_BF16 || dtype == FA_DTYPE_F16) && d != 64 && d != 128)
+  if ((dtype == FA_DTYPE_BF16 || dtype == FA_DTYPE_F16) && d != 64 && d != 128 && d != 256)
     return FA_ERR_UNSUPPORTED;
   if (dtype == FA_DTYPE_F32 && d != 64) return FA_ERR_UNSUPPORTED;
   if (dtype == FA_DTYPE_F32_SIMT && d > 128) return FA_ERR_UNSUPPORTED;
@@ -130,6 +130,22 @@ int encode_map(CUtensorMap *map, const void *base, int dtype, int BH, int N, int
 
 int ceil_div(int a, int b) { return (a + b - 1) / b; }
 
+// The tensor-core forward instantiation for (dtype, d); the combination has
+// been checked by validate().
+cudaError_t launch_tc_any(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv,
+                          const CUtensorMap &mo, const fa::TcParams &p, int B, int causal, int d,
+                          int dtype, cudaStream_t s) {
+  if (dtype == FA_DTYPE_F16)
+    return d == 64    ? fa::launch_tc_f16_d64(mq, mk, mv, mo, p, B, causal, s)
+           : d == 128 ? fa::launch_tc_f16_d128(mq, mk, mv, mo, p, B, causal, s)
+                      : fa::launch_tc_f16_d256(mq, mk, mv, mo, p, B, causal, s);
+  if (dtype == FA_DTYPE_BF16)
+    return d == 64    ? fa::launch_tc_bf16_d64(mq, mk, mv, mo, p, B, causal, s)
+           : d == 128 ? fa::launch_tc_bf16_d128(mq, mk, mv, mo, p, B, causal, s)
+                      : fa::launch_tc_bf16_d256(mq, mk, mv, mo, p, B, causal, s);
+  return fa::launch_tc_f32_d64(mq, mk, mv, mo, p, B, causal, s);
+}
+
 // The tensor-core kernels take |scale| * log2(e) > 0 and apply a negative
 // scale by negating Q inside the S = Q K^T product.  A zero scale becomes
 // 1e-30: for scores below 1e20 in magnitude every exponent is then below
@@ -197,15 +213,7 @@ int fa_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int
   p.wait_limit_ns = lim ? lim : fa::kDefaultWaitLimitNs;
   p.skip_v_load = g_skip_v_load.load();
 
-  cudaError_t e;
-  if (dtype == FA_DTYPE_F16)
-    e = (d == 64) ? fa::launch_tc_f16_d64(mq, mk, mv, mo, p, B, causal, s)
-                  : fa::launch_tc_f16_d128(mq, mk, mv, mo, p, B, causal, s);
-  else if (dtype == FA_DTYPE_BF16)
-    e = (d == 64) ? fa::launch_tc_bf16_d64(mq, mk, mv, mo, p, B, causal, s)
-                  : fa::launch_tc_bf16_d128(mq, mk, mv, mo, p, B, causal, s);
-  else
-    e = fa::launch_tc_f32_d64(mq, mk, mv, mo, p, B, causal, s);
+  cudaError_t e = launch_tc_any(mq, mk, mv, mo, p, B, causal, d, dtype, s);
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
@@ -385,15 +393,7 @@ extern "C" int fa_fwd_noalloc(const void *q, const void *k, const void *v, void 
     const unsigned long long lim = g_wait_limit_ns.load();
     p.wait_limit_ns = lim ? lim : fa::kDefaultWaitLimitNs;
     p.skip_v_load = g_skip_v_load.load();
-    cudaError_t e;
-    if (dtype == FA_DTYPE_F16)
-      e = (d == 64) ? fa::launch_tc_f16_d64(mq, mk, mv, mo, p, B, causal, s)
-                    : fa::launch_tc_f16_d128(mq, mk, mv, mo, p, B, causal, s);
-    else if (dtype == FA_DTYPE_BF16)
-      e = (d == 64) ? fa::launch_tc_bf16_d64(mq, mk, mv, mo, p, B, causal, s)
-                    : fa::launch_tc_bf16_d128(mq, mk, mv, mo, p, B, causal, s);
-    else
-      e = fa::launch_tc_f32_d64(mq, mk, mv, mo, p, B, causal, s);
+    cudaError_t e = launch_tc_any(mq, mk, mv, mo, p, B, causal, d, dtype, s);
     if (e != cudaSuccess) return FA_ERR_CUDA;
   }
   if (device_status == nullptr) return FA_OK;
@@ -515,15 +515,7 @@ extern "C" int fa_fwd_splitkv(const void *q, const void *k, const void *v, void 
   p.n_splits = nsp;
   p.ws_o = ws_o;
   p.ws_lse = ws_lse;
-  cudaError_t e;
-  if (dtype == FA_DTYPE_F16)
-    e = (d == 64) ? fa::launch_tc_f16_d64(mq, mk, mv, mo, p, B, causal, s)
-                  : fa::launch_tc_f16_d128(mq, mk, mv, mo, p, B, causal, s);
-  else if (dtype == FA_DTYPE_BF16)
-    e = (d == 64) ? fa::launch_tc_bf16_d64(mq, mk, mv, mo, p, B, causal, s)
-                  : fa::launch_tc_bf16_d128(mq, mk, mv, mo, p, B, causal, s);
-  else
-    e = fa::launch_tc_f32_d64(mq, mk, mv, mo, p, B, causal, s);
+  cudaError_t e = launch_tc_any(mq, mk, mv, mo, p, B, causal, d, dtype, s);
   if (e != cudaSuccess) return FA_ERR_CUDA;
   e = fa::launch_splitkv_combine(ws_o, ws_lse, o, lse, BH, Nq, d, n_ktiles, nsp, causal, dtype, s);
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
@@ -597,15 +589,7 @@ extern "C" int fa_fwd_varlen(const void *q, const void *k, const void *v, void *
   p.cu_q = cu_seqlens_q;
   p.cu_k = cu_seqlens_k;
   p.total_q = total_q;
-  cudaError_t e;
-  if (dtype == FA_DTYPE_F16)
-    e = (d == 64) ? fa::launch_tc_f16_d64(mq, mk, mv, mo, p, B, causal, s)
-                  : fa::launch_tc_f16_d128(mq, mk, mv, mo, p, B, causal, s);
-  else if (dtype == FA_DTYPE_BF16)
-    e = (d == 64) ? fa::launch_tc_bf16_d64(mq, mk, mv, mo, p, B, causal, s)
-                  : fa::launch_tc_bf16_d128(mq, mk, mv, mo, p, B, causal, s);
-  else
-    e = fa::launch_tc_f32_d64(mq, mk, mv, mo, p, B, causal, s);
+  cudaError_t e = launch_tc_any(mq, mk, mv, mo, p, B, causal, d, dtype, s);
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
@@ -665,6 +649,7 @@ extern "C" int fa_bwd(const void *q, const void *k, const void *v, const void *o
       if (overlap(out[a].p, out[a].n, out[b].p, out[b].n)) return FA_ERR_INVALID_ARG;
   }
   if (dtype != FA_DTYPE_BF16 && dtype != FA_DTYPE_F16) return FA_ERR_UNSUPPORTED;
+  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;  // dK, dV of d = 256 do not fit in TMEM
 
   unsigned *status = nullptr;
   if ((rc = device_setup(&status)) != FA_OK) return rc;

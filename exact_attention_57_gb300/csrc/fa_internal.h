@@ -79,6 +79,12 @@ cudaError_t launch_tc_f16_d64(const CUtensorMap &q, const CUtensorMap &k, const 
 cudaError_t launch_tc_f16_d128(const CUtensorMap &q, const CUtensorMap &k, const CUtensorMap &v,
                                const CUtensorMap &o, const TcParams &p, int B, int causal,
                                cudaStream_t s);
+cudaError_t launch_tc_bf16_d256(const CUtensorMap &q, const CUtensorMap &k, const CUtensorMap &v,
+                                const CUtensorMap &o, const TcParams &p, int B, int causal,
+                                cudaStream_t s);
+cudaError_t launch_tc_f16_d256(const CUtensorMap &q, const CUtensorMap &k, const CUtensorMap &v,
+                               const CUtensorMap &o, const TcParams &p, int B, int causal,
+                               cudaStream_t s);
 
 // Merge of the split-mode chunks into o (dtype: bf16, f16 or f32) and lse.
 cudaError_t launch_splitkv_combine(const float *ws_o, const float *ws_lse, void *o, float *lse,

@@ -106,9 +106,14 @@ cudaError_t launch_splitkv_combine(const float *ws_o, const float *ws_lse, void 
       return launch_combine<64, FA_DTYPE_F16>(ws_o, ws_lse, o, lse, BH, Nq, n_ktiles, nsp, causal, s);
     return launch_combine<64, FA_DTYPE_F32>(ws_o, ws_lse, o, lse, BH, Nq, n_ktiles, nsp, causal, s);
   }
+  if (d == 128) {
+    if (dtype == FA_DTYPE_BF16)
+      return launch_combine<128, FA_DTYPE_BF16>(ws_o, ws_lse, o, lse, BH, Nq, n_ktiles, nsp, causal, s);
+    return launch_combine<128, FA_DTYPE_F16>(ws_o, ws_lse, o, lse, BH, Nq, n_ktiles, nsp, causal, s);
+  }
   if (dtype == FA_DTYPE_BF16)
-    return launch_combine<128, FA_DTYPE_BF16>(ws_o, ws_lse, o, lse, BH, Nq, n_ktiles, nsp, causal, s);
-  return launch_combine<128, FA_DTYPE_F16>(ws_o, ws_lse, o, lse, BH, Nq, n_ktiles, nsp, causal, s);
+    return launch_combine<256, FA_DTYPE_BF16>(ws_o, ws_lse, o, lse, BH, Nq, n_ktiles, nsp, causal, s);
+  return launch_combine<256, FA_DTYPE_F16>(ws_o, ws_lse, o, lse, BH, Nq, n_ktiles, nsp, causal, s);
 }
 
 }  // namespace fa

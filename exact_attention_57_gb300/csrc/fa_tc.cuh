@@ -41,7 +41,9 @@
 // tf32.  kind::tf32 takes its B operand K-major only, so the softmax warps
 // also transpose each V_j into a tf32 V_j^T buffer (d rows of 128 keys).
 // Tensor memory: S_b cols [128b, 128b+128) for b < NS, then O (D cols), then Q
-// when it fits (bf16 D=64, fp32 D=64); bf16 D=128 keeps Q in shared memory.
+// when it fits (bf16 D=64, fp32 D=64); bf16 D=128 and D=256 keep Q in shared
+// memory.  D=256 has two score buffers and single-stage K/V rings (64 KB
+// tiles).
 //
 // Rescaling: the running max used as the exponent offset only moves when a
 // row's max grows by more than 2^8; otherwise the stale offset is kept.  The
@@ -74,7 +76,7 @@ struct TcCfg {
   // Score buffers in tensor memory: S_j lives in buffer j % NS; S_j may be
   // issued once P_{j-NS} V_{j-NS} is done, so NS - 1 score tiles can be
   // computed ahead of the softmax.
-  static constexpr int NS = TF32 ? 2 : 3;
+  static constexpr int NS = (TF32 || D >= 256) ? 2 : 3;
   static constexpr uint32_t TMEM_COLS = 512;
   static constexpr uint32_t COL_O = NS * 128;               // O after the score buffers
   static constexpr int Q_COLS = D * ESZ / 4;                // 32-bit columns of one Q row
@@ -83,8 +85,10 @@ struct TcCfg {
   static constexpr bool QTMEM = COL_O + D + Q_COLS <= TMEM_COLS;
   static constexpr uint32_t COL_Q = COL_O + D;
   static constexpr int NQ = QTMEM ? 0 : 1;                  // Q tiles in shared memory
-  static constexpr int KST = TF32 ? 2 : (TILE_BYTES <= 16384 ? 4 : 3); // K ring depth
-  static constexpr int VST = TF32 ? 2 : (TILE_BYTES <= 16384 ? 4 : 3); // V ring depth
+  // K / V ring depths: as deep as shared memory allows (64 KB tiles at
+  // D = 256 leave room for one stage each beside Q).
+  static constexpr int KST = TF32 ? 2 : (TILE_BYTES <= 16384 ? 4 : TILE_BYTES <= 32768 ? 3 : 1);
+  static constexpr int VST = KST;
   // fp32 path: V_j is transposed by the softmax warps into a K-major copy
   // (V^T, d rows of 128 keys, tf32-rounded) because P V runs as kind::tf32
   // with V^T as a K-major B operand.  Two copies alternate.

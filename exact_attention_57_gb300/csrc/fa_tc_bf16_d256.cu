@@ -1,0 +1,13 @@
+// fa_tc_bf16_d256.cu — instantiation of the tensor-core forward for head dim 256,
+// bf16 inputs (tcgen05 kind::f16).
+#include "fa_tc.cuh"
+
+namespace fa {
+
+cudaError_t launch_tc_bf16_d256(const CUtensorMap &q, const CUtensorMap &k, const CUtensorMap &v,
+                         const CUtensorMap &o, const TcParams &p, int B, int causal,
+                         cudaStream_t s) {
+  return launch_tc<256, false>(q, k, v, o, p, B, causal, s);
+}
+
+}  // namespace fa

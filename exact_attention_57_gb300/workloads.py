@@ -92,6 +92,13 @@ PROFILE_WORKLOADS = {
     "b1h8nq128nk65536d128-bf16": Workload(
         "b1h8nq128nk65536d128-bf16", 1, 8, 128, 65536, 128, DTYPE_BF16,
         causal=(False,), seed=57006, note="decode-like: one query tile per head"),
+    # Head dim 256 at the benchmark's per-head FLOPs (half the heads).
+    "b4h16n8192d256-bf16-causal": Workload(
+        "b4h16n8192d256-bf16-causal", 4, 16, 8192, 8192, 256, DTYPE_BF16,
+        causal=(True,), seed=57007, note="head dim 256"),
+    "b4h16n8192d64-bf16-causal": Workload(
+        "b4h16n8192d64-bf16-causal", 4, 16, 8192, 8192, 64, DTYPE_BF16,
+        causal=(True,), seed=57008, note="head dim 64"),
 }
 
 

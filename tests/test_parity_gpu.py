@@ -35,7 +35,7 @@ def _dd(pairs):
 
 @pytest.mark.parametrize("dtype,d", _dd([(DTYPE_BF16, 64), (DTYPE_BF16, 128), (DTYPE_F32, 64),
                                          (DTYPE_F32_SIMT, 64), (DTYPE_F16, 64),
-                                         (DTYPE_F16, 128)]))
+                                         (DTYPE_F16, 128), (DTYPE_BF16, 256), (DTYPE_F16, 256)]))
 @pytest.mark.parametrize("causal", [False, True])
 def test_other_mask_per_dtype(dtype, d, causal):
     """Every kernel variant, causal and not, on a several-tile ragged case."""
@@ -50,7 +50,7 @@ EDGE_N = [1, 2, 127, 128, 129, 255, 256, 257]
 
 @pytest.mark.parametrize("N", EDGE_N)
 @pytest.mark.parametrize("dtype,d", _dd([(DTYPE_BF16, 64), (DTYPE_BF16, 128), (DTYPE_F32, 64),
-                                         (DTYPE_F32_SIMT, 64), (DTYPE_F16, 128)]))
+                                         (DTYPE_F32_SIMT, 64), (DTYPE_F16, 128), (DTYPE_BF16, 256)]))
 def test_edge_lengths(N, dtype, d):
     q, k, v = make_inputs(1, 2, N, N, d, dtype, seed=100 + N)
     for causal in (False, True):
@@ -62,7 +62,7 @@ def test_edge_lengths(N, dtype, d):
 @pytest.mark.parametrize("Nq,Nk", [(200, 77), (77, 200), (1, 1000), (1000, 1), (129, 384),
                                    (384, 129)])
 @pytest.mark.parametrize("dtype,d", _dd([(DTYPE_BF16, 128), (DTYPE_F32, 64), (DTYPE_F32_SIMT, 64),
-                                         (DTYPE_F16, 64)]))
+                                         (DTYPE_F16, 64), (DTYPE_F16, 256)]))
 def test_unequal_lengths(Nq, Nk, dtype, d):
     """Nq != Nk, causal top-left aligned (key j allowed iff j <= i)."""
     q, k, v = make_inputs(2, 1, Nq, Nk, d, dtype, seed=Nq * 7 + Nk)
@@ -74,7 +74,7 @@ def test_unequal_lengths(Nq, Nk, dtype, d):
 
 @pytest.mark.parametrize("scale", [0.0, -0.125, 0.5, 1e-3])
 @pytest.mark.parametrize("dtype,d", _dd([(DTYPE_BF16, 128), (DTYPE_F32, 64), (DTYPE_F32_SIMT, 32),
-                                         (DTYPE_F16, 128)]))
+                                         (DTYPE_F16, 128), (DTYPE_BF16, 256)]))
 def test_scales(scale, dtype, d):
     """Zero and negative scales are valid: scale multiplies q.k before the max."""
     q, k, v = make_inputs(1, 2, 300, 300, d, dtype, seed=5)

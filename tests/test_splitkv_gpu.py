@@ -19,6 +19,7 @@ CASES = [
     (1, 4, 256, 1024, 64, DTYPE_F32),
     (1, 3, 300, 900, 128, DTYPE_F16),
     (2, 4, 128, 4096, 64, DTYPE_BF16),
+    (1, 2, 200, 2000, 256, DTYPE_BF16),
 ]
 
 

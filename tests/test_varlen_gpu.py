@@ -19,6 +19,7 @@ CASES = [
     ([5, 0, 260, 40], [300, 7, 0, 40], 2, 64, DTYPE_F16),
     ([200, 33], [64, 500], 2, 64, DTYPE_F32),
     ([1000, 1, 513], [1000, 2048, 513], 4, 128, DTYPE_BF16),
+    ([130, 257], [300, 129], 2, 256, DTYPE_BF16),
 ]
 
 
