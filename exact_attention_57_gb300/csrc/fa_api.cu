@@ -62,7 +62,7 @@ int validate(const void *q, const void *k, const void *v, const void *o, const f
   // The compiled set of kernels.
   if ((dtype == FA_DTYPE_BF16 || dtype == FA_DTYPE_F16) && d != 64 && d != 128 && d != 256)
     return FA_ERR_UNSUPPORTED;
-  if (dtype == FA_DTYPE_F32 && d != 64) return FA_ERR_UNSUPPORTED;
+  if (dtype == FA_DTYPE_F32 && d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
   if (dtype == FA_DTYPE_F32_SIMT && d > 128) return FA_ERR_UNSUPPORTED;
   return FA_OK;
 }
@@ -143,7 +143,8 @@ cudaError_t launch_tc_any(const CUtensorMap &mq, const CUtensorMap &mk, const CU
     return d == 64    ? fa::launch_tc_bf16_d64(mq, mk, mv, mo, p, B, causal, s)
            : d == 128 ? fa::launch_tc_bf16_d128(mq, mk, mv, mo, p, B, causal, s)
                       : fa::launch_tc_bf16_d256(mq, mk, mv, mo, p, B, causal, s);
-  return fa::launch_tc_f32_d64(mq, mk, mv, mo, p, B, causal, s);
+  return d == 64 ? fa::launch_tc_f32_d64(mq, mk, mv, mo, p, B, causal, s)
+                 : fa::launch_tc_f32_d128(mq, mk, mv, mo, p, B, causal, s);
 }
 
 // The tensor-core kernels take |scale| * log2(e) > 0 and apply a negative

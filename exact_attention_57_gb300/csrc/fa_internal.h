@@ -72,6 +72,9 @@ cudaError_t launch_tc_bf16_d128(const CUtensorMap &q, const CUtensorMap &k, cons
 cudaError_t launch_tc_f32_d64(const CUtensorMap &q, const CUtensorMap &k, const CUtensorMap &v,
                               const CUtensorMap &o, const TcParams &p, int B, int causal,
                               cudaStream_t s);
+cudaError_t launch_tc_f32_d128(const CUtensorMap &q, const CUtensorMap &k, const CUtensorMap &v,
+                               const CUtensorMap &o, const TcParams &p, int B, int causal,
+                               cudaStream_t s);
 
 cudaError_t launch_tc_f16_d64(const CUtensorMap &q, const CUtensorMap &k, const CUtensorMap &v,
                               const CUtensorMap &o, const TcParams &p, int B, int causal,

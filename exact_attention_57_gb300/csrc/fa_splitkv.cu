@@ -96,24 +96,24 @@ cudaError_t launch_combine(const float *ws_o, const float *ws_lse, void *o, floa
 
 }  // namespace
 
+template <int D>
+cudaError_t launch_combine_d(const float *ws_o, const float *ws_lse, void *o, float *lse, int BH,
+                             int Nq, int n_ktiles, int nsp, int causal, int dtype, cudaStream_t s) {
+  if (dtype == FA_DTYPE_BF16)
+    return launch_combine<D, FA_DTYPE_BF16>(ws_o, ws_lse, o, lse, BH, Nq, n_ktiles, nsp, causal, s);
+  if (dtype == FA_DTYPE_F16)
+    return launch_combine<D, FA_DTYPE_F16>(ws_o, ws_lse, o, lse, BH, Nq, n_ktiles, nsp, causal, s);
+  return launch_combine<D, FA_DTYPE_F32>(ws_o, ws_lse, o, lse, BH, Nq, n_ktiles, nsp, causal, s);
+}
+
 cudaError_t launch_splitkv_combine(const float *ws_o, const float *ws_lse, void *o, float *lse,
                                    int BH, int Nq, int d, int n_ktiles, int nsp, int causal,
                                    int dtype, cudaStream_t s) {
-  if (d == 64) {
-    if (dtype == FA_DTYPE_BF16)
-      return launch_combine<64, FA_DTYPE_BF16>(ws_o, ws_lse, o, lse, BH, Nq, n_ktiles, nsp, causal, s);
-    if (dtype == FA_DTYPE_F16)
-      return launch_combine<64, FA_DTYPE_F16>(ws_o, ws_lse, o, lse, BH, Nq, n_ktiles, nsp, causal, s);
-    return launch_combine<64, FA_DTYPE_F32>(ws_o, ws_lse, o, lse, BH, Nq, n_ktiles, nsp, causal, s);
-  }
-  if (d == 128) {
-    if (dtype == FA_DTYPE_BF16)
-      return launch_combine<128, FA_DTYPE_BF16>(ws_o, ws_lse, o, lse, BH, Nq, n_ktiles, nsp, causal, s);
-    return launch_combine<128, FA_DTYPE_F16>(ws_o, ws_lse, o, lse, BH, Nq, n_ktiles, nsp, causal, s);
-  }
-  if (dtype == FA_DTYPE_BF16)
-    return launch_combine<256, FA_DTYPE_BF16>(ws_o, ws_lse, o, lse, BH, Nq, n_ktiles, nsp, causal, s);
-  return launch_combine<256, FA_DTYPE_F16>(ws_o, ws_lse, o, lse, BH, Nq, n_ktiles, nsp, causal, s);
+  if (d == 64)
+    return launch_combine_d<64>(ws_o, ws_lse, o, lse, BH, Nq, n_ktiles, nsp, causal, dtype, s);
+  if (d == 128)
+    return launch_combine_d<128>(ws_o, ws_lse, o, lse, BH, Nq, n_ktiles, nsp, causal, dtype, s);
+  return launch_combine_d<256>(ws_o, ws_lse, o, lse, BH, Nq, n_ktiles, nsp, causal, dtype, s);
 }
 
 }  // namespace fa

@@ -39,7 +39,8 @@
 // which biases the scores; so Q (on its way to TMEM) and K_j (in place, by the
 // softmax warps, before S_j is issued) are rounded to nearest first.  P is
 // tf32.  kind::tf32 takes its B operand K-major only, so the softmax warps
-// also transpose each V_j into a tf32 V_j^T buffer (d rows of 128 keys).
+// also transpose each V_j into a tf32 V_j^T buffer (d rows of 128 keys).  At
+// D=128 the fp32 tiles are 64 KB: one K, one V and one V^T buffer.
 // Tensor memory: S_b cols [128b, 128b+128) for b < NS, then O (D cols), then Q
 // when it fits (bf16 D=64, fp32 D=64); bf16 D=128 and D=256 keep Q in shared
 // memory.  D=256 has two score buffers and single-stage K/V rings (64 KB
@@ -87,12 +88,12 @@ struct TcCfg {
   static constexpr int NQ = QTMEM ? 0 : 1;                  // Q tiles in shared memory
   // K / V ring depths: as deep as shared memory allows (64 KB tiles at
   // D = 256 leave room for one stage each beside Q).
-  static constexpr int KST = TF32 ? 2 : (TILE_BYTES <= 16384 ? 4 : TILE_BYTES <= 32768 ? 3 : 1);
+  static constexpr int KST = TILE_BYTES >= 65536 ? 1 : TF32 ? 2 : TILE_BYTES <= 16384 ? 4 : 3;
   static constexpr int VST = KST;
   // fp32 path: V_j is transposed by the softmax warps into a K-major copy
   // (V^T, d rows of 128 keys, tf32-rounded) because P V runs as kind::tf32
   // with V^T as a K-major B operand.  Two copies alternate.
-  static constexpr int NVT = TF32 ? 2 : 0;
+  static constexpr int NVT = TF32 ? (TILE_BYTES >= 65536 ? 1 : 2) : 0;
   static constexpr int VT_CHUNK_BYTES = D * 128;            // 32 keys x D rows
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_K = OFF_Q + NQ * TILE_BYTES;
@@ -368,7 +369,7 @@ __global__ void __launch_bounds__(224, 1)
           uint64_t bdesc;
           if constexpr (TF32) {
             // V^T: D rows of 128 keys, K-major, 32 keys per 128-byte chunk
-            const uint32_t vt = sVT + (j & 1) * C::TILE_BYTES;
+            const uint32_t vt = sVT + (j % C::NVT) * C::TILE_BYTES;
             bdesc = sdesc_sw128(vt + (kk >> 2) * C::VT_CHUNK_BYTES + (kk & 3) * 32, 16, 1024);
           } else {
             // V: UK key rows of 128 bytes per step, MN-major
@@ -432,7 +433,7 @@ __global__ void __launch_bounds__(224, 1)
       const int s = j % C::VST;
       if (!__all_sync(kFull, bounded_wait(bVfull + 8 * s, (j / C::VST) & 1, w))) return false;
       const uint8_t *vt32 = smem + C::OFF_V + s * C::TILE_BYTES;
-      uint8_t *vtT = smem + C::OFF_VT + (j & 1) * C::TILE_BYTES;
+      uint8_t *vtT = smem + C::OFF_VT + (j % C::NVT) * C::TILE_BYTES;
       const int key_chunk = r >> 5, key_unit = (r & 31) >> 2, key_word = r & 3;
 #pragma unroll
       for (int ch = 0; ch < C::NCH; ++ch) {
@@ -611,8 +612,13 @@ __global__ void __launch_bounds__(224, 1)
         l += (a0 + a1) + (b0 + b1);
       }
       if constexpr (TF32) {
-        // V^T buffer j&1 was last read by P_{j-2} V_{j-2}, which completed
-        // before S_j was issued.
+        // V^T buffer j % NVT was last read by P_{j-NVT} V_{j-NVT}.  With two
+        // buffers that completed before S_j was issued; with one (D = 128)
+        // P_{j-1} V_{j-1} may still be running.
+        if (C::NVT == 1 && j > 0) {
+          ok = __all_sync(kFull, bounded_wait(bOdone + 8 * pbuf, pbph, w));
+          if (!ok) break;
+        }
         if (!(ok = transpose_v_row(j))) break;
       }
       tmem_st_wait();

@@ -1,0 +1,13 @@
+// fa_tc_f32_d128.cu — instantiation of the tensor-core forward for head dim 128,
+// fp32 inputs (tcgen05 kind::tf32).
+#include "fa_tc.cuh"
+
+namespace fa {
+
+cudaError_t launch_tc_f32_d128(const CUtensorMap &q, const CUtensorMap &k, const CUtensorMap &v,
+                         const CUtensorMap &o, const TcParams &p, int B, int causal,
+                         cudaStream_t s) {
+  return launch_tc<128, true>(q, k, v, o, p, B, causal, s);
+}
+
+}  // namespace fa

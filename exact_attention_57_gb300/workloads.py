@@ -96,6 +96,9 @@ PROFILE_WORKLOADS = {
     "b4h16n8192d256-bf16-causal": Workload(
         "b4h16n8192d256-bf16-causal", 4, 16, 8192, 8192, 256, DTYPE_BF16,
         causal=(True,), seed=57007, note="head dim 256"),
+    "b4h4n4096d128-f32-tf32": Workload(
+        "b4h4n4096d128-f32-tf32", 4, 4, 4096, 4096, 128, DTYPE_F32,
+        causal=(False,), seed=57009, note="fp32 at head dim 128 (TF32 tensor cores)"),
     "b4h16n8192d64-bf16-causal": Workload(
         "b4h16n8192d64-bf16-causal", 4, 16, 8192, 8192, 64, DTYPE_BF16,
         causal=(True,), seed=57008, note="head dim 64"),

@@ -43,6 +43,17 @@ def run_oracle(q, k, v, scale, causal):
                            scale, causal)
 
 
+def tf32_tol(q, k, v, scale, causal):
+    """Tolerances of the fp32 tensor-core path for these inputs: the stated
+    ones, widened to what TF32 rounding of the scores implies (the LSE moves
+    by at most the largest score error, O by at most twice that times
+    max|v|, plus P/V rounding) where that is larger."""
+    b = tf32_score_bound(q, k, scale, causal)
+    vmax = float(torch.as_tensor(v).abs().max())
+    return dict(max_lse=max(TOL[DTYPE_F32]["max_lse"], b),
+                max_o=max(TOL[DTYPE_F32]["max_o"], 2 * b * vmax + 1e-3))
+
+
 def tf32_score_bound(q, k, scale, causal):
     """Worst-case |score error| of the TF32 path: q and k are rounded to
     nearest tf32 (relative error u = 2^-11 each), so every product q_x*k_x is

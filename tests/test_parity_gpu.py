@@ -9,7 +9,7 @@ import oracle
 from exact_attention_57_gb300 import fa
 from exact_attention_57_gb300.workloads import (DTYPE_BF16, DTYPE_F16, DTYPE_F32, DTYPE_F32_SIMT,
                                                 WORKLOADS, make_inputs, workload_inputs)
-from parity_util import TOL, compare, run_gpu, run_oracle, tf32_score_bound
+from parity_util import TOL, compare, run_gpu, run_oracle, tf32_tol
 
 pytestmark = pytest.mark.gpu
 
@@ -35,14 +35,16 @@ def _dd(pairs):
 
 @pytest.mark.parametrize("dtype,d", _dd([(DTYPE_BF16, 64), (DTYPE_BF16, 128), (DTYPE_F32, 64),
                                          (DTYPE_F32_SIMT, 64), (DTYPE_F16, 64),
-                                         (DTYPE_F16, 128), (DTYPE_BF16, 256), (DTYPE_F16, 256)]))
+                                         (DTYPE_F16, 128), (DTYPE_BF16, 256), (DTYPE_F16, 256),
+                                         (DTYPE_F32, 128)]))
 @pytest.mark.parametrize("causal", [False, True])
 def test_other_mask_per_dtype(dtype, d, causal):
     """Every kernel variant, causal and not, on a several-tile ragged case."""
     q, k, v = make_inputs(2, 3, 700, 700, d, dtype, seed=11 + d + 7 * dtype)
     o, lse = run_gpu(q, k, v, 1.0 / math.sqrt(d), causal, dtype)
     ro, rl = run_oracle(q, k, v, 1.0 / math.sqrt(d), causal)
-    compare(o, lse, ro, rl, dtype, f"N=700 d={d} causal={causal}")
+    tol = tf32_tol(q, k, v, 1.0 / math.sqrt(d), causal) if dtype == DTYPE_F32 else None
+    compare(o, lse, ro, rl, dtype, f"N=700 d={d} causal={causal}", tol=tol)
 
 
 EDGE_N = [1, 2, 127, 128, 129, 255, 256, 257]
@@ -50,26 +52,29 @@ EDGE_N = [1, 2, 127, 128, 129, 255, 256, 257]
 
 @pytest.mark.parametrize("N", EDGE_N)
 @pytest.mark.parametrize("dtype,d", _dd([(DTYPE_BF16, 64), (DTYPE_BF16, 128), (DTYPE_F32, 64),
-                                         (DTYPE_F32_SIMT, 64), (DTYPE_F16, 128), (DTYPE_BF16, 256)]))
+                                         (DTYPE_F32_SIMT, 64), (DTYPE_F16, 128), (DTYPE_BF16, 256),
+                                         (DTYPE_F32, 128)]))
 def test_edge_lengths(N, dtype, d):
     q, k, v = make_inputs(1, 2, N, N, d, dtype, seed=100 + N)
     for causal in (False, True):
         o, lse = run_gpu(q, k, v, 1.0 / math.sqrt(d), causal, dtype)
         ro, rl = run_oracle(q, k, v, 1.0 / math.sqrt(d), causal)
-        compare(o, lse, ro, rl, dtype, f"N={N} d={d} causal={causal}")
+        tol = tf32_tol(q, k, v, 1.0 / math.sqrt(d), causal) if dtype == DTYPE_F32 else None
+        compare(o, lse, ro, rl, dtype, f"N={N} d={d} causal={causal}", tol=tol)
 
 
 @pytest.mark.parametrize("Nq,Nk", [(200, 77), (77, 200), (1, 1000), (1000, 1), (129, 384),
                                    (384, 129)])
 @pytest.mark.parametrize("dtype,d", _dd([(DTYPE_BF16, 128), (DTYPE_F32, 64), (DTYPE_F32_SIMT, 64),
-                                         (DTYPE_F16, 64), (DTYPE_F16, 256)]))
+                                         (DTYPE_F16, 64), (DTYPE_F16, 256), (DTYPE_F32, 128)]))
 def test_unequal_lengths(Nq, Nk, dtype, d):
     """Nq != Nk, causal top-left aligned (key j allowed iff j <= i)."""
     q, k, v = make_inputs(2, 1, Nq, Nk, d, dtype, seed=Nq * 7 + Nk)
     for causal in (False, True):
         o, lse = run_gpu(q, k, v, 0.1, causal, dtype)
         ro, rl = run_oracle(q, k, v, 0.1, causal)
-        compare(o, lse, ro, rl, dtype, f"Nq={Nq} Nk={Nk} causal={causal}")
+        tol = tf32_tol(q, k, v, 0.1, causal) if dtype == DTYPE_F32 else None
+        compare(o, lse, ro, rl, dtype, f"Nq={Nq} Nk={Nk} causal={causal}", tol=tol)
 
 
 @pytest.mark.parametrize("scale", [0.0, -0.125, 0.5, 1e-3])
@@ -81,16 +86,7 @@ def test_scales(scale, dtype, d):
     for causal in (False, True):
         o, lse = run_gpu(q, k, v, scale, causal, dtype)
         ro, rl = run_oracle(q, k, v, scale, causal)
-        tol = None
-        if dtype == DTYPE_F32:
-            # Beyond the 1/sqrt(d) scale of the fp32 workload the fixed
-            # tolerances no longer cover TF32 rounding of the scores; use the
-            # bound that rounding implies (LSE moves by at most the largest
-            # score error, O by at most twice that times max|v|).
-            b = tf32_score_bound(q, k, scale, causal)
-            vmax = float(v.abs().max())
-            tol = dict(max_lse=max(TOL[dtype]["max_lse"], b),
-                       max_o=max(TOL[dtype]["max_o"], 2 * b * vmax + 1e-3))
+        tol = tf32_tol(q, k, v, scale, causal) if dtype == DTYPE_F32 else None
         compare(o, lse, ro, rl, dtype, f"scale={scale} causal={causal}", tol=tol)
 
 
