@@ -60,9 +60,10 @@ int validate(const void *q, const void *k, const void *v, const void *o, const f
       overlap(lse, ln, v, kn))
     return FA_ERR_INVALID_ARG;
   // The compiled set of kernels.
-  if ((dtype == FA_DTYPE_BF16 || dtype == FA_DTYPE_F16) && d != 64 && d != 128 && d != 256)
+  if ((dtype == FA_DTYPE_BF16 || dtype == FA_DTYPE_F16) && d != 32 && d != 64 && d != 128 &&
+      d != 256)
     return FA_ERR_UNSUPPORTED;
-  if (dtype == FA_DTYPE_F32 && d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+  if (dtype == FA_DTYPE_F32 && d != 32 && d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
   if (dtype == FA_DTYPE_F32_SIMT && d > 128) return FA_ERR_UNSUPPORTED;
   return FA_OK;
 }
@@ -132,9 +133,19 @@ int ceil_div(int a, int b) { return (a + b - 1) / b; }
 
 // The tensor-core forward instantiation for (dtype, d); the combination has
 // been checked by validate().
+//
+// Head dim 32 runs on the d = 64 kernels zero-padded: the tensor maps over the
+// 32-wide rows zero-fill columns 32..63 on load (so S and P V are unchanged)
+// and clip them on store; d_io tells the kernel where its plain loads and
+// stores stop.
 cudaError_t launch_tc_any(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv,
-                          const CUtensorMap &mo, const fa::TcParams &p, int B, int causal, int d,
-                          int dtype, cudaStream_t s) {
+                          const CUtensorMap &mo, const fa::TcParams &p_in, int B, int causal,
+                          int d, int dtype, cudaStream_t s) {
+  fa::TcParams p = p_in;
+  if (d == 32) {
+    p.d_io = 32;
+    d = 64;
+  }
   if (dtype == FA_DTYPE_F16)
     return d == 64    ? fa::launch_tc_f16_d64(mq, mk, mv, mo, p, B, causal, s)
            : d == 128 ? fa::launch_tc_f16_d128(mq, mk, mv, mo, p, B, causal, s)

@@ -49,6 +49,9 @@ struct TcParams {
   const int *cu_q = nullptr;
   const int *cu_k = nullptr;
   int total_q = 0;
+  // Head dim of the tensors when narrower than the kernel's D (0 = D): the
+  // kernel runs zero-padded to D.
+  int d_io = 0;
 };
 
 struct SimtParams {

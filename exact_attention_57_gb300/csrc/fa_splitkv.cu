@@ -109,6 +109,8 @@ cudaError_t launch_combine_d(const float *ws_o, const float *ws_lse, void *o, fl
 cudaError_t launch_splitkv_combine(const float *ws_o, const float *ws_lse, void *o, float *lse,
                                    int BH, int Nq, int d, int n_ktiles, int nsp, int causal,
                                    int dtype, cudaStream_t s) {
+  if (d == 32)
+    return launch_combine_d<32>(ws_o, ws_lse, o, lse, BH, Nq, n_ktiles, nsp, causal, dtype, s);
   if (d == 64)
     return launch_combine_d<64>(ws_o, ws_lse, o, lse, BH, Nq, n_ktiles, nsp, causal, dtype, s);
   if (d == 128)

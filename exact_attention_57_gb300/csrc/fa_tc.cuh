@@ -173,6 +173,11 @@ __global__ void __launch_bounds__(224, 1)
   }
   const int qt = CAUSAL ? (n_qtiles - 1 - qidx) : qidx;
   const int q0 = qt * BM;
+  // Head dim of the tensors in memory: D, or less when the kernel runs a
+  // narrower head dim zero-padded to D (the TMA maps zero-fill the missing
+  // columns on load and clip them on store; plain loads and stores below
+  // stop at dio).
+  const int dio = p.d_io > 0 ? p.d_io : D;
   if (Nk == 0) {
     // A sequence without keys: the softmax over an empty set gives O = 0 and
     // LSE = log 0 = -inf (variable-length batches only).
@@ -182,7 +187,7 @@ __global__ void __launch_bounds__(224, 1)
         const long long gr = q_row0 + row;
         uint8_t *orow = static_cast<uint8_t *>(p.o) +
                         (hc * p.q_head_stride + gr * p.q_row_stride) * C::ESZ;
-        for (int x = 0; x < D * C::ESZ; x += 16) *reinterpret_cast<uint4 *>(orow + x) = make_uint4(0, 0, 0, 0);
+        for (int x = 0; x < dio * C::ESZ; x += 16) *reinterpret_cast<uint4 *>(orow + x) = make_uint4(0, 0, 0, 0);
         p.lse[hc * p.lse_head_stride + gr] = -INFINITY;
       }
     }
@@ -469,7 +474,8 @@ __global__ void __launch_bounds__(224, 1)
         uint32_t wq[32];
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
-          uint4 val = in ? __ldg(src + blk * 8 + u) : make_uint4(0u, 0u, 0u, 0u);
+          const bool ld = in && (blk * 8 + u) * 16 < dio * C::ESZ;
+          uint4 val = ld ? __ldg(src + blk * 8 + u) : make_uint4(0u, 0u, 0u, 0u);
           wq[4 * u + 0] = val.x;
           wq[4 * u + 1] = val.y;
           wq[4 * u + 2] = val.z;
@@ -646,8 +652,8 @@ __global__ void __launch_bounds__(224, 1)
           tmem_ld32(o_tm + c, o);
           tmem_ld_wait();
           reg_fence32(o);
-          if (row < Nq) {
-            float4 *dst = reinterpret_cast<float4 *>(p.ws_o + prow * D + c);
+          if (row < Nq && c < dio) {
+            float4 *dst = reinterpret_cast<float4 *>(p.ws_o + prow * dio + c);
 #pragma unroll
             for (int u = 0; u < 8; ++u)
               dst[u] = make_float4(__uint_as_float(o[4 * u + 0]) * inv_l,
@@ -673,7 +679,7 @@ __global__ void __launch_bounds__(224, 1)
           tmem_ld32(o_tm + c, o);
           tmem_ld_wait();
           reg_fence32(o);
-          if (row < Nq) {
+          if (row < Nq && c < dio) {
             if constexpr (TF32) {
 #pragma unroll
               for (int u = 0; u < 8; ++u)
@@ -755,7 +761,8 @@ __global__ void __launch_bounds__(224, 1)
     if (nsp == 1 && p.cu_q == nullptr && threadIdx.x == 0 && *abort_flag == 0) {
 #pragma unroll
       for (int c = 0; c < C::NCH; ++c)
-        tma_store_3d(&tm_o, sK + c * C::CHUNK_BYTES, c * C::CH_ELEMS, q0, bh);
+        if (c * C::CH_ELEMS < dio)  // a chunk wholly past the row is not stored
+          tma_store_3d(&tm_o, sK + c * C::CHUNK_BYTES, c * C::CH_ELEMS, q0, bh);
       tma_store_commit();
       tma_store_wait_read_all();
     }

@@ -82,8 +82,8 @@ typedef enum {
  *           written.
  * B, H      batch size and number of heads, 1 .. 65535.
  * Nq, Nk    query and key sequence lengths, >= 1 (ragged lengths allowed).
- * d         head dimension.  FA_DTYPE_BF16, FA_DTYPE_F16: 64, 128 or 256.
- *           FA_DTYPE_F32: 64 or 128.
+ * d         head dimension.  FA_DTYPE_BF16, FA_DTYPE_F16: 32, 64, 128 or 256.
+ *           FA_DTYPE_F32: 32, 64 or 128.
  *           FA_DTYPE_F32_SIMT: 1 .. 128.  Anything else is
  *           FA_ERR_UNSUPPORTED (the role of the "Failed to find groupsize ...
  *           Shared Memory constraint" error of "Flash Attention Shared Memory

@@ -70,9 +70,9 @@ def test_invalid_arguments(lib, kw):
 
 
 @pytest.mark.parametrize("kw", [
-    dict(dtype=fa.FA_DTYPE_BF16, d=32), dict(dtype=fa.FA_DTYPE_BF16, d=96),
+    dict(dtype=fa.FA_DTYPE_BF16, d=16), dict(dtype=fa.FA_DTYPE_BF16, d=96),
     dict(dtype=fa.FA_DTYPE_BF16, d=512), dict(dtype=fa.FA_DTYPE_F32, d=256),
-    dict(dtype=fa.FA_DTYPE_F32, d=32), dict(dtype=fa.FA_DTYPE_F32_SIMT, d=129),
+    dict(dtype=fa.FA_DTYPE_F32, d=48), dict(dtype=fa.FA_DTYPE_F32_SIMT, d=129),
     dict(dtype=fa.FA_DTYPE_F16, d=96), dict(dtype=fa.FA_DTYPE_F16, d=192),
 ], ids=lambda kw: ",".join(f"{k}={v}" for k, v in kw.items()))
 def test_unsupported_problems(lib, kw):

@@ -36,7 +36,8 @@ def _dd(pairs):
 @pytest.mark.parametrize("dtype,d", _dd([(DTYPE_BF16, 64), (DTYPE_BF16, 128), (DTYPE_F32, 64),
                                          (DTYPE_F32_SIMT, 64), (DTYPE_F16, 64),
                                          (DTYPE_F16, 128), (DTYPE_BF16, 256), (DTYPE_F16, 256),
-                                         (DTYPE_F32, 128)]))
+                                         (DTYPE_F32, 128), (DTYPE_BF16, 32), (DTYPE_F16, 32),
+                                         (DTYPE_F32, 32)]))
 @pytest.mark.parametrize("causal", [False, True])
 def test_other_mask_per_dtype(dtype, d, causal):
     """Every kernel variant, causal and not, on a several-tile ragged case."""
@@ -53,7 +54,7 @@ EDGE_N = [1, 2, 127, 128, 129, 255, 256, 257]
 @pytest.mark.parametrize("N", EDGE_N)
 @pytest.mark.parametrize("dtype,d", _dd([(DTYPE_BF16, 64), (DTYPE_BF16, 128), (DTYPE_F32, 64),
                                          (DTYPE_F32_SIMT, 64), (DTYPE_F16, 128), (DTYPE_BF16, 256),
-                                         (DTYPE_F32, 128)]))
+                                         (DTYPE_F32, 128), (DTYPE_BF16, 32)]))
 def test_edge_lengths(N, dtype, d):
     q, k, v = make_inputs(1, 2, N, N, d, dtype, seed=100 + N)
     for causal in (False, True):
@@ -66,7 +67,8 @@ def test_edge_lengths(N, dtype, d):
 @pytest.mark.parametrize("Nq,Nk", [(200, 77), (77, 200), (1, 1000), (1000, 1), (129, 384),
                                    (384, 129)])
 @pytest.mark.parametrize("dtype,d", _dd([(DTYPE_BF16, 128), (DTYPE_F32, 64), (DTYPE_F32_SIMT, 64),
-                                         (DTYPE_F16, 64), (DTYPE_F16, 256), (DTYPE_F32, 128)]))
+                                         (DTYPE_F16, 64), (DTYPE_F16, 256), (DTYPE_F32, 128),
+                                         (DTYPE_F16, 32)]))
 def test_unequal_lengths(Nq, Nk, dtype, d):
     """Nq != Nk, causal top-left aligned (key j allowed iff j <= i)."""
     q, k, v = make_inputs(2, 1, Nq, Nk, d, dtype, seed=Nq * 7 + Nk)

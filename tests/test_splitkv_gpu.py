@@ -21,6 +21,7 @@ CASES = [
     (2, 4, 128, 4096, 64, DTYPE_BF16),
     (1, 2, 200, 2000, 256, DTYPE_BF16),
     (1, 2, 130, 1500, 128, DTYPE_F32),
+    (2, 2, 100, 1100, 32, DTYPE_BF16),
 ]
 
 

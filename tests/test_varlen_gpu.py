@@ -21,6 +21,7 @@ CASES = [
     ([1000, 1, 513], [1000, 2048, 513], 4, 128, DTYPE_BF16),
     ([130, 257], [300, 129], 2, 256, DTYPE_BF16),
     ([77, 200], [300, 64], 2, 128, DTYPE_F32),
+    ([140, 3, 260], [140, 500, 0], 3, 32, DTYPE_F16),
 ]
 
 
