@@ -9,6 +9,11 @@ Workload at one GPU: B=8, H=32, Nq=Nk=8192, d=128, bf16, causal
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl fa|reference]
                   [--pass fwd|bwd]
 
+``--varlen`` times fa_fwd_varlen on a packed batch of 32 sequences with
+lengths drawn uniformly from 512..8192 (seeded; token-major [total, 16, 128]
+bf16, causal within each sequence); FLOPs are counted exactly per sequence
+(4*H*d per allowed (query, key) pair).
+
 ``--pass bwd`` times the backward instead (one step = one fa_bwd call: the
 per-row D / LSE kernel, the tensor-core gradient kernel and the dq rounding),
 reporting 2.5x the forward's FLOPs (five products of 2*Nq*Nk*d where the
@@ -247,6 +252,8 @@ def main():
     ap.add_argument("--splits", type=int, default=None,
                     help="run fa_fwd_splitkv with this many key chunks (0 = automatic)")
     ap.add_argument("--pass", dest="which", default="fwd", choices=["fwd", "bwd"])
+    ap.add_argument("--varlen", action="store_true",
+                    help="packed variable-length batch through fa_fwd_varlen")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
 
@@ -287,6 +294,25 @@ def main():
         wspace = torch.empty(max(wsb, 256), dtype=torch.uint8, device=dev)
 
     bwd = args.which == "bwd"
+    varlen = None
+    if args.varlen:
+        # 32 sequences, lengths uniform in 512..8192, causal within each.
+        import numpy as np
+        rs = np.random.default_rng(57100 + rank)
+        lens = rs.integers(512, 8193, size=32)
+        Hv, dv_ = 16, 128
+        total = int(lens.sum())
+        cu = torch.tensor(np.concatenate([[0], np.cumsum(lens)]), dtype=torch.int32, device=dev)
+        qv = torch.randn(total, Hv, dv_, device=dev, generator=g).to(torch.bfloat16)
+        kv = torch.randn(total, Hv, dv_, device=dev, generator=g).to(torch.bfloat16)
+        vv = torch.randn(total, Hv, dv_, device=dev, generator=g).to(torch.bfloat16)
+        ov = torch.empty_like(qv)
+        lv = torch.empty(Hv, total, device=dev, dtype=torch.float32)
+        pairs = float(sum(int(L) * (int(L) + 1) // 2 for L in lens))
+        varlen = dict(lens=lens, H=Hv, d=dv_, total=total, cu=cu, q=qv, k=kv, v=vv, o=ov,
+                      lse=lv, flops=4.0 * Hv * dv_ * pairs, maxlen=int(lens.max()))
+        args.no_e2e = True
+        args.no_cpu_baseline = True
     if bwd:
         if w.dtype not in (0, 3):
             raise SystemExit("--pass bwd needs a bf16 or fp16 workload")
@@ -300,6 +326,16 @@ def main():
         args.no_cpu_baseline = True
 
     def step():
+        if varlen is not None:
+            vl = varlen
+            st = fa.fa_fwd_varlen(vl["q"].data_ptr(), vl["k"].data_ptr(), vl["v"].data_ptr(),
+                                  vl["o"].data_ptr(), vl["lse"].data_ptr(), vl["cu"].data_ptr(),
+                                  vl["cu"].data_ptr(), len(vl["lens"]), vl["H"], vl["total"],
+                                  vl["total"], vl["maxlen"], vl["d"], vl["d"] ** -0.5, 1,
+                                  fa.FA_DTYPE_BF16, sh)
+            if st != fa.FA_OK:
+                raise fa.FaError(st, "fa_fwd_varlen")
+            return
         if bwd:
             st = fa.fa_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
                            dout.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), w.B,
@@ -350,7 +386,7 @@ def main():
     launch_ms = [ev[i].elapsed_time(ev[i + 1]) for i in range(args.steps)]
     total_ms = max_over_ranks(ev[0].elapsed_time(ev[-1]), dev)
     ms_per_step = total_ms / args.steps
-    flops_step = w.flops(causal) * (2.5 if bwd else 1.0)
+    flops_step = varlen["flops"] if varlen is not None else w.flops(causal) * (2.5 if bwd else 1.0)
     value = ws * flops_step * args.steps / (total_ms / 1e3) / 1e12
 
     # End to end through the host-buffer entry point: H2D of q, k, v from
@@ -424,6 +460,10 @@ def main():
                    "causal": causal, "flops_per_step": flops_step,
                    "parallelism": f"replicas{ws}" if ws > 1 else "single",
                    "key_splits": args.splits, "pass": args.which,
+                   "varlen": (None if varlen is None else
+                              {"sequences": len(varlen["lens"]), "total_tokens": varlen["total"],
+                               "lengths": "uniform 512..8192 (seeded)", "H": varlen["H"],
+                               "d": varlen["d"], "causal": True}),
                    "l2": "inputs larger than L2 (no flush)"},
         "roofline": roofline,
         "pct_of_peak": 100.0 * value / ws / peak,
@@ -432,6 +472,11 @@ def main():
         "gpu_launches": args.steps * (3 if bwd else 2 if wspace is not None else 1),
         "clocks": clocks,
     }
+    if varlen is not None:
+        line["config"] = {"workload": "varlen32-l512to8192-h16-d128-bf16-causal",
+                          "flops_per_step": flops_step, "parallelism": line["config"]["parallelism"],
+                          "varlen": line["config"]["varlen"],
+                          "l2": "inputs larger than L2 (no flush)"}
     print(json.dumps(line), flush=True)
     if ws > 1:
         dist.barrier()

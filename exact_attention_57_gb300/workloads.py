@@ -99,6 +99,9 @@ PROFILE_WORKLOADS = {
     "b4h4n4096d128-f32-tf32": Workload(
         "b4h4n4096d128-f32-tf32", 4, 4, 4096, 4096, 128, DTYPE_F32,
         causal=(False,), seed=57009, note="fp32 at head dim 128 (TF32 tensor cores)"),
+    "b4h16n8192d32-bf16-causal": Workload(
+        "b4h16n8192d32-bf16-causal", 4, 16, 8192, 8192, 32, DTYPE_BF16,
+        causal=(True,), seed=57010, note="head dim 32 (runs zero-padded on the d = 64 kernel)"),
     "b4h16n8192d64-bf16-causal": Workload(
         "b4h16n8192d64-bf16-causal", 4, 16, 8192, 8192, 64, DTYPE_BF16,
         causal=(True,), seed=57008, note="head dim 64"),
