@@ -252,6 +252,8 @@ def main():
     ap.add_argument("--splits", type=int, default=None,
                     help="run fa_fwd_splitkv with this many key chunks (0 = automatic)")
     ap.add_argument("--pass", dest="which", default="fwd", choices=["fwd", "bwd"])
+    ap.add_argument("--no-staging", action="store_true",
+                    help="fp32 workloads: time fa_fwd instead of fa_fwd_staged")
     ap.add_argument("--varlen", action="store_true",
                     help="packed variable-length batch through fa_fwd_varlen")
     args = ap.parse_args()
@@ -288,6 +290,12 @@ def main():
     sh = stream.cuda_stream
     impl = "simt" if w.dtype == 2 else "tc"
 
+    # fp32 (TF32) workloads run through fa_fwd_staged unless told otherwise:
+    # its workspace is allocated here, outside the timed region.
+    stage_ws = None
+    if w.dtype == 1 and not args.no_staging and args.splits is None:
+        sb = fa.fa_fwd_staged_workspace(w.B, w.H, w.Nk, w.d, w.dtype)
+        stage_ws = torch.empty(max(sb, 256), dtype=torch.uint8, device=dev)
     wspace = None  # split-KV workspace
     if args.splits is not None:
         wsb = fa.fa_fwd_splitkv_workspace(w.B, w.H, w.Nq, w.d, args.splits if args.splits else 64)
@@ -344,7 +352,12 @@ def main():
             if st != fa.FA_OK:
                 raise fa.FaError(st, "fa_bwd")
             return
-        if wspace is None:
+        if stage_ws is not None:
+            st = fa.fa_fwd_staged(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                  lse.data_ptr(), w.B, w.H, w.Nq, w.Nk, w.d, w.scale,
+                                  int(causal), w.dtype, stage_ws.data_ptr(), stage_ws.numel(),
+                                  sh)
+        elif wspace is None:
             st = fa.fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
                            w.B, w.H, w.Nq, w.Nk, w.d, w.scale, int(causal), w.dtype, sh)
         else:
@@ -460,6 +473,7 @@ def main():
                    "causal": causal, "flops_per_step": flops_step,
                    "parallelism": f"replicas{ws}" if ws > 1 else "single",
                    "key_splits": args.splits, "pass": args.which,
+                   "staged": stage_ws is not None,
                    "varlen": (None if varlen is None else
                               {"sequences": len(varlen["lens"]), "total_tokens": varlen["total"],
                                "lengths": "uniform 512..8192 (seeded)", "H": varlen["H"],
@@ -469,7 +483,8 @@ def main():
         "pct_of_peak": 100.0 * value / ws / peak,
         "cpu_baseline": cpu,
         "e2e": e2e,
-        "gpu_launches": args.steps * (3 if bwd else 2 if wspace is not None else 1),
+        "gpu_launches": args.steps * (3 if bwd or stage_ws is not None
+                                      else 2 if wspace is not None else 1),
         "clocks": clocks,
     }
     if varlen is not None:

@@ -708,3 +708,103 @@ extern "C" int fa_bwd(const void *q, const void *k, const void *v, const void *o
   e = fa::launch_bwd_convert(p.dq_acc, dq, static_cast<long long>(BH) * Nq * d, half, s);
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
+
+// ---------------------------------------------------------------------------
+// Forward with a staging workspace (fp32: operands converted once per call).
+// ---------------------------------------------------------------------------
+namespace {
+
+int nk_pad128(int Nk) { return ceil_div(Nk, fa::BN) * fa::BN; }
+
+// Workspace parts for fp32: K rounded to tf32 [B*H][Nk][d], then V^T
+// [B*H][d][Nk padded to 128].
+void staged_parts(int B, int H, int Nk, int d, size_t *kr, size_t *vt) {
+  const size_t bh = static_cast<size_t>(B) * H;
+  *kr = round256(bh * Nk * d * sizeof(float));
+  *vt = round256(bh * d * static_cast<size_t>(nk_pad128(Nk)) * sizeof(float));
+}
+
+// 3-D view {Nk_pad, d, B*H} of the staged V^T, boxes of 32 keys (128 bytes)
+// x dk rows (the kernel's head dim; rows past d read as zeros).
+int encode_map_vt(CUtensorMap *map, void *base, int BH, int nk_pad, int d, int dk) {
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(nk_pad), static_cast<cuuint64_t>(d),
+                        static_cast<cuuint64_t>(BH)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(nk_pad) * 4,
+                           static_cast<cuuint64_t>(nk_pad) * static_cast<cuuint64_t>(d) * 4};
+  cuuint32_t box[3] = {32, static_cast<cuuint32_t>(dk), 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, base, dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? FA_OK : FA_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" unsigned long long fa_fwd_staged_workspace(int B, int H, int Nk, int d, int dtype) {
+  if (B < 1 || H < 1 || Nk < 1 || d < 1) return 0;
+  if (dtype != FA_DTYPE_F32) return 0;  // only the fp32 path stages operands
+  size_t kr, vt;
+  staged_parts(B, H, Nk, d, &kr, &vt);
+  return kr + vt;
+}
+
+extern "C" int fa_fwd_staged(const void *q, const void *k, const void *v, void *o, float *lse,
+                             int B, int H, int Nq, int Nk, int d, float scale, int causal,
+                             int dtype, void *workspace, unsigned long long workspace_bytes,
+                             void *stream) {
+  int rc = validate(q, k, v, o, lse, B, H, Nq, Nk, d, scale, causal, dtype);
+  if (rc != FA_OK) return rc;
+  if (dtype != FA_DTYPE_F32)  // nothing to stage
+    return fa_fwd(q, k, v, o, lse, B, H, Nq, Nk, d, scale, causal, dtype, stream);
+  size_t kr_bytes, vt_bytes;
+  staged_parts(B, H, Nk, d, &kr_bytes, &vt_bytes);
+  const size_t need = kr_bytes + vt_bytes;
+  if (workspace == nullptr || reinterpret_cast<uintptr_t>(workspace) % 256 != 0 ||
+      workspace_bytes < need)
+    return FA_ERR_INVALID_ARG;
+  const size_t qn = static_cast<size_t>(B) * H * Nq * d * 4;
+  const size_t kn = static_cast<size_t>(B) * H * Nk * d * 4;
+  const size_t ln = static_cast<size_t>(B) * H * Nq * sizeof(float);
+  if (overlap(workspace, need, q, qn) || overlap(workspace, need, k, kn) ||
+      overlap(workspace, need, v, kn) || overlap(workspace, need, o, qn) ||
+      overlap(workspace, need, lse, ln))
+    return FA_ERR_INVALID_ARG;
+
+  unsigned *status = nullptr;
+  if ((rc = device_setup(&status)) != FA_OK) return rc;
+  if ((rc = get_encoder()) != FA_OK) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int BH = B * H, nkp = nk_pad128(Nk);
+  float *kr = static_cast<float *>(workspace);
+  float *vt = reinterpret_cast<float *>(static_cast<char *>(workspace) + kr_bytes);
+  if (fa::launch_stage_f32(static_cast<const float *>(k), static_cast<const float *>(v), kr, vt,
+                           BH, Nk, nkp, d, s) != cudaSuccess)
+    return FA_ERR_CUDA;
+
+  CUtensorMap mq, mk, mv, mo;
+  if ((rc = encode_map(&mq, q, dtype, BH, Nq, d)) != FA_OK) return rc;
+  if ((rc = encode_map(&mk, kr, dtype, BH, Nk, d)) != FA_OK) return rc;
+  if ((rc = encode_map_vt(&mv, vt, BH, nkp, d, d <= 64 ? 64 : 128)) != FA_OK) return rc;
+  if ((rc = encode_map(&mo, o, dtype, BH, Nq, d)) != FA_OK) return rc;
+  fa::TcParams p;
+  p.q = q;
+  p.o = o;
+  p.q_head_stride = static_cast<long long>(Nq) * d;
+  p.q_row_stride = d;
+  p.lse_head_stride = Nq;
+  p.lse = lse;
+  p.status = status;
+  p.H = H;
+  p.Nq = Nq;
+  p.Nk = Nk;
+  p.n_qtiles = ceil_div(Nq, fa::BM);
+  p.n_ktiles = ceil_div(Nk, fa::BN);
+  set_tc_scale(scale, &p);
+  const unsigned long long lim = g_wait_limit_ns.load();
+  p.wait_limit_ns = lim ? lim : fa::kDefaultWaitLimitNs;
+  p.skip_v_load = g_skip_v_load.load();
+  p.kv_staged = 1;
+  cudaError_t e = launch_tc_any(mq, mk, mv, mo, p, B, causal, d, dtype, s);
+  return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}

@@ -52,6 +52,9 @@ struct TcParams {
   // Head dim of the tensors when narrower than the kernel's D (0 = D): the
   // kernel runs zero-padded to D.
   int d_io = 0;
+  // fp32 path: K already rounded to tf32 and tm_v a map over a tf32 V^T
+  // ([B*H][d][Nk padded to 128], boxes of 32 keys x D rows).
+  int kv_staged = 0;
 };
 
 struct SimtParams {
@@ -98,6 +101,11 @@ cudaError_t launch_splitkv_combine(const float *ws_o, const float *ws_lse, void 
                                    int dtype, cudaStream_t s);
 
 cudaError_t launch_simt(const SimtParams &p, int B, cudaStream_t s);
+
+// fp32 staging pre-pass: kr = tf32(k) in k's layout, vt[bh][x][n] = tf32(v[bh][n][x])
+// for n < Nk and 0 for Nk <= n < nk_pad.
+cudaError_t launch_stage_f32(const float *k, const float *v, float *kr, float *vt, int BH, int Nk,
+                             int nk_pad, int d, cudaStream_t s);
 
 // ------------------------------------------------------------------ backward
 // Tensor-core backward: one CTA per (key tile, head, batch).  The TMA maps

@@ -40,7 +40,11 @@
 // softmax warps, before S_j is issued) are rounded to nearest first.  P is
 // tf32.  kind::tf32 takes its B operand K-major only, so the softmax warps
 // also transpose each V_j into a tf32 V_j^T buffer (d rows of 128 keys).  At
-// D=128 the fp32 tiles are 64 KB: one K, one V and one V^T buffer.
+// D=128 the fp32 tiles are 64 KB: one K, one V and one V^T buffer.  With
+// staged operands (kv_staged) a pre-pass has already rounded K and written
+// V^T once per call: K_j is used as loaded and V_j^T is loaded by TMA into
+// the V^T buffers (through the V ring's barriers), so the softmax warps only
+// do the softmax.
 // Tensor memory: S_b cols [128b, 128b+128) for b < NS, then O (D cols), then Q
 // when it fits (bf16 D=64, fp32 D=64); bf16 D=128 and D=256 keep Q in shared
 // memory.  D=256 has two score buffers and single-stage K/V rings (64 KB
@@ -111,6 +115,7 @@ struct TcCfg {
   static_assert(NCH >= 1 && D % 32 == 0, "head dim must fill whole 128-byte chunks");
   static_assert(COL_O + D <= TMEM_COLS, "tensor memory budget");
   static_assert(!TF32 || QTMEM, "the fp32 path rounds Q on its way into tensor memory");
+  static_assert(!TF32 || VST == NVT, "staged V^T tiles use the V ring's barriers");
   static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
 };
 
@@ -178,6 +183,9 @@ __global__ void __launch_bounds__(224, 1)
   // columns on load and clip them on store; plain loads and stores below
   // stop at dio).
   const int dio = p.d_io > 0 ? p.d_io : D;
+  // fp32 path with staged operands: K arrives rounded to tf32 and V as a
+  // K-major tf32 V^T, so neither is converted here.
+  const bool staged = TF32 && p.kv_staged != 0;
   if (Nk == 0) {
     // A sequence without keys: the softmax over an empty set gives O = 0 and
     // LSE = log 0 = -inf (variable-length batches only).
@@ -212,7 +220,7 @@ __global__ void __launch_bounds__(224, 1)
     for (int s = 0; s < C::VST; ++s) {
       mbar_init(bVfull + 8 * s, 1);
       // fp32 path: the softmax warps release a V stage once they transposed it
-      mbar_init(bVempty + 8 * s, TF32 ? 128 : 1);
+      mbar_init(bVempty + 8 * s, (TF32 && !p.kv_staged) ? 128 : 1);
     }
 #pragma unroll
     for (int s = 0; s < C::KST; ++s) mbar_init(bKready + 8 * s, 128);
@@ -284,10 +292,19 @@ __global__ void __launch_bounds__(224, 1)
           if (r > 0) ok = bounded_wait(bVempty + 8 * s, (r - 1) & 1, w);
           if (!ok) break;
           mbar_arrive_expect_tx(bVfull + 8 * s, C::TILE_BYTES);
+          if (staged) {
+            // V^T prepared by the staging kernel: D rows x 32 keys per chunk,
+            // straight into the K-major V^T buffer the P V product reads.
 #pragma unroll
-          for (int c = 0; c < C::NCH; ++c)
-            tma_load_3d(sV + s * C::TILE_BYTES + c * C::CHUNK_BYTES, &tm_v, bVfull + 8 * s,
-                        c * C::CH_ELEMS, k_row0 + (kt0 + j) * BN, hc, pol_kv);
+            for (int c = 0; c < BN / 32; ++c)
+              tma_load_3d(sVT + s * C::TILE_BYTES + c * C::VT_CHUNK_BYTES, &tm_v, bVfull + 8 * s,
+                          (kt0 + j) * BN + 32 * c, 0, hc, pol_kv);
+          } else {
+#pragma unroll
+            for (int c = 0; c < C::NCH; ++c)
+              tma_load_3d(sV + s * C::TILE_BYTES + c * C::CHUNK_BYTES, &tm_v, bVfull + 8 * s,
+                          c * C::CH_ELEMS, k_row0 + (kt0 + j) * BN, hc, pol_kv);
+          }
           ++nv;
         }
       }
@@ -322,7 +339,7 @@ __global__ void __launch_bounds__(224, 1)
       for (int j = 0; ok && j < n_kt; ++j) {
         if (j >= C::NS && !(ok = bounded_wait(bOdone + 8 * b, bph ^ 1, w))) break;
         // fp32 path: K_j must first be rounded to tf32 by the softmax warps
-        if (!(ok = bounded_wait((TF32 ? bKready : bKfull) + 8 * s, sph, w))) break;
+        if (!(ok = bounded_wait(((TF32 && !staged) ? bKready : bKfull) + 8 * s, sph, w))) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem + b * 128;
         const uint32_t kb = sK + s * C::TILE_BYTES;
@@ -361,9 +378,9 @@ __global__ void __launch_bounds__(224, 1)
       int b = 0, bph = 0;   // score buffer of tile j and the parity of its use
       int s = 0, sph = 0;   // V stage of tile j and its parity
       for (int j = 0; ok && j < n_kt; ++j) {
-        // P_j ready (fp32 path: also V_j^T written).
+        // P_j ready (fp32 path: also V_j^T written), V_j (or V_j^T) loaded.
         if (!(ok = bounded_wait(bPfull + 8 * b, bph, w))) break;
-        if constexpr (!TF32) {
+        if (!TF32 || staged) {
           if (!(ok = bounded_wait(bVfull + 8 * s, sph, w))) break;
         }
         tc_fence_after();
@@ -383,7 +400,7 @@ __global__ void __launch_bounds__(224, 1)
           umma_ts<TF32>(tmem + C::COL_O, a_tmem + kk * 8, bdesc, kIdescPV,
                         (j > 0 || kk > 0) ? 1u : 0u);
         }
-        if constexpr (!TF32) tc_commit(bVempty + 8 * s);
+        if (!TF32 || staged) tc_commit(bVempty + 8 * s);
         tc_commit(bOdone + 8 * b);
         if (++b == C::NS) { b = 0; bph ^= 1; }
         if (++s == C::VST) { s = 0; sph ^= 1; }
@@ -491,12 +508,12 @@ __global__ void __launch_bounds__(224, 1)
       tc_fence_before();
       mbar_arrive(bQ);
     }
-    if constexpr (TF32) ok = round_k_row(0);
+    if (TF32 && !staged) ok = round_k_row(0);
 
     int buf = 0, bph = 0;            // score buffer of tile j and the parity of its use
     int pbuf = C::NS - 1, pbph = 1;  // the same for tile j - 1
     for (int j = 0; ok && j < n_kt; ++j) {
-      if constexpr (TF32) {
+      if (TF32 && !staged) {
         // the next K tile is rounded before this tile's softmax so that
         // S_{j+1} = Q K_{j+1}^T still overlaps it
         if (j + 1 < n_kt && !(ok = round_k_row(j + 1))) break;
@@ -617,7 +634,7 @@ __global__ void __launch_bounds__(224, 1)
         upk2(acc[1], b0, b1);
         l += (a0 + a1) + (b0 + b1);
       }
-      if constexpr (TF32) {
+      if (TF32 && !staged) {
         // V^T buffer j % NVT was last read by P_{j-NVT} V_{j-NVT}.  With two
         // buffers that completed before S_j was issued; with one (D = 128)
         // P_{j-1} V_{j-1} may still be running.

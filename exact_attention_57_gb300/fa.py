@@ -31,7 +31,8 @@ FA_DTYPE_F16 = 3
 
 EXPORTED = ("fa_fwd", "fa_fwd_host", "fa_fwd_status", "fa_status_string", "fa_version",
             "fa_set_test_hooks", "fa_fwd_noalloc", "fa_fwd_splitkv", "fa_fwd_splitkv_workspace",
-            "fa_fwd_varlen", "fa_bwd", "fa_bwd_workspace")
+            "fa_fwd_varlen", "fa_bwd", "fa_bwd_workspace", "fa_fwd_staged",
+            "fa_fwd_staged_workspace")
 
 _lib = None
 
@@ -64,6 +65,11 @@ def load(path: str | None = None):
     lib.fa_fwd_splitkv_workspace.restype = ctypes.c_ulonglong
     lib.fa_fwd_varlen.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i, i, vp]
     lib.fa_fwd_varlen.restype = i
+    lib.fa_fwd_staged.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, i, vp,
+                                  ctypes.c_ulonglong, vp]
+    lib.fa_fwd_staged.restype = i
+    lib.fa_fwd_staged_workspace.argtypes = [i, i, i, i, i]
+    lib.fa_fwd_staged_workspace.restype = ctypes.c_ulonglong
     lib.fa_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, i, i, vp,
                            ctypes.c_ulonglong, vp]
     lib.fa_bwd.restype = i
@@ -155,6 +161,16 @@ def attention_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int,
     if st != FA_OK:
         raise FaError(st, "fa_fwd_varlen")
     return out, lse
+
+
+def fa_fwd_staged(q, k, v, o, lse, B, H, Nq, Nk, d, scale, causal, dtype, workspace,
+                  workspace_bytes, stream) -> int:
+    return load().fa_fwd_staged(q, k, v, o, lse, B, H, Nq, Nk, d, float(scale), int(causal),
+                                int(dtype), workspace, int(workspace_bytes), stream)
+
+
+def fa_fwd_staged_workspace(B, H, Nk, d, dtype) -> int:
+    return load().fa_fwd_staged_workspace(B, H, Nk, d, dtype)
 
 
 def fa_bwd(q, k, v, o, lse, dout, dq, dk, dv, B, H, Nq, Nk, d, scale, causal, dtype,
@@ -249,14 +265,16 @@ def _dtype_code(t, impl: str) -> int:
 
 
 def attention(q, k, v, scale: float | None = None, causal: bool = False, impl: str = "tc",
-              out=None, lse=None, stream=None, num_splits: int | None = None):
+              out=None, lse=None, stream=None, num_splits: int | None = None,
+              staged: bool = False):
     """O, LSE for contiguous CUDA tensors q [B,H,Nq,d], k/v [B,H,Nk,d].
 
     impl "tc": bf16 / fp16 -> tcgen05 kind::f16, fp32 -> tcgen05 kind::tf32;
     impl "simt": fp32 only, plain fp32 kernel.  num_splits (tensor-core
     dtypes): split each query tile's key range into that many chunks (0 =
     automatic) through fa_fwd_splitkv, with a torch-allocated workspace.
-    Raises FaError on failure.
+    staged (fp32, impl "tc"): run fa_fwd_staged, converting K and V once per
+    call into a torch-allocated workspace.  Raises FaError on failure.
     """
     import torch
     if not (q.is_cuda and k.is_cuda and v.is_cuda):
@@ -281,7 +299,14 @@ def attention(q, k, v, scale: float | None = None, causal: bool = False, impl: s
     if stream is None:
         stream = torch.cuda.current_stream(q.device).cuda_stream
     with torch.cuda.device(q.device):
-        if num_splits is None:
+        if staged and code == FA_DTYPE_F32:
+            ws_bytes = fa_fwd_staged_workspace(B, H, Nk, d, code)
+            ws = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=q.device)
+            st = fa_fwd_staged(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                               lse.data_ptr(), B, H, Nq, Nk, d, scale, int(bool(causal)), code,
+                               ws.data_ptr(), ws_bytes, stream)
+            where = "fa_fwd_staged"
+        elif num_splits is None:
             st = fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
                         lse.data_ptr(), B, H, Nq, Nk, d, scale, int(bool(causal)), code, stream)
             where = "fa_fwd"

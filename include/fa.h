@@ -197,6 +197,33 @@ int fa_fwd_varlen(const void *q, const void *k, const void *v, void *o, float *l
                   int causal, int dtype, void *stream);
 
 /*
+ * fa_fwd_staged — the forward with a caller-provided staging area.  For
+ * FA_DTYPE_F32 (tcgen05 kind::tf32) a pre-pass rounds K to tf32 and writes V,
+ * rounded and transposed, into the K-major V^T layout the tf32 P V product
+ * takes, once per call; the kernel then loads both ready-made instead of
+ * every query-tile CTA converting the same tiles again.  Same results as
+ * fa_fwd (the same rounding, applied once).  Other dtypes have nothing to
+ * stage and run fa_fwd (workspace may then be NULL).
+ *
+ * Arguments q .. dtype and stream as for fa_fwd.
+ * workspace        FA_DTYPE_F32: caller-owned device memory, 256-byte
+ *                  aligned, of at least fa_fwd_staged_workspace(B, H, Nk, d,
+ *                  dtype) bytes, not overlapping q, k, v, o or lse.  Calls
+ *                  that share a workspace must not overlap on the GPU.
+ * Returns FA_ERR_INVALID_ARG for a missing, misaligned, short or overlapping
+ * workspace (fp32), before anything is enqueued.
+ */
+int fa_fwd_staged(const void *q, const void *k, const void *v, void *o, float *lse,
+                  int B, int H, int Nq, int Nk, int d, float scale, int causal,
+                  int dtype, void *workspace, unsigned long long workspace_bytes,
+                  void *stream);
+
+/* Bytes of workspace fa_fwd_staged needs: for FA_DTYPE_F32, B*H*Nk*d floats
+ * (K in tf32) plus B*H*d*ceil(Nk/128)*128 floats (V^T), each part rounded up
+ * to 256 bytes; 0 for other dtypes and for invalid arguments. */
+unsigned long long fa_fwd_staged_workspace(int B, int H, int Nk, int d, int dtype);
+
+/*
  * fa_bwd — gradients of the forward for an upstream gradient dout: the
  * backward kernel of "flash_attention_2.cu"
  * (leloykun/flash-hyperbolic-attention-minimal), with the probabilities

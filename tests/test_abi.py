@@ -194,3 +194,33 @@ def test_bwd_invalid_arguments(lib, kw):
 ], ids=lambda kw: ",".join(f"{k}={v}" for k, v in kw.items()))
 def test_bwd_unsupported_problems(lib, kw):
     assert call_bwd(**kw) == fa.FA_ERR_UNSUPPORTED
+
+
+def test_staged_workspace_size(lib):
+    """fp32: B*H*Nk*d + B*H*d*ceil(Nk/128)*128 floats, parts rounded up to 256
+    bytes; other dtypes stage nothing."""
+    up = lambda n: (n + 255) // 256 * 256
+    for B, H, Nk, d in [(1, 1, 1, 64), (4, 4, 4096, 64), (2, 3, 300, 128), (1, 2, 77, 32)]:
+        pad = (Nk + 127) // 128 * 128
+        assert (fa.fa_fwd_staged_workspace(B, H, Nk, d, fa.FA_DTYPE_F32)
+                == up(B * H * Nk * d * 4) + up(B * H * d * pad * 4))
+    for dt in (fa.FA_DTYPE_BF16, fa.FA_DTYPE_F16, fa.FA_DTYPE_F32_SIMT):
+        assert fa.fa_fwd_staged_workspace(1, 1, 128, 64, dt) == 0
+    assert fa.fa_fwd_staged_workspace(0, 1, 128, 64, fa.FA_DTYPE_F32) == 0
+
+
+@pytest.mark.parametrize("kw", [
+    dict(ws=None), dict(ws=WS + 16), dict(ws_bytes=1000), dict(ws=Q), dict(ws=O - 64),
+    dict(q=None), dict(Nk=0), dict(d=0),
+], ids=lambda kw: ",".join(f"{k}={v}" for k, v in kw.items()))
+def test_staged_invalid_arguments(lib, kw):
+    """fp32 staging refuses a missing, misaligned, short or overlapping
+    workspace before any device work."""
+    a = dict(q=Q, ws=WS, ws_bytes=None, Nk=16, d=64)
+    a.update(kw)
+    wsb = a["ws_bytes"]
+    if wsb is None:
+        wsb = fa.fa_fwd_staged_workspace(1, 1, max(a["Nk"], 1), max(a["d"], 1), fa.FA_DTYPE_F32)
+    r = fa.fa_fwd_staged(a["q"], K, V, O, L, 1, 1, 16, a["Nk"], a["d"], 0.125, 0,
+                         fa.FA_DTYPE_F32, a["ws"], wsb, None)
+    assert r == fa.FA_ERR_INVALID_ARG
