@@ -661,7 +661,9 @@ extern "C" int fa_bwd(const void *q, const void *k, const void *v, const void *o
       if (overlap(out[a].p, out[a].n, out[b].p, out[b].n)) return FA_ERR_INVALID_ARG;
   }
   if (dtype != FA_DTYPE_BF16 && dtype != FA_DTYPE_F16) return FA_ERR_UNSUPPORTED;
-  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;  // dK, dV of d = 256 do not fit in TMEM
+  // d = 32 runs zero-padded on the d = 64 kernel; dK, dV of d = 256 do not
+  // fit in tensor memory.
+  if (d != 32 && d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
 
   unsigned *status = nullptr;
   if ((rc = device_setup(&status)) != FA_OK) return rc;
@@ -691,6 +693,7 @@ extern "C" int fa_bwd(const void *q, const void *k, const void *v, const void *o
   p.Nq_pad = p.n_qtiles * fa::BM;
   p.scale = scale;
   p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+  p.d_io = d == 32 ? 32 : 0;
   const unsigned long long lim = g_wait_limit_ns.load();
   p.wait_limit_ns = lim ? lim : fa::kDefaultWaitLimitNs;
   const int half = dtype == FA_DTYPE_F16 ? 1 : 0;
@@ -699,10 +702,10 @@ extern "C" int fa_bwd(const void *q, const void *k, const void *v, const void *o
                                       half, s);
   if (e != cudaSuccess) return FA_ERR_CUDA;
   if (half)
-    e = (d == 64) ? fa::launch_bwd_f16_d64(mq, mk, mv, mdo, p, B, causal, s)
+    e = (d <= 64) ? fa::launch_bwd_f16_d64(mq, mk, mv, mdo, p, B, causal, s)
                   : fa::launch_bwd_f16_d128(mq, mk, mv, mdo, p, B, causal, s);
   else
-    e = (d == 64) ? fa::launch_bwd_bf16_d64(mq, mk, mv, mdo, p, B, causal, s)
+    e = (d <= 64) ? fa::launch_bwd_bf16_d64(mq, mk, mv, mdo, p, B, causal, s)
                   : fa::launch_bwd_bf16_d128(mq, mk, mv, mdo, p, B, causal, s);
   if (e != cudaSuccess) return FA_ERR_CUDA;
   e = fa::launch_bwd_convert(p.dq_acc, dq, static_cast<long long>(BH) * Nq * d, half, s);

@@ -133,6 +133,10 @@ __global__ void __launch_bounds__(320, 1)
   // Query tiles that see this key tile (top-left causal: query >= key).
   const int i_first = CAUSAL ? jt : 0;
   const int n_it = max(0, p.n_qtiles - i_first);
+  // Head dim of the tensors in memory: D, or less when a narrower head dim
+  // runs zero-padded to D (the TMA loads zero-fill the missing columns; the
+  // plain dQ, dK, dV writes below stop at dio).
+  const int dio = p.d_io > 0 ? p.d_io : D;
 
   if (threadIdx.x == 0) {
     mbar_init(bKV, 1);
@@ -373,16 +377,16 @@ __global__ void __launch_bounds__(320, 1)
         ok = __all_sync(kFullMask, bounded_wait(bDQfull + 8 * h, it & 1, w));
         if (!ok) break;
         tc_fence_after();
-        if (r < D) {   // whole warps
+        if (r < dio) {   // whole warps (dio is a multiple of 32)
           uint32_t v[32];
           tmem_ld32(tmem + lane_off + col + C::DP_OFF + cq, v);
           tmem_ld_wait();
           reg_fence32(v);
           const int qbase = qt * BM + h * C::HQ + cq;
-          float *dst = p.dq_acc + (static_cast<size_t>(bh) * p.Nq + qbase) * D + r;
+          float *dst = p.dq_acc + (static_cast<size_t>(bh) * p.Nq + qbase) * dio + r;
 #pragma unroll
           for (int i = 0; i < 32; ++i)
-            if (qbase + i < p.Nq) red_add(dst + static_cast<size_t>(i) * D, __uint_as_float(v[i]));
+            if (qbase + i < p.Nq) red_add(dst + static_cast<size_t>(i) * dio, __uint_as_float(v[i]));
         }
         tc_fence_before();
         mbar_arrive(bDQfree + 8 * h);
@@ -397,7 +401,7 @@ __global__ void __launch_bounds__(320, 1)
       tc_fence_after();
       const int key = k0 + r;
       uint8_t *dst = static_cast<uint8_t *>(g == 0 ? p.dv : p.dk) +
-                     (static_cast<size_t>(bh) * p.Nk + key) * D * 2;
+                     (static_cast<size_t>(bh) * p.Nk + key) * dio * 2;
       const uint32_t colv = g == 0 ? C::COL_DV : C::COL_DK;
 #pragma unroll
       for (int c = 0; c < D; c += 32) {
@@ -411,7 +415,7 @@ __global__ void __launch_bounds__(320, 1)
 #pragma unroll
           for (int i = 0; i < 32; ++i) v[i] = 0u;
         }
-        if (key < p.Nk) {
+        if (key < p.Nk && c < dio) {
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
             uint4 val;

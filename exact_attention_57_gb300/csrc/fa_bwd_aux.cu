@@ -52,21 +52,22 @@ __global__ void __launch_bounds__(32 * kPrepRowsPerBlock)
   // lane covers elements [2*lane + 64*i, +2)
   float acc = 0.f;
 #pragma unroll
-  for (int i = 0; i < D / 64; ++i) {
-    const size_t idx = row * D + 64 * i + 2 * lane;
-    const float2 a = load2(o, idx, half != 0), b = load2(dout, idx, half != 0);
-    acc = fmaf(a.x, b.x, acc);
-    acc = fmaf(a.y, b.y, acc);
+  for (int i = 0; i < (D + 63) / 64; ++i) {
+    if (64 * i + 2 * lane < D) {
+      const size_t idx = row * D + 64 * i + 2 * lane;
+      const float2 a = load2(o, idx, half != 0), b = load2(dout, idx, half != 0);
+      acc = fmaf(a.x, b.x, acc);
+      acc = fmaf(a.y, b.y, acc);
+    }
   }
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
   float *zrow = dq_acc + row * D;
+  // D / 4 float4 per row, 32 per pass
 #pragma unroll
-  for (int i = 0; i < D / 128; ++i)
-    reinterpret_cast<float4 *>(zrow)[32 * i + lane] = make_float4(0.f, 0.f, 0.f, 0.f);
-  if constexpr (D % 128 != 0) {
-    if (lane < 16) reinterpret_cast<float4 *>(zrow)[(D / 128) * 32 + lane] = make_float4(0.f, 0.f, 0.f, 0.f);
-  }
+  for (int i = 0; i < (D / 4 + 31) / 32; ++i)
+    if (32 * i + lane < D / 4)
+      reinterpret_cast<float4 *>(zrow)[32 * i + lane] = make_float4(0.f, 0.f, 0.f, 0.f);
   if (lane == 0) {
     lse2[prow] = lse[row] * 1.4426950408889634f;
     dd[prow] = acc;
@@ -101,7 +102,10 @@ cudaError_t launch_bwd_prep(const void *o, const void *dout, const float *lse, f
                             cudaStream_t s) {
   const long long rows = static_cast<long long>(BH) * Nq_pad;
   const unsigned blocks = static_cast<unsigned>((rows + kPrepRowsPerBlock - 1) / kPrepRowsPerBlock);
-  if (d == 64)
+  if (d == 32)
+    fa_bwd_prep_kernel<32><<<blocks, 32 * kPrepRowsPerBlock, 0, s>>>(o, dout, lse, lse2, dd,
+                                                                     dq_acc, BH, Nq, Nq_pad, half);
+  else if (d == 64)
     fa_bwd_prep_kernel<64><<<blocks, 32 * kPrepRowsPerBlock, 0, s>>>(o, dout, lse, lse2, dd,
                                                                      dq_acc, BH, Nq, Nq_pad, half);
   else
@@ -112,7 +116,7 @@ cudaError_t launch_bwd_prep(const void *o, const void *dout, const float *lse, f
 
 cudaError_t launch_bwd_convert(const float *dq_acc, void *dq, long long n, int half,
                                cudaStream_t s) {
-  const long long n8 = n / 8;  // n is a multiple of 64 (d is 64 or 128)
+  const long long n8 = n / 8;  // n is a multiple of 32 (d is 32, 64 or 128)
   const unsigned blocks = static_cast<unsigned>((n8 + 255) / 256);
   fa_bwd_convert_kernel<<<blocks, 256, 0, s>>>(dq_acc, dq, n8, half);
   return cudaGetLastError();

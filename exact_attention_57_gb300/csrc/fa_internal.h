@@ -121,6 +121,7 @@ struct BwdParams {
   float scale;                    // signed softmax scale
   float scale_log2;               // scale * log2(e), signed
   unsigned long long wait_limit_ns;
+  int d_io = 0;                   // head dim in memory when below the kernel's D (0 = D)
 };
 
 cudaError_t launch_bwd_bf16_d64(const CUtensorMap &q, const CUtensorMap &k, const CUtensorMap &v,

@@ -237,7 +237,7 @@ unsigned long long fa_fwd_staged_workspace(int B, int H, int Nk, int d, int dtyp
  * dout             upstream gradient [B,H,Nq,d], the type of q.
  * dq [B,H,Nq,d], dk and dv [B,H,Nk,d]: outputs, the type of q, every element
  *                  written (keys that no query sees get zero gradients).
- * dtype            FA_DTYPE_BF16 or FA_DTYPE_F16 with d 64 or 128 (tcgen05
+ * dtype            FA_DTYPE_BF16 or FA_DTYPE_F16 with d 32, 64 or 128 (tcgen05
  *                  kind::f16; P and dS are rounded to the input type, the
  *                  products accumulate in fp32); anything else is
  *                  FA_ERR_UNSUPPORTED.

@@ -38,6 +38,8 @@ CASES = [
     (1, 2, 256, 300, 64, False, DTYPE_BF16, 0.0),
     (1, 4, 1024, 1024, 128, True, DTYPE_BF16, None),
     (1, 4, 1024, 1024, 64, False, DTYPE_BF16, None),
+    (2, 2, 300, 300, 32, True, DTYPE_BF16, None),     # runs zero-padded on the d = 64 kernel
+    (1, 3, 200, 457, 32, False, DTYPE_F16, None),
 ]
 
 
@@ -100,8 +102,8 @@ def test_bwd_rejects_bad_arguments():
     bad[6] = q.data_ptr()   # dq over q
     assert fa.fa_bwd(*bad, ws.data_ptr(), need, s) == fa.FA_ERR_INVALID_ARG
     bad = list(args)
-    bad[13] = 32   # head dim outside the compiled set (extents within the buffers)
-    assert fa.fa_bwd(*bad, ws.data_ptr(), fa.fa_bwd_workspace(1, 1, 128, 32),
+    bad[13] = 48   # head dim outside the compiled set (extents within the buffers)
+    assert fa.fa_bwd(*bad, ws.data_ptr(), fa.fa_bwd_workspace(1, 1, 128, 48),
                      s) == fa.FA_ERR_UNSUPPORTED
     assert fa.fa_bwd(*args, ws.data_ptr(), need, s) == fa.FA_OK
     assert fa.fa_fwd_status(s)[0] == fa.FA_OK
