@@ -811,3 +811,115 @@ extern "C" int fa_fwd_staged(const void *q, const void *k, const void *v, void *
   cudaError_t e = launch_tc_any(mq, mk, mv, mo, p, B, causal, d, dtype, s);
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
+
+// ---------------------------------------------------------------------------
+// Backward over variable-length batches.
+// ---------------------------------------------------------------------------
+namespace {
+
+void bwd_varlen_parts(int B, int H, int total_q, int max_q, int d, size_t *acc, size_t *row) {
+  const size_t pad = static_cast<size_t>(ceil_div(max_q, fa::BM)) * fa::BM;
+  *acc = round256(static_cast<size_t>(total_q) * H * d * sizeof(float));
+  *row = round256(static_cast<size_t>(H) * B * pad * sizeof(float));
+}
+
+}  // namespace
+
+extern "C" unsigned long long fa_bwd_varlen_workspace(int B, int H, int total_q, int max_seqlen_q,
+                                                      int d) {
+  if (B < 1 || H < 1 || total_q < 1 || max_seqlen_q < 1 || d < 1) return 0;
+  size_t acc, row;
+  bwd_varlen_parts(B, H, total_q, max_seqlen_q, d, &acc, &row);
+  return acc + 2 * row;
+}
+
+extern "C" int fa_bwd_varlen(const void *q, const void *k, const void *v, const void *o,
+                             const float *lse, const void *dout, void *dq, void *dk, void *dv,
+                             const int *cu_seqlens_q, const int *cu_seqlens_k, int B, int H,
+                             int total_q, int total_k, int max_seqlen_q, int max_seqlen_k, int d,
+                             float scale, int causal, int dtype, void *workspace,
+                             unsigned long long workspace_bytes, void *stream) {
+  if (!cu_seqlens_q || !cu_seqlens_k) return FA_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(cu_seqlens_q) % 4 || reinterpret_cast<uintptr_t>(cu_seqlens_k) % 4)
+    return FA_ERR_INVALID_ARG;
+  if (max_seqlen_q < 1 || max_seqlen_q > total_q || max_seqlen_k < 1 || max_seqlen_k > total_k)
+    return FA_ERR_INVALID_ARG;
+  // The tensors as one [1, H, total, d]-sized problem for the shared checks.
+  int rc = validate(q, k, v, o, lse, 1, H, total_q, total_k, d, scale, causal, dtype);
+  if (rc != FA_OK) return rc;
+  if (B < 1 || B > 65535) return FA_ERR_INVALID_ARG;
+  if (!dout || !dq || !dk || !dv || !workspace) return FA_ERR_INVALID_ARG;
+  for (const void *ptr : {dout, static_cast<const void *>(dq), static_cast<const void *>(dk),
+                          static_cast<const void *>(dv)})
+    if (reinterpret_cast<uintptr_t>(ptr) % 16 != 0) return FA_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(workspace) % 256 != 0) return FA_ERR_INVALID_ARG;
+  size_t acc, row;
+  bwd_varlen_parts(B, H, total_q, max_seqlen_q, d, &acc, &row);
+  const size_t need = acc + 2 * row;
+  if (workspace_bytes < need) return FA_ERR_INVALID_ARG;
+  const size_t es = elem_size(dtype);
+  const size_t qn = static_cast<size_t>(total_q) * H * d * es;
+  const size_t kn = static_cast<size_t>(total_k) * H * d * es;
+  const size_t ln = static_cast<size_t>(H) * total_q * sizeof(float);
+  const struct { const void *p; size_t n; } in[] = {{q, qn}, {k, kn}, {v, kn}, {o, qn},
+                                                    {lse, ln}, {dout, qn}};
+  const struct { const void *p; size_t n; } out[] = {{dq, qn}, {dk, kn}, {dv, kn},
+                                                     {workspace, need}};
+  for (int a = 0; a < 4; ++a) {
+    for (const auto &x : in)
+      if (overlap(out[a].p, out[a].n, x.p, x.n)) return FA_ERR_INVALID_ARG;
+    for (int b = a + 1; b < 4; ++b)
+      if (overlap(out[a].p, out[a].n, out[b].p, out[b].n)) return FA_ERR_INVALID_ARG;
+  }
+  if (dtype != FA_DTYPE_BF16 && dtype != FA_DTYPE_F16) return FA_ERR_UNSUPPORTED;
+  if (d != 32 && d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+
+  unsigned *status = nullptr;
+  if ((rc = device_setup(&status)) != FA_OK) return rc;
+  if ((rc = get_encoder()) != FA_OK) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  CUtensorMap mq, mk, mv, mdo;
+  if ((rc = encode_map_tokens(&mq, q, dtype, total_q, H, d)) != FA_OK) return rc;
+  if ((rc = encode_map_tokens(&mk, k, dtype, total_k, H, d)) != FA_OK) return rc;
+  if ((rc = encode_map_tokens(&mv, v, dtype, total_k, H, d)) != FA_OK) return rc;
+  if ((rc = encode_map_tokens(&mdo, dout, dtype, total_q, H, d)) != FA_OK) return rc;
+
+  fa::BwdParams p;
+  p.dq_acc = static_cast<float *>(workspace);
+  float *lse2 = reinterpret_cast<float *>(static_cast<char *>(workspace) + acc);
+  float *dd = reinterpret_cast<float *>(static_cast<char *>(workspace) + acc + row);
+  p.lse2 = lse2;
+  p.dd = dd;
+  p.dk = dk;
+  p.dv = dv;
+  p.status = status;
+  p.H = H;
+  p.Nq = max_seqlen_q;
+  p.Nk = max_seqlen_k;
+  p.n_qtiles = ceil_div(max_seqlen_q, fa::BM);
+  p.n_ktiles = ceil_div(max_seqlen_k, fa::BN);  // the grid covers the longest sequence
+  p.Nq_pad = p.n_qtiles * fa::BM;
+  p.scale = scale;
+  p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+  const unsigned long long lim = g_wait_limit_ns.load();
+  p.wait_limit_ns = lim ? lim : fa::kDefaultWaitLimitNs;
+  p.d_io = d == 32 ? 32 : 0;
+  p.cu_q = cu_seqlens_q;
+  p.cu_k = cu_seqlens_k;
+  p.total_q = total_q;
+  p.total_k = total_k;
+  const int half = dtype == FA_DTYPE_F16 ? 1 : 0;
+
+  cudaError_t e = fa::launch_bwd_prep_varlen(o, dout, lse, lse2, dd, p.dq_acc, cu_seqlens_q, B, H,
+                                             total_q, p.Nq_pad, d, half, s);
+  if (e != cudaSuccess) return FA_ERR_CUDA;
+  if (half)
+    e = (d <= 64) ? fa::launch_bwd_f16_d64(mq, mk, mv, mdo, p, B, causal, s)
+                  : fa::launch_bwd_f16_d128(mq, mk, mv, mdo, p, B, causal, s);
+  else
+    e = (d <= 64) ? fa::launch_bwd_bf16_d64(mq, mk, mv, mdo, p, B, causal, s)
+                  : fa::launch_bwd_bf16_d128(mq, mk, mv, mdo, p, B, causal, s);
+  if (e != cudaSuccess) return FA_ERR_CUDA;
+  e = fa::launch_bwd_convert(p.dq_acc, dq, static_cast<long long>(total_q) * H * d, half, s);
+  return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}

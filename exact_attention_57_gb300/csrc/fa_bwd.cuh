@@ -130,13 +130,40 @@ __global__ void __launch_bounds__(320, 1)
   const int jt = static_cast<int>(blockIdx.x);  // key tile
   const int bh = static_cast<int>(blockIdx.z) * p.H + static_cast<int>(blockIdx.y);
   const int k0 = jt * BN;
-  // Query tiles that see this key tile (top-left causal: query >= key).
-  const int i_first = CAUSAL ? jt : 0;
-  const int n_it = max(0, p.n_qtiles - i_first);
   // Head dim of the tensors in memory: D, or less when a narrower head dim
   // runs zero-padded to D (the TMA loads zero-fill the missing columns; the
   // plain dQ, dK, dV writes below stop at dio).
   const int dio = p.d_io > 0 ? p.d_io : D;
+  // This CTA's problem: rows [q_row0, q_row0 + Nq) of Q/dO/dQ and
+  // [k_row0, k_row0 + Nk) of K/V/dK/dV in TMA plane hc.  Element offsets of
+  // row 0 and the row stride: [B,H,N,d] (plane b*H+h, rows dio apart) or,
+  // for variable-length batches, token-major [total, H, d] (plane h, rows
+  // H*dio apart).
+  const bool varlen = p.cu_q != nullptr;
+  int Nq = p.Nq, Nk = p.Nk, q_row0 = 0, k_row0 = 0, hc = bh, n_qtiles = p.n_qtiles;
+  size_t row_base = static_cast<size_t>(bh) * p.Nq_pad;  // LSE/D rows of this problem
+  long long dq_base = static_cast<long long>(bh) * p.Nq * dio, dq_rs = dio;
+  long long kv_base = static_cast<long long>(bh) * p.Nk * dio, kv_rs = dio;
+  if (varlen) {
+    const int b = static_cast<int>(blockIdx.z), h = static_cast<int>(blockIdx.y);
+    // Offsets are clamped to [0, total] (row indices never leave the
+    // tensors) and lengths to the stated maxima (the padded LSE/D rows).
+    q_row0 = min(max(p.cu_q[b], 0), p.total_q);
+    k_row0 = min(max(p.cu_k[b], 0), p.total_k);
+    Nq = min(max(0, min(p.cu_q[b + 1], p.total_q) - q_row0), p.Nq);
+    Nk = min(max(0, min(p.cu_k[b + 1], p.total_k) - k_row0), p.Nk);
+    hc = h;
+    n_qtiles = (Nq + BM - 1) / BM;
+    row_base = (static_cast<size_t>(h) * gridDim.z + b) * p.Nq_pad;
+    dq_base = (static_cast<long long>(q_row0) * p.H + h) * dio;
+    dq_rs = static_cast<long long>(p.H) * dio;
+    kv_base = (static_cast<long long>(k_row0) * p.H + h) * dio;
+    kv_rs = dq_rs;
+    if (k0 >= Nk) return;  // the grid covers the longest sequence
+  }
+  // Query tiles that see this key tile (top-left causal: query >= key).
+  const int i_first = CAUSAL ? jt : 0;
+  const int n_it = max(0, n_qtiles - i_first);
 
   if (threadIdx.x == 0) {
     mbar_init(bKV, 1);
@@ -183,8 +210,8 @@ __global__ void __launch_bounds__(320, 1)
       mbar_arrive_expect_tx(bKV, 2 * C::TILE_BYTES);
 #pragma unroll
       for (int c = 0; c < C::NCH; ++c) {
-        tma_load_3d(sK + c * C::CHUNK_BYTES, &tm_k, bKV, c * C::CH_ELEMS, k0, bh, pol_kv);
-        tma_load_3d(sV + c * C::CHUNK_BYTES, &tm_v, bKV, c * C::CH_ELEMS, k0, bh, pol_kv);
+        tma_load_3d(sK + c * C::CHUNK_BYTES, &tm_k, bKV, c * C::CH_ELEMS, k_row0 + k0, hc, pol_kv);
+        tma_load_3d(sV + c * C::CHUNK_BYTES, &tm_v, bKV, c * C::CH_ELEMS, k_row0 + k0, hc, pol_kv);
       }
       int issued = 0;
       bool ok = true;
@@ -197,11 +224,11 @@ __global__ void __launch_bounds__(320, 1)
 #pragma unroll
         for (int c = 0; c < C::NCH; ++c) {
           tma_load_3d(sQ + s * C::TILE_BYTES + c * C::CHUNK_BYTES, &tm_q, bar, c * C::CH_ELEMS,
-                      q0, bh, pol_q);
+                      q_row0 + q0, hc, pol_q);
           tma_load_3d(sDO + s * C::TILE_BYTES + c * C::CHUNK_BYTES, &tm_do, bar,
-                      c * C::CH_ELEMS, q0, bh, pol_q);
+                      c * C::CH_ELEMS, q_row0 + q0, hc, pol_q);
         }
-        const size_t roff = static_cast<size_t>(bh) * p.Nq_pad + q0;
+        const size_t roff = row_base + q0;
         bulk_load(sRow + s * C::ROW_BYTES, p.lse2 + roff, 512, bar);
         bulk_load(sRow + s * C::ROW_BYTES + 512, p.dd + roff, 512, bar);
         ++issued;
@@ -312,6 +339,11 @@ __global__ void __launch_bounds__(320, 1)
       const float *lse2 = reinterpret_cast<const float *>(smem + C::OFF_ROW + s * C::ROW_BYTES);
       const float *dd = lse2 + 128;
       const bool diag = CAUSAL && qt == jt;   // key r sees query c only if r <= c
+      // Variable-length batches: rows past this sequence's keys or queries
+      // belong to the next sequence (not zero-filled), so their P is set to 0.
+      const int qlim = Nq - qt * BM;          // valid query columns [0, qlim)
+      const bool krow_ok = k0 + r < Nk;
+      const bool tail = varlen && (!krow_ok || qlim < BM);
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         const uint32_t col = C::COL_S0 + h * C::COL_HALF;
@@ -340,9 +372,9 @@ __global__ void __launch_bounds__(320, 1)
             float x0, x1;
             upk2(x2, x0, x1);
             float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
-            if (diag) {
-              if (c0 + c < r) p0 = 0.f;
-              if (c0 + c + 1 < r) p1 = 0.f;
+            if (diag || tail) {
+              if ((diag && c0 + c < r) || (tail && (!krow_ok || c0 + c >= qlim))) p0 = 0.f;
+              if ((diag && c0 + c + 1 < r) || (tail && (!krow_ok || c0 + c + 1 >= qlim))) p1 = 0.f;
             }
             const uint64_t g2 = fadd2(pk2(__uint_as_float(dr[c]), __uint_as_float(dr[c + 1])),
                                       pk2(-da, -db));
@@ -383,10 +415,10 @@ __global__ void __launch_bounds__(320, 1)
           tmem_ld_wait();
           reg_fence32(v);
           const int qbase = qt * BM + h * C::HQ + cq;
-          float *dst = p.dq_acc + (static_cast<size_t>(bh) * p.Nq + qbase) * dio + r;
+          float *dst = p.dq_acc + dq_base + qbase * dq_rs + r;
 #pragma unroll
           for (int i = 0; i < 32; ++i)
-            if (qbase + i < p.Nq) red_add(dst + static_cast<size_t>(i) * dio, __uint_as_float(v[i]));
+            if (qbase + i < Nq) red_add(dst + i * dq_rs, __uint_as_float(v[i]));
         }
         tc_fence_before();
         mbar_arrive(bDQfree + 8 * h);
@@ -401,7 +433,7 @@ __global__ void __launch_bounds__(320, 1)
       tc_fence_after();
       const int key = k0 + r;
       uint8_t *dst = static_cast<uint8_t *>(g == 0 ? p.dv : p.dk) +
-                     (static_cast<size_t>(bh) * p.Nk + key) * dio * 2;
+                     (kv_base + static_cast<long long>(key) * kv_rs) * 2;
       const uint32_t colv = g == 0 ? C::COL_DV : C::COL_DK;
 #pragma unroll
       for (int c = 0; c < D; c += 32) {
@@ -415,7 +447,7 @@ __global__ void __launch_bounds__(320, 1)
 #pragma unroll
           for (int i = 0; i < 32; ++i) v[i] = 0u;
         }
-        if (key < p.Nk && c < dio) {
+        if (key < Nk && c < dio) {
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
             uint4 val;

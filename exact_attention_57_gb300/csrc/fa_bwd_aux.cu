@@ -74,6 +74,56 @@ __global__ void __launch_bounds__(32 * kPrepRowsPerBlock)
   }
 }
 
+// Variable-length batches: padded row prow = (h*B + b)*Nq_pad + pos of the
+// LSE/D buffers; token t = cu_q[b] + pos of q/o/dout and dq_acc (token-major
+// [total_q, H, D]); lse [H, total_q].
+template <int D>
+__global__ void __launch_bounds__(32 * kPrepRowsPerBlock)
+    fa_bwd_prep_varlen_kernel(const void *__restrict__ o, const void *__restrict__ dout,
+                              const float *__restrict__ lse, float *__restrict__ lse2,
+                              float *__restrict__ dd, float *__restrict__ dq_acc,
+                              const int *__restrict__ cu_q, int B, int H, int total_q,
+                              int Nq_pad, int half) {
+  const int lane = threadIdx.x & 31;
+  const long long prow =
+      static_cast<long long>(blockIdx.x) * kPrepRowsPerBlock + (threadIdx.x >> 5);
+  if (prow >= static_cast<long long>(H) * B * Nq_pad) return;  // whole warp
+  const long long hb = prow / Nq_pad;
+  const int pos = static_cast<int>(prow - hb * Nq_pad);
+  const int b = static_cast<int>(hb % B), h = static_cast<int>(hb / B);
+  const int t0 = min(max(cu_q[b], 0), total_q);  // clamped, as in the kernel
+  const int nq = min(max(0, min(cu_q[b + 1], total_q) - t0), Nq_pad);
+  if (pos >= nq) {
+    if (lane == 0) {
+      lse2[prow] = INFINITY;
+      dd[prow] = 0.f;
+    }
+    return;
+  }
+  const size_t row = static_cast<size_t>(t0 + pos) * H + h;  // token-major row
+  float acc = 0.f;
+#pragma unroll
+  for (int i = 0; i < (D + 63) / 64; ++i) {
+    if (64 * i + 2 * lane < D) {
+      const size_t idx = row * D + 64 * i + 2 * lane;
+      const float2 a = load2(o, idx, half != 0), c = load2(dout, idx, half != 0);
+      acc = fmaf(a.x, c.x, acc);
+      acc = fmaf(a.y, c.y, acc);
+    }
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+  float *zrow = dq_acc + row * D;
+#pragma unroll
+  for (int i = 0; i < (D / 4 + 31) / 32; ++i)
+    if (32 * i + lane < D / 4)
+      reinterpret_cast<float4 *>(zrow)[32 * i + lane] = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (lane == 0) {
+    lse2[prow] = lse[static_cast<size_t>(h) * total_q + t0 + pos] * 1.4426950408889634f;
+    dd[prow] = acc;
+  }
+}
+
 __global__ void fa_bwd_convert_kernel(const float *__restrict__ src, void *__restrict__ dst,
                                       long long n8, int half) {
   const long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
@@ -111,6 +161,24 @@ cudaError_t launch_bwd_prep(const void *o, const void *dout, const float *lse, f
   else
     fa_bwd_prep_kernel<128><<<blocks, 32 * kPrepRowsPerBlock, 0, s>>>(o, dout, lse, lse2, dd,
                                                                       dq_acc, BH, Nq, Nq_pad, half);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_prep_varlen(const void *o, const void *dout, const float *lse, float *lse2,
+                                   float *dd, float *dq_acc, const int *cu_q, int B, int H,
+                                   int total_q, int Nq_pad, int d, int half, cudaStream_t s) {
+  const long long rows = static_cast<long long>(H) * B * Nq_pad;
+  const unsigned blocks = static_cast<unsigned>((rows + kPrepRowsPerBlock - 1) / kPrepRowsPerBlock);
+  const dim3 block(32 * kPrepRowsPerBlock);
+  if (d == 32)
+    fa_bwd_prep_varlen_kernel<32><<<blocks, block, 0, s>>>(o, dout, lse, lse2, dd, dq_acc, cu_q, B,
+                                                           H, total_q, Nq_pad, half);
+  else if (d == 64)
+    fa_bwd_prep_varlen_kernel<64><<<blocks, block, 0, s>>>(o, dout, lse, lse2, dd, dq_acc, cu_q, B,
+                                                           H, total_q, Nq_pad, half);
+  else
+    fa_bwd_prep_varlen_kernel<128><<<blocks, block, 0, s>>>(o, dout, lse, lse2, dd, dq_acc, cu_q, B,
+                                                            H, total_q, Nq_pad, half);
   return cudaGetLastError();
 }
 

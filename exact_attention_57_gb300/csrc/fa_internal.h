@@ -122,6 +122,11 @@ struct BwdParams {
   float scale_log2;               // scale * log2(e), signed
   unsigned long long wait_limit_ns;
   int d_io = 0;                   // head dim in memory when below the kernel's D (0 = D)
+  // Variable-length batches (token-major [total, H, d]; LSE/D rows laid out
+  // [H][B][Nq_pad]): device offsets of B+1 entries each, or null.
+  const int *cu_q = nullptr;
+  const int *cu_k = nullptr;
+  int total_q = 0, total_k = 0;
 };
 
 cudaError_t launch_bwd_bf16_d64(const CUtensorMap &q, const CUtensorMap &k, const CUtensorMap &v,
@@ -141,6 +146,11 @@ cudaError_t launch_bwd_f16_d128(const CUtensorMap &q, const CUtensorMap &k, cons
 cudaError_t launch_bwd_prep(const void *o, const void *dout, const float *lse, float *lse2,
                             float *dd, float *dq_acc, int BH, int Nq, int Nq_pad, int d, int half,
                             cudaStream_t s);
+// The same for variable-length batches: rows [H][B][Nq_pad] of lse2 and dd,
+// dq_acc token-major [total_q, H, d].
+cudaError_t launch_bwd_prep_varlen(const void *o, const void *dout, const float *lse, float *lse2,
+                                   float *dd, float *dq_acc, const int *cu_q, int B, int H,
+                                   int total_q, int Nq_pad, int d, int half, cudaStream_t s);
 // dq = dq_acc rounded to the input type.
 cudaError_t launch_bwd_convert(const float *dq_acc, void *dq, long long n, int half,
                                cudaStream_t s);

@@ -167,8 +167,9 @@ __global__ void __launch_bounds__(224, 1)
   int n_qtiles = p.n_qtiles, n_ktiles = p.n_ktiles;
   if (p.cu_q != nullptr) {
     const int b = static_cast<int>(blockIdx.z);
-    q_row0 = p.cu_q[b];
-    k_row0 = p.cu_k[b];
+    // Offsets clamped to [0, total]: row indices never leave the tensors.
+    q_row0 = min(max(p.cu_q[b], 0), p.total_q);
+    k_row0 = max(p.cu_k[b], 0);
     Nq = max(0, min(p.cu_q[b + 1], p.total_q) - q_row0);
     Nk = max(0, p.cu_k[b + 1] - k_row0);
     hc = static_cast<int>(blockIdx.y);

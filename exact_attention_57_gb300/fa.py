@@ -32,7 +32,7 @@ FA_DTYPE_F16 = 3
 EXPORTED = ("fa_fwd", "fa_fwd_host", "fa_fwd_status", "fa_status_string", "fa_version",
             "fa_set_test_hooks", "fa_fwd_noalloc", "fa_fwd_splitkv", "fa_fwd_splitkv_workspace",
             "fa_fwd_varlen", "fa_bwd", "fa_bwd_workspace", "fa_fwd_staged",
-            "fa_fwd_staged_workspace")
+            "fa_fwd_staged_workspace", "fa_bwd_varlen", "fa_bwd_varlen_workspace")
 
 _lib = None
 
@@ -70,6 +70,11 @@ def load(path: str | None = None):
     lib.fa_fwd_staged.restype = i
     lib.fa_fwd_staged_workspace.argtypes = [i, i, i, i, i]
     lib.fa_fwd_staged_workspace.restype = ctypes.c_ulonglong
+    lib.fa_bwd_varlen.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i,
+                                  f, i, i, vp, ctypes.c_ulonglong, vp]
+    lib.fa_bwd_varlen.restype = i
+    lib.fa_bwd_varlen_workspace.argtypes = [i, i, i, i, i]
+    lib.fa_bwd_varlen_workspace.restype = ctypes.c_ulonglong
     lib.fa_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, i, i, vp,
                            ctypes.c_ulonglong, vp]
     lib.fa_bwd.restype = i
@@ -217,6 +222,46 @@ def attention_backward(q, k, v, out, lse, dout, scale: float | None = None,
                     workspace.numel() * workspace.element_size(), stream)
     if st != FA_OK:
         raise FaError(st, "fa_bwd")
+    return dq, dk, dv
+
+
+def fa_bwd_varlen(q, k, v, o, lse, dout, dq, dk, dv, cu_seqlens_q, cu_seqlens_k, B, H, total_q,
+                  total_k, max_seqlen_q, max_seqlen_k, d, scale, causal, dtype, workspace,
+                  workspace_bytes, stream) -> int:
+    return load().fa_bwd_varlen(q, k, v, o, lse, dout, dq, dk, dv, cu_seqlens_q, cu_seqlens_k, B,
+                                H, total_q, total_k, max_seqlen_q, max_seqlen_k, d, float(scale),
+                                int(causal), int(dtype), workspace, int(workspace_bytes), stream)
+
+
+def fa_bwd_varlen_workspace(B, H, total_q, max_seqlen_q, d) -> int:
+    return load().fa_bwd_varlen_workspace(B, H, total_q, max_seqlen_q, d)
+
+
+def attention_backward_varlen(q, k, v, out, lse, dout, cu_seqlens_q, cu_seqlens_k,
+                              max_seqlen_q: int, max_seqlen_k: int, scale: float | None = None,
+                              causal: bool = False, stream=None):
+    """Gradients (dq, dk, dv) of attention_varlen() for the upstream gradient
+    dout (token-major [total_q, H, d]).  Raises FaError on failure."""
+    import torch
+    total_q, H, d = q.shape
+    total_k = k.shape[0]
+    B = cu_seqlens_q.numel() - 1
+    code = _dtype_code(q, "tc")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ws_bytes = fa_bwd_varlen_workspace(B, H, total_q, max_seqlen_q, d)
+    ws = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=q.device)
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device).cuda_stream
+    with torch.cuda.device(q.device):
+        st = fa_bwd_varlen(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
+                           dout.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
+                           cu_seqlens_q.data_ptr(), cu_seqlens_k.data_ptr(), B, H, total_q,
+                           total_k, max_seqlen_q, max_seqlen_k, d, scale, int(bool(causal)), code,
+                           ws.data_ptr(), ws_bytes, stream)
+    if st != FA_OK:
+        raise FaError(st, "fa_bwd_varlen")
     return dq, dk, dv
 
 

@@ -261,6 +261,32 @@ int fa_bwd(const void *q, const void *k, const void *v, const void *o, const flo
 unsigned long long fa_bwd_workspace(int B, int H, int Nq, int d);
 
 /*
+ * fa_bwd_varlen — fa_bwd over a batch of sequences of different lengths
+ * packed end to end (the layout of fa_fwd_varlen): q, o, dout, dq
+ * [total_q, H, d]; k, v, dk, dv [total_k, H, d]; lse [H, total_q] from
+ * fa_fwd_varlen; cu_seqlens_q/k device int32 offsets (B+1 each, nondecreasing,
+ * from 0 to total_q / total_k, covering every token: rows outside every
+ * sequence get no dq).  Causal masking is top-left within each sequence;
+ * keys that no query sees get zero dk, dv.  max_seqlen_q, max_seqlen_k: the
+ * longest query and key lengths (1 .. total).  dtype, d, scale, causal as for
+ * fa_bwd.  workspace: at least fa_bwd_varlen_workspace(B, H, total_q,
+ * max_seqlen_q, d) bytes, 256-byte aligned (an fp32 dq accumulator and two
+ * floats per padded query row).  The offsets are read on the device and not
+ * checked on the host; every row index stays below total_q / total_k.
+ */
+int fa_bwd_varlen(const void *q, const void *k, const void *v, const void *o, const float *lse,
+                  const void *dout, void *dq, void *dk, void *dv,
+                  const int *cu_seqlens_q, const int *cu_seqlens_k, int B, int H,
+                  int total_q, int total_k, int max_seqlen_q, int max_seqlen_k, int d,
+                  float scale, int causal, int dtype, void *workspace,
+                  unsigned long long workspace_bytes, void *stream);
+
+/* Bytes of workspace fa_bwd_varlen needs: total_q*H*d floats plus
+ * 2*H*B*ceil(max_seqlen_q/128)*128 floats, parts rounded up to 256 bytes;
+ * 0 for invalid arguments. */
+unsigned long long fa_bwd_varlen_workspace(int B, int H, int total_q, int max_seqlen_q, int d);
+
+/*
  * fa_fwd_host — the same forward on HOST buffers.
  *
  * q_h, k_h, v_h   host inputs (pinned memory gives full copy speed).

@@ -224,3 +224,28 @@ def test_staged_invalid_arguments(lib, kw):
     r = fa.fa_fwd_staged(a["q"], K, V, O, L, 1, 1, 16, a["Nk"], a["d"], 0.125, 0,
                          fa.FA_DTYPE_F32, a["ws"], wsb, None)
     assert r == fa.FA_ERR_INVALID_ARG
+
+
+def test_bwd_varlen_workspace_size(lib):
+    up = lambda n: (n + 255) // 256 * 256
+    for B, H, tq, mq, d in [(1, 1, 1, 1, 64), (3, 4, 1000, 700, 128), (2, 2, 300, 129, 32)]:
+        pad = (mq + 127) // 128 * 128
+        assert (fa.fa_bwd_varlen_workspace(B, H, tq, mq, d)
+                == up(tq * H * d * 4) + 2 * up(H * B * pad * 4))
+    assert fa.fa_bwd_varlen_workspace(0, 1, 10, 10, 64) == 0
+
+
+@pytest.mark.parametrize("kw", [
+    dict(cu_q=None), dict(cu_k=CUK + 2), dict(B=0), dict(max_q=0), dict(max_q=17), dict(max_k=17),
+    dict(ws=None), dict(ws=WS + 16), dict(ws_bytes=64), dict(dq=Q), dict(dv=DO + 16),
+], ids=lambda kw: ",".join(f"{k}={v}" for k, v in kw.items()))
+def test_bwd_varlen_invalid_arguments(lib, kw):
+    a = dict(cu_q=CUQ, cu_k=CUK, B=2, max_q=8, max_k=8, ws=WS, ws_bytes=None, dq=DQ, dv=DV)
+    a.update(kw)
+    wsb = a["ws_bytes"]
+    if wsb is None:
+        wsb = fa.fa_bwd_varlen_workspace(2, 2, 16, 8, 64)
+    r = fa.fa_bwd_varlen(Q, K, V, O, L, DO, a["dq"], DK, a["dv"], a["cu_q"], a["cu_k"], a["B"], 2,
+                         16, 16, a["max_q"], a["max_k"], 64, 0.125, 1, fa.FA_DTYPE_BF16, a["ws"],
+                         wsb, None)
+    assert r == fa.FA_ERR_INVALID_ARG
