@@ -443,7 +443,12 @@ def main():
     avg_launch_ms = sum(launch_ms) / len(launch_ms)
     achieved = flops_step / (avg_launch_ms / 1e3) / 1e12
     half_io = w.dtype in (0, 3)   # bf16 / fp16: the same kind::f16 tensor rate
-    peak = float(peaks["bf16_tflops"]) if half_io else float(peaks["bf16_tflops"]) / 2.0
+    simt = w.dtype == 2
+    # SIMT: no tensor cores; the FP32 FMA rate is 152 SMs x 128 lanes x 2
+    # FLOP per cycle at the maximum SM clock.
+    fma_peak = 152 * 128 * 2 * float(peaks.get("sm_max_mhz", 2070.0)) * 1e6 / 1e12
+    peak = (float(peaks["bf16_tflops"]) if half_io else
+            fma_peak if simt else float(peaks["bf16_tflops"]) / 2.0)
     kname = {0: "fa_tc_fwd_kernel<bf16>", 1: "fa_tc_fwd_kernel<tf32>",
              2: "fa_simt_fwd_kernel", 3: "fa_tc_fwd_kernel<f16>"}[w.dtype]
     if bwd:
@@ -452,9 +457,11 @@ def main():
         # kernel alone; `traffic` is the gradient kernel's.
         kname = {0: "fa_bwd_kernel<bf16>", 3: "fa_bwd_kernel<f16>"}[w.dtype]
     traffic = profiled_traffic(kname, w.name)
-    roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                "frac": achieved / peak, "traffic": traffic,
-                "peak_source": f"{peak_src} {'bf16 burst' if half_io else 'bf16 burst / 2 (tf32 nominal ratio)'}",
+    roofline = {"bound": "alu" if simt else "tensor", "achieved": achieved, "peak": peak,
+                "unit": "TFLOP/s", "frac": achieved / peak, "traffic": traffic,
+                "peak_source": (f"{peak_src} bf16 burst" if half_io else
+                                "FP32 FMA: 152 SMs x 128 lanes x 2 x max SM clock" if simt else
+                                f"{peak_src} bf16 burst / 2 (tf32 nominal ratio)"),
                 "kernel": kname}
 
     cpu = None
