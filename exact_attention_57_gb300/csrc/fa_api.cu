@@ -131,6 +131,14 @@ int encode_map(CUtensorMap *map, const void *base, int dtype, int BH, int N, int
 
 int ceil_div(int a, int b) { return (a + b - 1) / b; }
 
+// Query tiles per CTA of the plain 16-bit forward: two (heaviest with
+// lightest), so a CTA's second tile overlaps the first one's epilogue and
+// every causal CTA has the same work.  The fp32 path keeps one.
+constexpr int kItemsPerCta = 2;
+int items_per_cta(int dtype) {
+  return (dtype == FA_DTYPE_BF16 || dtype == FA_DTYPE_F16) ? kItemsPerCta : 1;
+}
+
 // The tensor-core forward instantiation for (dtype, d); the combination has
 // been checked by validate().
 //
@@ -224,6 +232,7 @@ int fa_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int
   const unsigned long long lim = g_wait_limit_ns.load();
   p.wait_limit_ns = lim ? lim : fa::kDefaultWaitLimitNs;
   p.skip_v_load = g_skip_v_load.load();
+  p.items_per_cta = items_per_cta(dtype);
 
   cudaError_t e = launch_tc_any(mq, mk, mv, mo, p, B, causal, d, dtype, s);
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
@@ -390,10 +399,6 @@ extern "C" int fa_fwd_noalloc(const void *q, const void *k, const void *v, void 
     p.q_head_stride = static_cast<long long>(Nq) * d;
     p.q_row_stride = d;
     p.lse_head_stride = Nq;
-  p.o = o;
-  p.q_head_stride = static_cast<long long>(Nq) * d;
-  p.q_row_stride = d;
-  p.lse_head_stride = Nq;
     p.lse = lse;
     p.status = status;
     p.H = H;
@@ -405,6 +410,7 @@ extern "C" int fa_fwd_noalloc(const void *q, const void *k, const void *v, void 
     const unsigned long long lim = g_wait_limit_ns.load();
     p.wait_limit_ns = lim ? lim : fa::kDefaultWaitLimitNs;
     p.skip_v_load = g_skip_v_load.load();
+    p.items_per_cta = items_per_cta(dtype);
     cudaError_t e = launch_tc_any(mq, mk, mv, mo, p, B, causal, d, dtype, s);
     if (e != cudaSuccess) return FA_ERR_CUDA;
   }

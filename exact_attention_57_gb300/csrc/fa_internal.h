@@ -55,6 +55,10 @@ struct TcParams {
   // fp32 path: K already rounded to tf32 and tm_v a map over a tf32 V^T
   // ([B*H][d][Nk padded to 128], boxes of 32 keys x D rows).
   int kv_staged = 0;
+  // Query tiles per CTA (plain problems, 16-bit types): 1, or an even number
+  // taken from the zigzag heaviest/lightest order (the grid then has
+  // ceil(n_qtiles / items_per_cta) CTAs per head).
+  int items_per_cta = 1;
 };
 
 struct SimtParams {

@@ -106,7 +106,8 @@ struct TcCfg {
   static constexpr int OFF_BAR = OFF_VT + NVT * TILE_BYTES;
   // q, kfull[KST], kempty[KST], vfull[VST], vempty[VST], sfull[NS], pfull[NS],
   // odone[NS], fin[2], kready[KST]
-  static constexpr int NBAR = 1 + 2 * KST + 2 * VST + 3 * NS + 2 + KST;
+  // ... then qempty, ofree (several query tiles per CTA)
+  static constexpr int NBAR = 1 + 2 * KST + 2 * VST + 3 * NS + 2 + KST + 2;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;       // tmem base, abort flag
   static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;   // + alignment slack
   static constexpr int THREADS = 224;
@@ -151,6 +152,8 @@ __global__ void __launch_bounds__(224, 1)
   const uint32_t bFin = bOdone + 8 * C::NS;            // S issuer's teardown
   const uint32_t bFin2 = bFin + 8;                     // P V issuer's teardown
   const uint32_t bKready = bFin2 + 8;                  // + 8*stage (fp32 path)
+  const uint32_t bQempty = bKready + 8 * C::KST;       // Q of an item read by its last S
+  const uint32_t bOfree = bQempty + 8;                 // O of an item read by the epilogue
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::OFF_MISC);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::OFF_MISC + 4);
 
@@ -177,7 +180,22 @@ __global__ void __launch_bounds__(224, 1)
     n_ktiles = (Nk + BN - 1) / BN;
     if (qidx >= n_qtiles) return;  // the grid covers the longest sequence
   }
-  const int qt = CAUSAL ? (n_qtiles - 1 - qidx) : qidx;
+  // Several query tiles per CTA (plain problems only): CTA x takes tiles
+  // G*x .. G*x+G-1 of the zigzag order heaviest, lightest, 2nd heaviest, ...,
+  // so with an even G every CTA has the same causal work, and an item's loads
+  // and first products overlap the previous item's epilogue.
+  const int G = p.items_per_cta > 1 ? p.items_per_cta : 1;
+  auto item_qt = [&](int g) -> int {  // query tile of item g, or -1
+    if (G == 1) return g == 0 ? (CAUSAL ? (n_qtiles - 1 - qidx) : qidx) : -1;
+    const int zi = G * static_cast<int>(blockIdx.x) + g;
+    if (zi >= n_qtiles) return -1;
+    const int qi = (zi & 1) ? n_qtiles - 1 - (zi >> 1) : (zi >> 1);
+    return CAUSAL ? (n_qtiles - 1 - qi) : qi;
+  };
+  // Key tiles of query tile t: [kt0, kt0 + n_kt) (top-left causal: keys <=
+  // its last row; in split mode chunk `split` of them).
+  auto item_nall = [&](int t) { return CAUSAL ? min(t + 1, n_ktiles) : n_ktiles; };
+  const int qt = item_qt(0);
   const int q0 = qt * BM;
   // Head dim of the tensors in memory: D, or less when the kernel runs a
   // narrower head dim zero-padded to D (the TMA maps zero-fill the missing
@@ -233,6 +251,8 @@ __global__ void __launch_bounds__(224, 1)
     }
     mbar_init(bFin, 1);
     mbar_init(bFin2, 1);
+    mbar_init(bQempty, 1);
+    mbar_init(bOfree, 128);
     *abort_flag = 0;
     fence_barrier_init();
     fence_proxy_async_smem();
@@ -258,59 +278,70 @@ __global__ void __launch_bounds__(224, 1)
     w.role = kStatusProducer;
     if (lane == 0) {
       const uint64_t pol_kv = l2_policy_evict_last();
-      if constexpr (!C::QTMEM) {
-        mbar_arrive_expect_tx(bQ, C::TILE_BYTES);
-#pragma unroll
-        for (int c = 0; c < C::NCH; ++c)
-          tma_load_3d(sQ + c * C::CHUNK_BYTES, &tm_q, bQ, c * C::CH_ELEMS, q_row0 + q0, hc,
-                      l2_policy_evict_first());
-      }
-      int nk = 0, nv = 0;  // loads issued
+      int nk = 0, nv = 0, nq = 0;  // loads issued (K and V ring positions, Q tiles)
       bool ok = true;
-      // Load order = consumption order: S runs NS - 1 tiles ahead of P V, so
-      // K_{j+NS-1} is loaded just before V_j (K0, K1, K2, V0, K3, V1, ... for
-      // NS = 3).
-      constexpr int kAhead = C::NS - 1;
-      for (int j = -kAhead; ok && j < n_kt; ++j) {
-        const int jk = j + kAhead;  // next K tile
-        if (jk < n_kt) {
-          const int s = jk % C::KST, r = jk / C::KST;
-          if (r > 0) ok = bounded_wait(bKempty + 8 * s, (r - 1) & 1, w);
-          if (!ok) break;
-          mbar_arrive_expect_tx(bKfull + 8 * s, C::TILE_BYTES);
+      for (int g = 0; ok && g < G; ++g) {
+        const int tq = item_qt(g);
+        if (tq < 0) break;
+        const int n_all_g = item_nall(tq);
+        const int kt0_g = G == 1 ? kt0 : 0;
+        const int n_kt_g = G == 1 ? n_kt : n_all_g;
+        if constexpr (!C::QTMEM) {
+          // The Q buffer is free once the previous item's last S has read it.
+          if (g > 0 && !(ok = bounded_wait(bQempty, (g - 1) & 1, w))) break;
+          mbar_arrive_expect_tx(bQ, C::TILE_BYTES);
 #pragma unroll
           for (int c = 0; c < C::NCH; ++c)
-            tma_load_3d(sK + s * C::TILE_BYTES + c * C::CHUNK_BYTES, &tm_k, bKfull + 8 * s,
-                        c * C::CH_ELEMS, k_row0 + (kt0 + jk) * BN, hc, pol_kv);
-          ++nk;
+            tma_load_3d(sQ + c * C::CHUNK_BYTES, &tm_q, bQ, c * C::CH_ELEMS, q_row0 + tq * BM, hc,
+                        l2_policy_evict_first());
+          ++nq;
         }
-        if (j >= 0) {
-          if (p.skip_v_load && j == 0) {  // test hook: starve the MMA issuer
-            atomicOr(p.status, kStatusInjected);
-            break;
-          }
-          const int s = j % C::VST, r = j / C::VST;
-          if (r > 0) ok = bounded_wait(bVempty + 8 * s, (r - 1) & 1, w);
-          if (!ok) break;
-          mbar_arrive_expect_tx(bVfull + 8 * s, C::TILE_BYTES);
-          if (staged) {
-            // V^T prepared by the staging kernel: D rows x 32 keys per chunk,
-            // straight into the K-major V^T buffer the P V product reads.
-#pragma unroll
-            for (int c = 0; c < BN / 32; ++c)
-              tma_load_3d(sVT + s * C::TILE_BYTES + c * C::VT_CHUNK_BYTES, &tm_v, bVfull + 8 * s,
-                          (kt0 + j) * BN + 32 * c, 0, hc, pol_kv);
-          } else {
+        // Load order = consumption order: S runs NS - 1 tiles ahead of P V, so
+        // K_{j+NS-1} is loaded just before V_j (K0, K1, K2, V0, K3, V1, ... for
+        // NS = 3).
+        constexpr int kAhead = C::NS - 1;
+        for (int j = -kAhead; ok && j < n_kt_g; ++j) {
+          const int jk = j + kAhead;  // next K tile
+          if (jk < n_kt_g) {
+            const int s = nk % C::KST, r = nk / C::KST;
+            if (r > 0) ok = bounded_wait(bKempty + 8 * s, (r - 1) & 1, w);
+            if (!ok) break;
+            mbar_arrive_expect_tx(bKfull + 8 * s, C::TILE_BYTES);
 #pragma unroll
             for (int c = 0; c < C::NCH; ++c)
-              tma_load_3d(sV + s * C::TILE_BYTES + c * C::CHUNK_BYTES, &tm_v, bVfull + 8 * s,
-                          c * C::CH_ELEMS, k_row0 + (kt0 + j) * BN, hc, pol_kv);
+              tma_load_3d(sK + s * C::TILE_BYTES + c * C::CHUNK_BYTES, &tm_k, bKfull + 8 * s,
+                          c * C::CH_ELEMS, k_row0 + (kt0_g + jk) * BN, hc, pol_kv);
+            ++nk;
           }
-          ++nv;
+          if (j >= 0) {
+            if (p.skip_v_load && g == 0 && j == 0) {  // test hook: starve the MMA issuer
+              atomicOr(p.status, kStatusInjected);
+              ok = false;
+              break;
+            }
+            const int s = nv % C::VST, r = nv / C::VST;
+            if (r > 0) ok = bounded_wait(bVempty + 8 * s, (r - 1) & 1, w);
+            if (!ok) break;
+            mbar_arrive_expect_tx(bVfull + 8 * s, C::TILE_BYTES);
+            if (staged) {
+              // V^T prepared by the staging kernel: D rows x 32 keys per chunk,
+              // straight into the K-major V^T buffer the P V product reads.
+#pragma unroll
+              for (int c = 0; c < BN / 32; ++c)
+                tma_load_3d(sVT + s * C::TILE_BYTES + c * C::VT_CHUNK_BYTES, &tm_v,
+                            bVfull + 8 * s, (kt0_g + j) * BN + 32 * c, 0, hc, pol_kv);
+            } else {
+#pragma unroll
+              for (int c = 0; c < C::NCH; ++c)
+                tma_load_3d(sV + s * C::TILE_BYTES + c * C::CHUNK_BYTES, &tm_v, bVfull + 8 * s,
+                            c * C::CH_ELEMS, k_row0 + (kt0_g + j) * BN, hc, pol_kv);
+            }
+            ++nv;
+          }
         }
       }
       // Drain: no TMA write may still be in flight when the CTA exits.
-      if constexpr (!C::QTMEM) bounded_wait(bQ, 0, w, false);
+      if (nq > 0) bounded_wait(bQ, (nq - 1) & 1, w, false);
       for (int s = 0; s < C::KST; ++s) {
         const int cnt = (nk > s) ? (nk - 1 - s) / C::KST + 1 : 0;
         if (cnt > 0) bounded_wait(bKfull + 8 * s, (cnt - 1) & 1, w, false);
@@ -333,12 +364,19 @@ __global__ void __launch_bounds__(224, 1)
       // A negative scale is applied as S = (-Q) K^T (the descriptor's negate-A
       // bit) with |scale|, so the softmax only ever sees a positive scale.
       const uint32_t idesc_qk = kIdescQK | (p.scale_neg ? (1u << 13) : 0u);
-      bool ok = bounded_wait(bQ, 0, w);
-      if (ok) tc_fence_after();
-      int b = 0, bph = 0;   // score buffer of tile j and the parity of its use
-      int s = 0, sph = 0;   // K stage of tile j and its parity
-      for (int j = 0; ok && j < n_kt; ++j) {
-        if (j >= C::NS && !(ok = bounded_wait(bOdone + 8 * b, bph ^ 1, w))) break;
+      bool ok = true;
+      int b = 0, bph = 0;   // score buffer of the next S and the parity of its use
+      int s = 0, sph = 0;   // K stage of the next S and its parity
+      int ns = 0;           // S products issued (all items)
+      for (int g = 0; ok && g < G; ++g) {
+      const int tq = item_qt(g);
+      if (tq < 0) break;
+      const int n_kt_g = G == 1 ? n_kt : item_nall(tq);
+      // Q of item g in place (TMEM or shared memory).
+      if (!(ok = bounded_wait(bQ, g & 1, w))) break;
+      tc_fence_after();
+      for (int j = 0; ok && j < n_kt_g; ++j, ++ns) {
+        if (ns >= C::NS && !(ok = bounded_wait(bOdone + 8 * b, bph ^ 1, w))) break;
         // fp32 path: K_j must first be rounded to tf32 by the softmax warps
         if (!(ok = bounded_wait(((TF32 && !staged) ? bKready : bKfull) + 8 * s, sph, w))) break;
         tc_fence_after();
@@ -361,6 +399,9 @@ __global__ void __launch_bounds__(224, 1)
         if (++b == C::NS) { b = 0; bph ^= 1; }
         if (++s == C::KST) { s = 0; sph ^= 1; }
       }
+      // Q of item g is free once its S products complete.
+      if (ok) tc_commit(bQempty);
+      }
       // Every UMMA issued above must be complete before TMEM is freed.
       tc_commit(bFin);
       bounded_wait(bFin, 0, w, false);
@@ -376,9 +417,18 @@ __global__ void __launch_bounds__(224, 1)
       // bf16: V is an MN-major B operand.  fp32: V^T is a K-major B operand.
       constexpr uint32_t kIdescPV = make_idesc(kFmt, BM, D, 0u, TF32 ? 0u : 1u);
       bool ok = true;
-      int b = 0, bph = 0;   // score buffer of tile j and the parity of its use
-      int s = 0, sph = 0;   // V stage of tile j and its parity
-      for (int j = 0; ok && j < n_kt; ++j) {
+      int b = 0, bph = 0;   // score buffer of the next P V and the parity of its use
+      int s = 0, sph = 0;   // V stage of the next P V and its parity
+      for (int g = 0; ok && g < G; ++g) {
+      const int tq = item_qt(g);
+      if (tq < 0) break;
+      const int n_kt_g = G == 1 ? n_kt : item_nall(tq);
+      // O of the previous item has been read out by the epilogue.
+      if (g > 0) {
+        if (!(ok = bounded_wait(bOfree, (g - 1) & 1, w))) break;
+        tc_fence_after();
+      }
+      for (int j = 0; ok && j < n_kt_g; ++j) {
         // P_j ready (fp32 path: also V_j^T written), V_j (or V_j^T) loaded.
         if (!(ok = bounded_wait(bPfull + 8 * b, bph, w))) break;
         if (!TF32 || staged) {
@@ -406,6 +456,7 @@ __global__ void __launch_bounds__(224, 1)
         if (++b == C::NS) { b = 0; bph ^= 1; }
         if (++s == C::VST) { s = 0; sph ^= 1; }
       }
+      }
       tc_commit(bFin2);
       bounded_wait(bFin2, 0, w, false);
     }
@@ -414,11 +465,11 @@ __global__ void __launch_bounds__(224, 1)
     // ------------------------------------------------ softmax + epilogue
     w.role = kStatusSoftmax;
     const int r = threadIdx.x;  // TMEM lane == row within the tile
-    const int row = q0 + r;
+    int row = q0 + r;
     const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
     const uint32_t o_tm = tmem + lane_off + C::COL_O;
     const float sl2 = p.scale_log2;
-    const int row_lim = CAUSAL ? min(row + 1, Nk) : Nk;  // keys [0, row_lim)
+    int row_lim = CAUSAL ? min(row + 1, Nk) : Nk;  // keys [0, row_lim)
     float m_used = -INFINITY;  // exponent offset, log2 units of the scaled score
     float l = 0.f;
     bool ok = true;
@@ -482,11 +533,12 @@ __global__ void __launch_bounds__(224, 1)
     // Q row -> tensor memory (A operand layout: lane = row, 32-bit column c
     // holds bf16 elements 2c, 2c+1, or one tf32 element).  Rows past Nq are 0.
     // (Otherwise the producer loads Q into shared memory with TMA.)
-    if constexpr (C::QTMEM) {
-      const bool in = row < Nq;
+    auto stage_q = [&](int tq) {
+      const int qrow = tq * BM + r;
+      const bool in = qrow < Nq;
       const uint4 *src = reinterpret_cast<const uint4 *>(
           static_cast<const uint8_t *>(p.q) +
-          (hc * p.q_head_stride + (q_row0 + (in ? row : 0)) * p.q_row_stride) * C::ESZ);
+          (hc * p.q_head_stride + (q_row0 + (in ? qrow : 0)) * p.q_row_stride) * C::ESZ);
 #pragma unroll
       for (int blk = 0; blk < C::Q_COLS / 32; ++blk) {
         uint32_t wq[32];
@@ -508,16 +560,25 @@ __global__ void __launch_bounds__(224, 1)
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(bQ);
-    }
+    };
+    if constexpr (C::QTMEM) stage_q(qt);
     if (TF32 && !staged) ok = round_k_row(0);
 
     int buf = 0, bph = 0;            // score buffer of tile j and the parity of its use
     int pbuf = C::NS - 1, pbph = 1;  // the same for tile j - 1
-    for (int j = 0; ok && j < n_kt; ++j) {
+    for (int g = 0; g < G; ++g) {
+    const int tq = item_qt(g);
+    if (tq < 0) break;
+    const int n_kt_g = G == 1 ? n_kt : item_nall(tq);
+    row = tq * BM + r;
+    row_lim = CAUSAL ? min(row + 1, Nk) : Nk;
+    m_used = -INFINITY;
+    l = 0.f;
+    for (int j = 0; ok && j < n_kt_g; ++j) {
       if (TF32 && !staged) {
         // the next K tile is rounded before this tile's softmax so that
         // S_{j+1} = Q K_{j+1}^T still overlaps it
-        if (j + 1 < n_kt && !(ok = round_k_row(j + 1))) break;
+        if (j + 1 < n_kt_g && !(ok = round_k_row(j + 1))) break;
       }
       ok = __all_sync(kFull, bounded_wait(bSfull + 8 * buf, bph, w));
       if (!ok) break;
@@ -653,6 +714,16 @@ __global__ void __launch_bounds__(224, 1)
       if (++buf == C::NS) { buf = 0; bph ^= 1; }
     }
 
+    // Q-in-TMEM: the next item's Q rows go in once this item's S products
+    // have read the current ones, so its first S overlaps this epilogue.
+    if constexpr (C::QTMEM) {
+      const int tn = (g + 1 < G) ? item_qt(g + 1) : -1;
+      if (ok && tn >= 0) {
+        ok = __all_sync(kFull, bounded_wait(bQempty, g & 1, w));
+        if (ok) stage_q(tn);
+      }
+    }
+
     // ------------------------------------------------ epilogue
     // The last P V; its commit also covers every earlier UMMA.
     if (ok)
@@ -682,9 +753,10 @@ __global__ void __launch_bounds__(224, 1)
         }
         if (row < Nq) p.ws_lse[prow] = m_used * kLn2 + logf(l);
       }
-    } else if (p.cu_q != nullptr) {
+    } else if (p.cu_q != nullptr || G > 1) {
       // Variable-length batches: the rows after this sequence belong to the
-      // next one, so O is written row by row from registers (no TMA store).
+      // next one, so O is written row by row from registers (no TMA store);
+      // likewise with several items per CTA, whose K stages stay in use.
       if (ok) {
         tc_fence_after();
         const float inv_l = 1.f / l;
@@ -723,6 +795,9 @@ __global__ void __launch_bounds__(224, 1)
           }
         }
         if (row < Nq) p.lse[hc * p.lse_head_stride + gr] = m_used * kLn2 + logf(l);
+        // O of this item has been read: the next item's P V may start.
+        tc_fence_before();
+        mbar_arrive(bOfree);
       }
     } else if (ok) {
       tc_fence_after();
@@ -776,7 +851,7 @@ __global__ void __launch_bounds__(224, 1)
     }
     fence_proxy_async_smem();
     named_bar_sync(1, 128);
-    if (nsp == 1 && p.cu_q == nullptr && threadIdx.x == 0 && *abort_flag == 0) {
+    if (G == 1 && nsp == 1 && p.cu_q == nullptr && threadIdx.x == 0 && *abort_flag == 0) {
 #pragma unroll
       for (int c = 0; c < C::NCH; ++c)
         if (c * C::CH_ELEMS < dio)  // a chunk wholly past the row is not stored
@@ -784,6 +859,10 @@ __global__ void __launch_bounds__(224, 1)
       tma_store_commit();
       tma_store_wait_read_all();
     }
+    // The four warps have all passed the named barrier above, so they read
+    // the same abort flag and leave the item loop together.
+    if (*abort_flag) break;
+    }  // items
   }
 
   // ------------------------------------------------------------ teardown
@@ -807,7 +886,9 @@ cudaError_t launch_tc(const CUtensorMap &q, const CUtensorMap &k, const CUtensor
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(p.n_qtiles * p.n_splits), static_cast<unsigned>(p.H),
+  const int gx = p.items_per_cta > 1 ? (p.n_qtiles + p.items_per_cta - 1) / p.items_per_cta
+                                    : p.n_qtiles * p.n_splits;
+  cfg.gridDim = dim3(static_cast<unsigned>(gx), static_cast<unsigned>(p.H),
                      static_cast<unsigned>(B));
   cfg.blockDim = dim3(C::THREADS, 1, 1);
   cfg.dynamicSmemBytes = C::SMEM_BYTES;
