@@ -618,11 +618,16 @@ namespace {
 
 size_t round256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
-// Workspace parts: dq_acc [B*H][Nq][d] fp32, then lse2 and dd [B*H][Nq_pad].
+// Row length of the fp32 dQ accumulator: the gradient kernel's head dim
+// (d = 32 runs on the d = 64 kernel).
+size_t bwd_acc_dim(int d) { return d < 64 ? 64 : static_cast<size_t>(d); }
+
+// Workspace parts: dq_acc [B*H][Nq][max(d, 64)] fp32, then lse2 and dd
+// [B*H][Nq_pad].
 void bwd_ws_parts(int B, int H, int Nq, int d, size_t *acc, size_t *row) {
   const size_t bh = static_cast<size_t>(B) * H;
   const size_t nq_pad = static_cast<size_t>(ceil_div(Nq, fa::BM)) * fa::BM;
-  *acc = round256(bh * Nq * d * sizeof(float));
+  *acc = round256(bh * Nq * bwd_acc_dim(d) * sizeof(float));
   *row = round256(bh * nq_pad * sizeof(float));
 }
 
@@ -714,7 +719,7 @@ extern "C" int fa_bwd(const void *q, const void *k, const void *v, const void *o
     e = (d <= 64) ? fa::launch_bwd_bf16_d64(mq, mk, mv, mdo, p, B, causal, s)
                   : fa::launch_bwd_bf16_d128(mq, mk, mv, mdo, p, B, causal, s);
   if (e != cudaSuccess) return FA_ERR_CUDA;
-  e = fa::launch_bwd_convert(p.dq_acc, dq, static_cast<long long>(BH) * Nq * d, half, s);
+  e = fa::launch_bwd_convert(p.dq_acc, dq, static_cast<long long>(BH) * Nq, d, H, 0, half, s);
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
@@ -823,9 +828,11 @@ extern "C" int fa_fwd_staged(const void *q, const void *k, const void *v, void *
 // ---------------------------------------------------------------------------
 namespace {
 
+// Workspace parts: dq_acc [H][total_q][max(d, 64)] fp32, then lse2 and dd
+// [H][B][Nq_pad].
 void bwd_varlen_parts(int B, int H, int total_q, int max_q, int d, size_t *acc, size_t *row) {
   const size_t pad = static_cast<size_t>(ceil_div(max_q, fa::BM)) * fa::BM;
-  *acc = round256(static_cast<size_t>(total_q) * H * d * sizeof(float));
+  *acc = round256(static_cast<size_t>(total_q) * H * bwd_acc_dim(d) * sizeof(float));
   *row = round256(static_cast<size_t>(H) * B * pad * sizeof(float));
 }
 
@@ -926,6 +933,7 @@ extern "C" int fa_bwd_varlen(const void *q, const void *k, const void *v, const 
     e = (d <= 64) ? fa::launch_bwd_bf16_d64(mq, mk, mv, mdo, p, B, causal, s)
                   : fa::launch_bwd_bf16_d128(mq, mk, mv, mdo, p, B, causal, s);
   if (e != cudaSuccess) return FA_ERR_CUDA;
-  e = fa::launch_bwd_convert(p.dq_acc, dq, static_cast<long long>(total_q) * H * d, half, s);
+  e = fa::launch_bwd_convert(p.dq_acc, dq, static_cast<long long>(total_q) * H, d, H, total_q, half,
+                             s);
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }

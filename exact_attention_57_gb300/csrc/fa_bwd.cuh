@@ -134,15 +134,17 @@ __global__ void __launch_bounds__(320, 1)
   // runs zero-padded to D (the TMA loads zero-fill the missing columns; the
   // plain dQ, dK, dV writes below stop at dio).
   const int dio = p.d_io > 0 ? p.d_io : D;
-  // This CTA's problem: rows [q_row0, q_row0 + Nq) of Q/dO/dQ and
-  // [k_row0, k_row0 + Nk) of K/V/dK/dV in TMA plane hc.  Element offsets of
-  // row 0 and the row stride: [B,H,N,d] (plane b*H+h, rows dio apart) or,
-  // for variable-length batches, token-major [total, H, d] (plane h, rows
-  // H*dio apart).
+  // This CTA's problem: rows [q_row0, q_row0 + Nq) of Q/dO and
+  // [k_row0, k_row0 + Nk) of K/V/dK/dV in TMA plane hc.  dK/dV element
+  // offset of row 0 and the row stride: [B,H,N,d] (plane b*H+h, rows dio
+  // apart) or, for variable-length batches, token-major [total, H, d] (plane
+  // h, rows H*dio apart).  The fp32 dQ accumulator is plane-major in both
+  // cases, [B*H][Nq][D] or [H][total_q][D], so its row stride is the
+  // compile-time D (the drain's 32 adds then share one address register).
   const bool varlen = p.cu_q != nullptr;
   int Nq = p.Nq, Nk = p.Nk, q_row0 = 0, k_row0 = 0, hc = bh, n_qtiles = p.n_qtiles;
   size_t row_base = static_cast<size_t>(bh) * p.Nq_pad;  // LSE/D rows of this problem
-  long long dq_base = static_cast<long long>(bh) * p.Nq * dio, dq_rs = dio;
+  size_t acc_base = static_cast<size_t>(bh) * p.Nq * D;   // dQ accumulator row 0
   long long kv_base = static_cast<long long>(bh) * p.Nk * dio, kv_rs = dio;
   if (varlen) {
     const int b = static_cast<int>(blockIdx.z), h = static_cast<int>(blockIdx.y);
@@ -155,10 +157,9 @@ __global__ void __launch_bounds__(320, 1)
     hc = h;
     n_qtiles = (Nq + BM - 1) / BM;
     row_base = (static_cast<size_t>(h) * gridDim.z + b) * p.Nq_pad;
-    dq_base = (static_cast<long long>(q_row0) * p.H + h) * dio;
-    dq_rs = static_cast<long long>(p.H) * dio;
+    acc_base = (static_cast<size_t>(h) * p.total_q + q_row0) * D;
     kv_base = (static_cast<long long>(k_row0) * p.H + h) * dio;
-    kv_rs = dq_rs;
+    kv_rs = static_cast<long long>(p.H) * dio;
     if (k0 >= Nk) return;  // the grid covers the longest sequence
   }
   // Query tiles that see this key tile (top-left causal: query >= key).
@@ -339,11 +340,11 @@ __global__ void __launch_bounds__(320, 1)
       const float *lse2 = reinterpret_cast<const float *>(smem + C::OFF_ROW + s * C::ROW_BYTES);
       const float *dd = lse2 + 128;
       const bool diag = CAUSAL && qt == jt;   // key r sees query c only if r <= c
-      // Variable-length batches: rows past this sequence's keys or queries
-      // belong to the next sequence (not zero-filled), so their P is set to 0.
-      const int qlim = Nq - qt * BM;          // valid query columns [0, qlim)
+      // Query columns past Nq have LSE = +inf (prep kernel), so P = 0 there.
+      // Key rows past Nk: their dK, dV rows are not stored, and their dS is
+      // zeroed below, so they add nothing to dQ (for variable-length batches
+      // those rows hold the next sequence's keys, not zeros).
       const bool krow_ok = k0 + r < Nk;
-      const bool tail = varlen && (!krow_ok || qlim < BM);
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         const uint32_t col = C::COL_S0 + h * C::COL_HALF;
@@ -372,9 +373,9 @@ __global__ void __launch_bounds__(320, 1)
             float x0, x1;
             upk2(x2, x0, x1);
             float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
-            if (diag || tail) {
-              if ((diag && c0 + c < r) || (tail && (!krow_ok || c0 + c >= qlim))) p0 = 0.f;
-              if ((diag && c0 + c + 1 < r) || (tail && (!krow_ok || c0 + c + 1 >= qlim))) p1 = 0.f;
+            if (diag) {
+              if (c0 + c < r) p0 = 0.f;
+              if (c0 + c + 1 < r) p1 = 0.f;
             }
             const uint64_t g2 = fadd2(pk2(__uint_as_float(dr[c]), __uint_as_float(dr[c + 1])),
                                       pk2(-da, -db));
@@ -383,6 +384,10 @@ __global__ void __launch_bounds__(320, 1)
             pp[c >> 1] = HALF ? pack_f16x2(p0, p1) : pack_bf16x2(p0, p1);
             dsp[c >> 1] = HALF ? pack_f16x2(s0, s1) : pack_bf16x2(s0, s1);
           }
+        }
+        if (!krow_ok) {
+#pragma unroll
+          for (int u = 0; u < 16; ++u) dsp[u] = 0u;
         }
         // P^T columns 16 + 16g ..: inside the 32 columns this quarter read.
         tmem_st16(tmem + lane_off + col + C::P_OFF + 16 * g, pp);
@@ -415,10 +420,10 @@ __global__ void __launch_bounds__(320, 1)
           tmem_ld_wait();
           reg_fence32(v);
           const int qbase = qt * BM + h * C::HQ + cq;
-          float *dst = p.dq_acc + dq_base + qbase * dq_rs + r;
+          float *dst = p.dq_acc + acc_base + static_cast<size_t>(qbase) * D + r;
 #pragma unroll
           for (int i = 0; i < 32; ++i)
-            if (qbase + i < Nq) red_add(dst + i * dq_rs, __uint_as_float(v[i]));
+            if (qbase + i < Nq) red_add(dst + i * D, __uint_as_float(v[i]));
         }
         tc_fence_before();
         mbar_arrive(bDQfree + 8 * h);

@@ -6,6 +6,10 @@
 // from Nq up to the padded tile end get LSE = +inf and D = 0, which makes
 // their probabilities exactly 0 in the main kernel.
 // After it: dQ rounded from the fp32 accumulator to the input type.
+//
+// The accumulator is plane-major with rows of DA = max(d, 64) floats (the
+// gradient kernel's head dim): [B*H][Nq][DA], or [H][total_q][DA] for
+// variable-length batches; only the first d floats of a row are used.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -18,6 +22,9 @@ namespace fa {
 namespace {
 
 constexpr int kPrepRowsPerBlock = 8;  // one warp per row
+
+template <int D>
+constexpr int acc_dim() { return D < 64 ? 64 : D; }
 
 __device__ __forceinline__ float2 load2(const void *base, size_t idx, bool half) {
   const uint32_t w = *reinterpret_cast<const uint32_t *>(static_cast<const uint16_t *>(base) + idx);
@@ -62,7 +69,7 @@ __global__ void __launch_bounds__(32 * kPrepRowsPerBlock)
   }
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-  float *zrow = dq_acc + row * D;
+  float *zrow = dq_acc + row * acc_dim<D>();
   // D / 4 float4 per row, 32 per pass
 #pragma unroll
   for (int i = 0; i < (D / 4 + 31) / 32; ++i)
@@ -75,8 +82,8 @@ __global__ void __launch_bounds__(32 * kPrepRowsPerBlock)
 }
 
 // Variable-length batches: padded row prow = (h*B + b)*Nq_pad + pos of the
-// LSE/D buffers; token t = cu_q[b] + pos of q/o/dout and dq_acc (token-major
-// [total_q, H, D]); lse [H, total_q].
+// LSE/D buffers; token t = cu_q[b] + pos of q/o/dout (token-major
+// [total_q, H, D]) and of accumulator plane h; lse [H, total_q].
 template <int D>
 __global__ void __launch_bounds__(32 * kPrepRowsPerBlock)
     fa_bwd_prep_varlen_kernel(const void *__restrict__ o, const void *__restrict__ dout,
@@ -113,7 +120,7 @@ __global__ void __launch_bounds__(32 * kPrepRowsPerBlock)
   }
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-  float *zrow = dq_acc + row * D;
+  float *zrow = dq_acc + (static_cast<size_t>(h) * total_q + t0 + pos) * acc_dim<D>();
 #pragma unroll
   for (int i = 0; i < (D / 4 + 31) / 32; ++i)
     if (32 * i + lane < D / 4)
@@ -124,12 +131,24 @@ __global__ void __launch_bounds__(32 * kPrepRowsPerBlock)
   }
 }
 
+// Output row o of dq (d elements; 8 per thread): [B,H,Nq,d] order, which is
+// also the accumulator's row order, or for variable-length batches
+// token-major, o = t*H + h, read from accumulator row h*total_q + t.
+template <bool VARLEN>
 __global__ void fa_bwd_convert_kernel(const float *__restrict__ src, void *__restrict__ dst,
-                                      long long n8, int half) {
+                                      long long rows, int chunk_shift, int acc_d, int H,
+                                      int total_q, int half) {
   const long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (i >= n8) return;
-  const float4 a = reinterpret_cast<const float4 *>(src)[2 * i];
-  const float4 b = reinterpret_cast<const float4 *>(src)[2 * i + 1];
+  if (i >= (rows << chunk_shift)) return;
+  const long long o = i >> chunk_shift;
+  const int c = static_cast<int>(i - (o << chunk_shift)) * 8;
+  long long srow = o;
+  if (VARLEN) {
+    const long long t = o / H;
+    srow = static_cast<long long>(o - t * H) * total_q + t;
+  }
+  const float4 *in = reinterpret_cast<const float4 *>(src + srow * acc_d + c);
+  const float4 a = in[0], b = in[1];
   uint4 out;
   if (half) {
     const __half2 h0 = __floats2half2_rn(a.x, a.y), h1 = __floats2half2_rn(a.z, a.w);
@@ -142,7 +161,8 @@ __global__ void fa_bwd_convert_kernel(const float *__restrict__ src, void *__res
     out = make_uint4(*reinterpret_cast<const uint32_t *>(&h0), *reinterpret_cast<const uint32_t *>(&h1),
                      *reinterpret_cast<const uint32_t *>(&h2), *reinterpret_cast<const uint32_t *>(&h3));
   }
-  reinterpret_cast<uint4 *>(dst)[i] = out;
+  // d is a multiple of 8, so o*d + c is a multiple of 8 elements (16 bytes).
+  reinterpret_cast<uint4 *>(static_cast<uint16_t *>(dst) + (o << (chunk_shift + 3)) + c)[0] = out;
 }
 
 }  // namespace
@@ -182,11 +202,19 @@ cudaError_t launch_bwd_prep_varlen(const void *o, const void *dout, const float 
   return cudaGetLastError();
 }
 
-cudaError_t launch_bwd_convert(const float *dq_acc, void *dq, long long n, int half,
-                               cudaStream_t s) {
-  const long long n8 = n / 8;  // n is a multiple of 32 (d is 32, 64 or 128)
-  const unsigned blocks = static_cast<unsigned>((n8 + 255) / 256);
-  fa_bwd_convert_kernel<<<blocks, 256, 0, s>>>(dq_acc, dq, n8, half);
+cudaError_t launch_bwd_convert(const float *dq_acc, void *dq, long long rows, int d, int H,
+                               int total_q, int half, cudaStream_t s) {
+  // d is 32, 64 or 128: d / 8 = 1 << chunk_shift chunks per row.
+  const int chunk_shift = d == 32 ? 2 : d == 64 ? 3 : 4;
+  const int acc_d = d < 64 ? 64 : d;
+  const long long n = rows << chunk_shift;
+  const unsigned blocks = static_cast<unsigned>((n + 255) / 256);
+  if (total_q > 0)
+    fa_bwd_convert_kernel<true><<<blocks, 256, 0, s>>>(dq_acc, dq, rows, chunk_shift, acc_d, H,
+                                                       total_q, half);
+  else
+    fa_bwd_convert_kernel<false><<<blocks, 256, 0, s>>>(dq_acc, dq, rows, chunk_shift, acc_d, H,
+                                                        0, half);
   return cudaGetLastError();
 }
 

@@ -155,8 +155,9 @@ cudaError_t launch_bwd_prep(const void *o, const void *dout, const float *lse, f
 cudaError_t launch_bwd_prep_varlen(const void *o, const void *dout, const float *lse, float *lse2,
                                    float *dd, float *dq_acc, const int *cu_q, int B, int H,
                                    int total_q, int Nq_pad, int d, int half, cudaStream_t s);
-// dq = dq_acc rounded to the input type.
-cudaError_t launch_bwd_convert(const float *dq_acc, void *dq, long long n, int half,
-                               cudaStream_t s);
+// dq (rows of d elements) = dq_acc rounded to the input type; total_q > 0
+// selects the variable-length layouts (token-major dq, [H][total_q] rows).
+cudaError_t launch_bwd_convert(const float *dq_acc, void *dq, long long rows, int d, int H,
+                               int total_q, int half, cudaStream_t s);
 
 }  // namespace fa

@@ -256,8 +256,10 @@ int fa_bwd(const void *q, const void *k, const void *v, const void *o, const flo
            int B, int H, int Nq, int Nk, int d, float scale, int causal, int dtype,
            void *workspace, unsigned long long workspace_bytes, void *stream);
 
-/* Bytes of workspace fa_bwd needs: B*H*Nq*d floats plus 2*B*H*ceil(Nq/128)*128
- * floats, each part rounded up to 256 bytes.  0 for invalid arguments. */
+/* Bytes of workspace fa_bwd needs: B*H*Nq*max(d, 64) floats (the dq
+ * accumulator, rows of the gradient kernel's head dim) plus
+ * 2*B*H*ceil(Nq/128)*128 floats, each part rounded up to 256 bytes.  0 for
+ * invalid arguments. */
 unsigned long long fa_bwd_workspace(int B, int H, int Nq, int d);
 
 /*
@@ -281,7 +283,7 @@ int fa_bwd_varlen(const void *q, const void *k, const void *v, const void *o, co
                   float scale, int causal, int dtype, void *workspace,
                   unsigned long long workspace_bytes, void *stream);
 
-/* Bytes of workspace fa_bwd_varlen needs: total_q*H*d floats plus
+/* Bytes of workspace fa_bwd_varlen needs: total_q*H*max(d, 64) floats plus
  * 2*H*B*ceil(max_seqlen_q/128)*128 floats, parts rounded up to 256 bytes;
  * 0 for invalid arguments. */
 unsigned long long fa_bwd_varlen_workspace(int B, int H, int total_q, int max_seqlen_q, int d);

@@ -154,12 +154,14 @@ DO, DQ, DK, DV, WS = 0x800000, 0x900000, 0xA00000, 0xB00000, 0xC00000
 
 
 def test_bwd_workspace_size(lib):
-    """B*H*Nq*d floats plus two floats per padded query row, parts rounded up
-    to 256 bytes."""
+    """B*H*Nq*max(d, 64) floats (dq accumulator rows of the gradient kernel's
+    head dim) plus two floats per padded query row, parts rounded up to 256
+    bytes."""
     up = lambda n: (n + 255) // 256 * 256
-    for B, H, Nq, d in [(1, 1, 1, 64), (2, 16, 8192, 128), (1, 3, 300, 64)]:
+    for B, H, Nq, d in [(1, 1, 1, 64), (2, 16, 8192, 128), (1, 3, 300, 64), (2, 3, 300, 32)]:
         pad = (Nq + 127) // 128 * 128
-        assert fa.fa_bwd_workspace(B, H, Nq, d) == up(B * H * Nq * d * 4) + 2 * up(B * H * pad * 4)
+        assert (fa.fa_bwd_workspace(B, H, Nq, d)
+                == up(B * H * Nq * max(d, 64) * 4) + 2 * up(B * H * pad * 4))
     for bad in [(0, 1, 1, 64), (1, 0, 1, 64), (1, 1, 0, 64), (1, 1, 1, 0)]:
         assert fa.fa_bwd_workspace(*bad) == 0
 
@@ -231,7 +233,7 @@ def test_bwd_varlen_workspace_size(lib):
     for B, H, tq, mq, d in [(1, 1, 1, 1, 64), (3, 4, 1000, 700, 128), (2, 2, 300, 129, 32)]:
         pad = (mq + 127) // 128 * 128
         assert (fa.fa_bwd_varlen_workspace(B, H, tq, mq, d)
-                == up(tq * H * d * 4) + 2 * up(H * B * pad * 4))
+                == up(tq * H * max(d, 64) * 4) + 2 * up(H * B * pad * 4))
     assert fa.fa_bwd_varlen_workspace(0, 1, 10, 10, 64) == 0
 
 
