@@ -493,6 +493,9 @@ def main():
         "gpu_launches": args.steps * (3 if bwd or stage_ws is not None
                                       else 2 if wspace is not None else 1),
         "clocks": clocks,
+        # per step, between consecutive events (the value above is their mean)
+        "step_ms": {"min": min(launch_ms), "median": sorted(launch_ms)[len(launch_ms) // 2],
+                    "max": max(launch_ms)},
     }
     if varlen is not None:
         line["config"] = {"workload": "varlen32-l512to8192-h16-d128-bf16-causal",

@@ -25,6 +25,7 @@ int g_dev_ok[kMaxDevices] = {};         // 0 unknown, 1 sm_103, -1 other
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 std::atomic<int> g_skip_v_load{0};
 std::atomic<unsigned long long> g_wait_limit_ns{0};
+std::atomic<int> g_force_items{0};  // query tiles per CTA forced by a test (0 = automatic)
 
 size_t elem_size(int dtype) { return (dtype == FA_DTYPE_BF16 || dtype == FA_DTYPE_F16) ? 2 : 4; }
 
@@ -131,12 +132,47 @@ int encode_map(CUtensorMap *map, const void *base, int dtype, int BH, int N, int
 
 int ceil_div(int a, int b) { return (a + b - 1) / b; }
 
-// Query tiles per CTA of the plain 16-bit forward: two (heaviest with
-// lightest), so a CTA's second tile overlaps the first one's epilogue and
-// every causal CTA has the same work.  The fp32 path keeps one.
-constexpr int kItemsPerCta = 2;
-int items_per_cta(int dtype) {
-  return (dtype == FA_DTYPE_BF16 || dtype == FA_DTYPE_F16) ? kItemsPerCta : 1;
+int sm_count();
+
+// Query tiles per CTA of the plain 16-bit forward, G in {1, 2, 4}; the
+// tiles of a CTA are taken in zigzag pairs (heaviest with lightest), so with
+// G >= 2 every causal CTA has the same work.  A CTA's fixed cost (set-up,
+// pipeline fill, its last epilogue) is paid once for all its tiles, and each
+// next tile's loads and first products overlap the previous epilogue; but
+// fewer, longer CTAs can leave the SMs' last wave part empty.  The choice
+// minimises a makespan model in units of one key tile's time t:
+//   G >= 2: ceil(CTAs / SMs) * (G * nbar + c)          (equal CTAs)
+//   G = 1:  CTAs * (nbar + c1) / SMs + nbar             (causal: uneven CTAs,
+//           heaviest first; non-causal: as G >= 2 with c1)
+// nbar = mean key tiles per query tile; c and c1 = fixed cost per CTA with
+// and without a following tile to hide the epilogue.  Fitted on GB300 at
+// d = 128 (t = 0.77 us, c = 2.0 us, c1 = 3.0 us); a tile's time scales with
+// the head dim, the fixed cost does not.  The fp32 path keeps one.
+int items_per_cta(int dtype, int d, int causal, long long planes, int n_qtiles, int n_ktiles) {
+  if (dtype != FA_DTYPE_BF16 && dtype != FA_DTYPE_F16) return 1;
+  const int forced = g_force_items.load();
+  if (forced > 0) return forced < fa::kMaxItemsPerCta ? forced : fa::kMaxItemsPerCta;
+  const double sms = sm_count() > 0 ? sm_count() : 1;
+  // key tiles summed over the query tiles of one (batch, head)
+  const double nq = n_qtiles, nk = n_ktiles;
+  const double ksum = !causal ? nq * nk
+                      : (nq <= nk ? nq * (nq + 1) / 2 : nk * (nk + 1) / 2 + (nq - nk) * nk);
+  const double nbar = ksum / nq;
+  const double tile = d <= 64 ? 0.5 : d <= 128 ? 1.0 : 2.0;  // relative key-tile time
+  const double c = 2.6 / tile, c1 = 3.9 / tile;
+  const double qtiles = static_cast<double>(planes) * n_qtiles;
+  double best = causal ? qtiles * (nbar + c1) / sms + nbar
+                       : std::ceil(qtiles / sms) * (nbar + c1);
+  int pick = 1;
+  for (int g = 2; g <= fa::kMaxItemsPerCta; g *= 2) {
+    const double ctas = std::ceil(qtiles / g);
+    const double cost = std::ceil(ctas / sms) * (g * nbar + c);
+    if (cost < best) {
+      best = cost;
+      pick = g;
+    }
+  }
+  return pick;
 }
 
 // The tensor-core forward instantiation for (dtype, d); the combination has
@@ -232,7 +268,8 @@ int fa_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int
   const unsigned long long lim = g_wait_limit_ns.load();
   p.wait_limit_ns = lim ? lim : fa::kDefaultWaitLimitNs;
   p.skip_v_load = g_skip_v_load.load();
-  p.items_per_cta = items_per_cta(dtype);
+  p.items_per_cta = items_per_cta(dtype, d, causal, static_cast<long long>(B) * H, p.n_qtiles,
+                                  p.n_ktiles);
 
   cudaError_t e = launch_tc_any(mq, mk, mv, mo, p, B, causal, d, dtype, s);
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
@@ -297,6 +334,12 @@ int fa_version(void) { return FA_VERSION; }
 int fa_set_test_hooks(int skip_v_load, unsigned long long wait_limit_ns) {
   g_skip_v_load.store(skip_v_load ? 1 : 0);
   g_wait_limit_ns.store(wait_limit_ns);
+  return FA_OK;
+}
+
+int fa_set_items_per_cta(int n) {
+  if (n < 0 || n > fa::kMaxItemsPerCta) return FA_ERR_INVALID_ARG;
+  g_force_items.store(n);
   return FA_OK;
 }
 
@@ -410,7 +453,8 @@ extern "C" int fa_fwd_noalloc(const void *q, const void *k, const void *v, void 
     const unsigned long long lim = g_wait_limit_ns.load();
     p.wait_limit_ns = lim ? lim : fa::kDefaultWaitLimitNs;
     p.skip_v_load = g_skip_v_load.load();
-    p.items_per_cta = items_per_cta(dtype);
+    p.items_per_cta = items_per_cta(dtype, d, causal, static_cast<long long>(B) * H, p.n_qtiles,
+                                    p.n_ktiles);
     cudaError_t e = launch_tc_any(mq, mk, mv, mo, p, B, causal, d, dtype, s);
     if (e != cudaSuccess) return FA_ERR_CUDA;
   }

@@ -57,9 +57,18 @@ struct TcParams {
   int kv_staged = 0;
   // Query tiles per CTA (plain problems, 16-bit types): 1, or an even number
   // taken from the zigzag heaviest/lightest order (the grid then has
-  // ceil(n_qtiles / items_per_cta) CTAs per head).
+  // ceil(n_qtiles / items) CTAs per head, items = tc_items(*this)).
   int items_per_cta = 1;
 };
+
+// Query tiles per CTA of the forward kernel (at most kMaxItemsPerCta: the
+// kernel has one O-staged barrier per item); the launcher sizes the grid
+// with the same value.
+constexpr int kMaxItemsPerCta = 4;
+__host__ __device__ inline int tc_items(const TcParams &p) {
+  return p.items_per_cta <= 1 ? 1 : (p.items_per_cta < kMaxItemsPerCta ? p.items_per_cta
+                                                                         : kMaxItemsPerCta);
+}
 
 struct SimtParams {
   const float *q, *k, *v;

@@ -106,8 +106,9 @@ struct TcCfg {
   static constexpr int OFF_BAR = OFF_VT + NVT * TILE_BYTES;
   // q, kfull[KST], kempty[KST], vfull[VST], vempty[VST], sfull[NS], pfull[NS],
   // odone[NS], fin[2], kready[KST]
-  // ... then qempty, ofree (several query tiles per CTA)
-  static constexpr int NBAR = 1 + 2 * KST + 2 * VST + 3 * NS + 2 + KST + 2;
+  // ... then qempty, ofree, ostaged[kMaxItemsPerCta] (several query tiles
+  // per CTA)
+  static constexpr int NBAR = 1 + 2 * KST + 2 * VST + 3 * NS + 2 + KST + 2 + kMaxItemsPerCta;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;       // tmem base, abort flag
   static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;   // + alignment slack
   static constexpr int THREADS = 224;
@@ -154,6 +155,7 @@ __global__ void __launch_bounds__(224, 1)
   const uint32_t bKready = bFin2 + 8;                  // + 8*stage (fp32 path)
   const uint32_t bQempty = bKready + 8 * C::KST;       // Q of an item read by its last S
   const uint32_t bOfree = bQempty + 8;                 // O of an item read by the epilogue
+  const uint32_t bOstaged = bOfree + 8;                // + 8*item: its O staged for TMA
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::OFF_MISC);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::OFF_MISC + 4);
 
@@ -184,7 +186,7 @@ __global__ void __launch_bounds__(224, 1)
   // G*x .. G*x+G-1 of the zigzag order heaviest, lightest, 2nd heaviest, ...,
   // so with an even G every CTA has the same causal work, and an item's loads
   // and first products overlap the previous item's epilogue.
-  const int G = p.items_per_cta > 1 ? p.items_per_cta : 1;
+  const int G = tc_items(p);
   auto item_qt = [&](int g) -> int {  // query tile of item g, or -1
     if (G == 1) return g == 0 ? (CAUSAL ? (n_qtiles - 1 - qidx) : qidx) : -1;
     const int zi = G * static_cast<int>(blockIdx.x) + g;
@@ -253,6 +255,8 @@ __global__ void __launch_bounds__(224, 1)
     mbar_init(bFin2, 1);
     mbar_init(bQempty, 1);
     mbar_init(bOfree, 128);
+#pragma unroll
+    for (int g = 0; g < kMaxItemsPerCta; ++g) mbar_init(bOstaged + 8 * g, 128);
     *abort_flag = 0;
     fence_barrier_init();
     fence_proxy_async_smem();
@@ -280,6 +284,23 @@ __global__ void __launch_bounds__(224, 1)
       const uint64_t pol_kv = l2_policy_evict_last();
       int nk = 0, nv = 0, nq = 0;  // loads issued (K and V ring positions, Q tiles)
       bool ok = true;
+      // Several query tiles per CTA: the epilogue of every item but the last
+      // stages O in the V stage of the item's last tile (free once its P V
+      // completed).  This thread stores it with TMA, and refills that stage
+      // only after the store has read it.
+      int last_v[kMaxItemsPerCta];  // V ring position of each item's last tile
+      int n_items = 0, pend = 0;    // items loaded; next item whose O is stored here
+      auto store_o = [&](int gi) -> bool {
+        if (!bounded_wait(bOstaged + 8 * gi, 0, w)) return false;
+        const uint32_t src = sV + (last_v[gi] % C::VST) * C::TILE_BYTES;
+#pragma unroll
+        for (int c = 0; c < C::NCH; ++c)
+          if (c * C::CH_ELEMS < dio)  // a chunk wholly past the row is not stored
+            tma_store_3d(&tm_o, src + c * C::CHUNK_BYTES, c * C::CH_ELEMS, item_qt(gi) * BM, bh);
+        tma_store_commit();
+        tma_store_wait_read_all();
+        return true;
+      };
       for (int g = 0; ok && g < G; ++g) {
         const int tq = item_qt(g);
         if (tq < 0) break;
@@ -320,6 +341,10 @@ __global__ void __launch_bounds__(224, 1)
               break;
             }
             const int s = nv % C::VST, r = nv / C::VST;
+            if (pend < g && last_v[pend] == nv - C::VST) {
+              if (!(ok = store_o(pend))) break;  // this stage holds item pend's O
+              ++pend;
+            }
             if (r > 0) ok = bounded_wait(bVempty + 8 * s, (r - 1) & 1, w);
             if (!ok) break;
             mbar_arrive_expect_tx(bVfull + 8 * s, C::TILE_BYTES);
@@ -339,7 +364,11 @@ __global__ void __launch_bounds__(224, 1)
             ++nv;
           }
         }
+        if (ok) last_v[g] = nv - 1;
+        n_items = g + 1;
       }
+      // O of the items before the last whose V stage was not refilled.
+      for (; ok && pend < n_items - 1; ++pend) ok = store_o(pend);
       // Drain: no TMA write may still be in flight when the CTA exits.
       if (nq > 0) bounded_wait(bQ, (nq - 1) & 1, w, false);
       for (int s = 0; s < C::KST; ++s) {
@@ -566,6 +595,7 @@ __global__ void __launch_bounds__(224, 1)
 
     int buf = 0, bph = 0;            // score buffer of tile j and the parity of its use
     int pbuf = C::NS - 1, pbph = 1;  // the same for tile j - 1
+    int tiles_done = 0;              // key tiles of all items so far (= V ring position)
     for (int g = 0; g < G; ++g) {
     const int tq = item_qt(g);
     if (tq < 0) break;
@@ -709,6 +739,7 @@ __global__ void __launch_bounds__(224, 1)
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(bPfull + 8 * buf);
+      ++tiles_done;
       pbuf = buf;
       pbph = bph;
       if (++buf == C::NS) { buf = 0; bph ^= 1; }
@@ -725,6 +756,7 @@ __global__ void __launch_bounds__(224, 1)
     }
 
     // ------------------------------------------------ epilogue
+    const bool last_item = g + 1 >= G || item_qt(g + 1) < 0;
     // The last P V; its commit also covers every earlier UMMA.
     if (ok)
       ok = __all_sync(kFull, bounded_wait(bOdone + 8 * pbuf, pbph, w));
@@ -753,10 +785,9 @@ __global__ void __launch_bounds__(224, 1)
         }
         if (row < Nq) p.ws_lse[prow] = m_used * kLn2 + logf(l);
       }
-    } else if (p.cu_q != nullptr || G > 1) {
+    } else if (p.cu_q != nullptr) {
       // Variable-length batches: the rows after this sequence belong to the
-      // next one, so O is written row by row from registers (no TMA store);
-      // likewise with several items per CTA, whose K stages stay in use.
+      // next one, so O is written row by row from registers (no TMA store).
       if (ok) {
         tc_fence_after();
         const float inv_l = 1.f / l;
@@ -795,16 +826,17 @@ __global__ void __launch_bounds__(224, 1)
           }
         }
         if (row < Nq) p.lse[hc * p.lse_head_stride + gr] = m_used * kLn2 + logf(l);
-        // O of this item has been read: the next item's P V may start.
-        tc_fence_before();
-        mbar_arrive(bOfree);
       }
     } else if (ok) {
       tc_fence_after();
       const float inv_l = 1.f / l;
-      // Staging in K stage 0: every S_j is complete, so no UMMA reads K any
-      // more and the producer has no K load outstanding.
-      uint8_t *stage = smem + C::OFF_K;
+      // Staging for the TMA store.  The last item: K stage 0 (every S_j is
+      // complete, so no UMMA reads K any more and the producer has no K load
+      // outstanding).  An earlier item: the V stage of its last tile, whose
+      // P V has completed; the producer stores it and refills the stage
+      // after that.
+      uint8_t *stage = last_item ? smem + C::OFF_K
+                                 : smem + C::OFF_V + ((tiles_done - 1) % C::VST) * C::TILE_BYTES;
 #pragma unroll
       for (int c = 0; c < D; c += 32) {
         uint32_t o[32];
@@ -848,14 +880,24 @@ __global__ void __launch_bounds__(224, 1)
         }
       }
       if (row < Nq) p.lse[static_cast<size_t>(bh) * Nq + row] = m_used * kLn2 + logf(l);
+      if (!last_item) {
+        fence_proxy_async_smem();
+        mbar_arrive(bOstaged + 8 * g);   // the producer stores this item's O
+      }
+    }
+    // O of this item has been read from tensor memory: the next item's
+    // P V may start.
+    if (ok && !last_item) {
+      tc_fence_before();
+      mbar_arrive(bOfree);
     }
     fence_proxy_async_smem();
     named_bar_sync(1, 128);
-    if (G == 1 && nsp == 1 && p.cu_q == nullptr && threadIdx.x == 0 && *abort_flag == 0) {
+    if (last_item && nsp == 1 && p.cu_q == nullptr && threadIdx.x == 0 && *abort_flag == 0) {
 #pragma unroll
       for (int c = 0; c < C::NCH; ++c)
         if (c * C::CH_ELEMS < dio)  // a chunk wholly past the row is not stored
-          tma_store_3d(&tm_o, sK + c * C::CHUNK_BYTES, c * C::CH_ELEMS, q0, bh);
+          tma_store_3d(&tm_o, sK + c * C::CHUNK_BYTES, c * C::CH_ELEMS, tq * BM, bh);
       tma_store_commit();
       tma_store_wait_read_all();
     }
@@ -886,8 +928,8 @@ cudaError_t launch_tc(const CUtensorMap &q, const CUtensorMap &k, const CUtensor
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
-  const int gx = p.items_per_cta > 1 ? (p.n_qtiles + p.items_per_cta - 1) / p.items_per_cta
-                                    : p.n_qtiles * p.n_splits;
+  const int items = tc_items(p);
+  const int gx = items > 1 ? (p.n_qtiles + items - 1) / items : p.n_qtiles * p.n_splits;
   cfg.gridDim = dim3(static_cast<unsigned>(gx), static_cast<unsigned>(p.H),
                      static_cast<unsigned>(B));
   cfg.blockDim = dim3(C::THREADS, 1, 1);

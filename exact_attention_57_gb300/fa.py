@@ -30,7 +30,7 @@ FA_DTYPE_F32_SIMT = 2
 FA_DTYPE_F16 = 3
 
 EXPORTED = ("fa_fwd", "fa_fwd_host", "fa_fwd_status", "fa_status_string", "fa_version",
-            "fa_set_test_hooks", "fa_fwd_noalloc", "fa_fwd_splitkv", "fa_fwd_splitkv_workspace",
+            "fa_set_test_hooks", "fa_set_items_per_cta", "fa_fwd_noalloc", "fa_fwd_splitkv", "fa_fwd_splitkv_workspace",
             "fa_fwd_varlen", "fa_bwd", "fa_bwd_workspace", "fa_fwd_staged",
             "fa_fwd_staged_workspace", "fa_bwd_varlen", "fa_bwd_varlen_workspace")
 
@@ -91,6 +91,8 @@ def load(path: str | None = None):
     lib.fa_version.restype = i
     lib.fa_set_test_hooks.argtypes = [i, ctypes.c_ulonglong]
     lib.fa_set_test_hooks.restype = i
+    lib.fa_set_items_per_cta.argtypes = [i]
+    lib.fa_set_items_per_cta.restype = i
     if path is None:
         _lib = lib
     return lib
@@ -291,6 +293,11 @@ def fa_version() -> int:
 
 def fa_set_test_hooks(skip_v_load: int = 0, wait_limit_ns: int = 0) -> int:
     return load().fa_set_test_hooks(int(skip_v_load), int(wait_limit_ns))
+
+
+def fa_set_items_per_cta(n: int = 0) -> int:
+    """Testing aid: query tiles per CTA of the 16-bit forward (0 = automatic)."""
+    return load().fa_set_items_per_cta(int(n))
 
 
 # --------------------------------------------------------------- torch helpers

@@ -332,6 +332,17 @@ int fa_version(void);
  */
 int fa_set_test_hooks(int skip_v_load, unsigned long long wait_limit_ns);
 
+/*
+ * fa_set_items_per_cta — testing aid, process-wide; no counterpart on the
+ * pages (a scheduling choice of this implementation).  The bf16/fp16
+ * forward of fa_fwd and fa_fwd_noalloc runs n query tiles per CTA, taken in
+ * zigzag order (tile x with tile n_qtiles-1-x, ...), instead of its own
+ * choice (0 = automatic: 1, 2 or 4, whichever a makespan model of the grid
+ * on the SMs rates fastest).  Results do not depend on n: every tile does
+ * the same arithmetic.  n in 0..4, else FA_ERR_INVALID_ARG; returns FA_OK.
+ */
+int fa_set_items_per_cta(int n);
+
 #ifdef __cplusplus
 }
 #endif

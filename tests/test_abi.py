@@ -153,6 +153,14 @@ def test_varlen_refuses_simt_and_unsupported_dims(lib):
 DO, DQ, DK, DV, WS = 0x800000, 0x900000, 0xA00000, 0xB00000, 0xC00000
 
 
+def test_items_per_cta_hook_range(lib):
+    """The testing aid takes 0 (automatic) .. 4 and refuses anything else."""
+    for n in (-1, 5, 100):
+        assert fa.fa_set_items_per_cta(n) == fa.FA_ERR_INVALID_ARG
+    for n in (4, 1, 0):
+        assert fa.fa_set_items_per_cta(n) == fa.FA_OK
+
+
 def test_bwd_workspace_size(lib):
     """B*H*Nq*max(d, 64) floats (dq accumulator rows of the gradient kernel's
     head dim) plus two floats per padded query row, parts rounded up to 256

@@ -1,0 +1,80 @@
+"""Several query tiles per CTA in the 16-bit forward (needs a GB300).
+
+A CTA runs n query tiles (zigzag order: tile x with tile n_qtiles-1-x, ...)
+through one pipeline; which CTA computes a tile must not change the tile's
+arithmetic.  Each forced count is checked against the float64 oracle and bit
+for bit against one tile per CTA, on ragged and unequal lengths, causal and
+not, for every 16-bit head dim.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from exact_attention_57_gb300 import fa
+from exact_attention_57_gb300.workloads import DTYPE_BF16, DTYPE_F16, make_inputs
+from parity_util import compare, run_gpu, run_oracle
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(autouse=True)
+def automatic_items_afterwards():
+    yield
+    assert fa.fa_set_items_per_cta(0) == fa.FA_OK
+
+
+CASES = [
+    (DTYPE_BF16, 128, 700, 700),    # 6 query tiles, ragged last tile
+    (DTYPE_BF16, 128, 1000, 1000),  # 8 query tiles
+    (DTYPE_BF16, 64, 1000, 1000),   # Q in tensor memory
+    (DTYPE_BF16, 256, 700, 700),    # one K and one V stage
+    (DTYPE_BF16, 32, 700, 700),     # zero-padded to the d = 64 kernel
+    (DTYPE_F16, 128, 1000, 1000),
+    (DTYPE_BF16, 128, 129, 129),    # two tiles, the second one row
+    (DTYPE_BF16, 128, 1, 1),        # fewer tiles than one CTA takes
+    (DTYPE_BF16, 128, 900, 300),    # Nq > Nk
+    (DTYPE_BF16, 128, 300, 900),    # Nq < Nk
+]
+
+
+def _id(c):
+    dt, d, nq, nk = c
+    return f"{'bf16' if dt == DTYPE_BF16 else 'f16'}-d{d}-{nq}x{nk}"
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("case", CASES, ids=[_id(c) for c in CASES])
+def test_items_per_cta_same_results(case, causal):
+    dtype, d, Nq, Nk = case
+    q, k, v = make_inputs(2, 3, Nq, Nk, d, dtype, seed=500 + d + Nq + 3 * Nk)
+    scale = 1.0 / math.sqrt(d)
+    assert fa.fa_set_items_per_cta(1) == fa.FA_OK
+    o1, l1 = run_gpu(q, k, v, scale, causal, dtype)
+    ro, rl = run_oracle(q, k, v, scale, causal)
+    compare(o1, l1, ro, rl, dtype, f"{_id(case)} causal={causal} items=1")
+    for items in (2, 3, 4):
+        assert fa.fa_set_items_per_cta(items) == fa.FA_OK
+        o, lse = run_gpu(q, k, v, scale, causal, dtype)
+        assert np.array_equal(o, o1), f"items={items}: O differs from one tile per CTA"
+        assert np.array_equal(lse, l1), f"items={items}: LSE differs from one tile per CTA"
+
+
+def test_noalloc_with_items_per_cta():
+    """fa_fwd_noalloc takes the same choice of tiles per CTA."""
+    dev = torch.device("cuda:0")
+    B, H, N, d = 2, 3, 1000, 128
+    q, k, v = (t.to(dev) for t in make_inputs(B, H, N, N, d, DTYPE_BF16, seed=77))
+    stream = torch.cuda.current_stream(dev).cuda_stream
+    outs = []
+    for items in (1, 4):
+        assert fa.fa_set_items_per_cta(items) == fa.FA_OK
+        o = torch.full_like(q, float("nan"))
+        lse = torch.full((B, H, N), float("nan"), device=dev, dtype=torch.float32)
+        st, word = fa.fa_fwd_noalloc(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                     lse.data_ptr(), B, H, N, N, d, 1.0 / math.sqrt(d), 1,
+                                     DTYPE_BF16, stream, wait=True)
+        assert (st, word) == (fa.FA_OK, 0)
+        outs.append((o.cpu(), lse.cpu()))
+    assert torch.equal(outs[0][0], outs[1][0]) and torch.equal(outs[0][1], outs[1][1])
