@@ -11,23 +11,32 @@
 // atomic adds.  The page's dV update reads the upstream gradient of the key's
 // row instead of the query's; the product above is the derivative.
 //
-// GB300 design (one CTA = one (batch, head, 128-key tile)).  Each 128-query
-// tile is processed as two halves h of 64 queries with their own tensor
-// memory, so that the dQ drain of one half overlaps the other half's softmax
-// and products:
+// GB300 design (one CTA = one (batch, head, 128-key tile), 16 warps).  Each
+// 128-query tile is processed as two halves h of 64 queries with their own
+// tensor memory, so that one half's softmax overlaps the other half's
+// products:
 //   warps 0-7   per half: read S_h^T and dP_h^T from tensor memory (lane =
 //               key, warp w covers lanes 32*(w%4) and queries 32*(w/4) of the
 //               half), form P^T (packed to 16 bits, back into tensor memory:
 //               the A operand of dV) and dS = scale * P (dP - D) (16 bits,
-//               shared memory).  Then drain dQ_h^T from tensor memory with fp32
-//               atomic adds.  At the end, write dV and dK.
-//   warp 8      TMA producer: K_j and V_j once, then per query tile Q_i, dO_i
+//               shared memory).  At the end, write dV and dK.
+//   warps 8-11  dQ drain: dQ_h^T out of tensor memory, then fp32 atomic adds
+//               into the accumulator (an SM adds about 21 bytes per clock
+//               whatever the number of warps, so the adds run beside the
+//               softmax instead of after it).
+//   warp 12     TMA producer: K_j and V_j once, then per query tile Q_i, dO_i
 //               (2-stage ring) and the 128 rows' LSE*log2(e) and D (bulk copies).
-//   warp 9      UMMA issuer (one lane), owner of tensor memory, per half h:
-//                 S_h^T = K_j Q_h^T,  dP_h^T = V_j dO_h^T   (both operands K-major)
+//   warp 13     UMMA issuer (one lane), owner of tensor memory, per half h:
 //                 dV  += P_h^T dO_h                         (A in TMEM, B MN-major)
 //                 dK  += dS_h^T Q_h                         (A K-major, B MN-major)
 //                 dQ_h^T = K_j^T dS_h^T                     (A, B MN-major)
+//               then at once the next tile's
+//                 S_h^T = K_j Q_h^T,  dP_h^T = V_j dO_h^T   (both operands K-major)
+//               so half 0 of the next tile need not wait for half 1's products.
+// The block is launched with 128 registers a thread; setmaxnreg gives the
+// softmax warpgroups 152, the drain 104 and the producer/issuer group 104
+// (the issuer's fully unrolled UMMA loops need them: rolled, each UMMA took
+// about twice as long to issue).
 // dS_h is stored once, one 128-byte-swizzled row of 64 queries per key, and
 // read as two operands: rows = keys with queries contiguous is dS_h^T K-major
 // (dK) and dS_h^T MN-major (dQ^T).  dQ^T has the head dimension on the TMEM
@@ -39,7 +48,7 @@
 // columns) goes over columns 16..47 of S_h^T: each query quarter then writes
 // only columns it has itself read, so neither waits for the other.  dQ_h^T
 // goes over dP_h^T once the softmax has read it; the next tile's dP_h^T is
-// issued once dQ_h^T has been drained.
+// issued once the drain warps have taken dQ_h^T into registers.
 //
 // Every wait is bounded (globaltimer); on expiry the CTA raises an abort
 // flag, records its role in the status word, drains in-flight copies and
@@ -87,14 +96,22 @@ struct BwdCfg {
   static constexpr int USED = OFF_MISC + 16;
   static constexpr int MAX_SMEM = 227 * 1024;
   static constexpr int SMEM_BYTES = USED + 1024 <= MAX_SMEM ? USED + 1024 : MAX_SMEM;
-  static constexpr int THREADS = 320;
+  // 16 warps: 0-7 softmax, 8-11 dQ drain, 12 producer, 13 UMMA issuer and
+  // TMEM owner (14, 15 idle).  The block is launched with 128 registers a
+  // thread; setmaxnreg moves them to the softmax warpgroups.
+  static constexpr int THREADS = 512;
+  static constexpr int WARP_PROD = 12;
+  static constexpr int WARP_MMA = 13;
+  static constexpr uint32_t REG_SOFTMAX = 152, REG_DRAIN = 104, REG_MISC = 104;
+  static_assert(8 * 32 * REG_SOFTMAX + 4 * 32 * REG_DRAIN + 4 * 32 * REG_MISC <= THREADS * 128,
+                "the register split must fit in what the block is launched with");
   static_assert(D == 64 || D == 128, "head dim");
   static_assert(COL_S0 + 2 * COL_HALF <= TMEM_COLS, "tensor memory budget");
   static_assert(USED + 16 <= SMEM_BYTES, "shared memory budget");
 };
 
 template <int D, bool CAUSAL, bool HALF>
-__global__ void __launch_bounds__(320, 1)
+__global__ void __launch_bounds__(512, 1)
     fa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v,
                   const __grid_constant__ CUtensorMap tm_do, const BwdParams p) {
@@ -178,7 +195,7 @@ __global__ void __launch_bounds__(320, 1)
       mbar_init(bSfull + 8 * h, 1);
       mbar_init(bPfull + 8 * h, 256);
       mbar_init(bDQfull + 8 * h, 1);
-      mbar_init(bDQfree + 8 * h, 256);
+      mbar_init(bDQfree + 8 * h, 128);
       mbar_init(bHdone + 8 * h, 1);
     }
     mbar_init(bFin, 1);
@@ -186,13 +203,13 @@ __global__ void __launch_bounds__(320, 1)
     fence_barrier_init();
     fence_proxy_async_smem();
   }
-  if (warp == 8 && lane == 0) {
+  if (warp == C::WARP_PROD && lane == 0) {
     tma_prefetch_desc(&tm_q);
     tma_prefetch_desc(&tm_k);
     tma_prefetch_desc(&tm_v);
     tma_prefetch_desc(&tm_do);
   }
-  if (warp == 9) {
+  if (warp == C::WARP_MMA) {
     tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
     tmem_relinquish();
   }
@@ -202,79 +219,77 @@ __global__ void __launch_bounds__(320, 1)
   const uint32_t tmem = *tmem_slot;
   WaitCtl w{abort_flag, p.status, p.wait_limit_ns, 0u};
 
-  if (warp == 8) {
-    // ------------------------------------------------------------ producer
-    w.role = kStatusProducer;
-    if (lane == 0 && n_it > 0) {
-      const uint64_t pol_kv = l2_policy_evict_first();   // read by this CTA only
-      const uint64_t pol_q = l2_policy_evict_last();     // read by every key tile
-      mbar_arrive_expect_tx(bKV, 2 * C::TILE_BYTES);
-#pragma unroll
-      for (int c = 0; c < C::NCH; ++c) {
-        tma_load_3d(sK + c * C::CHUNK_BYTES, &tm_k, bKV, c * C::CH_ELEMS, k_row0 + k0, hc, pol_kv);
-        tma_load_3d(sV + c * C::CHUNK_BYTES, &tm_v, bKV, c * C::CH_ELEMS, k_row0 + k0, hc, pol_kv);
-      }
-      int issued = 0;
-      bool ok = true;
-      for (int it = 0; it < n_it; ++it) {
-        const int s = it % C::NQS, r = it / C::NQS;
-        if (r > 0 && !(ok = bounded_wait(bQempty + 8 * s, (r - 1) & 1, w))) break;
-        const int q0 = (i_first + it) * BM;
-        const uint32_t bar = bQfull + 8 * s;
-        mbar_arrive_expect_tx(bar, 2 * C::TILE_BYTES + C::ROW_BYTES);
-#pragma unroll
+  const int wg = warp >> 2;  // warpgroup: 0, 1 softmax; 2 dQ drain; 3 producer, issuer
+  if (wg == 3) {
+    setmaxnreg_dec<C::REG_MISC>();
+    if (warp == C::WARP_PROD) {
+      // ------------------------------------------------------------ producer
+      w.role = kStatusProducer;
+      if (lane == 0 && n_it > 0) {
+        const uint64_t pol_kv = l2_policy_evict_first();   // read by this CTA only
+        const uint64_t pol_q = l2_policy_evict_last();     // read by every key tile
+        mbar_arrive_expect_tx(bKV, 2 * C::TILE_BYTES);
+  #pragma unroll
         for (int c = 0; c < C::NCH; ++c) {
-          tma_load_3d(sQ + s * C::TILE_BYTES + c * C::CHUNK_BYTES, &tm_q, bar, c * C::CH_ELEMS,
-                      q_row0 + q0, hc, pol_q);
-          tma_load_3d(sDO + s * C::TILE_BYTES + c * C::CHUNK_BYTES, &tm_do, bar,
-                      c * C::CH_ELEMS, q_row0 + q0, hc, pol_q);
+          tma_load_3d(sK + c * C::CHUNK_BYTES, &tm_k, bKV, c * C::CH_ELEMS, k_row0 + k0, hc, pol_kv);
+          tma_load_3d(sV + c * C::CHUNK_BYTES, &tm_v, bKV, c * C::CH_ELEMS, k_row0 + k0, hc, pol_kv);
         }
-        const size_t roff = row_base + q0;
-        bulk_load(sRow + s * C::ROW_BYTES, p.lse2 + roff, 512, bar);
-        bulk_load(sRow + s * C::ROW_BYTES + 512, p.dd + roff, 512, bar);
-        ++issued;
+        int issued = 0;
+        bool ok = true;
+        for (int it = 0; it < n_it; ++it) {
+          const int s = it % C::NQS, r = it / C::NQS;
+          if (r > 0 && !(ok = bounded_wait(bQempty + 8 * s, (r - 1) & 1, w))) break;
+          const int q0 = (i_first + it) * BM;
+          const uint32_t bar = bQfull + 8 * s;
+          mbar_arrive_expect_tx(bar, 2 * C::TILE_BYTES + C::ROW_BYTES);
+  #pragma unroll
+          for (int c = 0; c < C::NCH; ++c) {
+            tma_load_3d(sQ + s * C::TILE_BYTES + c * C::CHUNK_BYTES, &tm_q, bar, c * C::CH_ELEMS,
+                        q_row0 + q0, hc, pol_q);
+            tma_load_3d(sDO + s * C::TILE_BYTES + c * C::CHUNK_BYTES, &tm_do, bar,
+                        c * C::CH_ELEMS, q_row0 + q0, hc, pol_q);
+          }
+          const size_t roff = row_base + q0;
+          bulk_load(sRow + s * C::ROW_BYTES, p.lse2 + roff, 512, bar);
+          bulk_load(sRow + s * C::ROW_BYTES + 512, p.dd + roff, 512, bar);
+          ++issued;
+        }
+        (void)ok;
+        // Drain: no copy may still be writing shared memory when the CTA exits.
+        bounded_wait(bKV, 0, w, false);
+        for (int s = 0; s < C::NQS; ++s) {
+          const int cnt = (issued > s) ? (issued - 1 - s) / C::NQS + 1 : 0;
+          if (cnt > 0) bounded_wait(bQfull + 8 * s, (cnt - 1) & 1, w, false);
+        }
       }
-      (void)ok;
-      // Drain: no copy may still be writing shared memory when the CTA exits.
-      bounded_wait(bKV, 0, w, false);
-      for (int s = 0; s < C::NQS; ++s) {
-        const int cnt = (issued > s) ? (issued - 1 - s) / C::NQS + 1 : 0;
-        if (cnt > 0) bounded_wait(bQfull + 8 * s, (cnt - 1) & 1, w, false);
-      }
-    }
-    __syncwarp();
-  } else if (warp == 9) {
-    // ------------------------------------------------------------ UMMA issuer
-    w.role = kStatusMma;
-    if (lane == 0 && n_it > 0) {
-      constexpr uint32_t kFmt = HALF ? 0u : 1u;                        // f16 / bf16
-      constexpr uint32_t kIdescS = make_idesc(kFmt, 128, C::HQ, 0u, 0u); // S^T, dP^T
-      constexpr uint32_t kIdescAcc = make_idesc(kFmt, 128, D, 0u, 1u);   // dV, dK
-      constexpr uint32_t kIdescDQ = make_idesc(kFmt, 128, C::HQ, 1u, 1u); // dQ^T
-      bool ok = bounded_wait(bKV, 0, w);
-      for (int it = 0; ok && it < n_it; ++it) {
-        const int s = it % C::NQS;
-        if (!(ok = bounded_wait(bQfull + 8 * s, (it / C::NQS) & 1, w))) break;
-        const uint32_t qb = sQ + s * C::TILE_BYTES, db = sDO + s * C::TILE_BYTES;
-        // S_h^T and dP_h^T for both halves.  S_h^T overwrites P_h^T of the
-        // previous tile (and dS_h is rewritten after it): that tile's products
-        // of half h must be complete.  dP_h^T overwrites its dQ_h^T, which
-        // must have been drained.
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
+      __syncwarp();
+    } else if (warp == C::WARP_MMA) {
+      // ------------------------------------------------------------ UMMA issuer
+      w.role = kStatusMma;
+      if (lane == 0 && n_it > 0) {
+        constexpr uint32_t kFmt = HALF ? 0u : 1u;                        // f16 / bf16
+        constexpr uint32_t kIdescS = make_idesc(kFmt, 128, C::HQ, 0u, 0u); // S^T, dP^T
+        constexpr uint32_t kIdescAcc = make_idesc(kFmt, 128, D, 0u, 1u);   // dV, dK
+        constexpr uint32_t kIdescDQ = make_idesc(kFmt, 128, C::HQ, 1u, 1u); // dQ^T
+        // S_h^T = K_j Q_h^T (over P_h^T of the previous tile) and
+        // dP_h^T = V_j dO_h^T (over dQ_h^T of the previous tile) of tile t.
+        auto issue_s = [&](int t, int h) {
+          const int s = t % C::NQS;
+          const uint32_t qb = sQ + s * C::TILE_BYTES;
           const uint32_t col = C::COL_S0 + h * C::COL_HALF;
-          if (it > 0 && !(ok = bounded_wait(bHdone + 8 * h, (it - 1) & 1, w))) break;
-          tc_fence_after();
-#pragma unroll
+  #pragma unroll
           for (int kk = 0; kk < D / C::UK; ++kk) {
             const uint32_t off = (kk >> 2) * C::CHUNK_BYTES + (kk & 3) * 32;
             umma_ss<false>(tmem + col, sdesc_sw128(sK + off, 16, 1024),
                            sdesc_sw128(qb + h * C::HQ * 128 + off, 16, 1024), kIdescS,
                            kk > 0 ? 1u : 0u);
           }
-          if (it > 0 && !(ok = bounded_wait(bDQfree + 8 * h, (it - 1) & 1, w))) break;
-          tc_fence_after();
-#pragma unroll
+        };
+        auto issue_dp = [&](int t, int h) {
+          const int s = t % C::NQS;
+          const uint32_t db = sDO + s * C::TILE_BYTES;
+          const uint32_t col = C::COL_S0 + h * C::COL_HALF;
+  #pragma unroll
           for (int kk = 0; kk < D / C::UK; ++kk) {
             const uint32_t off = (kk >> 2) * C::CHUNK_BYTES + (kk & 3) * 32;
             umma_ss<false>(tmem + col + C::DP_OFF, sdesc_sw128(sV + off, 16, 1024),
@@ -282,45 +297,119 @@ __global__ void __launch_bounds__(320, 1)
                            kk > 0 ? 1u : 0u);
           }
           tc_commit(bSfull + 8 * h);
-        }
-        if (!ok) break;
-        // The products of each half once its P^T and dS are written.
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const uint32_t col = C::COL_S0 + h * C::COL_HALF;
-          if (!(ok = bounded_wait(bPfull + 8 * h, it & 1, w))) break;
+        };
+        bool ok = bounded_wait(bKV, 0, w) && bounded_wait(bQfull, 0, w);
+        if (ok) {
           tc_fence_after();
-          const uint32_t ds = sDS + h * C::DS_HALF_BYTES;
-          // dV += P_h^T dO_h and dK += dS_h^T Q_h: 16 queries per UMMA (8
-          // packed TMEM columns of P^T, 32 bytes of a dS row; 16 rows of
-          // 128 bytes of the MN-major B).
-#pragma unroll
-          for (int kk = 0; kk < C::HQ / C::UK; ++kk) {
-            const uint32_t brow = (h * C::HQ + kk * C::UK) * 128;
-            const uint32_t acc = (it > 0 || h > 0 || kk > 0) ? 1u : 0u;
-            umma_ts<false>(tmem + C::COL_DV, tmem + col + C::P_OFF + kk * 8,
-                           sdesc_sw128(db + brow, C::CHUNK_BYTES, 1024), kIdescAcc, acc);
-            umma_ss<false>(tmem + C::COL_DK, sdesc_sw128(ds + kk * 32, 16, 1024),
-                           sdesc_sw128(qb + brow, C::CHUNK_BYTES, 1024), kIdescAcc, acc);
+  #pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            issue_s(0, h);
+            issue_dp(0, h);
           }
-          // dQ_h^T = K_j^T dS_h^T over dP_h^T: 16 keys per UMMA.
-#pragma unroll
-          for (int kk = 0; kk < BN / C::UK; ++kk)
-            umma_ss<false>(tmem + col + C::DP_OFF,
-                           sdesc_sw128(sK + kk * C::UK * 128, C::CHUNK_BYTES, 1024),
-                           sdesc_sw128(ds + kk * C::UK * 128, C::CHUNK_BYTES, 1024), kIdescDQ,
-                           kk > 0 ? 1u : 0u);
-          tc_commit(bHdone + 8 * h);
-          tc_commit(bDQfull + 8 * h);
         }
-        tc_commit(bQempty + 8 * s);
+        // Per half h of tile t: the products once its P^T and dS are written,
+        // then at once the next tile's S_h^T, dP_h^T into the same columns (so
+        // the softmax of half 0 of tile t+1 need not wait for half 1's
+        // products of tile t).
+        for (int it = 0; ok && it < n_it; ++it) {
+          const int s = it % C::NQS;
+          const uint32_t qb = sQ + s * C::TILE_BYTES, db = sDO + s * C::TILE_BYTES;
+          const bool next = it + 1 < n_it;
+  #pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const uint32_t col = C::COL_S0 + h * C::COL_HALF;
+            if (!(ok = bounded_wait(bPfull + 8 * h, it & 1, w))) break;
+            tc_fence_after();
+            const uint32_t ds = sDS + h * C::DS_HALF_BYTES;
+            // dV += P_h^T dO_h and dK += dS_h^T Q_h: 16 queries per UMMA (8
+            // packed TMEM columns of P^T, 32 bytes of a dS row; 16 rows of
+            // 128 bytes of the MN-major B).
+  #pragma unroll
+            for (int kk = 0; kk < C::HQ / C::UK; ++kk) {
+              const uint32_t brow = (h * C::HQ + kk * C::UK) * 128;
+              const uint32_t acc = (it > 0 || h > 0 || kk > 0) ? 1u : 0u;
+              umma_ts<false>(tmem + C::COL_DV, tmem + col + C::P_OFF + kk * 8,
+                             sdesc_sw128(db + brow, C::CHUNK_BYTES, 1024), kIdescAcc, acc);
+              umma_ss<false>(tmem + C::COL_DK, sdesc_sw128(ds + kk * 32, 16, 1024),
+                             sdesc_sw128(qb + brow, C::CHUNK_BYTES, 1024), kIdescAcc, acc);
+            }
+            // dQ_h^T = K_j^T dS_h^T over dP_h^T: 16 keys per UMMA.
+  #pragma unroll
+            for (int kk = 0; kk < BN / C::UK; ++kk)
+              umma_ss<false>(tmem + col + C::DP_OFF,
+                             sdesc_sw128(sK + kk * C::UK * 128, C::CHUNK_BYTES, 1024),
+                             sdesc_sw128(ds + kk * C::UK * 128, C::CHUNK_BYTES, 1024), kIdescDQ,
+                             kk > 0 ? 1u : 0u);
+            tc_commit(bHdone + 8 * h);
+            tc_commit(bDQfull + 8 * h);
+            if (next) {
+              // Tile t+1 in its stage; half h's products complete (they read
+              // P_h^T and dS_h, which S_h^T and the softmax overwrite); dQ_h^T
+              // moved out of tensor memory by the drain warps.
+              if (h == 0 && !(ok = bounded_wait(bQfull + 8 * ((it + 1) % C::NQS),
+                                                ((it + 1) / C::NQS) & 1, w)))
+                break;
+              if (!(ok = bounded_wait(bHdone + 8 * h, it & 1, w))) break;
+              tc_fence_after();
+              issue_s(it + 1, h);
+              if (!(ok = bounded_wait(bDQfree + 8 * h, it & 1, w))) break;
+              tc_fence_after();
+              issue_dp(it + 1, h);
+            }
+          }
+          tc_commit(bQempty + 8 * s);
+        }
+        (void)ok;
+        tc_commit(bFin);
+        bounded_wait(bFin, 0, w, false);
       }
-      (void)ok;
-      tc_commit(bFin);
-      bounded_wait(bFin, 0, w, false);
+      __syncwarp();
+    }
+  } else if (wg == 2) {
+    setmaxnreg_dec<C::REG_DRAIN>();
+    // ------------------------------------------------------------ dQ drain
+    // dQ_h^T -> dq_acc with fp32 atomic adds: lane r = head-dim index, the
+    // half's 64 queries; the warp's 32 lanes add to 32 consecutive floats of
+    // one dQ row.  The values are taken out of tensor memory first, so the
+    // next tile's dP_h^T may go in while the adds (limited to about 21 bytes
+    // per clock per SM) run beside the softmax warps.  (D = 64: lanes 64-127
+    // hold no dQ.)
+    w.role = kStatusSoftmax;
+    const int r = (warp & 3) * 32 + lane;
+    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    bool ok = true;
+    for (int it = 0; ok && it < n_it; ++it) {
+      const int qt = i_first + it;
+#pragma unroll 1
+      for (int h = 0; h < 2; ++h) {
+        const uint32_t col = C::COL_S0 + h * C::COL_HALF;
+        ok = __all_sync(kFullMask, bounded_wait(bDQfull + 8 * h, it & 1, w));
+        if (!ok) break;
+        tc_fence_after();
+        uint32_t v[64];
+        if (r < dio) {   // whole warps (dio is a multiple of 32)
+          uint32_t (&v0)[32] = *reinterpret_cast<uint32_t (*)[32]>(v);
+          uint32_t (&v1)[32] = *reinterpret_cast<uint32_t (*)[32]>(v + 32);
+          tmem_ld32(tmem + lane_off + col + C::DP_OFF, v0);
+          tmem_ld32(tmem + lane_off + col + C::DP_OFF + 32, v1);
+          tmem_ld_wait();
+          reg_fence32(v0);
+          reg_fence32(v1);
+        }
+        tc_fence_before();
+        mbar_arrive(bDQfree + 8 * h);
+        if (r < dio) {
+          const int qbase = qt * BM + h * C::HQ;
+          float *dst = p.dq_acc + acc_base + static_cast<size_t>(qbase) * D + r;
+#pragma unroll
+          for (int i = 0; i < 64; ++i)
+            if (qbase + i < Nq) red_add(dst + i * D, __uint_as_float(v[i]));
+        }
+      }
     }
     __syncwarp();
   } else {
+    setmaxnreg_inc<C::REG_SOFTMAX>();
     // ------------------------------------------------------------ softmax warps
     w.role = kStatusSoftmax;
     const int g = warp >> 2;                  // query quarter within a half
@@ -403,31 +492,6 @@ __global__ void __launch_bounds__(320, 1)
         tc_fence_before();
         mbar_arrive(bPfull + 8 * h);
       }
-      if (!ok) break;
-
-      // dQ_h^T -> dq_acc with fp32 atomic adds: lane r = head-dim index,
-      // this quarter's 32 queries of the half; the warp's 32 lanes add to 32
-      // consecutive floats of one dQ row.  (D = 64: lanes 64-127 hold no dQ.)
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const uint32_t col = C::COL_S0 + h * C::COL_HALF;
-        ok = __all_sync(kFullMask, bounded_wait(bDQfull + 8 * h, it & 1, w));
-        if (!ok) break;
-        tc_fence_after();
-        if (r < dio) {   // whole warps (dio is a multiple of 32)
-          uint32_t v[32];
-          tmem_ld32(tmem + lane_off + col + C::DP_OFF + cq, v);
-          tmem_ld_wait();
-          reg_fence32(v);
-          const int qbase = qt * BM + h * C::HQ + cq;
-          float *dst = p.dq_acc + acc_base + static_cast<size_t>(qbase) * D + r;
-#pragma unroll
-          for (int i = 0; i < 32; ++i)
-            if (qbase + i < Nq) red_add(dst + i * D, __uint_as_float(v[i]));
-        }
-        tc_fence_before();
-        mbar_arrive(bDQfree + 8 * h);
-      }
     }
 
     // ---------------------------------------------------------- dV, dK out
@@ -474,7 +538,7 @@ __global__ void __launch_bounds__(320, 1)
   // ------------------------------------------------------------ teardown
   tc_fence_before();
   __syncthreads();
-  if (warp == 9) {
+  if (warp == C::WARP_MMA) {
     tc_fence_after();
     tmem_dealloc(tmem, C::TMEM_COLS);
   }

@@ -210,6 +210,18 @@ __host__ __device__ constexpr uint32_t make_idesc(uint32_t ab_fmt, uint32_t M, u
          ((N >> 3) << 17) | ((M >> 4) << 24);
 }
 
+// Register reallocation between warpgroups (every thread of a warpgroup
+// executes the same one): give back down to N registers a thread, or wait
+// for the pool to grant up to N.
+template <uint32_t N>
+__device__ __forceinline__ void setmaxnreg_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <uint32_t N>
+__device__ __forceinline__ void setmaxnreg_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+
 // 32 lanes x 32 columns of 32-bit words: thread t of the warp receives its
 // lane's 32 consecutive columns starting at taddr.
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
