@@ -368,20 +368,22 @@ def main():
         if st != fa.FA_OK:
             raise fa.FaError(st, "fa_fwd")
 
+    # The clock sampler starts before the warm-up, so that no idle gap (in
+    # which the GPU would clock down) separates the warm-up from the timed
+    # steps.
+    sampler = ClockSampler(dev.index) if rank == 0 or ws > 1 else None
+    if sampler:
+        sampler.start()
+        time.sleep(0.3)
     torch.cuda.synchronize(dev)
     for _ in range(args.warmup):
         step()
     st, word = fa.fa_fwd_status(sh)
     if st != fa.FA_OK:
         raise RuntimeError(f"warm-up device status {word}")
-
-    sampler = ClockSampler(dev.index) if rank == 0 or ws > 1 else None
     if ws > 1:
         dist.barrier()
     torch.cuda.synchronize(dev)
-    if sampler:
-        sampler.start()
-        time.sleep(0.3)
     ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
     with torch.cuda.stream(stream):
         ev[0].record(stream)

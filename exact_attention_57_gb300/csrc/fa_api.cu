@@ -147,7 +147,9 @@ int sm_count();
 // nbar = mean key tiles per query tile; c and c1 = fixed cost per CTA with
 // and without a following tile to hide the epilogue.  Fitted on GB300 at
 // d = 128 (t = 0.77 us, c = 2.0 us, c1 = 3.0 us); a tile's time scales with
-// the head dim, the fixed cost does not.  The fp32 path keeps one.
+// the head dim, the fixed cost does not.  A G that leaves fewer CTAs than
+// SMs is not taken (b2h8n3001d128: 96 CTAs of four tiles ran 6% slower than
+// 384 of one, where the model has them equal).  The fp32 path keeps one.
 int items_per_cta(int dtype, int d, int causal, long long planes, int n_qtiles, int n_ktiles) {
   if (dtype != FA_DTYPE_BF16 && dtype != FA_DTYPE_F16) return 1;
   const int forced = g_force_items.load();
@@ -166,6 +168,7 @@ int items_per_cta(int dtype, int d, int causal, long long planes, int n_qtiles, 
   int pick = 1;
   for (int g = 2; g <= fa::kMaxItemsPerCta; g *= 2) {
     const double ctas = std::ceil(qtiles / g);
+    if (ctas < sms) break;
     const double cost = std::ceil(ctas / sms) * (g * nbar + c);
     if (cost < best) {
       best = cost;

@@ -186,7 +186,9 @@ __global__ void __launch_bounds__(224, 1)
   // G*x .. G*x+G-1 of the zigzag order heaviest, lightest, 2nd heaviest, ...,
   // so with an even G every CTA has the same causal work, and an item's loads
   // and first products overlap the previous item's epilogue.
-  const int G = tc_items(p);
+  // (The fp32 path always runs one item: a constant, so its kernels carry
+  // none of the multi-item code and keep their registers.)
+  const int G = TF32 ? 1 : tc_items(p);
   auto item_qt = [&](int g) -> int {  // query tile of item g, or -1
     if (G == 1) return g == 0 ? (CAUSAL ? (n_qtiles - 1 - qidx) : qidx) : -1;
     const int zi = G * static_cast<int>(blockIdx.x) + g;
@@ -902,8 +904,10 @@ __global__ void __launch_bounds__(224, 1)
       tma_store_wait_read_all();
     }
     // The four warps have all passed the named barrier above, so they read
-    // the same abort flag and leave the item loop together.
-    if (*abort_flag) break;
+    // the same abort flag and leave the item loop together.  (Only with
+    // several items: with one the check is moot, and as a loop exit it cost
+    // the fp32 kernels their last free registers.)
+    if (G > 1 && *abort_flag) break;
     }  // items
   }
 
