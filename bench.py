@@ -402,6 +402,12 @@ def main():
     total_ms = max_over_ranks(ev[0].elapsed_time(ev[-1]), dev)
     ms_per_step = total_ms / args.steps
     flops_step = varlen["flops"] if varlen is not None else w.flops(causal) * (2.5 if bwd else 1.0)
+    # query tiles per CTA of the timed forward (fa_fwd's own choice; the
+    # other entry points run one)
+    plain_fwd = not bwd and varlen is None and stage_ws is None and wspace is None
+    tiles_per_cta = (fa.fa_items_per_cta(w.B, w.H, w.Nq, w.Nk, w.d, causal, w.dtype,
+                                         torch.cuda.get_device_properties(dev).multi_processor_count)
+                     if plain_fwd else 1)
     value = ws * flops_step * args.steps / (total_ms / 1e3) / 1e12
 
     # End to end through the host-buffer entry point: H2D of q, k, v from
@@ -482,6 +488,7 @@ def main():
                    "causal": causal, "flops_per_step": flops_step,
                    "parallelism": f"replicas{ws}" if ws > 1 else "single",
                    "key_splits": args.splits, "pass": args.which,
+                   "tiles_per_cta": tiles_per_cta,
                    "staged": stage_ws is not None,
                    "varlen": (None if varlen is None else
                               {"sequences": len(varlen["lens"]), "total_tokens": varlen["total"],

@@ -150,11 +150,11 @@ int sm_count();
 // the head dim, the fixed cost does not.  A G that leaves fewer CTAs than
 // SMs is not taken (b2h8n3001d128: 96 CTAs of four tiles ran 6% slower than
 // 384 of one, where the model has them equal).  The fp32 path keeps one.
-int items_per_cta(int dtype, int d, int causal, long long planes, int n_qtiles, int n_ktiles) {
+int items_model(int dtype, int d, int causal, long long planes, int n_qtiles, int n_ktiles,
+                int num_sms) {
   if (dtype != FA_DTYPE_BF16 && dtype != FA_DTYPE_F16) return 1;
-  const int forced = g_force_items.load();
-  if (forced > 0) return forced < fa::kMaxItemsPerCta ? forced : fa::kMaxItemsPerCta;
-  const double sms = sm_count() > 0 ? sm_count() : 1;
+  if (n_qtiles < 1 || n_ktiles < 1 || planes < 1) return 1;
+  const double sms = num_sms > 0 ? num_sms : 1;
   // key tiles summed over the query tiles of one (batch, head)
   const double nq = n_qtiles, nk = n_ktiles;
   const double ksum = !causal ? nq * nk
@@ -166,8 +166,9 @@ int items_per_cta(int dtype, int d, int causal, long long planes, int n_qtiles, 
   double best = causal ? qtiles * (nbar + c1) / sms + nbar
                        : std::ceil(qtiles / sms) * (nbar + c1);
   int pick = 1;
-  for (int g = 2; g <= fa::kMaxItemsPerCta; g *= 2) {
-    const double ctas = std::ceil(qtiles / g);
+  // (a CTA's tiles come from one head: no more than it has)
+  for (int g = 2; g <= fa::kMaxItemsPerCta && g <= n_qtiles; g *= 2) {
+    const double ctas = static_cast<double>(planes) * std::ceil(nq / g);
     if (ctas < sms) break;
     const double cost = std::ceil(ctas / sms) * (g * nbar + c);
     if (cost < best) {
@@ -176,6 +177,13 @@ int items_per_cta(int dtype, int d, int causal, long long planes, int n_qtiles, 
     }
   }
   return pick;
+}
+
+int items_per_cta(int dtype, int d, int causal, long long planes, int n_qtiles, int n_ktiles) {
+  if (dtype != FA_DTYPE_BF16 && dtype != FA_DTYPE_F16) return 1;
+  const int forced = g_force_items.load();
+  if (forced > 0) return forced < fa::kMaxItemsPerCta ? forced : fa::kMaxItemsPerCta;
+  return items_model(dtype, d, causal, planes, n_qtiles, n_ktiles, sm_count());
 }
 
 // The tensor-core forward instantiation for (dtype, d); the combination has
@@ -338,6 +346,12 @@ int fa_set_test_hooks(int skip_v_load, unsigned long long wait_limit_ns) {
   g_skip_v_load.store(skip_v_load ? 1 : 0);
   g_wait_limit_ns.store(wait_limit_ns);
   return FA_OK;
+}
+
+int fa_items_per_cta(int B, int H, int Nq, int Nk, int d, int causal, int dtype, int num_sms) {
+  if (B < 1 || H < 1 || Nq < 1 || Nk < 1 || d < 1 || num_sms < 1) return 0;
+  return items_model(dtype, d, causal != 0, static_cast<long long>(B) * H, ceil_div(Nq, fa::BM),
+                     ceil_div(Nk, fa::BN), num_sms);
 }
 
 int fa_set_items_per_cta(int n) {

@@ -30,7 +30,7 @@ FA_DTYPE_F32_SIMT = 2
 FA_DTYPE_F16 = 3
 
 EXPORTED = ("fa_fwd", "fa_fwd_host", "fa_fwd_status", "fa_status_string", "fa_version",
-            "fa_set_test_hooks", "fa_set_items_per_cta", "fa_fwd_noalloc", "fa_fwd_splitkv", "fa_fwd_splitkv_workspace",
+            "fa_set_test_hooks", "fa_set_items_per_cta", "fa_items_per_cta", "fa_fwd_noalloc", "fa_fwd_splitkv", "fa_fwd_splitkv_workspace",
             "fa_fwd_varlen", "fa_bwd", "fa_bwd_workspace", "fa_fwd_staged",
             "fa_fwd_staged_workspace", "fa_bwd_varlen", "fa_bwd_varlen_workspace")
 
@@ -93,6 +93,8 @@ def load(path: str | None = None):
     lib.fa_set_test_hooks.restype = i
     lib.fa_set_items_per_cta.argtypes = [i]
     lib.fa_set_items_per_cta.restype = i
+    lib.fa_items_per_cta.argtypes = [i] * 8
+    lib.fa_items_per_cta.restype = i
     if path is None:
         _lib = lib
     return lib
@@ -298,6 +300,13 @@ def fa_set_test_hooks(skip_v_load: int = 0, wait_limit_ns: int = 0) -> int:
 def fa_set_items_per_cta(n: int = 0) -> int:
     """Testing aid: query tiles per CTA of the 16-bit forward (0 = automatic)."""
     return load().fa_set_items_per_cta(int(n))
+
+
+def fa_items_per_cta(B: int, H: int, Nq: int, Nk: int, d: int, causal: bool, dtype: int,
+                     num_sms: int) -> int:
+    """The automatic query tiles per CTA of fa_fwd on a GPU with num_sms SMs."""
+    return load().fa_items_per_cta(int(B), int(H), int(Nq), int(Nk), int(d), int(bool(causal)),
+                                   int(dtype), int(num_sms))
 
 
 # --------------------------------------------------------------- torch helpers

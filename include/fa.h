@@ -343,6 +343,14 @@ int fa_set_test_hooks(int skip_v_load, unsigned long long wait_limit_ns);
  */
 int fa_set_items_per_cta(int n);
 
+/*
+ * fa_items_per_cta — the query tiles per CTA fa_fwd would run for this
+ * problem on a GPU with num_sms SMs when nothing is forced (1, 2 or 4; 1 for
+ * types other than bf16/fp16); a host-only function, for reports and tests.
+ * 0 for arguments below 1.
+ */
+int fa_items_per_cta(int B, int H, int Nq, int Nk, int d, int causal, int dtype, int num_sms);
+
 #ifdef __cplusplus
 }
 #endif

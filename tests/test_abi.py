@@ -153,6 +153,34 @@ def test_varlen_refuses_simt_and_unsupported_dims(lib):
 DO, DQ, DK, DV, WS = 0x800000, 0x900000, 0xA00000, 0xB00000, 0xC00000
 
 
+@pytest.mark.parametrize("shape,causal,dtype,want", [
+    # measured on GB300 (152 SMs): four tiles per CTA wherever the grid keeps
+    # several full waves, two on b2h16, one where fewer CTAs than SMs remain
+    ((8, 32, 8192, 8192, 128), True, fa.FA_DTYPE_BF16, 4),
+    ((4, 16, 8192, 8192, 128), True, fa.FA_DTYPE_BF16, 4),
+    ((2, 16, 8192, 8192, 128), True, fa.FA_DTYPE_BF16, 2),
+    ((3, 16, 8192, 8192, 128), True, fa.FA_DTYPE_BF16, 2),
+    ((4, 16, 8192, 8192, 64), False, fa.FA_DTYPE_F16, 4),
+    ((2, 8, 3001, 3001, 128), True, fa.FA_DTYPE_BF16, 1),
+    ((2, 4, 1024, 1024, 64), True, fa.FA_DTYPE_BF16, 1),
+    ((4, 4, 4096, 4096, 64), False, fa.FA_DTYPE_F32, 1),
+    ((4, 4, 4096, 4096, 64), False, fa.FA_DTYPE_F32_SIMT, 1),
+])
+def test_items_per_cta_choice(lib, shape, causal, dtype, want):
+    """The makespan model behind fa_fwd's tiles per CTA (host logic only)."""
+    B, H, Nq, Nk, d = shape
+    assert fa.fa_items_per_cta(B, H, Nq, Nk, d, causal, dtype, 152) == want
+
+
+def test_items_per_cta_choice_edges(lib):
+    assert fa.fa_items_per_cta(0, 1, 128, 128, 64, 0, fa.FA_DTYPE_BF16, 152) == 0
+    assert fa.fa_items_per_cta(1, 1, 128, 128, 64, 0, fa.FA_DTYPE_BF16, 0) == 0
+    # one SM: any count keeps the SM busy; a single tile per head stays 1
+    assert fa.fa_items_per_cta(1, 1, 128, 128, 64, 1, fa.FA_DTYPE_BF16, 1) == 1
+    for sms in (1, 2, 152, 1000):
+        assert fa.fa_items_per_cta(8, 32, 8192, 8192, 128, 1, fa.FA_DTYPE_BF16, sms) in (1, 2, 4)
+
+
 def test_items_per_cta_hook_range(lib):
     """The testing aid takes 0 (automatic) .. 4 and refuses anything else."""
     for n in (-1, 5, 100):
