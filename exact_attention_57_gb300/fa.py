@@ -30,7 +30,8 @@ FA_DTYPE_F32_SIMT = 2
 FA_DTYPE_F16 = 3
 
 EXPORTED = ("fa_fwd", "fa_fwd_host", "fa_fwd_status", "fa_status_string", "fa_version",
-            "fa_set_test_hooks", "fa_set_items_per_cta", "fa_items_per_cta", "fa_fwd_noalloc", "fa_fwd_splitkv", "fa_fwd_splitkv_workspace",
+            "fa_set_test_hooks", "fa_set_items_per_cta", "fa_items_per_cta", "fa_fwd_noalloc",
+            "fa_fwd_splitkv", "fa_fwd_splitkv_workspace",
             "fa_fwd_varlen", "fa_bwd", "fa_bwd_workspace", "fa_fwd_staged",
             "fa_fwd_staged_workspace", "fa_bwd_varlen", "fa_bwd_varlen_workspace")
 

@@ -295,9 +295,16 @@ unsigned long long fa_bwd_varlen_workspace(int B, int H, int total_q, int max_se
  * o_h, lse_h      host outputs.
  * q_d .. lse_d    caller-owned device buffers of the same sizes, used as the
  *                 staging area; same alignment rules as fa_fwd.
- * The call copies the inputs host->device on `stream`, runs fa_fwd, copies o
- * and lse device->host, and synchronises `stream` before returning, so the
- * host outputs are ready on return.  Returns the first failing status.
+ * The call splits the B*H planes into chunks (one per 64 MB of input, at
+ * most eight) and pipelines them:
+ * a chunk's inputs are copied host->device on an internal stream, its
+ * forward runs on `stream` once they have landed, and its o, lse are copied
+ * device->host on a second internal stream, so copies in, kernels and copies
+ * out of different chunks overlap.  The internal streams and events are
+ * created on first use per device and kept; concurrent calls on one device
+ * are serialised.  Work already on `stream` completes before the inputs are
+ * overwritten, and every enqueued step has finished when the call returns,
+ * so the host outputs are ready on return.  Returns the first failing status.
  */
 int fa_fwd_host(const void *q_h, const void *k_h, const void *v_h,
                 void *o_h, float *lse_h,
