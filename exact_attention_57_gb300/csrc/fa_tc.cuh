@@ -5,22 +5,24 @@
 // online softmax with a running row max m and row sum l, the partial output
 // rescaled by exp(m_old - m_new), and at the end O = O / l, L = m + log(l).
 // Loop order: the swapped one from "parallel execution of read/write
-// operations (paper vs implementation)" (one query tile per CTA, keys inner,
-// O kept on chip and written once).  Parallelism: over queries as well as
+// operations (paper vs implementation)" (query tiles outer, keys inner, O kept
+// on chip and written once).  Parallelism: over queries as well as
 // batch and heads, as in "Meta's xFormers has Attention kernel written in
 // CUTLASS".  exp2 with log2(e) folded into the scale, as in "Add Fused
 // Multi-Head Attention example" (cuTile.jl).
 //
-// GB300 design (one CTA = one (batch, head, 128-row query tile)):
+// GB300 design (one CTA = one (batch, head) and one to four 128-row query
+// tiles, "items", run through one pipeline; see tc_items and item_qt):
 //   warps 0-3    softmax, correction and epilogue: one query row per thread
 //                (= one TMEM lane).  Where Q lives in tensor memory, first copy
 //                the thread's Q row there from global memory (the A operand of
 //                S = Q K^T).  Per key tile: load the
 //                row's 128 scores, mask the causal diagonal / ragged key tail,
-//                update m and l, write P back over S in TMEM.  A fixed share
-//                of the exponentials runs as a polynomial on the FMA pipes to
-//                relieve the MUFU unit.  At the end normalise O, stage it
-//                swizzled in shared memory for a TMA store, and write LSE.
+//                update m and l, write P back over S in TMEM.  (A polynomial
+//                exp2 on the FMA pipes is built in for a share of the
+//                exponentials; measured, that share is best at 0.)  At the
+//                end of an item normalise O, stage it swizzled in shared
+//                memory for a TMA store, and write LSE.
 //   warp 4       TMA producer: Q (when in shared memory), then K_j / V_j
 //                through shared-memory rings (full/empty mbarriers), L2
 //                evict-last for K/V.
