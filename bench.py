@@ -56,14 +56,44 @@ KERNEL_SOURCES = {
 COMMON_SOURCES = ["ptx.cuh", "fa_wait.cuh", "fa_internal.h", "fa_api.cu"]
 
 
-def kernel_source_hash(kernel: str) -> str:
-    """Hash of the sources of the kernel family named by the key's prefix."""
+def code_only(text: str) -> str:
+    """C/C++ source without its comments and with whitespace runs collapsed
+    (string literals kept as they are): an edit of comments or layout leaves
+    the code, and so the validity of a profile taken on it, unchanged."""
+    out, i, n = [], 0, len(text)
+    while i < n:
+        if text.startswith("//", i):
+            j = text.find("\n", i)
+            i = n if j < 0 else j
+        elif text.startswith("/*", i):
+            j = text.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+            out.append(" ")
+        elif text[i] == '"':
+            j = i + 1
+            while j < n and text[j] != '"':
+                j += 2 if text[j] == "\\" else 1
+            out.append(text[i:j + 1])
+            i = j + 1
+        else:
+            out.append(text[i])
+            i += 1
+    return " ".join("".join(out).split())
+
+
+def kernel_source_hash(kernel: str, read=None) -> str:
+    """Hash of the code (comments and layout aside) of the sources of the
+    kernel family named by the key's prefix; read(name) gives a source's
+    text (default: the working tree)."""
     fam = next(f for f in KERNEL_SOURCES if kernel.startswith(f))
+    if read is None:
+        def read(name):
+            with open(os.path.join(ROOT, "exact_attention_57_gb300", "csrc", name)) as f:
+                return f.read()
     h = hashlib.sha256()
     for name in sorted(KERNEL_SOURCES[fam] + COMMON_SOURCES):
-        with open(os.path.join(ROOT, "exact_attention_57_gb300", "csrc", name), "rb") as f:
-            h.update(name.encode())
-            h.update(f.read())
+        h.update(name.encode())
+        h.update(code_only(read(name)).encode())
     return h.hexdigest()[:16]
 
 
