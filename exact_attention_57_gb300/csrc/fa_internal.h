@@ -8,8 +8,8 @@
 
 namespace fa {
 
-// Tile shape of the tensor-core kernels: one CTA owns BM query rows of one
-// (batch, head) and streams the keys in tiles of BN.
+// Tile shape of the tensor-core kernels: a query tile is BM rows of one
+// (batch, head); the keys stream in tiles of BN.
 constexpr int BM = 128;
 constexpr int BN = 128;
 
@@ -55,9 +55,9 @@ struct TcParams {
   // fp32 path: K already rounded to tf32 and tm_v a map over a tf32 V^T
   // ([B*H][d][Nk padded to 128], boxes of 32 keys x D rows).
   int kv_staged = 0;
-  // Query tiles per CTA (plain problems, 16-bit types): 1, or an even number
-  // taken from the zigzag heaviest/lightest order (the grid then has
-  // ceil(n_qtiles / items) CTAs per head, items = tc_items(*this)).
+  // Query tiles per CTA (plain problems, 16-bit types): 1 to
+  // kMaxItemsPerCta, taken from the zigzag heaviest/lightest order (the grid
+  // then has ceil(n_qtiles / items) CTAs per head, items = tc_items(*this)).
   int items_per_cta = 1;
 };
 

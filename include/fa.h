@@ -267,8 +267,8 @@ unsigned long long fa_bwd_workspace(int B, int H, int Nq, int d);
  * packed end to end (the layout of fa_fwd_varlen): q, o, dout, dq
  * [total_q, H, d]; k, v, dk, dv [total_k, H, d]; lse [H, total_q] from
  * fa_fwd_varlen; cu_seqlens_q/k device int32 offsets (B+1 each, nondecreasing,
- * from 0 to total_q / total_k, covering every token: rows outside every
- * sequence get no dq).  Causal masking is top-left within each sequence;
+ * from 0 to total_q / total_k, covering every token: dq of rows outside
+ * every sequence is unspecified).  Causal masking is top-left within each sequence;
  * keys that no query sees get zero dk, dv.  max_seqlen_q, max_seqlen_k: the
  * longest query and key lengths (1 .. total).  dtype, d, scale, causal as for
  * fa_bwd.  workspace: at least fa_bwd_varlen_workspace(B, H, total_q,
