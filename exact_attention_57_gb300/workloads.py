@@ -105,6 +105,12 @@ PROFILE_WORKLOADS = {
     "b4h16n8192d64-bf16-causal": Workload(
         "b4h16n8192d64-bf16-causal", 4, 16, 8192, 8192, 64, DTYPE_BF16,
         causal=(True,), seed=57008, note="head dim 64"),
+    "b4h16n8192d128-bf16": Workload(
+        "b4h16n8192d128-bf16", 4, 16, 8192, 8192, 128, DTYPE_BF16,
+        causal=(False,), seed=57011, note="no mask"),
+    "b4h16n8192d128-f16-causal": Workload(
+        "b4h16n8192d128-f16-causal", 4, 16, 8192, 8192, 128, DTYPE_F16,
+        causal=(True,), seed=57012, note="fp16 inputs"),
 }
 
 
