@@ -337,7 +337,7 @@ int fa_fwd_host(const void *q_h, const void *k_h, const void *v_h, void *o_h, fl
   const size_t es = elem_size(dtype);
   const size_t q_plane = static_cast<size_t>(Nq) * d * es, k_plane = static_cast<size_t>(Nk) * d * es;
   const size_t l_plane = static_cast<size_t>(Nq) * sizeof(float);
-  const int planes = B * H;
+  const long long planes = static_cast<long long>(B) * H;
   // One chunk per 64 MB copied in (up to eight): small problems run as one
   // (there the launches and events of several would outweigh the overlap;
   // b2h4n1024d64 went from 19 to 8 TFLOP/s with eight).
@@ -345,7 +345,10 @@ int fa_fwd_host(const void *q_h, const void *k_h, const void *v_h, void *o_h, fl
   size_t want = in_bytes / (size_t{64} << 20);
   if (want < 1) want = 1;
   if (want > static_cast<size_t>(kHostChunks)) want = kHostChunks;
-  const int nch = planes < static_cast<int>(want) ? planes : static_cast<int>(want);
+  int nch = planes < static_cast<long long>(want) ? static_cast<int>(planes) : static_cast<int>(want);
+  // A chunk runs as a problem of its planes with one head each, and the grid
+  // takes at most 65535 of them: beyond that the whole problem runs as one.
+  if ((planes + nch - 1) / nch > 65535) nch = 1;
   // the inputs must not be overwritten while an earlier call's work on
   // `stream` may still read them
   if (cudaEventRecord(hp->done[0], s) != cudaSuccess ||
@@ -356,9 +359,8 @@ int fa_fwd_host(const void *q_h, const void *k_h, const void *v_h, void *o_h, fl
   };
   int first_rc = FA_OK;
   for (int c = 0; c < nch && first_rc == FA_OK; ++c) {
-    const int p0 = static_cast<int>(static_cast<long long>(planes) * c / nch);
-    const int p1 = static_cast<int>(static_cast<long long>(planes) * (c + 1) / nch);
-    const int np = p1 - p0;
+    const long long p0 = planes * c / nch, p1 = planes * (c + 1) / nch;
+    const long long np = p1 - p0;
     if (np == 0) continue;
     if (cudaMemcpyAsync(ptr(q_d, p0 * q_plane), ptr(q_h, p0 * q_plane), np * q_plane,
                         cudaMemcpyHostToDevice, hp->in) != cudaSuccess ||
@@ -371,10 +373,12 @@ int fa_fwd_host(const void *q_h, const void *k_h, const void *v_h, void *o_h, fl
       first_rc = FA_ERR_CUDA;
       break;
     }
-    // the chunk as a problem of np planes of one head each
+    // the chunk as a problem of np planes of one head each (one chunk: the
+    // problem as given)
+    const int cb = nch == 1 ? B : static_cast<int>(np), ch = nch == 1 ? H : 1;
     const int rc_c = fa_fwd(ptr(q_d, p0 * q_plane), ptr(k_d, p0 * k_plane),
                             ptr(v_d, p0 * k_plane), ptr(o_d, p0 * q_plane),
-                            static_cast<float *>(ptr(lse_d, p0 * l_plane)), np, 1, Nq, Nk, d,
+                            static_cast<float *>(ptr(lse_d, p0 * l_plane)), cb, ch, Nq, Nk, d,
                             scale, causal, dtype, stream);
     if (rc_c != FA_OK) {
       first_rc = rc_c;
