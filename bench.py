@@ -106,17 +106,19 @@ def measured_peaks():
 
 
 def profiled_traffic(kernel: str, workload: str):
-    """DRAM bytes per launch from the committed ncu summary, if it was taken on
-    the current kernel sources; else None."""
+    """(DRAM bytes per launch, note) from the committed ncu summary, if it was
+    taken on the current kernel sources; else (None, None).  The note says
+    how to read the figure (e.g. a lower bound when the capture's writes
+    stayed in L2)."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(path):
-        return None
+        return None, None
     with open(path) as f:
         rec = json.load(f)
     ent = rec.get(kernel, {}).get(workload)
     if not ent or ent.get("source_hash") != kernel_source_hash(kernel):
-        return None
-    return ent.get("dram_bytes_per_launch")
+        return None, None
+    return ent.get("dram_bytes_per_launch"), ent.get("note")
 
 
 class ClockSampler:
@@ -482,9 +484,10 @@ def main():
     achieved = flops_step / (avg_launch_ms / 1e3) / 1e12
     half_io = w.dtype in (0, 3)   # bf16 / fp16: the same kind::f16 tensor rate
     simt = w.dtype == 2
-    # SIMT: no tensor cores; the FP32 FMA rate is 152 SMs x 128 lanes x 2
-    # FLOP per cycle at the maximum SM clock.
-    fma_peak = 152 * 128 * 2 * float(peaks.get("sm_max_mhz", 2070.0)) * 1e6 / 1e12
+    # SIMT: no tensor cores; the FP32 FMA rate is SMs x 128 lanes x 2 FLOP
+    # per cycle at the maximum SM clock.
+    n_sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    fma_peak = n_sms * 128 * 2 * float(peaks.get("sm_max_mhz", 2070.0)) * 1e6 / 1e12
     peak = (float(peaks["bf16_tflops"]) if half_io else
             fma_peak if simt else float(peaks["bf16_tflops"]) / 2.0)
     kname = {0: "fa_tc_fwd_kernel<bf16>", 1: "fa_tc_fwd_kernel<tf32>",
@@ -494,13 +497,15 @@ def main():
         # timed together, so `achieved` is a lower bound for the gradient
         # kernel alone; `traffic` is the gradient kernel's.
         kname = {0: "fa_bwd_kernel<bf16>", 3: "fa_bwd_kernel<f16>"}[w.dtype]
-    traffic = profiled_traffic(kname, w.name)
+    traffic, traffic_note = profiled_traffic(kname, w.name)
     roofline = {"bound": "alu" if simt else "tensor", "achieved": achieved, "peak": peak,
                 "unit": "TFLOP/s", "frac": achieved / peak, "traffic": traffic,
                 "peak_source": (f"{peak_src} bf16 burst" if half_io else
-                                "FP32 FMA: 152 SMs x 128 lanes x 2 x max SM clock" if simt else
+                                f"FP32 FMA: {n_sms} SMs x 128 lanes x 2 x max SM clock" if simt else
                                 f"{peak_src} bf16 burst / 2 (tf32 nominal ratio)"),
                 "kernel": kname}
+    if traffic_note:
+        roofline["traffic_note"] = traffic_note
 
     cpu = None
     if not args.no_cpu_baseline:

@@ -40,6 +40,8 @@ int validate(const void *q, const void *k, const void *v, const void *o, const f
   if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
   if (B < 1 || H < 1 || Nq < 1 || Nk < 1 || d < 1) return FA_ERR_INVALID_ARG;
   if (B > 65535 || H > 65535) return FA_ERR_INVALID_ARG;
+  // The kernels index (batch, head) planes with 32-bit ints (b * H + h).
+  if (static_cast<long long>(B) * H > 2147483647LL) return FA_ERR_INVALID_ARG;
   if (!std::isfinite(scale)) return FA_ERR_INVALID_ARG;
   if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
   if (dtype != FA_DTYPE_BF16 && dtype != FA_DTYPE_F32 && dtype != FA_DTYPE_F32_SIMT &&
@@ -69,13 +71,9 @@ int validate(const void *q, const void *k, const void *v, const void *o, const f
   return FA_OK;
 }
 
-// The current device must be sm_103 (the only code compiled in); also makes
-// sure its status word exists.  Returns FA_OK and the status pointer.
-int device_setup(unsigned **status) {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return FA_ERR_CUDA;
-  if (dev < 0 || dev >= kMaxDevices) return FA_ERR_UNSUPPORTED;
-  std::lock_guard<std::mutex> lock(g_mu);
+// FA_OK when device `dev` is an sm_103 (the only code compiled in), else
+// FA_ERR_UNSUPPORTED; the answer is cached per device.  Called with g_mu held.
+int check_sm103(int dev) {
   if (g_dev_ok[dev] == 0) {
     int major = 0, minor = 0;
     if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
@@ -83,7 +81,17 @@ int device_setup(unsigned **status) {
       return FA_ERR_CUDA;
     g_dev_ok[dev] = (major == 10 && minor == 3) ? 1 : -1;
   }
-  if (g_dev_ok[dev] != 1) return FA_ERR_UNSUPPORTED;
+  return g_dev_ok[dev] == 1 ? FA_OK : FA_ERR_UNSUPPORTED;
+}
+
+// The current device must be sm_103; also makes sure its status word exists.
+// Returns FA_OK and the status pointer.
+int device_setup(unsigned **status) {
+  int rc, dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return FA_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return FA_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_mu);
+  if ((rc = check_sm103(dev)) != FA_OK) return rc;
   if (g_status[dev] == nullptr) {
     unsigned *ptr = nullptr;
     if (cudaMalloc(&ptr, 256) != cudaSuccess) return FA_ERR_CUDA;
@@ -224,18 +232,13 @@ void set_tc_scale(float scale, fa::TcParams *p) {
   p->scale_neg = scale < 0.f ? 1 : 0;
 }
 
-}  // namespace
-
-extern "C" {
-
-int fa_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H,
-           int Nq, int Nk, int d, float scale, int causal, int dtype, void *stream) {
-  int rc = validate(q, k, v, o, lse, B, H, Nq, Nk, d, scale, causal, dtype);
-  if (rc != FA_OK) return rc;
-  unsigned *status = nullptr;
-  if ((rc = device_setup(&status)) != FA_OK) return rc;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-
+// The forward on device buffers once the arguments are validated: the SIMT
+// kernel or the tensor-core kernel for (dtype, d), reporting bounded-wait
+// give-ups into `status`.  Shared by fa_fwd and fa_fwd_noalloc, which differ
+// only in where that word lives.
+int fwd_enqueue(unsigned *status, const void *q, const void *k, const void *v, void *o,
+                float *lse, int B, int H, int Nq, int Nk, int d, float scale, int causal,
+                int dtype, cudaStream_t s) {
   if (dtype == FA_DTYPE_F32_SIMT) {
     fa::SimtParams p;
     p.q = static_cast<const float *>(q);
@@ -254,9 +257,10 @@ int fa_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int
     return fa::launch_simt(p, B, s) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
   }
 
+  int rc;
   if ((rc = get_encoder()) != FA_OK) return rc;
   CUtensorMap mq, mk, mv, mo;
-  const int BH = B * H;
+  const int BH = B * H;  // <= 2^31 - 1 (validate)
   if ((rc = encode_map(&mq, q, dtype, BH, Nq, d)) != FA_OK) return rc;
   if ((rc = encode_map(&mk, k, dtype, BH, Nk, d)) != FA_OK) return rc;
   if ((rc = encode_map(&mv, v, dtype, BH, Nk, d)) != FA_OK) return rc;
@@ -284,6 +288,20 @@ int fa_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int
 
   cudaError_t e = launch_tc_any(mq, mk, mv, mo, p, B, causal, d, dtype, s);
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+int fa_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H,
+           int Nq, int Nk, int d, float scale, int causal, int dtype, void *stream) {
+  int rc = validate(q, k, v, o, lse, B, H, Nq, Nk, d, scale, causal, dtype);
+  if (rc != FA_OK) return rc;
+  unsigned *status = nullptr;
+  if ((rc = device_setup(&status)) != FA_OK) return rc;
+  return fwd_enqueue(status, q, k, v, o, lse, B, H, Nq, Nk, d, scale, causal, dtype,
+                     static_cast<cudaStream_t>(stream));
 }
 
 // fa_fwd_host's pipeline: per device, a stream for host->device copies, one
@@ -483,18 +501,11 @@ unsigned *g_noalloc_status[kMaxDevices] = {};  // device address of word 0, per 
 // sm_103 check and the scratch's device address for the current device; the
 // address is looked up once per device, with that device current.
 int noalloc_setup(unsigned **status) {
-  int dev = 0;
+  int rc, dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return FA_ERR_CUDA;
   if (dev < 0 || dev >= kMaxDevices) return FA_ERR_UNSUPPORTED;
   std::lock_guard<std::mutex> lock(g_mu);
-  if (g_dev_ok[dev] == 0) {
-    int major = 0, minor = 0;
-    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
-      return FA_ERR_CUDA;
-    g_dev_ok[dev] = (major == 10 && minor == 3) ? 1 : -1;
-  }
-  if (g_dev_ok[dev] != 1) return FA_ERR_UNSUPPORTED;
+  if ((rc = check_sm103(dev)) != FA_OK) return rc;
   if (g_noalloc_status[dev] == nullptr) {
     void *ptr = nullptr;
     if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || ptr == nullptr)
@@ -522,53 +533,9 @@ extern "C" int fa_fwd_noalloc(const void *q, const void *k, const void *v, void 
   // The array keeps the previous call's contents: the status word must start
   // at zero for this call.
   if (cudaMemsetAsync(status, 0, need, s) != cudaSuccess) return FA_ERR_CUDA;
-
-  if (dtype == FA_DTYPE_F32_SIMT) {
-    fa::SimtParams p;
-    p.q = static_cast<const float *>(q);
-    p.k = static_cast<const float *>(k);
-    p.v = static_cast<const float *>(v);
-    p.o = static_cast<float *>(o);
-    p.lse = lse;
-    p.status = status;
-    p.H = H;
-    p.Nq = Nq;
-    p.Nk = Nk;
-    p.d = d;
-    p.n_qtiles = ceil_div(Nq, fa::BM);
-    p.scale = scale;
-    p.causal = causal;
-    if (fa::launch_simt(p, B, s) != cudaSuccess) return FA_ERR_CUDA;
-  } else {
-    if ((rc = get_encoder()) != FA_OK) return rc;
-    CUtensorMap mq, mk, mv, mo;
-    const int BH = B * H;
-    if ((rc = encode_map(&mq, q, dtype, BH, Nq, d)) != FA_OK) return rc;
-    if ((rc = encode_map(&mk, k, dtype, BH, Nk, d)) != FA_OK) return rc;
-    if ((rc = encode_map(&mv, v, dtype, BH, Nk, d)) != FA_OK) return rc;
-    if ((rc = encode_map(&mo, o, dtype, BH, Nq, d)) != FA_OK) return rc;
-    fa::TcParams p;
-    p.q = q;
-    p.o = o;
-    p.q_head_stride = static_cast<long long>(Nq) * d;
-    p.q_row_stride = d;
-    p.lse_head_stride = Nq;
-    p.lse = lse;
-    p.status = status;
-    p.H = H;
-    p.Nq = Nq;
-    p.Nk = Nk;
-    p.n_qtiles = ceil_div(Nq, fa::BM);
-    p.n_ktiles = ceil_div(Nk, fa::BN);
-    set_tc_scale(scale, &p);
-    const unsigned long long lim = g_wait_limit_ns.load();
-    p.wait_limit_ns = lim ? lim : fa::kDefaultWaitLimitNs;
-    p.skip_v_load = g_skip_v_load.load();
-    p.items_per_cta = items_per_cta(dtype, d, causal, static_cast<long long>(B) * H, p.n_qtiles,
-                                    p.n_ktiles);
-    cudaError_t e = launch_tc_any(mq, mk, mv, mo, p, B, causal, d, dtype, s);
-    if (e != cudaSuccess) return FA_ERR_CUDA;
-  }
+  if ((rc = fwd_enqueue(status, q, k, v, o, lse, B, H, Nq, Nk, d, scale, causal, dtype, s)) !=
+      FA_OK)
+    return rc;
   if (device_status == nullptr) return FA_OK;
   // Synchronous form: wait for the kernel and report its status word.
   unsigned word = 0;
@@ -762,6 +729,7 @@ extern "C" int fa_fwd_varlen(const void *q, const void *k, const void *v, void *
   p.cu_q = cu_seqlens_q;
   p.cu_k = cu_seqlens_k;
   p.total_q = total_q;
+  p.total_k = total_k;
   cudaError_t e = launch_tc_any(mq, mk, mv, mo, p, B, causal, d, dtype, s);
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }

@@ -45,10 +45,11 @@ struct TcParams {
   long long q_head_stride = 0, q_row_stride = 0, lse_head_stride = 0;
   // Variable-length batches: device cu_seqlens (B+1 entries each), or null.
   // Sequence b covers rows [cu_q[b], cu_q[b+1]) of Q/O and [cu_k[b], cu_k[b+1])
-  // of K/V; total_q bounds every row index (defends against bad offsets).
+  // of K/V; total_q and total_k bound every row index (defends against bad
+  // offsets).
   const int *cu_q = nullptr;
   const int *cu_k = nullptr;
-  int total_q = 0;
+  int total_q = 0, total_k = 0;
   // Head dim of the tensors when narrower than the kernel's D (0 = D): the
   // kernel runs zero-padded to D.
   int d_io = 0;

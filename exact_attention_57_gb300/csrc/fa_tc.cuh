@@ -18,9 +18,7 @@
 //                the thread's Q row there from global memory (the A operand of
 //                S = Q K^T).  Per key tile: load the
 //                row's 128 scores, mask the causal diagonal / ragged key tail,
-//                update m and l, write P back over S in TMEM.  (A polynomial
-//                exp2 on the FMA pipes is built in for a share of the
-//                exponentials; measured, that share is best at 0.)  At the
+//                update m and l, write P back over S in TMEM.  At the
 //                end of an item normalise O, stage it swizzled in shared
 //                memory for a TMA store, and write LSE.
 //   warp 4       TMA producer: Q (when in shared memory), then K_j / V_j
@@ -114,8 +112,6 @@ struct TcCfg {
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;       // tmem base, abort flag
   static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;   // + alignment slack
   static constexpr int THREADS = 224;
-  // Exponentials per 8 column pairs computed by the FMA-pipe polynomial.
-  static constexpr int EMU_PER_8 = 0;
   static_assert(NCH >= 1 && D % 32 == 0, "head dim must fill whole 128-byte chunks");
   static_assert(COL_O + D <= TMEM_COLS, "tensor memory budget");
   static_assert(!TF32 || QTMEM, "the fp32 path rounds Q on its way into tensor memory");
@@ -174,11 +170,12 @@ __global__ void __launch_bounds__(224, 1)
   int n_qtiles = p.n_qtiles, n_ktiles = p.n_ktiles;
   if (p.cu_q != nullptr) {
     const int b = static_cast<int>(blockIdx.z);
-    // Offsets clamped to [0, total]: row indices never leave the tensors.
+    // Offsets clamped to [0, total]: row indices never leave the tensors,
+    // and bad offsets cannot make a CTA walk more key tiles than exist.
     q_row0 = min(max(p.cu_q[b], 0), p.total_q);
-    k_row0 = max(p.cu_k[b], 0);
+    k_row0 = min(max(p.cu_k[b], 0), p.total_k);
     Nq = max(0, min(p.cu_q[b + 1], p.total_q) - q_row0);
-    Nk = max(0, p.cu_k[b + 1] - k_row0);
+    Nk = max(0, min(p.cu_k[b + 1], p.total_k) - k_row0);
     hc = static_cast<int>(blockIdx.y);
     n_qtiles = (Nq + BM - 1) / BM;
     n_ktiles = (Nk + BN - 1) / BN;
@@ -704,15 +701,9 @@ __global__ void __launch_bounds__(224, 1)
           for (int i = 0; i < kBlk; ++i) {
             const int c0 = 2 * (blk * kBlk + i);
             const uint64_t x2 = ffma2(pk2(S(c0), S(c0 + 1)), sl2_2, nm_2);
-            float p0, p1;
-            if ((i & 7) < C::EMU_PER_8) {
-              exp2_poly_pair(x2, p0, p1);
-            } else {
-              float x0, x1;
-              upk2(x2, x0, x1);
-              p0 = ex2_approx(x0);
-              p1 = ex2_approx(x1);
-            }
+            float x0, x1;
+            upk2(x2, x0, x1);
+            const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
             acc[i & 1] = fadd2(acc[i & 1], pk2(p0, p1));
             if constexpr (TF32) {
               pk[2 * i] = to_tf32(p0);

@@ -371,31 +371,4 @@ __device__ __forceinline__ float min3f(float a, float b, float c) {
   return d;
 }
 
-// 2^x for a pair, on the FMA pipes instead of the MUFU unit.  Range reduction
-// x = n + f with n = round(x), |f| <= 1/2 (Cody and Waite), taken from the
-// low mantissa bits of x + 1.5*2^23; 2^f by a cubic whose coefficients are the
-// minimax relative-error fit printed by csrc/fit_exp2_poly.py (max relative
-// error 7.5e-5, far below bf16/tf32 resolution); 2^n applied by adding n to
-// the exponent field.  Inputs are clamped to >= -125 (results below 2^-125
-// are treated as negligible, like the flush-to-zero of the hardware exp2);
-// inputs above 126 are not expected (the offset keeps x <= 8).
-__device__ __forceinline__ void exp2_poly_pair(uint64_t x2, float &p0, float &p1) {
-  constexpr float kMagic = 12582912.0f;  // 1.5 * 2^23
-  constexpr float kC0 = 0.9999281f, kC1 = 0.69326097f, kC2 = 0.24261084f, kC3 = 0.055171497f;
-  float x0, x1;
-  upk2(x2, x0, x1);
-  const uint64_t xc = pk2(fmaxf(x0, -125.f), fmaxf(x1, -125.f));
-  const uint64_t t = fadd2(xc, pk2(kMagic, kMagic));
-  const uint64_t n = fadd2(t, pk2(-kMagic, -kMagic));
-  const uint64_t f = ffma2(n, pk2(-1.f, -1.f), xc);
-  uint64_t q = ffma2(pk2(kC3, kC3), f, pk2(kC2, kC2));
-  q = ffma2(q, f, pk2(kC1, kC1));
-  q = ffma2(q, f, pk2(kC0, kC0));
-  float q0, q1, t0, t1;
-  upk2(q, q0, q1);
-  upk2(t, t0, t1);
-  p0 = __int_as_float(__float_as_int(q0) + (__float_as_int(t0) << 23));
-  p1 = __int_as_float(__float_as_int(q1) + (__float_as_int(t1) << 23));
-}
-
 }  // namespace fa

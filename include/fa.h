@@ -80,7 +80,8 @@ typedef enum {
  *           row i < Nq is written.
  * lse       device pointer to B*H*Nq floats, 4-byte aligned; every entry is
  *           written.
- * B, H      batch size and number of heads, 1 .. 65535.
+ * B, H      batch size and number of heads, 1 .. 65535 each, with
+ *           B * H <= 2^31 - 1 (else FA_ERR_INVALID_ARG).
  * Nq, Nk    query and key sequence lengths, >= 1 (ragged lengths allowed).
  * d         head dimension.  FA_DTYPE_BF16, FA_DTYPE_F16: 32, 64, 128 or 256.
  *           FA_DTYPE_F32: 32, 64 or 128.
@@ -122,7 +123,11 @@ int fa_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
  * problem size; a need beyond the 256-byte array would be refused with
  * FA_ERR_UNSUPPORTED before anything is enqueued.
  * device_status  NULL: the call returns once the work is enqueued and does
- *                not report the status word.  Non-NULL: the call waits for the
+ *                not report the status word.  A bounded-wait give-up in this
+ *                form reaches no one: the word stays in the array until the
+ *                next call clears it (fa_fwd_status reads fa_fwd's word, not
+ *                this one), so callers that need the report use the waiting
+ *                form.  Non-NULL: the call waits for the
  *                stream, stores the raw status word there (bits as in
  *                fa_fwd_status) and returns FA_ERR_DEVICE_TIMEOUT if it is
  *                non-zero.
@@ -183,8 +188,10 @@ unsigned long long fa_fwd_splitkv_workspace(int B, int H, int Nq, int d, int num
  *   holds rows [cu_seqlens_q[b], cu_seqlens_q[b+1]) of q/o and
  *   [cu_seqlens_k[b], cu_seqlens_k[b+1]) of k/v; nondecreasing, starting at
  *   0 and ending at total_q / total_k.  They are read on the device, so they
- *   are not checked on the host: rows are never read or written past total_q
- *   or total_k whatever they hold, but wrong offsets give wrong results.
+ *   are not checked on the host; the kernels clamp every offset to
+ *   [0, total_q] or [0, total_k], so whatever they hold no row past total_q
+ *   or total_k is read or written and no sequence spans more rows than
+ *   exist, but wrong offsets give wrong results.
  * max_seqlen_q  the longest query length (sizes the grid; 1 .. total_q).
  * A sequence with queries and no keys gets O = 0 and LSE = -inf.
  * Other arguments as for fa_fwd (tensor-core dtypes only; the SIMT dtype is

@@ -69,6 +69,19 @@ def test_invalid_arguments(lib, kw):
     assert call(**kw) == fa.FA_ERR_INVALID_ARG
 
 
+@pytest.mark.parametrize("B,H", [(65535, 65535), (65535, 32769), (32769, 65535)])
+def test_plane_count_above_int32_is_refused(lib, B, H):
+    """B * H above 2^31 - 1 planes is refused (the kernels index planes with
+    32-bit ints).  The buffers are spaced 2^44 bytes apart so that only the
+    plane count, not an overlap, can reject the call."""
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("host-only check: fake device addresses")
+    far = [(i + 1) << 44 for i in range(5)]
+    r = fa.fa_fwd(*far, B, H, 1, 1, 64, 0.125, 0, fa.FA_DTYPE_BF16, None)
+    assert r == fa.FA_ERR_INVALID_ARG
+
+
 @pytest.mark.parametrize("kw", [
     dict(dtype=fa.FA_DTYPE_BF16, d=16), dict(dtype=fa.FA_DTYPE_BF16, d=96),
     dict(dtype=fa.FA_DTYPE_BF16, d=512), dict(dtype=fa.FA_DTYPE_F32, d=256),

@@ -183,3 +183,40 @@ def test_large_workload_sampled_rows():
     ks = k.view(-1, d)[torch.from_numpy(rows)].float()
     self_score = (qs * ks).sum(-1).double().numpy() * w.scale
     assert np.all(gl >= self_score - 1e-2)
+
+
+def test_large_workload_every_row():
+    """The 256-head N=8192 causal workload at full size, in the launch the
+    benchmark times (fa_fwd, tiles per CTA chosen as in the benchmark), against
+    the oracle on every element of O and LSE.  The oracle runs one batch (32
+    heads) at a time to bound host memory; the statistics are over the whole
+    output."""
+    w = WORKLOADS["b8h32n8192d128-bf16-causal"]
+    q, k, v = workload_inputs(w)
+    dev = torch.device("cuda:0")
+    qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
+    o = torch.full_like(qd, float("nan"))
+    lse = torch.full(q.shape[:3], float("nan"), device=dev, dtype=torch.float32)
+    fa.attention(qd, kd, vd, scale=w.scale, causal=True, out=o, lse=lse)
+    st, word = fa.fa_fwd_status(torch.cuda.current_stream(dev).cuda_stream)
+    assert st == fa.FA_OK, f"device status word {word}"
+    o, lse = o.cpu(), lse.cpu()
+    del qd, kd, vd
+    max_o = sum_o = max_lse = 0.0
+    for b in range(w.B):
+        ro, rl = oracle.attn_fwd(q[b:b + 1].float().numpy(), k[b:b + 1].float().numpy(),
+                                 v[b:b + 1].float().numpy(), w.scale, True)
+        go = o[b:b + 1].double().numpy()
+        gl = lse[b:b + 1].double().numpy()
+        assert np.isfinite(go).all() and np.isfinite(gl).all(), f"batch {b}: unwritten rows"
+        eo = np.abs(go - ro)
+        max_o = max(max_o, float(eo.max()))
+        sum_o += float(eo.sum())
+        max_lse = max(max_lse, float(np.abs(gl - rl).max()))
+    mean_o = sum_o / o.numel()
+    print(f"\nb8h32n8192d128 causal, every row: max|dO| {max_o:.3e} mean|dO| {mean_o:.3e} "
+          f"max|dLSE| {max_lse:.3e}")
+    tol = TOL[w.dtype]
+    assert max_o <= tol["max_o"], max_o
+    assert mean_o <= tol["mean_o"], mean_o
+    assert max_lse <= tol["max_lse"], max_lse

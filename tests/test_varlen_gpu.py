@@ -2,6 +2,7 @@
 [total, H, d]) against the float64 oracle run on each sequence alone
 (needs a GB300)."""
 import math
+import time
 
 import numpy as np
 import pytest
@@ -80,3 +81,44 @@ def test_varlen_equals_fixed_length():
     torch.cuda.synchronize()
     assert torch.equal(o, tok(o_ref))
     assert torch.equal(lse, l_ref.permute(1, 0, 2).reshape(H, B * N))
+
+
+@pytest.mark.parametrize("cu_k_vals", [[0, 100, 2**31 - 1], [-50, 100, 10**9]])
+def test_varlen_key_offsets_past_total_are_clamped(cu_k_vals):
+    """Key offsets outside [0, total_k] (read on the device, not checked on
+    the host) are clamped there: the call returns promptly, writes nothing
+    outside O and LSE, and each sequence sees the keys that exist."""
+    dev = torch.device("cuda:0")
+    H, d, total_q, total_k = 2, 128, 160, 150
+    q, k, v = make_inputs(1, H, total_q, total_k, d, DTYPE_BF16, seed=41)
+    tok = lambda t: t[0].transpose(0, 1).contiguous()
+    qp, kp, vp = tok(q).to(dev), tok(k).to(dev), tok(v).to(dev)
+    cu_q = torch.tensor([0, 100, total_q], dtype=torch.int32, device=dev)
+    cu_k = torch.tensor(cu_k_vals, dtype=torch.int32, device=dev)
+    guard = 4096
+    n_o, n_l = total_q * H * d, H * total_q
+    obuf = torch.full((n_o + 2 * guard,), 7.0, device=dev, dtype=torch.bfloat16)
+    lbuf = torch.full((n_l + 2 * guard,), 7.0, device=dev, dtype=torch.float32)
+    o = obuf[guard:guard + n_o].view(total_q, H, d)
+    lse = lbuf[guard:guard + n_l].view(H, total_q)
+    scale = 1.0 / math.sqrt(d)
+    # warm-up with valid offsets (module load, kernel attributes)
+    good_k = torch.tensor([0, 100, total_k], dtype=torch.int32, device=dev)
+    fa.attention_varlen(qp, kp, vp, cu_q, good_k, 100, scale=scale, causal=False)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    fa.attention_varlen(qp, kp, vp, cu_q, cu_k, 100, scale=scale, causal=False, out=o, lse=lse)
+    st, word = fa.fa_fwd_status(torch.cuda.current_stream(dev).cuda_stream)
+    elapsed = time.perf_counter() - t0
+    assert st == fa.FA_OK, word
+    assert elapsed < 1.0, f"{elapsed:.2f} s: the key range was not clamped"
+    assert torch.all(obuf[:guard] == 7.0) and torch.all(obuf[guard + n_o:] == 7.0)
+    assert torch.all(lbuf[:guard] == 7.0) and torch.all(lbuf[guard + n_l:] == 7.0)
+    o, lse = o.double().cpu(), lse.double().cpu()
+    # sequence 0: queries [0, 100), keys [0, 100); sequence 1: queries
+    # [100, 160), keys [100, total_k)
+    for (q0, q1), (k0, k1) in [((0, 100), (0, 100)), ((100, total_q), (100, total_k))]:
+        ro, rl = run_oracle(q[:, :, q0:q1], k[:, :, k0:k1], v[:, :, k0:k1], scale, False)
+        go = o[q0:q1].transpose(0, 1).unsqueeze(0).numpy()
+        gl = lse[:, q0:q1].unsqueeze(0).numpy()
+        compare(go, gl, ro, rl, DTYPE_BF16, f"clamped keys [{k0}, {k1})")
