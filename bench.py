@@ -434,12 +434,16 @@ def main():
     total_ms = max_over_ranks(ev[0].elapsed_time(ev[-1]), dev)
     ms_per_step = total_ms / args.steps
     flops_step = varlen["flops"] if varlen is not None else w.flops(causal) * (2.5 if bwd else 1.0)
-    # query tiles per CTA of the timed forward (fa_fwd's own choice; the
-    # other entry points run one)
+    # the persistent grid of the timed forward (fa_fwd's own choice; the
+    # other entry points run one CTA per query tile)
     plain_fwd = not bwd and varlen is None and stage_ws is None and wspace is None
-    tiles_per_cta = (fa.fa_items_per_cta(w.B, w.H, w.Nq, w.Nk, w.d, causal, w.dtype,
-                                         torch.cuda.get_device_properties(dev).multi_processor_count)
-                     if plain_fwd else 1)
+    grid = None
+    if plain_fwd:
+        _, ctas, groups = fa.fa_fwd_schedule(
+            w.B, w.H, w.Nq, w.Nk, w.d, w.dtype,
+            torch.cuda.get_device_properties(dev).multi_processor_count)
+        if ctas > 0:
+            grid = {"persistent_ctas": ctas, "planes_per_group": groups}
     value = ws * flops_step * args.steps / (total_ms / 1e3) / 1e12
 
     # End to end through the host-buffer entry point: H2D of q, k, v from
@@ -523,7 +527,7 @@ def main():
                    "causal": causal, "flops_per_step": flops_step,
                    "parallelism": f"replicas{ws}" if ws > 1 else "single",
                    "key_splits": args.splits, "pass": args.which,
-                   "tiles_per_cta": tiles_per_cta,
+                   "grid": grid,
                    "staged": stage_ws is not None,
                    "varlen": (None if varlen is None else
                               {"sequences": len(varlen["lens"]), "total_tokens": varlen["total"],

@@ -80,5 +80,53 @@ def build_library(force: bool = False, verbose: bool = False) -> str:
     return LIB
 
 
+def ptxas_summary(log_path: str | None = None) -> str:
+    """Markdown table of the ptxas statistics of every kernel in the last
+    build: registers per thread, stack frame, spill stores and loads, static
+    shared memory (the tensor-core kernels' shared memory is dynamic and set
+    at launch).  Kernel names are demangled with c++filt when it is present."""
+    import re
+    text = open(log_path or os.path.join(BUILD, "ptxas.log")).read()
+    rows, cur = [], None
+    for line in text.splitlines():
+        m = re.search(r"Compiling entry function '(\S+)'", line)
+        if m:
+            cur = {"name": m.group(1), "regs": "?", "stack": "?", "spill_st": "?",
+                   "spill_ld": "?", "smem": "0"}
+            rows.append(cur)
+            continue
+        if cur is None:
+            continue
+        m = re.search(r"(\d+) bytes stack frame, (\d+) bytes spill stores, (\d+) bytes spill loads",
+                      line)
+        if m:
+            cur["stack"], cur["spill_st"], cur["spill_ld"] = m.groups()
+        m = re.search(r"Used (\d+) registers", line)
+        if m:
+            cur["regs"] = m.group(1)
+        m = re.search(r"(\d+) bytes smem", line)
+        if m:
+            cur["smem"] = m.group(1)
+    names = [r["name"] for r in rows]
+    filt = shutil.which("c++filt")
+    if filt and names:
+        out = subprocess.run([filt], input="\n".join(names), capture_output=True, text=True)
+        dem = out.stdout.splitlines()
+        if len(dem) == len(names):
+            for r, n in zip(rows, dem):
+                n = n.replace("(anonymous namespace)::", "")
+                r["name"] = re.sub(r"\([^()]*\)$", "", n)
+    lines = ["| kernel | registers | stack (B) | spill stores (B) | spill loads (B) | static smem (B) |",
+             "|---|---|---|---|---|---|"]
+    for r in sorted(rows, key=lambda r: r["name"]):
+        lines.append(f"| `{r['name']}` | {r['regs']} | {r['stack']} | {r['spill_st']} | "
+                     f"{r['spill_ld']} | {r['smem']} |")
+    return "\n".join(lines) + "\n"
+
+
 if __name__ == "__main__":
-    print(build_library(force="--force" in sys.argv, verbose="-v" in sys.argv))
+    if "--ptxas-summary" in sys.argv:
+        build_library(force="--force" in sys.argv)
+        print(ptxas_summary(), end="")
+    else:
+        print(build_library(force="--force" in sys.argv, verbose="-v" in sys.argv))

@@ -11,6 +11,7 @@
 #include <cstdint>
 #include <cstring>
 #include <mutex>
+#include <vector>
 
 #include "fa.h"
 #include "fa_internal.h"
@@ -25,7 +26,8 @@ int g_dev_ok[kMaxDevices] = {};         // 0 unknown, 1 sm_103, -1 other
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 std::atomic<int> g_skip_v_load{0};
 std::atomic<unsigned long long> g_wait_limit_ns{0};
-std::atomic<int> g_force_items{0};  // query tiles per CTA forced by a test (0 = automatic)
+std::atomic<int> g_force_ctas{0};   // persistent grid size forced by a test (0 = automatic)
+std::atomic<int> g_force_group{0};  // planes per group forced by a test (0 = automatic)
 
 size_t elem_size(int dtype) { return (dtype == FA_DTYPE_BF16 || dtype == FA_DTYPE_F16) ? 2 : 4; }
 
@@ -142,56 +144,30 @@ int ceil_div(int a, int b) { return (a + b - 1) / b; }
 
 int sm_count();
 
-// Query tiles per CTA of the plain 16-bit forward, G in {1, 2, 4}; the
-// tiles of a CTA are taken in zigzag pairs (heaviest with lightest), so with
-// G >= 2 every causal CTA has the same work.  A CTA's fixed cost (set-up,
-// pipeline fill, its last epilogue) is paid once for all its tiles, and each
-// next tile's loads and first products overlap the previous epilogue; but
-// fewer, longer CTAs can leave the SMs' last wave part empty.  The choice
-// minimises a makespan model in units of one key tile's time t:
-//   G >= 2: ceil(CTAs / SMs) * (G * nbar + c)          (equal CTAs)
-//   G = 1:  CTAs * (nbar + c1) / SMs + nbar             (causal: uneven CTAs,
-//           heaviest first; non-causal: as G >= 2 with c1)
-// nbar = mean key tiles per query tile; c and c1 = fixed cost per CTA with
-// and without a following tile to hide the epilogue.  Fitted on GB300 at
-// d = 128 (t = 0.77 us, c = 2.0 us, c1 = 3.0 us); a tile's time scales with
-// the head dim, the fixed cost does not.  A G that leaves fewer CTAs than
-// SMs is not taken (b2h8n3001d128: 96 CTAs of four tiles ran 6% slower than
-// 384 of one, where the model has them equal).  The fp32 path keeps one.
-int items_model(int dtype, int d, int causal, long long planes, int n_qtiles, int n_ktiles,
-                int num_sms) {
-  if (dtype != FA_DTYPE_BF16 && dtype != FA_DTYPE_F16) return 1;
-  if (n_qtiles < 1 || n_ktiles < 1 || planes < 1) return 1;
-  const double sms = num_sms > 0 ? num_sms : 1;
-  // key tiles summed over the query tiles of one (batch, head)
-  const double nq = n_qtiles, nk = n_ktiles;
-  const double ksum = !causal ? nq * nk
-                      : (nq <= nk ? nq * (nq + 1) / 2 : nk * (nk + 1) / 2 + (nq - nk) * nk);
-  const double nbar = ksum / nq;
-  const double tile = d <= 64 ? 0.5 : d <= 128 ? 1.0 : 2.0;  // relative key-tile time
-  const double c = 2.6 / tile, c1 = 3.9 / tile;
-  const double qtiles = static_cast<double>(planes) * n_qtiles;
-  double best = causal ? qtiles * (nbar + c1) / sms + nbar
-                       : std::ceil(qtiles / sms) * (nbar + c1);
-  int pick = 1;
-  // (a CTA's tiles come from one head: no more than it has)
-  for (int g = 2; g <= fa::kMaxItemsPerCta && g <= n_qtiles; g *= 2) {
-    const double ctas = static_cast<double>(planes) * std::ceil(nq / g);
-    if (ctas < sms) break;
-    const double cost = std::ceil(ctas / sms) * (g * nbar + c);
-    if (cost < best) {
-      best = cost;
-      pick = g;
-    }
-  }
-  return pick;
-}
+// K and V bytes of the planes that run at the same time in a persistent grid
+// (one group of fwd_item): sized to stay in L2 (129 MB on GB300) next to the
+// Q tiles and O stores passing through, so each head's K/V tiles come from
+// HBM about once while all of its query tiles run.
+constexpr double kL2GroupBytes = 48.0 * (1 << 20);
 
-int items_per_cta(int dtype, int d, int causal, long long planes, int n_qtiles, int n_ktiles) {
-  if (dtype != FA_DTYPE_BF16 && dtype != FA_DTYPE_F16) return 1;
-  const int forced = g_force_items.load();
-  if (forced > 0) return forced < fa::kMaxItemsPerCta ? forced : fa::kMaxItemsPerCta;
-  return items_model(dtype, d, causal, planes, n_qtiles, n_ktiles, sm_count());
+// Persistent schedule of the plain 16-bit forward: *ctas CTAs (one per SM, or
+// fewer when there are fewer query tiles; a test can force the count) and
+// *group_heads planes per group of fwd_item.  Other dtypes run one CTA per
+// query tile (*ctas = 0).
+void fwd_schedule(int dtype, int d, long long planes, int n_qtiles, int Nk, int num_sms,
+                  int forced, int forced_group, int *ctas, int *group_heads) {
+  *ctas = 0;
+  *group_heads = 1;
+  if (dtype != FA_DTYPE_BF16 && dtype != FA_DTYPE_F16) return;
+  const long long items = planes * n_qtiles;
+  long long c = forced > 0 ? forced : (num_sms > 0 ? num_sms : 1);
+  if (c > items) c = items;
+  *ctas = static_cast<int>(c);
+  const double kv = 2.0 * Nk * (d < 64 ? 64 : d) * static_cast<double>(elem_size(dtype));
+  long long g = forced_group > 0 ? forced_group : static_cast<long long>(kL2GroupBytes / kv);
+  if (g < 1) g = 1;
+  if (g > planes) g = planes;
+  *group_heads = static_cast<int>(g);
 }
 
 // The tensor-core forward instantiation for (dtype, d); the combination has
@@ -201,24 +177,29 @@ int items_per_cta(int dtype, int d, int causal, long long planes, int n_qtiles, 
 // 32-wide rows zero-fill columns 32..63 on load (so S and P V are unchanged)
 // and clip them on store; d_io tells the kernel where its plain loads and
 // stores stop.
+//
+// mklo: the staged fp32 path's map over K_lo (null otherwise; the kernels
+// then get the K map in its place and never read it).
 cudaError_t launch_tc_any(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv,
                           const CUtensorMap &mo, const fa::TcParams &p_in, int B, int causal,
-                          int d, int dtype, cudaStream_t s) {
+                          int d, int dtype, cudaStream_t s,
+                          const CUtensorMap *mklo = nullptr) {
   fa::TcParams p = p_in;
   if (d == 32) {
     p.d_io = 32;
     d = 64;
   }
+  const CUtensorMap &ml = mklo ? *mklo : mk;
   if (dtype == FA_DTYPE_F16)
-    return d == 64    ? fa::launch_tc_f16_d64(mq, mk, mv, mo, p, B, causal, s)
-           : d == 128 ? fa::launch_tc_f16_d128(mq, mk, mv, mo, p, B, causal, s)
-                      : fa::launch_tc_f16_d256(mq, mk, mv, mo, p, B, causal, s);
+    return d == 64    ? fa::launch_tc_f16_d64(mq, mk, mv, mo, ml, p, B, causal, s)
+           : d == 128 ? fa::launch_tc_f16_d128(mq, mk, mv, mo, ml, p, B, causal, s)
+                      : fa::launch_tc_f16_d256(mq, mk, mv, mo, ml, p, B, causal, s);
   if (dtype == FA_DTYPE_BF16)
-    return d == 64    ? fa::launch_tc_bf16_d64(mq, mk, mv, mo, p, B, causal, s)
-           : d == 128 ? fa::launch_tc_bf16_d128(mq, mk, mv, mo, p, B, causal, s)
-                      : fa::launch_tc_bf16_d256(mq, mk, mv, mo, p, B, causal, s);
-  return d == 64 ? fa::launch_tc_f32_d64(mq, mk, mv, mo, p, B, causal, s)
-                 : fa::launch_tc_f32_d128(mq, mk, mv, mo, p, B, causal, s);
+    return d == 64    ? fa::launch_tc_bf16_d64(mq, mk, mv, mo, ml, p, B, causal, s)
+           : d == 128 ? fa::launch_tc_bf16_d128(mq, mk, mv, mo, ml, p, B, causal, s)
+                      : fa::launch_tc_bf16_d256(mq, mk, mv, mo, ml, p, B, causal, s);
+  return d == 64 ? fa::launch_tc_f32_d64(mq, mk, mv, mo, ml, p, B, causal, s)
+                 : fa::launch_tc_f32_d128(mq, mk, mv, mo, ml, p, B, causal, s);
 }
 
 // The tensor-core kernels take |scale| * log2(e) > 0 and apply a negative
@@ -283,8 +264,9 @@ int fwd_enqueue(unsigned *status, const void *q, const void *k, const void *v, v
   const unsigned long long lim = g_wait_limit_ns.load();
   p.wait_limit_ns = lim ? lim : fa::kDefaultWaitLimitNs;
   p.skip_v_load = g_skip_v_load.load();
-  p.items_per_cta = items_per_cta(dtype, d, causal, static_cast<long long>(B) * H, p.n_qtiles,
-                                  p.n_ktiles);
+  p.planes = BH;
+  fwd_schedule(dtype, d, BH, p.n_qtiles, Nk, sm_count(), g_force_ctas.load(),
+               g_force_group.load(), &p.ctas, &p.group_heads);
 
   cudaError_t e = launch_tc_any(mq, mk, mv, mo, p, B, causal, d, dtype, s);
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
@@ -460,15 +442,41 @@ int fa_set_test_hooks(int skip_v_load, unsigned long long wait_limit_ns) {
   return FA_OK;
 }
 
-int fa_items_per_cta(int B, int H, int Nq, int Nk, int d, int causal, int dtype, int num_sms) {
-  if (B < 1 || H < 1 || Nq < 1 || Nk < 1 || d < 1 || num_sms < 1) return 0;
-  return items_model(dtype, d, causal != 0, static_cast<long long>(B) * H, ceil_div(Nq, fa::BM),
-                     ceil_div(Nk, fa::BN), num_sms);
+int fa_fwd_schedule(int B, int H, int Nq, int Nk, int d, int dtype, int num_sms, int *ctas,
+                    int *group_heads) {
+  if (!ctas || !group_heads) return FA_ERR_INVALID_ARG;
+  if (B < 1 || H < 1 || Nq < 1 || Nk < 1 || d < 1 || num_sms < 1) return FA_ERR_INVALID_ARG;
+  if (static_cast<long long>(B) * H > 2147483647LL) return FA_ERR_INVALID_ARG;
+  fwd_schedule(dtype, d, static_cast<long long>(B) * H, ceil_div(Nq, fa::BM), Nk, num_sms,
+               g_force_ctas.load(), g_force_group.load(), ctas, group_heads);
+  return FA_OK;
 }
 
-int fa_set_items_per_cta(int n) {
-  if (n < 0 || n > fa::kMaxItemsPerCta) return FA_ERR_INVALID_ARG;
-  g_force_items.store(n);
+int fa_fwd_schedule_covers(int planes, int n_qtiles, int ctas, int group_heads) {
+  if (planes < 1 || n_qtiles < 1 || ctas < 1 || group_heads < 1) return 0;
+  const long long items = static_cast<long long>(planes) * n_qtiles;
+  if (items > (1LL << 24) || ctas > items) return 0;
+  std::vector<unsigned char> seen(static_cast<size_t>(items), 0);
+  for (int c = 0; c < ctas; ++c) {
+    for (int k = 0;; ++k) {
+      int plane = -1;
+      const int t = fa::fwd_item(k, c, ctas, planes, n_qtiles, group_heads, &plane);
+      if (t < 0) break;
+      if (t >= n_qtiles || plane < 0 || plane >= planes) return 0;
+      unsigned char &v = seen[static_cast<size_t>(plane) * n_qtiles + t];
+      if (v) return 0;
+      v = 1;
+    }
+  }
+  for (unsigned char v : seen)
+    if (!v) return 0;
+  return 1;
+}
+
+int fa_set_fwd_schedule(int ctas, int group_heads) {
+  if (ctas < 0 || group_heads < 0) return FA_ERR_INVALID_ARG;
+  g_force_ctas.store(ctas);
+  g_force_group.store(group_heads);
   return FA_OK;
 }
 
@@ -853,7 +861,8 @@ namespace {
 
 int nk_pad128(int Nk) { return ceil_div(Nk, fa::BN) * fa::BN; }
 
-// Workspace parts for fp32: K rounded to tf32 [B*H][Nk][d], then V^T
+// Workspace parts for fp32: K_hi = tf32(K) [B*H][Nk][d], K_lo =
+// tf32(K - K_hi) [B*H][Nk][d] (each part kr bytes), then V^T
 // [B*H][d][Nk padded to 128].
 void staged_parts(int B, int H, int Nk, int d, size_t *kr, size_t *vt) {
   const size_t bh = static_cast<size_t>(B) * H;
@@ -883,7 +892,7 @@ extern "C" unsigned long long fa_fwd_staged_workspace(int B, int H, int Nk, int 
   if (dtype != FA_DTYPE_F32) return 0;  // only the fp32 path stages operands
   size_t kr, vt;
   staged_parts(B, H, Nk, d, &kr, &vt);
-  return kr + vt;
+  return 2 * kr + vt;
 }
 
 extern "C" int fa_fwd_staged(const void *q, const void *k, const void *v, void *o, float *lse,
@@ -896,7 +905,7 @@ extern "C" int fa_fwd_staged(const void *q, const void *k, const void *v, void *
     return fa_fwd(q, k, v, o, lse, B, H, Nq, Nk, d, scale, causal, dtype, stream);
   size_t kr_bytes, vt_bytes;
   staged_parts(B, H, Nk, d, &kr_bytes, &vt_bytes);
-  const size_t need = kr_bytes + vt_bytes;
+  const size_t need = 2 * kr_bytes + vt_bytes;
   if (workspace == nullptr || reinterpret_cast<uintptr_t>(workspace) % 256 != 0 ||
       workspace_bytes < need)
     return FA_ERR_INVALID_ARG;
@@ -914,14 +923,16 @@ extern "C" int fa_fwd_staged(const void *q, const void *k, const void *v, void *
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int BH = B * H, nkp = nk_pad128(Nk);
   float *kr = static_cast<float *>(workspace);
-  float *vt = reinterpret_cast<float *>(static_cast<char *>(workspace) + kr_bytes);
-  if (fa::launch_stage_f32(static_cast<const float *>(k), static_cast<const float *>(v), kr, vt,
-                           BH, Nk, nkp, d, s) != cudaSuccess)
+  float *kl = reinterpret_cast<float *>(static_cast<char *>(workspace) + kr_bytes);
+  float *vt = reinterpret_cast<float *>(static_cast<char *>(workspace) + 2 * kr_bytes);
+  if (fa::launch_stage_f32(static_cast<const float *>(k), static_cast<const float *>(v), kr, kl,
+                           vt, BH, Nk, nkp, d, s) != cudaSuccess)
     return FA_ERR_CUDA;
 
-  CUtensorMap mq, mk, mv, mo;
+  CUtensorMap mq, mk, mv, mo, mkl;
   if ((rc = encode_map(&mq, q, dtype, BH, Nq, d)) != FA_OK) return rc;
   if ((rc = encode_map(&mk, kr, dtype, BH, Nk, d)) != FA_OK) return rc;
+  if ((rc = encode_map(&mkl, kl, dtype, BH, Nk, d)) != FA_OK) return rc;
   if ((rc = encode_map_vt(&mv, vt, BH, nkp, d, d <= 64 ? 64 : 128)) != FA_OK) return rc;
   if ((rc = encode_map(&mo, o, dtype, BH, Nq, d)) != FA_OK) return rc;
   fa::TcParams p;
@@ -942,7 +953,7 @@ extern "C" int fa_fwd_staged(const void *q, const void *k, const void *v, void *
   p.wait_limit_ns = lim ? lim : fa::kDefaultWaitLimitNs;
   p.skip_v_load = g_skip_v_load.load();
   p.kv_staged = 1;
-  cudaError_t e = launch_tc_any(mq, mk, mv, mo, p, B, causal, d, dtype, s);
+  cudaError_t e = launch_tc_any(mq, mk, mv, mo, p, B, causal, d, dtype, s, &mkl);
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 

@@ -53,23 +53,46 @@ struct TcParams {
   // Head dim of the tensors when narrower than the kernel's D (0 = D): the
   // kernel runs zero-padded to D.
   int d_io = 0;
-  // fp32 path: K already rounded to tf32 and tm_v a map over a tf32 V^T
-  // ([B*H][d][Nk padded to 128], boxes of 32 keys x D rows).
+  // fp32 path: K already split into K_hi (tm_k) and K_lo (tm_klo), and tm_v
+  // a map over a tf32 V^T ([B*H][d][Nk padded to 128], boxes of 32 keys x D
+  // rows).
   int kv_staged = 0;
-  // Query tiles per CTA (plain problems, 16-bit types): 1 to
-  // kMaxItemsPerCta, taken from the zigzag heaviest/lightest order (the grid
-  // then has ceil(n_qtiles / items) CTAs per head, items = tc_items(*this)).
-  int items_per_cta = 1;
+  // Persistent schedule (plain problems, 16-bit types): ctas > 0 launches a
+  // grid of that many CTAs, each running the items (query tiles) that
+  // fwd_item() assigns it; planes = B*H; group_heads as in fwd_item().
+  // ctas = 0: one CTA per (query tile, head, batch).
+  int ctas = 0;
+  int planes = 0;
+  int group_heads = 1;
 };
 
-// Query tiles per CTA of the forward kernel (at most kMaxItemsPerCta: the
-// kernel has one O-staged barrier per item); the launcher sizes the grid
-// with the same value.
-constexpr int kMaxItemsPerCta = 4;
-__host__ __device__ inline int tc_items(const TcParams &p) {
-  return p.items_per_cta <= 1 ? 1 : (p.items_per_cta < kMaxItemsPerCta ? p.items_per_cta
-                                                                         : kMaxItemsPerCta);
+// Item k of CTA c of a persistent grid of P CTAs: returns the query tile and
+// sets *plane (the (batch, head) index b*H + h), or returns -1 when the CTA
+// has no k-th item.  Order: the planes in groups of group_heads (a group's
+// K and V are sized to stay in L2 while its query tiles run); within a group,
+// query tile n_qtiles-1 of every plane, then n_qtiles-2, and so on (heaviest
+// first when causal).  Items are dealt in rounds of P, alternately to CTAs
+// 0..P-1 and P-1..0, so the heaviest and lightest items of successive rounds
+// pair up and every CTA gets about the same work.  Every item 0 ..
+// planes*n_qtiles-1 goes to exactly one (CTA, k).
+__host__ __device__ inline int fwd_item(int k, int c, int P, int planes, int n_qtiles,
+                                        int group_heads, int *plane) {
+  const long long i = static_cast<long long>(k) * P + ((k & 1) ? P - 1 - c : c);
+  if (i >= static_cast<long long>(planes) * n_qtiles) return -1;
+  const long long gsz = static_cast<long long>(group_heads) * n_qtiles;
+  const long long grp = i / gsz;
+  const long long r = i - grp * gsz;
+  const int h0 = static_cast<int>(grp * group_heads);
+  const int hg = planes - h0 < group_heads ? planes - h0 : group_heads;
+  const int t = static_cast<int>(r / hg);
+  *plane = h0 + static_cast<int>(r - static_cast<long long>(t) * hg);
+  return n_qtiles - 1 - t;
 }
+
+// Ring of per-item state in the forward kernel (O-staged barriers, the
+// producer's record of where each item's O is staged): items whose O waits in
+// a V stage for its TMA store number at most VST + 1 <= kItemRing.
+constexpr int kItemRing = 8;
 
 struct SimtParams {
   const float *q, *k, *v;
@@ -82,32 +105,33 @@ struct SimtParams {
 };
 
 // Tensor-core forward for one (head dim, input type); causal chosen inside.
-// Returns the launch's cudaError_t.
+// klo: the fp32 path's staged K_lo map (p.kv_staged), else unused (any valid
+// map).  Returns the launch's cudaError_t.
 cudaError_t launch_tc_bf16_d64(const CUtensorMap &q, const CUtensorMap &k, const CUtensorMap &v,
-                               const CUtensorMap &o, const TcParams &p, int B, int causal,
-                               cudaStream_t s);
+                               const CUtensorMap &o, const CUtensorMap &klo, const TcParams &p,
+                               int B, int causal, cudaStream_t s);
 cudaError_t launch_tc_bf16_d128(const CUtensorMap &q, const CUtensorMap &k, const CUtensorMap &v,
-                                const CUtensorMap &o, const TcParams &p, int B, int causal,
-                                cudaStream_t s);
+                                const CUtensorMap &o, const CUtensorMap &klo, const TcParams &p,
+                                int B, int causal, cudaStream_t s);
 cudaError_t launch_tc_f32_d64(const CUtensorMap &q, const CUtensorMap &k, const CUtensorMap &v,
-                              const CUtensorMap &o, const TcParams &p, int B, int causal,
-                              cudaStream_t s);
+                              const CUtensorMap &o, const CUtensorMap &klo, const TcParams &p,
+                              int B, int causal, cudaStream_t s);
 cudaError_t launch_tc_f32_d128(const CUtensorMap &q, const CUtensorMap &k, const CUtensorMap &v,
-                               const CUtensorMap &o, const TcParams &p, int B, int causal,
-                               cudaStream_t s);
+                               const CUtensorMap &o, const CUtensorMap &klo, const TcParams &p,
+                               int B, int causal, cudaStream_t s);
 
 cudaError_t launch_tc_f16_d64(const CUtensorMap &q, const CUtensorMap &k, const CUtensorMap &v,
-                              const CUtensorMap &o, const TcParams &p, int B, int causal,
-                              cudaStream_t s);
+                              const CUtensorMap &o, const CUtensorMap &klo, const TcParams &p,
+                              int B, int causal, cudaStream_t s);
 cudaError_t launch_tc_f16_d128(const CUtensorMap &q, const CUtensorMap &k, const CUtensorMap &v,
-                               const CUtensorMap &o, const TcParams &p, int B, int causal,
-                               cudaStream_t s);
+                               const CUtensorMap &o, const CUtensorMap &klo, const TcParams &p,
+                               int B, int causal, cudaStream_t s);
 cudaError_t launch_tc_bf16_d256(const CUtensorMap &q, const CUtensorMap &k, const CUtensorMap &v,
-                                const CUtensorMap &o, const TcParams &p, int B, int causal,
-                                cudaStream_t s);
+                                const CUtensorMap &o, const CUtensorMap &klo, const TcParams &p,
+                                int B, int causal, cudaStream_t s);
 cudaError_t launch_tc_f16_d256(const CUtensorMap &q, const CUtensorMap &k, const CUtensorMap &v,
-                               const CUtensorMap &o, const TcParams &p, int B, int causal,
-                               cudaStream_t s);
+                               const CUtensorMap &o, const CUtensorMap &klo, const TcParams &p,
+                               int B, int causal, cudaStream_t s);
 
 // Merge of the split-mode chunks into o (dtype: bf16, f16 or f32) and lse.
 cudaError_t launch_splitkv_combine(const float *ws_o, const float *ws_lse, void *o, float *lse,
@@ -116,10 +140,10 @@ cudaError_t launch_splitkv_combine(const float *ws_o, const float *ws_lse, void 
 
 cudaError_t launch_simt(const SimtParams &p, int B, cudaStream_t s);
 
-// fp32 staging pre-pass: kr = tf32(k) in k's layout, vt[bh][x][n] = tf32(v[bh][n][x])
-// for n < Nk and 0 for Nk <= n < nk_pad.
-cudaError_t launch_stage_f32(const float *k, const float *v, float *kr, float *vt, int BH, int Nk,
-                             int nk_pad, int d, cudaStream_t s);
+// fp32 staging pre-pass: kr = tf32(k) and kl = tf32(k - kr) in k's layout,
+// vt[bh][x][n] = tf32(v[bh][n][x]) for n < Nk and 0 for Nk <= n < nk_pad.
+cudaError_t launch_stage_f32(const float *k, const float *v, float *kr, float *kl, float *vt,
+                             int BH, int Nk, int nk_pad, int d, cudaStream_t s);
 
 // ------------------------------------------------------------------ backward
 // Tensor-core backward: one CTA per (key tile, head, batch).  The TMA maps

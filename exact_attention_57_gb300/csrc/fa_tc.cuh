@@ -80,15 +80,21 @@ struct TcCfg {
   static constexpr int UK = 32 / ESZ;                       // K extent of one UMMA
   // Score buffers in tensor memory: S_j lives in buffer j % NS; S_j may be
   // issued once P_{j-NS} V_{j-NS} is done, so NS - 1 score tiles can be
-  // computed ahead of the softmax.
-  static constexpr int NS = (TF32 || D >= 256) ? 2 : 3;
+  // computed ahead of the softmax.  (fp32 at D = 128: one buffer, because
+  // both halves of the split Q fill the rest of tensor memory.)
+  static constexpr int NS = TF32 ? (D >= 128 ? 1 : 2) : (D >= 256 ? 2 : 3);
   static constexpr uint32_t TMEM_COLS = 512;
   static constexpr uint32_t COL_O = NS * 128;               // O after the score buffers
   static constexpr int Q_COLS = D * ESZ / 4;                // 32-bit columns of one Q row
+  // fp32 path: S = Q K^T runs as three tf32 products of the split operands,
+  // Q_hi K_hi + Q_hi K_lo + Q_lo K_hi, x_hi = tf32(x), x_lo = tf32(x - x_hi),
+  // so the scores carry about fp32 accuracy instead of tf32's 2^-11.
+  static constexpr int NQSPLIT = TF32 ? 2 : 1;
   // Q is the A operand of S = Q K^T: from tensor memory when it fits after O,
   // else from shared memory (bf16, D = 128).
-  static constexpr bool QTMEM = COL_O + D + Q_COLS <= TMEM_COLS;
+  static constexpr bool QTMEM = COL_O + D + NQSPLIT * Q_COLS <= TMEM_COLS;
   static constexpr uint32_t COL_Q = COL_O + D;
+  static constexpr uint32_t COL_QLO = COL_Q + Q_COLS;      // fp32 path: Q_lo
   static constexpr int NQ = QTMEM ? 0 : 1;                  // Q tiles in shared memory
   // K / V ring depths: as deep as shared memory allows (64 KB tiles at
   // D = 256 leave room for one stage each beside Q).
@@ -99,16 +105,22 @@ struct TcCfg {
   // with V^T as a K-major B operand.  Two copies alternate.
   static constexpr int NVT = TF32 ? (TILE_BYTES >= 65536 ? 1 : 2) : 0;
   static constexpr int VT_CHUNK_BYTES = D * 128;            // 32 keys x D rows
+  // fp32 path, K_lo of the split: with staged operands it is loaded into the
+  // V ring's stage s beside K_hi in K stage s (the V ring is free: V^T goes
+  // straight to the V^T buffers).  Converted in the kernel, it goes to one
+  // buffer of its own at D = 64, and at D = 128 to the one V^T buffer, which
+  // holds K_lo_j until S_j completes and V_j^T after that.
+  static constexpr int NKLO = (TF32 && NVT >= 2) ? 1 : 0;
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_K = OFF_Q + NQ * TILE_BYTES;
   static constexpr int OFF_V = OFF_K + KST * TILE_BYTES;
-  static constexpr int OFF_VT = OFF_V + VST * TILE_BYTES;
+  static constexpr int OFF_KLO = OFF_V + VST * TILE_BYTES;
+  static constexpr int OFF_VT = OFF_KLO + NKLO * TILE_BYTES;
   static constexpr int OFF_BAR = OFF_VT + NVT * TILE_BYTES;
   // q, kfull[KST], kempty[KST], vfull[VST], vempty[VST], sfull[NS], pfull[NS],
   // odone[NS], fin[2], kready[KST]
-  // ... then qempty, ofree, ostaged[kMaxItemsPerCta] (several query tiles
-  // per CTA)
-  static constexpr int NBAR = 1 + 2 * KST + 2 * VST + 3 * NS + 2 + KST + 2 + kMaxItemsPerCta;
+  // ... then qempty, ofree, ostaged[kItemRing] (several query tiles per CTA)
+  static constexpr int NBAR = 1 + 2 * KST + 2 * VST + 3 * NS + 2 + KST + 2 + kItemRing;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;       // tmem base, abort flag
   static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;   // + alignment slack
   static constexpr int THREADS = 224;
@@ -116,7 +128,11 @@ struct TcCfg {
   static_assert(COL_O + D <= TMEM_COLS, "tensor memory budget");
   static_assert(!TF32 || QTMEM, "the fp32 path rounds Q on its way into tensor memory");
   static_assert(!TF32 || VST == NVT, "staged V^T tiles use the V ring's barriers");
+  static_assert(!TF32 || KST == VST, "staged K_lo tiles sit in the V stage of their K stage");
+  static_assert(!TF32 || NKLO == 1 || NS == 1,
+                "K_lo shares the V^T buffer only where S_j completes before V_j^T is written");
   static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
+  static_assert(VST + 1 <= kItemRing, "items with O staged in a V stage fit the item ring");
 };
 
 constexpr float kRescaleThreshold = 8.0f;   // log2 units: factor 256
@@ -130,7 +146,8 @@ __global__ void __launch_bounds__(224, 1)
     fa_tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                      const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_v,
-                     const __grid_constant__ CUtensorMap tm_o, const TcParams p) {
+                     const __grid_constant__ CUtensorMap tm_o,
+                     const __grid_constant__ CUtensorMap tm_klo, const TcParams p) {
   using C = TcCfg<D, TF32>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
@@ -140,6 +157,7 @@ __global__ void __launch_bounds__(224, 1)
   const uint32_t sK = sbase + C::OFF_K;
   const uint32_t sV = sbase + C::OFF_V;
   const uint32_t sVT = sbase + C::OFF_VT;
+  const uint32_t sKLO = sbase + C::OFF_KLO;  // fp32, converted in the kernel, D = 64
   const uint32_t bQ = sbase + C::OFF_BAR;             // Q in place (TMEM or smem)
   const uint32_t bKfull = bQ + 8;                      // + 8*stage
   const uint32_t bKempty = bKfull + 8 * C::KST;
@@ -153,7 +171,7 @@ __global__ void __launch_bounds__(224, 1)
   const uint32_t bKready = bFin2 + 8;                  // + 8*stage (fp32 path)
   const uint32_t bQempty = bKready + 8 * C::KST;       // Q of an item read by its last S
   const uint32_t bOfree = bQempty + 8;                 // O of an item read by the epilogue
-  const uint32_t bOstaged = bOfree + 8;                // + 8*item: its O staged for TMA
+  const uint32_t bOstaged = bOfree + 8;                // + 8*(item % kItemRing): O staged
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::OFF_MISC);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::OFF_MISC + 4);
 
@@ -181,24 +199,28 @@ __global__ void __launch_bounds__(224, 1)
     n_ktiles = (Nk + BN - 1) / BN;
     if (qidx >= n_qtiles) return;  // the grid covers the longest sequence
   }
-  // Several query tiles per CTA (plain problems only): CTA x takes tiles
-  // G*x .. G*x+G-1 of the zigzag order heaviest, lightest, 2nd heaviest, ...,
-  // so with an even G every CTA has the same causal work, and an item's loads
-  // and first products overlap the previous item's epilogue.
-  // (The fp32 path always runs one item: a constant, so its kernels carry
-  // none of the multi-item code and keep their registers.)
-  const int G = TF32 ? 1 : tc_items(p);
-  auto item_qt = [&](int g) -> int {  // query tile of item g, or -1
-    if (G == 1) return g == 0 ? (CAUSAL ? (n_qtiles - 1 - qidx) : qidx) : -1;
-    const int zi = G * static_cast<int>(blockIdx.x) + g;
-    if (zi >= n_qtiles) return -1;
-    const int qi = (zi & 1) ? n_qtiles - 1 - (zi >> 1) : (zi >> 1);
-    return CAUSAL ? (n_qtiles - 1 - qi) : qi;
+  // Persistent schedule (plain problems, 16-bit types): the grid has about
+  // one CTA per SM, and CTA x runs the query tiles fwd_item() deals it, of
+  // any heads, one after another through one pipeline, so an item's loads
+  // and first products overlap the previous item's epilogue and the CTA's
+  // set-up is paid once.  (The fp32 path always runs one item: a constant, so
+  // its kernels carry none of the multi-item code and keep their registers.)
+  const bool persist = !TF32 && p.ctas > 0;
+  // Query tile of this CTA's item g, or -1; *plane = its (batch, head) plane.
+  auto item_qt = [&](int g, int *plane) -> int {
+    if (!persist) {
+      *plane = bh;
+      return g == 0 ? (CAUSAL ? (n_qtiles - 1 - qidx) : qidx) : -1;
+    }
+    return fwd_item(g, static_cast<int>(blockIdx.x), static_cast<int>(gridDim.x), p.planes,
+                    n_qtiles, p.group_heads, plane);
   };
   // Key tiles of query tile t: [kt0, kt0 + n_kt) (top-left causal: keys <=
   // its last row; in split mode chunk `split` of them).
   auto item_nall = [&](int t) { return CAUSAL ? min(t + 1, n_ktiles) : n_ktiles; };
-  const int qt = item_qt(0);
+  int bh0;  // plane of item 0
+  const int qt = item_qt(0, &bh0);
+  if (qt < 0) return;  // no item for this CTA (a persistent grid larger than the work)
   const int q0 = qt * BM;
   // Head dim of the tensors in memory: D, or less when the kernel runs a
   // narrower head dim zero-padded to D (the TMA maps zero-fill the missing
@@ -257,13 +279,14 @@ __global__ void __launch_bounds__(224, 1)
     mbar_init(bQempty, 1);
     mbar_init(bOfree, 128);
 #pragma unroll
-    for (int g = 0; g < kMaxItemsPerCta; ++g) mbar_init(bOstaged + 8 * g, 128);
+    for (int g = 0; g < kItemRing; ++g) mbar_init(bOstaged + 8 * g, 128);
     *abort_flag = 0;
     fence_barrier_init();
     fence_proxy_async_smem();
   }
   if (warp == 4 && lane == 0) {
     if constexpr (!C::QTMEM) tma_prefetch_desc(&tm_q);
+    if (staged) tma_prefetch_desc(&tm_klo);
     tma_prefetch_desc(&tm_k);
     tma_prefetch_desc(&tm_v);
     tma_prefetch_desc(&tm_o);
@@ -289,32 +312,36 @@ __global__ void __launch_bounds__(224, 1)
       // stages O in the V stage of the item's last tile (free once its P V
       // completed).  This thread stores it with TMA, and refills that stage
       // only after the store has read it.
-      int last_v[kMaxItemsPerCta];  // V ring position of each item's last tile
-      int n_items = 0, pend = 0;    // items loaded; next item whose O is stored here
+      int last_v[kItemRing];     // V ring position of item g's last tile, at g % kItemRing
+      int n_items = 0, pend = 0;  // items loaded; next item whose O is stored here
       auto store_o = [&](int gi) -> bool {
-        if (!bounded_wait(bOstaged + 8 * gi, 0, w)) return false;
-        const uint32_t src = sV + (last_v[gi] % C::VST) * C::TILE_BYTES;
+        if (!bounded_wait(bOstaged + 8 * (gi % kItemRing), (gi / kItemRing) & 1, w))
+          return false;
+        const uint32_t src = sV + (last_v[gi % kItemRing] % C::VST) * C::TILE_BYTES;
+        int sp;
+        const int sq = item_qt(gi, &sp);
 #pragma unroll
         for (int c = 0; c < C::NCH; ++c)
           if (c * C::CH_ELEMS < dio)  // a chunk wholly past the row is not stored
-            tma_store_3d(&tm_o, src + c * C::CHUNK_BYTES, c * C::CH_ELEMS, item_qt(gi) * BM, bh);
+            tma_store_3d(&tm_o, src + c * C::CHUNK_BYTES, c * C::CH_ELEMS, sq * BM, sp);
         tma_store_commit();
         tma_store_wait_read_all();
         return true;
       };
-      for (int g = 0; ok && g < G; ++g) {
-        const int tq = item_qt(g);
+      for (int g = 0; ok; ++g) {
+        int gp;  // the item's plane
+        const int tq = item_qt(g, &gp);
         if (tq < 0) break;
-        const int n_all_g = item_nall(tq);
-        const int kt0_g = G == 1 ? kt0 : 0;
-        const int n_kt_g = G == 1 ? n_kt : n_all_g;
+        const int hcg = persist ? gp : hc;
+        const int kt0_g = persist ? 0 : kt0;
+        const int n_kt_g = persist ? item_nall(tq) : n_kt;
         if constexpr (!C::QTMEM) {
           // The Q buffer is free once the previous item's last S has read it.
           if (g > 0 && !(ok = bounded_wait(bQempty, (g - 1) & 1, w))) break;
           mbar_arrive_expect_tx(bQ, C::TILE_BYTES);
 #pragma unroll
           for (int c = 0; c < C::NCH; ++c)
-            tma_load_3d(sQ + c * C::CHUNK_BYTES, &tm_q, bQ, c * C::CH_ELEMS, q_row0 + tq * BM, hc,
+            tma_load_3d(sQ + c * C::CHUNK_BYTES, &tm_q, bQ, c * C::CH_ELEMS, q_row0 + tq * BM, hcg,
                         l2_policy_evict_first());
           ++nq;
         }
@@ -328,11 +355,18 @@ __global__ void __launch_bounds__(224, 1)
             const int s = nk % C::KST, r = nk / C::KST;
             if (r > 0) ok = bounded_wait(bKempty + 8 * s, (r - 1) & 1, w);
             if (!ok) break;
-            mbar_arrive_expect_tx(bKfull + 8 * s, C::TILE_BYTES);
+            // staged fp32: K_hi, and K_lo into the V stage of the same index
+            mbar_arrive_expect_tx(bKfull + 8 * s, staged ? 2 * C::TILE_BYTES : C::TILE_BYTES);
 #pragma unroll
             for (int c = 0; c < C::NCH; ++c)
               tma_load_3d(sK + s * C::TILE_BYTES + c * C::CHUNK_BYTES, &tm_k, bKfull + 8 * s,
-                          c * C::CH_ELEMS, k_row0 + (kt0_g + jk) * BN, hc, pol_kv);
+                          c * C::CH_ELEMS, k_row0 + (kt0_g + jk) * BN, hcg, pol_kv);
+            if (staged) {
+#pragma unroll
+              for (int c = 0; c < C::NCH; ++c)
+                tma_load_3d(sV + s * C::TILE_BYTES + c * C::CHUNK_BYTES, &tm_klo, bKfull + 8 * s,
+                            c * C::CH_ELEMS, k_row0 + (kt0_g + jk) * BN, hcg, pol_kv);
+            }
             ++nk;
           }
           if (j >= 0) {
@@ -342,7 +376,7 @@ __global__ void __launch_bounds__(224, 1)
               break;
             }
             const int s = nv % C::VST, r = nv / C::VST;
-            if (pend < g && last_v[pend] == nv - C::VST) {
+            if (pend < g && last_v[pend % kItemRing] == nv - C::VST) {
               if (!(ok = store_o(pend))) break;  // this stage holds item pend's O
               ++pend;
             }
@@ -355,17 +389,17 @@ __global__ void __launch_bounds__(224, 1)
 #pragma unroll
               for (int c = 0; c < BN / 32; ++c)
                 tma_load_3d(sVT + s * C::TILE_BYTES + c * C::VT_CHUNK_BYTES, &tm_v,
-                            bVfull + 8 * s, (kt0_g + j) * BN + 32 * c, 0, hc, pol_kv);
+                            bVfull + 8 * s, (kt0_g + j) * BN + 32 * c, 0, hcg, pol_kv);
             } else {
 #pragma unroll
               for (int c = 0; c < C::NCH; ++c)
                 tma_load_3d(sV + s * C::TILE_BYTES + c * C::CHUNK_BYTES, &tm_v, bVfull + 8 * s,
-                            c * C::CH_ELEMS, k_row0 + (kt0_g + j) * BN, hc, pol_kv);
+                            c * C::CH_ELEMS, k_row0 + (kt0_g + j) * BN, hcg, pol_kv);
             }
             ++nv;
           }
         }
-        if (ok) last_v[g] = nv - 1;
+        if (ok) last_v[g % kItemRing] = nv - 1;
         n_items = g + 1;
       }
       // O of the items before the last whose V stage was not refilled.
@@ -398,10 +432,11 @@ __global__ void __launch_bounds__(224, 1)
       int b = 0, bph = 0;   // score buffer of the next S and the parity of its use
       int s = 0, sph = 0;   // K stage of the next S and its parity
       int ns = 0;           // S products issued (all items)
-      for (int g = 0; ok && g < G; ++g) {
-      const int tq = item_qt(g);
+      for (int g = 0; ok; ++g) {
+      int gp;
+      const int tq = item_qt(g, &gp);
       if (tq < 0) break;
-      const int n_kt_g = G == 1 ? n_kt : item_nall(tq);
+      const int n_kt_g = persist ? item_nall(tq) : n_kt;
       // Q of item g in place (TMEM or shared memory).
       if (!(ok = bounded_wait(bQ, g & 1, w))) break;
       tc_fence_after();
@@ -412,17 +447,27 @@ __global__ void __launch_bounds__(224, 1)
         tc_fence_after();
         const uint32_t d_tmem = tmem + b * 128;
         const uint32_t kb = sK + s * C::TILE_BYTES;
+        // fp32: K_lo of this tile (see TcCfg::NKLO)
+        const uint32_t klo = staged ? sV + s * C::TILE_BYTES : C::NKLO ? sKLO : sVT;
 #pragma unroll
         for (int kk = 0; kk < D / C::UK; ++kk) {
           // 32 bytes of K per UMMA (4 steps per 128-byte swizzle chunk); the
           // matching Q slice is 8 TMEM columns or the same 32 bytes of Q.
           const uint32_t off = (kk >> 2) * C::CHUNK_BYTES + (kk & 3) * 32;
-          if constexpr (C::QTMEM)
+          if constexpr (TF32) {
+            // Q_hi K_hi + Q_hi K_lo + Q_lo K_hi
+            const uint64_t khi = sdesc_sw128(kb + off, 16, 1024);
+            umma_ts<TF32>(d_tmem, tmem + C::COL_Q + kk * 8, khi, idesc_qk, kk > 0 ? 1u : 0u);
+            umma_ts<TF32>(d_tmem, tmem + C::COL_Q + kk * 8, sdesc_sw128(klo + off, 16, 1024),
+                          idesc_qk, 1u);
+            umma_ts<TF32>(d_tmem, tmem + C::COL_QLO + kk * 8, khi, idesc_qk, 1u);
+          } else if constexpr (C::QTMEM) {
             umma_ts<TF32>(d_tmem, tmem + C::COL_Q + kk * 8, sdesc_sw128(kb + off, 16, 1024),
                           idesc_qk, kk > 0 ? 1u : 0u);
-          else
+          } else {
             umma_ss<TF32>(d_tmem, sdesc_sw128(sQ + off, 16, 1024),
                           sdesc_sw128(kb + off, 16, 1024), idesc_qk, kk > 0 ? 1u : 0u);
+          }
         }
         tc_commit(bKempty + 8 * s);
         tc_commit(bSfull + 8 * b);
@@ -449,10 +494,11 @@ __global__ void __launch_bounds__(224, 1)
       bool ok = true;
       int b = 0, bph = 0;   // score buffer of the next P V and the parity of its use
       int s = 0, sph = 0;   // V stage of the next P V and its parity
-      for (int g = 0; ok && g < G; ++g) {
-      const int tq = item_qt(g);
+      for (int g = 0; ok; ++g) {
+      int gp;
+      const int tq = item_qt(g, &gp);
       if (tq < 0) break;
-      const int n_kt_g = G == 1 ? n_kt : item_nall(tq);
+      const int n_kt_g = persist ? item_nall(tq) : n_kt;
       // O of the previous item has been read out by the epilogue.
       if (g > 0) {
         if (!(ok = bounded_wait(bOfree, (g - 1) & 1, w))) break;
@@ -504,25 +550,33 @@ __global__ void __launch_bounds__(224, 1)
     float l = 0.f;
     bool ok = true;
 
-    // fp32 path: round this thread's row r of K tile t (stage t % KST) to
-    // tf32 in place, then release it to the UMMA issuer.  Row r occupies 16
-    // 16-byte units of the 128-byte-swizzled tile (2 chunks of 32 elements).
-    auto round_k_row = [&](int t) -> bool {
+    // fp32 path: split this thread's row r of K tile t (stage t % KST) into
+    // K_hi = tf32(k), written in place, and K_lo = tf32(k - K_hi), written at
+    // the same place of the K_lo buffer; then release both to the UMMA
+    // issuer.  Row r occupies NCH * 8 16-byte units of the 128-byte-swizzled
+    // tile.  The K_lo buffer must be free: S_{t-1} has completed (D = 64), or
+    // P_{t-1} V_{t-1} has, whose V^T it shares (D = 128).
+    auto split_k_row = [&](int t) -> bool {
       const int s = t % C::KST;
       if (!__all_sync(kFull, bounded_wait(bKfull + 8 * s, (t / C::KST) & 1, w))) return false;
       uint8_t *kt = smem + C::OFF_K + s * C::TILE_BYTES;
+      uint8_t *kl = smem + (C::NKLO ? C::OFF_KLO : C::OFF_VT);
 #pragma unroll
       for (int ch = 0; ch < C::NCH; ++ch) {
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
-          uint4 *ptr = reinterpret_cast<uint4 *>(kt + ch * C::CHUNK_BYTES + r * 128 +
-                                                 ((u ^ (r & 7)) << 4));
-          uint4 val = *ptr;
-          val.x = to_tf32(__uint_as_float(val.x));
-          val.y = to_tf32(__uint_as_float(val.y));
-          val.z = to_tf32(__uint_as_float(val.z));
-          val.w = to_tf32(__uint_as_float(val.w));
-          *ptr = val;
+          const int off = ch * C::CHUNK_BYTES + r * 128 + ((u ^ (r & 7)) << 4);
+          uint4 *ptr = reinterpret_cast<uint4 *>(kt + off);
+          const uint4 val = *ptr;
+          const uint32_t e[4] = {val.x, val.y, val.z, val.w};
+          uint32_t hi[4], lo[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            hi[i] = to_tf32(__uint_as_float(e[i]));
+            lo[i] = to_tf32(__uint_as_float(e[i]) - __uint_as_float(hi[i]));
+          }
+          *ptr = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+          *reinterpret_cast<uint4 *>(kl + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
         }
       }
       fence_proxy_async_smem();
@@ -563,12 +617,12 @@ __global__ void __launch_bounds__(224, 1)
     // Q row -> tensor memory (A operand layout: lane = row, 32-bit column c
     // holds bf16 elements 2c, 2c+1, or one tf32 element).  Rows past Nq are 0.
     // (Otherwise the producer loads Q into shared memory with TMA.)
-    auto stage_q = [&](int tq) {
+    auto stage_q = [&](int tq, int plane) {
       const int qrow = tq * BM + r;
       const bool in = qrow < Nq;
       const uint4 *src = reinterpret_cast<const uint4 *>(
           static_cast<const uint8_t *>(p.q) +
-          (hc * p.q_head_stride + (q_row0 + (in ? qrow : 0)) * p.q_row_stride) * C::ESZ);
+          (plane * p.q_head_stride + (q_row0 + (in ? qrow : 0)) * p.q_row_stride) * C::ESZ);
 #pragma unroll
       for (int blk = 0; blk < C::Q_COLS / 32; ++blk) {
         uint32_t wq[32];
@@ -582,8 +636,16 @@ __global__ void __launch_bounds__(224, 1)
           wq[4 * u + 3] = val.w;
         }
         if constexpr (TF32) {
+          // Q_hi = tf32(q) and Q_lo = tf32(q - Q_hi), the A operands of the
+          // split S product
+          uint32_t wl[32];
 #pragma unroll
-          for (int i = 0; i < 32; ++i) wq[i] = to_tf32(__uint_as_float(wq[i]));
+          for (int i = 0; i < 32; ++i) {
+            const float x = __uint_as_float(wq[i]);
+            wq[i] = to_tf32(x);
+            wl[i] = to_tf32(x - __uint_as_float(wq[i]));
+          }
+          tmem_st32(tmem + lane_off + C::COL_QLO + blk * 32, wl);
         }
         tmem_st32(tmem + lane_off + C::COL_Q + blk * 32, wq);
       }
@@ -591,29 +653,30 @@ __global__ void __launch_bounds__(224, 1)
       tc_fence_before();
       mbar_arrive(bQ);
     };
-    if constexpr (C::QTMEM) stage_q(qt);
-    if (TF32 && !staged) ok = round_k_row(0);
+    if constexpr (C::QTMEM) stage_q(qt, persist ? bh0 : hc);
+    if (TF32 && !staged) ok = split_k_row(0);
 
     int buf = 0, bph = 0;            // score buffer of tile j and the parity of its use
     int pbuf = C::NS - 1, pbph = 1;  // the same for tile j - 1
     int tiles_done = 0;              // key tiles of all items so far (= V ring position)
-    for (int g = 0; g < G; ++g) {
-    const int tq = item_qt(g);
+    for (int g = 0;; ++g) {
+    int gp;  // the item's plane
+    const int tq = item_qt(g, &gp);
     if (tq < 0) break;
-    const int n_kt_g = G == 1 ? n_kt : item_nall(tq);
+    const int n_kt_g = persist ? item_nall(tq) : n_kt;
     row = tq * BM + r;
     row_lim = CAUSAL ? min(row + 1, Nk) : Nk;
     m_used = -INFINITY;
     l = 0.f;
     for (int j = 0; ok && j < n_kt_g; ++j) {
-      if (TF32 && !staged) {
-        // the next K tile is rounded before this tile's softmax so that
-        // S_{j+1} = Q K_{j+1}^T still overlaps it
-        if (j + 1 < n_kt_g && !(ok = round_k_row(j + 1))) break;
-      }
       ok = __all_sync(kFull, bounded_wait(bSfull + 8 * buf, bph, w));
       if (!ok) break;
       tc_fence_after();
+      if (TF32 && !staged && C::NKLO && j + 1 < n_kt_g) {
+        // S_j has completed, so its K_lo buffer is free: the next K tile is
+        // split before this tile's softmax so that S_{j+1} overlaps it
+        if (!(ok = split_k_row(j + 1))) break;
+      }
       const uint32_t s_tm = tmem + lane_off + buf * 128;
       uint32_t sr[4][32];
       tmem_ld32(s_tm + 0, sr[0]);
@@ -722,18 +785,23 @@ __global__ void __launch_bounds__(224, 1)
         l += (a0 + a1) + (b0 + b1);
       }
       if (TF32 && !staged) {
-        // V^T buffer j % NVT was last read by P_{j-NVT} V_{j-NVT}.  With two
-        // buffers that completed before S_j was issued; with one (D = 128)
-        // P_{j-1} V_{j-1} may still be running.
-        if (C::NVT == 1 && j > 0) {
-          ok = __all_sync(kFull, bounded_wait(bOdone + 8 * pbuf, pbph, w));
-          if (!ok) break;
-        }
+        // V^T buffer j % NVT was last read by P_{j-NVT} V_{j-NVT}: with two
+        // buffers that completed before S_j was issued (NS = 2); the one
+        // buffer of D = 128 held K_lo_j, free since S_j completed, and
+        // P_{j-1} V_{j-1} completed before S_j was issued (NS = 1).
         if (!(ok = transpose_v_row(j))) break;
       }
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(bPfull + 8 * buf);
+      if (TF32 && !staged && !C::NKLO && j + 1 < n_kt_g) {
+        // D = 128: K_lo_{j+1} goes into the V^T buffer once P_j V_j has read
+        // it (and S_{j+1} could not start before that anyway: one score
+        // buffer)
+        ok = __all_sync(kFull, bounded_wait(bOdone + 8 * buf, bph, w));
+        if (!ok) break;
+        if (!(ok = split_k_row(j + 1))) break;
+      }
       ++tiles_done;
       pbuf = buf;
       pbph = bph;
@@ -742,16 +810,17 @@ __global__ void __launch_bounds__(224, 1)
 
     // Q-in-TMEM: the next item's Q rows go in once this item's S products
     // have read the current ones, so its first S overlaps this epilogue.
+    int np;  // plane of the next item
+    const int tn = item_qt(g + 1, &np);
     if constexpr (C::QTMEM) {
-      const int tn = (g + 1 < G) ? item_qt(g + 1) : -1;
       if (ok && tn >= 0) {
         ok = __all_sync(kFull, bounded_wait(bQempty, g & 1, w));
-        if (ok) stage_q(tn);
+        if (ok) stage_q(tn, np);
       }
     }
 
     // ------------------------------------------------ epilogue
-    const bool last_item = g + 1 >= G || item_qt(g + 1) < 0;
+    const bool last_item = tn < 0;
     // The last P V; its commit also covers every earlier UMMA.
     if (ok)
       ok = __all_sync(kFull, bounded_wait(bOdone + 8 * pbuf, pbph, w));
@@ -874,10 +943,10 @@ __global__ void __launch_bounds__(224, 1)
           }
         }
       }
-      if (row < Nq) p.lse[static_cast<size_t>(bh) * Nq + row] = m_used * kLn2 + logf(l);
+      if (row < Nq) p.lse[static_cast<size_t>(gp) * Nq + row] = m_used * kLn2 + logf(l);
       if (!last_item) {
         fence_proxy_async_smem();
-        mbar_arrive(bOstaged + 8 * g);   // the producer stores this item's O
+        mbar_arrive(bOstaged + 8 * (g % kItemRing));   // the producer stores this item's O
       }
     }
     // O of this item has been read from tensor memory: the next item's
@@ -892,7 +961,7 @@ __global__ void __launch_bounds__(224, 1)
 #pragma unroll
       for (int c = 0; c < C::NCH; ++c)
         if (c * C::CH_ELEMS < dio)  // a chunk wholly past the row is not stored
-          tma_store_3d(&tm_o, sK + c * C::CHUNK_BYTES, c * C::CH_ELEMS, tq * BM, bh);
+          tma_store_3d(&tm_o, sK + c * C::CHUNK_BYTES, c * C::CH_ELEMS, tq * BM, gp);
       tma_store_commit();
       tma_store_wait_read_all();
     }
@@ -900,7 +969,7 @@ __global__ void __launch_bounds__(224, 1)
     // the same abort flag and leave the item loop together.  (Only with
     // several items: with one the check is moot, and as a loop exit it cost
     // the fp32 kernels their last free registers.)
-    if (G > 1 && *abort_flag) break;
+    if (persist && *abort_flag) break;
     }  // items
   }
 
@@ -915,26 +984,27 @@ __global__ void __launch_bounds__(224, 1)
 
 template <int D, bool TF32, bool HALF = false>
 cudaError_t launch_tc(const CUtensorMap &q, const CUtensorMap &k, const CUtensorMap &v,
-                      const CUtensorMap &o, const TcParams &p, int B, int causal,
-                      cudaStream_t stream) {
+                      const CUtensorMap &o, const CUtensorMap &klo, const TcParams &p, int B,
+                      int causal, cudaStream_t stream) {
   using C = TcCfg<D, TF32>;
   void (*kern)(const CUtensorMap, const CUtensorMap, const CUtensorMap, const CUtensorMap,
-               const TcParams) =
+               const CUtensorMap, const TcParams) =
       causal ? fa_tc_fwd_kernel<D, TF32, true, HALF> : fa_tc_fwd_kernel<D, TF32, false, HALF>;
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
-  const int items = tc_items(p);
-  const int gx = items > 1 ? (p.n_qtiles + items - 1) / items : p.n_qtiles * p.n_splits;
-  cfg.gridDim = dim3(static_cast<unsigned>(gx), static_cast<unsigned>(p.H),
-                     static_cast<unsigned>(B));
+  if (p.ctas > 0 && !TF32)
+    cfg.gridDim = dim3(static_cast<unsigned>(p.ctas), 1, 1);  // persistent
+  else
+    cfg.gridDim = dim3(static_cast<unsigned>(p.n_qtiles * p.n_splits), static_cast<unsigned>(p.H),
+                       static_cast<unsigned>(B));
   cfg.blockDim = dim3(C::THREADS, 1, 1);
   cfg.dynamicSmemBytes = C::SMEM_BYTES;
   cfg.stream = stream;
   cfg.attrs = nullptr;
   cfg.numAttrs = 0;
-  return cudaLaunchKernelEx(&cfg, kern, q, k, v, o, p);
+  return cudaLaunchKernelEx(&cfg, kern, q, k, v, o, klo, p);
 }
 
 }  // namespace fa

@@ -5,9 +5,9 @@
 namespace fa {
 
 cudaError_t launch_tc_f16_d64(const CUtensorMap &q, const CUtensorMap &k, const CUtensorMap &v,
-                              const CUtensorMap &o, const TcParams &p, int B, int causal,
-                              cudaStream_t s) {
-  return launch_tc<64, false, true>(q, k, v, o, p, B, causal, s);
+                              const CUtensorMap &o, const CUtensorMap &klo, const TcParams &p,
+                              int B, int causal, cudaStream_t s) {
+  return launch_tc<64, false, true>(q, k, v, o, klo, p, B, causal, s);
 }
 
 }  // namespace fa

@@ -30,7 +30,8 @@ FA_DTYPE_F32_SIMT = 2
 FA_DTYPE_F16 = 3
 
 EXPORTED = ("fa_fwd", "fa_fwd_host", "fa_fwd_status", "fa_status_string", "fa_version",
-            "fa_set_test_hooks", "fa_set_items_per_cta", "fa_items_per_cta", "fa_fwd_noalloc",
+            "fa_set_test_hooks", "fa_set_fwd_schedule", "fa_fwd_schedule", "fa_fwd_schedule_covers",
+            "fa_fwd_noalloc",
             "fa_fwd_splitkv", "fa_fwd_splitkv_workspace",
             "fa_fwd_varlen", "fa_bwd", "fa_bwd_workspace", "fa_fwd_staged",
             "fa_fwd_staged_workspace", "fa_bwd_varlen", "fa_bwd_varlen_workspace")
@@ -92,10 +93,12 @@ def load(path: str | None = None):
     lib.fa_version.restype = i
     lib.fa_set_test_hooks.argtypes = [i, ctypes.c_ulonglong]
     lib.fa_set_test_hooks.restype = i
-    lib.fa_set_items_per_cta.argtypes = [i]
-    lib.fa_set_items_per_cta.restype = i
-    lib.fa_items_per_cta.argtypes = [i] * 8
-    lib.fa_items_per_cta.restype = i
+    lib.fa_set_fwd_schedule.argtypes = [i, i]
+    lib.fa_set_fwd_schedule.restype = i
+    lib.fa_fwd_schedule.argtypes = [i] * 7 + [ctypes.POINTER(i)] * 2
+    lib.fa_fwd_schedule.restype = i
+    lib.fa_fwd_schedule_covers.argtypes = [i] * 4
+    lib.fa_fwd_schedule_covers.restype = i
     if path is None:
         _lib = lib
     return lib
@@ -298,16 +301,25 @@ def fa_set_test_hooks(skip_v_load: int = 0, wait_limit_ns: int = 0) -> int:
     return load().fa_set_test_hooks(int(skip_v_load), int(wait_limit_ns))
 
 
-def fa_set_items_per_cta(n: int = 0) -> int:
-    """Testing aid: query tiles per CTA of the 16-bit forward (0 = automatic)."""
-    return load().fa_set_items_per_cta(int(n))
+def fa_set_fwd_schedule(ctas: int = 0, group_heads: int = 0) -> int:
+    """Testing aid: CTAs and planes per group of the 16-bit forward's
+    persistent grid (0 = automatic)."""
+    return load().fa_set_fwd_schedule(int(ctas), int(group_heads))
 
 
-def fa_items_per_cta(B: int, H: int, Nq: int, Nk: int, d: int, causal: bool, dtype: int,
-                     num_sms: int) -> int:
-    """The automatic query tiles per CTA of fa_fwd on a GPU with num_sms SMs."""
-    return load().fa_items_per_cta(int(B), int(H), int(Nq), int(Nk), int(d), int(bool(causal)),
-                                   int(dtype), int(num_sms))
+def fa_fwd_schedule(B: int, H: int, Nq: int, Nk: int, d: int, dtype: int, num_sms: int):
+    """(status, CTAs, planes per group) of fa_fwd's persistent schedule on a
+    GPU with num_sms SMs (host-only)."""
+    c, g = ctypes.c_int(0), ctypes.c_int(0)
+    st = load().fa_fwd_schedule(int(B), int(H), int(Nq), int(Nk), int(d), int(dtype),
+                                int(num_sms), ctypes.byref(c), ctypes.byref(g))
+    return st, c.value, g.value
+
+
+def fa_fwd_schedule_covers(planes: int, n_qtiles: int, ctas: int, group_heads: int) -> bool:
+    """Host-only check that the schedule deals every query tile exactly once."""
+    return bool(load().fa_fwd_schedule_covers(int(planes), int(n_qtiles), int(ctas),
+                                              int(group_heads)))
 
 
 # --------------------------------------------------------------- torch helpers

@@ -24,7 +24,9 @@
  *           element (b, h, n, x) of q sits at ((b*H + h)*Nq + n)*d + x.
  * Types:    dtype FA_DTYPE_BF16      q, k, v, o are bf16; fp32 accumulation.
  *           dtype FA_DTYPE_F32       q, k, v, o are fp32; tensor-core TF32
- *                                    products, fp32 accumulation.
+ *                                    products, fp32 accumulation; the
+ *                                    scores as three tf32 products of the
+ *                                    split operands (hi/lo), P and V in tf32.
  *           dtype FA_DTYPE_F32_SIMT  q, k, v, o are fp32; plain fp32 FMA
  *                                    kernel, no tensor cores.
  *           dtype FA_DTYPE_F16       q, k, v, o are fp16; fp32 accumulation
@@ -205,11 +207,12 @@ int fa_fwd_varlen(const void *q, const void *k, const void *v, void *o, float *l
 
 /*
  * fa_fwd_staged — the forward with a caller-provided staging area.  For
- * FA_DTYPE_F32 (tcgen05 kind::tf32) a pre-pass rounds K to tf32 and writes V,
- * rounded and transposed, into the K-major V^T layout the tf32 P V product
- * takes, once per call; the kernel then loads both ready-made instead of
- * every query-tile CTA converting the same tiles again.  Same results as
- * fa_fwd (the same rounding, applied once).  Other dtypes have nothing to
+ * FA_DTYPE_F32 (tcgen05 kind::tf32) a pre-pass splits K into K_hi = tf32(K)
+ * and K_lo = tf32(K - K_hi) and writes V, rounded and transposed, into the
+ * K-major V^T layout the tf32 P V product takes, once per call; the kernel
+ * then loads them ready-made instead of every query-tile CTA converting the
+ * same tiles again.  Same results as fa_fwd (the same roundings, applied
+ * once).  Other dtypes have nothing to
  * stage and run fa_fwd (workspace may then be NULL).
  *
  * Arguments q .. dtype and stream as for fa_fwd.
@@ -225,9 +228,9 @@ int fa_fwd_staged(const void *q, const void *k, const void *v, void *o, float *l
                   int dtype, void *workspace, unsigned long long workspace_bytes,
                   void *stream);
 
-/* Bytes of workspace fa_fwd_staged needs: for FA_DTYPE_F32, B*H*Nk*d floats
- * (K in tf32) plus B*H*d*ceil(Nk/128)*128 floats (V^T), each part rounded up
- * to 256 bytes; 0 for other dtypes and for invalid arguments. */
+/* Bytes of workspace fa_fwd_staged needs: for FA_DTYPE_F32, twice B*H*Nk*d
+ * floats (K_hi and K_lo) plus B*H*d*ceil(Nk/128)*128 floats (V^T), each part
+ * rounded up to 256 bytes; 0 for other dtypes and for invalid arguments. */
 unsigned long long fa_fwd_staged_workspace(int B, int H, int Nk, int d, int dtype);
 
 /*
@@ -347,23 +350,40 @@ int fa_version(void);
 int fa_set_test_hooks(int skip_v_load, unsigned long long wait_limit_ns);
 
 /*
- * fa_set_items_per_cta — testing aid, process-wide; no counterpart on the
+ * fa_set_fwd_schedule — testing aid, process-wide; no counterpart on the
  * pages (a scheduling choice of this implementation).  The bf16/fp16
- * forward of fa_fwd and fa_fwd_noalloc runs n query tiles per CTA, taken in
- * zigzag order (tile x with tile n_qtiles-1-x, ...), instead of its own
- * choice (0 = automatic: 1, 2 or 4, whichever a makespan model of the grid
- * on the SMs rates fastest).  Results do not depend on n: every tile does
- * the same arithmetic.  n in 0..4, else FA_ERR_INVALID_ARG; returns FA_OK.
+ * forward of fa_fwd and fa_fwd_noalloc runs as a persistent grid: about one
+ * CTA per SM, each running the query tiles that the schedule deals it (see
+ * fa_fwd_schedule).  ctas > 0 forces a grid of that many CTAs (at most one
+ * per query tile) and group_heads > 0 the planes per group (at most all);
+ * 0 restores the automatic choice of each.  Results do not depend on either:
+ * every query tile does the same arithmetic wherever it runs.  Returns FA_OK,
+ * or FA_ERR_INVALID_ARG for a negative argument.
  */
-int fa_set_items_per_cta(int n);
+int fa_set_fwd_schedule(int ctas, int group_heads);
 
 /*
- * fa_items_per_cta — the query tiles per CTA fa_fwd would run for this
- * problem on a GPU with num_sms SMs when nothing is forced (1, 2 or 4; 1 for
- * types other than bf16/fp16); a host-only function, for reports and tests.
- * 0 for arguments below 1.
+ * fa_fwd_schedule — the persistent schedule fa_fwd would use for this
+ * problem on a GPU with num_sms SMs; a host-only function, for reports and
+ * tests.  *ctas = CTAs of the grid (0 for dtypes that run one CTA per query
+ * tile), *group_heads = (batch, head) planes per group: the planes are
+ * taken in groups whose K and V stay in L2 together (48 MB), and within a
+ * group the query tiles are dealt heaviest first (the last query tile of
+ * every plane, then the one before, ...), in rounds of *ctas items that go
+ * alternately to CTAs 0, 1, ... and to CTAs ..., 1, 0.  Returns FA_OK, or
+ * FA_ERR_INVALID_ARG for null outputs or sizes below 1.
  */
-int fa_items_per_cta(int B, int H, int Nq, int Nk, int d, int causal, int dtype, int num_sms);
+int fa_fwd_schedule(int B, int H, int Nq, int Nk, int d, int dtype, int num_sms, int *ctas,
+                    int *group_heads);
+
+/*
+ * fa_fwd_schedule_covers — host-only check of that schedule, for tests:
+ * 1 if, for `planes` planes of n_qtiles query tiles on a grid of `ctas` CTAs
+ * with groups of group_heads planes, every query tile is dealt to exactly
+ * one CTA; else 0 (also for sizes below 1, more CTAs than query tiles or
+ * more than 2^24 query tiles).
+ */
+int fa_fwd_schedule_covers(int planes, int n_qtiles, int ctas, int group_heads);
 
 #ifdef __cplusplus
 }

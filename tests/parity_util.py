@@ -43,33 +43,6 @@ def run_oracle(q, k, v, scale, causal):
                            scale, causal)
 
 
-def tf32_tol(q, k, v, scale, causal):
-    """Tolerances of the fp32 tensor-core path for these inputs: the stated
-    ones, widened to what TF32 rounding of the scores implies (the LSE moves
-    by at most the largest score error, O by at most twice that times
-    max|v|, plus P/V rounding) where that is larger."""
-    b = tf32_score_bound(q, k, scale, causal)
-    vmax = float(torch.as_tensor(v).abs().max())
-    return dict(max_lse=max(TOL[DTYPE_F32]["max_lse"], b),
-                max_o=max(TOL[DTYPE_F32]["max_o"], 2 * b * vmax + 1e-3))
-
-
-def tf32_score_bound(q, k, scale, causal):
-    """Worst-case |score error| of the TF32 path: q and k are rounded to
-    nearest tf32 (relative error u = 2^-11 each), so every product q_x*k_x is
-    off by at most (2u + u^2)|q_x k_x|, plus fp32 accumulation; a score moves
-    by at most |scale| * 2^-10 * 1.01 * sum_x |q_x||k_x| (max over allowed
-    pairs), and the log-sum-exp of the scores by no more than that."""
-    import torch as _t
-    qa, ka = _t.as_tensor(q).double().abs(), _t.as_tensor(k).double().abs()
-    dots = qa @ ka.transpose(-1, -2)
-    if causal:
-        Nq, Nk = dots.shape[-2:]
-        allowed = _t.ones(Nq, Nk, dtype=_t.bool).tril()
-        dots = dots.masked_fill(~allowed, 0.0)
-    return float(abs(scale) * 2.0 ** -10 * 1.01 * dots.max())
-
-
 def compare(o, lse, ro, rl, dtype, tag="", tol=None):
     tol = dict(TOL[dtype], **(tol or {}))
     assert np.isfinite(o).all(), f"{tag}: non-finite O (unwritten rows?)"

@@ -166,40 +166,52 @@ def test_varlen_refuses_simt_and_unsupported_dims(lib):
 DO, DQ, DK, DV, WS = 0x800000, 0x900000, 0xA00000, 0xB00000, 0xC00000
 
 
-@pytest.mark.parametrize("shape,causal,dtype,want", [
-    # measured on GB300 (152 SMs): four tiles per CTA wherever the grid keeps
-    # several full waves, two on b2h16, one where fewer CTAs than SMs remain
-    ((8, 32, 8192, 8192, 128), True, fa.FA_DTYPE_BF16, 4),
-    ((4, 16, 8192, 8192, 128), True, fa.FA_DTYPE_BF16, 4),
-    ((2, 16, 8192, 8192, 128), True, fa.FA_DTYPE_BF16, 2),
-    ((3, 16, 8192, 8192, 128), True, fa.FA_DTYPE_BF16, 2),
-    ((4, 16, 8192, 8192, 64), False, fa.FA_DTYPE_F16, 4),
-    ((2, 8, 3001, 3001, 128), True, fa.FA_DTYPE_BF16, 1),
-    ((2, 4, 1024, 1024, 64), True, fa.FA_DTYPE_BF16, 1),
-    ((4, 4, 4096, 4096, 64), False, fa.FA_DTYPE_F32, 1),
-    ((4, 4, 4096, 4096, 64), False, fa.FA_DTYPE_F32_SIMT, 1),
+@pytest.mark.parametrize("shape,dtype,want", [
+    # one CTA per SM while there are more query tiles than SMs; planes per
+    # group: 48 MB of K and V (2 * Nk * d * element size per plane)
+    ((8, 32, 8192, 8192, 128), fa.FA_DTYPE_BF16, (152, 12)),
+    ((2, 8, 3001, 3001, 128), fa.FA_DTYPE_BF16, (152, 16)),
+    ((2, 4, 1024, 1024, 64), fa.FA_DTYPE_BF16, (64, 8)),     # 64 query tiles
+    ((1, 1, 128, 128, 128), fa.FA_DTYPE_F16, (1, 1)),
+    ((4, 16, 8192, 8192, 32), fa.FA_DTYPE_BF16, (152, 24)),  # runs at d = 64
+    ((4, 4, 4096, 4096, 64), fa.FA_DTYPE_F32, (0, 1)),       # one CTA per tile
+    ((4, 4, 4096, 4096, 64), fa.FA_DTYPE_F32_SIMT, (0, 1)),
 ])
-def test_items_per_cta_choice(lib, shape, causal, dtype, want):
-    """The makespan model behind fa_fwd's tiles per CTA (host logic only)."""
+def test_fwd_schedule_choice(lib, shape, dtype, want):
+    """The persistent grid size and head groups of fa_fwd (host logic only)."""
     B, H, Nq, Nk, d = shape
-    assert fa.fa_items_per_cta(B, H, Nq, Nk, d, causal, dtype, 152) == want
+    assert fa.fa_fwd_schedule(B, H, Nq, Nk, d, dtype, 152) == (fa.FA_OK,) + want
 
 
-def test_items_per_cta_choice_edges(lib):
-    assert fa.fa_items_per_cta(0, 1, 128, 128, 64, 0, fa.FA_DTYPE_BF16, 152) == 0
-    assert fa.fa_items_per_cta(1, 1, 128, 128, 64, 0, fa.FA_DTYPE_BF16, 0) == 0
-    # one SM: any count keeps the SM busy; a single tile per head stays 1
-    assert fa.fa_items_per_cta(1, 1, 128, 128, 64, 1, fa.FA_DTYPE_BF16, 1) == 1
-    for sms in (1, 2, 152, 1000):
-        assert fa.fa_items_per_cta(8, 32, 8192, 8192, 128, 1, fa.FA_DTYPE_BF16, sms) in (1, 2, 4)
+def test_fwd_schedule_edges(lib):
+    assert fa.fa_fwd_schedule(0, 1, 128, 128, 64, fa.FA_DTYPE_BF16, 152)[0] == fa.FA_ERR_INVALID_ARG
+    assert fa.fa_fwd_schedule(1, 1, 128, 128, 64, fa.FA_DTYPE_BF16, 0)[0] == fa.FA_ERR_INVALID_ARG
+    assert fa.fa_fwd_schedule(1, 1, 128, 128, 64, fa.FA_DTYPE_BF16, 1) == (fa.FA_OK, 1, 1)
 
 
-def test_items_per_cta_hook_range(lib):
-    """The testing aid takes 0 (automatic) .. 4 and refuses anything else."""
-    for n in (-1, 5, 100):
-        assert fa.fa_set_items_per_cta(n) == fa.FA_ERR_INVALID_ARG
-    for n in (4, 1, 0):
-        assert fa.fa_set_items_per_cta(n) == fa.FA_OK
+@pytest.mark.parametrize("planes,n_qtiles,ctas,group_heads", [
+    (256, 64, 152, 12), (16, 24, 152, 16), (8, 8, 64, 8), (1, 1, 1, 1), (7, 5, 3, 2),
+    (5, 3, 15, 5), (12, 9, 100, 5), (3, 100, 7, 1), (300, 2, 151, 17), (1, 1000, 152, 1),
+])
+def test_fwd_schedule_deals_every_tile_once(lib, planes, n_qtiles, ctas, group_heads):
+    """Every query tile goes to exactly one CTA, whatever the grid and group
+    sizes (the mapping the kernel itself uses, evaluated on the host)."""
+    assert fa.fa_fwd_schedule_covers(planes, n_qtiles, ctas, group_heads)
+
+
+def test_fwd_schedule_covers_rejects_bad_sizes(lib):
+    for args in [(0, 1, 1, 1), (1, 0, 1, 1), (1, 1, 0, 1), (1, 1, 1, 0), (2, 2, 5, 1)]:
+        assert not fa.fa_fwd_schedule_covers(*args)
+
+
+def test_fwd_schedule_hook_range(lib):
+    """The testing aid takes 0 (automatic) or positive counts."""
+    for args in [(-1, 0), (-100, 0), (0, -1), (4, -2)]:
+        assert fa.fa_set_fwd_schedule(*args) == fa.FA_ERR_INVALID_ARG
+    for args in [(4, 0), (1, 3), (0, 0)]:
+        assert fa.fa_set_fwd_schedule(*args) == fa.FA_OK
+    st, ctas, groups = fa.fa_fwd_schedule(8, 32, 8192, 8192, 128, fa.FA_DTYPE_BF16, 152)
+    assert (st, ctas, groups) == (fa.FA_OK, 152, 12)
 
 
 def test_bwd_workspace_size(lib):
@@ -248,13 +260,13 @@ def test_bwd_unsupported_problems(lib, kw):
 
 
 def test_staged_workspace_size(lib):
-    """fp32: B*H*Nk*d + B*H*d*ceil(Nk/128)*128 floats, parts rounded up to 256
-    bytes; other dtypes stage nothing."""
+    """fp32: 2*B*H*Nk*d (K_hi, K_lo) + B*H*d*ceil(Nk/128)*128 (V^T) floats,
+    parts rounded up to 256 bytes; other dtypes stage nothing."""
     up = lambda n: (n + 255) // 256 * 256
     for B, H, Nk, d in [(1, 1, 1, 64), (4, 4, 4096, 64), (2, 3, 300, 128), (1, 2, 77, 32)]:
         pad = (Nk + 127) // 128 * 128
         assert (fa.fa_fwd_staged_workspace(B, H, Nk, d, fa.FA_DTYPE_F32)
-                == up(B * H * Nk * d * 4) + up(B * H * d * pad * 4))
+                == 2 * up(B * H * Nk * d * 4) + up(B * H * d * pad * 4))
     for dt in (fa.FA_DTYPE_BF16, fa.FA_DTYPE_F16, fa.FA_DTYPE_F32_SIMT):
         assert fa.fa_fwd_staged_workspace(1, 1, 128, 64, dt) == 0
     assert fa.fa_fwd_staged_workspace(0, 1, 128, 64, fa.FA_DTYPE_F32) == 0
