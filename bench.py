@@ -439,11 +439,13 @@ def main():
     plain_fwd = not bwd and varlen is None and stage_ws is None and wspace is None
     grid = None
     if plain_fwd:
-        _, ctas, groups = fa.fa_fwd_schedule(
-            w.B, w.H, w.Nq, w.Nk, w.d, w.dtype,
+        _, ctas, groups, block = fa.fa_fwd_schedule(
+            w.B, w.H, w.Nq, w.Nk, w.d, causal, w.dtype,
             torch.cuda.get_device_properties(dev).multi_processor_count)
-        if ctas > 0:
-            grid = {"persistent_ctas": ctas, "planes_per_group": groups}
+        if ctas > 0 and block > 0:
+            grid = {"schedule": "blocked", "ctas": ctas, "items_per_cta": block}
+        elif ctas > 0:
+            grid = {"schedule": "persistent", "ctas": ctas, "planes_per_group": groups}
     value = ws * flops_step * args.steps / (total_ms / 1e3) / 1e12
 
     # End to end through the host-buffer entry point: H2D of q, k, v from

@@ -4,6 +4,11 @@ Each translation unit under ``csrc/`` is compiled in parallel to an object
 file, then linked into ``exact_attention_57_gb300/libfa.so``.  ptxas
 statistics (registers, spills, shared memory) are kept in
 ``exact_attention_57_gb300/_build/ptxas.log``.
+
+``build_library(debug=True)`` builds ``libfa_debug.so`` (objects in
+``_build_debug/``) with ``-DFA_DEBUG``: the kernels then check the index of
+every plain global load and store and report a failed check in the status
+word (bit 32) instead of making the access.
 """
 from __future__ import annotations
 
@@ -19,6 +24,8 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libfa.so")
+BUILD_DEBUG = os.path.join(PKG, "_build_debug")
+LIB_DEBUG = os.path.join(PKG, "libfa_debug.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC",
@@ -43,17 +50,19 @@ def _stale(out: str, deps) -> bool:
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def build_library(force: bool = False, verbose: bool = False) -> str:
-    os.makedirs(BUILD, exist_ok=True)
+def build_library(force: bool = False, verbose: bool = False, debug: bool = False) -> str:
+    build_dir, lib = (BUILD_DEBUG, LIB_DEBUG) if debug else (BUILD, LIB)
+    flags = NVCC_FLAGS + (["-DFA_DEBUG"] if debug else [])
+    os.makedirs(build_dir, exist_ok=True)
     headers = (glob.glob(os.path.join(CSRC, "*.cuh")) + glob.glob(os.path.join(CSRC, "*.h"))
                + glob.glob(os.path.join(INCLUDE, "*.h")))
     srcs = sources()
     objs, procs = [], []
     for src in srcs:
-        obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")
+        obj = os.path.join(build_dir, os.path.basename(src)[:-3] + ".o")
         objs.append(obj)
         if force or _stale(obj, [src] + headers):
-            cmd = [nvcc(), *ARCH, *NVCC_FLAGS, "-c", src, "-o", obj]
+            cmd = [nvcc(), *ARCH, *flags, "-c", src, "-o", obj]
             log = open(obj + ".log", "w")
             procs.append((src, subprocess.Popen(cmd, stdout=log, stderr=subprocess.STDOUT), log))
     failed = []
@@ -62,22 +71,22 @@ def build_library(force: bool = False, verbose: bool = False) -> str:
         log.close()
         if pr.returncode != 0:
             failed.append(src)
-    with open(os.path.join(BUILD, "ptxas.log"), "w") as out:
+    with open(os.path.join(build_dir, "ptxas.log"), "w") as out:
         for obj in objs:
             if os.path.exists(obj + ".log"):
                 out.write(open(obj + ".log").read())
     if failed:
-        msgs = "".join(open(os.path.join(BUILD, os.path.basename(s)[:-3] + ".o.log")).read()
+        msgs = "".join(open(os.path.join(build_dir, os.path.basename(s)[:-3] + ".o.log")).read()
                        for s in failed)
         raise RuntimeError(f"nvcc failed for {failed}:\n{msgs[-6000:]}")
-    if force or _stale(LIB, objs):
-        tmp = LIB + f".tmp{os.getpid()}"
+    if force or _stale(lib, objs):
+        tmp = lib + f".tmp{os.getpid()}"
         cmd = [nvcc(), *ARCH, "-shared", "-o", tmp, *objs, "-lcudart"]
         subprocess.run(cmd, check=True)
-        os.replace(tmp, LIB)
+        os.replace(tmp, lib)
     if verbose:
-        print(open(os.path.join(BUILD, "ptxas.log")).read())
-    return LIB
+        print(open(os.path.join(build_dir, "ptxas.log")).read())
+    return lib
 
 
 def ptxas_summary(log_path: str | None = None) -> str:

@@ -28,6 +28,8 @@ std::atomic<int> g_skip_v_load{0};
 std::atomic<unsigned long long> g_wait_limit_ns{0};
 std::atomic<int> g_force_ctas{0};   // persistent grid size forced by a test (0 = automatic)
 std::atomic<int> g_force_group{0};  // planes per group forced by a test (0 = automatic)
+std::atomic<int> g_force_block{0};  // blocked schedule forced by a test (0 = automatic)
+std::atomic<long long> g_dbg_lse_shrink{0};  // debug build: LSE extent understated by a test
 
 size_t elem_size(int dtype) { return (dtype == FA_DTYPE_BF16 || dtype == FA_DTYPE_F16) ? 2 : 4; }
 
@@ -150,17 +152,81 @@ int sm_count();
 // HBM about once while all of its query tiles run.
 constexpr double kL2GroupBytes = 48.0 * (1 << 20);
 
-// Persistent schedule of the plain 16-bit forward: *ctas CTAs (one per SM, or
-// fewer when there are fewer query tiles; a test can force the count) and
-// *group_heads planes per group of fwd_item.  Other dtypes run one CTA per
-// query tile (*ctas = 0).
-void fwd_schedule(int dtype, int d, long long planes, int n_qtiles, int Nk, int num_sms,
-                  int forced, int forced_group, int *ctas, int *group_heads) {
+// Blocked schedule: items per CTA G in {1, 2, 4} for the one-tile kernel.
+// A CTA's fixed cost (set-up, pipeline fill, its last epilogue) is paid once
+// for its G items, each next item's loads and first products overlap the
+// previous epilogue, and with G >= 2 the zigzag order gives every causal
+// CTA the same work; but fewer, longer CTAs can leave the SMs' last wave part
+// empty.  G minimises a makespan model in units of one key tile's time t:
+//   G >= 2: ceil(CTAs / SMs) * (G * nbar + c)          (equal CTAs)
+//   G = 1:  CTAs * (nbar + c1) / SMs + nbar             (causal: uneven CTAs,
+//           heaviest first; non-causal: as G >= 2 with c1)
+// nbar = mean key tiles per query tile; c and c1 = fixed cost per CTA with
+// and without a following item to hide the epilogue.  Fitted on GB300 at
+// d = 128 (t = 0.77 us, c = 2.0 us, c1 = 3.0 us); a tile's time scales with
+// the head dim, the fixed cost does not.  A G that leaves fewer CTAs than
+// SMs is not taken.
+int blocked_items(int d, int causal, long long planes, int n_qtiles, int n_ktiles, int num_sms) {
+  if (n_qtiles < 1 || n_ktiles < 1 || planes < 1) return 1;
+  const double sms = num_sms > 0 ? num_sms : 1;
+  // key tiles summed over the query tiles of one (batch, head)
+  const double nq = n_qtiles, nk = n_ktiles;
+  const double ksum = !causal ? nq * nk
+                      : (nq <= nk ? nq * (nq + 1) / 2 : nk * (nk + 1) / 2 + (nq - nk) * nk);
+  const double nbar = ksum / nq;
+  const double tile = d <= 64 ? 0.5 : d <= 128 ? 1.0 : 2.0;  // relative key-tile time
+  const double c = 2.6 / tile, c1 = 3.9 / tile;
+  const double qtiles = static_cast<double>(planes) * n_qtiles;
+  double best = causal ? qtiles * (nbar + c1) / sms + nbar
+                       : std::ceil(qtiles / sms) * (nbar + c1);
+  int pick = 1;
+  for (int g = 2; g <= 4 && g <= n_qtiles; g *= 2) {
+    const double ctas = static_cast<double>(planes) * std::ceil(nq / g);
+    if (ctas < sms) break;
+    const double cost = std::ceil(ctas / sms) * (g * nbar + c);
+    if (cost < best) {
+      best = cost;
+      pick = g;
+    }
+  }
+  return pick;
+}
+
+// Waves of items above which the blocked schedule replaces the persistent
+// one.  Measured on GB300 (bf16, causal, d = 128): persistent ran 25% faster
+// on b2h8n3001 (2.5 waves of query tiles) and 3% on b2h16n8192 (13.5 waves);
+// blocked ran 4% faster on b8h32n8192 (108 waves) — the hardware hands out
+// many CTAs as SMs free up, which evens out SMs that run at different speeds,
+// where a fixed assignment waits for the slowest.
+constexpr double kPersistentMaxWaves = 16.0;
+
+// Schedule of the plain 16-bit forward (see fwd_item): *ctas CTAs of a 1-D
+// grid, *group_heads planes per group (persistent), *block_items query
+// tiles per CTA (blocked; 0 = persistent).  A test can force the persistent
+// grid size
+// (forced > 0), its group size (forced_group > 0) or the blocked schedule
+// (forced_block > 0).  Other dtypes run one CTA per query tile (*ctas = 0).
+void fwd_schedule(int dtype, int d, int causal, long long planes, int n_qtiles, int Nk,
+                  int num_sms, int forced, int forced_group, int forced_block, int *ctas,
+                  int *group_heads, int *block_items) {
   *ctas = 0;
   *group_heads = 1;
+  *block_items = 0;
   if (dtype != FA_DTYPE_BF16 && dtype != FA_DTYPE_F16) return;
   const long long items = planes * n_qtiles;
-  long long c = forced > 0 ? forced : (num_sms > 0 ? num_sms : 1);
+  const double sms = num_sms > 0 ? num_sms : 1;
+  int block = forced_block;
+  if (block <= 0 && forced <= 0 && forced_group <= 0 && items > kPersistentMaxWaves * sms)
+    block = blocked_items(d, causal, planes, n_qtiles, (Nk + fa::BN - 1) / fa::BN, num_sms);
+  if (block > 0) {
+    const long long grid = planes * ((n_qtiles + block - 1) / block);
+    if (grid <= 2147483647LL) {
+      *ctas = static_cast<int>(grid);
+      *block_items = block;
+      return;
+    }
+  }
+  long long c = forced > 0 ? forced : static_cast<long long>(sms);
   if (c > items) c = items;
   *ctas = static_cast<int>(c);
   const double kv = 2.0 * Nk * (d < 64 ? 64 : d) * static_cast<double>(elem_size(dtype));
@@ -202,6 +268,15 @@ cudaError_t launch_tc_any(const CUtensorMap &mq, const CUtensorMap &mk, const CU
                  : fa::launch_tc_f32_d128(mq, mk, mv, mo, ml, p, B, causal, s);
 }
 
+// Extents of Q (= O) and LSE for the debug build's index checks: `rows`
+// query rows of d elements.  A test can understate the LSE extent
+// (fa_set_debug_lse_shrink) to make the checks fire without any access
+// leaving the buffers.
+void set_extents(fa::TcParams *p, long long rows, int d) {
+  p->q_elems = rows * d;
+  p->lse_elems = rows - g_dbg_lse_shrink.load();
+}
+
 // The tensor-core kernels take |scale| * log2(e) > 0 and apply a negative
 // scale by negating Q inside the S = Q K^T product.  A zero scale becomes
 // 1e-30: for scores below 1e20 in magnitude every exponent is then below
@@ -228,6 +303,7 @@ int fwd_enqueue(unsigned *status, const void *q, const void *k, const void *v, v
     p.o = static_cast<float *>(o);
     p.lse = lse;
     p.status = status;
+    p.B = B;
     p.H = H;
     p.Nq = Nq;
     p.Nk = Nk;
@@ -253,6 +329,7 @@ int fwd_enqueue(unsigned *status, const void *q, const void *k, const void *v, v
   p.q_head_stride = static_cast<long long>(Nq) * d;
   p.q_row_stride = d;
   p.lse_head_stride = Nq;
+  set_extents(&p, static_cast<long long>(B) * H * Nq, d);
   p.lse = lse;
   p.status = status;
   p.H = H;
@@ -265,8 +342,9 @@ int fwd_enqueue(unsigned *status, const void *q, const void *k, const void *v, v
   p.wait_limit_ns = lim ? lim : fa::kDefaultWaitLimitNs;
   p.skip_v_load = g_skip_v_load.load();
   p.planes = BH;
-  fwd_schedule(dtype, d, BH, p.n_qtiles, Nk, sm_count(), g_force_ctas.load(),
-               g_force_group.load(), &p.ctas, &p.group_heads);
+  fwd_schedule(dtype, d, causal, BH, p.n_qtiles, Nk, sm_count(), g_force_ctas.load(),
+               g_force_group.load(), g_force_block.load(), &p.ctas, &p.group_heads,
+               &p.block_items);
 
   cudaError_t e = launch_tc_any(mq, mk, mv, mo, p, B, causal, d, dtype, s);
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
@@ -442,28 +520,34 @@ int fa_set_test_hooks(int skip_v_load, unsigned long long wait_limit_ns) {
   return FA_OK;
 }
 
-int fa_fwd_schedule(int B, int H, int Nq, int Nk, int d, int dtype, int num_sms, int *ctas,
-                    int *group_heads) {
-  if (!ctas || !group_heads) return FA_ERR_INVALID_ARG;
+int fa_fwd_schedule(int B, int H, int Nq, int Nk, int d, int causal, int dtype, int num_sms,
+                    int *ctas, int *group_heads, int *block_items) {
+  if (!ctas || !group_heads || !block_items) return FA_ERR_INVALID_ARG;
   if (B < 1 || H < 1 || Nq < 1 || Nk < 1 || d < 1 || num_sms < 1) return FA_ERR_INVALID_ARG;
+  if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
   if (static_cast<long long>(B) * H > 2147483647LL) return FA_ERR_INVALID_ARG;
-  fwd_schedule(dtype, d, static_cast<long long>(B) * H, ceil_div(Nq, fa::BM), Nk, num_sms,
-               g_force_ctas.load(), g_force_group.load(), ctas, group_heads);
+  fwd_schedule(dtype, d, causal, static_cast<long long>(B) * H, ceil_div(Nq, fa::BM), Nk, num_sms,
+               g_force_ctas.load(), g_force_group.load(), g_force_block.load(), ctas,
+               group_heads, block_items);
   return FA_OK;
 }
 
-int fa_fwd_schedule_covers(int planes, int n_qtiles, int ctas, int group_heads) {
-  if (planes < 1 || n_qtiles < 1 || ctas < 1 || group_heads < 1) return 0;
-  const long long items = static_cast<long long>(planes) * n_qtiles;
-  if (items > (1LL << 24) || ctas > items) return 0;
+int fa_fwd_schedule_covers(int planes, int n, int ctas, int group_heads, int block_items) {
+  if (planes < 1 || n < 1 || ctas < 1 || group_heads < 1 || block_items < 0) return 0;
+  const long long items = static_cast<long long>(planes) * n;
+  if (items > (1LL << 24)) return 0;
+  if (block_items == 0 && ctas > items) return 0;
+  if (block_items > 0 &&
+      ctas != static_cast<long long>(planes) * ((n + block_items - 1) / block_items))
+    return 0;
   std::vector<unsigned char> seen(static_cast<size_t>(items), 0);
   for (int c = 0; c < ctas; ++c) {
     for (int k = 0;; ++k) {
       int plane = -1;
-      const int t = fa::fwd_item(k, c, ctas, planes, n_qtiles, group_heads, &plane);
+      const int t = fa::fwd_item(k, c, ctas, planes, n, group_heads, block_items, &plane);
       if (t < 0) break;
-      if (t >= n_qtiles || plane < 0 || plane >= planes) return 0;
-      unsigned char &v = seen[static_cast<size_t>(plane) * n_qtiles + t];
+      if (t >= n || plane < 0 || plane >= planes) return 0;
+      unsigned char &v = seen[static_cast<size_t>(plane) * n + t];
       if (v) return 0;
       v = 1;
     }
@@ -473,10 +557,30 @@ int fa_fwd_schedule_covers(int planes, int n_qtiles, int ctas, int group_heads) 
   return 1;
 }
 
-int fa_set_fwd_schedule(int ctas, int group_heads) {
-  if (ctas < 0 || group_heads < 0) return FA_ERR_INVALID_ARG;
+int fa_debug_build(void) {
+#ifdef FA_DEBUG
+  return 1;
+#else
+  return 0;
+#endif
+}
+
+int fa_set_debug_lse_shrink(long long elems) {
+#ifdef FA_DEBUG
+  if (elems < 0) return FA_ERR_INVALID_ARG;
+  g_dbg_lse_shrink.store(elems);
+  return FA_OK;
+#else
+  (void)elems;
+  return FA_ERR_UNSUPPORTED;
+#endif
+}
+
+int fa_set_fwd_schedule(int ctas, int group_heads, int block_items) {
+  if (ctas < 0 || group_heads < 0 || block_items < 0) return FA_ERR_INVALID_ARG;
   g_force_ctas.store(ctas);
   g_force_group.store(group_heads);
+  g_force_block.store(block_items);
   return FA_OK;
 }
 
@@ -649,6 +753,7 @@ extern "C" int fa_fwd_splitkv(const void *q, const void *k, const void *v, void 
   p.q_head_stride = static_cast<long long>(Nq) * d;
   p.q_row_stride = d;
   p.lse_head_stride = Nq;
+  set_extents(&p, static_cast<long long>(B) * H * Nq, d);
   p.lse = lse;
   p.status = status;
   p.H = H;
@@ -665,7 +770,8 @@ extern "C" int fa_fwd_splitkv(const void *q, const void *k, const void *v, void 
   p.ws_lse = ws_lse;
   cudaError_t e = launch_tc_any(mq, mk, mv, mo, p, B, causal, d, dtype, s);
   if (e != cudaSuccess) return FA_ERR_CUDA;
-  e = fa::launch_splitkv_combine(ws_o, ws_lse, o, lse, BH, Nq, d, n_ktiles, nsp, causal, dtype, s);
+  e = fa::launch_splitkv_combine(ws_o, ws_lse, o, lse, BH, Nq, d, n_ktiles, nsp, causal, dtype,
+                                 status, s);
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
@@ -734,6 +840,7 @@ extern "C" int fa_fwd_varlen(const void *q, const void *k, const void *v, void *
   p.q_head_stride = d;
   p.q_row_stride = static_cast<long long>(H) * d;
   p.lse_head_stride = total_q;
+  set_extents(&p, static_cast<long long>(H) * total_q, d);
   p.cu_q = cu_seqlens_q;
   p.cu_k = cu_seqlens_k;
   p.total_q = total_q;
@@ -838,6 +945,9 @@ extern "C" int fa_bwd(const void *q, const void *k, const void *v, const void *o
   p.d_io = d == 32 ? 32 : 0;
   const unsigned long long lim = g_wait_limit_ns.load();
   p.wait_limit_ns = lim ? lim : fa::kDefaultWaitLimitNs;
+  p.dq_elems = static_cast<long long>(BH) * Nq * static_cast<long long>(bwd_acc_dim(d));
+  p.row_elems = static_cast<long long>(BH) * p.Nq_pad;
+  p.kv_elems = static_cast<long long>(BH) * Nk * d;
   const int half = dtype == FA_DTYPE_F16 ? 1 : 0;
 
   cudaError_t e = fa::launch_bwd_prep(o, dout, lse, lse2, dd, p.dq_acc, BH, Nq, p.Nq_pad, d,
@@ -941,6 +1051,7 @@ extern "C" int fa_fwd_staged(const void *q, const void *k, const void *v, void *
   p.q_head_stride = static_cast<long long>(Nq) * d;
   p.q_row_stride = d;
   p.lse_head_stride = Nq;
+  set_extents(&p, static_cast<long long>(B) * H * Nq, d);
   p.lse = lse;
   p.status = status;
   p.H = H;
@@ -1055,6 +1166,9 @@ extern "C" int fa_bwd_varlen(const void *q, const void *k, const void *v, const 
   p.cu_k = cu_seqlens_k;
   p.total_q = total_q;
   p.total_k = total_k;
+  p.dq_elems = static_cast<long long>(total_q) * H * static_cast<long long>(bwd_acc_dim(d));
+  p.row_elems = static_cast<long long>(H) * B * p.Nq_pad;
+  p.kv_elems = static_cast<long long>(total_k) * H * d;
   const int half = dtype == FA_DTYPE_F16 ? 1 : 0;
 
   cudaError_t e = fa::launch_bwd_prep_varlen(o, dout, lse, lse2, dd, p.dq_acc, cu_seqlens_q, B, H,

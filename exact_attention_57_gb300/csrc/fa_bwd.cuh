@@ -249,7 +249,9 @@ __global__ void __launch_bounds__(512, 1)
             tma_load_3d(sDO + s * C::TILE_BYTES + c * C::CHUNK_BYTES, &tm_do, bar,
                         c * C::CH_ELEMS, q_row0 + q0, hc, pol_q);
           }
-          const size_t roff = row_base + q0;
+          // (debug build: a row block outside the buffers is replaced by
+          // block 0, so the barrier still gets its bytes)
+          const size_t roff = FA_IN(p.status, row_base + q0, 128, p.row_elems) ? row_base + q0 : 0;
           bulk_load(sRow + s * C::ROW_BYTES, p.lse2 + roff, 512, bar);
           bulk_load(sRow + s * C::ROW_BYTES + 512, p.dd + roff, 512, bar);
           ++issued;
@@ -403,7 +405,9 @@ __global__ void __launch_bounds__(512, 1)
           float *dst = p.dq_acc + acc_base + static_cast<size_t>(qbase) * D + r;
 #pragma unroll
           for (int i = 0; i < 64; ++i)
-            if (qbase + i < Nq) red_add(dst + i * D, __uint_as_float(v[i]));
+            if (qbase + i < Nq &&
+                FA_IN(p.status, acc_base + static_cast<size_t>(qbase + i) * D + r, 1, p.dq_elems))
+              red_add(dst + i * D, __uint_as_float(v[i]));
         }
       }
     }
@@ -516,7 +520,8 @@ __global__ void __launch_bounds__(512, 1)
 #pragma unroll
           for (int i = 0; i < 32; ++i) v[i] = 0u;
         }
-        if (key < Nk && c < dio) {
+        if (key < Nk && c < dio &&
+            FA_IN(p.status, kv_base + static_cast<long long>(key) * kv_rs + c, 32, p.kv_elems)) {
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
             uint4 val;

@@ -19,6 +19,28 @@ constexpr unsigned kStatusMma = 2u;
 constexpr unsigned kStatusSoftmax = 4u;
 constexpr unsigned kStatusInjected = 8u;
 constexpr unsigned kStatusSmemLayout = 16u;  // shared memory base not aligned as needed
+constexpr unsigned kStatusBounds = 32u;      // debug build: an index check failed
+
+// Index checks of the debug build (compiled with FA_DEBUG): every plain
+// global load and store of the kernels (those not made by TMA, whose tensor
+// maps bound them already) first checks that elements [first, first+count)
+// lie inside the buffer's `extent` elements; a failed check ORs
+// kStatusBounds into the status word and the access is skipped, so a wrong
+// index shows up in fa_fwd_status instead of faulting the GPU.  The release
+// build compiles the checks away.
+#ifdef FA_DEBUG
+__device__ __forceinline__ bool dbg_in(unsigned *status, long long first, long long count,
+                                       long long extent) {
+  if (first >= 0 && count >= 0 && first + count <= extent) return true;
+  atomicOr(status, kStatusBounds);
+  return false;
+}
+#define FA_IN(status, first, count, extent)                                              \
+  ::fa::dbg_in((status), static_cast<long long>(first), static_cast<long long>(count), \
+               static_cast<long long>(extent))
+#else
+#define FA_IN(status, first, count, extent) true
+#endif
 
 constexpr unsigned long long kDefaultWaitLimitNs = 2000000000ull;  // 2 s
 
@@ -53,40 +75,68 @@ struct TcParams {
   // Head dim of the tensors when narrower than the kernel's D (0 = D): the
   // kernel runs zero-padded to D.
   int d_io = 0;
+  // Elements of Q (= of O) and of LSE, for the debug build's index checks.
+  long long q_elems = 0, lse_elems = 0;
   // fp32 path: K already split into K_hi (tm_k) and K_lo (tm_klo), and tm_v
   // a map over a tf32 V^T ([B*H][d][Nk padded to 128], boxes of 32 keys x D
   // rows).
   int kv_staged = 0;
-  // Persistent schedule (plain problems, 16-bit types): ctas > 0 launches a
-  // grid of that many CTAs, each running the items (query tiles) that
-  // fwd_item() assigns it; planes = B*H; group_heads as in fwd_item().
-  // ctas = 0: one CTA per (query tile, head, batch).
+  // Schedule of the plain problems of the 16-bit types (ctas > 0): a 1-D
+  // grid of `ctas` CTAs, each running the query tiles ("items") fwd_item()
+  // assigns it; planes = B*H; group_heads and block_items as in
+  // fwd_item().  ctas = 0: one CTA per (query tile, head, batch) on a 3-D
+  // grid.
   int ctas = 0;
   int planes = 0;
   int group_heads = 1;
+  int block_items = 0;
 };
 
-// Item k of CTA c of a persistent grid of P CTAs: returns the query tile and
-// sets *plane (the (batch, head) index b*H + h), or returns -1 when the CTA
-// has no k-th item.  Order: the planes in groups of group_heads (a group's
-// K and V are sized to stay in L2 while its query tiles run); within a group,
-// query tile n_qtiles-1 of every plane, then n_qtiles-2, and so on (heaviest
-// first when causal).  Items are dealt in rounds of P, alternately to CTAs
-// 0..P-1 and P-1..0, so the heaviest and lightest items of successive rounds
-// pair up and every CTA gets about the same work.  Every item 0 ..
-// planes*n_qtiles-1 goes to exactly one (CTA, k).
-__host__ __device__ inline int fwd_item(int k, int c, int P, int planes, int n_qtiles,
-                                        int group_heads, int *plane) {
+// Item k of CTA c of a grid of P CTAs, for planes of n items (query tiles)
+// each: returns the item's index within its
+// plane and sets *plane (the (batch, head) index b*H + h), or returns -1
+// when the CTA has no k-th item.  Item n-1 is the heaviest under causal
+// masking (the most key tiles), item 0 the lightest.  Two schedules:
+//
+// block_items = 0, persistent (P is about one CTA per SM): the planes in
+// groups of group_heads (a group's K and V are sized to stay in L2 while its
+// items run); within a group, item n-1 of every plane, then n-2, and so on
+// (heaviest first); dealt in rounds of P, alternately to CTAs 0..P-1 and
+// P-1..0, so the heaviest and lightest items of successive rounds pair up
+// and every CTA gets about the same work.  Suits grids of a few waves, where
+// the last wave's imbalance would otherwise cost most.
+//
+// block_items = G >= 1, blocked (P = planes * ceil(n / G)): CTA c takes G
+// consecutive positions of its plane's zigzag order (heaviest, lightest,
+// next heaviest, ...), so with an even G every causal CTA has the same
+// work; with G = 1 the CTAs of a plane go heaviest first.  CTAs of one plane
+// are adjacent, and the hardware hands CTAs to SMs as they free up, which
+// balances many waves better than any fixed assignment.
+//
+// Either way every item 0 .. planes*n-1 goes to exactly one (CTA, k).
+__host__ __device__ inline int fwd_item(int k, int c, int P, int planes, int n, int group_heads,
+                                        int block_items, int *plane) {
+  if (block_items > 0) {
+    const int nb = (n + block_items - 1) / block_items;  // CTAs per plane
+    if (k >= block_items) return -1;
+    *plane = c / nb;
+    const int x = c - *plane * nb;
+    if (block_items == 1) return n - 1 - x;
+    const int zi = block_items * x + k;
+    if (zi >= n) return -1;
+    const int qi = (zi & 1) ? n - 1 - (zi >> 1) : (zi >> 1);
+    return n - 1 - qi;
+  }
   const long long i = static_cast<long long>(k) * P + ((k & 1) ? P - 1 - c : c);
-  if (i >= static_cast<long long>(planes) * n_qtiles) return -1;
-  const long long gsz = static_cast<long long>(group_heads) * n_qtiles;
+  if (i >= static_cast<long long>(planes) * n) return -1;
+  const long long gsz = static_cast<long long>(group_heads) * n;
   const long long grp = i / gsz;
   const long long r = i - grp * gsz;
   const int h0 = static_cast<int>(grp * group_heads);
   const int hg = planes - h0 < group_heads ? planes - h0 : group_heads;
   const int t = static_cast<int>(r / hg);
   *plane = h0 + static_cast<int>(r - static_cast<long long>(t) * hg);
-  return n_qtiles - 1 - t;
+  return n - 1 - t;
 }
 
 // Ring of per-item state in the forward kernel (O-staged barriers, the
@@ -98,7 +148,7 @@ struct SimtParams {
   const float *q, *k, *v;
   float *o, *lse;
   unsigned *status;
-  int H, Nq, Nk, d;
+  int B, H, Nq, Nk, d;
   int n_qtiles;
   float scale;
   int causal;
@@ -136,7 +186,7 @@ cudaError_t launch_tc_f16_d256(const CUtensorMap &q, const CUtensorMap &k, const
 // Merge of the split-mode chunks into o (dtype: bf16, f16 or f32) and lse.
 cudaError_t launch_splitkv_combine(const float *ws_o, const float *ws_lse, void *o, float *lse,
                                    int BH, int Nq, int d, int n_ktiles, int nsp, int causal,
-                                   int dtype, cudaStream_t s);
+                                   int dtype, unsigned *status, cudaStream_t s);
 
 cudaError_t launch_simt(const SimtParams &p, int B, cudaStream_t s);
 
@@ -165,6 +215,9 @@ struct BwdParams {
   const int *cu_q = nullptr;
   const int *cu_k = nullptr;
   int total_q = 0, total_k = 0;
+  // Elements of dq_acc, of lse2 (= of dd) and of dK (= of dV), for the debug
+  // build's index checks.
+  long long dq_elems = 0, row_elems = 0, kv_elems = 0;
 };
 
 cudaError_t launch_bwd_bf16_d64(const CUtensorMap &q, const CUtensorMap &k, const CUtensorMap &v,

@@ -42,11 +42,16 @@ __global__ void __launch_bounds__(kSimtRows) fa_simt_fwd_kernel(const SimtParams
   const float *qh = p.q + bh * p.Nq * d;
   const float *kh = p.k + bh * p.Nk * d;
   const float *vh = p.v + bh * p.Nk * d;
+  // extents for the debug build's index checks
+  const long long planes = static_cast<long long>(p.B) * p.H;
+  const long long q_elems = planes * p.Nq * d, kv_elems = planes * p.Nk * d;
+  const bool q_ok =
+      active && FA_IN(p.status, static_cast<long long>(bh * p.Nq + row) * d, d, q_elems);
 
   float qr[DP], acc[DP];
 #pragma unroll
   for (int x = 0; x < DP; ++x) {
-    qr[x] = (active && x < d) ? qh[static_cast<size_t>(row) * d + x] : 0.f;
+    qr[x] = (q_ok && x < d) ? qh[static_cast<size_t>(row) * d + x] : 0.f;
     acc[x] = 0.f;
   }
   float m = -INFINITY, l = 0.f;
@@ -60,7 +65,8 @@ __global__ void __launch_bounds__(kSimtRows) fa_simt_fwd_kernel(const SimtParams
     for (int e = threadIdx.x; e < kSimtKeys * DP; e += kSimtRows) {
       const int c = e / DP, x = e % DP;
       const int key = k0 + c;
-      const bool in = key < p.Nk && x < d;
+      const bool in = key < p.Nk && x < d &&
+                      FA_IN(p.status, static_cast<long long>(bh * p.Nk + key) * d + x, 1, kv_elems);
       Ks[e] = in ? kh[static_cast<size_t>(key) * d + x] : 0.f;
       Vs[e] = in ? vh[static_cast<size_t>(key) * d + x] : 0.f;
     }
@@ -95,10 +101,12 @@ __global__ void __launch_bounds__(kSimtRows) fa_simt_fwd_kernel(const SimtParams
   if (active) {
     const float inv_l = 1.f / l;
     float *orow = p.o + (bh * p.Nq + row) * d;
+    if (FA_IN(p.status, static_cast<long long>(bh * p.Nq + row) * d, d, q_elems)) {
 #pragma unroll
-    for (int x = 0; x < DP; ++x)
-      if (x < d) orow[x] = acc[x] * inv_l;
-    p.lse[bh * p.Nq + row] = m + logf(l);
+      for (int x = 0; x < DP; ++x)
+        if (x < d) orow[x] = acc[x] * inv_l;
+    }
+    if (FA_IN(p.status, bh * p.Nq + row, 1, planes * p.Nq)) p.lse[bh * p.Nq + row] = m + logf(l);
   }
 }
 

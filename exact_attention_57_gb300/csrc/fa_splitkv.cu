@@ -37,7 +37,7 @@ template <int D, int OUT>  // OUT: an fa_dtype of the output (bf16, f16 or f32)
 __global__ void __launch_bounds__(32 * kRowsPerBlock)
     fa_splitkv_combine_kernel(const float *__restrict__ ws_o, const float *__restrict__ ws_lse,
                               void *__restrict__ o, float *__restrict__ lse, int BH, int Nq,
-                              int n_ktiles, int nsp, int causal) {
+                              int n_ktiles, int nsp, int causal, unsigned *status) {
   const int lane = threadIdx.x & 31;
   const long long row_g = static_cast<long long>(blockIdx.x) * kRowsPerBlock + (threadIdx.x >> 5);
   if (row_g >= static_cast<long long>(BH) * Nq) return;  // whole warp
@@ -47,9 +47,13 @@ __global__ void __launch_bounds__(32 * kRowsPerBlock)
   const size_t plane = static_cast<size_t>(BH) * Nq;  // rows per chunk
 
   // LSE = log sum_s e^{LSE_s} over the non-empty chunks (at most 64: two per lane).
+  const long long ws_rows = static_cast<long long>(nsp) * plane;  // debug index checks
   float l0 = -INFINITY, l1 = -INFINITY;
-  if (lane < nsp && !chunk_empty(lane, nsp, n_all)) l0 = ws_lse[lane * plane + row_g];
-  if (lane + 32 < nsp && !chunk_empty(lane + 32, nsp, n_all))
+  if (lane < nsp && !chunk_empty(lane, nsp, n_all) &&
+      FA_IN(status, lane * plane + row_g, 1, ws_rows))
+    l0 = ws_lse[lane * plane + row_g];
+  if (lane + 32 < nsp && !chunk_empty(lane + 32, nsp, n_all) &&
+      FA_IN(status, (lane + 32) * plane + row_g, 1, ws_rows))
     l1 = ws_lse[(lane + 32) * plane + row_g];
   float m = fmaxf(l0, l1);
 #pragma unroll
@@ -65,12 +69,14 @@ __global__ void __launch_bounds__(32 * kRowsPerBlock)
   for (int i = 0; i < D / 32; ++i) acc[i] = 0.f;
   for (int s = 0; s < nsp; ++s) {
     if (chunk_empty(s, nsp, n_all)) continue;  // uniform across the warp
+    if (!FA_IN(status, (s * plane + row_g) * D, D, ws_rows * D)) continue;
     const float w = expf(ws_lse[s * plane + row_g] - L);
     const float *src = ws_o + (s * plane + row_g) * D;
 #pragma unroll
     for (int i = 0; i < D / 32; ++i) acc[i] = fmaf(w, src[lane + 32 * i], acc[i]);
   }
   const size_t obase = static_cast<size_t>(row_g) * D;
+  if (!FA_IN(status, obase, D, static_cast<long long>(plane) * D)) return;
 #pragma unroll
   for (int i = 0; i < D / 32; ++i) {
     const size_t idx = obase + lane + 32 * i;
@@ -86,11 +92,12 @@ __global__ void __launch_bounds__(32 * kRowsPerBlock)
 
 template <int D, int OUT>
 cudaError_t launch_combine(const float *ws_o, const float *ws_lse, void *o, float *lse, int BH,
-                           int Nq, int n_ktiles, int nsp, int causal, cudaStream_t s) {
+                           int Nq, int n_ktiles, int nsp, int causal, unsigned *status,
+                           cudaStream_t s) {
   const long long rows = static_cast<long long>(BH) * Nq;
   const unsigned blocks = static_cast<unsigned>((rows + kRowsPerBlock - 1) / kRowsPerBlock);
   fa_splitkv_combine_kernel<D, OUT><<<blocks, 32 * kRowsPerBlock, 0, s>>>(
-      ws_o, ws_lse, o, lse, BH, Nq, n_ktiles, nsp, causal);
+      ws_o, ws_lse, o, lse, BH, Nq, n_ktiles, nsp, causal, status);
   return cudaGetLastError();
 }
 
@@ -98,24 +105,25 @@ cudaError_t launch_combine(const float *ws_o, const float *ws_lse, void *o, floa
 
 template <int D>
 cudaError_t launch_combine_d(const float *ws_o, const float *ws_lse, void *o, float *lse, int BH,
-                             int Nq, int n_ktiles, int nsp, int causal, int dtype, cudaStream_t s) {
+                             int Nq, int n_ktiles, int nsp, int causal, int dtype,
+                             unsigned *status, cudaStream_t s) {
   if (dtype == FA_DTYPE_BF16)
-    return launch_combine<D, FA_DTYPE_BF16>(ws_o, ws_lse, o, lse, BH, Nq, n_ktiles, nsp, causal, s);
+    return launch_combine<D, FA_DTYPE_BF16>(ws_o, ws_lse, o, lse, BH, Nq, n_ktiles, nsp, causal, status, s);
   if (dtype == FA_DTYPE_F16)
-    return launch_combine<D, FA_DTYPE_F16>(ws_o, ws_lse, o, lse, BH, Nq, n_ktiles, nsp, causal, s);
-  return launch_combine<D, FA_DTYPE_F32>(ws_o, ws_lse, o, lse, BH, Nq, n_ktiles, nsp, causal, s);
+    return launch_combine<D, FA_DTYPE_F16>(ws_o, ws_lse, o, lse, BH, Nq, n_ktiles, nsp, causal, status, s);
+  return launch_combine<D, FA_DTYPE_F32>(ws_o, ws_lse, o, lse, BH, Nq, n_ktiles, nsp, causal, status, s);
 }
 
 cudaError_t launch_splitkv_combine(const float *ws_o, const float *ws_lse, void *o, float *lse,
                                    int BH, int Nq, int d, int n_ktiles, int nsp, int causal,
-                                   int dtype, cudaStream_t s) {
+                                   int dtype, unsigned *status, cudaStream_t s) {
   if (d == 32)
-    return launch_combine_d<32>(ws_o, ws_lse, o, lse, BH, Nq, n_ktiles, nsp, causal, dtype, s);
+    return launch_combine_d<32>(ws_o, ws_lse, o, lse, BH, Nq, n_ktiles, nsp, causal, dtype, status, s);
   if (d == 64)
-    return launch_combine_d<64>(ws_o, ws_lse, o, lse, BH, Nq, n_ktiles, nsp, causal, dtype, s);
+    return launch_combine_d<64>(ws_o, ws_lse, o, lse, BH, Nq, n_ktiles, nsp, causal, dtype, status, s);
   if (d == 128)
-    return launch_combine_d<128>(ws_o, ws_lse, o, lse, BH, Nq, n_ktiles, nsp, causal, dtype, s);
-  return launch_combine_d<256>(ws_o, ws_lse, o, lse, BH, Nq, n_ktiles, nsp, causal, dtype, s);
+    return launch_combine_d<128>(ws_o, ws_lse, o, lse, BH, Nq, n_ktiles, nsp, causal, dtype, status, s);
+  return launch_combine_d<256>(ws_o, ws_lse, o, lse, BH, Nq, n_ktiles, nsp, causal, dtype, status, s);
 }
 
 }  // namespace fa

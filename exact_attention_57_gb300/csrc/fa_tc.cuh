@@ -213,7 +213,7 @@ __global__ void __launch_bounds__(224, 1)
       return g == 0 ? (CAUSAL ? (n_qtiles - 1 - qidx) : qidx) : -1;
     }
     return fwd_item(g, static_cast<int>(blockIdx.x), static_cast<int>(gridDim.x), p.planes,
-                    n_qtiles, p.group_heads, plane);
+                    n_qtiles, p.group_heads, p.block_items, plane);
   };
   // Key tiles of query tile t: [kt0, kt0 + n_kt) (top-left causal: keys <=
   // its last row; in split mode chunk `split` of them).
@@ -237,10 +237,13 @@ __global__ void __launch_bounds__(224, 1)
       const int row = q0 + static_cast<int>(threadIdx.x);
       if (row < Nq) {
         const long long gr = q_row0 + row;
-        uint8_t *orow = static_cast<uint8_t *>(p.o) +
-                        (hc * p.q_head_stride + gr * p.q_row_stride) * C::ESZ;
-        for (int x = 0; x < dio * C::ESZ; x += 16) *reinterpret_cast<uint4 *>(orow + x) = make_uint4(0, 0, 0, 0);
-        p.lse[hc * p.lse_head_stride + gr] = -INFINITY;
+        const long long off = hc * p.q_head_stride + gr * p.q_row_stride;
+        uint8_t *orow = static_cast<uint8_t *>(p.o) + off * C::ESZ;
+        if (FA_IN(p.status, off, dio, p.q_elems))
+          for (int x = 0; x < dio * C::ESZ; x += 16)
+            *reinterpret_cast<uint4 *>(orow + x) = make_uint4(0, 0, 0, 0);
+        const long long li = hc * p.lse_head_stride + gr;
+        if (FA_IN(p.status, li, 1, p.lse_elems)) p.lse[li] = -INFINITY;
       }
     }
     return;
@@ -619,10 +622,11 @@ __global__ void __launch_bounds__(224, 1)
     // (Otherwise the producer loads Q into shared memory with TMA.)
     auto stage_q = [&](int tq, int plane) {
       const int qrow = tq * BM + r;
-      const bool in = qrow < Nq;
+      const long long qoff =
+          plane * p.q_head_stride + (q_row0 + (qrow < Nq ? qrow : 0)) * p.q_row_stride;
+      const bool in = qrow < Nq && FA_IN(p.status, qoff, dio, p.q_elems);
       const uint4 *src = reinterpret_cast<const uint4 *>(
-          static_cast<const uint8_t *>(p.q) +
-          (plane * p.q_head_stride + (q_row0 + (in ? qrow : 0)) * p.q_row_stride) * C::ESZ);
+          static_cast<const uint8_t *>(p.q) + qoff * C::ESZ);
 #pragma unroll
       for (int blk = 0; blk < C::Q_COLS / 32; ++blk) {
         uint32_t wq[32];
@@ -837,7 +841,8 @@ __global__ void __launch_bounds__(224, 1)
           tmem_ld32(o_tm + c, o);
           tmem_ld_wait();
           reg_fence32(o);
-          if (row < Nq && c < dio) {
+          if (row < Nq && c < dio &&
+              FA_IN(p.status, prow * dio + c, 32, static_cast<long long>(nsp) * p.lse_elems * dio)) {
             float4 *dst = reinterpret_cast<float4 *>(p.ws_o + prow * dio + c);
 #pragma unroll
             for (int u = 0; u < 8; ++u)
@@ -847,7 +852,8 @@ __global__ void __launch_bounds__(224, 1)
                                    __uint_as_float(o[4 * u + 3]) * inv_l);
           }
         }
-        if (row < Nq) p.ws_lse[prow] = m_used * kLn2 + logf(l);
+        if (row < Nq && FA_IN(p.status, prow, 1, static_cast<long long>(nsp) * p.lse_elems))
+          p.ws_lse[prow] = m_used * kLn2 + logf(l);
       }
     } else if (p.cu_q != nullptr) {
       // Variable-length batches: the rows after this sequence belong to the
@@ -856,15 +862,15 @@ __global__ void __launch_bounds__(224, 1)
         tc_fence_after();
         const float inv_l = 1.f / l;
         const long long gr = q_row0 + row;
-        uint8_t *orow = static_cast<uint8_t *>(p.o) +
-                        (hc * p.q_head_stride + gr * p.q_row_stride) * C::ESZ;
+        const long long off = hc * p.q_head_stride + gr * p.q_row_stride;
+        uint8_t *orow = static_cast<uint8_t *>(p.o) + off * C::ESZ;
 #pragma unroll
         for (int c = 0; c < D; c += 32) {
           uint32_t o[32];
           tmem_ld32(o_tm + c, o);
           tmem_ld_wait();
           reg_fence32(o);
-          if (row < Nq && c < dio) {
+          if (row < Nq && c < dio && FA_IN(p.status, off + c, 32, p.q_elems)) {
             if constexpr (TF32) {
 #pragma unroll
               for (int u = 0; u < 8; ++u)
@@ -889,7 +895,8 @@ __global__ void __launch_bounds__(224, 1)
             }
           }
         }
-        if (row < Nq) p.lse[hc * p.lse_head_stride + gr] = m_used * kLn2 + logf(l);
+        const long long li = hc * p.lse_head_stride + gr;
+        if (row < Nq && FA_IN(p.status, li, 1, p.lse_elems)) p.lse[li] = m_used * kLn2 + logf(l);
       }
     } else if (ok) {
       tc_fence_after();
@@ -943,7 +950,8 @@ __global__ void __launch_bounds__(224, 1)
           }
         }
       }
-      if (row < Nq) p.lse[static_cast<size_t>(gp) * Nq + row] = m_used * kLn2 + logf(l);
+      const long long li = static_cast<long long>(gp) * Nq + row;
+      if (row < Nq && FA_IN(p.status, li, 1, p.lse_elems)) p.lse[li] = m_used * kLn2 + logf(l);
       if (!last_item) {
         fence_proxy_async_smem();
         mbar_arrive(bOstaged + 8 * (g % kItemRing));   // the producer stores this item's O
@@ -956,8 +964,10 @@ __global__ void __launch_bounds__(224, 1)
       mbar_arrive(bOfree);
     }
     fence_proxy_async_smem();
-    named_bar_sync(1, 128);
-    if (last_item && nsp == 1 && p.cu_q == nullptr && threadIdx.x == 0 && *abort_flag == 0) {
+    // All four warps reach this barrier once per item whatever their own
+    // waits gave; the OR over it hands them one decision to go on or stop.
+    const bool stop = named_bar_or(1, 128, !ok || *abort_flag != 0);
+    if (last_item && nsp == 1 && p.cu_q == nullptr && threadIdx.x == 0 && !stop) {
 #pragma unroll
       for (int c = 0; c < C::NCH; ++c)
         if (c * C::CH_ELEMS < dio)  // a chunk wholly past the row is not stored
@@ -965,11 +975,10 @@ __global__ void __launch_bounds__(224, 1)
       tma_store_commit();
       tma_store_wait_read_all();
     }
-    // The four warps have all passed the named barrier above, so they read
-    // the same abort flag and leave the item loop together.  (Only with
-    // several items: with one the check is moot, and as a loop exit it cost
-    // the fp32 kernels their last free registers.)
-    if (persist && *abort_flag) break;
+    // The same `stop` in all four warps: they leave the item loop together.
+    // (Only with several items: with one the check is moot, and as a loop
+    // exit it cost the fp32 kernels their last free registers.)
+    if (persist && stop) break;
     }  // items
   }
 

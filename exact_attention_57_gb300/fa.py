@@ -30,7 +30,8 @@ FA_DTYPE_F32_SIMT = 2
 FA_DTYPE_F16 = 3
 
 EXPORTED = ("fa_fwd", "fa_fwd_host", "fa_fwd_status", "fa_status_string", "fa_version",
-            "fa_set_test_hooks", "fa_set_fwd_schedule", "fa_fwd_schedule", "fa_fwd_schedule_covers",
+            "fa_set_test_hooks", "fa_debug_build", "fa_set_debug_lse_shrink",
+            "fa_set_fwd_schedule", "fa_fwd_schedule", "fa_fwd_schedule_covers",
             "fa_fwd_noalloc",
             "fa_fwd_splitkv", "fa_fwd_splitkv_workspace",
             "fa_fwd_varlen", "fa_bwd", "fa_bwd_workspace", "fa_fwd_staged",
@@ -93,11 +94,15 @@ def load(path: str | None = None):
     lib.fa_version.restype = i
     lib.fa_set_test_hooks.argtypes = [i, ctypes.c_ulonglong]
     lib.fa_set_test_hooks.restype = i
-    lib.fa_set_fwd_schedule.argtypes = [i, i]
+    lib.fa_debug_build.argtypes = []
+    lib.fa_debug_build.restype = i
+    lib.fa_set_debug_lse_shrink.argtypes = [ctypes.c_longlong]
+    lib.fa_set_debug_lse_shrink.restype = i
+    lib.fa_set_fwd_schedule.argtypes = [i, i, i]
     lib.fa_set_fwd_schedule.restype = i
-    lib.fa_fwd_schedule.argtypes = [i] * 7 + [ctypes.POINTER(i)] * 2
+    lib.fa_fwd_schedule.argtypes = [i] * 8 + [ctypes.POINTER(i)] * 3
     lib.fa_fwd_schedule.restype = i
-    lib.fa_fwd_schedule_covers.argtypes = [i] * 4
+    lib.fa_fwd_schedule_covers.argtypes = [i] * 5
     lib.fa_fwd_schedule_covers.restype = i
     if path is None:
         _lib = lib
@@ -301,25 +306,27 @@ def fa_set_test_hooks(skip_v_load: int = 0, wait_limit_ns: int = 0) -> int:
     return load().fa_set_test_hooks(int(skip_v_load), int(wait_limit_ns))
 
 
-def fa_set_fwd_schedule(ctas: int = 0, group_heads: int = 0) -> int:
-    """Testing aid: CTAs and planes per group of the 16-bit forward's
-    persistent grid (0 = automatic)."""
-    return load().fa_set_fwd_schedule(int(ctas), int(group_heads))
+def fa_set_fwd_schedule(ctas: int = 0, group_heads: int = 0, block_items: int = 0) -> int:
+    """Testing aid: force the 16-bit forward's schedule (0 = automatic)."""
+    return load().fa_set_fwd_schedule(int(ctas), int(group_heads), int(block_items))
 
 
-def fa_fwd_schedule(B: int, H: int, Nq: int, Nk: int, d: int, dtype: int, num_sms: int):
-    """(status, CTAs, planes per group) of fa_fwd's persistent schedule on a
-    GPU with num_sms SMs (host-only)."""
-    c, g = ctypes.c_int(0), ctypes.c_int(0)
-    st = load().fa_fwd_schedule(int(B), int(H), int(Nq), int(Nk), int(d), int(dtype),
-                                int(num_sms), ctypes.byref(c), ctypes.byref(g))
-    return st, c.value, g.value
+def fa_fwd_schedule(B: int, H: int, Nq: int, Nk: int, d: int, causal: bool, dtype: int,
+                    num_sms: int):
+    """(status, CTAs, planes per group, items per CTA of the blocked schedule
+    or 0) of fa_fwd's schedule on a GPU with num_sms SMs (host-only)."""
+    c, g, b = ctypes.c_int(0), ctypes.c_int(0), ctypes.c_int(0)
+    st = load().fa_fwd_schedule(int(B), int(H), int(Nq), int(Nk), int(d), int(bool(causal)),
+                                int(dtype), int(num_sms), ctypes.byref(c), ctypes.byref(g),
+                                ctypes.byref(b))
+    return st, c.value, g.value, b.value
 
 
-def fa_fwd_schedule_covers(planes: int, n_qtiles: int, ctas: int, group_heads: int) -> bool:
-    """Host-only check that the schedule deals every query tile exactly once."""
-    return bool(load().fa_fwd_schedule_covers(int(planes), int(n_qtiles), int(ctas),
-                                              int(group_heads)))
+def fa_fwd_schedule_covers(planes: int, n: int, ctas: int, group_heads: int,
+                           block_items: int = 0) -> bool:
+    """Host-only check that the schedule deals every item exactly once."""
+    return bool(load().fa_fwd_schedule_covers(int(planes), int(n), int(ctas), int(group_heads),
+                                              int(block_items)))
 
 
 # --------------------------------------------------------------- torch helpers

@@ -328,7 +328,8 @@ int fa_fwd_host(const void *q_h, const void *k_h, const void *v_h,
  * 0 when every kernel finished normally; otherwise bit r set means a warp of
  * role r gave up on a bounded wait (1 = TMA producer, 2 = MMA issuer,
  * 4 = softmax/epilogue warps, 8 = fault injected by the test hook,
- * 16 = shared memory not aligned as the backward kernel needs).
+ * 16 = shared memory not aligned as the backward kernel needs, 32 = an index
+ * check of the debug build failed and the access was skipped).
  * Returns FA_OK, FA_ERR_DEVICE_TIMEOUT (word != 0) or FA_ERR_CUDA.
  */
 int fa_fwd_status(void *stream, int *device_status);
@@ -350,40 +351,65 @@ int fa_version(void);
 int fa_set_test_hooks(int skip_v_load, unsigned long long wait_limit_ns);
 
 /*
+ * fa_debug_build — 1 for the debug build of the library (libfa_debug.so,
+ * compiled with FA_DEBUG), 0 for the release build.  In the debug build the
+ * kernels check the index of every plain global load and store they make
+ * (the forward, the split-KV merge and the backward gradient kernel; TMA
+ * copies are bounded by their tensor maps) against the buffer's extent: a
+ * failed check skips the access and sets bit 32 in the status word that
+ * fa_fwd_status reports.  No counterpart on the pages.
+ */
+int fa_debug_build(void);
+
+/*
+ * fa_set_debug_lse_shrink — testing aid of the debug build: the LSE extent
+ * the index checks use is understated by `elems` entries (process-wide;
+ * 0 restores it), so a test can see a check fire and the access skipped
+ * without any access leaving a buffer.  Returns FA_OK, FA_ERR_INVALID_ARG
+ * for elems < 0, or FA_ERR_UNSUPPORTED in the release build.
+ */
+int fa_set_debug_lse_shrink(long long elems);
+
+/*
  * fa_set_fwd_schedule — testing aid, process-wide; no counterpart on the
  * pages (a scheduling choice of this implementation).  The bf16/fp16
- * forward of fa_fwd and fa_fwd_noalloc runs as a persistent grid: about one
- * CTA per SM, each running the query tiles that the schedule deals it (see
- * fa_fwd_schedule).  ctas > 0 forces a grid of that many CTAs (at most one
- * per query tile) and group_heads > 0 the planes per group (at most all);
- * 0 restores the automatic choice of each.  Results do not depend on either:
- * every query tile does the same arithmetic wherever it runs.  Returns FA_OK,
- * or FA_ERR_INVALID_ARG for a negative argument.
+ * forward of fa_fwd and fa_fwd_noalloc picks one of two schedules (see
+ * fa_fwd_schedule).  block_items > 0 forces the blocked schedule with that
+ * many items per CTA; otherwise ctas > 0 forces a persistent grid of that
+ * many CTAs (at most one per item) and group_heads > 0 its planes per group
+ * (at most all); zeros restore the automatic choice.  Results do not depend
+ * on the schedule: every query tile does the same arithmetic wherever it
+ * runs.  Returns FA_OK, or FA_ERR_INVALID_ARG for a negative argument.
  */
-int fa_set_fwd_schedule(int ctas, int group_heads);
+int fa_set_fwd_schedule(int ctas, int group_heads, int block_items);
 
 /*
- * fa_fwd_schedule — the persistent schedule fa_fwd would use for this
- * problem on a GPU with num_sms SMs; a host-only function, for reports and
- * tests.  *ctas = CTAs of the grid (0 for dtypes that run one CTA per query
- * tile), *group_heads = (batch, head) planes per group: the planes are
- * taken in groups whose K and V stay in L2 together (48 MB), and within a
- * group the query tiles are dealt heaviest first (the last query tile of
- * every plane, then the one before, ...), in rounds of *ctas items that go
- * alternately to CTAs 0, 1, ... and to CTAs ..., 1, 0.  Returns FA_OK, or
- * FA_ERR_INVALID_ARG for null outputs or sizes below 1.
+ * fa_fwd_schedule — the schedule fa_fwd would use for this problem on a GPU
+ * with num_sms SMs; a host-only function, for reports and tests.  The
+ * 16-bit forward runs a 1-D grid of *ctas CTAs over items (query tiles).
+ *   *block_items = 0, persistent: about one CTA per SM; the planes are
+ *     taken in groups of *group_heads whose K and V stay in L2 together
+ *     (48 MB), within a group the items are dealt heaviest first, in rounds
+ *     of *ctas items that go alternately to CTAs 0, 1, ... and ..., 1, 0.
+ *   *block_items = G > 0, blocked: B*H*ceil(query tiles / G) CTAs, each
+ *     taking G consecutive items of its plane's zigzag order (heaviest,
+ *     lightest, ...), handed to SMs by the hardware as they free up.
+ * The persistent schedule serves grids of up to 16 waves of items, the
+ * blocked one larger grids.  *ctas = 0 for dtypes that run one CTA per
+ * query tile.  Returns FA_OK, or FA_ERR_INVALID_ARG for null outputs, sizes
+ * below 1 or causal not 0/1.
  */
-int fa_fwd_schedule(int B, int H, int Nq, int Nk, int d, int dtype, int num_sms, int *ctas,
-                    int *group_heads);
+int fa_fwd_schedule(int B, int H, int Nq, int Nk, int d, int causal, int dtype, int num_sms,
+                    int *ctas, int *group_heads, int *block_items);
 
 /*
- * fa_fwd_schedule_covers — host-only check of that schedule, for tests:
- * 1 if, for `planes` planes of n_qtiles query tiles on a grid of `ctas` CTAs
- * with groups of group_heads planes, every query tile is dealt to exactly
- * one CTA; else 0 (also for sizes below 1, more CTAs than query tiles or
- * more than 2^24 query tiles).
+ * fa_fwd_schedule_covers — host-only check of those schedules, for tests:
+ * 1 if, for `planes` planes of n items on a grid of `ctas` CTAs (groups of
+ * group_heads planes, block_items as above), every item is dealt to exactly
+ * one CTA; else 0 (also for sizes below 1, a persistent grid with more CTAs
+ * than items, a blocked grid of the wrong size, or more than 2^24 items).
  */
-int fa_fwd_schedule_covers(int planes, int n_qtiles, int ctas, int group_heads);
+int fa_fwd_schedule_covers(int planes, int n, int ctas, int group_heads, int block_items);
 
 #ifdef __cplusplus
 }

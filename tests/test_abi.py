@@ -166,52 +166,69 @@ def test_varlen_refuses_simt_and_unsupported_dims(lib):
 DO, DQ, DK, DV, WS = 0x800000, 0x900000, 0xA00000, 0xB00000, 0xC00000
 
 
-@pytest.mark.parametrize("shape,dtype,want", [
-    # one CTA per SM while there are more query tiles than SMs; planes per
-    # group: 48 MB of K and V (2 * Nk * d * element size per plane)
-    ((8, 32, 8192, 8192, 128), fa.FA_DTYPE_BF16, (152, 12)),
-    ((2, 8, 3001, 3001, 128), fa.FA_DTYPE_BF16, (152, 16)),
-    ((2, 4, 1024, 1024, 64), fa.FA_DTYPE_BF16, (64, 8)),     # 64 query tiles
-    ((1, 1, 128, 128, 128), fa.FA_DTYPE_F16, (1, 1)),
-    ((4, 16, 8192, 8192, 32), fa.FA_DTYPE_BF16, (152, 24)),  # runs at d = 64
-    ((4, 4, 4096, 4096, 64), fa.FA_DTYPE_F32, (0, 1)),       # one CTA per tile
-    ((4, 4, 4096, 4096, 64), fa.FA_DTYPE_F32_SIMT, (0, 1)),
+@pytest.mark.parametrize("shape,causal,dtype,want", [
+    # persistent (up to 16 waves of query tiles): one CTA per SM while there
+    # are more query tiles than SMs; planes per group: 48 MB of K and V
+    # (2 * Nk * d * element size per plane)
+    ((2, 8, 3001, 3001, 128), True, fa.FA_DTYPE_BF16, (152, 16, 0)),
+    ((2, 16, 8192, 8192, 128), True, fa.FA_DTYPE_BF16, (152, 12, 0)),
+    ((2, 4, 1024, 1024, 64), True, fa.FA_DTYPE_BF16, (64, 8, 0)),      # 64 query tiles
+    ((1, 1, 128, 128, 128), False, fa.FA_DTYPE_F16, (1, 1, 0)),
+    # blocked (more than 16 waves): the makespan model's query tiles per CTA
+    ((8, 32, 8192, 8192, 128), True, fa.FA_DTYPE_BF16, (4096, 1, 4)),
+    ((4, 16, 8192, 8192, 128), False, fa.FA_DTYPE_F16, (1024, 1, 4)),
+    ((8, 32, 8192, 8192, 64), True, fa.FA_DTYPE_BF16, (4096, 1, 4)),
+    # one CTA per query tile for the fp32 dtypes
+    ((4, 4, 4096, 4096, 64), False, fa.FA_DTYPE_F32, (0, 1, 0)),
+    ((4, 4, 4096, 4096, 64), False, fa.FA_DTYPE_F32_SIMT, (0, 1, 0)),
 ])
-def test_fwd_schedule_choice(lib, shape, dtype, want):
-    """The persistent grid size and head groups of fa_fwd (host logic only)."""
+def test_fwd_schedule_choice(lib, shape, causal, dtype, want):
+    """The schedule of fa_fwd's 16-bit forward (host logic only)."""
     B, H, Nq, Nk, d = shape
-    assert fa.fa_fwd_schedule(B, H, Nq, Nk, d, dtype, 152) == (fa.FA_OK,) + want
+    assert fa.fa_fwd_schedule(B, H, Nq, Nk, d, causal, dtype, 152) == (fa.FA_OK,) + want
 
 
 def test_fwd_schedule_edges(lib):
-    assert fa.fa_fwd_schedule(0, 1, 128, 128, 64, fa.FA_DTYPE_BF16, 152)[0] == fa.FA_ERR_INVALID_ARG
-    assert fa.fa_fwd_schedule(1, 1, 128, 128, 64, fa.FA_DTYPE_BF16, 0)[0] == fa.FA_ERR_INVALID_ARG
-    assert fa.fa_fwd_schedule(1, 1, 128, 128, 64, fa.FA_DTYPE_BF16, 1) == (fa.FA_OK, 1, 1)
+    bf = fa.FA_DTYPE_BF16
+    assert fa.fa_fwd_schedule(0, 1, 128, 128, 64, 0, bf, 152)[0] == fa.FA_ERR_INVALID_ARG
+    assert fa.fa_fwd_schedule(1, 1, 128, 128, 64, 0, bf, 0)[0] == fa.FA_ERR_INVALID_ARG
+    assert fa.fa_fwd_schedule(1, 1, 128, 128, 128, 1, bf, 1) == (fa.FA_OK, 1, 1, 0)
 
 
-@pytest.mark.parametrize("planes,n_qtiles,ctas,group_heads", [
-    (256, 64, 152, 12), (16, 24, 152, 16), (8, 8, 64, 8), (1, 1, 1, 1), (7, 5, 3, 2),
-    (5, 3, 15, 5), (12, 9, 100, 5), (3, 100, 7, 1), (300, 2, 151, 17), (1, 1000, 152, 1),
+@pytest.mark.parametrize("planes,n,ctas,group_heads,block", [
+    (256, 64, 152, 12, 0), (16, 24, 152, 16, 0), (8, 8, 64, 8, 0), (1, 1, 1, 1, 0),
+    (7, 5, 3, 2, 0), (5, 3, 15, 5, 0), (12, 9, 100, 5, 0), (3, 100, 7, 1, 0), (300, 2, 151, 17, 0),
+    (1, 1000, 152, 1, 0),
+    (256, 64, 4096, 1, 4), (16, 24, 192, 1, 2), (7, 5, 14, 1, 3), (3, 9, 27, 1, 1),
+    (2, 7, 4, 1, 4), (5, 1, 5, 1, 2),
 ])
-def test_fwd_schedule_deals_every_tile_once(lib, planes, n_qtiles, ctas, group_heads):
-    """Every query tile goes to exactly one CTA, whatever the grid and group
-    sizes (the mapping the kernel itself uses, evaluated on the host)."""
-    assert fa.fa_fwd_schedule_covers(planes, n_qtiles, ctas, group_heads)
+def test_fwd_schedule_deals_every_item_once(lib, planes, n, ctas, group_heads, block):
+    """Every item goes to exactly one CTA, whatever the grid, group and block
+    sizes (the mapping the kernels themselves use, evaluated on the host)."""
+    assert fa.fa_fwd_schedule_covers(planes, n, ctas, group_heads, block)
 
 
 def test_fwd_schedule_covers_rejects_bad_sizes(lib):
-    for args in [(0, 1, 1, 1), (1, 0, 1, 1), (1, 1, 0, 1), (1, 1, 1, 0), (2, 2, 5, 1)]:
+    for args in [(0, 1, 1, 1, 0), (1, 0, 1, 1, 0), (1, 1, 0, 1, 0), (1, 1, 1, 0, 0),
+                 (2, 2, 5, 1, 0), (4, 8, 7, 1, 4), (1, 1, 1, 1, -1)]:
         assert not fa.fa_fwd_schedule_covers(*args)
 
 
 def test_fwd_schedule_hook_range(lib):
     """The testing aid takes 0 (automatic) or positive counts."""
-    for args in [(-1, 0), (-100, 0), (0, -1), (4, -2)]:
+    for args in [(-1, 0, 0), (0, -1, 0), (0, 0, -3)]:
         assert fa.fa_set_fwd_schedule(*args) == fa.FA_ERR_INVALID_ARG
-    for args in [(4, 0), (1, 3), (0, 0)]:
-        assert fa.fa_set_fwd_schedule(*args) == fa.FA_OK
-    st, ctas, groups = fa.fa_fwd_schedule(8, 32, 8192, 8192, 128, fa.FA_DTYPE_BF16, 152)
-    assert (st, ctas, groups) == (fa.FA_OK, 152, 12)
+    try:
+        assert fa.fa_set_fwd_schedule(0, 0, 2) == fa.FA_OK
+        assert fa.fa_fwd_schedule(2, 8, 3001, 3001, 128, 1, fa.FA_DTYPE_BF16, 152)[1:] == (
+            16 * 12, 1, 2)
+        assert fa.fa_set_fwd_schedule(7, 3, 0) == fa.FA_OK
+        assert fa.fa_fwd_schedule(8, 32, 8192, 8192, 128, 1, fa.FA_DTYPE_BF16, 152)[1:] == (
+            7, 3, 0)
+    finally:
+        assert fa.fa_set_fwd_schedule(0, 0, 0) == fa.FA_OK
+    st, ctas, groups, block = fa.fa_fwd_schedule(8, 32, 8192, 8192, 128, 1, fa.FA_DTYPE_BF16, 152)
+    assert (st, ctas, groups, block) == (fa.FA_OK, 4096, 1, 4)
 
 
 def test_bwd_workspace_size(lib):

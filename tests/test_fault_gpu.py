@@ -13,9 +13,10 @@ from parity_util import compare, run_gpu, run_oracle
 pytestmark = pytest.mark.gpu
 
 
-def test_starved_kernel_times_out_and_recovers():
+@pytest.mark.parametrize("d", [128, 64])  # the one-tile and the two-tile kernel
+def test_starved_kernel_times_out_and_recovers(d):
     dev = torch.device("cuda:0")
-    q, k, v = (t.to(dev) for t in make_inputs(1, 2, 512, 512, 128, DTYPE_BF16, seed=3))
+    q, k, v = (t.to(dev) for t in make_inputs(1, 2, 512, 512, d, DTYPE_BF16, seed=3))
     stream = torch.cuda.current_stream(dev).cuda_stream
     assert fa.fa_fwd_status(stream)[0] == fa.FA_OK
     try:
@@ -30,6 +31,6 @@ def test_starved_kernel_times_out_and_recovers():
     # the status word was cleared by the read, and the context still works
     assert fa.fa_fwd_status(stream) == (fa.FA_OK, 0)
     qc, kc, vc = (t.cpu() for t in (q, k, v))
-    o, lse = run_gpu(qc, kc, vc, 1 / math.sqrt(128), False, DTYPE_BF16)
-    ro, rl = run_oracle(qc, kc, vc, 1 / math.sqrt(128), False)
+    o, lse = run_gpu(qc, kc, vc, 1 / math.sqrt(d), False, DTYPE_BF16)
+    ro, rl = run_oracle(qc, kc, vc, 1 / math.sqrt(d), False)
     compare(o, lse, ro, rl, DTYPE_BF16, "after timeout")

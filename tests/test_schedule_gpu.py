@@ -23,7 +23,7 @@ pytestmark = pytest.mark.gpu
 @pytest.fixture(autouse=True)
 def automatic_grid_afterwards():
     yield
-    assert fa.fa_set_fwd_schedule(0) == fa.FA_OK
+    assert fa.fa_set_fwd_schedule(0, 0, 0) == fa.FA_OK
 
 
 ONE_PER_TILE = 1 << 30  # clamped to the number of query tiles: one tile per CTA
@@ -54,15 +54,17 @@ def test_grid_size_same_results(case, causal):
     dtype, d, Nq, Nk = case
     q, k, v = make_inputs(2, 3, Nq, Nk, d, dtype, seed=500 + d + Nq + 3 * Nk)
     scale = 1.0 / math.sqrt(d)
-    assert fa.fa_set_fwd_schedule(ONE_PER_TILE) == fa.FA_OK
+    assert fa.fa_set_fwd_schedule(ONE_PER_TILE, 0, 0) == fa.FA_OK
     o1, l1 = run_gpu(q, k, v, scale, causal, dtype)
     ro, rl = run_oracle(q, k, v, scale, causal)
     compare(o1, l1, ro, rl, dtype, f"{_id(case)} causal={causal} one tile per CTA")
-    for ctas, groups in ((1, 0), (2, 1), (3, 0), (7, 2), (0, 1), (0, 0)):
-        assert fa.fa_set_fwd_schedule(ctas, groups) == fa.FA_OK
+    for ctas, groups, block in ((1, 0, 0), (2, 1, 0), (3, 0, 0), (7, 2, 0), (0, 1, 0),
+                                (0, 0, 0), (0, 0, 1), (0, 0, 2), (0, 0, 3), (0, 0, 4)):
+        assert fa.fa_set_fwd_schedule(ctas, groups, block) == fa.FA_OK
         o, lse = run_gpu(q, k, v, scale, causal, dtype)
-        assert np.array_equal(o, o1), f"ctas={ctas} groups={groups}: O differs"
-        assert np.array_equal(lse, l1), f"ctas={ctas} groups={groups}: LSE differs"
+        tag = f"ctas={ctas} groups={groups} block={block}"
+        assert np.array_equal(o, o1), f"{tag}: O differs"
+        assert np.array_equal(lse, l1), f"{tag}: LSE differs"
 
 
 def test_grid_size_many_heads_and_groups():
@@ -70,10 +72,11 @@ def test_grid_size_many_heads_and_groups():
     several rounds per CTA: the automatic grid against one tile per CTA."""
     B, H, N, d = 1, 14, 8192, 128
     q, k, v = make_inputs(B, H, N, N, d, DTYPE_BF16, seed=91)
-    assert fa.fa_fwd_schedule(B, H, N, N, d, DTYPE_BF16, 152)[2] < H
+    assert fa.fa_fwd_schedule(B, H, N, N, d, True, DTYPE_BF16, 152)[2] < H
     outs = []
-    for ctas, groups in ((ONE_PER_TILE, 0), (0, 0), (5, 0), (0, 3)):
-        assert fa.fa_set_fwd_schedule(ctas, groups) == fa.FA_OK
+    for ctas, groups, block in ((ONE_PER_TILE, 0, 0), (0, 0, 0), (5, 0, 0), (0, 3, 0),
+                                (0, 0, 4)):
+        assert fa.fa_set_fwd_schedule(ctas, groups, block) == fa.FA_OK
         outs.append(run_gpu(q, k, v, 1.0 / math.sqrt(d), True, DTYPE_BF16))
     for o, lse in outs[1:]:
         assert np.array_equal(o, outs[0][0]) and np.array_equal(lse, outs[0][1])
@@ -86,8 +89,8 @@ def test_noalloc_with_grid_size():
     q, k, v = (t.to(dev) for t in make_inputs(B, H, N, N, d, DTYPE_BF16, seed=77))
     stream = torch.cuda.current_stream(dev).cuda_stream
     outs = []
-    for ctas in (ONE_PER_TILE, 4):
-        assert fa.fa_set_fwd_schedule(ctas) == fa.FA_OK
+    for ctas, block in ((ONE_PER_TILE, 0), (4, 0), (0, 2)):
+        assert fa.fa_set_fwd_schedule(ctas, 0, block) == fa.FA_OK
         o = torch.full_like(q, float("nan"))
         lse = torch.full((B, H, N), float("nan"), device=dev, dtype=torch.float32)
         st, word = fa.fa_fwd_noalloc(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),

@@ -68,11 +68,14 @@ def test_varlen_matches_oracle(lens_q, lens_k, H, d, dtype, causal):
         compare(go, gl, ro, rl, dtype, f"seq lq={lq} lk={lk} causal={causal}")
 
 
-def test_varlen_equals_fixed_length():
-    """Equal lengths: the packed call matches fa_fwd on [B, H, N, d]."""
+@pytest.mark.parametrize("d,dtype", [(128, DTYPE_BF16), (64, DTYPE_BF16), (64, DTYPE_F16),
+                                     (32, DTYPE_BF16)])
+def test_varlen_equals_fixed_length(d, dtype):
+    """Equal lengths: the packed call matches fa_fwd on [B, H, N, d] bit for
+    bit (the same kernel, run with sequence offsets instead of planes)."""
     dev = torch.device("cuda:0")
-    B, H, N, d = 3, 2, 384, 128
-    q, k, v = (t.to(dev) for t in make_inputs(B, H, N, N, d, DTYPE_BF16, seed=9))
+    B, H, N = 3, 2, 384
+    q, k, v = (t.to(dev) for t in make_inputs(B, H, N, N, d, dtype, seed=9))
     o_ref, l_ref = fa.attention(q, k, v, causal=True)
     tok = lambda t: t.permute(0, 2, 1, 3).reshape(B * N, H, d).contiguous()
     cu = torch.arange(0, (B + 1) * N, N, dtype=torch.int32, device=dev)
