@@ -288,6 +288,8 @@ def main():
                     help="fp32 workloads: time fa_fwd instead of fa_fwd_staged")
     ap.add_argument("--varlen", action="store_true",
                     help="packed variable-length batch through fa_fwd_varlen")
+    ap.add_argument("--no-graph", action="store_true",
+                    help="launch the timed steps one by one instead of replaying a CUDA graph")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
 
@@ -318,6 +320,20 @@ def main():
     v = torch.randn(w.B, w.H, w.Nk, w.d, device=dev, generator=g).to(tdt)
     o = torch.empty_like(q)
     lse = torch.empty(w.B, w.H, w.Nq, device=dev, dtype=torch.float32)
+    # A workload whose tensors fit in L2 gets copies used in turn, together
+    # at least twice the L2 size, so that each step reads its inputs from HBM
+    # as a large one does (no L2 flush between steps is needed either way).
+    l2_bytes = torch.cuda.get_device_properties(dev).L2_cache_size
+    set_bytes = sum(t.numel() * t.element_size() for t in (q, k, v, o, lse))
+    copies = [(q, k, v, o, lse)]
+    if set_bytes < 2 * l2_bytes and not args.varlen and args.which == "fwd":
+        n_copies = min(256, -(-2 * l2_bytes // set_bytes))
+        copies += [tuple(t.clone() for t in (q, k, v, o, lse)) for _ in range(n_copies - 1)]
+    l2_note = ("inputs larger than L2 (no flush)" if len(copies) == 1 and set_bytes >= l2_bytes
+               else f"{len(copies)} copies of the tensors used in turn, together "
+                    f"{len(copies) * set_bytes / 2 ** 20:.0f} MB >= 2x L2 (no flush)"
+               if len(copies) > 1 else "tensors fit in L2: steps after the first may hit L2")
+    turn = [0]  # next copy
     stream = torch.cuda.Stream(device=dev)
     sh = stream.cuda_stream
     impl = "simt" if w.dtype == 2 else "tc"
@@ -354,8 +370,8 @@ def main():
         args.no_e2e = True
         args.no_cpu_baseline = True
     if bwd:
-        if w.dtype not in (0, 3):
-            raise SystemExit("--pass bwd needs a bf16 or fp16 workload")
+        if w.dtype not in (0, 1, 3):
+            raise SystemExit("--pass bwd needs a bf16, fp16 or fp32 workload")
         # forward outputs and upstream gradient, resident before timing
         fa.attention(q, k, v, scale=w.scale, causal=causal, out=o, lse=lse)
         dout = torch.randn(w.B, w.H, w.Nq, w.d, device=dev, generator=g).to(tdt)
@@ -384,17 +400,20 @@ def main():
             if st != fa.FA_OK:
                 raise fa.FaError(st, "fa_bwd")
             return
+        qc, kc, vc, oc, lc = copies[turn[0] % len(copies)]
+        turn[0] += 1
         if stage_ws is not None:
-            st = fa.fa_fwd_staged(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
-                                  lse.data_ptr(), w.B, w.H, w.Nq, w.Nk, w.d, w.scale,
+            st = fa.fa_fwd_staged(qc.data_ptr(), kc.data_ptr(), vc.data_ptr(), oc.data_ptr(),
+                                  lc.data_ptr(), w.B, w.H, w.Nq, w.Nk, w.d, w.scale,
                                   int(causal), w.dtype, stage_ws.data_ptr(), stage_ws.numel(),
                                   sh)
         elif wspace is None:
-            st = fa.fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
-                           w.B, w.H, w.Nq, w.Nk, w.d, w.scale, int(causal), w.dtype, sh)
+            st = fa.fa_fwd(qc.data_ptr(), kc.data_ptr(), vc.data_ptr(), oc.data_ptr(),
+                           lc.data_ptr(), w.B, w.H, w.Nq, w.Nk, w.d, w.scale, int(causal),
+                           w.dtype, sh)
         else:
-            st = fa.fa_fwd_splitkv(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
-                                   lse.data_ptr(), w.B, w.H, w.Nq, w.Nk, w.d, w.scale,
+            st = fa.fa_fwd_splitkv(qc.data_ptr(), kc.data_ptr(), vc.data_ptr(), oc.data_ptr(),
+                                   lc.data_ptr(), w.B, w.H, w.Nq, w.Nk, w.d, w.scale,
                                    int(causal), w.dtype, args.splits, wspace.data_ptr(),
                                    wspace.numel(), sh)
         if st != fa.FA_OK:
@@ -413,26 +432,52 @@ def main():
     st, word = fa.fa_fwd_status(sh)
     if st != fa.FA_OK:
         raise RuntimeError(f"warm-up device status {word}")
+    # The K timed steps are captured once into a CUDA graph on the stream the
+    # library launches on, and the timed region replays it: every kernel of
+    # the K steps runs back to back, with no host launch gap between steps
+    # (which otherwise dominates workloads of a few tens of microseconds).
+    # --no-graph launches the steps one by one instead.
+    graph = None
+    if not args.no_graph:
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            for _ in range(args.steps):
+                step()
+        torch.cuda.synchronize(dev)
     if ws > 1:
         dist.barrier()
     torch.cuda.synchronize(dev)
     ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
     with torch.cuda.stream(stream):
         ev[0].record(stream)
-        for i in range(args.steps):
-            step()
-            ev[i + 1].record(stream)
+        if graph is not None:
+            graph.replay()
+            ev[-1].record(stream)
+        else:
+            for i in range(args.steps):
+                step()
+                ev[i + 1].record(stream)
     stream.synchronize()
     torch.cuda.synchronize(dev)
     if ws > 1:
         dist.barrier()
+    local_ms = ev[0].elapsed_time(ev[-1])
+    total_ms = max_over_ranks(local_ms, dev)
+    ms_per_step = total_ms / args.steps
+    # per-step times (diagnostic, not the value): the same steps launched one
+    # by one, an event between consecutive steps
+    if graph is not None:
+        with torch.cuda.stream(stream):
+            ev[0].record(stream)
+            for i in range(args.steps):
+                step()
+                ev[i + 1].record(stream)
+        stream.synchronize()
     clocks = sampler.stop() if sampler else None
     st, word = fa.fa_fwd_status(sh)
     if st != fa.FA_OK:
         raise RuntimeError(f"timed-region device status {word}")
     launch_ms = [ev[i].elapsed_time(ev[i + 1]) for i in range(args.steps)]
-    total_ms = max_over_ranks(ev[0].elapsed_time(ev[-1]), dev)
-    ms_per_step = total_ms / args.steps
     flops_step = varlen["flops"] if varlen is not None else w.flops(causal) * (2.5 if bwd else 1.0)
     # the persistent grid of the timed forward (fa_fwd's own choice; the
     # other entry points run one CTA per query tile)
@@ -486,12 +531,16 @@ def main():
         return
 
     peaks, peak_src = measured_peaks()
-    avg_launch_ms = sum(launch_ms) / len(launch_ms)
+    # the timed region's average step on this rank (a step is one launch of
+    # the forward kernel; two or three launches for staged, split-KV and
+    # backward steps, where `achieved` is then a lower bound for the main kernel)
+    avg_launch_ms = local_ms / args.steps
     achieved = flops_step / (avg_launch_ms / 1e3) / 1e12
     half_io = w.dtype in (0, 3)   # bf16 / fp16: the same kind::f16 tensor rate
-    simt = w.dtype == 2
-    # SIMT: no tensor cores; the FP32 FMA rate is SMs x 128 lanes x 2 FLOP
+    # SIMT kernels (the plain fp32 forward, every fp32 backward): no tensor
+    # cores; the FP32 FMA rate is SMs x 128 lanes x 2 FLOP
     # per cycle at the maximum SM clock.
+    simt = w.dtype == 2 or (bwd and w.dtype == 1)
     n_sms = torch.cuda.get_device_properties(dev).multi_processor_count
     fma_peak = n_sms * 128 * 2 * float(peaks.get("sm_max_mhz", 2070.0)) * 1e6 / 1e12
     peak = (float(peaks["bf16_tflops"]) if half_io else
@@ -502,7 +551,8 @@ def main():
         # The step's three launches (prep, gradient kernel, dq rounding) are
         # timed together, so `achieved` is a lower bound for the gradient
         # kernel alone; `traffic` is the gradient kernel's.
-        kname = {0: "fa_bwd_kernel<bf16>", 3: "fa_bwd_kernel<f16>"}[w.dtype]
+        kname = {0: "fa_bwd_kernel<bf16>", 1: "fa_bwd_simt_kernel<f32>",
+                 3: "fa_bwd_kernel<f16>"}[w.dtype]
     traffic, traffic_note = profiled_traffic(kname, w.name)
     roofline = {"bound": "alu" if simt else "tensor", "achieved": achieved, "peak": peak,
                 "unit": "TFLOP/s", "frac": achieved / peak, "traffic": traffic,
@@ -535,7 +585,9 @@ def main():
                               {"sequences": len(varlen["lens"]), "total_tokens": varlen["total"],
                                "lengths": "uniform 512..8192 (seeded)", "H": varlen["H"],
                                "d": varlen["d"], "causal": True}),
-                   "l2": "inputs larger than L2 (no flush)"},
+                   "l2": l2_note,
+                   "launch": ("CUDA graph of the timed steps" if graph is not None
+                              else "one by one")},
         "roofline": roofline,
         "pct_of_peak": 100.0 * value / ws / peak,
         "cpu_baseline": cpu,
@@ -543,7 +595,8 @@ def main():
         "gpu_launches": args.steps * (3 if bwd or stage_ws is not None
                                       else 2 if wspace is not None else 1),
         "clocks": clocks,
-        # per step, between consecutive events (the value above is their mean)
+        # per step, the steps launched one by one with an event between
+        # consecutive steps (diagnostic; the value comes from the timed region)
         "step_ms": {"min": min(launch_ms), "median": sorted(launch_ms)[len(launch_ms) // 2],
                     "max": max(launch_ms)},
     }

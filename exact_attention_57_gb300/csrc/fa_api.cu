@@ -909,7 +909,20 @@ extern "C" int fa_bwd(const void *q, const void *k, const void *v, const void *o
     for (int b = a + 1; b < 4; ++b)
       if (overlap(out[a].p, out[a].n, out[b].p, out[b].n)) return FA_ERR_INVALID_ARG;
   }
-  if (dtype != FA_DTYPE_BF16 && dtype != FA_DTYPE_F16) return FA_ERR_UNSUPPORTED;
+  if (dtype == FA_DTYPE_F32 || dtype == FA_DTYPE_F32_SIMT) {
+    // fp32: the CUDA-core backward (head dim up to 128); the workspace
+    // holds D per query row.
+    if (d > 128) return FA_ERR_UNSUPPORTED;
+    unsigned *status = nullptr;
+    if ((rc = device_setup(&status)) != FA_OK) return rc;
+    const cudaError_t e = fa::launch_bwd_simt(
+        static_cast<const float *>(q), static_cast<const float *>(k),
+        static_cast<const float *>(v), static_cast<const float *>(o), lse,
+        static_cast<const float *>(dout), static_cast<float *>(dq), static_cast<float *>(dk),
+        static_cast<float *>(dv), static_cast<float *>(workspace), B, H, Nq, Nk, d, scale, causal,
+        status, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+  }
   // d = 32 runs zero-padded on the d = 64 kernel; dK, dV of d = 256 do not
   // fit in tensor memory.
   if (d != 32 && d != 64 && d != 128) return FA_ERR_UNSUPPORTED;

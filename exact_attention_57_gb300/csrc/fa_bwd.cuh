@@ -557,8 +557,8 @@ cudaError_t launch_bwd(const CUtensorMap &q, const CUtensorMap &k, const CUtenso
   void (*kern)(const CUtensorMap, const CUtensorMap, const CUtensorMap, const CUtensorMap,
                const BwdParams) =
       causal ? fa_bwd_kernel<D, true, HALF> : fa_bwd_kernel<D, false, HALF>;
-  cudaError_t e =
-      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+  static std::atomic<unsigned long long> attr_done[2];  // per causal flag
+  cudaError_t e = smem_attr_once(kern, C::SMEM_BYTES, &attr_done[causal ? 1 : 0]);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(p.n_ktiles), static_cast<unsigned>(p.H),

@@ -2,11 +2,27 @@
 // translation units (not part of the public ABI).
 #pragma once
 
+#include <atomic>
 #include <cstdint>
 #include <cuda.h>
 #include <cuda_runtime.h>
 
 namespace fa {
+
+// The dynamic shared-memory opt-in of a kernel, set once per device: `done`
+// keeps one bit per device (devices past 63 set it on every launch).  Saves a
+// runtime call on every launch of a small problem.
+template <typename Kernel>
+cudaError_t smem_attr_once(Kernel kern, int bytes, std::atomic<unsigned long long> *done) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const unsigned long long bit = (dev >= 0 && dev < 64) ? 1ull << dev : 0ull;
+  if (bit != 0 && (done->load(std::memory_order_acquire) & bit) != 0) return cudaSuccess;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess && bit != 0) done->fetch_or(bit, std::memory_order_release);
+  return e;
+}
 
 // Tile shape of the tensor-core kernels: a query tile is BM rows of one
 // (batch, head); the keys stream in tiles of BN.
@@ -232,6 +248,14 @@ cudaError_t launch_bwd_f16_d64(const CUtensorMap &q, const CUtensorMap &k, const
 cudaError_t launch_bwd_f16_d128(const CUtensorMap &q, const CUtensorMap &k, const CUtensorMap &v,
                                 const CUtensorMap &dout, const BwdParams &p, int B, int causal,
                                 cudaStream_t s);
+
+// fp32 backward on the CUDA cores (FA_DTYPE_F32 and FA_DTYPE_F32_SIMT, head
+// dim 1..128): dd receives D = rowsum(dO * O) per query row (B*H*Nq floats),
+// dq is zeroed and then accumulated with atomics, dk and dv are written.
+cudaError_t launch_bwd_simt(const float *q, const float *k, const float *v, const float *o,
+                            const float *lse, const float *dout, float *dq, float *dk, float *dv,
+                            float *dd, int B, int H, int Nq, int Nk, int d, float scale,
+                            int causal, unsigned *status, cudaStream_t s);
 
 // D = rowsum(dO * O) and LSE * log2(e) per padded row, and dq_acc zeroed.
 cudaError_t launch_bwd_prep(const void *o, const void *dout, const float *lse, float *lse2,

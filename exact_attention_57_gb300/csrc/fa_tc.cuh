@@ -999,8 +999,8 @@ cudaError_t launch_tc(const CUtensorMap &q, const CUtensorMap &k, const CUtensor
   void (*kern)(const CUtensorMap, const CUtensorMap, const CUtensorMap, const CUtensorMap,
                const CUtensorMap, const TcParams) =
       causal ? fa_tc_fwd_kernel<D, TF32, true, HALF> : fa_tc_fwd_kernel<D, TF32, false, HALF>;
-  cudaError_t e =
-      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+  static std::atomic<unsigned long long> attr_done[2];  // per causal flag
+  cudaError_t e = smem_attr_once(kern, C::SMEM_BYTES, &attr_done[causal ? 1 : 0]);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   if (p.ctas > 0 && !TF32)

@@ -206,7 +206,8 @@ def attention_backward(q, k, v, out, lse, dout, scale: float | None = None,
                        stream=None):
     """Gradients (dq, dk, dv) of attention() for the upstream gradient dout.
 
-    q, k, v, dout, out: contiguous bf16 / fp16 CUDA tensors as for attention();
+    q, k, v, dout, out: contiguous bf16 / fp16 / fp32 CUDA tensors as for
+    attention() (fp32 runs the CUDA-core backward, head dim up to 128);
     out and lse are that forward's outputs.  The workspace (fa_bwd_workspace
     bytes) is allocated with torch unless given.  Raises FaError on failure."""
     import torch
@@ -217,7 +218,9 @@ def attention_backward(q, k, v, out, lse, dout, scale: float | None = None,
             raise ValueError("q, k, v, out, dout: contiguous tensors of one dtype")
     if out.shape != q.shape or dout.shape != q.shape or v.shape != k.shape:
         raise ValueError("shape mismatch")
-    code = _dtype_code(q, "tc")
+    # fp32 gradients come from the CUDA-core backward whichever fp32 forward
+    # ran; its dtype code admits every head dim up to 128
+    code = _dtype_code(q, "simt" if q.dtype == torch.float32 else "tc")
     if scale is None:
         scale = 1.0 / math.sqrt(d)
     dq = torch.empty_like(q) if dq is None else dq

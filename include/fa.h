@@ -56,6 +56,15 @@ extern "C" {
 
 #define FA_VERSION 10000 /* 1.0.0 */
 
+/* The library is built with hidden symbol visibility (-fvisibility=hidden);
+ * only the functions declared here are exported, so two builds loaded in one
+ * process (the release and the debug library) share no internal symbols. */
+#if defined(__GNUC__)
+#define FA_API __attribute__((visibility("default")))
+#else
+#define FA_API
+#endif
+
 typedef enum {
     FA_DTYPE_BF16 = 0,
     FA_DTYPE_F32 = 1,
@@ -101,7 +110,7 @@ typedef enum {
  * its internal barriers (a bounded wait, about two seconds) records it in the
  * per-device status word; read it with fa_fwd_status.
  */
-int fa_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
+FA_API int fa_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
            int B, int H, int Nq, int Nk, int d, float scale, int causal,
            int dtype, void *stream);
 
@@ -139,7 +148,7 @@ int fa_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
  * stream before launching; calls whose work overlaps on the GPU (different
  * streams, or another thread) race on that word, so serialise them.
  */
-int fa_fwd_noalloc(const void *q, const void *k, const void *v, void *o, float *lse,
+FA_API int fa_fwd_noalloc(const void *q, const void *k, const void *v, void *o, float *lse,
                    int B, int H, int Nq, int Nk, int d, float scale, int causal,
                    int dtype, void *stream, int *device_status);
 
@@ -168,7 +177,7 @@ int fa_fwd_noalloc(const void *q, const void *k, const void *v, void *o, float *
  * Returns FA_ERR_INVALID_ARG for a missing, misaligned or too small workspace
  * (when num_splits > 1), before anything is enqueued.
  */
-int fa_fwd_splitkv(const void *q, const void *k, const void *v, void *o, float *lse,
+FA_API int fa_fwd_splitkv(const void *q, const void *k, const void *v, void *o, float *lse,
                    int B, int H, int Nq, int Nk, int d, float scale, int causal,
                    int dtype, int num_splits, void *workspace,
                    unsigned long long workspace_bytes, void *stream);
@@ -176,7 +185,7 @@ int fa_fwd_splitkv(const void *q, const void *k, const void *v, void *o, float *
 /* Bytes of workspace fa_fwd_splitkv needs for num_splits chunks (1 .. 64):
  * num_splits * B * H * Nq * (d + 1) floats, each part rounded up to 256
  * bytes.  0 for invalid arguments. */
-unsigned long long fa_fwd_splitkv_workspace(int B, int H, int Nq, int d, int num_splits);
+FA_API unsigned long long fa_fwd_splitkv_workspace(int B, int H, int Nq, int d, int num_splits);
 
 /*
  * fa_fwd_varlen — the forward over a batch of sequences of different lengths
@@ -200,7 +209,7 @@ unsigned long long fa_fwd_splitkv_workspace(int B, int H, int Nq, int d, int num
  * FA_ERR_UNSUPPORTED).  All pointers 16-byte aligned except lse and the
  * offsets (4 bytes).
  */
-int fa_fwd_varlen(const void *q, const void *k, const void *v, void *o, float *lse,
+FA_API int fa_fwd_varlen(const void *q, const void *k, const void *v, void *o, float *lse,
                   const int *cu_seqlens_q, const int *cu_seqlens_k, int B, int H,
                   int total_q, int total_k, int max_seqlen_q, int d, float scale,
                   int causal, int dtype, void *stream);
@@ -223,7 +232,7 @@ int fa_fwd_varlen(const void *q, const void *k, const void *v, void *o, float *l
  * Returns FA_ERR_INVALID_ARG for a missing, misaligned, short or overlapping
  * workspace (fp32), before anything is enqueued.
  */
-int fa_fwd_staged(const void *q, const void *k, const void *v, void *o, float *lse,
+FA_API int fa_fwd_staged(const void *q, const void *k, const void *v, void *o, float *lse,
                   int B, int H, int Nq, int Nk, int d, float scale, int causal,
                   int dtype, void *workspace, unsigned long long workspace_bytes,
                   void *stream);
@@ -231,7 +240,7 @@ int fa_fwd_staged(const void *q, const void *k, const void *v, void *o, float *l
 /* Bytes of workspace fa_fwd_staged needs: for FA_DTYPE_F32, twice B*H*Nk*d
  * floats (K_hi and K_lo) plus B*H*d*ceil(Nk/128)*128 floats (V^T), each part
  * rounded up to 256 bytes; 0 for other dtypes and for invalid arguments. */
-unsigned long long fa_fwd_staged_workspace(int B, int H, int Nk, int d, int dtype);
+FA_API unsigned long long fa_fwd_staged_workspace(int B, int H, int Nk, int d, int dtype);
 
 /*
  * fa_bwd — gradients of the forward for an upstream gradient dout: the
@@ -249,19 +258,23 @@ unsigned long long fa_fwd_staged_workspace(int B, int H, int Nk, int d, int dtyp
  *                  written (keys that no query sees get zero gradients).
  * dtype            FA_DTYPE_BF16 or FA_DTYPE_F16 with d 32, 64 or 128 (tcgen05
  *                  kind::f16; P and dS are rounded to the input type, the
- *                  products accumulate in fp32); anything else is
+ *                  products accumulate in fp32), or FA_DTYPE_F32 /
+ *                  FA_DTYPE_F32_SIMT with d 1 .. 128 (fp32 on the CUDA cores:
+ *                  dq, dk, dv fp32, dq accumulated with atomic adds, so its
+ *                  last bits may differ between runs); anything else is
  *                  FA_ERR_UNSUPPORTED.
  * workspace        caller-owned device memory, 256-byte aligned, of at least
  *                  fa_bwd_workspace(B, H, Nq, d) bytes: an fp32 dq
  *                  accumulator and two fp32 values per query row.  Calls that
  *                  share a workspace must not overlap on the GPU.
  * All pointers 16-byte aligned except lse (4 bytes); outputs and workspace
- * must not overlap each other or any input.  Asynchronous on `stream` (three
- * kernels: per-row D and LSE, the tensor-core kernel, dq rounding); bounded
- * waits report through the status word (fa_fwd_status).  Arguments are
- * checked before anything is enqueued (FA_ERR_INVALID_ARG).
+ * must not overlap each other or any input.  Asynchronous on `stream` (16-bit:
+ * three kernels, per-row D and LSE, the tensor-core kernel, dq rounding;
+ * fp32: two, per-row D with dq zeroed, the gradient kernel); bounded waits
+ * report through the status word (fa_fwd_status).  Arguments are checked
+ * before anything is enqueued (FA_ERR_INVALID_ARG).
  */
-int fa_bwd(const void *q, const void *k, const void *v, const void *o, const float *lse,
+FA_API int fa_bwd(const void *q, const void *k, const void *v, const void *o, const float *lse,
            const void *dout, void *dq, void *dk, void *dv,
            int B, int H, int Nq, int Nk, int d, float scale, int causal, int dtype,
            void *workspace, unsigned long long workspace_bytes, void *stream);
@@ -270,7 +283,7 @@ int fa_bwd(const void *q, const void *k, const void *v, const void *o, const flo
  * accumulator, rows of the gradient kernel's head dim) plus
  * 2*B*H*ceil(Nq/128)*128 floats, each part rounded up to 256 bytes.  0 for
  * invalid arguments. */
-unsigned long long fa_bwd_workspace(int B, int H, int Nq, int d);
+FA_API unsigned long long fa_bwd_workspace(int B, int H, int Nq, int d);
 
 /*
  * fa_bwd_varlen — fa_bwd over a batch of sequences of different lengths
@@ -286,7 +299,7 @@ unsigned long long fa_bwd_workspace(int B, int H, int Nq, int d);
  * floats per padded query row).  The offsets are read on the device and not
  * checked on the host; every row index stays below total_q / total_k.
  */
-int fa_bwd_varlen(const void *q, const void *k, const void *v, const void *o, const float *lse,
+FA_API int fa_bwd_varlen(const void *q, const void *k, const void *v, const void *o, const float *lse,
                   const void *dout, void *dq, void *dk, void *dv,
                   const int *cu_seqlens_q, const int *cu_seqlens_k, int B, int H,
                   int total_q, int total_k, int max_seqlen_q, int max_seqlen_k, int d,
@@ -296,7 +309,7 @@ int fa_bwd_varlen(const void *q, const void *k, const void *v, const void *o, co
 /* Bytes of workspace fa_bwd_varlen needs: total_q*H*max(d, 64) floats plus
  * 2*H*B*ceil(max_seqlen_q/128)*128 floats, parts rounded up to 256 bytes;
  * 0 for invalid arguments. */
-unsigned long long fa_bwd_varlen_workspace(int B, int H, int total_q, int max_seqlen_q, int d);
+FA_API unsigned long long fa_bwd_varlen_workspace(int B, int H, int total_q, int max_seqlen_q, int d);
 
 /*
  * fa_fwd_host — the same forward on HOST buffers.
@@ -316,7 +329,7 @@ unsigned long long fa_bwd_varlen_workspace(int B, int H, int total_q, int max_se
  * overwritten, and every enqueued step has finished when the call returns,
  * so the host outputs are ready on return.  Returns the first failing status.
  */
-int fa_fwd_host(const void *q_h, const void *k_h, const void *v_h,
+FA_API int fa_fwd_host(const void *q_h, const void *k_h, const void *v_h,
                 void *o_h, float *lse_h,
                 void *q_d, void *k_d, void *v_d, void *o_d, float *lse_d,
                 int B, int H, int Nq, int Nk, int d, float scale, int causal,
@@ -332,13 +345,13 @@ int fa_fwd_host(const void *q_h, const void *k_h, const void *v_h,
  * check of the debug build failed and the access was skipped).
  * Returns FA_OK, FA_ERR_DEVICE_TIMEOUT (word != 0) or FA_ERR_CUDA.
  */
-int fa_fwd_status(void *stream, int *device_status);
+FA_API int fa_fwd_status(void *stream, int *device_status);
 
 /* Human-readable name of an fa_status value (static storage). */
-const char *fa_status_string(int status);
+FA_API const char *fa_status_string(int status);
 
 /* FA_VERSION of the compiled library. */
-int fa_version(void);
+FA_API int fa_version(void);
 
 /*
  * fa_set_test_hooks — testing aid, process-wide.
@@ -348,7 +361,7 @@ int fa_version(void);
  * wait_limit_ns sets the bounded-wait limit in nanoseconds (0 = default,
  * 2e9).  Returns FA_OK.
  */
-int fa_set_test_hooks(int skip_v_load, unsigned long long wait_limit_ns);
+FA_API int fa_set_test_hooks(int skip_v_load, unsigned long long wait_limit_ns);
 
 /*
  * fa_debug_build — 1 for the debug build of the library (libfa_debug.so,
@@ -359,7 +372,7 @@ int fa_set_test_hooks(int skip_v_load, unsigned long long wait_limit_ns);
  * failed check skips the access and sets bit 32 in the status word that
  * fa_fwd_status reports.  No counterpart on the pages.
  */
-int fa_debug_build(void);
+FA_API int fa_debug_build(void);
 
 /*
  * fa_set_debug_lse_shrink — testing aid of the debug build: the LSE extent
@@ -368,7 +381,7 @@ int fa_debug_build(void);
  * without any access leaving a buffer.  Returns FA_OK, FA_ERR_INVALID_ARG
  * for elems < 0, or FA_ERR_UNSUPPORTED in the release build.
  */
-int fa_set_debug_lse_shrink(long long elems);
+FA_API int fa_set_debug_lse_shrink(long long elems);
 
 /*
  * fa_set_fwd_schedule — testing aid, process-wide; no counterpart on the
@@ -381,7 +394,7 @@ int fa_set_debug_lse_shrink(long long elems);
  * on the schedule: every query tile does the same arithmetic wherever it
  * runs.  Returns FA_OK, or FA_ERR_INVALID_ARG for a negative argument.
  */
-int fa_set_fwd_schedule(int ctas, int group_heads, int block_items);
+FA_API int fa_set_fwd_schedule(int ctas, int group_heads, int block_items);
 
 /*
  * fa_fwd_schedule — the schedule fa_fwd would use for this problem on a GPU
@@ -399,7 +412,7 @@ int fa_set_fwd_schedule(int ctas, int group_heads, int block_items);
  * query tile.  Returns FA_OK, or FA_ERR_INVALID_ARG for null outputs, sizes
  * below 1 or causal not 0/1.
  */
-int fa_fwd_schedule(int B, int H, int Nq, int Nk, int d, int causal, int dtype, int num_sms,
+FA_API int fa_fwd_schedule(int B, int H, int Nq, int Nk, int d, int causal, int dtype, int num_sms,
                     int *ctas, int *group_heads, int *block_items);
 
 /*
@@ -409,7 +422,7 @@ int fa_fwd_schedule(int B, int H, int Nq, int Nk, int d, int causal, int dtype, 
  * one CTA; else 0 (also for sizes below 1, a persistent grid with more CTAs
  * than items, a blocked grid of the wrong size, or more than 2^24 items).
  */
-int fa_fwd_schedule_covers(int planes, int n, int ctas, int group_heads, int block_items);
+FA_API int fa_fwd_schedule_covers(int planes, int n, int ctas, int group_heads, int block_items);
 
 #ifdef __cplusplus
 }

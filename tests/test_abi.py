@@ -35,6 +35,17 @@ def test_library_exports_every_declared_symbol(lib):
         assert hasattr(lib, name), f"libfa.so does not export {name}"
 
 
+def test_only_the_header_functions_are_exported(lib):
+    """The library is built with hidden visibility: internal functions (here
+    the launchers of the SIMT forward and of a tensor-core instantiation) are
+    not in its dynamic symbol table, so a second build loaded in the same
+    process (the debug library) cannot share their statics or symbols."""
+    for internal in ("_ZN2fa11launch_simtERKNS_10SimtParamsEiP11CUstream_st",
+                     "_ZN2fa19launch_tc_bf16_d128ERK14CUtensorMap_stS2_S2_S2_S2_RKNS_8TcParamsEiiP11CUstream_st"):
+        with pytest.raises(AttributeError):
+            getattr(lib, internal)
+
+
 def test_version_and_strings(lib):
     assert fa.fa_version() == 10000
     assert fa.fa_status_string(0) == "FA_OK"
@@ -269,7 +280,7 @@ def test_bwd_invalid_arguments(lib, kw):
 
 
 @pytest.mark.parametrize("kw", [
-    dict(dtype=fa.FA_DTYPE_F32), dict(dtype=fa.FA_DTYPE_F32_SIMT), dict(d=96),
+    dict(dtype=fa.FA_DTYPE_F32, d=192), dict(dtype=fa.FA_DTYPE_F32_SIMT, d=256), dict(d=96),
     dict(dtype=fa.FA_DTYPE_F16, d=256), dict(d=256),
 ], ids=lambda kw: ",".join(f"{k}={v}" for k, v in kw.items()))
 def test_bwd_unsupported_problems(lib, kw):

@@ -9,7 +9,8 @@ import torch
 
 import oracle
 from exact_attention_57_gb300 import fa
-from exact_attention_57_gb300.workloads import DTYPE_BF16, DTYPE_F16, make_dout, make_inputs
+from exact_attention_57_gb300.workloads import (DTYPE_BF16, DTYPE_F16, DTYPE_F32, make_dout,
+                                                make_inputs)
 
 pytestmark = pytest.mark.gpu
 
@@ -22,6 +23,13 @@ pytestmark = pytest.mark.gpu
 # error is about u of the typical gradient: mean_rel = 2.5u, max_rel = 8u.
 U = {DTYPE_BF16: 2.0 ** -9, DTYPE_F16: 2.0 ** -12}
 TOL = {dt: dict(max_rel=8 * u, mean_rel=2.5 * u) for dt, u in U.items()}
+# fp32 (CUDA-core backward after the plain fp32 forward): every step is fp32
+# arithmetic, so each gradient is a sum of N products each within a few units
+# of u = 2^-24 (expf within 2 ulp, P from the forward's fp32 LSE); sums of N
+# such terms drift by about sqrt(N) u in the mean and N u at worst.  Bound
+# with N = 1024 (the longest key range tested): mean 32u, max 1024u of the
+# gradient's size.
+TOL[DTYPE_F32] = dict(max_rel=1024 * 2.0 ** -24, mean_rel=32 * 2.0 ** -24)
 
 CASES = [
     # B, H, Nq, Nk, d, causal, dtype, scale (None = 1/sqrt(d))
@@ -40,13 +48,27 @@ CASES = [
     (1, 4, 1024, 1024, 64, False, DTYPE_BF16, None),
     (2, 2, 300, 300, 32, True, DTYPE_BF16, None),     # runs zero-padded on the d = 64 kernel
     (1, 3, 200, 457, 32, False, DTYPE_F16, None),
+    # fp32: the CUDA-core backward (any head dim up to 128)
+    (1, 2, 128, 128, 64, False, DTYPE_F32, None),
+    (2, 2, 300, 300, 128, True, DTYPE_F32, None),
+    (1, 2, 200, 457, 64, False, DTYPE_F32, None),
+    (1, 2, 457, 200, 128, True, DTYPE_F32, None),
+    (1, 2, 100, 400, 128, True, DTYPE_F32, None),    # keys past the last query
+    (1, 3, 1, 1, 64, False, DTYPE_F32, None),
+    (2, 2, 150, 150, 33, True, DTYPE_F32, None),
+    (1, 2, 256, 256, 128, True, DTYPE_F32, -0.2),
+    (1, 2, 256, 300, 96, False, DTYPE_F32, 0.0),
+    (1, 2, 1024, 1024, 128, True, DTYPE_F32, None),
 ]
 
 
 def run_bwd(q, k, v, do, scale, causal):
     dev = torch.device("cuda:0")
     qd, kd, vd, dod = (t.to(dev) for t in (q, k, v, do))
-    o, lse = fa.attention(qd, kd, vd, scale=scale, causal=causal)
+    # fp32: the forward's o and lse from the plain fp32 kernel, so that the
+    # gradients are fp32 arithmetic throughout
+    impl = "simt" if q.dtype == torch.float32 else "tc"
+    o, lse = fa.attention(qd, kd, vd, scale=scale, causal=causal, impl=impl)
     grads = [torch.full_like(t, float("nan")) for t in (qd, kd, vd)]
     fa.attention_backward(qd, kd, vd, o, lse, dod, scale=scale, causal=causal,
                           dq=grads[0], dk=grads[1], dv=grads[2])
