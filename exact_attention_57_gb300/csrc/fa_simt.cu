@@ -16,8 +16,11 @@
 //     loop before a __syncthreads, a divergent-barrier hazard);
 //   * keys past Nk and, when causal, keys after the query are excluded
 //     element by element, on every tile, not only within a row's own tile.
-// One thread owns one query row; K/V tiles of 32 keys are staged in shared
-// memory and read as broadcasts.
+// One thread owns one query row (64 rows per CTA, so that small problems
+// still spread over several SMs); K/V tiles of 32 keys are staged in shared
+// memory and read as broadcasts.  The 32 dot products of a tile run side by
+// side (head-dim index outer, key inner), so no FMA waits on the previous
+// one.
 #include <cmath>
 
 #include "fa_internal.h"
@@ -26,7 +29,19 @@ namespace fa {
 
 namespace {
 
-constexpr int kSimtRows = 128;  // query rows per CTA (one per thread)
+constexpr int kSimtRows = 64;   // query rows per CTA (one per thread)
+
+// Asynchronous 4-byte copy global -> shared (cp.async; zero fill when
+// `valid` is false, in which case `src` is not read).
+__device__ __forceinline__ void cp_async4(float *dst, const float *src, bool valid) {
+  const uint32_t d = static_cast<uint32_t>(__cvta_generic_to_shared(dst));
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(d), "l"(src),
+               "r"(valid ? 4 : 0)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+}
 constexpr int kSimtKeys = 32;   // keys per shared-memory tile
 
 template <int DP>  // head dim padded up to 32, 64 or 128
@@ -62,25 +77,32 @@ __global__ void __launch_bounds__(kSimtRows) fa_simt_fwd_kernel(const SimtParams
 
   for (int k0 = 0; k0 < cta_lim; k0 += kSimtKeys) {
     __syncthreads();
+    // every copy of the tile in flight at once (one memory round trip)
     for (int e = threadIdx.x; e < kSimtKeys * DP; e += kSimtRows) {
       const int c = e / DP, x = e % DP;
       const int key = k0 + c;
       const bool in = key < p.Nk && x < d &&
                       FA_IN(p.status, static_cast<long long>(bh * p.Nk + key) * d + x, 1, kv_elems);
-      Ks[e] = in ? kh[static_cast<size_t>(key) * d + x] : 0.f;
-      Vs[e] = in ? vh[static_cast<size_t>(key) * d + x] : 0.f;
+      const size_t off = in ? static_cast<size_t>(key) * d + x : 0;
+      cp_async4(Ks + e, kh + off, in);
+      cp_async4(Vs + e, vh + off, in);
     }
+    cp_async_wait_all();
     __syncthreads();
     const int lim = row_lim - k0;  // valid columns c < lim
     if (active && lim > 0) {
       float s[kSimtKeys];
+#pragma unroll
+      for (int c = 0; c < kSimtKeys; ++c) s[c] = 0.f;
+#pragma unroll
+      for (int x = 0; x < DP; ++x) {
+#pragma unroll
+        for (int c = 0; c < kSimtKeys; ++c) s[c] = fmaf(qr[x], Ks[c * DP + x], s[c]);
+      }
       float mt = -INFINITY;
 #pragma unroll
       for (int c = 0; c < kSimtKeys; ++c) {
-        float dot = 0.f;
-#pragma unroll
-        for (int x = 0; x < DP; ++x) dot = fmaf(qr[x], Ks[c * DP + x], dot);
-        s[c] = dot * p.scale;
+        s[c] *= p.scale;
         if (c < lim) mt = fmaxf(mt, s[c]);
       }
       const float m_new = fmaxf(m, mt);
@@ -111,7 +133,9 @@ __global__ void __launch_bounds__(kSimtRows) fa_simt_fwd_kernel(const SimtParams
 }
 
 template <int DP>
-cudaError_t launch_simt_dp(const SimtParams &p, int B, cudaStream_t s) {
+cudaError_t launch_simt_dp(const SimtParams &p_in, int B, cudaStream_t s) {
+  SimtParams p = p_in;
+  p.n_qtiles = (p.Nq + kSimtRows - 1) / kSimtRows;  // this kernel's row tiles
   dim3 grid(static_cast<unsigned>(p.n_qtiles), static_cast<unsigned>(p.H),
             static_cast<unsigned>(B));
   fa_simt_fwd_kernel<DP><<<grid, kSimtRows, 0, s>>>(p);
