@@ -703,91 +703,113 @@ __global__ void __launch_bounds__(224, 1)
         for (int c = 0; c < BN; ++c)
           if (c >= lim) sr[c >> 5][c & 31] = 0xff800000u;  // -inf
       }
-      // Row max: eight independent chains of three-input max keep the
-      // dependency depth at 8 for the 128 columns.
-      float mx;
-      {
-        float part[8];
+      // After the first tile of an item, P is computed with the current
+      // offset straight away, and the row max is taken only when the row sum
+      // exceeds 2^kRescaleThreshold.  Any P above that bound (the max grew by
+      // more than the threshold, the one case where the offset must move)
+      // makes the sum exceed it, so the offsets, and with them P and l, are
+      // those of taking the max first on every tile.  When that max shows no
+      // row of the warp has to move, the first pass stands; otherwise the
+      // rows that must move rescale O and the warp recomputes P.  The first
+      // tile of an item takes its max first.
+      constexpr float kSumLimit = 256.f;  // 2^kRescaleThreshold
+      bool with_max = (j == 0);
+      float tsum = 0.f;
+      for (;;) {
+        if (with_max) {
+          // Row max: eight independent chains of three-input max keep the
+          // dependency depth at 8 for the 128 columns.
+          float mx;
+          {
+            float part[8];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) part[i] = -INFINITY;
+            for (int i = 0; i < 8; ++i) part[i] = -INFINITY;
 #pragma unroll
-        for (int c = 0; c < BN; c += 2) part[(c >> 1) & 7] = max3f(part[(c >> 1) & 7], S(c), S(c + 1));
-        mx = max3f(max3f(part[0], part[1], part[2]), max3f(part[3], part[4], part[5]),
-                   fmaxf(part[6], part[7]));
-      }
-      const float m_new = fmaxf(m_used, mx * sl2);
-      if (j == 0) {
-        m_used = m_new;
-      } else {
-        // P_j may overwrite P_{j-NS} without waiting: S_j was only issued
-        // after P_{j-NS} V_{j-NS} had completed.  Only a rescale of O has to
-        // wait, for P_{j-1} V_{j-1} (the last UMMA into O before P_j V_j); the
-        // done-barriers are per score buffer, and the previous use of tile
-        // j-1's buffer (P_{j-1-NS} V_{j-1-NS}) completed before S_{j-1} was
-        // issued, so a skipped wait never makes a later one ambiguous.
-        const bool need = (m_new - m_used) > kRescaleThreshold;
-        if (__any_sync(kFull, need)) {
-          ok = __all_sync(kFull, bounded_wait(bOdone + 8 * pbuf, pbph, w));
-          if (!ok) break;
-          tc_fence_after();
-          const float alpha = need ? ex2_approx(m_used - m_new) : 1.f;
-          const uint64_t a2 = pk2(alpha, alpha);
-#pragma unroll
-          for (int c = 0; c < D; c += 32) {
-            uint32_t o[32];
-            tmem_ld32(o_tm + c, o);
-            tmem_ld_wait();
-            reg_fence32(o);
-#pragma unroll
-            for (int i = 0; i < 32; i += 2) {
-              float lo, hi;
-              upk2(fmul2(pk2(__uint_as_float(o[i]), __uint_as_float(o[i + 1])), a2), lo, hi);
-              o[i] = __float_as_uint(lo);
-              o[i + 1] = __float_as_uint(hi);
-            }
-            tmem_st32(o_tm + c, o);
+            for (int c = 0; c < BN; c += 2)
+              part[(c >> 1) & 7] = max3f(part[(c >> 1) & 7], S(c), S(c + 1));
+            mx = max3f(max3f(part[0], part[1], part[2]), max3f(part[3], part[4], part[5]),
+                       fmaxf(part[6], part[7]));
           }
-          tmem_st_wait();
-          if (need) {
-            l *= alpha;
+          const float m_new = fmaxf(m_used, mx * sl2);
+          if (j == 0) {
             m_used = m_new;
-          }
-        }
-      }
-      // P = exp2(s * scale*log2e - m_used), written over S in TMEM; pairs of
-      // columns go through packed f32x2 arithmetic.
-      const uint64_t sl2_2 = pk2(sl2, sl2);
-      const uint64_t nm_2 = pk2(-m_used, -m_used);
-      uint64_t acc[2] = {0ull, 0ull};  // packed partial row sums (+0.0f bits)
-      {
-        constexpr int kBlk = TF32 ? 16 : 32;  // column pairs per TMEM store
+          } else {
+            // P_j may overwrite P_{j-NS} without waiting: S_j was only
+            // issued after P_{j-NS} V_{j-NS} had completed.  Only a rescale
+            // of O has to wait, for P_{j-1} V_{j-1} (the last UMMA into O
+            // before P_j V_j); the done-barriers are per score buffer, and the
+            // previous use of tile j-1's buffer (P_{j-1-NS} V_{j-1-NS})
+            // completed before S_{j-1} was issued, so a skipped wait never
+            // makes a later one ambiguous.
+            const bool need = (m_new - m_used) > kRescaleThreshold;
+            if (!__any_sync(kFull, need)) break;  // P and tsum of the first pass stand
+            ok = __all_sync(kFull, bounded_wait(bOdone + 8 * pbuf, pbph, w));
+            if (!ok) break;
+            tc_fence_after();
+            const float alpha = need ? ex2_approx(m_used - m_new) : 1.f;
+            const uint64_t a2 = pk2(alpha, alpha);
 #pragma unroll
-        for (int blk = 0; blk < 64 / kBlk; ++blk) {
-          uint32_t pk[32];
+            for (int c = 0; c < D; c += 32) {
+              uint32_t o[32];
+              tmem_ld32(o_tm + c, o);
+              tmem_ld_wait();
+              reg_fence32(o);
 #pragma unroll
-          for (int i = 0; i < kBlk; ++i) {
-            const int c0 = 2 * (blk * kBlk + i);
-            const uint64_t x2 = ffma2(pk2(S(c0), S(c0 + 1)), sl2_2, nm_2);
-            float x0, x1;
-            upk2(x2, x0, x1);
-            const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
-            acc[i & 1] = fadd2(acc[i & 1], pk2(p0, p1));
-            if constexpr (TF32) {
-              pk[2 * i] = to_tf32(p0);
-              pk[2 * i + 1] = to_tf32(p1);
-            } else {
-              pk[i] = HALF ? pack_f16x2(p0, p1) : pack_bf16x2(p0, p1);
+              for (int i = 0; i < 32; i += 2) {
+                float lo, hi;
+                upk2(fmul2(pk2(__uint_as_float(o[i]), __uint_as_float(o[i + 1])), a2), lo, hi);
+                o[i] = __float_as_uint(lo);
+                o[i + 1] = __float_as_uint(hi);
+              }
+              tmem_st32(o_tm + c, o);
+            }
+            tmem_st_wait();
+            if (need) {
+              l *= alpha;
+              m_used = m_new;
             }
           }
-          tmem_st32(s_tm + blk * 32, pk);
         }
+        // P = exp2(s * scale*log2e - m_used), written over S in TMEM; pairs of
+        // columns go through packed f32x2 arithmetic.
+        const uint64_t sl2_2 = pk2(sl2, sl2);
+        const uint64_t nm_2 = pk2(-m_used, -m_used);
+        uint64_t acc[2] = {0ull, 0ull};  // packed partial row sums (+0.0f bits)
+        {
+          constexpr int kBlk = TF32 ? 16 : 32;  // column pairs per TMEM store
+#pragma unroll
+          for (int blk = 0; blk < 64 / kBlk; ++blk) {
+            uint32_t pk[32];
+#pragma unroll
+            for (int i = 0; i < kBlk; ++i) {
+              const int c0 = 2 * (blk * kBlk + i);
+              const uint64_t x2 = ffma2(pk2(S(c0), S(c0 + 1)), sl2_2, nm_2);
+              float x0, x1;
+              upk2(x2, x0, x1);
+              const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+              acc[i & 1] = fadd2(acc[i & 1], pk2(p0, p1));
+              if constexpr (TF32) {
+                pk[2 * i] = to_tf32(p0);
+                pk[2 * i + 1] = to_tf32(p1);
+              } else {
+                pk[i] = HALF ? pack_f16x2(p0, p1) : pack_bf16x2(p0, p1);
+              }
+            }
+            tmem_st32(s_tm + blk * 32, pk);
+          }
+        }
+        {
+          float a0, a1, b0, b1;
+          upk2(acc[0], a0, a1);
+          upk2(acc[1], b0, b1);
+          tsum = (a0 + a1) + (b0 + b1);
+        }
+        if (with_max || __all_sync(kFull, tsum <= kSumLimit)) break;
+        with_max = true;
+        tmem_st_wait();  // the second pass rewrites the same P columns
       }
-      {
-        float a0, a1, b0, b1;
-        upk2(acc[0], a0, a1);
-        upk2(acc[1], b0, b1);
-        l += (a0 + a1) + (b0 + b1);
-      }
+      if (!ok) break;
+      l += tsum;
       if (TF32 && !staged) {
         // V^T buffer j % NVT was last read by P_{j-NVT} V_{j-NVT}: with two
         // buffers that completed before S_j was issued (NS = 2); the one
