@@ -50,7 +50,8 @@ METRIC_BWD = "attn bwd TFLOP/s (10·B·H·N²·d, ½ if causal) and % of GB300 d
 # shared headers and the host code that encodes its tensor maps and launches.
 KERNEL_SOURCES = {
     "fa_tc_fwd_kernel": ["fa_tc.cuh", "fa_tc_bf16_d128.cu", "fa_tc_bf16_d64.cu", "fa_tc_f16_d128.cu",
-                         "fa_tc_f16_d64.cu", "fa_tc_f32_d64.cu"],
+                         "fa_tc_f16_d64.cu", "fa_tc_f32_d64.cu", "fa_tc_f32s_d64.cu",
+                         "fa_tc_f32s_d128.cu"],
     "fa_bwd": ["fa_bwd.cuh", "fa_bwd_bf16.cu", "fa_bwd_f16.cu", "fa_bwd_aux.cu"],
 }
 COMMON_SOURCES = ["ptx.cuh", "fa_wait.cuh", "fa_internal.h", "fa_api.cu"]

@@ -989,7 +989,7 @@ int nk_pad128(int Nk) { return ceil_div(Nk, fa::BN) * fa::BN; }
 // [B*H][d][Nk padded to 128].
 void staged_parts(int B, int H, int Nk, int d, size_t *kr, size_t *vt) {
   const size_t bh = static_cast<size_t>(B) * H;
-  *kr = round256(bh * Nk * d * sizeof(float));
+  *kr = round256(bh * Nk * d * sizeof(__nv_bfloat16));  // one bf16 half of the split K
   *vt = round256(bh * d * static_cast<size_t>(nk_pad128(Nk)) * sizeof(float));
 }
 
@@ -1045,8 +1045,8 @@ extern "C" int fa_fwd_staged(const void *q, const void *k, const void *v, void *
   if ((rc = get_encoder()) != FA_OK) return rc;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int BH = B * H, nkp = nk_pad128(Nk);
-  float *kr = static_cast<float *>(workspace);
-  float *kl = reinterpret_cast<float *>(static_cast<char *>(workspace) + kr_bytes);
+  auto *kr = static_cast<__nv_bfloat16 *>(workspace);
+  auto *kl = reinterpret_cast<__nv_bfloat16 *>(static_cast<char *>(workspace) + kr_bytes);
   float *vt = reinterpret_cast<float *>(static_cast<char *>(workspace) + 2 * kr_bytes);
   if (fa::launch_stage_f32(static_cast<const float *>(k), static_cast<const float *>(v), kr, kl,
                            vt, BH, Nk, nkp, d, s) != cudaSuccess)
@@ -1054,8 +1054,8 @@ extern "C" int fa_fwd_staged(const void *q, const void *k, const void *v, void *
 
   CUtensorMap mq, mk, mv, mo, mkl;
   if ((rc = encode_map(&mq, q, dtype, BH, Nq, d)) != FA_OK) return rc;
-  if ((rc = encode_map(&mk, kr, dtype, BH, Nk, d)) != FA_OK) return rc;
-  if ((rc = encode_map(&mkl, kl, dtype, BH, Nk, d)) != FA_OK) return rc;
+  if ((rc = encode_map(&mk, kr, FA_DTYPE_BF16, BH, Nk, d)) != FA_OK) return rc;
+  if ((rc = encode_map(&mkl, kl, FA_DTYPE_BF16, BH, Nk, d)) != FA_OK) return rc;
   if ((rc = encode_map_vt(&mv, vt, BH, nkp, d, d <= 64 ? 64 : 128)) != FA_OK) return rc;
   if ((rc = encode_map(&mo, o, dtype, BH, Nq, d)) != FA_OK) return rc;
   fa::TcParams p;
@@ -1077,7 +1077,12 @@ extern "C" int fa_fwd_staged(const void *q, const void *k, const void *v, void *
   p.wait_limit_ns = lim ? lim : fa::kDefaultWaitLimitNs;
   p.skip_v_load = g_skip_v_load.load();
   p.kv_staged = 1;
-  cudaError_t e = launch_tc_any(mq, mk, mv, mo, p, B, causal, d, dtype, s, &mkl);
+  if (d == 32) {
+    p.d_io = 32;
+    d = 64;
+  }
+  cudaError_t e = d == 64 ? fa::launch_tc_f32s_d64(mq, mk, mv, mo, mkl, p, B, causal, s)
+                          : fa::launch_tc_f32s_d128(mq, mk, mv, mo, mkl, p, B, causal, s);
   return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 

@@ -5,6 +5,7 @@
 #include <atomic>
 #include <cstdint>
 #include <cuda.h>
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
 namespace fa {
@@ -185,6 +186,14 @@ cudaError_t launch_tc_f32_d64(const CUtensorMap &q, const CUtensorMap &k, const 
 cudaError_t launch_tc_f32_d128(const CUtensorMap &q, const CUtensorMap &k, const CUtensorMap &v,
                                const CUtensorMap &o, const CUtensorMap &klo, const TcParams &p,
                                int B, int causal, cudaStream_t s);
+// fp32 inputs with staged operands: k and klo are the bf16 halves of the
+// split K (the scores as three bf16 products).
+cudaError_t launch_tc_f32s_d64(const CUtensorMap &q, const CUtensorMap &k, const CUtensorMap &v,
+                               const CUtensorMap &o, const CUtensorMap &klo, const TcParams &p,
+                               int B, int causal, cudaStream_t s);
+cudaError_t launch_tc_f32s_d128(const CUtensorMap &q, const CUtensorMap &k, const CUtensorMap &v,
+                                const CUtensorMap &o, const CUtensorMap &klo, const TcParams &p,
+                                int B, int causal, cudaStream_t s);
 
 cudaError_t launch_tc_f16_d64(const CUtensorMap &q, const CUtensorMap &k, const CUtensorMap &v,
                               const CUtensorMap &o, const CUtensorMap &klo, const TcParams &p,
@@ -206,10 +215,12 @@ cudaError_t launch_splitkv_combine(const float *ws_o, const float *ws_lse, void 
 
 cudaError_t launch_simt(const SimtParams &p, int B, cudaStream_t s);
 
-// fp32 staging pre-pass: kr = tf32(k) and kl = tf32(k - kr) in k's layout,
-// vt[bh][x][n] = tf32(v[bh][n][x]) for n < Nk and 0 for Nk <= n < nk_pad.
-cudaError_t launch_stage_f32(const float *k, const float *v, float *kr, float *kl, float *vt,
-                             int BH, int Nk, int nk_pad, int d, cudaStream_t s);
+// fp32 staging pre-pass: kr = bf16(k) and kl = bf16(k - kr) (bf16 arrays in
+// k's layout), vt[bh][x][n] = tf32(v[bh][n][x]) for n < Nk and 0 for
+// Nk <= n < nk_pad.
+cudaError_t launch_stage_f32(const float *k, const float *v, __nv_bfloat16 *kr,
+                             __nv_bfloat16 *kl, float *vt, int BH, int Nk, int nk_pad, int d,
+                             cudaStream_t s);
 
 // ------------------------------------------------------------------ backward
 // Tensor-core backward: one CTA per (key tile, head, batch).  The TMA maps

@@ -1,9 +1,10 @@
 // fa_stage.cu — staging pre-pass of the fp32 (TF32) forward: K split once
-// per call into K_hi = tf32(K) and K_lo = tf32(K - K_hi), the B operands of
-// the three-product score, and V rounded and transposed into the K-major V^T
-// the tf32 P V product takes, instead of both being converted by every
-// query-tile CTA.  Rounding is to nearest (ties away), the rounding the kernel
-// itself applies to Q.
+// per call into bf16 halves K_hi = bf16(K) and K_lo = bf16(K - K_hi), the B
+// operands of the three-product score (bf16 products at the 16-bit rate; the
+// kernel splits Q the same way), and V rounded to tf32 and transposed into
+// the K-major V^T the tf32 P V product takes, instead of both being
+// converted by every query-tile CTA.  Rounding: to nearest even for bf16, to
+// nearest (ties away) for tf32.
 #include "fa_internal.h"
 #include "ptx.cuh"
 
@@ -11,23 +12,21 @@ namespace fa {
 
 namespace {
 
-// x_hi = tf32(x) and x_lo = tf32(x - x_hi): the split operands of the three
-// tf32 products that give the scores about fp32 accuracy.
-__device__ __forceinline__ void split_tf32(float x, float &hi, float &lo) {
-  hi = __uint_as_float(to_tf32(x));
-  lo = __uint_as_float(to_tf32(x - hi));
+// Two values x -> packed bf16 pairs hi = bf16(x) and lo = bf16(x - hi): the
+// split operands of the three bf16 products (about 2^-16 of x left out).
+__device__ __forceinline__ void split_bf16x2(float x0, float x1, uint32_t &hi, uint32_t &lo) {
+  hi = pack_bf16x2(x0, x1);
+  lo = pack_bf16x2(x0 - __uint_as_float(hi << 16), x1 - __uint_as_float(hi & 0xffff0000u));
 }
 
-__global__ void fa_stage_split_kernel(const float4 *__restrict__ k, float4 *__restrict__ kr,
-                                      float4 *__restrict__ kl, long long n4) {
+__global__ void fa_stage_split_kernel(const float4 *__restrict__ k, uint2 *__restrict__ kr,
+                                      uint2 *__restrict__ kl, long long n4) {
   for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < n4;
        i += static_cast<long long>(gridDim.x) * blockDim.x) {
     const float4 a = k[i];
-    float4 h, l;
-    split_tf32(a.x, h.x, l.x);
-    split_tf32(a.y, h.y, l.y);
-    split_tf32(a.z, h.z, l.z);
-    split_tf32(a.w, h.w, l.w);
+    uint2 h, l;
+    split_bf16x2(a.x, a.y, h.x, l.x);
+    split_bf16x2(a.z, a.w, h.y, l.y);
     kr[i] = h;
     kl[i] = l;
   }
@@ -60,12 +59,13 @@ __global__ void __launch_bounds__(256)
 
 }  // namespace
 
-cudaError_t launch_stage_f32(const float *k, const float *v, float *kr, float *kl, float *vt,
-                             int BH, int Nk, int nk_pad, int d, cudaStream_t s) {
+cudaError_t launch_stage_f32(const float *k, const float *v, __nv_bfloat16 *kr,
+                             __nv_bfloat16 *kl, float *vt, int BH, int Nk, int nk_pad, int d,
+                             cudaStream_t s) {
   const long long n4 = static_cast<long long>(BH) * Nk * d / 4;  // d is a multiple of 32
   fa_stage_split_kernel<<<1216, 256, 0, s>>>(reinterpret_cast<const float4 *>(k),
-                                             reinterpret_cast<float4 *>(kr),
-                                             reinterpret_cast<float4 *>(kl), n4);
+                                             reinterpret_cast<uint2 *>(kr),
+                                             reinterpret_cast<uint2 *>(kl), n4);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const dim3 grid(static_cast<unsigned>(nk_pad / 32), static_cast<unsigned>((d + 31) / 32),

@@ -41,10 +41,11 @@
 // tf32.  kind::tf32 takes its B operand K-major only, so the softmax warps
 // also transpose each V_j into a tf32 V_j^T buffer (d rows of 128 keys).  At
 // D=128 the fp32 tiles are 64 KB: one K, one V and one V^T buffer.  With
-// staged operands (kv_staged) a pre-pass has already rounded K and written
-// V^T once per call: K_j is used as loaded and V_j^T is loaded by TMA into
-// the V^T buffers (through the V ring's barriers), so the softmax warps only
-// do the softmax.
+// staged operands (the S16 instantiations) a pre-pass has already split K
+// into bf16 halves and written V^T once per call: the scores are three bf16
+// products of the split Q and K, K_j's halves are used as loaded and V_j^T is
+// loaded by TMA into the V^T buffers (through the V ring's barriers), so the
+// softmax warps only do the softmax.
 // Tensor memory: S_b cols [128b, 128b+128) for b < NS, then O (D cols), then Q
 // when it fits (bf16 D=64, fp32 D=64); bf16 D=128 and D=256 keep Q in shared
 // memory.  D=256 has two score buffers and single-stage K/V rings (64 KB
@@ -70,8 +71,11 @@
 
 namespace fa {
 
-template <int D, bool TF32>
+// S16 (fp32 inputs with staged operands only): the scores are three bf16
+// products of split operands instead of three tf32 ones (see NQSPLIT).
+template <int D, bool TF32, bool S16 = false>
 struct TcCfg {
+  static_assert(!S16 || TF32, "bf16 split scores are a variant of the fp32 path");
   static constexpr int ESZ = TF32 ? 4 : 2;                 // bytes per element
   static constexpr int NCH = D * ESZ / 128;                 // 128-byte swizzle chunks per row
   static constexpr int CH_ELEMS = 128 / ESZ;                // elements per chunk
@@ -81,15 +85,23 @@ struct TcCfg {
   // Score buffers in tensor memory: S_j lives in buffer j % NS; S_j may be
   // issued once P_{j-NS} V_{j-NS} is done, so NS - 1 score tiles can be
   // computed ahead of the softmax.  (fp32 at D = 128: one buffer, because
-  // both halves of the split Q fill the rest of tensor memory.)
-  static constexpr int NS = TF32 ? (D >= 128 ? 1 : 2) : (D >= 256 ? 2 : 3);
+  // both halves of the split Q fill the rest of tensor memory; with bf16
+  // halves, half as wide, one more.)
+  static constexpr int NS = TF32 ? (D >= 128 ? 1 : 2) + (S16 ? 1 : 0) : (D >= 256 ? 2 : 3);
   static constexpr uint32_t TMEM_COLS = 512;
   static constexpr uint32_t COL_O = NS * 128;               // O after the score buffers
-  static constexpr int Q_COLS = D * ESZ / 4;                // 32-bit columns of one Q row
-  // fp32 path: S = Q K^T runs as three tf32 products of the split operands,
-  // Q_hi K_hi + Q_hi K_lo + Q_lo K_hi, x_hi = tf32(x), x_lo = tf32(x - x_hi),
-  // so the scores carry about fp32 accuracy instead of tf32's 2^-11.
+  // 32-bit columns of one Q row (S16: of one bf16 half of the split Q)
+  static constexpr int Q_COLS = S16 ? D / 2 : D * ESZ / 4;
+  // fp32 path: S = Q K^T runs as three products of the split operands,
+  // Q_hi K_hi + Q_hi K_lo + Q_lo K_hi, x_hi = r(x), x_lo = r(x - x_hi) with r
+  // the rounding to tf32 (about 2^-22 of x left out), or (S16) to bf16 (about
+  // 2^-16 left out, at twice the tf32 rate and half the instructions).  Either
+  // way the scores carry far more than one product's accuracy (tf32: 2^-11).
   static constexpr int NQSPLIT = TF32 ? 2 : 1;
+  // S16: K_hi and K_lo arrive as bf16 tiles (KCH chunks of 128 rows).
+  static constexpr int KCH = S16 ? D * 2 / 128 : D * ESZ / 128;
+  static constexpr int K_CH_ELEMS = S16 ? 64 : 128 / ESZ;
+  static constexpr int K_TILE_BYTES = KCH * 128 * 128;
   // Q is the A operand of S = Q K^T: from tensor memory when it fits after O,
   // else from shared memory (bf16, D = 128).
   static constexpr bool QTMEM = COL_O + D + NQSPLIT * Q_COLS <= TMEM_COLS;
@@ -129,7 +141,7 @@ struct TcCfg {
   static_assert(!TF32 || QTMEM, "the fp32 path rounds Q on its way into tensor memory");
   static_assert(!TF32 || VST == NVT, "staged V^T tiles use the V ring's barriers");
   static_assert(!TF32 || KST == VST, "staged K_lo tiles sit in the V stage of their K stage");
-  static_assert(!TF32 || NKLO == 1 || NS == 1,
+  static_assert(!TF32 || S16 || NKLO == 1 || NS == 1,
                 "K_lo shares the V^T buffer only where S_j completes before V_j^T is written");
   static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
   static_assert(VST + 1 <= kItemRing, "items with O staged in a V stage fit the item ring");
@@ -141,14 +153,14 @@ constexpr unsigned kFull = 0xffffffffu;
 
 // HALF selects fp16 instead of bf16 for the 16-bit path (kind::f16 either
 // way; P and O are packed in the input type).
-template <int D, bool TF32, bool CAUSAL, bool HALF>
+template <int D, bool TF32, bool CAUSAL, bool HALF, bool S16 = false>
 __global__ void __launch_bounds__(224, 1)
     fa_tc_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                      const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_v,
                      const __grid_constant__ CUtensorMap tm_o,
                      const __grid_constant__ CUtensorMap tm_klo, const TcParams p) {
-  using C = TcCfg<D, TF32>;
+  using C = TcCfg<D, TF32, S16>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -229,7 +241,7 @@ __global__ void __launch_bounds__(224, 1)
   const int dio = p.d_io > 0 ? p.d_io : D;
   // fp32 path with staged operands: K arrives rounded to tf32 and V as a
   // K-major tf32 V^T, so neither is converted here.
-  const bool staged = TF32 && p.kv_staged != 0;
+  const bool staged = TF32 && (S16 || p.kv_staged != 0);
   if (Nk == 0) {
     // A sequence without keys: the softmax over an empty set gives O = 0 and
     // LSE = log 0 = -inf (variable-length batches only).
@@ -359,16 +371,18 @@ __global__ void __launch_bounds__(224, 1)
             if (r > 0) ok = bounded_wait(bKempty + 8 * s, (r - 1) & 1, w);
             if (!ok) break;
             // staged fp32: K_hi, and K_lo into the V stage of the same index
-            mbar_arrive_expect_tx(bKfull + 8 * s, staged ? 2 * C::TILE_BYTES : C::TILE_BYTES);
+            // (S16: bf16 tiles, half the bytes)
+            mbar_arrive_expect_tx(bKfull + 8 * s,
+                                  staged ? 2 * C::K_TILE_BYTES : C::K_TILE_BYTES);
 #pragma unroll
-            for (int c = 0; c < C::NCH; ++c)
+            for (int c = 0; c < C::KCH; ++c)
               tma_load_3d(sK + s * C::TILE_BYTES + c * C::CHUNK_BYTES, &tm_k, bKfull + 8 * s,
-                          c * C::CH_ELEMS, k_row0 + (kt0_g + jk) * BN, hcg, pol_kv);
+                          c * C::K_CH_ELEMS, k_row0 + (kt0_g + jk) * BN, hcg, pol_kv);
             if (staged) {
 #pragma unroll
-              for (int c = 0; c < C::NCH; ++c)
+              for (int c = 0; c < C::KCH; ++c)
                 tma_load_3d(sV + s * C::TILE_BYTES + c * C::CHUNK_BYTES, &tm_klo, bKfull + 8 * s,
-                            c * C::CH_ELEMS, k_row0 + (kt0_g + jk) * BN, hcg, pol_kv);
+                            c * C::K_CH_ELEMS, k_row0 + (kt0_g + jk) * BN, hcg, pol_kv);
             }
             ++nk;
           }
@@ -431,6 +445,8 @@ __global__ void __launch_bounds__(224, 1)
       // A negative scale is applied as S = (-Q) K^T (the descriptor's negate-A
       // bit) with |scale|, so the softmax only ever sees a positive scale.
       const uint32_t idesc_qk = kIdescQK | (p.scale_neg ? (1u << 13) : 0u);
+      // S16: the split products in bf16 (kind::f16, format 1)
+      const uint32_t idesc_qk16 = make_idesc(1u, BM, BN, 0u, 0u) | (p.scale_neg ? (1u << 13) : 0u);
       bool ok = true;
       int b = 0, bph = 0;   // score buffer of the next S and the parity of its use
       int s = 0, sph = 0;   // K stage of the next S and its parity
@@ -452,6 +468,19 @@ __global__ void __launch_bounds__(224, 1)
         const uint32_t kb = sK + s * C::TILE_BYTES;
         // fp32: K_lo of this tile (see TcCfg::NKLO)
         const uint32_t klo = staged ? sV + s * C::TILE_BYTES : C::NKLO ? sKLO : sVT;
+        if constexpr (S16) {
+          // Q_hi K_hi + Q_hi K_lo + Q_lo K_hi in bf16: 32 bytes (16 values) of
+          // K per UMMA, 8 TMEM columns of Q.
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * C::CHUNK_BYTES + (kk & 3) * 32;
+            const uint64_t khi = sdesc_sw128(kb + off, 16, 1024);
+            umma_ts<false>(d_tmem, tmem + C::COL_Q + kk * 8, khi, idesc_qk16, kk > 0 ? 1u : 0u);
+            umma_ts<false>(d_tmem, tmem + C::COL_Q + kk * 8, sdesc_sw128(klo + off, 16, 1024),
+                           idesc_qk16, 1u);
+            umma_ts<false>(d_tmem, tmem + C::COL_QLO + kk * 8, khi, idesc_qk16, 1u);
+          }
+        } else
 #pragma unroll
         for (int kk = 0; kk < D / C::UK; ++kk) {
           // 32 bytes of K per UMMA (4 steps per 128-byte swizzle chunk); the
@@ -627,6 +656,30 @@ __global__ void __launch_bounds__(224, 1)
       const bool in = qrow < Nq && FA_IN(p.status, qoff, dio, p.q_elems);
       const uint4 *src = reinterpret_cast<const uint4 *>(
           static_cast<const uint8_t *>(p.q) + qoff * C::ESZ);
+      if constexpr (S16) {
+        // Q_hi = bf16(q) and Q_lo = bf16(q - Q_hi), two per column: 64
+        // fp32 values of the row per block of 32 columns.
+#pragma unroll
+        for (int blk = 0; blk < C::Q_COLS / 32; ++blk) {
+          uint32_t wh[32], wl[32];
+#pragma unroll
+          for (int u = 0; u < 16; ++u) {
+            const bool ld = in && (blk * 16 + u) * 16 < dio * C::ESZ;
+            const uint4 val = ld ? __ldg(src + blk * 16 + u) : make_uint4(0u, 0u, 0u, 0u);
+            const float x[4] = {__uint_as_float(val.x), __uint_as_float(val.y),
+                                __uint_as_float(val.z), __uint_as_float(val.w)};
+#pragma unroll
+            for (int e = 0; e < 4; e += 2) {
+              const uint32_t h = pack_bf16x2(x[e], x[e + 1]);
+              wh[2 * u + e / 2] = h;
+              wl[2 * u + e / 2] = pack_bf16x2(x[e] - __uint_as_float(h << 16),
+                                              x[e + 1] - __uint_as_float(h & 0xffff0000u));
+            }
+          }
+          tmem_st32(tmem + lane_off + C::COL_Q + blk * 32, wh);
+          tmem_st32(tmem + lane_off + C::COL_QLO + blk * 32, wl);
+        }
+      } else
 #pragma unroll
       for (int blk = 0; blk < C::Q_COLS / 32; ++blk) {
         uint32_t wq[32];
@@ -1013,14 +1066,15 @@ __global__ void __launch_bounds__(224, 1)
   }
 }
 
-template <int D, bool TF32, bool HALF = false>
+template <int D, bool TF32, bool HALF = false, bool S16 = false>
 cudaError_t launch_tc(const CUtensorMap &q, const CUtensorMap &k, const CUtensorMap &v,
                       const CUtensorMap &o, const CUtensorMap &klo, const TcParams &p, int B,
                       int causal, cudaStream_t stream) {
-  using C = TcCfg<D, TF32>;
+  using C = TcCfg<D, TF32, S16>;
   void (*kern)(const CUtensorMap, const CUtensorMap, const CUtensorMap, const CUtensorMap,
                const CUtensorMap, const TcParams) =
-      causal ? fa_tc_fwd_kernel<D, TF32, true, HALF> : fa_tc_fwd_kernel<D, TF32, false, HALF>;
+      causal ? fa_tc_fwd_kernel<D, TF32, true, HALF, S16>
+             : fa_tc_fwd_kernel<D, TF32, false, HALF, S16>;
   static std::atomic<unsigned long long> attr_done[2];  // per causal flag
   cudaError_t e = smem_attr_once(kern, C::SMEM_BYTES, &attr_done[causal ? 1 : 0]);
   if (e != cudaSuccess) return e;

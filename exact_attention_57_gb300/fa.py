@@ -358,7 +358,8 @@ def attention(q, k, v, scale: float | None = None, causal: bool = False, impl: s
     dtypes): split each query tile's key range into that many chunks (0 =
     automatic) through fa_fwd_splitkv, with a torch-allocated workspace.
     staged (fp32, impl "tc"): run fa_fwd_staged, converting K and V once per
-    call into a torch-allocated workspace.  Raises FaError on failure.
+    call into a torch-allocated workspace (scores as three bf16 products of
+    split operands instead of fa_fwd's three tf32 ones).  Raises FaError on failure.
     """
     import torch
     if not (q.is_cuda and k.is_cuda and v.is_cuda):

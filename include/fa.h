@@ -216,12 +216,16 @@ FA_API int fa_fwd_varlen(const void *q, const void *k, const void *v, void *o, f
 
 /*
  * fa_fwd_staged — the forward with a caller-provided staging area.  For
- * FA_DTYPE_F32 (tcgen05 kind::tf32) a pre-pass splits K into K_hi = tf32(K)
- * and K_lo = tf32(K - K_hi) and writes V, rounded and transposed, into the
- * K-major V^T layout the tf32 P V product takes, once per call; the kernel
- * then loads them ready-made instead of every query-tile CTA converting the
- * same tiles again.  Same results as fa_fwd (the same roundings, applied
- * once).  Other dtypes have nothing to
+ * FA_DTYPE_F32 a pre-pass splits K into bf16 halves K_hi = bf16(K) and
+ * K_lo = bf16(K - K_hi) and writes V, rounded to tf32 and transposed, into
+ * the K-major V^T layout the tf32 P V product (tcgen05 kind::tf32) takes,
+ * once per call; the kernel then loads them ready-made instead of every
+ * query-tile CTA converting the same tiles again.  The kernel splits Q the
+ * same way and computes the scores as three bf16 products (kind::f16),
+ * Q_hi K_hi + Q_hi K_lo + Q_lo K_hi: about 2^-16 of each term left out,
+ * against 2^-22 for fa_fwd's three tf32 products, at twice the tensor rate.
+ * Results therefore differ slightly from fa_fwd's; both meet the fp32
+ * tolerances (max |dO| 5e-3, |dLSE| 1e-3).  Other dtypes have nothing to
  * stage and run fa_fwd (workspace may then be NULL).
  *
  * Arguments q .. dtype and stream as for fa_fwd.
@@ -238,8 +242,9 @@ FA_API int fa_fwd_staged(const void *q, const void *k, const void *v, void *o, f
                   void *stream);
 
 /* Bytes of workspace fa_fwd_staged needs: for FA_DTYPE_F32, twice B*H*Nk*d
- * floats (K_hi and K_lo) plus B*H*d*ceil(Nk/128)*128 floats (V^T), each part
- * rounded up to 256 bytes; 0 for other dtypes and for invalid arguments. */
+ * bf16 values (K_hi and K_lo) plus B*H*d*ceil(Nk/128)*128 floats (V^T), each
+ * part rounded up to 256 bytes; 0 for other dtypes and for invalid
+ * arguments. */
 FA_API unsigned long long fa_fwd_staged_workspace(int B, int H, int Nk, int d, int dtype);
 
 /*

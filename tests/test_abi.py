@@ -288,13 +288,13 @@ def test_bwd_unsupported_problems(lib, kw):
 
 
 def test_staged_workspace_size(lib):
-    """fp32: 2*B*H*Nk*d (K_hi, K_lo) + B*H*d*ceil(Nk/128)*128 (V^T) floats,
-    parts rounded up to 256 bytes; other dtypes stage nothing."""
+    """fp32: 2*B*H*Nk*d bf16 values (K_hi, K_lo) + B*H*d*ceil(Nk/128)*128
+    floats (V^T), parts rounded up to 256 bytes; other dtypes stage nothing."""
     up = lambda n: (n + 255) // 256 * 256
     for B, H, Nk, d in [(1, 1, 1, 64), (4, 4, 4096, 64), (2, 3, 300, 128), (1, 2, 77, 32)]:
         pad = (Nk + 127) // 128 * 128
         assert (fa.fa_fwd_staged_workspace(B, H, Nk, d, fa.FA_DTYPE_F32)
-                == 2 * up(B * H * Nk * d * 4) + up(B * H * d * pad * 4))
+                == 2 * up(B * H * Nk * d * 2) + up(B * H * d * pad * 4))
     for dt in (fa.FA_DTYPE_BF16, fa.FA_DTYPE_F16, fa.FA_DTYPE_F32_SIMT):
         assert fa.fa_fwd_staged_workspace(1, 1, 128, 64, dt) == 0
     assert fa.fa_fwd_staged_workspace(0, 1, 128, 64, fa.FA_DTYPE_F32) == 0
