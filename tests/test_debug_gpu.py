@@ -65,6 +65,27 @@ def test_debug_forward_same_bits_no_check_fires(dbg, dtype, d, N, causal):
     assert torch.equal(o1, o2) and torch.equal(l1, l2)
 
 
+@pytest.mark.parametrize("d,N", [(64, 300), (128, 257), (32, 129)])
+def test_debug_staged_same_bits_no_check_fires(dbg, d, N):
+    """fa_fwd_staged (fp32, bf16 split scores): the kernel's Q rows are plain
+    loads checked against Q's extent."""
+    dev = torch.device("cuda:0")
+    stream = torch.cuda.current_stream(dev).cuda_stream
+    q, k, v = (t.to(dev) for t in make_inputs(2, 3, N, N, d, DTYPE_F32, seed=N + 5 * d))
+    outs = []
+    for lib in (fa.load(), dbg):
+        o = torch.full_like(q, float("nan"))
+        lse = torch.full((2, 3, N), float("nan"), device=dev, dtype=torch.float32)
+        wsb = lib.fa_fwd_staged_workspace(2, 3, N, d, DTYPE_F32)
+        ws = torch.empty(wsb, device=dev, dtype=torch.uint8)
+        assert lib.fa_fwd_staged(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                 lse.data_ptr(), 2, 3, N, N, d, d ** -0.5, 1, DTYPE_F32,
+                                 ws.data_ptr(), wsb, stream) == fa.FA_OK
+        assert _status(lib, stream) == (fa.FA_OK, 0)
+        outs.append((o, lse))
+    assert torch.equal(outs[0][0], outs[1][0]) and torch.equal(outs[0][1], outs[1][1])
+
+
 def test_debug_splitkv_varlen_backward_no_check_fires(dbg):
     dev = torch.device("cuda:0")
     stream = torch.cuda.current_stream(dev).cuda_stream

@@ -49,6 +49,17 @@ def test_staged_matches_oracle(B, H, Nq, Nk, d, causal, big_scale):
     print(f"staged {B,H,Nq,Nk,d} causal={causal} scale={scale:.3f}: {st}")
 
 
+@pytest.mark.parametrize("scale", [-0.3, 0.0])
+def test_staged_negative_and_zero_scale(scale):
+    """A negative scale runs as S = (-Q) K^T with |scale| (the negate bit of
+    the bf16 products' descriptor); scale 0 gives uniform weights."""
+    q, k, v = make_inputs(1, 2, 300, 500, 64, DTYPE_F32, seed=77)
+    for causal in (False, True):
+        o, lse = run_staged(q, k, v, scale, causal)
+        ro, rl = run_oracle(q, k, v, scale, causal)
+        compare(o, lse, ro, rl, DTYPE_F32, f"staged scale={scale} causal={causal}")
+
+
 def test_staged_fp32_workload_full():
     """The fp32 workload b4h4n4096d64 (non-causal) through the path its
     benchmark times, every element against the oracle."""
