@@ -32,26 +32,43 @@ __global__ void fa_stage_split_kernel(const float4 *__restrict__ k, uint2 *__res
   }
 }
 
-// One 32 x 32 tile per block and head: v[n0 + r][x0 + c] -> vt[x0 + c][n0 + r];
-// heads stride by gridDim.z (which is capped at 65535).
+// One 64-key x 32-column tile per block and head: v[n0 + r][x0 + c] ->
+// vt[x0 + c][n0 + r], rounded to tf32; keys n0 + r >= Nk give 0 up to nk_pad.
+// Loads and stores are 16 bytes a thread (two of each per thread); heads
+// stride by gridDim.z (which is capped at 65535).
 __global__ void __launch_bounds__(256)
     fa_stage_transpose_kernel(const float *__restrict__ v, float *__restrict__ vt, long long BH,
                               int Nk, int nk_pad, int d) {
-  __shared__ float tile[32][33];
-  const int n0 = blockIdx.x * 32, x0 = blockIdx.y * 32;
-  const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;  // 32 x 8
+  __shared__ float tile[64][33];
+  const int n0 = blockIdx.x * 64, x0 = blockIdx.y * 32;
+  const int t = threadIdx.x;
   for (long long bh = blockIdx.z; bh < BH; bh += gridDim.z) {
 #pragma unroll
-    for (int i = 0; i < 32; i += 8) {
-      const int n = n0 + ty + i, x = x0 + tx;
-      tile[ty + i][tx] = (n < Nk && x < d) ? v[(bh * Nk + n) * d + x] : 0.f;
+    for (int i = 0; i < 2; ++i) {
+      // row r of the tile, columns 4c .. 4c+3 (d is a multiple of 32)
+      const int r = (t >> 3) + 32 * i, c = t & 7;
+      const int n = n0 + r, x = x0 + 4 * c;
+      float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (n < Nk && x < d) a = *reinterpret_cast<const float4 *>(v + (bh * Nk + n) * d + x);
+      tile[r][4 * c + 0] = a.x;
+      tile[r][4 * c + 1] = a.y;
+      tile[r][4 * c + 2] = a.z;
+      tile[r][4 * c + 3] = a.w;
     }
     __syncthreads();
 #pragma unroll
-    for (int i = 0; i < 32; i += 8) {
-      const int x = x0 + ty + i, n = n0 + tx;
-      if (x < d && n < nk_pad)
-        vt[(bh * d + x) * nk_pad + n] = __uint_as_float(to_tf32(tile[tx][ty + i]));
+    for (int i = 0; i < 2; ++i) {
+      // output row x0 + xr, keys n0 + 4u .. n0 + 4u + 3
+      const int xr = t >> 3, u = (t & 7) + 8 * i;
+      const int x = x0 + xr, n = n0 + 4 * u;
+      if (x < d && n < nk_pad) {
+        float4 b;
+        b.x = __uint_as_float(to_tf32(tile[4 * u + 0][xr]));
+        b.y = __uint_as_float(to_tf32(tile[4 * u + 1][xr]));
+        b.z = __uint_as_float(to_tf32(tile[4 * u + 2][xr]));
+        b.w = __uint_as_float(to_tf32(tile[4 * u + 3][xr]));
+        *reinterpret_cast<float4 *>(vt + (bh * d + x) * nk_pad + n) = b;
+      }
     }
     __syncthreads();
   }
@@ -68,7 +85,7 @@ cudaError_t launch_stage_f32(const float *k, const float *v, __nv_bfloat16 *kr,
                                              reinterpret_cast<uint2 *>(kl), n4);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  const dim3 grid(static_cast<unsigned>(nk_pad / 32), static_cast<unsigned>((d + 31) / 32),
+  const dim3 grid(static_cast<unsigned>(nk_pad / 64), static_cast<unsigned>((d + 31) / 32),
                   static_cast<unsigned>(BH < 65535 ? BH : 65535));
   fa_stage_transpose_kernel<<<grid, 256, 0, s>>>(v, vt, BH, Nk, nk_pad, d);
   return cudaGetLastError();

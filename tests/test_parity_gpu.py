@@ -100,6 +100,20 @@ def test_large_score_range():
         compare(o, lse, ro, rl, DTYPE_BF16, f"ramped keys causal={causal}")
 
 
+@pytest.mark.parametrize("H,Nq,Nk,causal", [(1, 1, 131072, False), (2, 300, 131072, False),
+                                            (4, 8192, 8192, True)])
+@pytest.mark.parametrize("dtype,d", _dd([(DTYPE_BF16, 128), (DTYPE_F16, 64), (DTYPE_F32, 64)]))
+def test_long_sequences(H, Nq, Nk, causal, dtype, d):
+    """Long key ranges: 1 024 key tiles through one query tile's pipeline (the
+    running offset, the row sum and O carried across all of them), and
+    8 192-token causal heads whose query tiles run 1 to 64 key tiles."""
+    q, k, v = make_inputs(1, H, Nq, Nk, d, dtype, seed=Nq + Nk + d)
+    scale = 1.0 / math.sqrt(d)
+    o, lse = run_gpu(q, k, v, scale, causal, dtype)
+    ro, rl = run_oracle(q, k, v, scale, causal)
+    compare(o, lse, ro, rl, dtype, f"Nq={Nq} Nk={Nk} causal={causal}")
+
+
 @pytest.mark.parametrize("d", [1, 8, 17, 33, 100, 128])
 def test_simt_head_dims(d):
     q, k, v = make_inputs(2, 1, 150, 150, d, DTYPE_F32_SIMT, seed=d)
