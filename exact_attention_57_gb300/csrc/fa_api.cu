@@ -311,6 +311,7 @@ int fwd_enqueue(unsigned *status, const void *q, const void *k, const void *v, v
     p.n_qtiles = ceil_div(Nq, fa::BM);
     p.scale = scale;
     p.causal = causal;
+    p.num_sms = sm_count();
     return fa::launch_simt(p, B, s) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
   }
 

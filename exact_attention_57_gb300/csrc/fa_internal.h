@@ -169,6 +169,7 @@ struct SimtParams {
   int n_qtiles;
   float scale;
   int causal;
+  int num_sms;  // SMs of the device (chooses the kernel's work split)
 };
 
 // Tensor-core forward for one (head dim, input type); causal chosen inside.

@@ -7,7 +7,7 @@
 // O = O / l and L = m + log(l) at the end — computed with fp32 FMAs.
 //
 // Differences from that page's kernel, each deliberate:
-//   * one CTA per (batch, head, 128-row query tile) instead of one per
+//   * one CTA per (batch, head, query tile of R rows) instead of one per
 //     (batch, head), so the grid does not depend on B*H;
 //   * O accumulates in registers and is written once (the page
 //     read-modify-writes O in global memory every key tile and therefore
@@ -16,11 +16,29 @@
 //     loop before a __syncthreads, a divergent-barrier hazard);
 //   * keys past Nk and, when causal, keys after the query are excluded
 //     element by element, on every tile, not only within a row's own tile.
-// One thread owns one query row (64 rows per CTA, so that small problems
-// still spread over several SMs); K/V tiles of 32 keys are staged in shared
-// memory and read as broadcasts.  The 32 dot products of a tile run side by
-// side (head-dim index outer, key inner), so no FMA waits on the previous
-// one.
+//
+// Work split.  G neighbouring lanes of a warp share one query row (R = 128/G
+// rows per 128-thread CTA).  For the scores the G lanes split the keys of a
+// shared-memory tile (lane g takes keys g, g+G, ...), each holding the whole
+// query row in registers.  The tile's row max is combined across the G lanes
+// by shuffles; each lane turns its own scores into probabilities, and the
+// lanes then hand them round (one shuffle per key) so that each lane
+// accumulates P·V for its own output columns (4-column chunks g, g+G, ...).
+// The online-softmax state (m, and the partial O) is therefore the same in
+// all G lanes and needs no merge at the end beyond summing l.
+//   G trades work per FMA against parallelism.  G = 1 (one thread per row,
+// every K/V read a broadcast, no shuffles) is the cheapest per FMA but puts
+// 128 rows in a CTA; G = 4, 8, 16 spread a smaller problem over 4, 8, 16
+// times as many CTAs at the cost of one shuffle per key and the row-max
+// shuffles.  The launcher takes the smallest G whose grid still gives every
+// SM two CTAs.  Staged rows are padded by 16 B so that the G different key
+// rows one access touches fall in different banks.
+//   K/V tiles go through a ring of NS shared-memory stages filled by
+// cp.async, NS - 1 tiles ahead of the arithmetic.  The dot products (for
+// G >= 8) and the P·V sums (for at most two column chunks per lane) are split
+// over independent partial sums so that consecutive FMAs do not wait on one
+// another.
+#include <atomic>
 #include <cmath>
 
 #include "fa_internal.h"
@@ -29,30 +47,63 @@ namespace fa {
 
 namespace {
 
-constexpr int kSimtRows = 64;   // query rows per CTA (one per thread)
+constexpr int kSimtThreads = 128;  // threads per CTA
+constexpr int kSimtKeys = 32;      // keys per shared-memory tile
+constexpr int kSimtPad = 4;        // floats of padding after each staged row
 
-// Asynchronous 4-byte copy global -> shared (cp.async; zero fill when
-// `valid` is false, in which case `src` is not read).
+// Asynchronous global -> shared copies (cp.async); when `valid` is false the
+// destination is zero-filled and `src` is not read.
 __device__ __forceinline__ void cp_async4(float *dst, const float *src, bool valid) {
   const uint32_t d = static_cast<uint32_t>(__cvta_generic_to_shared(dst));
   asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(d), "l"(src),
                "r"(valid ? 4 : 0)
                : "memory");
 }
-__device__ __forceinline__ void cp_async_wait_all() {
-  asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+__device__ __forceinline__ void cp_async16(float *dst, const float *src, bool valid) {
+  const uint32_t d = static_cast<uint32_t>(__cvta_generic_to_shared(dst));
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(d), "l"(src),
+               "r"(valid ? 16 : 0)
+               : "memory");
 }
-constexpr int kSimtKeys = 32;   // keys per shared-memory tile
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+template <int N>  // wait until at most N committed groups are still in flight
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
 
-template <int DP>  // head dim padded up to 32, 64 or 128
-__global__ void __launch_bounds__(kSimtRows) fa_simt_fwd_kernel(const SimtParams p) {
-  __shared__ float Ks[kSimtKeys * DP];
-  __shared__ float Vs[kSimtKeys * DP];
+template <int DP, int G>
+constexpr int simt_stages() {  // K/V ring depth
+  return DP >= 128 ? 3 : 4;
+}
+template <int DP, int G>
+constexpr int simt_smem_bytes() {  // K and V, simt_stages() tiles each
+  return 2 * simt_stages<DP, G>() * kSimtKeys * (DP + kSimtPad) * static_cast<int>(sizeof(float));
+}
+
+template <int DP, int G>  // DP: head dim padded up to 32, 64 or 128
+__global__ void __launch_bounds__(kSimtThreads, 1) fa_simt_fwd_kernel(const SimtParams p) {
+  constexpr int R = kSimtThreads / G;      // query rows per CTA
+  constexpr int LD = DP + kSimtPad;        // staged row stride (floats)
+  constexpr int KPL = kSimtKeys / G;       // scores per lane per tile
+  constexpr int CPL = DP / (4 * G);        // 4-column output chunks per lane
+  constexpr int TILE = kSimtKeys * LD;     // floats of one staged K (or V) tile
+  constexpr int NS = simt_stages<DP, G>();
+  constexpr int PVA = CPL <= 2 ? 2 : 1;   // P·V partial sums per output (even/odd keys)
+  constexpr int SP = KPL >= 8 ? 1 : 2;    // partial sums per dot product
+  static_assert(KPL >= 1 && CPL >= 1 && 32 % G == 0, "G must divide the warp and the tile");
+  static_assert(NS >= 2, "the ring needs two stages");
+  extern __shared__ float4 simt_smem[];
+  float *const Ks = reinterpret_cast<float *>(simt_smem);  // [NS][kSimtKeys][LD]
+  float *const Vs = Ks + NS * TILE;                        // [NS][kSimtKeys][LD]
+
   const int qt = p.causal ? (p.n_qtiles - 1 - static_cast<int>(blockIdx.x))
                           : static_cast<int>(blockIdx.x);
   const size_t bh = static_cast<size_t>(blockIdx.z) * p.H + blockIdx.y;
   const int d = p.d;
-  const int row = qt * kSimtRows + static_cast<int>(threadIdx.x);
+  const int g = static_cast<int>(threadIdx.x) % G;  // lane within the row's group
+  const int row = qt * R + static_cast<int>(threadIdx.x) / G;
   const bool active = row < p.Nq;
   const float *qh = p.q + bh * p.Nq * d;
   const float *kh = p.k + bh * p.Nk * d;
@@ -63,91 +114,226 @@ __global__ void __launch_bounds__(kSimtRows) fa_simt_fwd_kernel(const SimtParams
   const bool q_ok =
       active && FA_IN(p.status, static_cast<long long>(bh * p.Nq + row) * d, d, q_elems);
 
-  float qr[DP], acc[DP];
+  float qr[DP];
 #pragma unroll
-  for (int x = 0; x < DP; ++x) {
+  for (int x = 0; x < DP; ++x)
     qr[x] = (q_ok && x < d) ? qh[static_cast<size_t>(row) * d + x] : 0.f;
-    acc[x] = 0.f;
-  }
-  float m = -INFINITY, l = 0.f;
+
   // keys [0, row_lim) take part for this row; the CTA visits keys up to the
   // largest row_lim among its rows.
   const int row_lim = p.causal ? min(row + 1, p.Nk) : p.Nk;
-  const int cta_lim = p.causal ? min(qt * kSimtRows + kSimtRows, p.Nk) : p.Nk;
+  const int cta_lim = p.causal ? min(qt * R + R, p.Nk) : p.Nk;
+  const int n_tiles = (cta_lim + kSimtKeys - 1) / kSimtKeys;
 
-  for (int k0 = 0; k0 < cta_lim; k0 += kSimtKeys) {
-    __syncthreads();
-    // every copy of the tile in flight at once (one memory round trip)
-    for (int e = threadIdx.x; e < kSimtKeys * DP; e += kSimtRows) {
-      const int c = e / DP, x = e % DP;
-      const int key = k0 + c;
-      const bool in = key < p.Nk && x < d &&
-                      FA_IN(p.status, static_cast<long long>(bh * p.Nk + key) * d + x, 1, kv_elems);
-      const size_t off = in ? static_cast<size_t>(key) * d + x : 0;
-      cp_async4(Ks + e, kh + off, in);
-      cp_async4(Vs + e, vh + off, in);
-    }
-    cp_async_wait_all();
-    __syncthreads();
-    const int lim = row_lim - k0;  // valid columns c < lim
-    if (active && lim > 0) {
-      float s[kSimtKeys];
-#pragma unroll
-      for (int c = 0; c < kSimtKeys; ++c) s[c] = 0.f;
-#pragma unroll
-      for (int x = 0; x < DP; ++x) {
-#pragma unroll
-        for (int c = 0; c < kSimtKeys; ++c) s[c] = fmaf(qr[x], Ks[c * DP + x], s[c]);
+  // Stage key tile t (K and V rows k0 .. k0+31) into buffer `buf`; columns
+  // past d and keys past Nk are zero-filled.
+  auto stage = [&](int t, int buf) {
+    const int k0 = t * kSimtKeys;
+    float *kd = Ks + buf * TILE;
+    float *vd = Vs + buf * TILE;
+    if ((d & 3) == 0) {  // rows are whole 16-byte chunks
+      constexpr int CPR = DP / 4;
+      for (int e = static_cast<int>(threadIdx.x); e < kSimtKeys * CPR; e += kSimtThreads) {
+        const int c = e / CPR, x = (e % CPR) * 4;
+        const int key = k0 + c;
+        const bool in = key < p.Nk && x < d &&
+                        FA_IN(p.status, static_cast<long long>(bh * p.Nk + key) * d + x, 4,
+                              kv_elems);
+        const size_t off = in ? static_cast<size_t>(key) * d + x : 0;
+        cp_async16(kd + c * LD + x, kh + off, in);
+        cp_async16(vd + c * LD + x, vh + off, in);
       }
+    } else {
+      for (int e = static_cast<int>(threadIdx.x); e < kSimtKeys * DP; e += kSimtThreads) {
+        const int c = e / DP, x = e % DP;
+        const int key = k0 + c;
+        const bool in = key < p.Nk && x < d &&
+                        FA_IN(p.status, static_cast<long long>(bh * p.Nk + key) * d + x, 1,
+                              kv_elems);
+        const size_t off = in ? static_cast<size_t>(key) * d + x : 0;
+        cp_async4(kd + c * LD + x, kh + off, in);
+        cp_async4(vd + c * LD + x, vh + off, in);
+      }
+    }
+    cp_async_commit();
+  };
+
+  float acc[PVA][CPL][4];
+#pragma unroll
+  for (int a = 0; a < PVA; ++a)
+#pragma unroll
+    for (int i = 0; i < CPL; ++i)
+#pragma unroll
+      for (int u = 0; u < 4; ++u) acc[a][i][u] = 0.f;
+  float m = -INFINITY, l = 0.f;  // l: this lane's share of the row sum
+
+  // Tiles 0 .. NS-2 in flight before the loop; one copy group per tile
+  // (empty past the last tile), so that "at most NS-2 groups pending" at
+  // iteration t means tile t has landed.
+#pragma unroll 1
+  for (int t = 0; t < NS - 1; ++t) {
+    if (t < n_tiles)
+      stage(t, t);
+    else
+      cp_async_commit();
+  }
+  for (int t = 0; t < n_tiles; ++t) {
+    cp_async_wait<NS - 2>();
+    __syncthreads();  // tile t visible to all; stage (t-1) % NS no longer read
+    {
+      const int tn = t + NS - 1;
+      if (tn < n_tiles)
+        stage(tn, tn % NS);
+      else
+        cp_async_commit();
+    }
+    const int buf = t % NS;
+    const float *kt = Ks + buf * TILE;
+    const float *vt = Vs + buf * TILE;
+    const int lim = row_lim - t * kSimtKeys;  // valid tile columns c < lim
+    // A warp whose rows all end before this tile skips it (causal only);
+    // the condition is the same in all its lanes.
+    if (__any_sync(0xffffffffu, lim > 0)) {
+      // partial dot products: SP of them per key (4-column chunks taken in turn)
+      float sp[SP][KPL];
+#pragma unroll
+      for (int h = 0; h < SP; ++h)
+#pragma unroll
+        for (int j = 0; j < KPL; ++j) sp[h][j] = 0.f;
+#pragma unroll
+      for (int x = 0; x < DP; x += 4 * SP) {
+#pragma unroll
+        for (int j = 0; j < KPL; ++j) {
+#pragma unroll
+          for (int h = 0; h < SP; ++h) {
+            const int xh = x + 4 * h;
+            const float4 kv = *reinterpret_cast<const float4 *>(kt + (g + G * j) * LD + xh);
+            sp[h][j] = fmaf(qr[xh], kv.x, sp[h][j]);
+            sp[h][j] = fmaf(qr[xh + 1], kv.y, sp[h][j]);
+            sp[h][j] = fmaf(qr[xh + 2], kv.z, sp[h][j]);
+            sp[h][j] = fmaf(qr[xh + 3], kv.w, sp[h][j]);
+          }
+        }
+      }
+      float s[KPL];
       float mt = -INFINITY;
 #pragma unroll
-      for (int c = 0; c < kSimtKeys; ++c) {
-        s[c] *= p.scale;
-        if (c < lim) mt = fmaxf(mt, s[c]);
+      for (int j = 0; j < KPL; ++j) {
+        float dot = sp[0][j];
+#pragma unroll
+        for (int h = 1; h < SP; ++h) dot += sp[h][j];
+        s[j] = (g + G * j < lim) ? dot * p.scale : -INFINITY;
+        mt = fmaxf(mt, s[j]);
       }
+#pragma unroll
+      for (int o = G / 2; o > 0; o >>= 1) mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, o, G));
+      // Key 0 is in the first tile of every row, so m is finite from then on
+      // and a fully masked later tile leaves it unchanged (alpha = 1).
       const float m_new = fmaxf(m, mt);
-      const float alpha = expf(m - m_new);  // 0 on the first visited tile
+      const float alpha = expf(m - m_new);  // 0 on the first tile
       l *= alpha;
 #pragma unroll
-      for (int x = 0; x < DP; ++x) acc[x] *= alpha;
+      for (int a = 0; a < PVA; ++a)
 #pragma unroll
-      for (int c = 0; c < kSimtKeys; ++c) {
-        const float pc = (c < lim) ? expf(s[c] - m_new) : 0.f;
-        l += pc;
+        for (int i = 0; i < CPL; ++i)
 #pragma unroll
-        for (int x = 0; x < DP; ++x) acc[x] = fmaf(pc, Vs[c * DP + x], acc[x]);
+          for (int u = 0; u < 4; ++u) acc[a][i][u] *= alpha;
+      float pr[KPL];
+#pragma unroll
+      for (int j = 0; j < KPL; ++j) {
+        pr[j] = expf(s[j] - m_new);  // 0 for masked keys
+        l += pr[j];
       }
       m = m_new;
+      // P·V: the probability of key c comes from lane c % G of the group.
+#pragma unroll
+      for (int c = 0; c < kSimtKeys; ++c) {
+        float pc;
+        if constexpr (G == 1)
+          pc = pr[c];
+        else
+          pc = __shfl_sync(0xffffffffu, pr[c / G], c % G, G);
+        const float *vr = vt + c * LD;
+        float(&ac)[CPL][4] = acc[c % PVA];
+#pragma unroll
+        for (int i = 0; i < CPL; ++i) {
+          const float4 vv = *reinterpret_cast<const float4 *>(vr + 4 * (i * G + g));
+          ac[i][0] = fmaf(pc, vv.x, ac[i][0]);
+          ac[i][1] = fmaf(pc, vv.y, ac[i][1]);
+          ac[i][2] = fmaf(pc, vv.z, ac[i][2]);
+          ac[i][3] = fmaf(pc, vv.w, ac[i][3]);
+        }
+      }
     }
   }
+  cp_async_wait<0>();  // only empty groups can still be open; close them all
+#pragma unroll
+  for (int a = 1; a < PVA; ++a)
+#pragma unroll
+    for (int i = 0; i < CPL; ++i)
+#pragma unroll
+      for (int u = 0; u < 4; ++u) acc[0][i][u] += acc[a][i][u];
+
+#pragma unroll
+  for (int o = G / 2; o > 0; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o, G);
   if (active) {
     const float inv_l = 1.f / l;
     float *orow = p.o + (bh * p.Nq + row) * d;
     if (FA_IN(p.status, static_cast<long long>(bh * p.Nq + row) * d, d, q_elems)) {
 #pragma unroll
-      for (int x = 0; x < DP; ++x)
-        if (x < d) orow[x] = acc[x] * inv_l;
+      for (int i = 0; i < CPL; ++i) {
+        const int x = 4 * (i * G + g);
+        if ((d & 3) == 0) {
+          if (x < d)
+            *reinterpret_cast<float4 *>(orow + x) =
+                make_float4(acc[0][i][0] * inv_l, acc[0][i][1] * inv_l,
+                            acc[0][i][2] * inv_l, acc[0][i][3] * inv_l);
+        } else {
+#pragma unroll
+          for (int u = 0; u < 4; ++u)
+            if (x + u < d) orow[x + u] = acc[0][i][u] * inv_l;
+        }
+      }
     }
-    if (FA_IN(p.status, bh * p.Nq + row, 1, planes * p.Nq)) p.lse[bh * p.Nq + row] = m + logf(l);
+    if (g == 0 && FA_IN(p.status, bh * p.Nq + row, 1, planes * p.Nq))
+      p.lse[bh * p.Nq + row] = m + logf(l);
   }
 }
 
-template <int DP>
+template <int DP, int G>
 cudaError_t launch_simt_dp(const SimtParams &p_in, int B, cudaStream_t s) {
+  constexpr int R = kSimtThreads / G;
+  constexpr int smem = simt_smem_bytes<DP, G>();
+  static std::atomic<unsigned long long> attr_done;
+  cudaError_t e = smem_attr_once(fa_simt_fwd_kernel<DP, G>, smem, &attr_done);
+  if (e != cudaSuccess) return e;
   SimtParams p = p_in;
-  p.n_qtiles = (p.Nq + kSimtRows - 1) / kSimtRows;  // this kernel's row tiles
+  p.n_qtiles = (p.Nq + R - 1) / R;  // this kernel's row tiles
   dim3 grid(static_cast<unsigned>(p.n_qtiles), static_cast<unsigned>(p.H),
             static_cast<unsigned>(B));
-  fa_simt_fwd_kernel<DP><<<grid, kSimtRows, 0, s>>>(p);
+  fa_simt_fwd_kernel<DP, G><<<grid, kSimtThreads, smem, s>>>(p);
   return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_simt(const SimtParams &p, int B, cudaStream_t s) {
-  if (p.d <= 32) return launch_simt_dp<32>(p, B, s);
-  if (p.d <= 64) return launch_simt_dp<64>(p, B, s);
-  return launch_simt_dp<128>(p, B, s);
+  // The fewest lanes per row (the least shuffling and the fewest shared-memory
+  // reads per FMA) whose grid still puts two CTAs on every SM; small problems
+  // take the widest split.  G = 1 holds 64 output columns per thread at most,
+  // and head dim 32 has only 8 four-column chunks to share out.
+  const long long planes = static_cast<long long>(B) * p.H;
+  const long long want = 2LL * (p.num_sms > 0 ? p.num_sms : 1);
+  auto fills = [&](int g) { return planes * ((p.Nq + kSimtThreads / g - 1) / (kSimtThreads / g)) >= want; };
+  if (p.d <= 32)
+    return fills(1) ? launch_simt_dp<32, 1>(p, B, s)
+         : fills(4) ? launch_simt_dp<32, 4>(p, B, s)
+                    : launch_simt_dp<32, 8>(p, B, s);
+  if (p.d <= 64)
+    return fills(1) ? launch_simt_dp<64, 1>(p, B, s)
+         : fills(4) ? launch_simt_dp<64, 4>(p, B, s)
+                    : launch_simt_dp<64, 16>(p, B, s);
+  return fills(4) ? launch_simt_dp<128, 4>(p, B, s) : launch_simt_dp<128, 16>(p, B, s);
 }
 
 }  // namespace fa
