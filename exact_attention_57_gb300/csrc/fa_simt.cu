@@ -42,6 +42,7 @@
 #include <cmath>
 
 #include "fa_internal.h"
+#include "ptx.cuh"
 
 namespace fa {
 
@@ -111,6 +112,12 @@ __global__ void __launch_bounds__(kSimtThreads, 1) fa_simt_fwd_kernel(const Simt
   // extents for the debug build's index checks
   const long long planes = static_cast<long long>(p.B) * p.H;
   const long long q_elems = planes * p.Nq * d, kv_elems = planes * p.Nk * d;
+  // Launched with programmatic stream serialization: wait for the previous
+  // kernel on the stream before the first global access (the debug build's
+  // index checks write the status word), then let the next one start
+  // launching.
+  griddep_wait();
+  griddep_launch_dependents();
   const bool q_ok =
       active && FA_IN(p.status, static_cast<long long>(bh * p.Nq + row) * d, d, q_elems);
 
@@ -309,10 +316,18 @@ cudaError_t launch_simt_dp(const SimtParams &p_in, int B, cudaStream_t s) {
   if (e != cudaSuccess) return e;
   SimtParams p = p_in;
   p.n_qtiles = (p.Nq + R - 1) / R;  // this kernel's row tiles
-  dim3 grid(static_cast<unsigned>(p.n_qtiles), static_cast<unsigned>(p.H),
-            static_cast<unsigned>(B));
-  fa_simt_fwd_kernel<DP, G><<<grid, kSimtThreads, smem, s>>>(p);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(p.n_qtiles), static_cast<unsigned>(p.H),
+                     static_cast<unsigned>(B));
+  cfg.blockDim = dim3(kSimtThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, fa_simt_fwd_kernel<DP, G>, p);
 }
 
 }  // namespace

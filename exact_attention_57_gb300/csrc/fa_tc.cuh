@@ -199,6 +199,7 @@ __global__ void __launch_bounds__(224, 1)
   int Nq = p.Nq, Nk = p.Nk, q_row0 = 0, k_row0 = 0, hc = bh;
   int n_qtiles = p.n_qtiles, n_ktiles = p.n_ktiles;
   if (p.cu_q != nullptr) {
+    griddep_wait();  // the offsets are in global memory
     const int b = static_cast<int>(blockIdx.z);
     // Offsets clamped to [0, total]: row indices never leave the tensors,
     // and bad offsets cannot make a CTA walk more key tiles than exist.
@@ -313,6 +314,11 @@ __global__ void __launch_bounds__(224, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  // Launched with programmatic stream serialization, the set-up above
+  // overlaps the previous kernel's tail; its outputs may be this kernel's
+  // inputs, so no global memory is touched before this point.
+  griddep_wait();
+  griddep_launch_dependents();
   const uint32_t tmem = *tmem_slot;
   WaitCtl w{abort_flag, p.status, p.wait_limit_ns, 0u};
 
@@ -1087,8 +1093,11 @@ cudaError_t launch_tc(const CUtensorMap &q, const CUtensorMap &k, const CUtensor
   cfg.blockDim = dim3(C::THREADS, 1, 1);
   cfg.dynamicSmemBytes = C::SMEM_BYTES;
   cfg.stream = stream;
-  cfg.attrs = nullptr;
-  cfg.numAttrs = 0;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, kern, q, k, v, o, klo, p);
 }
 

@@ -19,6 +19,21 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
   return t;
 }
 
+// ------------------------------------------- programmatic dependent launch
+// A kernel launched with programmatic stream serialization may start while
+// the previous kernel on its stream is still running.  griddep_wait() blocks
+// until that kernel has completed and its memory operations are visible, so
+// every global load or store of this kernel's buffers must come after it;
+// without the launch attribute it returns at once.  griddep_launch_dependents()
+// lets the next such kernel start launching once every CTA of this grid has
+// issued it (or exited); it does not make the next kernel skip its own wait.
+__device__ __forceinline__ void griddep_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ------------------------------------------------------------------ mbarrier
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
