@@ -74,37 +74,47 @@ __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
-template <int DP, int G>
-constexpr int simt_stages() {  // K/V ring depth
-  return DP >= 128 ? 3 : 4;
+template <int DP, int KS>
+constexpr int simt_stages() {  // K/V ring depth: 2 to 4 stages within ~108 KB
+  constexpr int stage = 2 * KS * kSimtKeys * (DP + kSimtPad) * static_cast<int>(sizeof(float));
+  return 110592 / stage > 4 ? 4 : (110592 / stage < 2 ? 2 : 110592 / stage);
 }
-template <int DP, int G>
-constexpr int simt_smem_bytes() {  // K and V, simt_stages() tiles each
-  return 2 * simt_stages<DP, G>() * kSimtKeys * (DP + kSimtPad) * static_cast<int>(sizeof(float));
+template <int DP, int KS>
+constexpr int simt_smem_bytes() {  // K and V, simt_stages() stages each
+  return 2 * simt_stages<DP, KS>() * KS * kSimtKeys * (DP + kSimtPad) *
+         static_cast<int>(sizeof(float));
 }
 
-template <int DP, int G>  // DP: head dim padded up to 32, 64 or 128
+// KS: key groups.  The CTA's threads form KS groups of 128/KS (whole warps);
+// group k takes key sub-tile k of every stage of KS*32 keys for the same
+// rows, and the groups' softmax states are merged at the end.
+template <int DP, int G, int KS>  // DP: head dim padded up to 32, 64 or 128
 __global__ void __launch_bounds__(kSimtThreads, 1) fa_simt_fwd_kernel(const SimtParams p) {
-  constexpr int R = kSimtThreads / G;      // query rows per CTA
+  constexpr int TPG = kSimtThreads / KS;   // threads per key group
+  constexpr int R = TPG / G;               // query rows per CTA
   constexpr int LD = DP + kSimtPad;        // staged row stride (floats)
-  constexpr int KPL = kSimtKeys / G;       // scores per lane per tile
+  constexpr int KPL = kSimtKeys / G;       // scores per lane per sub-tile
   constexpr int CPL = DP / (4 * G);        // 4-column output chunks per lane
-  constexpr int TILE = kSimtKeys * LD;     // floats of one staged K (or V) tile
-  constexpr int NS = simt_stages<DP, G>();
+  constexpr int SUB = kSimtKeys * LD;      // floats of one staged K (or V) sub-tile
+  constexpr int TILE = KS * SUB;           // floats of one stage of K (or V)
+  constexpr int NS = simt_stages<DP, KS>();
   constexpr int PVA = CPL <= 2 ? 2 : 1;   // P·V partial sums per output (even/odd keys)
   constexpr int SP = KPL >= 8 ? 1 : 2;    // partial sums per dot product
   static_assert(KPL >= 1 && CPL >= 1 && 32 % G == 0, "G must divide the warp and the tile");
+  static_assert(TPG % 32 == 0, "a key group is whole warps");
   static_assert(NS >= 2, "the ring needs two stages");
   extern __shared__ float4 simt_smem[];
-  float *const Ks = reinterpret_cast<float *>(simt_smem);  // [NS][kSimtKeys][LD]
-  float *const Vs = Ks + NS * TILE;                        // [NS][kSimtKeys][LD]
+  float *const Ks = reinterpret_cast<float *>(simt_smem);  // [NS][KS*kSimtKeys][LD]
+  float *const Vs = Ks + NS * TILE;                        // [NS][KS*kSimtKeys][LD]
 
   const int qt = p.causal ? (p.n_qtiles - 1 - static_cast<int>(blockIdx.x))
                           : static_cast<int>(blockIdx.x);
   const size_t bh = static_cast<size_t>(blockIdx.z) * p.H + blockIdx.y;
   const int d = p.d;
-  const int g = static_cast<int>(threadIdx.x) % G;  // lane within the row's group
-  const int row = qt * R + static_cast<int>(threadIdx.x) / G;
+  const int ks = static_cast<int>(threadIdx.x) / TPG;  // key group (warp-uniform)
+  const int tig = static_cast<int>(threadIdx.x) % TPG;
+  const int g = tig % G;  // lane within the row's group
+  const int row = qt * R + tig / G;
   const bool active = row < p.Nq;
   const float *qh = p.q + bh * p.Nq * d;
   const float *kh = p.k + bh * p.Nk * d;
@@ -130,17 +140,17 @@ __global__ void __launch_bounds__(kSimtThreads, 1) fa_simt_fwd_kernel(const Simt
   // largest row_lim among its rows.
   const int row_lim = p.causal ? min(row + 1, p.Nk) : p.Nk;
   const int cta_lim = p.causal ? min(qt * R + R, p.Nk) : p.Nk;
-  const int n_tiles = (cta_lim + kSimtKeys - 1) / kSimtKeys;
+  const int n_tiles = (cta_lim + KS * kSimtKeys - 1) / (KS * kSimtKeys);
 
-  // Stage key tile t (K and V rows k0 .. k0+31) into buffer `buf`; columns
-  // past d and keys past Nk are zero-filled.
+  // Stage key tile t (K and V rows k0 .. k0 + KS*32 - 1) into buffer `buf`;
+  // columns past d and keys past Nk are zero-filled.
   auto stage = [&](int t, int buf) {
-    const int k0 = t * kSimtKeys;
+    const int k0 = t * KS * kSimtKeys;
     float *kd = Ks + buf * TILE;
     float *vd = Vs + buf * TILE;
     if ((d & 3) == 0) {  // rows are whole 16-byte chunks
       constexpr int CPR = DP / 4;
-      for (int e = static_cast<int>(threadIdx.x); e < kSimtKeys * CPR; e += kSimtThreads) {
+      for (int e = static_cast<int>(threadIdx.x); e < KS * kSimtKeys * CPR; e += kSimtThreads) {
         const int c = e / CPR, x = (e % CPR) * 4;
         const int key = k0 + c;
         const bool in = key < p.Nk && x < d &&
@@ -151,7 +161,7 @@ __global__ void __launch_bounds__(kSimtThreads, 1) fa_simt_fwd_kernel(const Simt
         cp_async16(vd + c * LD + x, vh + off, in);
       }
     } else {
-      for (int e = static_cast<int>(threadIdx.x); e < kSimtKeys * DP; e += kSimtThreads) {
+      for (int e = static_cast<int>(threadIdx.x); e < KS * kSimtKeys * DP; e += kSimtThreads) {
         const int c = e / DP, x = e % DP;
         const int key = k0 + c;
         const bool in = key < p.Nk && x < d &&
@@ -195,9 +205,9 @@ __global__ void __launch_bounds__(kSimtThreads, 1) fa_simt_fwd_kernel(const Simt
         cp_async_commit();
     }
     const int buf = t % NS;
-    const float *kt = Ks + buf * TILE;
-    const float *vt = Vs + buf * TILE;
-    const int lim = row_lim - t * kSimtKeys;  // valid tile columns c < lim
+    const float *kt = Ks + buf * TILE + ks * SUB;  // this group's sub-tile
+    const float *vt = Vs + buf * TILE + ks * SUB;
+    const int lim = row_lim - (t * KS + ks) * kSimtKeys;  // valid sub-tile columns c < lim
     // A warp whose rows all end before this tile skips it (causal only);
     // the condition is the same in all its lanes.
     if (__any_sync(0xffffffffu, lim > 0)) {
@@ -234,10 +244,13 @@ __global__ void __launch_bounds__(kSimtThreads, 1) fa_simt_fwd_kernel(const Simt
       }
 #pragma unroll
       for (int o = G / 2; o > 0; o >>= 1) mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, o, G));
-      // Key 0 is in the first tile of every row, so m is finite from then on
-      // and a fully masked later tile leaves it unchanged (alpha = 1).
+      // A group that has seen no valid key of the row yet keeps m = -inf;
+      // m_use = 0 then makes alpha and every p exactly 0 instead of NaN.
+      // Otherwise m_use = m_new: alpha = 0 on the first valid sub-tile, and
+      // 1 on a later fully masked one.
       const float m_new = fmaxf(m, mt);
-      const float alpha = expf(m - m_new);  // 0 on the first tile
+      const float m_use = m_new == -INFINITY ? 0.f : m_new;
+      const float alpha = expf(m - m_use);
       l *= alpha;
 #pragma unroll
       for (int a = 0; a < PVA; ++a)
@@ -248,7 +261,7 @@ __global__ void __launch_bounds__(kSimtThreads, 1) fa_simt_fwd_kernel(const Simt
       float pr[KPL];
 #pragma unroll
       for (int j = 0; j < KPL; ++j) {
-        pr[j] = expf(s[j] - m_new);  // 0 for masked keys
+        pr[j] = expf(s[j] - m_use);  // 0 for masked keys
         l += pr[j];
       }
       m = m_new;
@@ -281,6 +294,40 @@ __global__ void __launch_bounds__(kSimtThreads, 1) fa_simt_fwd_kernel(const Simt
 #pragma unroll
       for (int u = 0; u < 4; ++u) acc[0][i][u] += acc[a][i][u];
 
+  if constexpr (KS > 1) {
+    // Key groups 1 .. KS-1 leave (m, l, O) per thread in shared memory (the
+    // ring is no longer read); group 0 merges them into its own:
+    // m' = max m_k, l' = sum l_k exp(m_k - m'), O' likewise.  Group 0 holds
+    // key 0 of every row, so m' is finite.
+    constexpr int W = 2 + 4 * CPL;  // floats per thread
+    float *red = Ks;
+    __syncthreads();
+    if (ks > 0) {
+      float *dst = red + ((ks - 1) * TPG + tig) * W;
+      dst[0] = m;
+      dst[1] = l;
+#pragma unroll
+      for (int i = 0; i < CPL; ++i)
+#pragma unroll
+        for (int u = 0; u < 4; ++u) dst[2 + 4 * i + u] = acc[0][i][u];
+    }
+    __syncthreads();
+    if (ks > 0) return;  // whole warps: the shuffles below see full warps
+#pragma unroll
+    for (int k = 1; k < KS; ++k) {
+      const float *src = red + ((k - 1) * TPG + tig) * W;
+      const float mk = src[0];
+      const float mm = fmaxf(m, mk);
+      const float a0 = expf(m - mm), a1 = expf(mk - mm);  // a1 = 0 when mk = -inf
+      l = l * a0 + src[1] * a1;
+#pragma unroll
+      for (int i = 0; i < CPL; ++i)
+#pragma unroll
+        for (int u = 0; u < 4; ++u) acc[0][i][u] = acc[0][i][u] * a0 + src[2 + 4 * i + u] * a1;
+      m = mm;
+    }
+  }
+
 #pragma unroll
   for (int o = G / 2; o > 0; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o, G);
   if (active) {
@@ -307,12 +354,12 @@ __global__ void __launch_bounds__(kSimtThreads, 1) fa_simt_fwd_kernel(const Simt
   }
 }
 
-template <int DP, int G>
+template <int DP, int G, int KS = 1>
 cudaError_t launch_simt_dp(const SimtParams &p_in, int B, cudaStream_t s) {
-  constexpr int R = kSimtThreads / G;
-  constexpr int smem = simt_smem_bytes<DP, G>();
+  constexpr int R = kSimtThreads / (G * KS);
+  constexpr int smem = simt_smem_bytes<DP, KS>();
   static std::atomic<unsigned long long> attr_done;
-  cudaError_t e = smem_attr_once(fa_simt_fwd_kernel<DP, G>, smem, &attr_done);
+  cudaError_t e = smem_attr_once(fa_simt_fwd_kernel<DP, G, KS>, smem, &attr_done);
   if (e != cudaSuccess) return e;
   SimtParams p = p_in;
   p.n_qtiles = (p.Nq + R - 1) / R;  // this kernel's row tiles
@@ -327,7 +374,7 @@ cudaError_t launch_simt_dp(const SimtParams &p_in, int B, cudaStream_t s) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, fa_simt_fwd_kernel<DP, G>, p);
+  return cudaLaunchKernelEx(&cfg, fa_simt_fwd_kernel<DP, G, KS>, p);
 }
 
 }  // namespace
@@ -336,19 +383,40 @@ cudaError_t launch_simt(const SimtParams &p, int B, cudaStream_t s) {
   // The fewest lanes per row (the least shuffling and the fewest shared-memory
   // reads per FMA) whose grid still puts two CTAs on every SM; small problems
   // take the widest split.  G = 1 holds 64 output columns per thread at most,
-  // and head dim 32 has only 8 four-column chunks to share out.
+  // and head dim 32 has only 8 four-column chunks to share out.  A grid still
+  // short of that at the widest split also splits each row's keys over KS
+  // warp groups (the most, up to 4, that keeps it within two CTAs per SM).
   const long long planes = static_cast<long long>(B) * p.H;
   const long long want = 2LL * (p.num_sms > 0 ? p.num_sms : 1);
-  auto fills = [&](int g) { return planes * ((p.Nq + kSimtThreads / g - 1) / (kSimtThreads / g)) >= want; };
-  if (p.d <= 32)
-    return fills(1) ? launch_simt_dp<32, 1>(p, B, s)
-         : fills(4) ? launch_simt_dp<32, 4>(p, B, s)
-                    : launch_simt_dp<32, 8>(p, B, s);
-  if (p.d <= 64)
-    return fills(1) ? launch_simt_dp<64, 1>(p, B, s)
-         : fills(4) ? launch_simt_dp<64, 4>(p, B, s)
-                    : launch_simt_dp<64, 16>(p, B, s);
-  return fills(4) ? launch_simt_dp<128, 4>(p, B, s) : launch_simt_dp<128, 16>(p, B, s);
+  auto ctas = [&](int g, int ks) {
+    const int r = kSimtThreads / (g * ks);
+    return planes * ((p.Nq + r - 1) / r);
+  };
+  auto fills = [&](int g) { return ctas(g, 1) >= want; };
+  auto key_groups = [&](int g, int most) {
+    int k = 1;
+    while (k < most && ctas(g, 2 * k) <= want) k *= 2;
+    return k;
+  };
+  if (p.d <= 32) {
+    if (fills(1)) return launch_simt_dp<32, 1>(p, B, s);
+    if (fills(4)) return launch_simt_dp<32, 4>(p, B, s);
+    const int k = key_groups(8, 4);
+    return k == 4 ? launch_simt_dp<32, 8, 4>(p, B, s)
+         : k == 2 ? launch_simt_dp<32, 8, 2>(p, B, s)
+                  : launch_simt_dp<32, 8, 1>(p, B, s);
+  }
+  if (p.d <= 64) {
+    if (fills(1)) return launch_simt_dp<64, 1>(p, B, s);
+    if (fills(4)) return launch_simt_dp<64, 4>(p, B, s);
+    const int k = key_groups(16, 4);
+    return k == 4 ? launch_simt_dp<64, 16, 4>(p, B, s)
+         : k == 2 ? launch_simt_dp<64, 16, 2>(p, B, s)
+                  : launch_simt_dp<64, 16, 1>(p, B, s);
+  }
+  if (fills(4)) return launch_simt_dp<128, 4>(p, B, s);
+  return key_groups(16, 2) == 2 ? launch_simt_dp<128, 16, 2>(p, B, s)
+                                : launch_simt_dp<128, 16, 1>(p, B, s);
 }
 
 }  // namespace fa
