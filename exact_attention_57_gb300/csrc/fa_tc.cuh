@@ -102,9 +102,12 @@ struct TcCfg {
   static constexpr int KCH = S16 ? D * 2 / 128 : D * ESZ / 128;
   static constexpr int K_CH_ELEMS = S16 ? 64 : 128 / ESZ;
   static constexpr int K_TILE_BYTES = KCH * 128 * 128;
-  // Q is the A operand of S = Q K^T: from tensor memory when it fits after O,
-  // else from shared memory (bf16, D = 128).
-  static constexpr bool QTMEM = COL_O + D + NQSPLIT * Q_COLS <= TMEM_COLS;
+  // Q is the A operand of S = Q K^T.  The fp32 path rounds (splits) it on
+  // its way into tensor memory; the 16-bit path loads it into shared memory
+  // by TMA, even at D = 64 where it would fit in tensor memory: there the S
+  // products' tensor-memory reads competed with the softmax warps' loads and
+  // stores, and the kernel ran 3% slower.
+  static constexpr bool QTMEM = TF32 && COL_O + D + NQSPLIT * Q_COLS <= TMEM_COLS;
   static constexpr uint32_t COL_Q = COL_O + D;
   static constexpr uint32_t COL_QLO = COL_Q + Q_COLS;      // fp32 path: Q_lo
   static constexpr int NQ = QTMEM ? 0 : 1;                  // Q tiles in shared memory
