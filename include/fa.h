@@ -38,6 +38,12 @@
  * Scale:    any finite float; it multiplies q.k before the softmax.
  * Streams:  `stream` is a cudaStream_t passed as void*; NULL means the legacy
  *           default stream.  Work is enqueued asynchronously on that stream.
+ *           The forward kernels are launched with programmatic stream
+ *           serialization: a CTA may start its set-up (shared and tensor
+ *           memory, barriers) while the previous kernel on the stream is
+ *           still running, but it reads and writes no global memory before
+ *           that kernel has completed, so stream order holds for every
+ *           buffer as with a plain launch.
  * Ownership: the caller owns every buffer.  The library never frees caller
  *           memory and never keeps a pointer after the call returns.  Its
  *           only allocation is one small per-device status buffer, made with
