@@ -19,30 +19,38 @@ __device__ __forceinline__ void split_bf16x2(float x0, float x1, uint32_t &hi, u
   lo = pack_bf16x2(x0 - __uint_as_float(hi << 16), x1 - __uint_as_float(hi & 0xffff0000u));
 }
 
-__global__ void fa_stage_split_kernel(const float4 *__restrict__ k, uint2 *__restrict__ kr,
-                                      uint2 *__restrict__ kl, long long n4) {
-  for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < n4;
-       i += static_cast<long long>(gridDim.x) * blockDim.x) {
-    const float4 a = k[i];
-    uint2 h, l;
-    split_bf16x2(a.x, a.y, h.x, l.x);
-    split_bf16x2(a.z, a.w, h.y, l.y);
-    kr[i] = h;
-    kl[i] = l;
-  }
-}
-
-// One 64-key x 32-column tile per block and head: v[n0 + r][x0 + c] ->
-// vt[x0 + c][n0 + r], rounded to tf32; keys n0 + r >= Nk give 0 up to nk_pad.
-// Loads and stores are 16 bytes a thread (two of each per thread); heads
-// stride by gridDim.z (which is capped at 65535).
+// One launch for both passes, side by side: blocks [0, split_blocks) split K
+// (a grid-stride loop over its float4s), the others transpose V, one
+// 64-key x 32-column tile of one head at a time: v[n0 + r][x0 + c] ->
+// vt[x0 + c][n0 + r], rounded to tf32; keys n0 + r >= Nk give 0 up to
+// nk_pad.  Both are bound by memory; sharing the GPU, each fills the other's
+// gaps, and the call pays one launch.
 __global__ void __launch_bounds__(256)
-    fa_stage_transpose_kernel(const float *__restrict__ v, float *__restrict__ vt, long long BH,
-                              int Nk, int nk_pad, int d) {
+    fa_stage_kernel(const float4 *__restrict__ k, uint2 *__restrict__ kr,
+                    uint2 *__restrict__ kl, long long n4, int split_blocks,
+                    const float *__restrict__ v, float *__restrict__ vt, long long BH, int Nk,
+                    int nk_pad, int d) {
+  if (static_cast<int>(blockIdx.x) < split_blocks) {
+    for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < n4;
+         i += static_cast<long long>(split_blocks) * blockDim.x) {
+      const float4 a = k[i];
+      uint2 h, l;
+      split_bf16x2(a.x, a.y, h.x, l.x);
+      split_bf16x2(a.z, a.w, h.y, l.y);
+      kr[i] = h;
+      kl[i] = l;
+    }
+    return;  // the whole block: no barrier below is shared with it
+  }
   __shared__ float tile[64][33];
-  const int n0 = blockIdx.x * 64, x0 = blockIdx.y * 32;
+  const long long ntn = nk_pad / 64, ntx = (d + 31) / 32;
+  const long long ntiles = ntn * ntx * BH;
   const int t = threadIdx.x;
-  for (long long bh = blockIdx.z; bh < BH; bh += gridDim.z) {
+  for (long long ti = static_cast<long long>(blockIdx.x) - split_blocks; ti < ntiles;
+       ti += static_cast<long long>(gridDim.x) - split_blocks) {
+    const int n0 = static_cast<int>(ti % ntn) * 64;
+    const int x0 = static_cast<int>((ti / ntn) % ntx) * 32;
+    const long long bh = ti / (ntn * ntx);
 #pragma unroll
     for (int i = 0; i < 2; ++i) {
       // row r of the tile, columns 4c .. 4c+3 (d is a multiple of 32)
@@ -80,14 +88,17 @@ cudaError_t launch_stage_f32(const float *k, const float *v, __nv_bfloat16 *kr,
                              __nv_bfloat16 *kl, float *vt, int BH, int Nk, int nk_pad, int d,
                              cudaStream_t s) {
   const long long n4 = static_cast<long long>(BH) * Nk * d / 4;  // d is a multiple of 32
-  fa_stage_split_kernel<<<1216, 256, 0, s>>>(reinterpret_cast<const float4 *>(k),
-                                             reinterpret_cast<uint2 *>(kr),
-                                             reinterpret_cast<uint2 *>(kl), n4);
-  cudaError_t e = cudaGetLastError();
+  // 8 blocks of 256 threads fill an SM: half of them split K, half
+  // transpose V (the two move the same bytes).
+  int dev = 0, sms = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return e;
-  const dim3 grid(static_cast<unsigned>(nk_pad / 64), static_cast<unsigned>((d + 31) / 32),
-                  static_cast<unsigned>(BH < 65535 ? BH : 65535));
-  fa_stage_transpose_kernel<<<grid, 256, 0, s>>>(v, vt, BH, Nk, nk_pad, d);
+  const int half = 4 * (sms > 0 ? sms : 1);
+  fa_stage_kernel<<<2 * half, 256, 0, s>>>(reinterpret_cast<const float4 *>(k),
+                                          reinterpret_cast<uint2 *>(kr),
+                                          reinterpret_cast<uint2 *>(kl), n4, half, v, vt, BH,
+                                          Nk, nk_pad, d);
   return cudaGetLastError();
 }
 
