@@ -5,6 +5,8 @@
 // the K-major V^T the tf32 P V product takes, instead of both being
 // converted by every query-tile CTA.  Rounding: to nearest even for bf16, to
 // nearest (ties away) for tf32.
+#include <atomic>
+
 #include "fa_internal.h"
 #include "ptx.cuh"
 
@@ -89,11 +91,18 @@ cudaError_t launch_stage_f32(const float *k, const float *v, __nv_bfloat16 *kr,
                              cudaStream_t s) {
   const long long n4 = static_cast<long long>(BH) * Nk * d / 4;  // d is a multiple of 32
   // 8 blocks of 256 threads fill an SM: half of them split K, half
-  // transpose V (the two move the same bytes).
-  int dev = 0, sms = 0;
+  // transpose V (the two move the same bytes).  The SM count is read once
+  // per device.
+  static std::atomic<int> sm_cache[64];
+  int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
-  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return e;
+  int sms = (dev >= 0 && dev < 64) ? sm_cache[dev].load(std::memory_order_relaxed) : 0;
+  if (sms == 0) {
+    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64) sm_cache[dev].store(sms, std::memory_order_relaxed);
+  }
   const int half = 4 * (sms > 0 ? sms : 1);
   fa_stage_kernel<<<2 * half, 256, 0, s>>>(reinterpret_cast<const float4 *>(k),
                                           reinterpret_cast<uint2 *>(kr),
