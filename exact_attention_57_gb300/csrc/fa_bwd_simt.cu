@@ -21,6 +21,7 @@
 
 #include "fa.h"
 #include "fa_internal.h"
+#include "ptx.cuh"
 
 namespace fa {
 
@@ -59,18 +60,28 @@ struct SimtBwdParams {
   int causal;
 };
 
-// Shared memory: K, V, Q, dO tiles of 64 rows with a row stride of d + 1
-// floats (conflict-free column walks), then P and dS (64 x 65 each), then
-// the tile's LSE and D.
-__host__ __device__ inline size_t simt_bwd_smem(int d) {
-  const size_t row = static_cast<size_t>(d) + 1;
+// Shared memory: K, V, Q, dO tiles of 64 rows of DP + 4 floats (columns
+// past d zero; rows 16-byte aligned for float4 reads, and the 4-float
+// offset spreads eight consecutive rows over all banks), then P and dS
+// (64 x 65 each), then the tile's LSE and D.
+__host__ __device__ inline size_t simt_bwd_smem(int dp) {
+  const size_t row = static_cast<size_t>(dp) + 4;
   return (4 * 64 * row + 2 * 64 * 65 + 2 * 64) * sizeof(float);
 }
 
+__device__ __forceinline__ float4 ld4(const float *p) {
+  return *reinterpret_cast<const float4 *>(p);
+}
+
 template <int DP>  // head dim padded up to 32, 64 or 128
-__global__ void __launch_bounds__(kSbThreads) fa_bwd_simt_kernel(const SimtBwdParams p) {
-  extern __shared__ float sm[];
-  const int d = p.d, rs = d + 1;
+// (two blocks an SM up to head dim 64; at 128 the accumulators need more
+// than 128 registers a thread)
+__global__ void __launch_bounds__(kSbThreads, DP <= 64 ? 2 : 1)
+    fa_bwd_simt_kernel(const SimtBwdParams p) {
+  extern __shared__ float4 sm4[];
+  float *sm = reinterpret_cast<float *>(sm4);
+  const int d = p.d;
+  constexpr int rs = DP + 4;
   float *Ks = sm, *Vs = Ks + 64 * rs, *Qs = Vs + 64 * rs, *dOs = Qs + 64 * rs;
   float *Ps = dOs + 64 * rs, *dSs = Ps + 64 * 65, *lse_s = dSs + 64 * 65, *dd_s = lse_s + 64;
 
@@ -82,12 +93,12 @@ __global__ void __launch_bounds__(kSbThreads) fa_bwd_simt_kernel(const SimtBwdPa
   const long long rows_q = static_cast<long long>(p.B) * p.H * p.Nq;
   const float *qh = p.q + bh * p.Nq * d, *doh = p.dout + bh * p.Nq * d;
 
-  // K and V of this block (rows past Nk read as zeros)
-  for (int e = t; e < 64 * d; e += kSbThreads) {
-    const int j = e / d, x = e - j * d;
+  // K and V of this block (rows past Nk and columns past d read as zeros)
+  for (int e = t; e < 64 * DP; e += kSbThreads) {
+    const int j = e / DP, x = e % DP;
     const int key = k0 + j;
     const long long gi = (bh * p.Nk + key) * d + x;
-    const bool in = key < p.Nk && FA_IN(p.status, gi, 1, kv_elems);
+    const bool in = key < p.Nk && x < d && FA_IN(p.status, gi, 1, kv_elems);
     Ks[j * rs + x] = in ? p.k[gi] : 0.f;
     Vs[j * rs + x] = in ? p.v[gi] : 0.f;
   }
@@ -105,11 +116,11 @@ __global__ void __launch_bounds__(kSbThreads) fa_bwd_simt_kernel(const SimtBwdPa
   for (int qt = qt_first; qt < n_qt; ++qt) {
     const int q0 = qt * kSbQueries;
     __syncthreads();  // the previous tile's shared data is no longer read
-    for (int e = t; e < 64 * d; e += kSbThreads) {
-      const int i = e / d, x = e - i * d;
+    for (int e = t; e < 64 * DP; e += kSbThreads) {
+      const int i = e / DP, x = e % DP;
       const int qr = q0 + i;
       const long long gi = (bh * p.Nq + qr) * d + x;
-      const bool in = qr < p.Nq && FA_IN(p.status, gi, 1, q_elems);
+      const bool in = qr < p.Nq && x < d && FA_IN(p.status, gi, 1, q_elems);
       Qs[i * rs + x] = in ? qh[static_cast<long long>(qr) * d + x] : 0.f;
       dOs[i * rs + x] = in ? doh[static_cast<long long>(qr) * d + x] : 0.f;
     }
@@ -126,12 +137,20 @@ __global__ void __launch_bounds__(kSbThreads) fa_bwd_simt_kernel(const SimtBwdPa
       float s[16], dp[16];
 #pragma unroll
       for (int jj = 0; jj < 16; ++jj) s[jj] = dp[jj] = 0.f;
-      for (int x = 0; x < d; ++x) {
-        const float qv = Qs[i * rs + x], dov = dOs[i * rs + x];
+      const int d4 = (d + 3) & ~3;  // columns past d are zero
+      for (int x = 0; x < d4; x += 4) {
+        const float4 qv = ld4(Qs + i * rs + x), dov = ld4(dOs + i * rs + x);
 #pragma unroll
         for (int jj = 0; jj < 16; ++jj) {
-          s[jj] = fmaf(qv, Ks[(jb + jj) * rs + x], s[jj]);
-          dp[jj] = fmaf(dov, Vs[(jb + jj) * rs + x], dp[jj]);
+          const float4 kv = ld4(Ks + (jb + jj) * rs + x), vv = ld4(Vs + (jb + jj) * rs + x);
+          s[jj] = fmaf(qv.x, kv.x, s[jj]);
+          dp[jj] = fmaf(dov.x, vv.x, dp[jj]);
+          s[jj] = fmaf(qv.y, kv.y, s[jj]);
+          dp[jj] = fmaf(dov.y, vv.y, dp[jj]);
+          s[jj] = fmaf(qv.z, kv.z, s[jj]);
+          dp[jj] = fmaf(dov.z, vv.z, dp[jj]);
+          s[jj] = fmaf(qv.w, kv.w, s[jj]);
+          dp[jj] = fmaf(dov.w, vv.w, dp[jj]);
         }
       }
       const int qr = q0 + i;
@@ -146,14 +165,20 @@ __global__ void __launch_bounds__(kSbThreads) fa_bwd_simt_kernel(const SimtBwdPa
     }
     __syncthreads();
     // dV += P^T dO, dK += scale dS^T Q for key kr, columns c0 ..
+    // (columns past d hold zeros, so their sums stay 0 and are not stored)
     for (int i = 0; i < 64; ++i) {
       const float pv = Ps[i * 65 + kr], ds = dSs[i * 65 + kr];
 #pragma unroll
-      for (int c = 0; c < CW; ++c) {
-        if (c0 + c < d) {
-          dv_acc[c] = fmaf(pv, dOs[i * rs + c0 + c], dv_acc[c]);
-          dk_acc[c] = fmaf(ds, Qs[i * rs + c0 + c], dk_acc[c]);
-        }
+      for (int c = 0; c < CW; c += 4) {
+        const float4 ov = ld4(dOs + i * rs + c0 + c), qv = ld4(Qs + i * rs + c0 + c);
+        dv_acc[c] = fmaf(pv, ov.x, dv_acc[c]);
+        dv_acc[c + 1] = fmaf(pv, ov.y, dv_acc[c + 1]);
+        dv_acc[c + 2] = fmaf(pv, ov.z, dv_acc[c + 2]);
+        dv_acc[c + 3] = fmaf(pv, ov.w, dv_acc[c + 3]);
+        dk_acc[c] = fmaf(ds, qv.x, dk_acc[c]);
+        dk_acc[c + 1] = fmaf(ds, qv.y, dk_acc[c + 1]);
+        dk_acc[c + 2] = fmaf(ds, qv.z, dk_acc[c + 2]);
+        dk_acc[c + 3] = fmaf(ds, qv.w, dk_acc[c + 3]);
       }
     }
     // dQ += scale dS K for query t / 4, columns c0 .. (atomic: every key
@@ -167,14 +192,27 @@ __global__ void __launch_bounds__(kSbThreads) fa_bwd_simt_kernel(const SimtBwdPa
         for (int j = 0; j < 64; ++j) {
           const float ds = dSs[i * 65 + j];
 #pragma unroll
-          for (int c = 0; c < CW; ++c)
-            if (c0 + c < d) acc[c] = fmaf(ds, Ks[j * rs + c0 + c], acc[c]);
+          for (int c = 0; c < CW; c += 4) {
+            const float4 kv = ld4(Ks + j * rs + c0 + c);
+            acc[c] = fmaf(ds, kv.x, acc[c]);
+            acc[c + 1] = fmaf(ds, kv.y, acc[c + 1]);
+            acc[c + 2] = fmaf(ds, kv.z, acc[c + 2]);
+            acc[c + 3] = fmaf(ds, kv.w, acc[c + 3]);
+          }
         }
         const long long gbase = (bh * p.Nq + qr) * d + c0;
+        if ((d & 3) == 0) {  // rows 16-byte aligned: four adds per instruction
 #pragma unroll
-        for (int c = 0; c < CW; ++c)
-          if (c0 + c < d && FA_IN(p.status, gbase + c, 1, q_elems))
-            atomicAdd(p.dq + gbase + c, acc[c] * p.scale);
+          for (int c = 0; c < CW; c += 4)
+            if (c0 + c < d && FA_IN(p.status, gbase + c, 4, q_elems))
+              red_add_v4(p.dq + gbase + c, acc[c] * p.scale, acc[c + 1] * p.scale,
+                       acc[c + 2] * p.scale, acc[c + 3] * p.scale);
+        } else {
+#pragma unroll
+          for (int c = 0; c < CW; ++c)
+            if (c0 + c < d && FA_IN(p.status, gbase + c, 1, q_elems))
+              atomicAdd(p.dq + gbase + c, acc[c] * p.scale);
+        }
       }
     }
   }
@@ -194,10 +232,9 @@ __global__ void __launch_bounds__(kSbThreads) fa_bwd_simt_kernel(const SimtBwdPa
 
 template <int DP>
 cudaError_t launch_bwd_simt_dp(const SimtBwdParams &p, cudaStream_t s) {
-  const size_t smem = simt_bwd_smem(p.d);
-  static std::atomic<unsigned long long> attr_done;  // opt-in for the largest d of DP
-  cudaError_t e = smem_attr_once(fa_bwd_simt_kernel<DP>, static_cast<int>(simt_bwd_smem(DP)),
-                                 &attr_done);
+  const size_t smem = simt_bwd_smem(DP);
+  static std::atomic<unsigned long long> attr_done;
+  cudaError_t e = smem_attr_once(fa_bwd_simt_kernel<DP>, static_cast<int>(smem), &attr_done);
   if (e != cudaSuccess) return e;
   const dim3 grid(static_cast<unsigned>((p.Nk + kSbKeys - 1) / kSbKeys),
                   static_cast<unsigned>(p.H), static_cast<unsigned>(p.B));
