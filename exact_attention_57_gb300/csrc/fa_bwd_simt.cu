@@ -12,11 +12,10 @@
 // query tiles, accumulating dK and dV on chip; unlike it, dV takes the
 // query's row of dO (the page reads the key's row there), dQ is added into
 // the fp32 output with atomics from every key block instead of a
-// read-modify-write, and the work is spread over 256 threads:
-//   * S and dP for a 64 x 64 (query, key) tile: 16 entries a thread;
-//   * dK, dV: thread t owns key t/4 and a quarter of the head dim;
-//   * dQ: thread t owns query t/4 and a quarter of the head dim.
-// All arithmetic is fp32 (expf for the exponential).
+// read-modify-write, and the work is spread over 256 threads, each with a
+// 4 x 4 register block of every product (S and dP of a 64 x 64 tile, dK and
+// dV of 4 keys, dQ of 4 queries).  All arithmetic is fp32 (expf for the
+// exponential).
 #include <cmath>
 
 #include "fa.h"
@@ -62,36 +61,57 @@ struct SimtBwdParams {
 
 // Shared memory: K, V, Q, dO tiles of 64 rows of DP + 4 floats (columns
 // past d zero; rows 16-byte aligned for float4 reads, and the 4-float
-// offset spreads eight consecutive rows over all banks), then P and dS
-// (64 x 65 each), then the tile's LSE and D.
+// offset puts eight consecutive rows on distinct banks), then P and dS (64 x
+// 68 each, the same alignment), then the tile's LSE and D.
+constexpr int kSbPL = 68;  // row stride of P and dS
 __host__ __device__ inline size_t simt_bwd_smem(int dp) {
   const size_t row = static_cast<size_t>(dp) + 4;
-  return (4 * 64 * row + 2 * 64 * 65 + 2 * 64) * sizeof(float);
+  return (4 * 64 * row + 2 * 64 * kSbPL + 2 * 64) * sizeof(float);
 }
 
 __device__ __forceinline__ float4 ld4(const float *p) {
   return *reinterpret_cast<const float4 *>(p);
 }
+__device__ __forceinline__ float dot4(float4 a, float4 b, float acc) {
+  return fmaf(a.w, b.w, fmaf(a.z, b.z, fmaf(a.y, b.y, fmaf(a.x, b.x, acc))));
+}
+__device__ __forceinline__ void axpy4(float a, float4 x, float *y) {
+  y[0] = fmaf(a, x.x, y[0]);
+  y[1] = fmaf(a, x.y, y[1]);
+  y[2] = fmaf(a, x.z, y[2]);
+  y[3] = fmaf(a, x.w, y[3]);
+}
 
-template <int DP>  // head dim padded up to 32, 64 or 128
-// (two blocks an SM up to head dim 64; at 128 the accumulators need more
-// than 128 registers a thread)
+// Register blocking: each of the 256 threads computes a 4 x 4 block of S and
+// dP (queries lo + 16a, keys hi + 16b; lo = t % 16, hi = t / 16), of dK and
+// dV (keys 4lo .. 4lo+3 x columns hi*CB ..), and of dQ (queries lo + 16a x
+// columns hi*CB ..), CB = DP / 16: one 16-byte shared-memory read per 8
+// FMAs or fewer, the lanes of a warp reading consecutive rows (no bank
+// conflicts) or the same address (a broadcast).
+template <int DP>  // head dim padded up to 64 or 128
+// (two blocks an SM at 64; at 128 the accumulators need more than 128
+// registers a thread)
 __global__ void __launch_bounds__(kSbThreads, DP <= 64 ? 2 : 1)
     fa_bwd_simt_kernel(const SimtBwdParams p) {
+  constexpr int rs = DP + 4;
+  constexpr int PL = kSbPL;
+  constexpr int CB = DP / 16;  // columns per thread (dK, dV, dQ)
+  static_assert(CB % 4 == 0, "whole float4 column chunks");
   extern __shared__ float4 sm4[];
   float *sm = reinterpret_cast<float *>(sm4);
   const int d = p.d;
-  constexpr int rs = DP + 4;
   float *Ks = sm, *Vs = Ks + 64 * rs, *Qs = Vs + 64 * rs, *dOs = Qs + 64 * rs;
-  float *Ps = dOs + 64 * rs, *dSs = Ps + 64 * 65, *lse_s = dSs + 64 * 65, *dd_s = lse_s + 64;
+  float *Ps = dOs + 64 * rs, *dSs = Ps + 64 * PL, *lse_s = dSs + 64 * PL, *dd_s = lse_s + 64;
 
   const int t = threadIdx.x;
+  const int lo = t & 15, hi = t >> 4;
   const int k0 = blockIdx.x * kSbKeys;
   const long long bh = static_cast<long long>(blockIdx.z) * p.H + blockIdx.y;
   const long long q_elems = static_cast<long long>(p.B) * p.H * p.Nq * d;
   const long long kv_elems = static_cast<long long>(p.B) * p.H * p.Nk * d;
   const long long rows_q = static_cast<long long>(p.B) * p.H * p.Nq;
   const float *qh = p.q + bh * p.Nq * d, *doh = p.dout + bh * p.Nq * d;
+  const int d4 = (d + 3) & ~3;  // columns past d are zero
 
   // K and V of this block (rows past Nk and columns past d read as zeros)
   for (int e = t; e < 64 * DP; e += kSbThreads) {
@@ -102,12 +122,13 @@ __global__ void __launch_bounds__(kSbThreads, DP <= 64 ? 2 : 1)
     Ks[j * rs + x] = in ? p.k[gi] : 0.f;
     Vs[j * rs + x] = in ? p.v[gi] : 0.f;
   }
-  // this thread's share of dK, dV: key kr, columns [c0, c0 + DP/4)
-  constexpr int CW = DP / 4;
-  const int kr = t >> 2, c0 = (t & 3) * CW;
-  float dk_acc[CW], dv_acc[CW];
+  // dK, dV of keys 4lo + a, columns hi*CB + c
+  const int cb = hi * CB;
+  float dk_acc[4][CB], dv_acc[4][CB];
 #pragma unroll
-  for (int c = 0; c < CW; ++c) dk_acc[c] = dv_acc[c] = 0.f;
+  for (int a = 0; a < 4; ++a)
+#pragma unroll
+    for (int c = 0; c < CB; ++c) dk_acc[a][c] = dv_acc[a][c] = 0.f;
 
   const int n_qt = (p.Nq + kSbQueries - 1) / kSbQueries;
   // causal: query tiles whose last row is before the block's first key see
@@ -131,100 +152,116 @@ __global__ void __launch_bounds__(kSbThreads, DP <= 64 ? 2 : 1)
       dd_s[t] = in ? p.dd[bh * p.Nq + qr] : 0.f;
     }
     __syncthreads();
-    // S, dP -> P, dS for 16 entries: query i = t & 63, keys jb .. jb + 15
+    // S, dP -> P, dS: queries lo + 16a, keys hi + 16b
     {
-      const int i = t & 63, jb = (t >> 6) * 16;
-      float s[16], dp[16];
+      float s[4][4], dp[4][4];
 #pragma unroll
-      for (int jj = 0; jj < 16; ++jj) s[jj] = dp[jj] = 0.f;
-      const int d4 = (d + 3) & ~3;  // columns past d are zero
+      for (int a = 0; a < 4; ++a)
+#pragma unroll
+        for (int b = 0; b < 4; ++b) s[a][b] = dp[a][b] = 0.f;
       for (int x = 0; x < d4; x += 4) {
-        const float4 qv = ld4(Qs + i * rs + x), dov = ld4(dOs + i * rs + x);
+        float4 qv[4], ov[4];
 #pragma unroll
-        for (int jj = 0; jj < 16; ++jj) {
-          const float4 kv = ld4(Ks + (jb + jj) * rs + x), vv = ld4(Vs + (jb + jj) * rs + x);
-          s[jj] = fmaf(qv.x, kv.x, s[jj]);
-          dp[jj] = fmaf(dov.x, vv.x, dp[jj]);
-          s[jj] = fmaf(qv.y, kv.y, s[jj]);
-          dp[jj] = fmaf(dov.y, vv.y, dp[jj]);
-          s[jj] = fmaf(qv.z, kv.z, s[jj]);
-          dp[jj] = fmaf(dov.z, vv.z, dp[jj]);
-          s[jj] = fmaf(qv.w, kv.w, s[jj]);
-          dp[jj] = fmaf(dov.w, vv.w, dp[jj]);
+        for (int a = 0; a < 4; ++a) {
+          qv[a] = ld4(Qs + (lo + 16 * a) * rs + x);
+          ov[a] = ld4(dOs + (lo + 16 * a) * rs + x);
+        }
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {
+          const float4 kv = ld4(Ks + (hi + 16 * b) * rs + x);
+          const float4 vv = ld4(Vs + (hi + 16 * b) * rs + x);
+#pragma unroll
+          for (int a = 0; a < 4; ++a) {
+            s[a][b] = dot4(qv[a], kv, s[a][b]);
+            dp[a][b] = dot4(ov[a], vv, dp[a][b]);
+          }
         }
       }
-      const int qr = q0 + i;
 #pragma unroll
-      for (int jj = 0; jj < 16; ++jj) {
-        const int key = k0 + jb + jj;
-        const bool keep = key < p.Nk && (!p.causal || key <= qr);
-        const float pv = keep ? expf(s[jj] * p.scale - lse_s[i]) : 0.f;
-        Ps[i * 65 + jb + jj] = pv;
-        dSs[i * 65 + jb + jj] = pv * (dp[jj] - dd_s[i]);
+      for (int a = 0; a < 4; ++a) {
+        const int i = lo + 16 * a, qr = q0 + i;
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {
+          const int j = hi + 16 * b, key = k0 + j;
+          const bool keep = key < p.Nk && (!p.causal || key <= qr);
+          const float pv = keep ? expf(s[a][b] * p.scale - lse_s[i]) : 0.f;
+          Ps[i * PL + j] = pv;
+          dSs[i * PL + j] = pv * (dp[a][b] - dd_s[i]);
+        }
       }
     }
     __syncthreads();
-    // dV += P^T dO, dK += scale dS^T Q for key kr, columns c0 ..
+    // dV += P^T dO, dK += dS^T Q (scale applied at the store): keys 4lo + a
     // (columns past d hold zeros, so their sums stay 0 and are not stored)
     for (int i = 0; i < 64; ++i) {
-      const float pv = Ps[i * 65 + kr], ds = dSs[i * 65 + kr];
+      const float4 p4 = ld4(Ps + i * PL + 4 * lo), s4 = ld4(dSs + i * PL + 4 * lo);
+      const float pa[4] = {p4.x, p4.y, p4.z, p4.w}, sa[4] = {s4.x, s4.y, s4.z, s4.w};
 #pragma unroll
-      for (int c = 0; c < CW; c += 4) {
-        const float4 ov = ld4(dOs + i * rs + c0 + c), qv = ld4(Qs + i * rs + c0 + c);
-        dv_acc[c] = fmaf(pv, ov.x, dv_acc[c]);
-        dv_acc[c + 1] = fmaf(pv, ov.y, dv_acc[c + 1]);
-        dv_acc[c + 2] = fmaf(pv, ov.z, dv_acc[c + 2]);
-        dv_acc[c + 3] = fmaf(pv, ov.w, dv_acc[c + 3]);
-        dk_acc[c] = fmaf(ds, qv.x, dk_acc[c]);
-        dk_acc[c + 1] = fmaf(ds, qv.y, dk_acc[c + 1]);
-        dk_acc[c + 2] = fmaf(ds, qv.z, dk_acc[c + 2]);
-        dk_acc[c + 3] = fmaf(ds, qv.w, dk_acc[c + 3]);
+      for (int c = 0; c < CB; c += 4) {
+        const float4 ov = ld4(dOs + i * rs + cb + c), qv = ld4(Qs + i * rs + cb + c);
+#pragma unroll
+        for (int a = 0; a < 4; ++a) {
+          axpy4(pa[a], ov, &dv_acc[a][c]);
+          axpy4(sa[a], qv, &dk_acc[a][c]);
+        }
       }
     }
-    // dQ += scale dS K for query t / 4, columns c0 .. (atomic: every key
-    // block adds into the same rows)
+    // dQ += scale dS K: queries lo + 16a, columns cb .. cb + CB (atomic:
+    // every key block adds into the same rows)
     {
-      const int i = t >> 2, qr = q0 + i;
-      if (qr < p.Nq) {
-        float acc[CW];
+      float acc[4][CB];
 #pragma unroll
-        for (int c = 0; c < CW; ++c) acc[c] = 0.f;
-        for (int j = 0; j < 64; ++j) {
-          const float ds = dSs[i * 65 + j];
+      for (int a = 0; a < 4; ++a)
 #pragma unroll
-          for (int c = 0; c < CW; c += 4) {
-            const float4 kv = ld4(Ks + j * rs + c0 + c);
-            acc[c] = fmaf(ds, kv.x, acc[c]);
-            acc[c + 1] = fmaf(ds, kv.y, acc[c + 1]);
-            acc[c + 2] = fmaf(ds, kv.z, acc[c + 2]);
-            acc[c + 3] = fmaf(ds, kv.w, acc[c + 3]);
+        for (int c = 0; c < CB; ++c) acc[a][c] = 0.f;
+      for (int j = 0; j < 64; j += 4) {
+        float4 ds[4];
+#pragma unroll
+        for (int a = 0; a < 4; ++a) ds[a] = ld4(dSs + (lo + 16 * a) * PL + j);
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj) {
+#pragma unroll
+          for (int c = 0; c < CB; c += 4) {
+            const float4 kv = ld4(Ks + (j + jj) * rs + cb + c);
+#pragma unroll
+            for (int a = 0; a < 4; ++a) {
+              const float w = jj == 0 ? ds[a].x : jj == 1 ? ds[a].y : jj == 2 ? ds[a].z : ds[a].w;
+              axpy4(w, kv, &acc[a][c]);
+            }
           }
         }
-        const long long gbase = (bh * p.Nq + qr) * d + c0;
+      }
+#pragma unroll
+      for (int a = 0; a < 4; ++a) {
+        const int qr = q0 + lo + 16 * a;
+        if (qr >= p.Nq) continue;
+        const long long gbase = (bh * p.Nq + qr) * d + cb;
         if ((d & 3) == 0) {  // rows 16-byte aligned: four adds per instruction
 #pragma unroll
-          for (int c = 0; c < CW; c += 4)
-            if (c0 + c < d && FA_IN(p.status, gbase + c, 4, q_elems))
-              red_add_v4(p.dq + gbase + c, acc[c] * p.scale, acc[c + 1] * p.scale,
-                       acc[c + 2] * p.scale, acc[c + 3] * p.scale);
+          for (int c = 0; c < CB; c += 4)
+            if (cb + c < d && FA_IN(p.status, gbase + c, 4, q_elems))
+              red_add_v4(p.dq + gbase + c, acc[a][c] * p.scale, acc[a][c + 1] * p.scale,
+                         acc[a][c + 2] * p.scale, acc[a][c + 3] * p.scale);
         } else {
 #pragma unroll
-          for (int c = 0; c < CW; ++c)
-            if (c0 + c < d && FA_IN(p.status, gbase + c, 1, q_elems))
-              atomicAdd(p.dq + gbase + c, acc[c] * p.scale);
+          for (int c = 0; c < CB; ++c)
+            if (cb + c < d && FA_IN(p.status, gbase + c, 1, q_elems))
+              atomicAdd(p.dq + gbase + c, acc[a][c] * p.scale);
         }
       }
     }
   }
-  // dK, dV of key kr
-  const int key = k0 + kr;
-  if (key < p.Nk) {
-    const long long gbase = (bh * p.Nk + key) * d + c0;
+  // dK, dV of keys 4lo + a
 #pragma unroll
-    for (int c = 0; c < CW; ++c) {
-      if (c0 + c < d && FA_IN(p.status, gbase + c, 1, kv_elems)) {
-        p.dk[gbase + c] = dk_acc[c] * p.scale;
-        p.dv[gbase + c] = dv_acc[c];
+  for (int a = 0; a < 4; ++a) {
+    const int key = k0 + 4 * lo + a;
+    if (key >= p.Nk) continue;
+    const long long gbase = (bh * p.Nk + key) * d + cb;
+#pragma unroll
+    for (int c = 0; c < CB; ++c) {
+      if (cb + c < d && FA_IN(p.status, gbase + c, 1, kv_elems)) {
+        p.dk[gbase + c] = dk_acc[a][c] * p.scale;
+        p.dv[gbase + c] = dv_acc[a][c];
       }
     }
   }
@@ -271,7 +308,6 @@ cudaError_t launch_bwd_simt(const float *q, const float *k, const float *v, cons
   p.d = d;
   p.scale = scale;
   p.causal = causal;
-  if (d <= 32) return launch_bwd_simt_dp<32>(p, s);
   if (d <= 64) return launch_bwd_simt_dp<64>(p, s);
   return launch_bwd_simt_dp<128>(p, s);
 }
