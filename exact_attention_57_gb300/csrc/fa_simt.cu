@@ -17,8 +17,8 @@
 //   * keys past Nk and, when causal, keys after the query are excluded
 //     element by element, on every tile, not only within a row's own tile.
 //
-// Work split.  G neighbouring lanes of a warp share one query row (R = 128/G
-// rows per 128-thread CTA).  For the scores the G lanes split the keys of a
+// Work split.  G neighbouring lanes of a warp share one query row (R =
+// 128/(G*KS) rows per 128-thread CTA, KS the key groups below).  For the scores the G lanes split the keys of a
 // shared-memory tile (lane g takes keys g, g+G, ...), each holding the whole
 // query row in registers.  The tile's row max is combined across the G lanes
 // by shuffles; each lane turns its own scores into probabilities, and the
@@ -31,7 +31,8 @@
 // 128 rows in a CTA; G = 4, 8, 16 spread a smaller problem over 4, 8, 16
 // times as many CTAs at the cost of one shuffle per key and the row-max
 // shuffles.  The launcher takes the smallest G whose grid still gives every
-// SM two CTAs.  Staged rows are padded by 16 B so that the G different key
+// SM two CTAs; a grid still short of that also splits each row's keys over
+// KS = 2 or 4 warp groups of the CTA, whose states are merged at the end.  Staged rows are padded by 16 B so that the G different key
 // rows one access touches fall in different banks.
 //   K/V tiles go through a ring of NS shared-memory stages filled by
 // cp.async, NS - 1 tiles ahead of the arithmetic.  The dot products (for
