@@ -133,9 +133,21 @@ __global__ void __launch_bounds__(kSimtThreads, 1) fa_simt_fwd_kernel(const Simt
       active && FA_IN(p.status, static_cast<long long>(bh * p.Nq + row) * d, d, q_elems);
 
   float qr[DP];
+  if ((d & 3) == 0) {  // 16-byte-aligned rows: four columns a load
+    const float4 *q4 = reinterpret_cast<const float4 *>(qh + static_cast<size_t>(row) * d);
 #pragma unroll
-  for (int x = 0; x < DP; ++x)
-    qr[x] = (q_ok && x < d) ? qh[static_cast<size_t>(row) * d + x] : 0.f;
+    for (int x = 0; x < DP; x += 4) {
+      const float4 v = (q_ok && x < d) ? q4[x / 4] : make_float4(0.f, 0.f, 0.f, 0.f);
+      qr[x] = v.x;
+      qr[x + 1] = v.y;
+      qr[x + 2] = v.z;
+      qr[x + 3] = v.w;
+    }
+  } else {
+#pragma unroll
+    for (int x = 0; x < DP; ++x)
+      qr[x] = (q_ok && x < d) ? qh[static_cast<size_t>(row) * d + x] : 0.f;
+  }
 
   // keys [0, row_lim) take part for this row; the CTA visits keys up to the
   // largest row_lim among its rows.
